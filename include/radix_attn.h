@@ -1,0 +1,254 @@
+/*
+ * radix_attn.h -- C ABI of libradixattn.so: prefix-cached KV attention with a radix tree.
+ *
+ * The method: RadixAttention-style reuse of the KV cache across requests.
+ *  - "SGLang: Efficient Execution of Structured Language Model Programs" (unite.ai), the
+ *    RadixAttention bullet of the introduction: an LRU cache of KV kept in a radix tree,
+ *    with matching, insertion and eviction; and the nine-step walk-through of the tree
+ *    under an LRU policy (insert a turn as a node, reuse a cached prefix, split a node on
+ *    partial sharing, evict least recently used nodes under memory pressure).
+ *  - "Prompt Caching" (Ultralytics glossary), "How prompt caching works": with causal
+ *    attention a token's keys/values depend only on earlier tokens, so a cached prefix's
+ *    K/V can replace recomputation; only the new tokens run through the model; decode
+ *    attends each new token to all cached keys/values.
+ *
+ * Conventions (every entry point):
+ *  - Returns an int status (RX_OK or a negative RX_E* code); never throws or aborts.
+ *    rx_last_error() gives a thread-local message for the last failure.
+ *  - "d_" arguments are DEVICE pointers (caller-owned, e.g. torch tensors' data_ptr()),
+ *    "h_"/plain pointer arguments are HOST pointers (caller-owned).  The library never
+ *    allocates device memory; scratch space is passed in (decode workspace).
+ *  - Device calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *    Launch errors return RX_ECUDA.  Data-dependent failures detected on the device (a
+ *    slot out of range, a length beyond the table stride or a host hint) are written to
+ *    *d_status (int32, first failure wins, 0 = ok) and the offending element is skipped;
+ *    read it after synchronising.  Kernels never trap and never spin without a bound.
+ *  - Token ids and slots are int32; lengths and offsets ("indptr") are int64 unless noted.
+ *  - KV pools are [num_slots, hkv, head_dim], slot-major, row-contiguous, of the dtype in
+ *    rx_attn_desc.  A request's slot table row req_to_token[b, 0:len] lists the pool slot
+ *    of each of its tokens in logical order; unused entries are -1.
+ *  - A radix tree is not thread-safe: use one tree per host thread or lock externally.
+ */
+#ifndef RADIX_ATTN_H
+#define RADIX_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum rx_status {
+    RX_OK = 0,
+    RX_EINVAL = -1,    /* bad argument (null pointer, bad size, unknown handle, bad slot) */
+    RX_ENOMEM = -2,    /* not enough free KV slots (nothing was allocated) */
+    RX_ECUDA = -3,     /* a CUDA launch or runtime call failed */
+    RX_ELOCKED = -4,   /* unlock of a node that is not locked */
+    RX_ETIMEOUT = -5,  /* reserved: a bounded device wait gave up */
+    RX_EDEVICE = -6    /* unsupported device or configuration (e.g. not sm_103a for a tcgen05 kernel) */
+};
+
+/* Codes written to *d_status by kernels. */
+enum rx_device_status {
+    RX_DEV_OK = 0,
+    RX_DEV_BAD_SLOT = 1,     /* a slot outside [0, num_slots) was met; that row was skipped */
+    RX_DEV_BAD_LENGTH = 2,   /* a length exceeds the table stride or the host hint; request skipped */
+    RX_DEV_TIMEOUT = 3       /* a bounded wait inside a kernel gave up; outputs are invalid */
+};
+
+typedef enum { RX_F32 = 0, RX_BF16 = 1 } rx_dtype;
+
+/* Shape of one attention layer.  hq % hkv == 0; query head h reads kv head h / (hq/hkv).
+ * head_dim is 64 or 128.  scale multiplies q.k (1/sqrt(head_dim) in every workload). */
+typedef struct {
+    int32_t dtype;      /* rx_dtype of q, k, v, pools and outputs */
+    int32_t hq;
+    int32_t hkv;
+    int32_t head_dim;
+    int64_t num_slots;  /* rows of each KV pool */
+    float scale;
+} rx_attn_desc;
+
+/* ========================================================================= radix tree
+ * Host C++ radix tree mapping token sequences to KV-pool slots at token granularity,
+ * plus the pool's slot allocator.  Readings the pages leave open:
+ *  - a node boundary is cut at every divergence point and at the end of every match and
+ *    insert; nodes never merge again;
+ *  - a logical LRU clock advances by one per match_prefix/insert call and stamps every
+ *    node on the touched path;
+ *  - evict frees whole unlocked leaf nodes, least recent stamp first (ties by node id);
+ *  - the free list is FIFO: alloc pops from the head, frees append to the tail; it starts
+ *    as the slot ids ordered by the SplitMix64 output (state seed + (id+1)*0x9E3779B97F4A7C15,
+ *    Steele/Lea/Flood 2014), ties by id. */
+typedef struct rx_radix rx_radix;   /* opaque, host-owned */
+typedef int64_t rx_node;            /* node handle; 0 = root */
+
+typedef struct {
+    int64_t match_calls;
+    int64_t match_query_tokens;     /* tokens passed to match_prefix */
+    int64_t match_hit_tokens;       /* tokens matched (the cache hits) */
+    int64_t insert_calls;
+    int64_t inserted_tokens;        /* tokens newly owned by the tree */
+    int64_t evicted_tokens;
+    int64_t node_count;             /* nodes excluding the root */
+    int64_t cached_tokens;          /* tokens held by the tree */
+    int64_t free_slots;
+    int64_t num_slots;
+} rx_stats;
+
+/* Create a tree over a pool of num_slots slots (1 <= num_slots <= 2^31-1).
+ * *out receives the tree; free it with radix_destroy. */
+int radix_create(int64_t num_slots, uint64_t slot_perm_seed, rx_radix** out);
+void radix_destroy(rx_radix* t);
+
+/* Longest cached prefix of tokens[0:n].  Writes its slots to out_slots (capacity n),
+ * its length to *out_len and the handle of the node ending there to *out_last (0 if none).
+ * Splits the node in which the match ends and stamps the matched path. */
+int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slots,
+                 int64_t* out_len, rx_node* out_last);
+
+/* Pin / unpin the path from the root to a node so that evict never frees it
+ * (reference counted along the whole path).  RX_ELOCKED if unlocking an unlocked node. */
+int radix_lock(rx_radix* t, rx_node node);
+int radix_unlock(rx_radix* t, rx_node node);
+
+/* Pop n free slots (FIFO) into out_slots; RX_ENOMEM and nothing taken if fewer are free.
+ * Never evicts on its own: the caller calls evict and retries. */
+int alloc_slots(rx_radix* t, int64_t n, int32_t* out_slots);
+
+/* Return caller-held slots to the tail of the free list, in order.  RX_EINVAL (and no
+ * change) if a slot is out of range, already free or repeated. */
+int free_slots(rx_radix* t, const int32_t* slots, int64_t n);
+
+/* Insert tokens[0:n] with their slots.  Positions already cached keep the tree's slots:
+ * *out_dup_len receives how many leading positions were already present, and the caller
+ * still owns (and should free) slots[0:dup_len]; the tree takes slots[dup_len:n].
+ * *out_last receives the handle of the node ending at n. */
+int insert(rx_radix* t, const int32_t* tokens, const int32_t* slots, int64_t n,
+           int64_t* out_dup_len, rx_node* out_last);
+
+/* Free unlocked least-recently-used leaf nodes until at least num_tokens tokens are freed
+ * or nothing is evictable.  Freed slots go to the tail of the free list, node by node in
+ * position order; the first `cap` of them are also written to out_freed (may be NULL).
+ * *out_n receives the number of slots freed (may exceed num_tokens and cap). */
+int evict(rx_radix* t, int64_t num_tokens, int32_t* out_freed, int64_t cap, int64_t* out_n);
+
+/* Batched forms of match_prefix / insert for a batch of requests, processed in order
+ * b = 0..batch-1 with exactly the semantics (and LRU clock ticks) of one call each.
+ * Request b's tokens are tokens[tok_indptr[b] : tok_indptr[b+1]] (tok_indptr: [batch+1]).
+ * match_prefix_batch packs the matched slots: request b's are
+ * out_slots[out_indptr[b] : out_indptr[b+1]] (out_slots capacity tok_indptr[batch],
+ * out_indptr [batch+1]), ready to pass to kv_pool_write as the prefix slots and indptr.
+ * insert_batch takes one slot per token (same indptr) and returns dup lengths per request. */
+int match_prefix_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
+                       int32_t* out_slots, int64_t* out_indptr, rx_node* out_last);
+int insert_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
+                 const int32_t* slots, int64_t* out_dup_len, rx_node* out_last);
+
+int radix_stats(const rx_radix* t, rx_stats* out);
+
+/* Check the tree's invariants (edges, parents, slot ownership, stamps, locks);
+ * RX_OK or RX_EINVAL with the first violation in rx_last_error(). */
+int radix_check(const rx_radix* t);
+
+/* Shared-prefix groups for a decode batch, derived from the tree.  last_nodes[b] is the
+ * node where request b's cached path ends (out_last of its match_prefix/insert).  Requests
+ * whose paths leave the root through the same child node form one group; the group's
+ * shared length is the token depth of the deepest node common to all of its members'
+ * paths.  Groups with fewer than two members or a shared length below min_shared are not
+ * formed.  out_group_of[b] = group id or -1 (capacity batch); out_group_len[g] = shared
+ * tokens of group g (capacity batch); *out_num_groups = number of groups.  Group ids are
+ * assigned in order of each group's first member. */
+int radix_shared_groups(const rx_radix* t, const rx_node* last_nodes, int32_t batch,
+                        int64_t min_shared, int32_t* out_group_of, int64_t* out_group_len,
+                        int32_t* out_num_groups);
+
+/* ========================================================================= kernels */
+
+/* Build the slot table and scatter the new tokens' K/V into the pools.
+ * For request b (0 <= b < batch):
+ *   P_b = prefix_indptr[b+1]-prefix_indptr[b] matched slots d_prefix_slots[prefix_indptr[b]..],
+ *   n_b = qo_indptr[b+1]-qo_indptr[b] new slots d_new_slots[qo_indptr[b]..];
+ *   req_to_token[b, 0:P_b] = matched slots, [P_b:P_b+n_b] = new slots, rest = -1.
+ *   For every new token t, k_pool[new_slots[t]] = k_new[t], v_pool[new_slots[t]] = v_new[t]
+ *   (rows of hkv*head_dim elements).
+ * d_k_new/d_v_new: [T, hkv, head_dim] with T = total_new = qo_indptr[batch] (host copy;
+ * sizes the grid, and a request reaching past it is a length error).  d_req_to_token:
+ * [batch, r2t_stride] int32.  P_b + n_b > r2t_stride -> RX_DEV_BAD_LENGTH for that row;
+ * a slot outside [0, num_slots) -> RX_DEV_BAD_SLOT and that row is not written.
+ * "Prompt Caching", "How prompt caching works": only the new tokens' K/V are computed and
+ * stored; the prefix entries point at the cached copies. */
+int kv_pool_write(const rx_attn_desc* desc, int32_t batch,
+                  const int32_t* d_prefix_slots, const int64_t* d_prefix_indptr,
+                  const int32_t* d_new_slots, const int64_t* d_qo_indptr,
+                  const void* d_k_new, const void* d_v_new,
+                  void* d_k_pool, void* d_v_pool,
+                  int32_t* d_req_to_token, int64_t r2t_stride, int64_t total_new,
+                  int32_t* d_status, void* stream);
+
+/* Extend (prefill over the new tokens) attention with a cached prefix.
+ * For request b with P_b = d_prefix_lens[b] cached tokens and n_b = qo_indptr[b+1]-qo_indptr[b]
+ * new tokens, new row i (absolute position p = P_b + i) of query head h computes
+ *   o = softmax(scale * q K[0..p]^T) V[0..p]
+ * where K/V row j is the pool row req_to_token[b, j] of kv head h/(hq/hkv): the cached
+ * prefix is gathered from its slots and the new tokens attend causally to themselves
+ * (self included).  "Prompt Caching", "How prompt caching works" (causal attention; the
+ * cached prefix replaces recomputation).
+ * d_q, d_out: [T, hq, head_dim]; d_lse: optional [T, hq] float32 natural-log log-sum-exp
+ * of the scaled scores.  max_qo_len (host) must be >= every n_b (sizes the grid); rows of
+ * a request with n_b > max_qo_len or P_b + n_b > r2t_stride are skipped with
+ * RX_DEV_BAD_LENGTH.  bf16 runs on tcgen05 tensor cores (sm_103a); f32 on CUDA cores. */
+int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch,
+                            const void* d_q, const int64_t* d_qo_indptr, const int32_t* d_prefix_lens,
+                            const int32_t* d_req_to_token, int64_t r2t_stride,
+                            const void* d_k_pool, const void* d_v_pool,
+                            void* d_out, float* d_lse, int32_t max_qo_len,
+                            int32_t* d_status, void* stream);
+
+/* Optional description of requests that share a leading run of KV (a cached prefix)
+ * in a decode batch.  Members of group g have identical req_to_token[b, 0:len_g]; the
+ * shared part is read once per group instead of once per member. */
+typedef struct {
+    int32_t num_groups;
+    int32_t max_group_size;          /* host hint: largest group */
+    const int32_t* d_group_indptr;   /* [num_groups+1] offsets into d_group_members */
+    const int32_t* d_group_members;  /* request ids; a request is in at most one group */
+    const int32_t* d_group_len;      /* [num_groups] shared leading tokens, >= 1 */
+    int32_t max_group_len;           /* host hint: largest d_group_len */
+} rx_shared_groups;
+
+/* Bytes of device workspace decode_attention needs for this batch (>= 0), or 0 on error. */
+size_t decode_workspace_bytes(const rx_attn_desc* desc, int32_t batch, int32_t max_kv_len,
+                              const rx_shared_groups* groups);
+
+/* Decode attention: one query token per request attends all of its L_b = d_kv_lens[b]
+ * cached tokens (the new token's own K/V must already be in the pool, e.g. by
+ * kv_pool_write): o = softmax(scale * q K[0..L_b-1]^T) V[0..L_b-1] per query head.
+ * "Prompt Caching", "How prompt caching works": in decode each new token attends to all
+ * cached keys and values.  The keys are split into chunks processed by different CTAs
+ * (split-KV); per-chunk partial results (normalised output and log-sum-exp) are merged
+ * by a second kernel.  With `groups`, a group's shared leading tokens are processed once
+ * for all its members (their query rows stacked into one tile) and merged with each
+ * member's private remainder.
+ * d_q, d_out: [batch, hq, head_dim]; d_lse optional [batch, hq] float32.
+ * max_kv_len (host) must be >= every L_b.  d_workspace: >= decode_workspace_bytes(...)
+ * bytes of device memory, contents need not be initialised. */
+int decode_attention(const rx_attn_desc* desc, int32_t batch,
+                     const void* d_q, const int32_t* d_req_to_token, int64_t r2t_stride,
+                     const int32_t* d_kv_lens, const rx_shared_groups* groups,
+                     const void* d_k_pool, const void* d_v_pool,
+                     void* d_out, float* d_lse, int32_t max_kv_len,
+                     void* d_workspace, size_t ws_bytes,
+                     int32_t* d_status, void* stream);
+
+/* Thread-local message describing the last failure in this thread ("" if none). */
+const char* rx_last_error(void);
+
+/* Library version string. */
+const char* rx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RADIX_ATTN_H */

@@ -1,0 +1,324 @@
+"""Thin Python binding of libradixattn.so (ctypes).
+
+Argument marshalling only: every step runs in the library (host C++ radix tree, CUDA
+kernels).  Names follow the C ABI in include/radix_attn.h.  Device buffers are torch
+tensors on the current CUDA device; the call is enqueued on the given stream (default:
+torch's current stream).  A missing library raises at once: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libradixattn.so")
+
+RX_OK, RX_EINVAL, RX_ENOMEM, RX_ECUDA, RX_ELOCKED, RX_ETIMEOUT, RX_EDEVICE = 0, -1, -2, -3, -4, -5, -6
+RX_DEV_OK, RX_DEV_BAD_SLOT, RX_DEV_BAD_LENGTH, RX_DEV_TIMEOUT = 0, 1, 2, 3
+RX_F32, RX_BF16 = 0, 1
+
+EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "radix_lock", "radix_unlock", "alloc_slots",
+           "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "radix_stats", "radix_check",
+           "radix_shared_groups",
+           "kv_pool_write", "prefix_extend_attention", "decode_workspace_bytes", "decode_attention",
+           "rx_last_error", "rx_version")
+
+
+class RxError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed ({code}): {msg}")
+        self.code = code
+
+
+class rx_attn_desc(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("num_slots", ctypes.c_int64), ("scale", ctypes.c_float)]
+
+
+class rx_stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "match_calls", "match_query_tokens", "match_hit_tokens", "insert_calls", "inserted_tokens",
+        "evicted_tokens", "node_count", "cached_tokens", "free_slots", "num_slots")]
+
+
+class rx_shared_groups(ctypes.Structure):
+    _fields_ = [("num_groups", ctypes.c_int32), ("max_group_size", ctypes.c_int32),
+                ("d_group_indptr", ctypes.c_void_p), ("d_group_members", ctypes.c_void_p),
+                ("d_group_len", ctypes.c_void_p), ("max_group_len", ctypes.c_int32)]
+
+
+_lib = None
+P = ctypes.c_void_p
+I32, I64, U64, SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (build it first with prefix_cached_kv_radix_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libradixattn.so is not built ({path}); run "
+                           "`python -m prefix_cached_kv_radix_gb300.build`")
+    lib = ctypes.CDLL(path)
+    sig = {
+        "radix_create": (ctypes.c_int, [I64, U64, P]),
+        "radix_destroy": (None, [P]),
+        "match_prefix": (ctypes.c_int, [P, P, I64, P, P, P]),
+        "radix_lock": (ctypes.c_int, [P, I64]),
+        "radix_unlock": (ctypes.c_int, [P, I64]),
+        "alloc_slots": (ctypes.c_int, [P, I64, P]),
+        "free_slots": (ctypes.c_int, [P, P, I64]),
+        "insert": (ctypes.c_int, [P, P, P, I64, P, P]),
+        "evict": (ctypes.c_int, [P, I64, P, I64, P]),
+        "match_prefix_batch": (ctypes.c_int, [P, I32, P, P, P, P, P]),
+        "insert_batch": (ctypes.c_int, [P, I32, P, P, P, P, P]),
+        "radix_stats": (ctypes.c_int, [P, P]),
+        "radix_check": (ctypes.c_int, [P]),
+        "radix_shared_groups": (ctypes.c_int, [P, P, I32, I64, P, P, P]),
+        "kv_pool_write": (ctypes.c_int, [P, I32, P, P, P, P, P, P, P, P, P, I64, I64, P, P]),
+        "prefix_extend_attention": (ctypes.c_int, [P, I32, P, P, P, P, I64, P, P, P, P, I32, P, P]),
+        "decode_workspace_bytes": (SZ, [P, I32, I32, P]),
+        "decode_attention": (ctypes.c_int, [P, I32, P, P, I64, P, P, P, P, P, P, I32, P, SZ, P, P]),
+        "rx_last_error": (ctypes.c_char_p, []),
+        "rx_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, rc: int):
+    if rc != RX_OK:
+        raise RxError(fn, rc, load().rx_last_error().decode())
+
+
+def _np_i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr(t):
+    """Device pointer of a tensor (None -> NULL)."""
+    if t is None:
+        return None
+    assert t.is_cuda and t.is_contiguous(), "device buffers must be contiguous CUDA tensors"
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def version() -> str:
+    return load().rx_version().decode()
+
+
+def make_desc(dtype: int, hq: int, hkv: int, head_dim: int, num_slots: int, scale: float) -> rx_attn_desc:
+    return rx_attn_desc(dtype, hq, hkv, head_dim, num_slots, scale)
+
+
+# ============================================================================ radix tree
+def radix_create(num_slots: int, slot_perm_seed: int) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check("radix_create", load().radix_create(num_slots, slot_perm_seed & (2 ** 64 - 1), ctypes.byref(h)))
+    return h
+
+
+def radix_destroy(tree) -> None:
+    load().radix_destroy(tree)
+
+
+def match_prefix(tree, tokens):
+    """Returns (slots int32 [len], len, last node handle)."""
+    tok = _np_i32(tokens)
+    out = np.empty(max(len(tok), 1), np.int32)
+    n, last = I64(), I64()
+    _check("match_prefix", load().match_prefix(tree, tok.ctypes.data, len(tok), out.ctypes.data,
+                                               ctypes.byref(n), ctypes.byref(last)))
+    return out[: n.value].copy(), n.value, last.value
+
+
+def radix_lock(tree, node: int) -> None:
+    _check("radix_lock", load().radix_lock(tree, node))
+
+
+def radix_unlock(tree, node: int) -> None:
+    _check("radix_unlock", load().radix_unlock(tree, node))
+
+
+def alloc_slots(tree, n: int) -> np.ndarray:
+    out = np.empty(max(n, 1), np.int32)
+    _check("alloc_slots", load().alloc_slots(tree, n, out.ctypes.data))
+    return out[:n].copy()
+
+
+def free_slots(tree, slots) -> None:
+    s = _np_i32(slots)
+    _check("free_slots", load().free_slots(tree, s.ctypes.data if len(s) else None, len(s)))
+
+
+def insert(tree, tokens, slots):
+    """Returns (dup_len, last node handle)."""
+    tok, sl = _np_i32(tokens), _np_i32(slots)
+    assert len(tok) == len(sl)
+    dup, last = I64(), I64()
+    _check("insert", load().insert(tree, tok.ctypes.data if len(tok) else None,
+                                   sl.ctypes.data if len(sl) else None, len(tok),
+                                   ctypes.byref(dup), ctypes.byref(last)))
+    return dup.value, last.value
+
+
+def evict(tree, num_tokens: int, cap: int | None = None) -> np.ndarray:
+    """Frees LRU leaves until >= num_tokens are freed; returns the freed slots (up to cap)."""
+    cap = num_tokens + 1_000_000 if cap is None else cap
+    out = np.empty(max(cap, 1), np.int32)
+    n = I64()
+    _check("evict", load().evict(tree, num_tokens, out.ctypes.data, cap, ctypes.byref(n)))
+    return out[: min(n.value, cap)].copy()
+
+
+def match_prefix_batch(tree, tokens, tok_indptr):
+    """tokens: concatenated int32; tok_indptr int64 [batch+1].
+    Returns (packed slots int32, slot indptr int64 [batch+1], last nodes int64 [batch])."""
+    tok = _np_i32(tokens)
+    ind = np.ascontiguousarray(np.asarray(tok_indptr, np.int64))
+    b = len(ind) - 1
+    out = np.empty(max(len(tok), 1), np.int32)
+    oind = np.empty(b + 1, np.int64)
+    last = np.empty(max(b, 1), np.int64)
+    _check("match_prefix_batch", load().match_prefix_batch(tree, b, tok.ctypes.data, ind.ctypes.data, out.ctypes.data,
+                                                           oind.ctypes.data, last.ctypes.data))
+    return out[: oind[b]].copy(), oind, last[:b].copy()
+
+
+def insert_batch(tree, tokens, tok_indptr, slots):
+    """Returns (dup lengths int64 [batch], last nodes int64 [batch])."""
+    tok, sl = _np_i32(tokens), _np_i32(slots)
+    ind = np.ascontiguousarray(np.asarray(tok_indptr, np.int64))
+    b = len(ind) - 1
+    assert len(tok) == len(sl) == ind[b]
+    dup = np.empty(max(b, 1), np.int64)
+    last = np.empty(max(b, 1), np.int64)
+    _check("insert_batch", load().insert_batch(tree, b, tok.ctypes.data, ind.ctypes.data, sl.ctypes.data,
+                                               dup.ctypes.data, last.ctypes.data))
+    return dup[:b].copy(), last[:b].copy()
+
+
+def radix_stats(tree) -> dict:
+    st = rx_stats()
+    _check("radix_stats", load().radix_stats(tree, ctypes.byref(st)))
+    return {f: getattr(st, f) for f, _ in rx_stats._fields_}
+
+
+def radix_check(tree) -> None:
+    _check("radix_check", load().radix_check(tree))
+
+
+def radix_shared_groups(tree, last_nodes, min_shared: int = 1):
+    """Returns (group_of int32 [batch], group_len int64 [num_groups])."""
+    ln = np.ascontiguousarray(np.asarray(last_nodes, np.int64))
+    b = len(ln)
+    gof = np.empty(max(b, 1), np.int32)
+    glen = np.empty(max(b, 1), np.int64)
+    ng = I32()
+    _check("radix_shared_groups", load().radix_shared_groups(tree, ln.ctypes.data, b, min_shared, gof.ctypes.data,
+                                                             glen.ctypes.data, ctypes.byref(ng)))
+    return gof[:b].copy(), glen[: ng.value].copy()
+
+
+class RadixTree:
+    """Owning wrapper of an rx_radix handle."""
+
+    def __init__(self, num_slots: int, seed: int):
+        self.h = radix_create(num_slots, seed)
+        self.num_slots = num_slots
+
+    def __del__(self):
+        if getattr(self, "h", None) is not None and _lib is not None:
+            radix_destroy(self.h)
+            self.h = None
+
+    def match_prefix(self, tokens):
+        return match_prefix(self.h, tokens)
+
+    def insert(self, tokens, slots):
+        return insert(self.h, tokens, slots)
+
+    def evict(self, n, cap=None):
+        return evict(self.h, n, cap)
+
+    def alloc_slots(self, n):
+        return alloc_slots(self.h, n)
+
+    def free_slots(self, slots):
+        return free_slots(self.h, slots)
+
+    def lock(self, node):
+        return radix_lock(self.h, node)
+
+    def unlock(self, node):
+        return radix_unlock(self.h, node)
+
+    def match_prefix_batch(self, tokens, tok_indptr):
+        return match_prefix_batch(self.h, tokens, tok_indptr)
+
+    def insert_batch(self, tokens, tok_indptr, slots):
+        return insert_batch(self.h, tokens, tok_indptr, slots)
+
+    def stats(self):
+        return radix_stats(self.h)
+
+    def check(self):
+        return radix_check(self.h)
+
+    def shared_groups(self, last_nodes, min_shared=1):
+        return radix_shared_groups(self.h, last_nodes, min_shared)
+
+
+# ============================================================================ kernels
+def kv_pool_write(desc, batch, prefix_slots, prefix_indptr, new_slots, qo_indptr, k_new, v_new, k_pool, v_pool,
+                  req_to_token, total_new, status, stream=None) -> None:
+    _check("kv_pool_write", load().kv_pool_write(
+        ctypes.byref(desc), batch, _ptr(prefix_slots), _ptr(prefix_indptr), _ptr(new_slots), _ptr(qo_indptr),
+        _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(req_to_token), req_to_token.shape[1],
+        total_new, _ptr(status), _stream(stream)))
+
+
+def prefix_extend_attention(desc, batch, q, qo_indptr, prefix_lens, req_to_token, k_pool, v_pool, out, lse,
+                            max_qo_len, status, stream=None) -> None:
+    _check("prefix_extend_attention", load().prefix_extend_attention(
+        ctypes.byref(desc), batch, _ptr(q), _ptr(qo_indptr), _ptr(prefix_lens), _ptr(req_to_token),
+        req_to_token.shape[1], _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(lse), max_qo_len, _ptr(status),
+        _stream(stream)))
+
+
+def shared_groups_struct(num_groups, max_group_size, group_indptr, group_members, group_len, max_group_len):
+    """rx_shared_groups from device tensors (int32)."""
+    if num_groups == 0:
+        return None
+    return rx_shared_groups(num_groups, max_group_size, group_indptr.data_ptr(), group_members.data_ptr(),
+                            group_len.data_ptr(), max_group_len)
+
+
+def decode_workspace_bytes(desc, batch, max_kv_len, groups=None) -> int:
+    return int(load().decode_workspace_bytes(ctypes.byref(desc), batch, max_kv_len,
+                                             ctypes.byref(groups) if groups is not None else None))
+
+
+def decode_attention(desc, batch, q, req_to_token, kv_lens, k_pool, v_pool, out, lse, max_kv_len, workspace,
+                     status, groups=None, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("decode_attention", load().decode_attention(
+        ctypes.byref(desc), batch, _ptr(q), _ptr(req_to_token), req_to_token.shape[1], _ptr(kv_lens),
+        ctypes.byref(groups) if groups is not None else None, _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(lse),
+        max_kv_len, _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))

@@ -1,0 +1,519 @@
+// Split-KV decode attention over the pooled KV cache, on mma.sync tensor-core tiles.
+//
+// "Prompt Caching" (Ultralytics glossary), "How prompt caching works": in decode each new
+// token attends to all keys and values cached for its prompt.  With RadixAttention the
+// cached prefix rows live once in the pool and requests gather them through their slot
+// tables ("SGLang: Efficient Execution of Structured Language Model Programs", RadixAttention).
+//
+// Design (GB300): the step is HBM-bound (each K/V byte is used by the hq/hkv query heads of
+// one kv head only), so the kernel is built around streaming: one CTA per (request, kv head,
+// chunk of keys); 16-byte cp.async gathers of 64-key stages into a 3-stage 128B-swizzled
+// ring; each warp owns 16 keys of a stage and computes S^T = K Q^T with keys in the M
+// dimension of m16n8k16 (the <= 8 query heads of the group fill N, so only half of each
+// tile is padding), then O^T += V^T P^T with V^T fragments from ldmatrix.trans and P^T
+// moved into B-fragment layout by movmatrix.  Online softmax in the exp2 domain.  Each CTA
+// writes its chunk's normalised output and log-sum-exp; a second kernel merges the chunks:
+//   M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s.
+// Groups of requests sharing a cached prefix (rx_shared_groups) get their shared run
+// processed once per group: one CTA per (group, kv head, chunk, 16-row block of stacked
+// query rows) reads each shared K/V row once for all members, and the merge kernel adds
+// that partial to each member's private chunks.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "radix_attn.h"
+#include "rx_common.h"
+#include "rx_device.cuh"
+#include "rx_kernels.h"
+
+namespace rx {
+
+constexpr int DEC_THREADS = 128;   // 4 warps
+constexpr int DEC_STAGE_KEYS = 64; // 16 keys per warp per stage
+constexpr int DEC_NS = 3;          // cp.async ring depth
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+struct DecodeParams {
+    const __nv_bfloat16* q;     // [batch, hq, D]
+    const int32_t* r2t;
+    int64_t stride;
+    const int32_t* kv_lens;
+    const __nv_bfloat16* k_pool;
+    const __nv_bfloat16* v_pool;
+    int64_t num_slots;
+    int32_t batch, hq, hkv, group;
+    float scale_log2;
+    int32_t chunk;              // keys per split (multiple of DEC_STAGE_KEYS)
+    int32_t max_chunks;         // private partial slots per (request, head)
+    int32_t max_len;
+    float* part_o;              // [batch, hq, max_chunks + group_chunks, D]
+    float* part_lse;            // [batch, hq, max_chunks + group_chunks] (log2 domain)
+    int32_t* status;
+    // shared-prefix groups
+    int32_t num_groups;
+    const int32_t* grp_indptr;
+    const int32_t* grp_members;
+    const int32_t* grp_len;
+    int32_t grp_chunks;         // shared partial slots per (request, head)
+    int32_t grp_rows_max;       // max stacked rows (members * group) of a group
+    const int32_t* group_of;    // [batch] group id or -1 (workspace, filled by a prep kernel)
+};
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(chunk ^ (row & 7)); }
+
+// Gather one stage of K and V (64 keys starting at key k0) into smem.
+template <int D>
+__device__ __forceinline__ void dec_load_stage(const DecodeParams& p, const int32_t* slots_row, int k0, int k_end,
+                                               int g, uint32_t kbuf, uint32_t vbuf, int tid) {
+    constexpr int CPR = D / 8;                       // 16-byte chunks per row
+    constexpr int PER = DEC_STAGE_KEYS * CPR / DEC_THREADS;
+    const int c = tid % CPR;
+#pragma unroll
+    for (int x = 0; x < PER; ++x) {
+        const int key = tid / CPR + x * (DEC_THREADS / CPR);
+        const int kk = k0 + key;
+        int32_t s = kk < k_end ? slots_row[kk] : 0;
+        uint32_t bytes = 16;
+        if (kk >= k_end) bytes = 0;
+        else if (s < 0 || s >= p.num_slots) {
+            report(p.status, RX_DEV_BAD_SLOT);
+            s = 0;
+            bytes = 0;
+        }
+        const int64_t off = ((int64_t)s * p.hkv + g) * D + c * 8;
+        const uint32_t so = (uint32_t)(key * D * 2) + swz(key, c) * 16;
+        cp_async_16(kbuf + so, p.k_pool + off, bytes);
+        cp_async_16(vbuf + so, p.v_pool + off, bytes);
+    }
+}
+
+// Attention of up to 8 query rows (packed into N of m16n8k16) over keys [k_begin, k_end)
+// of one slot-table row; writes normalised partial outputs and log2-domain lse.
+// Row n of the tile is query (qrow_base[n]) -- given by row_q(n) -- and writes partial
+// slot part_idx(n).  Used for private chunks (rows = the group's heads of one request)
+// and for shared chunks (rows = stacked heads of several requests).
+template <int D>
+__device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* slots_row, int k_begin, int k_end,
+                                          int g, const int64_t* q_off, const int64_t* out_slot, int nrows,
+                                          unsigned char* smem) {
+    constexpr int KSTEPS = D / 16;
+    constexpr int MT = D / 16;                        // m-tiles of O^T
+    constexpr int ROWB = D * 2;
+    constexpr int STAGE_B = DEC_STAGE_KEYS * ROWB;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t4 = lane & 3, r8 = lane >> 2;
+    const uint32_t sbase = smem_u32(smem);
+    auto kbuf = [&](int st) { return sbase + (uint32_t)(st * 2 * STAGE_B); };
+    auto vbuf = [&](int st) { return sbase + (uint32_t)(st * 2 * STAGE_B + STAGE_B); };
+
+    // Q^T fragments (B operand of S^T = K Q^T): head n = r8, dims 16s + 2*t4 (+1), (+8).
+    uint32_t qb[KSTEPS][2];
+    {
+        const bool valid = r8 < nrows;
+        const __nv_bfloat16* qr = p.q + (valid ? q_off[r8] : 0);
+#pragma unroll
+        for (int s = 0; s < KSTEPS; ++s) {
+            qb[s][0] = valid ? *reinterpret_cast<const uint32_t*>(qr + 16 * s + 2 * t4) : 0u;
+            qb[s][1] = valid ? *reinterpret_cast<const uint32_t*>(qr + 16 * s + 8 + 2 * t4) : 0u;
+        }
+    }
+    float o[MT][4];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2*t4, 2*t4+1
+
+    const int nstages = (k_end - k_begin + DEC_STAGE_KEYS - 1) / DEC_STAGE_KEYS;
+#pragma unroll
+    for (int s = 0; s < DEC_NS - 1; ++s) {
+        if (s < nstages) dec_load_stage<D>(p, slots_row, k_begin + s * DEC_STAGE_KEYS, k_end, g, kbuf(s), vbuf(s), tid);
+        cp_async_commit();
+    }
+    for (int it = 0; it < nstages; ++it) {
+        cp_async_wait<DEC_NS - 2>();
+        __syncthreads();
+        {
+            const int nx = it + DEC_NS - 1;
+            if (nx < nstages)
+                dec_load_stage<D>(p, slots_row, k_begin + nx * DEC_STAGE_KEYS, k_end, g, kbuf(nx % DEC_NS),
+                                  vbuf(nx % DEC_NS), tid);
+            cp_async_commit();
+        }
+        const int st = it % DEC_NS;
+        const int key0 = k_begin + it * DEC_STAGE_KEYS + warp * 16;   // first key of this warp
+        if (key0 >= k_end) continue;                                   // nothing for this warp
+        // S^T (16 keys x 8 rows)
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int krow = warp * 16 + (mi & 1) * 8 + rr;
+#pragma unroll
+            for (int s = 0; s < KSTEPS; ++s) {
+                uint32_t a[4];
+                const int ch = 2 * s + (mi >> 1);
+                ldmatrix_x4(kbuf(st) + (uint32_t)(krow * ROWB) + swz(krow, ch) * 16, a[0], a[1], a[2], a[3]);
+                mma_bf16_16816(sacc, a, qb[s][0], qb[s][1]);
+            }
+        }
+        // scale, mask keys beyond the chunk, online softmax per query row (column)
+        const bool ok_lo = key0 + r8 < k_end, ok_hi = key0 + r8 + 8 < k_end;
+        float x0 = ok_lo ? sacc[0] * p.scale_log2 : -INFINITY;
+        float x1 = ok_lo ? sacc[1] * p.scale_log2 : -INFINITY;
+        float x2 = ok_hi ? sacc[2] * p.scale_log2 : -INFINITY;
+        float x3 = ok_hi ? sacc[3] * p.scale_log2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);   // finite: key0 < k_end
+        const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+        const float p0 = exp2f(x0 - n0), p1 = exp2f(x1 - n1), p2 = exp2f(x2 - n0), p3 = exp2f(x3 - n1);
+        l0 = l0 * a0 + p0 + p2;
+        l1 = l1 * a1 + p1 + p3;
+        m0 = n0;
+        m1 = n1;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            o[i][0] *= a0;
+            o[i][1] *= a1;
+            o[i][2] *= a0;
+            o[i][3] *= a1;
+        }
+        const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+        const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+        {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int vrow = warp * 16 + (mi >> 1) * 8 + rr;
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                uint32_t a[4];
+                const int ch = 2 * i + (mi & 1);
+                ldmatrix_x4_trans(vbuf(st) + (uint32_t)(vrow * ROWB) + swz(vrow, ch) * 16, a[0], a[1], a[2], a[3]);
+                mma_bf16_16816(o[i], a, pb0, pb1);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();   // all warps done with the ring: reuse it for the cross-warp merge
+
+    // Row sums across the 8 lanes sharing t4.
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    float* red_o = reinterpret_cast<float*>(smem);                 // [4 warps][8 rows][D]
+    float* red_ml = red_o + 4 * 8 * D;                             // [4 warps][8 rows][2]
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+        const int d = 16 * i + r8;
+        red_o[(warp * 8 + 2 * t4) * D + d] = o[i][0];
+        red_o[(warp * 8 + 2 * t4 + 1) * D + d] = o[i][1];
+        red_o[(warp * 8 + 2 * t4) * D + d + 8] = o[i][2];
+        red_o[(warp * 8 + 2 * t4 + 1) * D + d + 8] = o[i][3];
+    }
+    if (r8 == 0) {
+        red_ml[(warp * 8 + 2 * t4) * 2 + 0] = m0;
+        red_ml[(warp * 8 + 2 * t4) * 2 + 1] = l0;
+        red_ml[(warp * 8 + 2 * t4 + 1) * 2 + 0] = m1;
+        red_ml[(warp * 8 + 2 * t4 + 1) * 2 + 1] = l1;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nrows * D; idx += DEC_THREADS) {
+        const int n = idx / D, d = idx - n * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, red_ml[(w * 8 + n) * 2]);
+        float L = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float mw = red_ml[(w * 8 + n) * 2];
+            const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            L += sc * red_ml[(w * 8 + n) * 2 + 1];
+            acc += sc * red_o[(w * 8 + n) * D + d];
+        }
+        const int64_t slot = out_slot[n];
+        p.part_o[slot * D + d] = acc / L;
+        if (d == 0) p.part_lse[slot] = M + log2f(L);
+    }
+    __syncthreads();
+}
+
+// Private chunks: blockIdx = (chunk, kv head, request).  Keys [shared_len_b + c*chunk, ...).
+template <int D>
+__global__ void __launch_bounds__(DEC_THREADS) decode_private_kernel(DecodeParams p) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int32_t L = p.kv_lens[b];
+    if (L < 1 || L > p.max_len || L > p.stride) {
+        if (c == 0 && g == 0 && threadIdx.x == 0) report(p.status, RX_DEV_BAD_LENGTH);
+        return;
+    }
+    int shared = 0;
+    if (p.group_of) {
+        const int gid = p.group_of[b];
+        if (gid >= 0) shared = min(p.grp_len[gid], L);
+    }
+    const int k_begin = shared + c * p.chunk;
+    if (k_begin >= L) return;
+    const int k_end = min(L, k_begin + p.chunk);
+    int64_t q_off[8], out_slot[8];
+    const int per = p.max_chunks + p.grp_chunks;
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+        const int h = g * p.group + (n < p.group ? n : 0);
+        q_off[n] = ((int64_t)b * p.hq + h) * D;
+        out_slot[n] = ((int64_t)b * p.hq + h) * per + c;
+    }
+    dec_chunk<D>(p, p.r2t + (int64_t)b * p.stride, k_begin, k_end, g, q_off, out_slot, p.group, smem);
+}
+
+// Shared chunks: blockIdx = (chunk * row_blocks + row block, kv head, group).  Up to 8
+// stacked query rows (member, head) per CTA read the group's shared keys once.
+template <int D>
+__global__ void __launch_bounds__(DEC_THREADS) decode_shared_kernel(DecodeParams p, int32_t row_blocks) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int gid = blockIdx.z, g = blockIdx.y;
+    const int c = blockIdx.x / row_blocks, rb = blockIdx.x - c * row_blocks;
+    const int m0 = p.grp_indptr[gid], nm = p.grp_indptr[gid + 1] - m0;
+    const int rows = nm * p.group;
+    const int r0 = rb * 8;
+    if (r0 >= rows) return;
+    // shared length: bounded by every member's own length
+    int len = p.grp_len[gid];
+    const int first = p.grp_members[m0];
+    const int k_begin = c * p.chunk;
+    if (k_begin >= len) return;
+    const int k_end = min(len, k_begin + p.chunk);
+    int64_t q_off[8], out_slot[8];
+    const int per = p.max_chunks + p.grp_chunks;
+    const int nrows = min(8, rows - r0);
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+        const int r = r0 + (n < nrows ? n : 0);
+        const int b = p.grp_members[m0 + r / p.group];
+        const int h = g * p.group + r % p.group;
+        q_off[n] = ((int64_t)b * p.hq + h) * D;
+        out_slot[n] = ((int64_t)b * p.hq + h) * per + p.max_chunks + c;
+    }
+    dec_chunk<D>(p, p.r2t + (int64_t)first * p.stride, k_begin, k_end, g, q_off, out_slot, nrows, smem);
+}
+
+// Merge the private and shared partials of each (request, head).
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, __nv_bfloat16* out, float* lse) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * 4 + warp;   // (request, head)
+    if (item >= (int64_t)p.batch * p.hq) return;
+    const int b = (int)(item / p.hq);
+    const int32_t L = p.kv_lens[b];
+    if (L < 1 || L > p.max_len || L > p.stride) return;
+    int shared = 0;
+    if (p.group_of) {
+        const int gid = p.group_of[b];
+        if (gid >= 0) shared = min(p.grp_len[gid], L);
+    }
+    const int npriv = (L - shared + p.chunk - 1) / p.chunk;
+    const int nsh = (shared + p.chunk - 1) / p.chunk;
+    const int per = p.max_chunks + p.grp_chunks;
+    const float* po = p.part_o + item * per * D;
+    const float* pl = p.part_lse + item * per;
+    float M = -INFINITY;
+    for (int s = 0; s < npriv; ++s) M = fmaxf(M, pl[s]);
+    for (int s = 0; s < nsh; ++s) M = fmaxf(M, pl[p.max_chunks + s]);
+    constexpr int E = D / 32;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float W = 0.f;
+    auto add = [&](int s) {
+        const float w = exp2f(pl[s] - M);
+        W += w;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += w * po[(int64_t)s * D + lane + 32 * e];
+    };
+    for (int s = 0; s < npriv; ++s) add(s);
+    for (int s = 0; s < nsh; ++s) add(p.max_chunks + s);
+    __nv_bfloat16* orow = out + item * D;
+#pragma unroll
+    for (int e = 0; e < E; ++e) orow[lane + 32 * e] = __float2bfloat16_rn(acc[e] / W);
+    if (lse && lane == 0) lse[item] = (M + log2f(W)) * LN2;
+}
+
+// group_of[b] from the member lists; -1 for requests outside every group.
+__global__ void decode_group_of_kernel(DecodeParams p, int32_t* group_of) {
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < p.batch; b += gridDim.x * blockDim.x) group_of[b] = -1;
+}
+__global__ void decode_group_fill_kernel(DecodeParams p, int32_t* group_of) {
+    for (int gid = blockIdx.x; gid < p.num_groups; gid += gridDim.x)
+        for (int i = p.grp_indptr[gid] + threadIdx.x; i < p.grp_indptr[gid + 1]; i += blockDim.x) {
+            const int b = p.grp_members[i];
+            if (b >= 0 && b < p.batch) group_of[b] = gid;
+            else report(p.status, RX_DEV_BAD_LENGTH);
+        }
+}
+
+static int dec_chunk_keys(int32_t batch, int32_t hkv, int32_t max_kv_len) {
+    // Enough CTAs to fill 152 SMs several times over; chunks of 256..1024 keys.
+    int chunk = 512;
+    const int64_t ctas = (int64_t)batch * hkv * ((max_kv_len + chunk - 1) / chunk);
+    if (ctas < 152 * 4) chunk = 256;
+    if (max_kv_len > 65536 && ctas > 152 * 64) chunk = 1024;
+    return chunk;
+}
+
+struct DecodeLayout {
+    int chunk, max_chunks, grp_chunks;
+    size_t part_o_bytes, part_lse_bytes, group_of_bytes, total;
+};
+
+static DecodeLayout dec_layout(const rx_attn_desc* d, int32_t batch, int32_t max_kv_len, const rx_shared_groups* grp) {
+    DecodeLayout L{};
+    L.chunk = dec_chunk_keys(batch, d->hkv, max_kv_len);
+    L.max_chunks = (max_kv_len + L.chunk - 1) / L.chunk;
+    L.grp_chunks = (grp && grp->num_groups > 0) ? (grp->max_group_len + L.chunk - 1) / L.chunk : 0;
+    const size_t per = (size_t)(L.max_chunks + L.grp_chunks);
+    L.part_o_bytes = (size_t)batch * d->hq * per * d->head_dim * sizeof(float);
+    L.part_lse_bytes = (size_t)batch * d->hq * per * sizeof(float);
+    L.group_of_bytes = (grp && grp->num_groups > 0) ? (size_t)batch * sizeof(int32_t) : 0;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    L.total = up(L.part_o_bytes) + up(L.part_lse_bytes) + up(L.group_of_bytes);
+    return L;
+}
+
+static size_t dec_smem_bytes(int D) {
+    const size_t ring = (size_t)DEC_NS * 2 * DEC_STAGE_KEYS * D * 2;
+    const size_t red = (size_t)4 * 8 * D * 4 + 4 * 8 * 2 * 4;
+    return ring > red ? ring : red;
+}
+
+}  // namespace rx
+
+using namespace rx;
+
+extern "C" size_t decode_workspace_bytes(const rx_attn_desc* desc, int32_t batch, int32_t max_kv_len,
+                                         const rx_shared_groups* groups) {
+    if (!desc || batch < 0 || max_kv_len < 1) return 0;
+    return dec_layout(desc, batch, max_kv_len, groups).total;
+}
+
+extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const void* d_q,
+                                const int32_t* d_req_to_token, int64_t r2t_stride, const int32_t* d_kv_lens,
+                                const rx_shared_groups* groups, const void* d_k_pool, const void* d_v_pool,
+                                void* d_out, float* d_lse, int32_t max_kv_len, void* d_workspace,
+                                size_t ws_bytes, int32_t* d_status, void* stream_) {
+    RX_REQUIRE(desc && batch >= 0 && max_kv_len >= 1 && r2t_stride >= 0, "decode_attention: bad arguments");
+    RX_REQUIRE(desc->hq > 0 && desc->hkv > 0 && desc->hq % desc->hkv == 0, "decode_attention: bad head counts");
+    RX_REQUIRE(desc->head_dim == 64 || desc->head_dim == 128, "decode_attention: head_dim must be 64 or 128");
+    if (batch == 0) return RX_OK;
+    RX_REQUIRE(d_q && d_req_to_token && d_kv_lens && d_k_pool && d_v_pool && d_out,
+               "decode_attention: null device pointer");
+    cudaStream_t stream = (cudaStream_t)stream_;
+    const int group = desc->hq / desc->hkv;
+    if (desc->dtype == RX_F32 || group > 8) {
+        // CUDA-core path: fp32 (exact arithmetic of the tiny workload) or > 8 heads per kv head.
+        SimtParams sp{};
+        sp.batch = batch;
+        sp.hq = desc->hq;
+        sp.hkv = desc->hkv;
+        sp.total_rows = batch;
+        sp.q = d_q;
+        sp.kv_lens = d_kv_lens;
+        sp.r2t = d_req_to_token;
+        sp.stride = r2t_stride;
+        sp.k_pool = d_k_pool;
+        sp.v_pool = d_v_pool;
+        sp.num_slots = desc->num_slots;
+        sp.out = d_out;
+        sp.lse = d_lse;
+        sp.scale = desc->scale;
+        sp.max_len = max_kv_len;
+        sp.status = d_status;
+        return launch_attn_simt(sp, desc->dtype, desc->head_dim, stream);
+    }
+    RX_REQUIRE(desc->dtype == RX_BF16, "decode_attention: unknown dtype %d", desc->dtype);
+    const bool use_groups = groups && groups->num_groups > 0;
+    if (use_groups)
+        RX_REQUIRE(groups->d_group_indptr && groups->d_group_members && groups->d_group_len &&
+                       groups->max_group_size >= 1 && groups->max_group_len >= 1,
+                   "decode_attention: incomplete shared groups");
+    const DecodeLayout lay = dec_layout(desc, batch, max_kv_len, use_groups ? groups : nullptr);
+    RX_REQUIRE(d_workspace && ws_bytes >= lay.total, "decode_attention: workspace of %zu bytes, %zu needed",
+               ws_bytes, lay.total);
+    RX_REQUIRE(((uintptr_t)d_workspace & 255) == 0, "decode_attention: workspace must be 256-byte aligned");
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    unsigned char* ws = (unsigned char*)d_workspace;
+    DecodeParams p{};
+    p.q = (const __nv_bfloat16*)d_q;
+    p.r2t = d_req_to_token;
+    p.stride = r2t_stride;
+    p.kv_lens = d_kv_lens;
+    p.k_pool = (const __nv_bfloat16*)d_k_pool;
+    p.v_pool = (const __nv_bfloat16*)d_v_pool;
+    p.num_slots = desc->num_slots;
+    p.batch = batch;
+    p.hq = desc->hq;
+    p.hkv = desc->hkv;
+    p.group = group;
+    p.scale_log2 = desc->scale * LOG2E;
+    p.chunk = lay.chunk;
+    p.max_chunks = lay.max_chunks;
+    p.max_len = max_kv_len;
+    p.part_o = (float*)ws;
+    p.part_lse = (float*)(ws + up(lay.part_o_bytes));
+    p.status = d_status;
+    p.grp_chunks = lay.grp_chunks;
+    int32_t* group_of = nullptr;
+    if (use_groups) {
+        group_of = (int32_t*)(ws + up(lay.part_o_bytes) + up(lay.part_lse_bytes));
+        p.num_groups = groups->num_groups;
+        p.grp_indptr = groups->d_group_indptr;
+        p.grp_members = groups->d_group_members;
+        p.grp_len = groups->d_group_len;
+        p.grp_rows_max = groups->max_group_size * group;
+        p.group_of = group_of;
+    }
+    const int D = desc->head_dim;
+    const size_t smem = dec_smem_bytes(D);
+    static bool attr_set[2] = {false, false};
+    const int di = D == 128 ? 1 : 0;
+    if (!attr_set[di]) {
+        cudaError_t e1, e2;
+        if (D == 128) {
+            e1 = cudaFuncSetAttribute(decode_private_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            e2 = cudaFuncSetAttribute(decode_shared_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        } else {
+            e1 = cudaFuncSetAttribute(decode_private_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            e2 = cudaFuncSetAttribute(decode_shared_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        }
+        if (e1 != cudaSuccess || e2 != cudaSuccess) {
+            set_error("decode_attention: cannot set shared memory size: %s",
+                      cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+            return RX_ECUDA;
+        }
+        attr_set[di] = true;
+    }
+    if (use_groups) {
+        decode_group_of_kernel<<<(batch + 255) / 256, 256, 0, stream>>>(p, group_of);
+        decode_group_fill_kernel<<<groups->num_groups, 128, 0, stream>>>(p, group_of);
+        const int row_blocks = (groups->max_group_size * group + 7) / 8;
+        dim3 gs((unsigned)(lay.grp_chunks * row_blocks), (unsigned)desc->hkv, (unsigned)groups->num_groups);
+        if (D == 128) decode_shared_kernel<128><<<gs, DEC_THREADS, smem, stream>>>(p, row_blocks);
+        else decode_shared_kernel<64><<<gs, DEC_THREADS, smem, stream>>>(p, row_blocks);
+    }
+    dim3 grid((unsigned)lay.max_chunks, (unsigned)desc->hkv, (unsigned)batch);
+    if (D == 128) decode_private_kernel<128><<<grid, DEC_THREADS, smem, stream>>>(p);
+    else decode_private_kernel<64><<<grid, DEC_THREADS, smem, stream>>>(p);
+    const int64_t items = (int64_t)batch * desc->hq;
+    const unsigned mblocks = (unsigned)((items + 3) / 4);
+    if (D == 128) decode_merge_kernel<128><<<mblocks, 128, 0, stream>>>(p, (__nv_bfloat16*)d_out, d_lse);
+    else decode_merge_kernel<64><<<mblocks, 128, 0, stream>>>(p, (__nv_bfloat16*)d_out, d_lse);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("decode_attention: launch failed: %s", cudaGetErrorString(e));
+        return RX_ECUDA;
+    }
+    return RX_OK;
+}

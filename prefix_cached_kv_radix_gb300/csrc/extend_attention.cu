@@ -1,0 +1,467 @@
+// Extend (prefill over new tokens) attention with a radix-cached prefix, on tcgen05 tensor
+// cores with TMEM accumulators (sm_103a).
+//
+// "Prompt Caching" (Ultralytics glossary), "How prompt caching works": on a cache hit only
+// the new tokens run through the model; because attention is causal, the cached prefix's
+// keys/values (computed once, shared) stand in for recomputing it.  Row i of request b
+// (position p = P_b + i) attends keys 0..p: the prefix gathered from scattered pool slots
+// through req_to_token, then the request's own new tokens causally (self included).
+// "SGLang: Efficient Execution of Structured Language Model Programs", RadixAttention:
+// the prefix's KV is reused across requests rather than recomputed.
+//
+// GB300 design.  One CTA per (request, kv head, 256 packed query rows).  The query heads
+// of a kv head (GQA group) are packed with the tokens, head fastest: packed row R ->
+// token R / G, head g*G + R % G, so every K/V tile feeds G heads and the tile stays a
+// dense contraction.  Two 128-row Q tiles share each K/V tile (halves L2->SM traffic per
+// FLOP).  Warp roles (320 threads):
+//   warp 0     loader: 16-byte cp.async gathers of Q once and of K/V tiles (64 keys)
+//              through the slot table into a 3-stage ring, 128B-swizzled (the canonical
+//              K-major layout tcgen05 reads); completion is signalled on mbarriers.
+//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer:
+//              S_t = Q_t K^T (M=128, N=64, K=D) and O_t += P_t V (M=128, N=D, K=64, V read
+//              as an MN-major operand), completion via tcgen05.commit.
+//   warps 2-5  softmax of Q tile 0; warps 6-9 softmax of Q tile 1: tcgen05.ld of a score
+//              row per thread, causal mask, online softmax in the exp2 domain with a lazy
+//              rescale (the reference max only moves when the row max grows by more than
+//              2^8, which keeps every P <= 256), P written as bf16 to swizzled smem, O
+//              rescaled in TMEM only when the reference moved, final O / l to global.
+// The two Q tiles ping-pong: while one tile's softmax runs, the tensor core works on the
+// other's GEMMs.  Every wait is bounded; on time-out the kernel records RX_DEV_TIMEOUT,
+// drains its async copies, frees TMEM and returns.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "radix_attn.h"
+#include "rx_common.h"
+#include "rx_device.cuh"
+#include "rx_kernels.h"
+
+namespace rx {
+
+constexpr int EXT_BN = 64;        // keys per K/V tile
+constexpr int EXT_NS = 3;         // K/V ring depth
+constexpr int EXT_THREADS = 320;  // 10 warps
+constexpr float EXT_LOG2E = 1.4426950408889634f;
+constexpr float EXT_LN2 = 0.6931471805599453f;
+constexpr float EXT_RESCALE_THRESHOLD = 8.0f;   // log2 units
+
+struct ExtendParams {
+    const __nv_bfloat16* q;
+    const int64_t* qo_indptr;
+    const int32_t* prefix_lens;
+    const int32_t* r2t;
+    int64_t stride;
+    const __nv_bfloat16* k_pool;
+    const __nv_bfloat16* v_pool;
+    int64_t num_slots;
+    __nv_bfloat16* out;
+    float* lse;
+    int32_t batch, hq, hkv, group;
+    float scale_log2;
+    int32_t max_qo_len;
+    int32_t* status;
+};
+
+template <int D>
+struct ExtLayout {
+    static constexpr int Q_TILE = 128 * D * 2;
+    static constexpr int KV_TILE = EXT_BN * D * 2;
+    static constexpr int P_TILE = 128 * EXT_BN * 2;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
+    static constexpr int OFF_V = OFF_K + EXT_NS * KV_TILE;
+    static constexpr int OFF_P = OFF_V + EXT_NS * KV_TILE;
+    static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
+    // q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], mma_done
+    static constexpr int BAR_Q = 0, BAR_KVF = 1, BAR_KVE = 1 + EXT_NS, BAR_S = 1 + 2 * EXT_NS,
+                         BAR_P = BAR_S + 2, BAR_O = BAR_P + 2, BAR_DONE = BAR_O + 2, NBAR = BAR_DONE + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int ALLOC = BYTES + 1024;   // room to align the base to 1024 B
+    static constexpr uint32_t TMEM_COLS = (2 * EXT_BN + 2 * D) <= 256 ? 256u : 512u;
+    static constexpr uint32_t COL_S0 = 0, COL_O0 = 2 * EXT_BN;
+};
+
+template <int D>
+__global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams p) {
+    using LY = ExtLayout<D>;
+    constexpr int CPR = D / 8;   // 16-byte chunks per row
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + LY::OFF_BAR;
+    auto bar = [&](int i) { return bar0 + (uint32_t)(8 * i); };
+    volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + LY::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + LY::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.z, g = blockIdx.y;
+    const int64_t qo0 = p.qo_indptr[b];
+    const int n_b = (int)(p.qo_indptr[b + 1] - qo0);
+    const int P_b = p.prefix_lens[b];
+    const int G = p.group;
+    const int rows_total = n_b * G;
+    const int row0 = blockIdx.x * 256;
+    if (row0 >= rows_total || n_b <= 0) return;   // uniform for the whole CTA
+    if (n_b > p.max_qo_len || P_b < 0 || (int64_t)P_b + n_b > p.stride) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.status, RX_DEV_BAD_LENGTH);
+        return;
+    }
+    const int ntiles = rows_total - row0 > 128 ? 2 : 1;
+    const int last_row = min(row0 + 256, rows_total) - 1;
+    const int kv_end = P_b + last_row / G + 1;              // keys needed by this CTA
+    const int nkv = (kv_end + EXT_BN - 1) / EXT_BN;
+    const int32_t* slots_row = p.r2t + (int64_t)b * p.stride;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(LY::BAR_Q), 32);
+        for (int i = 0; i < EXT_NS; ++i) {
+            mbar_init(bar(LY::BAR_KVF + i), 32);
+            mbar_init(bar(LY::BAR_KVE + i), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(LY::BAR_S + t), 1);
+            mbar_init(bar(LY::BAR_P + t), 128);
+            mbar_init(bar(LY::BAR_O + t), 1);
+        }
+        mbar_init(bar(LY::BAR_DONE), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(base + LY::OFF_MISC, LY::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ loader
+        const uint32_t qs = base + LY::OFF_Q;
+        for (int x = 0; x < 256 * CPR / 32; ++x) {
+            const int qi = lane + 32 * x;
+            const int rr = qi / CPR, c = qi % CPR;
+            const int t = rr >> 7, r = rr & 127;
+            if (t >= ntiles) break;
+            const int R = min(row0 + rr, rows_total - 1);
+            const int tok = R / G, h = g * G + R % G;
+            const __nv_bfloat16* src = p.q + ((qo0 + tok) * p.hq + h) * D + c * 8;
+            const uint32_t dst = qs + (uint32_t)(t * LY::Q_TILE + (c >> 3) * 128 * 128 + r * 128 +
+                                                 (((c & 7) ^ (r & 7)) << 4));
+            cp_async_16(dst, src, 16);
+        }
+        cp_async_arrive_noinc(bar(LY::BAR_Q));
+        for (int j = 0; j < nkv; ++j) {
+            const int st = j % EXT_NS;
+            if (j >= EXT_NS && !warp_wait(bar(LY::BAR_KVE + st), ((j / EXT_NS) - 1) & 1, abort_flag, p.status)) break;
+            const int k0 = j * EXT_BN;
+            const int kk0 = k0 + lane, kk1 = k0 + lane + 32;
+            const int32_t s0 = kk0 < kv_end ? slots_row[kk0] : 0;
+            const int32_t s1 = kk1 < kv_end ? slots_row[kk1] : 0;
+            const uint32_t kb = base + LY::OFF_K + st * LY::KV_TILE;
+            const uint32_t vb = base + LY::OFF_V + st * LY::KV_TILE;
+#pragma unroll 4
+            for (int x = 0; x < EXT_BN * CPR / 32; ++x) {
+                const int qi = lane + 32 * x;
+                const int key = qi / CPR, c = qi % CPR;
+                const int32_t a = __shfl_sync(0xffffffffu, s0, key & 31);
+                const int32_t bb = __shfl_sync(0xffffffffu, s1, key & 31);
+                int32_t slot = key < 32 ? a : bb;
+                uint32_t bytes = 16;
+                if (k0 + key >= kv_end) {
+                    bytes = 0;
+                    slot = 0;
+                } else if (slot < 0 || slot >= p.num_slots) {
+                    report(p.status, RX_DEV_BAD_SLOT);
+                    bytes = 0;
+                    slot = 0;
+                }
+                const int64_t off = ((int64_t)slot * p.hkv + g) * D + c * 8;
+                const uint32_t so = (uint32_t)((c >> 3) * EXT_BN * 128 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
+                cp_async_16(kb + so, p.k_pool + off, bytes);
+                cp_async_16(vb + so, p.v_pool + off, bytes);
+            }
+            cp_async_arrive_noinc(bar(LY::BAR_KVF + st));
+        }
+        cp_async_wait<0>();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_S = idesc_bf16_f32(128, EXT_BN, 0, 0);
+            constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);
+            const uint32_t qs = base + LY::OFF_Q;
+            bool ok = mbar_wait(bar(LY::BAR_Q), 0, abort_flag, p.status);
+            fence_proxy_async_smem();
+            tc_fence_after();
+            auto issue_pv = [&](int t, int jj) {
+                const uint32_t vb = base + LY::OFF_V + (jj % EXT_NS) * LY::KV_TILE;
+                const uint32_t pb = base + LY::OFF_P + t * LY::P_TILE;
+#pragma unroll
+                for (int s = 0; s < EXT_BN / 16; ++s) {
+                    const uint64_t ad = sdesc_sw128(pb + s * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(vb + s * 16 * 128, EXT_BN * 128, 1024);
+                    umma_f16_ss(tmem + LY::COL_O0 + t * D, ad, bd, IDESC_PV, (jj > 0 || s > 0) ? 1u : 0u);
+                }
+                umma_commit(bar(LY::BAR_O + t));
+            };
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int st = j % EXT_NS;
+                if (!mbar_wait(bar(LY::BAR_KVF + st), (j / EXT_NS) & 1, abort_flag, p.status)) { ok = false; break; }
+                fence_proxy_async_smem();
+                tc_fence_after();
+                const uint32_t kb = base + LY::OFF_K + st * LY::KV_TILE;
+                for (int t = 0; t < ntiles; ++t) {
+                    if (j > 0) {
+                        if (!mbar_wait(bar(LY::BAR_P + t), (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+                    }
+#pragma unroll
+                    for (int s = 0; s < D / 16; ++s) {
+                        const uint32_t koff = (uint32_t)((s >> 2) * 128 * 128 + (s & 3) * 32);
+                        const uint32_t kboff = (uint32_t)((s >> 2) * EXT_BN * 128 + (s & 3) * 32);
+                        const uint64_t ad = sdesc_sw128(qs + t * LY::Q_TILE + koff, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(kb + kboff, 16, 1024);
+                        umma_f16_ss(tmem + LY::COL_S0 + t * EXT_BN, ad, bd, IDESC_S, s > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar(LY::BAR_S + t));
+                    if (j > 0) issue_pv(t, j - 1);
+                }
+                if (!ok) break;
+                if (j > 0) umma_commit(bar(LY::BAR_KVE + (j - 1) % EXT_NS));
+            }
+            for (int t = 0; ok && t < ntiles; ++t) {
+                if (!mbar_wait(bar(LY::BAR_P + t), (nkv - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                fence_proxy_async_smem();
+                tc_fence_after();
+                issue_pv(t, nkv - 1);
+            }
+            umma_commit(bar(LY::BAR_DONE));
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = (warp - 2) >> 2;
+        if (t < ntiles) {
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + lane;
+            const int R = row0 + t * 128 + r;
+            const bool valid = R < rows_total;
+            const int Rc = min(R, rows_total - 1);
+            const int tok = Rc / G;
+            const int pos = P_b + tok;   // attends keys 0..pos
+            const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+            const uint32_t s_addr = tmem + lane_base + LY::COL_S0 + t * EXT_BN;
+            const uint32_t o_addr = tmem + lane_base + LY::COL_O0 + t * D;
+            const uint32_t prow = base + LY::OFF_P + t * LY::P_TILE + r * 128;
+            float m_ref = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nkv; ++j) {
+                if (!warp_wait(bar(LY::BAR_S + t), j & 1, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                float s[EXT_BN];
+                tmem_ld32(s_addr, s);
+                tmem_ld32(s_addr + 32, s + 32);
+                tmem_wait_ld();
+                const int k0 = j * EXT_BN;
+                if (k0 + EXT_BN - 1 > pos) {
+#pragma unroll
+                    for (int c = 0; c < EXT_BN; ++c)
+                        if (k0 + c > pos) s[c] = -INFINITY;
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < EXT_BN; ++c) mx = fmaxf(mx, s[c]);
+                mx *= p.scale_log2;
+                float m_new = m_ref;
+                if (m_ref == -INFINITY || mx > m_ref + EXT_RESCALE_THRESHOLD) m_new = fmaxf(m_ref, mx);
+                const float alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < EXT_BN; ++c) {
+                    s[c] = exp2f(s[c] * p.scale_log2 - m_new);
+                    rs += s[c];
+                }
+                l = l * alpha + rs;
+                if (j > 0) {
+                    if (!warp_wait(bar(LY::BAR_O + t), (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, m_new != m_ref)) {
+#pragma unroll
+                        for (int cc = 0; cc < D; cc += 32) {
+                            float ov[32];
+                            tmem_ld32(o_addr + cc, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+                            tmem_st32(o_addr + cc, ov);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                m_ref = m_new;
+#pragma unroll
+                for (int ch = 0; ch < EXT_BN / 8; ++ch) {
+                    const uint32_t w0 = pack_bf16x2(s[8 * ch + 0], s[8 * ch + 1]);
+                    const uint32_t w1 = pack_bf16x2(s[8 * ch + 2], s[8 * ch + 3]);
+                    const uint32_t w2 = pack_bf16x2(s[8 * ch + 4], s[8 * ch + 5]);
+                    const uint32_t w3 = pack_bf16x2(s[8 * ch + 6], s[8 * ch + 7]);
+                    st_shared_v4(prow + (uint32_t)(((ch ^ (r & 7)) & 7) << 4), w0, w1, w2, w3);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(LY::BAR_P + t));
+            }
+            if (ok && warp_wait(bar(LY::BAR_O + t), (nkv - 1) & 1, abort_flag, p.status)) {
+                tc_fence_after();
+                const float inv = 1.f / l;
+                __nv_bfloat16* orow = p.out + ((qo0 + tok) * p.hq + g * G + Rc % G) * D;
+#pragma unroll
+                for (int cc = 0; cc < D; cc += 32) {
+                    float ov[32];
+                    tmem_ld32(o_addr + cc, ov);
+                    tmem_wait_ld();
+                    if (valid) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(ov[e + 0] * inv, ov[e + 1] * inv);
+                            v.y = pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv);
+                            v.z = pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv);
+                            v.w = pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv);
+                            *reinterpret_cast<uint4*>(orow + cc + e) = v;
+                        }
+                    }
+                }
+                if (valid && p.lse) p.lse[(qo0 + tok) * p.hq + g * G + Rc % G] = (m_ref + log2f(l)) * EXT_LN2;
+            }
+        }
+    }
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        // Every MMA this CTA issued has completed before TMEM is released; this wait does
+        // not stop on the abort flag (only on its own time bound).
+        volatile int no_abort = 0;
+        warp_wait(bar(LY::BAR_DONE), 0, &no_abort, p.status, 500000000ull);
+        tmem_dealloc(tmem, LY::TMEM_COLS);
+    }
+}
+
+static int g_cc_checked = 0;   // 1 = sm_103, -1 = other
+
+static int check_device() {
+    if (g_cc_checked == 0) {
+        int dev = 0, major = 0, minor = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            set_error("prefix_extend_attention: cannot query the device");
+            return RX_ECUDA;
+        }
+        g_cc_checked = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_cc_checked != 1) {
+        set_error("prefix_extend_attention: the tcgen05 kernel needs an sm_103 (GB300) device");
+        return RX_EDEVICE;
+    }
+    return RX_OK;
+}
+
+template <int D>
+static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t stream) {
+    static bool attr = false;
+    const int smem = ExtLayout<D>::ALLOC;
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) {
+            set_error("prefix_extend_attention: cannot set shared memory size: %s", cudaGetErrorString(e));
+            return RX_ECUDA;
+        }
+        attr = true;
+    }
+    dim3 grid((unsigned)tiles, (unsigned)p.hkv, (unsigned)p.batch);
+    extend_tc_kernel<D><<<grid, EXT_THREADS, smem, stream>>>(p);
+    return RX_OK;
+}
+
+}  // namespace rx
+
+using namespace rx;
+
+extern "C" int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch, const void* d_q,
+                                       const int64_t* d_qo_indptr, const int32_t* d_prefix_lens,
+                                       const int32_t* d_req_to_token, int64_t r2t_stride, const void* d_k_pool,
+                                       const void* d_v_pool, void* d_out, float* d_lse, int32_t max_qo_len,
+                                       int32_t* d_status, void* stream_) {
+    RX_REQUIRE(desc && batch >= 0 && max_qo_len >= 0 && r2t_stride >= 0, "prefix_extend_attention: bad arguments");
+    RX_REQUIRE(desc->hq > 0 && desc->hkv > 0 && desc->hq % desc->hkv == 0,
+               "prefix_extend_attention: bad head counts");
+    RX_REQUIRE(desc->head_dim == 64 || desc->head_dim == 128, "prefix_extend_attention: head_dim must be 64 or 128");
+    if (batch == 0 || max_qo_len == 0) return RX_OK;
+    RX_REQUIRE(d_q && d_qo_indptr && d_prefix_lens && d_req_to_token && d_k_pool && d_v_pool && d_out,
+               "prefix_extend_attention: null device pointer");
+    cudaStream_t stream = (cudaStream_t)stream_;
+    const int group = desc->hq / desc->hkv;
+    if (desc->dtype == RX_F32) {
+        // fp32 keeps fp32 arithmetic on CUDA cores; rows are sized by the host bound.
+        SimtParams sp{};
+        sp.batch = batch;
+        sp.hq = desc->hq;
+        sp.hkv = desc->hkv;
+        sp.total_rows = -1;
+        sp.q = d_q;
+        sp.qo_indptr = d_qo_indptr;
+        sp.prefix_lens = d_prefix_lens;
+        sp.r2t = d_req_to_token;
+        sp.stride = r2t_stride;
+        sp.k_pool = d_k_pool;
+        sp.v_pool = d_v_pool;
+        sp.num_slots = desc->num_slots;
+        sp.out = d_out;
+        sp.lse = d_lse;
+        sp.scale = desc->scale;
+        sp.max_len = max_qo_len;
+        sp.status = d_status;
+        // Rows are bounded by batch * max_qo_len; rows past qo_indptr[batch] exit at once.
+        sp.total_rows = (int64_t)batch * max_qo_len;
+        return launch_attn_simt(sp, desc->dtype, desc->head_dim, stream);
+    }
+    RX_REQUIRE(desc->dtype == RX_BF16, "prefix_extend_attention: unknown dtype %d", desc->dtype);
+    const int dc = check_device();
+    if (dc != RX_OK) return dc;
+    ExtendParams p{};
+    p.q = (const __nv_bfloat16*)d_q;
+    p.qo_indptr = d_qo_indptr;
+    p.prefix_lens = d_prefix_lens;
+    p.r2t = d_req_to_token;
+    p.stride = r2t_stride;
+    p.k_pool = (const __nv_bfloat16*)d_k_pool;
+    p.v_pool = (const __nv_bfloat16*)d_v_pool;
+    p.num_slots = desc->num_slots;
+    p.out = (__nv_bfloat16*)d_out;
+    p.lse = d_lse;
+    p.batch = batch;
+    p.hq = desc->hq;
+    p.hkv = desc->hkv;
+    p.group = group;
+    p.scale_log2 = desc->scale * EXT_LOG2E;
+    p.max_qo_len = max_qo_len;
+    p.status = d_status;
+    const int64_t tiles = ((int64_t)max_qo_len * group + 255) / 256;
+    RX_REQUIRE(tiles < 65536 && batch < 65536, "prefix_extend_attention: grid too large");
+    const int rc = desc->head_dim == 128 ? launch_extend_tc<128>(p, (int)tiles, stream)
+                                         : launch_extend_tc<64>(p, (int)tiles, stream);
+    if (rc != RX_OK) return rc;
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("prefix_extend_attention: launch failed: %s", cudaGetErrorString(e));
+        return RX_ECUDA;
+    }
+    return RX_OK;
+}

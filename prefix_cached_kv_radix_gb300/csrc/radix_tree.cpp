@@ -1,0 +1,478 @@
+// Host radix tree over KV-pool slots, with LRU eviction and a FIFO slot allocator.
+//
+// "SGLang: Efficient Execution of Structured Language Model Programs" (unite.ai):
+//  - RadixAttention bullet of the introduction: the runtime keeps an LRU cache of KV cache
+//    in a radix tree and uses it for matching, insertion and eviction;
+//  - the nine-step walk-through: edges carry token sequences; a new turn is inserted as a
+//    node; a prompt whose prefix is in the tree reuses that KV; an edge is split in two
+//    when a new sequence shares only part of it; under memory limits the least recently
+//    used nodes are evicted.
+// "Prompt Caching" (Ultralytics glossary): reuse needs an exactly matching prefix.
+//
+// Design: token-granular edges (each token owns one pool slot), children keyed by their
+// first token.  Readings where the pages are open: a boundary is cut at every divergence
+// point and at the end of every match and insert, and nodes never merge; a logical clock
+// (+1 per match/insert call) stamps every node on the touched path; eviction frees whole
+// unlocked leaves, least recent stamp first, ties by node id; locks are reference counts
+// held along the whole root path.  The allocator is a FIFO ring of free slots whose
+// initial order sorts slot ids by SplitMix64 (Steele, Lea & Flood, OOPSLA 2014).
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <memory>
+#include <new>
+#include <queue>
+#include <string>
+#include <tuple>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "rx_common.h"
+
+namespace rx {
+
+static thread_local std::string g_last_error;
+
+void set_error(const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+}
+
+void clear_error() { g_last_error.clear(); }
+
+struct Node {
+    int64_t id = 0;
+    Node* parent = nullptr;
+    std::vector<int32_t> key;     // edge tokens
+    std::vector<int32_t> slots;   // pool slot of each edge token
+    std::unordered_map<int32_t, Node*> children;  // by first token
+    uint64_t stamp = 0;
+    int64_t ref = 0;
+    int64_t depth = 0;            // tokens from the root to the END of this node
+};
+
+static uint64_t splitmix64_at(uint64_t seed, uint64_t counter) {
+    uint64_t z = seed + counter * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+}  // namespace rx
+
+struct rx_radix {
+    int64_t num_slots = 0;
+    // FIFO ring of free slots
+    std::vector<int32_t> ring;
+    int64_t head = 0, count = 0;
+    std::vector<uint8_t> is_free;
+    rx::Node root;
+    uint64_t clock = 0;
+    int64_t next_id = 1;
+    std::unordered_map<int64_t, rx::Node*> by_id;
+    rx_stats st{};
+
+    ~rx_radix() { destroy_children(&root); }
+
+    void destroy_children(rx::Node* x) {
+        std::vector<rx::Node*> stack;
+        for (auto& kv : x->children) stack.push_back(kv.second);
+        x->children.clear();
+        while (!stack.empty()) {
+            rx::Node* n = stack.back();
+            stack.pop_back();
+            for (auto& kv : n->children) stack.push_back(kv.second);
+            delete n;
+        }
+    }
+
+    void push_free(int32_t s) {
+        ring[(head + count) % num_slots] = s;
+        ++count;
+        is_free[s] = 1;
+    }
+
+    rx::Node* new_node() {
+        rx::Node* n = new rx::Node();
+        n->id = next_id++;
+        by_id[n->id] = n;
+        ++st.node_count;
+        return n;
+    }
+
+    // Split node c after its first k tokens.  The new upper node takes the first k tokens
+    // and a new id; c keeps its id (a handle keeps naming the node that ends where it did).
+    rx::Node* split(rx::Node* c, size_t k) {
+        rx::Node* top = new_node();
+        top->parent = c->parent;
+        top->key.assign(c->key.begin(), c->key.begin() + k);
+        top->slots.assign(c->slots.begin(), c->slots.begin() + k);
+        top->stamp = c->stamp;
+        top->ref = c->ref;
+        top->depth = c->depth - (int64_t)(c->key.size() - k);
+        c->key.erase(c->key.begin(), c->key.begin() + k);
+        c->slots.erase(c->slots.begin(), c->slots.begin() + k);
+        c->parent->children[top->key[0]] = top;
+        top->children[c->key[0]] = c;
+        c->parent = top;
+        return top;
+    }
+
+    // Walk the cached path of tokens[0:n]: split where it ends inside an edge, stamp every
+    // node on it, optionally collect slots.  Returns the matched length; *last = end node.
+    int64_t walk(const int32_t* tokens, int64_t n, int32_t* out_slots, rx::Node** last) {
+        rx::Node* x = &root;
+        int64_t pos = 0;
+        while (pos < n) {
+            auto it = x->children.find(tokens[pos]);
+            if (it == x->children.end()) break;
+            rx::Node* c = it->second;
+            const size_t len = c->key.size();
+            const int64_t lim = std::min<int64_t>((int64_t)len, n - pos);
+            int64_t k = 1;
+            while (k < lim && c->key[k] == tokens[pos + k]) ++k;
+            if ((size_t)k < len) c = split(c, (size_t)k);
+            c->stamp = clock;
+            if (out_slots) std::memcpy(out_slots + pos, c->slots.data(), sizeof(int32_t) * (size_t)k);
+            pos += k;
+            x = c;
+            if ((size_t)k < len) break;
+        }
+        *last = x;
+        return pos;
+    }
+};
+
+using rx::set_error;
+
+extern "C" {
+
+const char* rx_last_error(void) { return rx::g_last_error.c_str(); }
+
+const char* rx_version(void) { return "radixattn 0.1 (sm_103a)"; }
+
+int radix_create(int64_t num_slots, uint64_t slot_perm_seed, rx_radix** out) {
+    RX_REQUIRE(out != nullptr, "radix_create: out is NULL");
+    RX_REQUIRE(num_slots >= 1 && num_slots <= INT32_MAX, "radix_create: num_slots %lld out of range",
+               (long long)num_slots);
+    rx_radix* t = new (std::nothrow) rx_radix();
+    if (!t) {
+        set_error("radix_create: out of host memory");
+        return RX_ENOMEM;
+    }
+    try {
+        t->num_slots = num_slots;
+        std::vector<std::pair<uint64_t, int32_t>> keyed((size_t)num_slots);
+        for (int64_t i = 0; i < num_slots; ++i)
+            keyed[(size_t)i] = {rx::splitmix64_at(slot_perm_seed, (uint64_t)i + 1), (int32_t)i};
+        std::sort(keyed.begin(), keyed.end());
+        t->ring.resize((size_t)num_slots);
+        for (int64_t i = 0; i < num_slots; ++i) t->ring[(size_t)i] = keyed[(size_t)i].second;
+        t->count = num_slots;
+        t->is_free.assign((size_t)num_slots, 1);
+    } catch (const std::bad_alloc&) {
+        delete t;
+        set_error("radix_create: out of host memory");
+        return RX_ENOMEM;
+    }
+    t->root.id = 0;
+    t->by_id[0] = &t->root;
+    t->st.num_slots = num_slots;
+    *out = t;
+    return RX_OK;
+}
+
+void radix_destroy(rx_radix* t) { delete t; }
+
+int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slots, int64_t* out_len,
+                 rx_node* out_last) {
+    RX_REQUIRE(t && out_len && out_last && n >= 0 && (n == 0 || (tokens && out_slots)),
+               "match_prefix: bad arguments");
+    t->clock += 1;
+    rx::Node* last = nullptr;
+    const int64_t m = t->walk(tokens, n, out_slots, &last);
+    t->st.match_calls += 1;
+    t->st.match_query_tokens += n;
+    t->st.match_hit_tokens += m;
+    *out_len = m;
+    *out_last = last->id;
+    return RX_OK;
+}
+
+int radix_lock(rx_radix* t, rx_node node) {
+    RX_REQUIRE(t, "radix_lock: tree is NULL");
+    auto it = t->by_id.find(node);
+    RX_REQUIRE(it != t->by_id.end(), "radix_lock: unknown node %lld", (long long)node);
+    for (rx::Node* x = it->second; x != &t->root; x = x->parent) x->ref += 1;
+    return RX_OK;
+}
+
+int radix_unlock(rx_radix* t, rx_node node) {
+    RX_REQUIRE(t, "radix_unlock: tree is NULL");
+    auto it = t->by_id.find(node);
+    RX_REQUIRE(it != t->by_id.end(), "radix_unlock: unknown node %lld", (long long)node);
+    for (rx::Node* x = it->second; x != &t->root; x = x->parent)
+        if (x->ref <= 0) {
+            set_error("radix_unlock: node %lld is not locked", (long long)node);
+            return RX_ELOCKED;
+        }
+    for (rx::Node* x = it->second; x != &t->root; x = x->parent) x->ref -= 1;
+    return RX_OK;
+}
+
+int alloc_slots(rx_radix* t, int64_t n, int32_t* out_slots) {
+    RX_REQUIRE(t && n >= 0 && (n == 0 || out_slots), "alloc_slots: bad arguments");
+    if (n > t->count) {
+        set_error("alloc_slots: %lld slots requested, %lld free", (long long)n, (long long)t->count);
+        return RX_ENOMEM;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t s = t->ring[(size_t)((t->head + i) % t->num_slots)];
+        out_slots[i] = s;
+        t->is_free[(size_t)s] = 0;
+    }
+    t->head = (t->head + n) % t->num_slots;
+    t->count -= n;
+    return RX_OK;
+}
+
+int free_slots(rx_radix* t, const int32_t* slots, int64_t n) {
+    RX_REQUIRE(t && n >= 0 && (n == 0 || slots), "free_slots: bad arguments");
+    int64_t i = 0;
+    for (; i < n; ++i) {
+        const int32_t s = slots[i];
+        if (s < 0 || s >= t->num_slots || t->is_free[(size_t)s]) break;
+        t->is_free[(size_t)s] = 1;   // mark now to catch repeats within the call
+    }
+    if (i < n) {
+        const int32_t bad = slots[i];
+        for (int64_t j = 0; j < i; ++j) t->is_free[(size_t)slots[j]] = 0;   // roll back
+        set_error("free_slots: slot %d is out of range, already free or repeated", bad);
+        return RX_EINVAL;
+    }
+    for (i = 0; i < n; ++i) {
+        t->ring[(size_t)((t->head + t->count) % t->num_slots)] = slots[i];
+        t->count += 1;
+    }
+    return RX_OK;
+}
+
+int insert(rx_radix* t, const int32_t* tokens, const int32_t* slots, int64_t n, int64_t* out_dup_len,
+           rx_node* out_last) {
+    RX_REQUIRE(t && out_dup_len && out_last && n >= 0 && (n == 0 || (tokens && slots)),
+               "insert: bad arguments");
+    // Validate the slots the tree would take before changing anything.
+    {
+        rx::Node* x = &t->root;
+        int64_t pos = 0;   // non-mutating walk to find dup_len
+        while (pos < n) {
+            auto it = x->children.find(tokens[pos]);
+            if (it == x->children.end()) break;
+            rx::Node* c = it->second;
+            const int64_t lim = std::min<int64_t>((int64_t)c->key.size(), n - pos);
+            int64_t k = 1;
+            while (k < lim && c->key[k] == tokens[pos + k]) ++k;
+            pos += k;
+            if (k < (int64_t)c->key.size()) break;
+            x = c;
+        }
+        for (int64_t i = pos; i < n; ++i)
+            RX_REQUIRE(slots[i] >= 0 && slots[i] < t->num_slots && !t->is_free[(size_t)slots[i]],
+                       "insert: slot %d at position %lld is out of range or free", slots[i], (long long)i);
+    }
+    t->clock += 1;
+    rx::Node* x = nullptr;
+    const int64_t dup = t->walk(tokens, n, nullptr, &x);
+    if (dup < n) {
+        rx::Node* leaf = t->new_node();
+        leaf->parent = x;
+        leaf->key.assign(tokens + dup, tokens + n);
+        leaf->slots.assign(slots + dup, slots + n);
+        leaf->stamp = t->clock;
+        leaf->depth = x->depth + (n - dup);
+        x->children[tokens[dup]] = leaf;
+        x = leaf;
+        t->st.cached_tokens += n - dup;
+        t->st.inserted_tokens += n - dup;
+    }
+    t->st.insert_calls += 1;
+    *out_dup_len = dup;
+    *out_last = x->id;
+    return RX_OK;
+}
+
+int evict(rx_radix* t, int64_t num_tokens, int32_t* out_freed, int64_t cap, int64_t* out_n) {
+    RX_REQUIRE(t && out_n && num_tokens >= 0 && cap >= 0, "evict: bad arguments");
+    using Item = std::tuple<uint64_t, int64_t, rx::Node*>;
+    std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
+    // Collect the evictable leaves.
+    std::vector<rx::Node*> stack{&t->root};
+    while (!stack.empty()) {
+        rx::Node* x = stack.back();
+        stack.pop_back();
+        if (x != &t->root && x->children.empty() && x->ref == 0) heap.emplace(x->stamp, x->id, x);
+        for (auto& kv : x->children) stack.push_back(kv.second);
+    }
+    int64_t freed = 0;
+    while (freed < num_tokens && !heap.empty()) {
+        rx::Node* x = std::get<2>(heap.top());
+        heap.pop();
+        for (int32_t s : x->slots) {
+            if (out_freed && freed < cap) out_freed[freed] = s;
+            t->push_free(s);
+            ++freed;
+        }
+        rx::Node* p = x->parent;
+        p->children.erase(x->key[0]);
+        t->st.cached_tokens -= (int64_t)x->key.size();
+        t->by_id.erase(x->id);
+        --t->st.node_count;
+        delete x;
+        if (p != &t->root && p->children.empty() && p->ref == 0) heap.emplace(p->stamp, p->id, p);
+    }
+    t->st.evicted_tokens += freed;
+    *out_n = freed;
+    return RX_OK;
+}
+
+int match_prefix_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
+                       int32_t* out_slots, int64_t* out_indptr, rx_node* out_last) {
+    RX_REQUIRE(t && batch >= 0 && tok_indptr && out_indptr && (batch == 0 || out_last),
+               "match_prefix_batch: bad arguments");
+    out_indptr[0] = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t n = tok_indptr[b + 1] - tok_indptr[b];
+        RX_REQUIRE(n >= 0 && tok_indptr[b] >= 0, "match_prefix_batch: bad tok_indptr at %d", b);
+        int64_t len = 0;
+        const int rc = match_prefix(t, tokens + tok_indptr[b], n, out_slots + out_indptr[b], &len, out_last + b);
+        if (rc != RX_OK) return rc;
+        out_indptr[b + 1] = out_indptr[b] + len;
+    }
+    return RX_OK;
+}
+
+int insert_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
+                 const int32_t* slots, int64_t* out_dup_len, rx_node* out_last) {
+    RX_REQUIRE(t && batch >= 0 && tok_indptr && (batch == 0 || (out_dup_len && out_last)),
+               "insert_batch: bad arguments");
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t n = tok_indptr[b + 1] - tok_indptr[b];
+        RX_REQUIRE(n >= 0 && tok_indptr[b] >= 0, "insert_batch: bad tok_indptr at %d", b);
+        const int rc = insert(t, tokens + tok_indptr[b], slots + tok_indptr[b], n, out_dup_len + b, out_last + b);
+        if (rc != RX_OK) return rc;
+    }
+    return RX_OK;
+}
+
+int radix_stats(const rx_radix* t, rx_stats* out) {
+    RX_REQUIRE(t && out, "radix_stats: bad arguments");
+    *out = t->st;
+    out->free_slots = t->count;
+    out->num_slots = t->num_slots;
+    return RX_OK;
+}
+
+int radix_check(const rx_radix* t) {
+    RX_REQUIRE(t, "radix_check: tree is NULL");
+    std::vector<uint8_t> owned((size_t)t->num_slots, 0);
+    int64_t nodes = 0, tokens = 0;
+    std::vector<const rx::Node*> stack{&t->root};
+    while (!stack.empty()) {
+        const rx::Node* x = stack.back();
+        stack.pop_back();
+        int64_t child_ref = 0;
+        for (auto& kv : x->children) {
+            const rx::Node* c = kv.second;
+            RX_REQUIRE(c->parent == x, "radix_check: node %lld has a wrong parent", (long long)c->id);
+            RX_REQUIRE(!c->key.empty() && c->key.size() == c->slots.size(),
+                       "radix_check: node %lld has an empty or unbalanced edge", (long long)c->id);
+            RX_REQUIRE(c->key[0] == kv.first, "radix_check: node %lld is filed under a wrong token",
+                       (long long)c->id);
+            RX_REQUIRE(c->depth == x->depth + (int64_t)c->key.size(), "radix_check: node %lld depth",
+                       (long long)c->id);
+            RX_REQUIRE(x == &t->root || c->stamp <= x->stamp,
+                       "radix_check: node %lld is more recent than its parent", (long long)c->id);
+            RX_REQUIRE(c->ref >= 0, "radix_check: node %lld has a negative lock count", (long long)c->id);
+            auto it = t->by_id.find(c->id);
+            RX_REQUIRE(it != t->by_id.end() && it->second == c, "radix_check: handle of node %lld",
+                       (long long)c->id);
+            child_ref += c->ref;
+            stack.push_back(c);
+        }
+        RX_REQUIRE(x == &t->root || x->ref >= child_ref, "radix_check: node %lld holds fewer locks than its children",
+                   (long long)x->id);
+        if (x != &t->root) {
+            ++nodes;
+            tokens += (int64_t)x->key.size();
+            for (int32_t s : x->slots) {
+                RX_REQUIRE(s >= 0 && s < t->num_slots, "radix_check: slot %d out of range", s);
+                RX_REQUIRE(!owned[(size_t)s], "radix_check: slot %d held twice", s);
+                RX_REQUIRE(!t->is_free[(size_t)s], "radix_check: slot %d is cached and free", s);
+                owned[(size_t)s] = 1;
+            }
+        }
+    }
+    RX_REQUIRE(nodes == t->st.node_count && (int64_t)t->by_id.size() == nodes + 1,
+               "radix_check: node count %lld vs %lld", (long long)nodes, (long long)t->st.node_count);
+    RX_REQUIRE(tokens == t->st.cached_tokens, "radix_check: cached tokens %lld vs %lld", (long long)tokens,
+               (long long)t->st.cached_tokens);
+    int64_t nfree = 0;
+    for (uint8_t f : t->is_free) nfree += f;
+    RX_REQUIRE(nfree == t->count, "radix_check: free bitmap %lld vs ring %lld", (long long)nfree,
+               (long long)t->count);
+    for (int64_t i = 0; i < t->count; ++i) {
+        const int32_t s = t->ring[(size_t)((t->head + i) % t->num_slots)];
+        RX_REQUIRE(t->is_free[(size_t)s], "radix_check: ring holds a used slot %d", s);
+    }
+    return RX_OK;
+}
+
+int radix_shared_groups(const rx_radix* t, const rx_node* last_nodes, int32_t batch, int64_t min_shared,
+                        int32_t* out_group_of, int64_t* out_group_len, int32_t* out_num_groups) {
+    RX_REQUIRE(t && batch >= 0 && out_num_groups && (batch == 0 || (last_nodes && out_group_of && out_group_len)),
+               "radix_shared_groups: bad arguments");
+    // Root paths of every request's end node (root excluded), shallow to deep.
+    std::vector<std::vector<const rx::Node*>> paths((size_t)batch);
+    for (int32_t b = 0; b < batch; ++b) {
+        auto it = t->by_id.find(last_nodes[b]);
+        RX_REQUIRE(it != t->by_id.end(), "radix_shared_groups: unknown node %lld", (long long)last_nodes[b]);
+        for (const rx::Node* x = it->second; x != &t->root; x = x->parent) paths[(size_t)b].push_back(x);
+        std::reverse(paths[(size_t)b].begin(), paths[(size_t)b].end());
+    }
+    std::unordered_map<const rx::Node*, std::vector<int32_t>> by_top;
+    std::vector<const rx::Node*> order;
+    for (int32_t b = 0; b < batch; ++b) {
+        out_group_of[b] = -1;
+        if (paths[(size_t)b].empty()) continue;
+        const rx::Node* top = paths[(size_t)b][0];
+        auto& v = by_top[top];
+        if (v.empty()) order.push_back(top);
+        v.push_back(b);
+    }
+    int32_t ng = 0;
+    for (const rx::Node* top : order) {
+        const auto& mem = by_top[top];
+        if (mem.size() < 2) continue;
+        size_t common = paths[(size_t)mem[0]].size();
+        for (int32_t b : mem) {
+            const auto& p = paths[(size_t)b];
+            size_t i = 0;
+            while (i < common && i < p.size() && p[i] == paths[(size_t)mem[0]][i]) ++i;
+            common = i;
+        }
+        const int64_t len = paths[(size_t)mem[0]][common - 1]->depth;
+        if (len < min_shared) continue;
+        for (int32_t b : mem) out_group_of[b] = ng;
+        out_group_len[ng] = len;
+        ++ng;
+    }
+    *out_num_groups = ng;
+    return RX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,184 @@
+"""Host C++ radix tree (through the C ABI) against the oracle's prefix-cache model.
+
+No GPU needed: the tree and allocator are host code.  Slots, match lengths, dup lengths,
+eviction order, node counts and free-list order must be bit-exact against the oracle.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+from oracle import PrefixCacheModel, slot_order
+from prefix_cached_kv_radix_gb300 import api
+
+api.load()
+
+
+def test_allocator_order_matches_oracle():
+    t = api.RadixTree(1000, 123)
+    got = t.alloc_slots(1000)
+    assert got.tolist() == slot_order(1000, 123).tolist()
+    with pytest.raises(api.RxError) as e:
+        t.alloc_slots(1)
+    assert e.value.code == api.RX_ENOMEM
+    t.free_slots(got[[5, 3]])
+    assert t.alloc_slots(2).tolist() == [got[5], got[3]]
+
+
+def test_free_slot_errors_leave_state_unchanged():
+    t = api.RadixTree(16, 1)
+    s = t.alloc_slots(4)
+    with pytest.raises(api.RxError):
+        t.free_slots([s[0], s[0]])
+    with pytest.raises(api.RxError):
+        t.free_slots([s[1], 99])
+    assert t.stats()["free_slots"] == 12
+    t.free_slots(s)
+    assert t.stats()["free_slots"] == 16
+    t.check()
+
+
+def test_insert_rejects_unallocated_slots():
+    t = api.RadixTree(16, 1)
+    free_slot = int(slot_order(16, 1)[0])
+    with pytest.raises(api.RxError):
+        t.insert([1, 2], [free_slot, free_slot])
+    with pytest.raises(api.RxError):
+        t.insert([1], [16])
+
+
+def test_lock_semantics():
+    t = api.RadixTree(64, 0)
+    a = t.alloc_slots(3)
+    _, na = t.insert([1, 1, 1], a)
+    b = t.alloc_slots(3)
+    _, nb = t.insert([2, 2, 2], b)
+    t.lock(na)
+    assert t.evict(100).tolist() == b.tolist()
+    assert t.evict(100).tolist() == []
+    t.unlock(na)
+    with pytest.raises(api.RxError) as e:
+        t.unlock(na)
+    assert e.value.code == api.RX_ELOCKED
+    assert t.evict(1).tolist() == a.tolist()
+    with pytest.raises(api.RxError):
+        t.lock(na)                     # evicted node: unknown handle
+    t.check()
+
+
+def _run_script(ops, num_slots, seed):
+    """Apply the same operations to the C++ tree and the oracle model; compare everything."""
+    t = api.RadixTree(num_slots, seed)
+    m = PrefixCacheModel(num_slots, seed)
+    for op, arg in ops:
+        if op == "match":
+            s1, n1, _ = t.match_prefix(arg)
+            n2, s2 = m.match(arg)
+            assert n1 == n2 and s1.tolist() == s2.tolist()
+        elif op == "insert":
+            n_free = t.stats()["free_slots"]
+            if n_free < len(arg):
+                continue
+            new = t.alloc_slots(len(arg))
+            new2 = m.alloc.alloc(len(arg))
+            assert new.tolist() == new2.tolist()
+            d1, _ = t.insert(arg, new)
+            d2 = m.insert(arg, new2)
+            assert d1 == d2
+            t.free_slots(new[:d1])
+            m.alloc.release(new2[:d2])
+        elif op == "evict":
+            f1 = t.evict(arg)
+            f2 = m.evict(arg)
+            assert f1.tolist() == f2.tolist()
+        st = t.stats()
+        assert st["node_count"] == len(m.nodes())
+        assert st["cached_tokens"] == m.cached_tokens()
+        assert st["free_slots"] == len(m.alloc.free)
+        t.check()
+    # the free lists agree in order too
+    n = t.stats()["free_slots"]
+    assert t.alloc_slots(n).tolist() == m.alloc.alloc(n).tolist()
+
+
+@pytest.mark.parametrize("vocab", [2, 3, 4])
+def test_random_scripts_match_oracle(vocab):
+    rng = np.random.default_rng(100 + vocab)
+    for trial in range(25):
+        ops = []
+        for _ in range(25):
+            r = rng.random()
+            seq = rng.integers(0, vocab, size=rng.integers(1, 11)).tolist()
+            if r < 0.4:
+                ops.append(("match", seq))
+            elif r < 0.85:
+                ops.append(("insert", seq))
+            else:
+                ops.append(("evict", int(rng.integers(1, 8))))
+        _run_script(ops, 48, trial)
+
+
+def test_exhaustive_short_sequences():
+    seqs = [list(s) for L in range(1, 4) for s in itertools.product([0, 1], repeat=L)]
+    ops = []
+    for s in seqs:
+        ops.append(("insert", s))
+    for s in seqs:
+        ops.append(("match", s + [2]))
+    ops += [("evict", 3), ("match", [0, 1]), ("evict", 5), ("insert", [1, 1, 1, 1]), ("evict", 100)]
+    _run_script(ops, 64, 9)
+
+
+def test_batch_entry_points_equal_single_calls():
+    rng = np.random.default_rng(7)
+    seqs = [rng.integers(0, 3, size=rng.integers(1, 9)).astype(np.int32) for _ in range(20)]
+    t1, t2 = api.RadixTree(512, 3), api.RadixTree(512, 3)
+    ind = np.concatenate([[0], np.cumsum([len(s) for s in seqs])])
+    flat = np.concatenate(seqs)
+    slots = t1.alloc_slots(len(flat))
+    assert slots.tolist() == t2.alloc_slots(len(flat)).tolist()
+    dups, lasts = t1.insert_batch(flat, ind, slots)
+    for i, s in enumerate(seqs):
+        d, l = t2.insert(s, slots[ind[i]:ind[i + 1]])
+        assert d == dups[i] and l == lasts[i]
+    q = [np.concatenate([s, [5]]).astype(np.int32) for s in seqs]
+    qind = np.concatenate([[0], np.cumsum([len(s) for s in q])])
+    ms, mind, ml = t1.match_prefix_batch(np.concatenate(q), qind)
+    for i, s in enumerate(q):
+        s2, n2, l2 = t2.match_prefix(s)
+        assert mind[i + 1] - mind[i] == n2 and ms[mind[i]:mind[i + 1]].tolist() == s2.tolist() and ml[i] == l2
+    assert t1.stats() == t2.stats()
+
+
+def test_shared_groups():
+    t = api.RadixTree(4096, 0)
+    shared = list(range(100, 140))                       # 40-token shared prefix
+    seqs = [shared + [1000 + i, 7, 7] for i in range(5)] + [[9, 9, 9, 9]] + [shared[:10] + [55]]
+    lasts = []
+    for s in seqs:
+        sl = t.alloc_slots(len(s))
+        d, l = t.insert(s, sl)
+        t.free_slots(sl[:d])
+        lasts.append(l)
+    gof, glen = t.shared_groups(lasts, min_shared=1)
+    # the five requests share 40 tokens; the 7th shares only 10 with them -> all 6 under
+    # one top node with common depth 10; [9,9,9,9] is alone
+    assert gof.tolist() == [0, 0, 0, 0, 0, -1, 0] and glen.tolist() == [10]
+    gof, glen = t.shared_groups(lasts[:5], min_shared=1)
+    assert gof.tolist() == [0] * 5 and glen.tolist() == [40]
+    gof, glen = t.shared_groups(lasts[:5], min_shared=41)
+    assert gof.tolist() == [-1] * 5 and len(glen) == 0
+
+
+def test_nine_step_walkthrough_on_the_tree():
+    """The walk-through's event script run on the C++ tree and the oracle side by side."""
+    SYS = [1, 2, 3, 4]
+    ops = [("insert", SYS + [10, 11, 12, 12]),
+           ("match", SYS + [10, 11, 12, 12, 13]), ("insert", SYS + [10, 11, 12, 12, 13, 14, 14]),
+           ("match", SYS + [20, 21]), ("insert", SYS + [20, 21, 22, 22]),
+           ("match", SYS + [20, 21, 22, 22, 23]), ("evict", 3), ("insert", SYS + [20, 21, 22, 22, 23, 24, 24]),
+           ("insert", [30, 31, 32, 33, 34, 35, 36]),
+           ("insert", [30, 31, 32, 33, 34, 40, 36]), ("insert", [30, 31, 32, 33, 34, 41, 36]),
+           ("match", SYS + [10, 11, 12, 12, 15]), ("evict", 4), ("insert", SYS + [10, 11, 12, 12, 15, 16, 16, 16]),
+           ("evict", 3), ("insert", SYS + [10, 11, 12, 12, 15, 50, 50, 50])]
+    _run_script(ops, 64, 0)

@@ -1,0 +1,408 @@
+"""Benchmark: prefix-cached attention steps on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload c2]
+
+One step is one pass of the whole hot path over one batch: host radix match and slot
+allocation, upload of the step's index arrays, kv_pool_write (slot table + K/V scatter),
+the attention kernel(s) (extend, or split-KV decode + merge), insert of the new tokens
+and LRU eviction of as many cached tokens (so the cache stays at a steady size).  Every
+step's requests carry fresh new-token ids, so each step is a new batch of requests that
+hits the cached prefix.  Inputs (Q and the new K/V) are resident in HBM when the timed
+region starts; the e2e figure repeats the step through the same public calls with the
+inputs in pinned host memory, copying them in and the outputs back inside the timed region.
+
+Prints one JSON line.  With N > 1 (torchrun) every rank runs its own replica of the
+workload on its own GPU (the path shards over independent requests; no collective is
+needed), value = all ranks' tokens / max over ranks of the time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "prefix-cached attention tokens/s; % HBM (decode) / % bf16 TC peak (extend)"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------- work model
+def algorithmic_work(w):
+    """Attention FLOPs (4*D per causal (row, key) pair per q head) and unique bytes."""
+    s = w.spec
+    pairs = 0
+    for b in range(w.batch):
+        P, n = s.req_cached[b], s.req_new[b]
+        pairs += n * P + n * (n + 1) // 2
+    flops = 4.0 * s.d * s.hq * pairs
+    elt = 4 if s.dtype == "f32" else 2
+    row = s.hkv * s.d * elt * 2          # K + V per token
+    # unique KV the step must read: union of the contexts (shared prefixes once)
+    uniq = set()
+    tot_ctx = 0
+    for b in range(w.batch):
+        path = w.seg_path(s.req_seg[b])
+        c = s.req_cached[b]
+        acc = 0
+        for seg in path:
+            take = min(s.seg_len[seg], c - acc)
+            if take <= 0:
+                break
+            uniq.add((seg, take))
+            acc += take
+        tot_ctx += c + s.req_new[b]
+    seg_take = {}
+    for seg, take in uniq:
+        seg_take[seg] = max(seg_take.get(seg, 0), take)
+    uniq_tokens = sum(seg_take.values()) + w.total_new()
+    qo_bytes = 2 * w.total_new() * s.hq * s.d * elt
+    idx_bytes = 4 * tot_ctx
+    return dict(flops=flops, pairs=pairs, kv_unique_bytes=uniq_tokens * row,
+                bytes=uniq_tokens * row + qo_bytes + idx_bytes, kv_naive_bytes=tot_ctx * row)
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], f[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- our arm
+def fresh_prompts(w, step, used):
+    """The workload's prompts with step-specific new-token ids.  Requests that diverge from
+    the cache at the same point get distinct first tokens, which also differ from the
+    cached continuation there and from every first token used there in earlier steps, so
+    each step inserts exactly its new tokens as fresh leaves."""
+    s = w.spec
+    rng = np.random.default_rng([s.seed, 9000, step])
+    prompts = []
+    for b in range(w.batch):
+        n = s.req_new[b]
+        new = rng.integers(0, s.vocab, size=n).astype(np.int32)
+        base = w.request_prefix_tokens(b)
+        key = (s.req_seg[b], s.req_cached[b])
+        if key not in used:
+            forb = used[key] = set()
+            path = w.path_tokens(s.req_seg[b])
+            if s.req_cached[b] < len(path):
+                forb.add(int(path[s.req_cached[b]]))
+            for bb in range(w.batch):        # the workload's own first tokens at this point
+                if (s.req_seg[bb], s.req_cached[bb]) == key and s.req_new[bb]:
+                    forb.add(int(w.req_tokens[bb][0]))
+        forb = used[key]
+        if n:
+            while int(new[0]) in forb:
+                new[0] = int(rng.integers(0, s.vocab))
+            forb.add(int(new[0]))
+        prompts.append(np.concatenate([base, new]).astype(np.int32))
+    return prompts
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine, _dev_from_host
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    spec = W.config(args.workload)
+    w = W.generate(spec)
+    s = spec
+    eng = PrefixCacheEngine(s.dtype, s.hq, s.hkv, s.d, s.num_slots, s.seed, device=str(dev), poison=False)
+    for i in range(len(s.histories)):
+        k, v = w.history_kv(i)
+        eng.populate(w.history_tokens(i), k, v)
+    q, kn, vn = w.stacked_new()
+    qd, kd, vd = (_dev_from_host(x, s.dtype, dev) for x in (q, kn, vn))
+    out = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[0], s.hq, dtype=torch.float32, device=dev)
+    # pinned host copies for the end-to-end variant
+    qh, kh, vh = (x.cpu().pin_memory() for x in (qd, kd, vd))
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    T = w.total_new()
+    used = {}
+    stream = torch.cuda.current_stream()
+    att_ev = []
+    launches = [0]
+
+    def step(i, e2e=False, timed_att=False):
+        prompts = fresh_prompts(w, i, used)
+        plan = eng.plan(prompts, s.req_new)
+        d = eng.upload(plan)
+        if e2e:
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+        eng.write(plan, d, kd, vd)
+        if timed_att:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        if s.decode:
+            grp, keep = eng.groups(plan)
+            d["_keep"] = keep
+            eng.decode(plan, d, qd, out, lse, groups=grp)
+            # kv_pool_write + (group map, group fill, shared chunks) + private chunks + merge
+            n_launch = 1 + (3 if grp is not None else 0) + 2
+        else:
+            eng.extend(plan, d, qd, out, lse)
+            n_launch = 2   # kv_pool_write + extend
+        if timed_att or e2e:
+            launches[0] += n_launch
+        if timed_att:
+            e1.record(stream)
+            att_ev.append((e0, e1))
+        if e2e:
+            out_h.copy_(out, non_blocking=True)
+        eng.finish(plan, evict_tokens=T)
+        return plan
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if eng.device_status() != 0:
+        raise RuntimeError(f"device status {eng.device_status()} after warm-up")
+
+    def timed(e2e):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        times = []
+        for i in range(args.steps):
+            flush.zero_()                      # untimed: evict L2 between timed steps
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step(args.warmup + (args.steps if e2e else 0) + i, e2e=e2e, timed_att=not e2e)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ms = sum(a.elapsed_time(b) for a, b in times)
+        return ms
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ms = timed(False)
+    ms_e2e = timed(True)
+    clk = clocks.stop()
+    if eng.device_status() != 0:
+        raise RuntimeError(f"device status {eng.device_status()} after timed steps")
+    if world > 1:
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+    att_ms = [a.elapsed_time(b) for a, b in att_ev]
+    work = algorithmic_work(w)
+    hbm, bf16, bf16_s, src = load_peaks()
+    att = statistics.mean(att_ms) if att_ms else float("nan")
+    if s.decode:
+        achieved = work["bytes"] / (att * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": None, "kernel": "decode_attention (split-KV + merge)",
+                "algorithmic": f"{work['bytes'] / 1e9:.4f} GB unique (KV {work['kv_unique_bytes'] / 1e9:.4f} GB + Q/O + indices) per launch",
+                "launch_ms": att, "peak_source": f"{src} hbm_gbs"}
+    else:
+        achieved = work["flops"] / (att * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
+                "traffic": None, "kernel": "prefix_extend_attention (tcgen05)" if s.dtype == "bf16" else "prefix_extend_attention (CUDA cores, fp32)",
+                "algorithmic": f"{work['flops'] / 1e9:.3f} GFLOP per launch (4*D per causal pair per q head)",
+                "launch_ms": att, "peak_source": f"{src} bf16_tflops (burst)"}
+    tokens = T * args.steps * world
+    value = tokens / (ms * 1e-3)
+    h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+    d2h = out_h.numel() * out_h.element_size()
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if s.dtype == "f32" else "bf16", "data": "synthetic (seeded N(0,1) Q/K/V, uniform token ids)",
+        "config": {"workload": f"{s.name}: {s.note}", "batch": w.batch, "new_tokens_per_step": T,
+                   "cached_prefix_tokens": int(sum(s.req_cached)), "heads": f"{s.hq}/{s.hkv}x{s.d}",
+                   "kv_pool_slots": s.num_slots, "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches[0] // 2,   # per timed region (value); the e2e region launches as many
+        "clocks": clk,
+        "radix_stats": eng.tree.stats(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- oracle timing
+def oracle_step(w, rows_per_request=None):
+    """The oracle's own version of one step: list matcher + slot allocator replay for the
+    table, fp64 attention for the output rows.  Returns (tokens computed, threads)."""
+    import oracle
+    s = w.spec
+    lm = oracle.ListMatcher()
+    for i in range(len(s.histories)):
+        lm.add(w.history_tokens(i), np.zeros(len(w.history_tokens(i)), np.int32))
+    done = 0
+    for b in range(w.batch):
+        lm.match(w.request_tokens(b))
+        n = s.req_new[b]
+        idx = np.arange(n) if rows_per_request is None else np.arange(min(n, rows_per_request))
+        if len(idx) == 0:
+            continue
+        k, v = w.request_kv(b)
+        k = W.bf16_bits_to_f32(k) if s.dtype == "bf16" else k
+        v = W.bf16_bits_to_f32(v) if s.dtype == "bf16" else v
+        q = W.bf16_bits_to_f32(w.req_q[b]) if s.dtype == "bf16" else w.req_q[b]
+        oracle.attention_rows(q[idx], s.req_cached[b] + idx, k, v, s.scale)
+        done += len(idx)
+    return done, oracle.max_threads()
+
+
+def cpu_baseline(w, seconds):
+    """Time the oracle (as it stands) on the host cores on a bounded sample of the step."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    toks, reps = 0, 0
+    rows = None
+    s = w.spec
+    if s.name in ("c3", "c5"):
+        rows = 8            # a few rows per request: full rows would take minutes to hours
+    while True:
+        n, thr = oracle_step(w, rows)
+        toks += n
+        reps += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    sample = (f"{reps} full oracle step(s) of {s.name} (list matcher + fp64 attention of every new row)"
+              if rows is None else f"{reps} oracle pass(es) of {s.name} with the first {rows} new rows per request")
+    return {"value": toks / dt, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample, "seconds": dt}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    spec = W.config(args.workload)
+    w = W.generate(spec)
+    cb = cpu_baseline(w, args.cpu_seconds)
+    for _ in range(args.warmup):
+        pass
+    # the reference arm is the oracle: steps are bounded samples of the workload
+    t0 = time.perf_counter()
+    toks = 0
+    rows = 8 if spec.name in ("c3", "c5") else None
+    for _ in range(args.steps):
+        n, _thr = oracle_step(w, rows)
+        toks += n
+    dt = time.perf_counter() - t0
+    v = toks / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": f"{spec.name}: {spec.note}", "batch": w.batch,
+                       "sample": "full step" if rows is None else f"first {rows} new rows per request"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c2", choices=list(W.CONFIG_NAMES))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -113,6 +113,13 @@ int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slo
 int radix_lock(rx_radix* t, rx_node node);
 int radix_unlock(rx_radix* t, rx_node node);
 
+/* Lock / unlock n nodes, as n radix_lock / radix_unlock calls (an in-flight batch pins the
+ * prefixes it matched so that eviction during the step cannot free them).  The lock batch
+ * checks every handle first and changes nothing on an unknown one; the unlock batch stops
+ * at the first node that is not locked (RX_ELOCKED). */
+int radix_lock_batch(rx_radix* t, const rx_node* nodes, int32_t n);
+int radix_unlock_batch(rx_radix* t, const rx_node* nodes, int32_t n);
+
 /* Pop n free slots (FIFO) into out_slots; RX_ENOMEM and nothing taken if fewer are free.
  * Never evicts on its own: the caller calls evict and retries. */
 int alloc_slots(rx_radix* t, int64_t n, int32_t* out_slots);

@@ -20,7 +20,8 @@ RX_DEV_OK, RX_DEV_BAD_SLOT, RX_DEV_BAD_LENGTH, RX_DEV_TIMEOUT = 0, 1, 2, 3
 RX_F32, RX_BF16 = 0, 1
 
 EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "radix_lock", "radix_unlock", "alloc_slots",
-           "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "radix_stats", "radix_check",
+           "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "radix_lock_batch",
+           "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups",
            "kv_pool_write", "prefix_extend_attention", "decode_workspace_bytes", "decode_attention",
            "rx_last_error", "rx_version")
@@ -75,6 +76,8 @@ def load(path: str = LIB_PATH):
         "evict": (ctypes.c_int, [P, I64, P, I64, P]),
         "match_prefix_batch": (ctypes.c_int, [P, I32, P, P, P, P, P]),
         "insert_batch": (ctypes.c_int, [P, I32, P, P, P, P, P]),
+        "radix_lock_batch": (ctypes.c_int, [P, P, I32]),
+        "radix_unlock_batch": (ctypes.c_int, [P, P, I32]),
         "radix_stats": (ctypes.c_int, [P, P]),
         "radix_check": (ctypes.c_int, [P]),
         "radix_shared_groups": (ctypes.c_int, [P, P, I32, I64, P, P, P]),
@@ -154,6 +157,16 @@ def radix_lock(tree, node: int) -> None:
 
 def radix_unlock(tree, node: int) -> None:
     _check("radix_unlock", load().radix_unlock(tree, node))
+
+
+def radix_lock_batch(tree, nodes) -> None:
+    a = np.ascontiguousarray(np.asarray(nodes, np.int64))
+    _check("radix_lock_batch", load().radix_lock_batch(tree, a.ctypes.data if len(a) else None, len(a)))
+
+
+def radix_unlock_batch(tree, nodes) -> None:
+    a = np.ascontiguousarray(np.asarray(nodes, np.int64))
+    _check("radix_unlock_batch", load().radix_unlock_batch(tree, a.ctypes.data if len(a) else None, len(a)))
 
 
 def alloc_slots(tree, n: int) -> np.ndarray:
@@ -274,6 +287,12 @@ class RadixTree:
 
     def insert_batch(self, tokens, tok_indptr, slots):
         return insert_batch(self.h, tokens, tok_indptr, slots)
+
+    def lock_batch(self, nodes):
+        return radix_lock_batch(self.h, nodes)
+
+    def unlock_batch(self, nodes):
+        return radix_unlock_batch(self.h, nodes)
 
     def stats(self):
         return radix_stats(self.h)

@@ -225,6 +225,23 @@ int radix_unlock(rx_radix* t, rx_node node) {
     return RX_OK;
 }
 
+int radix_lock_batch(rx_radix* t, const rx_node* nodes, int32_t n) {
+    RX_REQUIRE(t && n >= 0 && (n == 0 || nodes), "radix_lock_batch: bad arguments");
+    for (int32_t i = 0; i < n; ++i)
+        RX_REQUIRE(t->by_id.count(nodes[i]), "radix_lock_batch: unknown node %lld", (long long)nodes[i]);
+    for (int32_t i = 0; i < n; ++i) radix_lock(t, nodes[i]);
+    return RX_OK;
+}
+
+int radix_unlock_batch(rx_radix* t, const rx_node* nodes, int32_t n) {
+    RX_REQUIRE(t && n >= 0 && (n == 0 || nodes), "radix_unlock_batch: bad arguments");
+    for (int32_t i = 0; i < n; ++i) {
+        const int rc = radix_unlock(t, nodes[i]);
+        if (rc != RX_OK) return rc;
+    }
+    return RX_OK;
+}
+
 int alloc_slots(rx_radix* t, int64_t n, int32_t* out_slots) {
     RX_REQUIRE(t && n >= 0 && (n == 0 || out_slots), "alloc_slots: bad arguments");
     if (n > t->count) {

@@ -1,0 +1,191 @@
+"""One attention layer's prefix cache on one GPU: radix tree + KV pools + kernels.
+
+A step over a batch of requests (each a full prompt whose tail is new):
+  a1 match_prefix_batch (host tree)   -> matched slots and lengths P_b
+  a2 alloc_slots (host allocator)     -> slots for the n_b new tokens
+  a3 kv_pool_write (CUDA)             -> req_to_token table, new K/V scattered into the pools
+  a4 prefix_extend_attention (CUDA)   or  a5/a6 decode_attention (CUDA, split-KV + merge)
+  a7 insert_batch (host tree)         -> the new tokens become cached
+  a8 evict (host tree)                -> LRU leaves freed under memory pressure
+"SGLang: Efficient Execution of Structured Language Model Programs" (RadixAttention) and
+"Prompt Caching" (Ultralytics glossary, "How prompt caching works").  This module only
+strings library calls together and moves the step's small index arrays to the device.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import api
+
+
+def _dev_from_host(a, dtype_bits, device):
+    """Host numpy array -> device tensor; bf16 arrives as uint16 bit patterns."""
+    if dtype_bits == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(device, non_blocking=False)
+
+
+@dataclass
+class StepPlan:
+    batch: int
+    tokens: np.ndarray          # concatenated full prompts (cached part + new tokens)
+    tok_indptr: np.ndarray      # [batch+1]
+    prefix_slots: np.ndarray    # packed matched slots
+    prefix_indptr: np.ndarray   # [batch+1]
+    prefix_lens: np.ndarray     # [batch] int32 (P_b)
+    new_slots: np.ndarray       # [T]
+    qo_indptr: np.ndarray       # [batch+1]
+    last_nodes: np.ndarray      # [batch] node where each match ended
+    max_qo_len: int
+    max_kv_len: int
+    stride: int
+
+
+class PrefixCacheEngine:
+    def __init__(self, dtype: str, hq: int, hkv: int, head_dim: int, num_slots: int, seed: int,
+                 device: str = "cuda", poison: bool = True):
+        self.dtype = dtype
+        self.tdtype = torch.float32 if dtype == "f32" else torch.bfloat16
+        self.hq, self.hkv, self.d = hq, hkv, head_dim
+        self.num_slots = num_slots
+        self.device = torch.device(device)
+        self.tree = api.RadixTree(num_slots, seed)
+        self.k_pool = torch.empty(num_slots, hkv, head_dim, dtype=self.tdtype, device=self.device)
+        self.v_pool = torch.empty_like(self.k_pool)
+        if poison:   # unused slots hold NaN so that any stray gather shows up
+            self.k_pool.fill_(float("nan"))
+            self.v_pool.fill_(float("nan"))
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.desc = api.make_desc(api.RX_F32 if dtype == "f32" else api.RX_BF16, hq, hkv, head_dim, num_slots,
+                                  1.0 / float(np.sqrt(head_dim)))
+        self._ws = None
+
+    # ------------------------------------------------------------------ helpers
+    def _i32(self, a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(self.device)
+
+    def _i64(self, a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int64)).to(self.device)
+
+    def device_status(self) -> int:
+        return int(self.status.item())
+
+    # ------------------------------------------------------------------ cached history
+    def populate(self, tokens: np.ndarray, k, v) -> int:
+        """Cache one earlier sequence: match, allocate the uncached tail, write its K/V,
+        insert.  k, v: [len, hkv, d] for the whole sequence (host arrays or device tensors).
+        Returns the number of tokens newly written."""
+        tokens = np.ascontiguousarray(tokens, np.int32)
+        slots, m, _ = self.tree.match_prefix(tokens)
+        n = len(tokens) - m
+        if n == 0:
+            return 0
+        new = self.tree.alloc_slots(n)
+        kn = k[m:] if isinstance(k, torch.Tensor) else _dev_from_host(k[m:], self.dtype, self.device)
+        vn = v[m:] if isinstance(v, torch.Tensor) else _dev_from_host(v[m:], self.dtype, self.device)
+        r2t = torch.empty(1, len(tokens), dtype=torch.int32, device=self.device)
+        api.kv_pool_write(self.desc, 1, self._i32(slots if m else [0]), self._i64([0, m]), self._i32(new),
+                          self._i64([0, n]), kn.contiguous(), vn.contiguous(), self.k_pool, self.v_pool, r2t, n,
+                          self.status)
+        dup, _ = self.tree.insert(tokens, np.concatenate([slots, new]))
+        if dup > m:
+            self.tree.free_slots(new[: dup - m])
+        return n
+
+    # ------------------------------------------------------------------ step
+    def plan(self, prompts, n_new) -> StepPlan:
+        """a1 + a2: match every prompt, check that exactly its last n_new[b] tokens are
+        uncached, allocate their slots."""
+        b = len(prompts)
+        lens = np.array([len(p) for p in prompts], np.int64)
+        tok_indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        tokens = np.concatenate(prompts).astype(np.int32) if b else np.zeros(0, np.int32)
+        ps, pind, last = self.tree.match_prefix_batch(tokens, tok_indptr)
+        P = np.diff(pind).astype(np.int64)
+        n_new = np.asarray(n_new, np.int64)
+        if not np.array_equal(P + n_new, lens):
+            bad = int(np.flatnonzero(P + n_new != lens)[0])
+            raise ValueError(f"request {bad}: {P[bad]} tokens cached, but {lens[bad] - n_new[bad]} expected")
+        T = int(n_new.sum())
+        new = self.tree.alloc_slots(T)
+        self.tree.lock_batch(last)          # in flight: the matched prefixes cannot be evicted
+        qo = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int64)
+        max_kv = int(lens.max()) if b else 1
+        return StepPlan(b, tokens, tok_indptr, ps, pind, P.astype(np.int32), new, qo, last,
+                        int(n_new.max()) if b else 0, max_kv, ((max_kv + 7) // 8) * 8)
+
+    def upload(self, plan: StepPlan) -> dict:
+        """Move the step's index arrays to the device."""
+        return dict(prefix_slots=self._i32(plan.prefix_slots if len(plan.prefix_slots) else [0]),
+                    prefix_indptr=self._i64(plan.prefix_indptr), new_slots=self._i32(plan.new_slots if len(plan.new_slots) else [0]),
+                    qo_indptr=self._i64(plan.qo_indptr), prefix_lens=self._i32(plan.prefix_lens),
+                    kv_lens=self._i32(plan.prefix_lens.astype(np.int64) + np.diff(plan.qo_indptr)),
+                    r2t=torch.empty(max(plan.batch, 1), plan.stride, dtype=torch.int32, device=self.device))
+
+    def write(self, plan: StepPlan, dev: dict, k_new, v_new, stream=None) -> None:
+        """a3: slot table + scatter of the new tokens' K/V."""
+        api.kv_pool_write(self.desc, plan.batch, dev["prefix_slots"], dev["prefix_indptr"], dev["new_slots"],
+                          dev["qo_indptr"], k_new, v_new, self.k_pool, self.v_pool, dev["r2t"],
+                          int(plan.qo_indptr[-1]), self.status, stream)
+
+    def extend(self, plan: StepPlan, dev: dict, q, out, lse=None, stream=None) -> None:
+        """a4: new tokens attend to their cached prefix and causally to themselves."""
+        api.prefix_extend_attention(self.desc, plan.batch, q, dev["qo_indptr"], dev["prefix_lens"], dev["r2t"],
+                                    self.k_pool, self.v_pool, out, lse, plan.max_qo_len, self.status, stream)
+
+    def groups(self, plan: StepPlan, min_shared: int = 64):
+        """Shared-prefix groups of a decode batch from the tree (host), as device arrays."""
+        gof, glen = self.tree.shared_groups(plan.last_nodes, min_shared)
+        if len(glen) == 0:
+            return None, None
+        members = [np.flatnonzero(gof == g) for g in range(len(glen))]
+        indptr = np.concatenate([[0], np.cumsum([len(m) for m in members])]).astype(np.int32)
+        keep = (self._i32(indptr), self._i32(np.concatenate(members)), self._i32(glen))
+        st = api.shared_groups_struct(len(glen), int(max(len(m) for m in members)), *keep, int(glen.max()))
+        return st, keep
+
+    def decode_workspace(self, plan: StepPlan, groups=None):
+        nbytes = api.decode_workspace_bytes(self.desc, plan.batch, plan.max_kv_len, groups)
+        if self._ws is None or self._ws.numel() < nbytes:
+            self._ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def decode(self, plan: StepPlan, dev: dict, q, out, lse=None, groups=None, stream=None) -> None:
+        """a5 + a6: one query token per request over all of its cached tokens."""
+        ws = self.decode_workspace(plan, groups)
+        api.decode_attention(self.desc, plan.batch, q, dev["r2t"], dev["kv_lens"], self.k_pool, self.v_pool, out,
+                             lse, plan.max_kv_len, ws, self.status, groups=groups, stream=stream)
+
+    def commit(self, plan: StepPlan) -> np.ndarray:
+        """a7: insert every prompt with its slots; frees new slots that turned out cached."""
+        slots = np.empty(len(plan.tokens), np.int32)
+        for b in range(plan.batch):
+            t0, t1 = plan.tok_indptr[b], plan.tok_indptr[b + 1]
+            P = plan.prefix_lens[b]
+            slots[t0:t0 + P] = plan.prefix_slots[plan.prefix_indptr[b]:plan.prefix_indptr[b + 1]]
+            slots[t0 + P:t1] = plan.new_slots[plan.qo_indptr[b]:plan.qo_indptr[b + 1]]
+        dup, _ = self.tree.insert_batch(plan.tokens, plan.tok_indptr, slots)
+        extra = []
+        for b in range(plan.batch):
+            d = int(dup[b]) - int(plan.prefix_lens[b])
+            if d > 0:
+                extra.append(plan.new_slots[plan.qo_indptr[b]:plan.qo_indptr[b] + d])
+        if extra:
+            self.tree.free_slots(np.concatenate(extra))
+        return dup
+
+    def release(self, num_tokens: int) -> np.ndarray:
+        """a8: evict least-recently-used unlocked leaves until num_tokens are freed."""
+        return self.tree.evict(num_tokens)
+
+    def finish(self, plan: StepPlan, evict_tokens: int = 0) -> np.ndarray:
+        """End of a step: a7 insert, a8 evict (the step's prefixes still pinned), unpin."""
+        self.commit(plan)
+        freed = self.release(evict_tokens) if evict_tokens else np.zeros(0, np.int32)
+        self.tree.unlock_batch(plan.last_nodes)
+        return freed

@@ -1,0 +1,236 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, element by element.
+
+Small and medium cases that span several tiles and ragged tails, plus edge cases.
+Slot tables are bit-exact; attention is within max-abs 2e-2, mean-abs 2e-3, relative
+Frobenius 1e-2 per head, and log-sum-exp within 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.gpu_cases import (TOL_LSE, compare, expected_slots, f32, oracle_rows, run_step, to_host_f32)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from prefix_cached_kv_radix_gb300 import api
+    api.load()
+
+
+def check_tables(w, eng, plan, dev):
+    pre, new, P = expected_slots(w)
+    assert np.array_equal(plan.prefix_lens, P), "match lengths differ from the oracle"
+    r2t = dev["r2t"].cpu().numpy()
+    for b in range(w.batch):
+        row = np.concatenate([pre[b], new[b]])
+        assert np.array_equal(r2t[b, :len(row)], row), f"slot table row {b}"
+        assert (r2t[b, len(row):] == -1).all()
+    # new K/V rows landed bit-exactly at their slots
+    q, kn, vn = w.stacked_new()
+    allnew = np.concatenate(new) if len(new) else np.zeros(0, np.int32)
+    if len(allnew):
+        kp = eng.k_pool[torch.from_numpy(allnew.astype(np.int64)).cuda()].cpu()
+        vp = eng.v_pool[torch.from_numpy(allnew.astype(np.int64)).cuda()].cpu()
+        if w.spec.dtype == "bf16":
+            assert np.array_equal(kp.view(torch.int16).numpy().view(np.uint16), kn)
+            assert np.array_equal(vp.view(torch.int16).numpy().view(np.uint16), vn)
+        else:
+            assert np.array_equal(kp.numpy(), kn) and np.array_equal(vp.numpy(), vn)
+
+
+def check_attention(w, out, lse, rows=None):
+    got = to_host_f32(out)
+    got_lse = lse.cpu().numpy() if lse is not None else None
+    qo = w.qo_indptr()
+    for b in range(w.batch):
+        if w.spec.req_new[b] == 0:
+            continue
+        idx = None if rows is None else rows[b]
+        want, wl = oracle_rows(w, b, idx)
+        sel = np.arange(qo[b], qo[b + 1]) if idx is None else qo[b] + np.asarray(idx)
+        compare(got[sel], want, f"request {b}")
+        if got_lse is not None:
+            assert np.abs(got_lse[sel] - wl).max() <= TOL_LSE, f"request {b}: lse"
+
+
+def run_and_check(spec, groups=False):
+    w = W.generate(spec)
+    eng, plan, dev, out, lse, _ = run_step(w, groups=groups)
+    assert eng.device_status() == 0
+    check_tables(w, eng, plan, dev)
+    check_attention(w, out, lse)
+    eng.tree.check()
+    return w, eng
+
+
+# ---------------------------------------------------------------- extend
+def test_extend_c1_fp32():
+    run_and_check(W.config("c1"))
+
+
+def test_extend_c2_bf16_mha_d64():
+    run_and_check(W.config("c2"))
+
+
+def test_extend_gqa4_d128_ragged():
+    # root 300 -> child 77; requests: full path + 130 new, half the root + 200 new (split),
+    # no prefix + 37 new, full path + 1 new, root + 0 new tokens
+    spec = W.Spec("gqa4-ragged", "bf16", 32, 8, 128, 1 << 14, W.QWEN_VOCAB, 11,
+                  seg_parent=[-1, 0], seg_len=[300, 77], histories=[1],
+                  req_seg=[1, 0, 0, 1, 0], req_cached=[377, 150, 0, 377, 300], req_new=[130, 200, 37, 1, 0])
+    run_and_check(spec)
+
+
+def test_extend_gqa8_d128_many_tiles():
+    spec = W.spec_multiturn("gqa8", "bf16", 64, 8, 128, 1 << 14, W.QWEN_VOCAB, 12, branches=2, branch_len=1200,
+                            hit_len=1000, n_new=100)
+    run_and_check(spec)
+
+
+def test_extend_gqa4_d64():
+    spec = W.spec_branching("gqa4-d64", "bf16", 16, 4, 64, 1 << 13, W.QWEN_VOCAB, 13, root=190, n_children=3,
+                            child_len=45, leaves_per_child=2, n_new=70)
+    run_and_check(spec)
+
+
+def test_extend_without_cache_is_plain_causal_prefill():
+    spec = W.Spec("nocache", "bf16", 8, 8, 128, 4096, W.QWEN_VOCAB, 14, seg_parent=[-1], seg_len=[5],
+                  histories=[0], req_seg=[0, 0], req_cached=[0, 0], req_new=[333, 64])
+    run_and_check(spec)
+
+
+def test_extend_fp32_gqa():
+    spec = W.spec_branching("f32-gqa", "f32", 8, 2, 128, 2048, W.QWEN_VOCAB, 15, root=100, n_children=2,
+                            child_len=20, leaves_per_child=2, n_new=9)
+    run_and_check(spec)
+
+
+# ---------------------------------------------------------------- decode
+def small_decode(dtype="bf16", hq=32, hkv=8, d=128, seed=21):
+    return W.spec_decode("dec-small", dtype, hq, hkv, d, 1 << 16, W.QWEN_VOCAB, seed, batch=24, share_frac=0.6,
+                         shared_len=700, min_len=1, max_len=3000)
+
+
+def test_decode_split_kv():
+    run_and_check(small_decode())
+
+
+def test_decode_shared_prefix_groups():
+    w, eng = run_and_check(small_decode(), groups=True)
+
+
+def test_decode_groups_equal_no_groups():
+    spec = small_decode(seed=22)
+    w = W.generate(spec)
+    _, _, _, o1, l1, _ = run_step(w, groups=False)
+    _, _, _, o2, l2, grp = run_step(w, groups=True)
+    assert grp is not None and grp.num_groups >= 1
+    a, b = to_host_f32(o1), to_host_f32(o2)
+    assert np.abs(a - b).max() <= 1e-2
+    assert np.abs(l1.cpu().numpy() - l2.cpu().numpy()).max() <= 1e-3
+
+
+def test_decode_mha_d64():
+    run_and_check(small_decode(hq=12, hkv=12, d=64, seed=23))
+
+
+def test_decode_fp32():
+    run_and_check(W.spec_decode("dec-f32", "f32", 8, 2, 64, 8192, W.QWEN_VOCAB, 24, batch=6, share_frac=0.5,
+                                shared_len=50, min_len=1, max_len=300))
+
+
+def test_decode_length_one():
+    spec = W.spec_decode("dec-one", "bf16", 32, 8, 128, 4096, W.QWEN_VOCAB, 25, batch=5, share_frac=0.0,
+                         shared_len=10, min_len=1, max_len=1)
+    run_and_check(spec)
+
+
+# ---------------------------------------------------------------- edge cases and errors
+def test_empty_batch_is_a_no_op():
+    from prefix_cached_kv_radix_gb300 import api
+    from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine
+    eng = PrefixCacheEngine("bf16", 32, 8, 128, 1024, 1)
+    z = torch.zeros(1, 32, 128, dtype=torch.bfloat16, device="cuda")
+    r2t = torch.zeros(1, 8, dtype=torch.int32, device="cuda")
+    i64 = torch.zeros(1, dtype=torch.int64, device="cuda")
+    i32 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.prefix_extend_attention(eng.desc, 0, z, i64, i32, r2t, eng.k_pool, eng.v_pool, z, None, 1, eng.status)
+    api.kv_pool_write(eng.desc, 0, i32, i64, i32, i64, z, z, eng.k_pool, eng.v_pool, r2t, 0, eng.status)
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
+
+
+def _bad_table_case(kind):
+    """A hand-built slot table with one out-of-range slot (or a length past the stride);
+    the kernels' own bounds checks must turn it into a device status, not a fault."""
+    from prefix_cached_kv_radix_gb300 import api
+    from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine
+    eng = PrefixCacheEngine("bf16", 8, 8, 128, 256, 2, poison=False)
+    eng.k_pool.zero_()
+    eng.v_pool.zero_()
+    L = 40
+    r2t = torch.arange(L, dtype=torch.int32, device="cuda").view(1, L)
+    if kind == "slot":
+        r2t[0, 17] = 256 + 5
+    q = torch.randn(4, 8, 128, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(q)
+    qo = torch.tensor([0, 4], dtype=torch.int64, device="cuda")
+    P = torch.tensor([L - 4 if kind == "slot" else L], dtype=torch.int32, device="cuda")
+    return api, eng, r2t, q, out, qo, P
+
+
+def test_bad_slot_sets_status_extend():
+    api, eng, r2t, q, out, qo, P = _bad_table_case("slot")
+    api.prefix_extend_attention(eng.desc, 1, q, qo, P, r2t, eng.k_pool, eng.v_pool, out, None, 4, eng.status)
+    torch.cuda.synchronize()
+    assert eng.device_status() == api.RX_DEV_BAD_SLOT
+
+
+def test_bad_length_sets_status_extend():
+    api, eng, r2t, q, out, qo, P = _bad_table_case("length")
+    api.prefix_extend_attention(eng.desc, 1, q, qo, P, r2t, eng.k_pool, eng.v_pool, out, None, 4, eng.status)
+    torch.cuda.synchronize()
+    assert eng.device_status() == api.RX_DEV_BAD_LENGTH
+
+
+def test_bad_slot_sets_status_decode():
+    api, eng, r2t, q, out, qo, P = _bad_table_case("slot")
+    qd = q[:1].contiguous()
+    od = torch.empty_like(qd)
+    lens = torch.tensor([40], dtype=torch.int32, device="cuda")
+    ws = torch.empty(api.decode_workspace_bytes(eng.desc, 1, 40), dtype=torch.uint8, device="cuda")
+    api.decode_attention(eng.desc, 1, qd, r2t, lens, eng.k_pool, eng.v_pool, od, None, 40, ws, eng.status)
+    torch.cuda.synchronize()
+    assert eng.device_status() == api.RX_DEV_BAD_SLOT
+
+
+def test_workspace_too_small_is_rejected_on_host():
+    from prefix_cached_kv_radix_gb300 import api
+    api_, eng, r2t, q, out, qo, P = _bad_table_case("length")
+    lens = torch.tensor([40], dtype=torch.int32, device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(api.RxError):
+        api.decode_attention(eng.desc, 1, q[:1].contiguous(), r2t, lens, eng.k_pool, eng.v_pool,
+                             torch.empty_like(q[:1]), None, 40, ws, eng.status)
+
+
+def test_step_then_evict_restores_cache():
+    spec = W.config("c2")
+    w = W.generate(spec)
+    eng, plan, dev, out, lse, _ = run_step(w)
+    before = eng.tree.stats()
+    eng.commit(plan)
+    after = eng.tree.stats()
+    assert after["cached_tokens"] == before["cached_tokens"] + w.total_new()
+    freed = eng.release(w.total_new())
+    assert len(freed) == w.total_new() and sorted(freed.tolist()) == sorted(plan.new_slots.tolist())
+    assert eng.tree.stats()["cached_tokens"] == before["cached_tokens"]
+    eng.tree.check()
+    # the same step again sees the same hits (the prefix stayed cached)
+    plan2 = eng.plan([w.request_tokens(b) for b in range(w.batch)], spec.req_new)
+    assert np.array_equal(plan2.prefix_lens, plan.prefix_lens)

@@ -168,7 +168,8 @@ def generate(spec: Spec, threads: int = 16) -> Workload:
         par = spec.seg_parent[s]
         used = first_of_children.setdefault(par, set())
         toks = _draw_first_distinct(tok_rng, spec.vocab, spec.seg_len[s], used)
-        used.add(int(toks[0]))
+        if len(toks):
+            used.add(int(toks[0]))
         w.seg_tokens.append(toks)
     # Request tokens: the first new token differs from the cached continuation at the
     # divergence point and from every sibling request diverging at the same point.
@@ -182,7 +183,10 @@ def generate(spec: Spec, threads: int = 16) -> Workload:
         forb = first_of_children.setdefault(("req", key), set())
         if c < len(path):
             forb.add(int(path[c]))
-        # At the end of a segment on the path: avoid every child segment's first token.
+        # At the end of a segment on the path (or at the very start): avoid every child
+        # segment's first token there.
+        if c == 0:
+            forb |= first_of_children.get(-1, set())
         end = 0
         for seg in (w.seg_path(s) if s >= 0 else []):
             end += spec.seg_len[seg]
@@ -263,8 +267,9 @@ def spec_decode(name, dtype, hq, hkv, d, num_slots, vocab, seed, batch, share_fr
     perm = rng.permutation(batch)
     sharer = np.zeros(batch, bool)
     sharer[perm[:n_share]] = True
-    lens = np.where(sharer, rng.integers(shared_len + 1, max_len + 1, size=batch),
-                    rng.integers(min_len, max_len + 1, size=batch))
+    own = rng.integers(min_len, max_len + 1, size=batch)
+    shr = rng.integers(shared_len + 1, max_len + 1, size=batch) if n_share else own
+    lens = np.where(sharer, shr, own)
     parent, seg_len = [], []
     if n_share:
         parent.append(-1)

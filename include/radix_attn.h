@@ -249,6 +249,31 @@ int decode_attention(const rx_attn_desc* desc, int32_t batch,
                      void* d_workspace, size_t ws_bytes,
                      int32_t* d_status, void* stream);
 
+/* decode_attention without a caller-provided workspace.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory per call -- a
+ * plug-in inside a host application whose allocator already owns the GPU's memory, a
+ * serving loop that must not stall on cudaMalloc/cudaFree (they can synchronise the
+ * device), or a plain C caller with no allocator to provide the workspace.  The split-KV
+ * scratch lives in one static device array of RX_DECODE_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading the library holds until the process exits; nothing is allocated per call.
+ *  - Arguments and results are those of decode_attention (inputs and outputs are still the
+ *    caller's buffers).
+ *  - A batch whose decode_workspace_bytes(...) exceeds RX_DECODE_NOALLOC_SCRATCH_BYTES is
+ *    rejected with RX_EINVAL and a message; split the batch or use decode_attention.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array (it keeps the last call's contents; every call writes
+ *    the scratch before reading it): calls that overlap on the GPU -- on different streams,
+ *    or from different host threads -- race and give wrong results.  Serialise them. */
+#define RX_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
+                             const void* d_q, const int32_t* d_req_to_token, int64_t r2t_stride,
+                             const int32_t* d_kv_lens, const rx_shared_groups* groups,
+                             const void* d_k_pool, const void* d_v_pool,
+                             void* d_out, float* d_lse, int32_t max_kv_len,
+                             int32_t* d_status, void* stream);
+
 /* Thread-local message describing the last failure in this thread ("" if none). */
 const char* rx_last_error(void);
 

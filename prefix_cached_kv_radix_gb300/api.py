@@ -18,12 +18,14 @@ LIB_PATH = os.path.join(_PKG, "_build", "libradixattn.so")
 RX_OK, RX_EINVAL, RX_ENOMEM, RX_ECUDA, RX_ELOCKED, RX_ETIMEOUT, RX_EDEVICE = 0, -1, -2, -3, -4, -5, -6
 RX_DEV_OK, RX_DEV_BAD_SLOT, RX_DEV_BAD_LENGTH, RX_DEV_TIMEOUT = 0, 1, 2, 3
 RX_F32, RX_BF16 = 0, 1
+RX_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20   # include/radix_attn.h
 
 EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "radix_lock", "radix_unlock", "alloc_slots",
            "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups",
            "kv_pool_write", "prefix_extend_attention", "decode_workspace_bytes", "decode_attention",
+           "decode_attention_noalloc",
            "rx_last_error", "rx_version")
 
 
@@ -85,6 +87,7 @@ def load(path: str = LIB_PATH):
         "prefix_extend_attention": (ctypes.c_int, [P, I32, P, P, P, P, I64, P, P, P, P, I32, P, P]),
         "decode_workspace_bytes": (SZ, [P, I32, I32, P]),
         "decode_attention": (ctypes.c_int, [P, I32, P, P, I64, P, P, P, P, P, P, I32, P, SZ, P, P]),
+        "decode_attention_noalloc": (ctypes.c_int, [P, I32, P, P, I64, P, P, P, P, P, P, I32, P, P]),
         "rx_last_error": (ctypes.c_char_p, []),
         "rx_version": (ctypes.c_char_p, []),
     }
@@ -341,3 +344,13 @@ def decode_attention(desc, batch, q, req_to_token, kv_lens, k_pool, v_pool, out,
         ctypes.byref(desc), batch, _ptr(q), _ptr(req_to_token), req_to_token.shape[1], _ptr(kv_lens),
         ctypes.byref(groups) if groups is not None else None, _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(lse),
         max_kv_len, _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
+
+
+def decode_attention_noalloc(desc, batch, q, req_to_token, kv_lens, k_pool, v_pool, out, lse, max_kv_len, status,
+                             groups=None, stream=None) -> None:
+    """decode_attention with the library's static scratch instead of a workspace: for callers
+    that cannot allocate device memory per call.  Overlapping calls race (one shared array)."""
+    _check("decode_attention_noalloc", load().decode_attention_noalloc(
+        ctypes.byref(desc), batch, _ptr(q), _ptr(req_to_token), req_to_token.shape[1], _ptr(kv_lens),
+        ctypes.byref(groups) if groups is not None else None, _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(lse),
+        max_kv_len, _ptr(status), _stream(stream)))

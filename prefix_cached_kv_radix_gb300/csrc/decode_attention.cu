@@ -21,6 +21,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "radix_attn.h"
 #include "rx_common.h"
 #include "rx_device.cuh"
@@ -516,4 +518,68 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
         return RX_ECUDA;
     }
     return RX_OK;
+}
+
+// ----------------------------------------------------------------------------------------
+// decode_attention_noalloc: decode_attention with its scratch in a fixed device array.
+//
+// Some callers cannot allocate device memory per call: a plug-in running inside a host
+// application whose allocator has already reserved the GPU's memory (a raw cudaMalloc would
+// fail or bypass the host's accounting), a serving loop that must not stall on
+// cudaMalloc/cudaFree (both may synchronise the device), or a plain C caller with no
+// allocator of its own to provide the split-KV workspace.  For them this entry point keeps
+// the workspace in one file-scope device array of RX_DECODE_NOALLOC_SCRATCH_BYTES, which
+// every GPU that loads the library holds until the process exits.  Host code cannot use
+// the array's name as a device address, so the address is looked up once per device with
+// cudaGetSymbolAddress (on that device's first call, with the device current) and cached.
+namespace rx {
+
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[RX_DECODE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+
+}  // namespace rx
+
+extern "C" int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch, const void* d_q,
+                                        const int32_t* d_req_to_token, int64_t r2t_stride,
+                                        const int32_t* d_kv_lens, const rx_shared_groups* groups,
+                                        const void* d_k_pool, const void* d_v_pool, void* d_out, float* d_lse,
+                                        int32_t max_kv_len, int32_t* d_status, void* stream) {
+    RX_REQUIRE(desc && batch >= 0 && max_kv_len >= 1, "decode_attention_noalloc: bad arguments");
+    if (batch == 0) return RX_OK;
+    const size_t need = decode_workspace_bytes(desc, batch, max_kv_len, groups);
+    RX_REQUIRE(need <= (size_t)RX_DECODE_NOALLOC_SCRATCH_BYTES,
+               "decode_attention_noalloc: this batch needs %zu bytes of scratch, the static scratch holds %zu "
+               "(use decode_attention with a caller-provided workspace, or split the batch)",
+               need, (size_t)RX_DECODE_NOALLOC_SCRATCH_BYTES);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_error("decode_attention_noalloc: cudaGetDevice failed: %s", cudaGetErrorString(e));
+        return RX_ECUDA;
+    }
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) {
+        set_error("decode_attention_noalloc: device %d beyond the %d supported", dev, NOALLOC_MAX_DEVICES);
+        return RX_EDEVICE;
+    }
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            e = cudaGetSymbolAddress(&scratch, g_decode_noalloc_scratch);
+            if (e != cudaSuccess) {
+                set_error("decode_attention_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+                return RX_ECUDA;
+            }
+            g_noalloc_ptr[dev] = scratch;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    // The split-KV partials and the group map are fully written before they are read in
+    // every call, so the scratch needs no clearing between calls.
+    return decode_attention(desc, batch, d_q, d_req_to_token, r2t_stride, d_kv_lens, groups, d_k_pool, d_v_pool,
+                            d_out, d_lse, max_kv_len, scratch, (size_t)RX_DECODE_NOALLOC_SCRATCH_BYTES, d_status,
+                            stream);
 }

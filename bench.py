@@ -174,6 +174,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     spec = W.config(args.workload)
+    if args.pool_slots:
+        spec.num_slots = args.pool_slots
     w = W.generate(spec)
     s = spec
     eng = PrefixCacheEngine(s.dtype, s.hq, s.hkv, s.d, s.num_slots, s.seed, device=str(dev), poison=False)
@@ -386,6 +388,8 @@ def main():
     ap.add_argument("--workload", default="c2", choices=list(W.CONFIG_NAMES))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-slots", type=int, default=0,
+                    help="override the KV pool size (profiling captures keep the device footprint small)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))

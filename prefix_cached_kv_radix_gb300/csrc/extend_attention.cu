@@ -13,18 +13,25 @@
 // of a kv head (GQA group) are packed with the tokens, head fastest: packed row R ->
 // token R / G, head g*G + R % G, so every K/V tile feeds G heads and the tile stays a
 // dense contraction.  Two 128-row Q tiles share each K/V tile (halves L2->SM traffic per
-// FLOP).  Warp roles (320 threads):
-//   warp 0     loader: 16-byte cp.async gathers of Q once and of K/V tiles (64 keys)
-//              through the slot table into a 3-stage ring, 128B-swizzled (the canonical
-//              K-major layout tcgen05 reads); completion is signalled on mbarriers.
-//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer:
-//              S_t = Q_t K^T (M=128, N=64, K=D) and O_t += P_t V (M=128, N=D, K=64, V read
-//              as an MN-major operand), completion via tcgen05.commit.
-//   warps 2-5  softmax of Q tile 0; warps 6-9 softmax of Q tile 1: tcgen05.ld of a score
+// FLOP).  Roles (384 threads, three warpgroups):
+//   warps 0-2  loaders: 16-byte cp.async gathers of Q once and of K/V tiles (64 keys)
+//              through the slot table into a 4-stage ring in the 128B-swizzled K-major
+//              layout tcgen05 reads.  A single warp cannot issue gathers fast enough to feed
+//              the tensor core, so three warps split every tile.  Each loader thread keeps
+//              two tiles of copies in flight, waits for its own oldest group, fences the
+//              generic->async proxy and arrives on the tile's barrier; slot ids are
+//              prefetched one tile ahead.
+//   warp 3     TMEM allocator and single-thread tcgen05.mma issuer:
+//              S_t = Q_t K^T (M=128, N=64, K=D, both operands from smem) and
+//              O_t += P_t V (M=128, N=D, K=64, P from TMEM, V an MN-major smem operand),
+//              completion via tcgen05.commit.
+//   warps 4-7  softmax of Q tile 0; warps 8-11 softmax of Q tile 1: tcgen05.ld of a score
 //              row per thread, causal mask, online softmax in the exp2 domain with a lazy
 //              rescale (the reference max only moves when the row max grows by more than
-//              2^8, which keeps every P <= 256), P written as bf16 to swizzled smem, O
-//              rescaled in TMEM only when the reference moved, final O / l to global.
+//              2^8, which keeps every P <= 256), P packed to bf16 and stored back to TMEM
+//              (tcgen05.st), O rescaled in TMEM only when the reference moved, O / l to
+//              global at the end.
+// TMEM columns: S0 [0,64) S1 [64,128) P0 [128,160) P1 [160,192) O0 [256,256+D) O1 after.
 // The two Q tiles ping-pong: while one tile's softmax runs, the tensor core works on the
 // other's GEMMs.  Every wait is bounded; on time-out the kernel records RX_DEV_TIMEOUT,
 // drains its async copies, frees TMEM and returns.
@@ -39,8 +46,11 @@
 namespace rx {
 
 constexpr int EXT_BN = 64;        // keys per K/V tile
-constexpr int EXT_NS = 3;         // K/V ring depth
-constexpr int EXT_THREADS = 320;  // 10 warps
+constexpr int EXT_NS = 4;         // K/V ring depth
+constexpr int EXT_LAG = 2;        // cp.async groups a loader thread keeps in flight (<= EXT_NS - 2)
+constexpr int EXT_LOADERS = 96;   // loader threads (warps 0-2)
+constexpr int EXT_MMA_WARP = 3;
+constexpr int EXT_THREADS = 384;  // 12 warps
 constexpr float EXT_LOG2E = 1.4426950408889634f;
 constexpr float EXT_LN2 = 0.6931471805599453f;
 constexpr float EXT_RESCALE_THRESHOLD = 8.0f;   // log2 units
@@ -66,26 +76,27 @@ template <int D>
 struct ExtLayout {
     static constexpr int Q_TILE = 128 * D * 2;
     static constexpr int KV_TILE = EXT_BN * D * 2;
-    static constexpr int P_TILE = 128 * EXT_BN * 2;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + EXT_NS * KV_TILE;
-    static constexpr int OFF_P = OFF_V + EXT_NS * KV_TILE;
-    static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
+    static constexpr int OFF_BAR = OFF_V + EXT_NS * KV_TILE;
     // q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], mma_done
     static constexpr int BAR_Q = 0, BAR_KVF = 1, BAR_KVE = 1 + EXT_NS, BAR_S = 1 + 2 * EXT_NS,
                          BAR_P = BAR_S + 2, BAR_O = BAR_P + 2, BAR_DONE = BAR_O + 2, NBAR = BAR_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;   // room to align the base to 1024 B
-    static constexpr uint32_t TMEM_COLS = (2 * EXT_BN + 2 * D) <= 256 ? 256u : 512u;
-    static constexpr uint32_t COL_S0 = 0, COL_O0 = 2 * EXT_BN;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S0 = 0, COL_P0 = 2 * EXT_BN, COL_O0 = 256;
+    static constexpr int CPR = D / 8;                                   // 16-byte chunks per row
+    static constexpr int NX = (EXT_BN * CPR + EXT_LOADERS - 1) / EXT_LOADERS;   // chunks per loader thread per tile
 };
 
 template <int D>
 __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams p) {
     using LY = ExtLayout<D>;
-    constexpr int CPR = D / 8;   // 16-byte chunks per row
+    constexpr int CPR = LY::CPR;
+    constexpr int NX = LY::NX;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -115,9 +126,9 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
     const int32_t* slots_row = p.r2t + (int64_t)b * p.stride;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(LY::BAR_Q), 32);
+        mbar_init(bar(LY::BAR_Q), EXT_LOADERS);
         for (int i = 0; i < EXT_NS; ++i) {
-            mbar_init(bar(LY::BAR_KVF + i), 32);
+            mbar_init(bar(LY::BAR_KVF + i), EXT_LOADERS);
             mbar_init(bar(LY::BAR_KVE + i), 1);
         }
         for (int t = 0; t < 2; ++t) {
@@ -129,7 +140,7 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == EXT_MMA_WARP) {
         tmem_alloc(base + LY::OFF_MISC, LY::TMEM_COLS);
         tmem_relinquish();
     }
@@ -138,14 +149,13 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ loader
+    if (warp < EXT_LOADERS / 32) {
+        // ------------------------------------------------------------ loaders
+        const int lt = threadIdx.x;
         const uint32_t qs = base + LY::OFF_Q;
-        for (int x = 0; x < 256 * CPR / 32; ++x) {
-            const int qi = lane + 32 * x;
+        for (int qi = lt; qi < ntiles * 128 * CPR; qi += EXT_LOADERS) {
             const int rr = qi / CPR, c = qi % CPR;
             const int t = rr >> 7, r = rr & 127;
-            if (t >= ntiles) break;
             const int R = min(row0 + rr, rows_total - 1);
             const int tok = R / G, h = g * G + R % G;
             const __nv_bfloat16* src = p.q + ((qo0 + tok) * p.hq + h) * D + c * 8;
@@ -153,80 +163,102 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                                                  (((c & 7) ^ (r & 7)) << 4));
             cp_async_16(dst, src, 16);
         }
-        cp_async_arrive_noinc(bar(LY::BAR_Q));
-        for (int j = 0; j < nkv; ++j) {
+        cp_async_commit();                     // group 0: Q (completes with tile 0)
+        int32_t slot_a[NX], slot_b[NX];      // slot ids, one tile ahead (two buffers)
+        auto load_slots = [&](int j, int32_t* dst) {
+#pragma unroll
+            for (int x = 0; x < NX; ++x) {
+                const int q = lt + EXT_LOADERS * x;
+                const int kk = j * EXT_BN + q / CPR;
+                dst[x] = (q < EXT_BN * CPR && kk < kv_end) ? slots_row[kk] : -1;
+            }
+        };
+        auto publish = [&](int jt) {           // copies of tile jt (and Q) are complete
+            fence_proxy_async_smem();
+            if (jt == 0) mbar_arrive(bar(LY::BAR_Q));
+            mbar_arrive(bar(LY::BAR_KVF + jt % EXT_NS));
+        };
+        // Issue tile j from `cur`, then start loading the slots of tile j+1 into `nxt`.
+        auto step = [&](int j, const int32_t* cur, int32_t* nxt) -> bool {
             const int st = j % EXT_NS;
-            if (j >= EXT_NS && !warp_wait(bar(LY::BAR_KVE + st), ((j / EXT_NS) - 1) & 1, abort_flag, p.status)) break;
-            const int k0 = j * EXT_BN;
-            const int kk0 = k0 + lane, kk1 = k0 + lane + 32;
-            const int32_t s0 = kk0 < kv_end ? slots_row[kk0] : 0;
-            const int32_t s1 = kk1 < kv_end ? slots_row[kk1] : 0;
+            if (j >= EXT_NS && !warp_wait(bar(LY::BAR_KVE + st), ((j / EXT_NS) - 1) & 1, abort_flag, p.status))
+                return false;
             const uint32_t kb = base + LY::OFF_K + st * LY::KV_TILE;
             const uint32_t vb = base + LY::OFF_V + st * LY::KV_TILE;
-#pragma unroll 4
-            for (int x = 0; x < EXT_BN * CPR / 32; ++x) {
-                const int qi = lane + 32 * x;
-                const int key = qi / CPR, c = qi % CPR;
-                const int32_t a = __shfl_sync(0xffffffffu, s0, key & 31);
-                const int32_t bb = __shfl_sync(0xffffffffu, s1, key & 31);
-                int32_t slot = key < 32 ? a : bb;
-                uint32_t bytes = 16;
-                if (k0 + key >= kv_end) {
-                    bytes = 0;
-                    slot = 0;
-                } else if (slot < 0 || slot >= p.num_slots) {
-                    report(p.status, RX_DEV_BAD_SLOT);
-                    bytes = 0;
-                    slot = 0;
+#pragma unroll
+            for (int x = 0; x < NX; ++x) {
+                const int q = lt + EXT_LOADERS * x;
+                if (q < EXT_BN * CPR) {
+                    const int key = q / CPR, c = q % CPR;
+                    int32_t slot = cur[x];
+                    uint32_t bytes = 16;
+                    if (slot < 0 || slot >= p.num_slots) {
+                        if (slot != -1 || j * EXT_BN + key < kv_end) report(p.status, RX_DEV_BAD_SLOT);
+                        slot = 0;
+                        bytes = 0;             // zero fill: beyond the context or a bad slot
+                    }
+                    const int64_t off = ((int64_t)slot * p.hkv + g) * D + c * 8;
+                    const uint32_t so =
+                        (uint32_t)((c >> 3) * EXT_BN * 128 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
+                    cp_async_16(kb + so, p.k_pool + off, bytes);
+                    cp_async_16(vb + so, p.v_pool + off, bytes);
                 }
-                const int64_t off = ((int64_t)slot * p.hkv + g) * D + c * 8;
-                const uint32_t so = (uint32_t)((c >> 3) * EXT_BN * 128 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
-                cp_async_16(kb + so, p.k_pool + off, bytes);
-                cp_async_16(vb + so, p.v_pool + off, bytes);
             }
-            cp_async_arrive_noinc(bar(LY::BAR_KVF + st));
+            cp_async_commit();
+            if (j + 1 < nkv) load_slots(j + 1, nxt);
+            if (j >= EXT_LAG) {
+                cp_async_wait<EXT_LAG>();
+                publish(j - EXT_LAG);
+            }
+            return true;
+        };
+        load_slots(0, slot_a);
+        bool ok = true;
+        for (int j = 0; ok && j < nkv; j += 2) {
+            ok = step(j, slot_a, slot_b);
+            if (ok && j + 1 < nkv) ok = step(j + 1, slot_b, slot_a);
         }
         cp_async_wait<0>();
-    } else if (warp == 1) {
+        if (ok)
+            for (int jt = max(0, nkv - EXT_LAG); jt < nkv; ++jt) publish(jt);
+    } else if (warp == EXT_MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, EXT_BN, 0, 0);
             constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);
-            const uint32_t qs = base + LY::OFF_Q;
+            const uint64_t qd0 = sdesc_sw128(base + LY::OFF_Q, 16, 1024);
+            const uint64_t kd0 = sdesc_sw128(base + LY::OFF_K, 16, 1024);
+            const uint64_t vd0 = sdesc_sw128(base + LY::OFF_V, EXT_BN * 128, 1024);
+            // descriptor start addresses advance in 16-byte units in the low bits
+            auto qdesc = [&](int t, int s) {
+                return qd0 + (uint64_t)((t * LY::Q_TILE + (s >> 2) * 128 * 128 + (s & 3) * 32) >> 4);
+            };
+            auto kdesc = [&](int st, int s) {
+                return kd0 + (uint64_t)((st * LY::KV_TILE + (s >> 2) * EXT_BN * 128 + (s & 3) * 32) >> 4);
+            };
+            auto vdesc = [&](int st, int s) { return vd0 + (uint64_t)((st * LY::KV_TILE + s * 16 * 128) >> 4); };
             bool ok = mbar_wait(bar(LY::BAR_Q), 0, abort_flag, p.status);
-            fence_proxy_async_smem();
             tc_fence_after();
             auto issue_pv = [&](int t, int jj) {
-                const uint32_t vb = base + LY::OFF_V + (jj % EXT_NS) * LY::KV_TILE;
-                const uint32_t pb = base + LY::OFF_P + t * LY::P_TILE;
+                const int pst = jj % EXT_NS;
 #pragma unroll
-                for (int s = 0; s < EXT_BN / 16; ++s) {
-                    const uint64_t ad = sdesc_sw128(pb + s * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(vb + s * 16 * 128, EXT_BN * 128, 1024);
-                    umma_f16_ss(tmem + LY::COL_O0 + t * D, ad, bd, IDESC_PV, (jj > 0 || s > 0) ? 1u : 0u);
-                }
+                for (int s = 0; s < EXT_BN / 16; ++s)
+                    umma_f16_ts(tmem + LY::COL_O0 + t * D, tmem + LY::COL_P0 + t * (EXT_BN / 2) + s * 8,
+                                vdesc(pst, s), IDESC_PV, (jj > 0 || s > 0) ? 1u : 0u);
                 umma_commit(bar(LY::BAR_O + t));
             };
             for (int j = 0; ok && j < nkv; ++j) {
                 const int st = j % EXT_NS;
                 if (!mbar_wait(bar(LY::BAR_KVF + st), (j / EXT_NS) & 1, abort_flag, p.status)) { ok = false; break; }
-                fence_proxy_async_smem();
                 tc_fence_after();
-                const uint32_t kb = base + LY::OFF_K + st * LY::KV_TILE;
                 for (int t = 0; t < ntiles; ++t) {
                     if (j > 0) {
                         if (!mbar_wait(bar(LY::BAR_P + t), (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-                        fence_proxy_async_smem();
                         tc_fence_after();
                     }
 #pragma unroll
-                    for (int s = 0; s < D / 16; ++s) {
-                        const uint32_t koff = (uint32_t)((s >> 2) * 128 * 128 + (s & 3) * 32);
-                        const uint32_t kboff = (uint32_t)((s >> 2) * EXT_BN * 128 + (s & 3) * 32);
-                        const uint64_t ad = sdesc_sw128(qs + t * LY::Q_TILE + koff, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(kb + kboff, 16, 1024);
-                        umma_f16_ss(tmem + LY::COL_S0 + t * EXT_BN, ad, bd, IDESC_S, s > 0 ? 1u : 0u);
-                    }
+                    for (int s = 0; s < D / 16; ++s)
+                        umma_f16_ss(tmem + LY::COL_S0 + t * EXT_BN, qdesc(t, s), kdesc(st, s), IDESC_S, s > 0 ? 1u : 0u);
                     umma_commit(bar(LY::BAR_S + t));
                     if (j > 0) issue_pv(t, j - 1);
                 }
@@ -235,7 +267,6 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             }
             for (int t = 0; ok && t < ntiles; ++t) {
                 if (!mbar_wait(bar(LY::BAR_P + t), (nkv - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-                fence_proxy_async_smem();
                 tc_fence_after();
                 issue_pv(t, nkv - 1);
             }
@@ -244,7 +275,7 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warpgroups
-        const int t = (warp - 2) >> 2;
+        const int t = (warp - 4) >> 2;
         if (t < ntiles) {
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
@@ -255,8 +286,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             const int pos = P_b + tok;   // attends keys 0..pos
             const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
             const uint32_t s_addr = tmem + lane_base + LY::COL_S0 + t * EXT_BN;
+            const uint32_t p_addr = tmem + lane_base + LY::COL_P0 + t * (EXT_BN / 2);
             const uint32_t o_addr = tmem + lane_base + LY::COL_O0 + t * D;
-            const uint32_t prow = base + LY::OFF_P + t * LY::P_TILE + r * 128;
             float m_ref = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j < nkv; ++j) {
@@ -272,19 +303,29 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                     for (int c = 0; c < EXT_BN; ++c)
                         if (k0 + c > pos) s[c] = -INFINITY;
                 }
-                float mx = -INFINITY;
+                float mx8[8];
 #pragma unroll
-                for (int c = 0; c < EXT_BN; ++c) mx = fmaxf(mx, s[c]);
+                for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+                for (int c = 8; c < EXT_BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 mx *= p.scale_log2;
                 float m_new = m_ref;
                 if (m_ref == -INFINITY || mx > m_ref + EXT_RESCALE_THRESHOLD) m_new = fmaxf(m_ref, mx);
                 const float alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
-                float rs = 0.f;
+                float rs8[8];
 #pragma unroll
-                for (int c = 0; c < EXT_BN; ++c) {
-                    s[c] = exp2f(s[c] * p.scale_log2 - m_new);
-                    rs += s[c];
+                for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+                uint32_t pk[EXT_BN / 2];
+#pragma unroll
+                for (int c = 0; c < EXT_BN; c += 2) {
+                    const float e0 = exp2f(fmaf(s[c], p.scale_log2, -m_new));
+                    const float e1 = exp2f(fmaf(s[c + 1], p.scale_log2, -m_new));
+                    rs8[(c >> 1) & 7] += e0 + e1;
+                    pk[c >> 1] = pack_bf16x2(e0, e1);
                 }
+                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
                 l = l * alpha + rs;
                 if (j > 0) {
                     if (!warp_wait(bar(LY::BAR_O + t), (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
@@ -299,19 +340,11 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                             for (int e = 0; e < 32; ++e) ov[e] *= alpha;
                             tmem_st32(o_addr + cc, ov);
                         }
-                        tmem_wait_st();
                     }
                 }
                 m_ref = m_new;
-#pragma unroll
-                for (int ch = 0; ch < EXT_BN / 8; ++ch) {
-                    const uint32_t w0 = pack_bf16x2(s[8 * ch + 0], s[8 * ch + 1]);
-                    const uint32_t w1 = pack_bf16x2(s[8 * ch + 2], s[8 * ch + 3]);
-                    const uint32_t w2 = pack_bf16x2(s[8 * ch + 4], s[8 * ch + 5]);
-                    const uint32_t w3 = pack_bf16x2(s[8 * ch + 6], s[8 * ch + 7]);
-                    st_shared_v4(prow + (uint32_t)(((ch ^ (r & 7)) & 7) << 4), w0, w1, w2, w3);
-                }
-                fence_proxy_async_smem();
+                tmem_st32u(p_addr, pk);
+                tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(LY::BAR_P + t));
             }
@@ -343,7 +376,7 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == EXT_MMA_WARP) {
         tc_fence_after();
         // Every MMA this CTA issued has completed before TMEM is released; this wait does
         // not stop on the abort flag (only on its own time bound).

@@ -153,6 +153,17 @@ int match_prefix_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const 
 int insert_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
                  const int32_t* slots, int64_t* out_dup_len, rx_node* out_last);
 
+/* Insert continued from where each request's match ended: request b's full prompt is
+ * tokens[tok_indptr[b] : tok_indptr[b+1]], its cached path ends at node nodes[b] (the
+ * out_last of its match, still cached -- e.g. locked) at depth d_b, and new_slots[
+ * new_indptr[b] : new_indptr[b+1]] holds one slot for each of its n_b - d_b later tokens.
+ * Same result, stamps and dup lengths (counted from position 0) as insert of the full
+ * prompt with the matched slots followed by the new ones, without re-walking the cached
+ * prefix.  The caller owns new slots [0, dup_len - d_b) of a request (cached meanwhile). */
+int insert_batch_at(rx_radix* t, int32_t batch, const rx_node* nodes, const int32_t* tokens,
+                    const int64_t* tok_indptr, const int32_t* new_slots, const int64_t* new_indptr,
+                    int64_t* out_dup_len, rx_node* out_last);
+
 int radix_stats(const rx_radix* t, rx_stats* out);
 
 /* Check the tree's invariants (edges, parents, slot ownership, stamps, locks);

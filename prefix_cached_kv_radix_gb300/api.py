@@ -21,7 +21,7 @@ RX_F32, RX_BF16 = 0, 1
 RX_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20   # include/radix_attn.h
 
 EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "radix_lock", "radix_unlock", "alloc_slots",
-           "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "radix_lock_batch",
+           "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "insert_batch_at", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups",
            "kv_pool_write", "prefix_extend_attention", "decode_workspace_bytes", "decode_attention",
@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH):
         "evict": (ctypes.c_int, [P, I64, P, I64, P]),
         "match_prefix_batch": (ctypes.c_int, [P, I32, P, P, P, P, P]),
         "insert_batch": (ctypes.c_int, [P, I32, P, P, P, P, P]),
+        "insert_batch_at": (ctypes.c_int, [P, I32, P, P, P, P, P, P, P]),
         "radix_lock_batch": (ctypes.c_int, [P, P, I32]),
         "radix_unlock_batch": (ctypes.c_int, [P, P, I32]),
         "radix_stats": (ctypes.c_int, [P, P]),
@@ -160,6 +161,21 @@ def radix_lock(tree, node: int) -> None:
 
 def radix_unlock(tree, node: int) -> None:
     _check("radix_unlock", load().radix_unlock(tree, node))
+
+
+def insert_batch_at(tree, nodes, tokens, tok_indptr, new_slots, new_indptr):
+    """Insert continued from each request's matched node.  Returns (dup lengths, last nodes)."""
+    nd = np.ascontiguousarray(np.asarray(nodes, np.int64))
+    tok, sl = _np_i32(tokens), _np_i32(new_slots)
+    ind = np.ascontiguousarray(np.asarray(tok_indptr, np.int64))
+    nind = np.ascontiguousarray(np.asarray(new_indptr, np.int64))
+    b = len(nd)
+    dup = np.empty(max(b, 1), np.int64)
+    last = np.empty(max(b, 1), np.int64)
+    _check("insert_batch_at", load().insert_batch_at(tree, b, nd.ctypes.data, tok.ctypes.data, ind.ctypes.data,
+                                                     sl.ctypes.data if len(sl) else None, nind.ctypes.data,
+                                                     dup.ctypes.data, last.ctypes.data))
+    return dup[:b].copy(), last[:b].copy()
 
 
 def radix_lock_batch(tree, nodes) -> None:
@@ -290,6 +306,9 @@ class RadixTree:
 
     def insert_batch(self, tokens, tok_indptr, slots):
         return insert_batch(self.h, tokens, tok_indptr, slots)
+
+    def insert_batch_at(self, nodes, tokens, tok_indptr, new_slots, new_indptr):
+        return insert_batch_at(self.h, nodes, tokens, tok_indptr, new_slots, new_indptr)
 
     def lock_batch(self, nodes):
         return radix_lock_batch(self.h, nodes)

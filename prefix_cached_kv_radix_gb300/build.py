@@ -78,7 +78,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         obj = os.path.join(OUT_DIR, f + ".o")
         objs.append(obj)
         if force or _stale(obj, src):
-            jobs.append(["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-I", CSRC,
+            jobs.append(["g++", "-O3", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-I", CSRC,
                          "-c", src, "-o", obj])
     if jobs:
         with ThreadPoolExecutor(max_workers=len(jobs)) as ex:

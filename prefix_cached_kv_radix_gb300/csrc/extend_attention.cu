@@ -15,7 +15,7 @@
 // dense contraction.  Two 128-row Q tiles share each K/V tile (halves L2->SM traffic per
 // FLOP).  Roles (384 threads, three warpgroups):
 //   warps 0-2  loaders: 16-byte cp.async gathers of Q once and of K/V tiles (64 keys)
-//              through the slot table into a 4-stage ring in the 128B-swizzled K-major
+//              through the slot table into a 5-stage ring in the 128B-swizzled K-major
 //              layout tcgen05 reads.  A single warp cannot issue gathers fast enough to feed
 //              the tensor core, so three warps split every tile.  Each loader thread keeps
 //              two tiles of copies in flight, waits for its own oldest group, fences the
@@ -46,7 +46,7 @@
 namespace rx {
 
 constexpr int EXT_BN = 64;        // keys per K/V tile
-constexpr int EXT_NS = 4;         // K/V ring depth
+constexpr int EXT_NS = 5;         // K/V ring depth (a loader runs EXT_NS-1-EXT_LAG tiles ahead)
 constexpr int EXT_LAG = 2;        // cp.async groups a loader thread keeps in flight (<= EXT_NS - 2)
 constexpr int EXT_LOADERS = 96;   // loader threads (warps 0-2)
 constexpr int EXT_MMA_WARP = 3;
@@ -320,8 +320,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                 uint32_t pk[EXT_BN / 2];
 #pragma unroll
                 for (int c = 0; c < EXT_BN; c += 2) {
-                    const float e0 = exp2f(fmaf(s[c], p.scale_log2, -m_new));
-                    const float e1 = exp2f(fmaf(s[c + 1], p.scale_log2, -m_new));
+                    const float e0 = fast_exp2(fmaf(s[c], p.scale_log2, -m_new));
+                    const float e1 = fast_exp2(fmaf(s[c + 1], p.scale_log2, -m_new));
                     rs8[(c >> 1) & 7] += e0 + e1;
                     pk[c >> 1] = pack_bf16x2(e0, e1);
                 }

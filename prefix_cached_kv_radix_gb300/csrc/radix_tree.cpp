@@ -63,6 +63,20 @@ static uint64_t splitmix64_at(uint64_t seed, uint64_t counter) {
     return z ^ (z >> 31);
 }
 
+// Length of the common prefix of a[0:n] and b[0:n], starting the search at `from`.  Blocks
+// of 16 are OR-reduced first so the compiler can vectorise the common case of equal runs.
+static inline int64_t common_prefix(const int32_t* a, const int32_t* b, int64_t from, int64_t n) {
+    int64_t k = from;
+    while (k + 16 <= n) {
+        uint32_t acc = 0;
+        for (int i = 0; i < 16; ++i) acc |= (uint32_t)(a[k + i] ^ b[k + i]);
+        if (acc) break;
+        k += 16;
+    }
+    while (k < n && a[k] == b[k]) ++k;
+    return k;
+}
+
 }  // namespace rx
 
 struct rx_radix {
@@ -126,16 +140,19 @@ struct rx_radix {
     // Walk the cached path of tokens[0:n]: split where it ends inside an edge, stamp every
     // node on it, optionally collect slots.  Returns the matched length; *last = end node.
     int64_t walk(const int32_t* tokens, int64_t n, int32_t* out_slots, rx::Node** last) {
-        rx::Node* x = &root;
-        int64_t pos = 0;
+        return walk_from(&root, 0, tokens, n, out_slots, last);
+    }
+
+    // The walk continued from node x, which ends at token position pos of the sequence.
+    int64_t walk_from(rx::Node* x, int64_t pos, const int32_t* tokens, int64_t n, int32_t* out_slots,
+                      rx::Node** last) {
         while (pos < n) {
             auto it = x->children.find(tokens[pos]);
             if (it == x->children.end()) break;
             rx::Node* c = it->second;
             const size_t len = c->key.size();
             const int64_t lim = std::min<int64_t>((int64_t)len, n - pos);
-            int64_t k = 1;
-            while (k < lim && c->key[k] == tokens[pos + k]) ++k;
+            const int64_t k = rx::common_prefix(c->key.data(), tokens + pos, 1, lim);
             if ((size_t)k < len) c = split(c, (size_t)k);
             c->stamp = clock;
             if (out_slots) std::memcpy(out_slots + pos, c->slots.data(), sizeof(int32_t) * (size_t)k);
@@ -382,6 +399,48 @@ int insert_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
         RX_REQUIRE(n >= 0 && tok_indptr[b] >= 0, "insert_batch: bad tok_indptr at %d", b);
         const int rc = insert(t, tokens + tok_indptr[b], slots + tok_indptr[b], n, out_dup_len + b, out_last + b);
         if (rc != RX_OK) return rc;
+    }
+    return RX_OK;
+}
+
+int insert_batch_at(rx_radix* t, int32_t batch, const rx_node* nodes, const int32_t* tokens,
+                    const int64_t* tok_indptr, const int32_t* new_slots, const int64_t* new_indptr,
+                    int64_t* out_dup_len, rx_node* out_last) {
+    RX_REQUIRE(t && batch >= 0 && (batch == 0 || (nodes && tokens && tok_indptr && new_indptr && out_dup_len && out_last)),
+               "insert_batch_at: bad arguments");
+    for (int32_t b = 0; b < batch; ++b) {
+        auto it = t->by_id.find(nodes[b]);
+        RX_REQUIRE(it != t->by_id.end(), "insert_batch_at: unknown node %lld", (long long)nodes[b]);
+        rx::Node* x = it->second;
+        const int64_t n = tok_indptr[b + 1] - tok_indptr[b];
+        const int64_t d = x->depth;
+        const int64_t m = new_indptr[b + 1] - new_indptr[b];
+        RX_REQUIRE(d >= 0 && d <= n && m == n - d, "insert_batch_at: request %d: node depth %lld, %lld tokens, %lld new slots",
+                   b, (long long)d, (long long)n, (long long)m);
+        const int32_t* tok = tokens + tok_indptr[b];
+        const int32_t* sl = new_slots + new_indptr[b];
+        for (int64_t i = 0; i < m; ++i)
+            RX_REQUIRE(sl[i] >= 0 && sl[i] < t->num_slots && !t->is_free[(size_t)sl[i]],
+                       "insert_batch_at: slot %d of request %d is out of range or free", sl[i], b);
+        t->clock += 1;
+        for (rx::Node* y = x; y != &t->root; y = y->parent) y->stamp = t->clock;   // the cached path
+        rx::Node* end = nullptr;
+        const int64_t dup = t->walk_from(x, d, tok, n, nullptr, &end);
+        if (dup < n) {
+            rx::Node* leaf = t->new_node();
+            leaf->parent = end;
+            leaf->key.assign(tok + dup, tok + n);
+            leaf->slots.assign(sl + (dup - d), sl + m);
+            leaf->stamp = t->clock;
+            leaf->depth = end->depth + (n - dup);
+            end->children[tok[dup]] = leaf;
+            end = leaf;
+            t->st.cached_tokens += n - dup;
+            t->st.inserted_tokens += n - dup;
+        }
+        t->st.insert_calls += 1;
+        out_dup_len[b] = dup;
+        out_last[b] = end->id;
     }
     return RX_OK;
 }

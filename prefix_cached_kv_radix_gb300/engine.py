@@ -64,6 +64,12 @@ class PrefixCacheEngine:
         self.desc = api.make_desc(api.RX_F32 if dtype == "f32" else api.RX_BF16, hq, hkv, head_dim, num_slots,
                                   1.0 / float(np.sqrt(head_dim)))
         self._ws = None
+        # step index arrays travel in one pinned buffer (two, alternating) and one H2D copy
+        self._pin = [None, None]
+        self._pin_ev = [None, None]
+        self._pin_i = 0
+        self._dev_idx = None
+        self._r2t = None
 
     # ------------------------------------------------------------------ helpers
     def _i32(self, a):
@@ -99,12 +105,21 @@ class PrefixCacheEngine:
 
     # ------------------------------------------------------------------ step
     def plan(self, prompts, n_new) -> StepPlan:
-        """a1 + a2: match every prompt, check that exactly its last n_new[b] tokens are
-        uncached, allocate their slots."""
+        """a1 + a2 for a list of prompts (see plan_concat)."""
         b = len(prompts)
         lens = np.array([len(p) for p in prompts], np.int64)
         tok_indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
         tokens = np.concatenate(prompts).astype(np.int32) if b else np.zeros(0, np.int32)
+        return self.plan_concat(tokens, tok_indptr, n_new)
+
+    def plan_concat(self, tokens, tok_indptr, n_new) -> StepPlan:
+        """a1 + a2: match every prompt (tokens[tok_indptr[b]:tok_indptr[b+1]]), check that
+        exactly its last n_new[b] tokens are uncached, allocate their slots, pin the matched
+        prefixes for the duration of the step."""
+        tokens = np.ascontiguousarray(tokens, np.int32)
+        tok_indptr = np.ascontiguousarray(tok_indptr, np.int64)
+        b = len(tok_indptr) - 1
+        lens = np.diff(tok_indptr)
         ps, pind, last = self.tree.match_prefix_batch(tokens, tok_indptr)
         P = np.diff(pind).astype(np.int64)
         n_new = np.asarray(n_new, np.int64)
@@ -119,13 +134,46 @@ class PrefixCacheEngine:
         return StepPlan(b, tokens, tok_indptr, ps, pind, P.astype(np.int32), new, qo, last,
                         int(n_new.max()) if b else 0, max_kv, ((max_kv + 7) // 8) * 8)
 
-    def upload(self, plan: StepPlan) -> dict:
-        """Move the step's index arrays to the device."""
-        return dict(prefix_slots=self._i32(plan.prefix_slots if len(plan.prefix_slots) else [0]),
-                    prefix_indptr=self._i64(plan.prefix_indptr), new_slots=self._i32(plan.new_slots if len(plan.new_slots) else [0]),
-                    qo_indptr=self._i64(plan.qo_indptr), prefix_lens=self._i32(plan.prefix_lens),
-                    kv_lens=self._i32(plan.prefix_lens.astype(np.int64) + np.diff(plan.qo_indptr)),
-                    r2t=torch.empty(max(plan.batch, 1), plan.stride, dtype=torch.int32, device=self.device))
+    def upload(self, plan: StepPlan, stream=None) -> dict:
+        """Move the step's index arrays to the device: packed into one pinned host buffer and
+        copied with one asynchronous H2D transfer on the stream (device views returned)."""
+        B = plan.batch
+        parts = [("prefix_slots", plan.prefix_slots if len(plan.prefix_slots) else np.zeros(1, np.int32), np.int32),
+                 ("prefix_indptr", plan.prefix_indptr, np.int64),
+                 ("new_slots", plan.new_slots if len(plan.new_slots) else np.zeros(1, np.int32), np.int32),
+                 ("qo_indptr", plan.qo_indptr, np.int64),
+                 ("prefix_lens", plan.prefix_lens, np.int32),
+                 ("kv_lens", plan.prefix_lens.astype(np.int64) + np.diff(plan.qo_indptr), np.int32)]
+        offs, total = [], 0
+        for _, a, dt in parts:
+            offs.append(total)
+            total += (len(a) * np.dtype(dt).itemsize + 255) // 256 * 256
+        i = self._pin_i
+        self._pin_i ^= 1
+        if self._pin[i] is None or self._pin[i].numel() < total:
+            self._pin[i] = torch.empty(max(total, 4096) * 2, dtype=torch.uint8).pin_memory()
+            self._pin_ev[i] = None
+        if self._dev_idx is None or self._dev_idx.numel() < total:
+            self._dev_idx = torch.empty(max(total, 4096) * 2, dtype=torch.uint8, device=self.device)
+        if self._pin_ev[i] is not None:
+            self._pin_ev[i].synchronize()          # the copy that last read this buffer is done
+        host = self._pin[i].numpy()
+        for (name, a, dt), o in zip(parts, offs):
+            host[o:o + len(a) * np.dtype(dt).itemsize] = np.ascontiguousarray(a, dt).view(np.uint8)
+        st = torch.cuda.current_stream(self.device) if stream is None else stream
+        with torch.cuda.stream(st):
+            self._dev_idx[:total].copy_(self._pin[i][:total], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(st)
+        self._pin_ev[i] = ev
+        out = {}
+        for (name, a, dt), o in zip(parts, offs):
+            nb = len(a) * np.dtype(dt).itemsize
+            out[name] = self._dev_idx[o:o + nb].view(torch.int32 if dt == np.int32 else torch.int64)
+        if self._r2t is None or self._r2t.numel() < max(B, 1) * plan.stride:
+            self._r2t = torch.empty(max(B, 1) * plan.stride * 2, dtype=torch.int32, device=self.device)
+        out["r2t"] = self._r2t[:max(B, 1) * plan.stride].view(max(B, 1), plan.stride)
+        return out
 
     def write(self, plan: StepPlan, dev: dict, k_new, v_new, stream=None) -> None:
         """a3: slot table + scatter of the new tokens' K/V."""
@@ -162,20 +210,13 @@ class PrefixCacheEngine:
                              lse, plan.max_kv_len, ws, self.status, groups=groups, stream=stream)
 
     def commit(self, plan: StepPlan) -> np.ndarray:
-        """a7: insert every prompt with its slots; frees new slots that turned out cached."""
-        slots = np.empty(len(plan.tokens), np.int32)
-        for b in range(plan.batch):
-            t0, t1 = plan.tok_indptr[b], plan.tok_indptr[b + 1]
-            P = plan.prefix_lens[b]
-            slots[t0:t0 + P] = plan.prefix_slots[plan.prefix_indptr[b]:plan.prefix_indptr[b + 1]]
-            slots[t0 + P:t1] = plan.new_slots[plan.qo_indptr[b]:plan.qo_indptr[b + 1]]
-        dup, _ = self.tree.insert_batch(plan.tokens, plan.tok_indptr, slots)
-        extra = []
-        for b in range(plan.batch):
-            d = int(dup[b]) - int(plan.prefix_lens[b])
-            if d > 0:
-                extra.append(plan.new_slots[plan.qo_indptr[b]:plan.qo_indptr[b] + d])
-        if extra:
+        """a7: insert every prompt, continuing from the node its match ended at; frees new
+        slots whose tokens turned out to be cached meanwhile (by an earlier request of the batch)."""
+        dup, _ = self.tree.insert_batch_at(plan.last_nodes, plan.tokens, plan.tok_indptr, plan.new_slots,
+                                           plan.qo_indptr)
+        over = dup - plan.prefix_lens
+        if (over > 0).any():
+            extra = [plan.new_slots[plan.qo_indptr[b]:plan.qo_indptr[b] + over[b]] for b in np.flatnonzero(over > 0)]
             self.tree.free_slots(np.concatenate(extra))
         return dup
 

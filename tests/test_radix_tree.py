@@ -182,3 +182,40 @@ def test_nine_step_walkthrough_on_the_tree():
            ("match", SYS + [10, 11, 12, 12, 15]), ("evict", 4), ("insert", SYS + [10, 11, 12, 12, 15, 16, 16, 16]),
            ("evict", 3), ("insert", SYS + [10, 11, 12, 12, 15, 50, 50, 50])]
     _run_script(ops, 64, 0)
+
+
+def test_insert_batch_at_equals_insert_batch():
+    """Continuing the insert from the matched node gives the same tree as inserting the whole
+    prompt (slots, dup lengths, stamps through eviction order, node counts)."""
+    rng = np.random.default_rng(21)
+    for trial in range(20):
+        t1, t2 = api.RadixTree(4096, trial), api.RadixTree(4096, trial)
+        for rnd in range(6):
+            prompts = [rng.integers(0, 3, size=rng.integers(1, 12)).astype(np.int32) for _ in range(8)]
+            ind = np.concatenate([[0], np.cumsum([len(p) for p in prompts])])
+            flat = np.concatenate(prompts)
+            res = []
+            for t in (t1, t2):
+                ps, pind, last = t.match_prefix_batch(flat, ind)
+                P = np.diff(pind)
+                n_new = np.array([len(p) for p in prompts]) - P
+                new = t.alloc_slots(int(n_new.sum()))
+                res.append((ps, pind, last, P, n_new, new))
+            (ps, pind, last, P, n_new, new) = res[0]
+            assert np.array_equal(new, res[1][5]) and np.array_equal(last, res[1][2])
+            nind = np.concatenate([[0], np.cumsum(n_new)])
+            d1, l1 = t1.insert_batch_at(last, flat, ind, new, nind)
+            full = np.empty(len(flat), np.int32)
+            for b in range(len(prompts)):
+                full[ind[b]:ind[b] + P[b]] = ps[pind[b]:pind[b + 1]]
+                full[ind[b] + P[b]:ind[b + 1]] = new[nind[b]:nind[b + 1]]
+            d2, l2 = t2.insert_batch(flat, ind, full)
+            assert np.array_equal(d1, d2) and np.array_equal(l1, l2)
+            for t, d in ((t1, d1), (t2, d2)):
+                extra = [new[nind[b]:nind[b] + (d[b] - P[b])] for b in range(len(prompts)) if d[b] > P[b]]
+                if extra:
+                    t.free_slots(np.concatenate(extra))
+            assert t1.stats() == t2.stats()
+            t1.check()
+            k = int(rng.integers(1, 20))
+            assert t1.evict(k).tolist() == t2.evict(k).tolist()

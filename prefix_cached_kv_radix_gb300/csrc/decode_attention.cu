@@ -15,9 +15,10 @@
 // writes its chunk's normalised output and log-sum-exp; a second kernel merges the chunks:
 //   M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s.
 // Groups of requests sharing a cached prefix (rx_shared_groups) get their shared run
-// processed once per group: one CTA per (group, kv head, chunk, 16-row block of stacked
-// query rows) reads each shared K/V row once for all members, and the merge kernel adds
-// that partial to each member's private chunks.
+// processed once per group on the tcgen05 kernel (extend_attention.cu, shared-prefix mode):
+// the members' query rows are stacked into dense 128-row tiles, so each shared K/V row is
+// read once per 256 stacked rows instead of once per request; the merge kernel adds that
+// partial to each member's private chunks.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -33,7 +34,15 @@ namespace rx {
 constexpr int DEC_THREADS = 128;   // 4 warps
 constexpr int DEC_STAGE_KEYS = 64; // 16 keys per warp per stage
 constexpr int DEC_NS = 3;          // cp.async ring depth
+constexpr int DEC_MAX_CHUNK = 1024;   // keys per split (the slot list is staged in smem)
 constexpr float LOG2E = 1.4426950408889634f;
+
+__host__ __device__ constexpr int dec_ring_bytes(int D) {
+    // K/V ring, or the cross-warp merge buffer that reuses it, whichever is larger
+    return (DEC_NS * 2 * DEC_STAGE_KEYS * D * 2) > (4 * 8 * D * 4 + 4 * 8 * 2 * 4)
+               ? (DEC_NS * 2 * DEC_STAGE_KEYS * D * 2)
+               : (4 * 8 * D * 4 + 4 * 8 * 2 * 4);
+}
 constexpr float LN2 = 0.6931471805599453f;
 
 struct DecodeParams {
@@ -64,9 +73,11 @@ struct DecodeParams {
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(chunk ^ (row & 7)); }
 
-// Gather one stage of K and V (64 keys starting at key k0) into smem.
+// Gather one stage of K and V (64 keys starting at chunk-relative key k0) into smem.
+// Slot ids come from the chunk's slot list staged in shared memory (slot_s): reading them
+// from global memory here would put one dependent round trip before every copy.
 template <int D>
-__device__ __forceinline__ void dec_load_stage(const DecodeParams& p, const int32_t* slots_row, int k0, int k_end,
+__device__ __forceinline__ void dec_load_stage(const DecodeParams& p, const int32_t* slot_s, int k0, int k_end,
                                                int g, uint32_t kbuf, uint32_t vbuf, int tid) {
     constexpr int CPR = D / 8;                       // 16-byte chunks per row
     constexpr int PER = DEC_STAGE_KEYS * CPR / DEC_THREADS;
@@ -75,7 +86,7 @@ __device__ __forceinline__ void dec_load_stage(const DecodeParams& p, const int3
     for (int x = 0; x < PER; ++x) {
         const int key = tid / CPR + x * (DEC_THREADS / CPR);
         const int kk = k0 + key;
-        int32_t s = kk < k_end ? slots_row[kk] : 0;
+        int32_t s = kk < k_end ? slot_s[kk] : 0;
         uint32_t bytes = 16;
         if (kk >= k_end) bytes = 0;
         else if (s < 0 || s >= p.num_slots) {
@@ -92,13 +103,12 @@ __device__ __forceinline__ void dec_load_stage(const DecodeParams& p, const int3
 
 // Attention of up to 8 query rows (packed into N of m16n8k16) over keys [k_begin, k_end)
 // of one slot-table row; writes normalised partial outputs and log2-domain lse.
-// Row n of the tile is query (qrow_base[n]) -- given by row_q(n) -- and writes partial
-// slot part_idx(n).  Used for private chunks (rows = the group's heads of one request)
-// and for shared chunks (rows = stacked heads of several requests).
+// Row n of the tile reads the query at q_off[n] and writes partial slot out_slot[n]
+// (rows = the query heads of one kv head of one request).
 template <int D>
 __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* slots_row, int k_begin, int k_end,
                                           int g, const int64_t* q_off, const int64_t* out_slot, int nrows,
-                                          unsigned char* smem) {
+                                          unsigned char* smem, int32_t* slot_s) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;                        // m-tiles of O^T
     constexpr int ROWB = D * 2;
@@ -126,9 +136,12 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2*t4, 2*t4+1
 
     const int nstages = (k_end - k_begin + DEC_STAGE_KEYS - 1) / DEC_STAGE_KEYS;
+    const int nk = k_end - k_begin;                  // <= DEC_MAX_CHUNK
+    for (int i = tid; i < nk; i += DEC_THREADS) slot_s[i] = slots_row[k_begin + i];
+    __syncthreads();
 #pragma unroll
     for (int s = 0; s < DEC_NS - 1; ++s) {
-        if (s < nstages) dec_load_stage<D>(p, slots_row, k_begin + s * DEC_STAGE_KEYS, k_end, g, kbuf(s), vbuf(s), tid);
+        if (s < nstages) dec_load_stage<D>(p, slot_s, s * DEC_STAGE_KEYS, nk, g, kbuf(s), vbuf(s), tid);
         cp_async_commit();
     }
     for (int it = 0; it < nstages; ++it) {
@@ -137,8 +150,7 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
         {
             const int nx = it + DEC_NS - 1;
             if (nx < nstages)
-                dec_load_stage<D>(p, slots_row, k_begin + nx * DEC_STAGE_KEYS, k_end, g, kbuf(nx % DEC_NS),
-                                  vbuf(nx % DEC_NS), tid);
+                dec_load_stage<D>(p, slot_s, nx * DEC_STAGE_KEYS, nk, g, kbuf(nx % DEC_NS), vbuf(nx % DEC_NS), tid);
             cp_async_commit();
         }
         const int st = it % DEC_NS;
@@ -269,38 +281,8 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_private_kernel(DecodeParam
         q_off[n] = ((int64_t)b * p.hq + h) * D;
         out_slot[n] = ((int64_t)b * p.hq + h) * per + c;
     }
-    dec_chunk<D>(p, p.r2t + (int64_t)b * p.stride, k_begin, k_end, g, q_off, out_slot, p.group, smem);
-}
-
-// Shared chunks: blockIdx = (chunk * row_blocks + row block, kv head, group).  Up to 8
-// stacked query rows (member, head) per CTA read the group's shared keys once.
-template <int D>
-__global__ void __launch_bounds__(DEC_THREADS) decode_shared_kernel(DecodeParams p, int32_t row_blocks) {
-    extern __shared__ __align__(1024) unsigned char smem[];
-    const int gid = blockIdx.z, g = blockIdx.y;
-    const int c = blockIdx.x / row_blocks, rb = blockIdx.x - c * row_blocks;
-    const int m0 = p.grp_indptr[gid], nm = p.grp_indptr[gid + 1] - m0;
-    const int rows = nm * p.group;
-    const int r0 = rb * 8;
-    if (r0 >= rows) return;
-    // shared length: bounded by every member's own length
-    int len = p.grp_len[gid];
-    const int first = p.grp_members[m0];
-    const int k_begin = c * p.chunk;
-    if (k_begin >= len) return;
-    const int k_end = min(len, k_begin + p.chunk);
-    int64_t q_off[8], out_slot[8];
-    const int per = p.max_chunks + p.grp_chunks;
-    const int nrows = min(8, rows - r0);
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-        const int r = r0 + (n < nrows ? n : 0);
-        const int b = p.grp_members[m0 + r / p.group];
-        const int h = g * p.group + r % p.group;
-        q_off[n] = ((int64_t)b * p.hq + h) * D;
-        out_slot[n] = ((int64_t)b * p.hq + h) * per + p.max_chunks + c;
-    }
-    dec_chunk<D>(p, p.r2t + (int64_t)first * p.stride, k_begin, k_end, g, q_off, out_slot, nrows, smem);
+    dec_chunk<D>(p, p.r2t + (int64_t)b * p.stride, k_begin, k_end, g, q_off, out_slot, p.group, smem,
+                 reinterpret_cast<int32_t*>(smem + dec_ring_bytes(D)));
 }
 
 // Merge the private and shared partials of each (request, head).
@@ -385,11 +367,7 @@ static DecodeLayout dec_layout(const rx_attn_desc* d, int32_t batch, int32_t max
     return L;
 }
 
-static size_t dec_smem_bytes(int D) {
-    const size_t ring = (size_t)DEC_NS * 2 * DEC_STAGE_KEYS * D * 2;
-    const size_t red = (size_t)4 * 8 * D * 4 + 4 * 8 * 2 * 4;
-    return ring > red ? ring : red;
-}
+static size_t dec_smem_bytes(int D) { return (size_t)dec_ring_bytes(D) + DEC_MAX_CHUNK * sizeof(int32_t); }
 
 }  // namespace rx
 
@@ -482,17 +460,11 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
     static bool attr_set[2] = {false, false};
     const int di = D == 128 ? 1 : 0;
     if (!attr_set[di]) {
-        cudaError_t e1, e2;
-        if (D == 128) {
-            e1 = cudaFuncSetAttribute(decode_private_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            e2 = cudaFuncSetAttribute(decode_shared_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        } else {
-            e1 = cudaFuncSetAttribute(decode_private_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            e2 = cudaFuncSetAttribute(decode_shared_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        }
-        if (e1 != cudaSuccess || e2 != cudaSuccess) {
-            set_error("decode_attention: cannot set shared memory size: %s",
-                      cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+        const cudaError_t e1 =
+            D == 128 ? cudaFuncSetAttribute(decode_private_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                     : cudaFuncSetAttribute(decode_private_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e1 != cudaSuccess) {
+            set_error("decode_attention: cannot set shared memory size: %s", cudaGetErrorString(e1));
             return RX_ECUDA;
         }
         attr_set[di] = true;
@@ -500,10 +472,34 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
     if (use_groups) {
         decode_group_of_kernel<<<(batch + 255) / 256, 256, 0, stream>>>(p, group_of);
         decode_group_fill_kernel<<<groups->num_groups, 128, 0, stream>>>(p, group_of);
-        const int row_blocks = (groups->max_group_size * group + 7) / 8;
-        dim3 gs((unsigned)(lay.grp_chunks * row_blocks), (unsigned)desc->hkv, (unsigned)groups->num_groups);
-        if (D == 128) decode_shared_kernel<128><<<gs, DEC_THREADS, smem, stream>>>(p, row_blocks);
-        else decode_shared_kernel<64><<<gs, DEC_THREADS, smem, stream>>>(p, row_blocks);
+        // The shared runs go through the tcgen05 kernel: a group's stacked query rows read
+        // each shared K/V row once per 256 rows.
+        SharedTcParams sp{};
+        sp.q = d_q;
+        sp.r2t = d_req_to_token;
+        sp.stride = r2t_stride;
+        sp.k_pool = d_k_pool;
+        sp.v_pool = d_v_pool;
+        sp.num_slots = desc->num_slots;
+        sp.batch = batch;
+        sp.hq = desc->hq;
+        sp.hkv = desc->hkv;
+        sp.head_dim = D;
+        sp.scale = desc->scale;
+        sp.status = d_status;
+        sp.num_groups = groups->num_groups;
+        sp.max_group_size = groups->max_group_size;
+        sp.grp_indptr = groups->d_group_indptr;
+        sp.grp_members = groups->d_group_members;
+        sp.grp_len = groups->d_group_len;
+        sp.chunk = lay.chunk;
+        sp.n_chunks = lay.grp_chunks;
+        sp.part_o = p.part_o;
+        sp.part_lse = p.part_lse;
+        sp.part_per = lay.max_chunks + lay.grp_chunks;
+        sp.part_base = lay.max_chunks;
+        const int rc = launch_shared_prefix_tc(sp, stream);
+        if (rc != RX_OK) return rc;
     }
     dim3 grid((unsigned)lay.max_chunks, (unsigned)desc->hkv, (unsigned)batch);
     if (D == 128) decode_private_kernel<128><<<grid, DEC_THREADS, smem, stream>>>(p);

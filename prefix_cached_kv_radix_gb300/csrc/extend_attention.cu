@@ -70,6 +70,18 @@ struct ExtendParams {
     float scale_log2;
     int32_t max_qo_len;
     int32_t* status;
+    // Shared-prefix mode (decode groups): CTA (row tile * n_chunks + chunk, kv head, group).
+    // Rows are the members' decode queries (member-major, head fastest); keys are one chunk of
+    // the group's shared run, unmasked; outputs are fp32 normalised partials and log2-domain
+    // log-sum-exp written to part_o/part_lse at partial index part_base + chunk.
+    int32_t shared_mode;
+    const int32_t* grp_indptr;
+    const int32_t* grp_members;
+    const int32_t* grp_len;
+    int32_t chunk, n_chunks;
+    float* part_o;
+    float* part_lse;
+    int32_t part_per, part_base;
 };
 
 template <int D>
@@ -107,23 +119,51 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + LY::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.z, g = blockIdx.y;
-    const int64_t qo0 = p.qo_indptr[b];
-    const int n_b = (int)(p.qo_indptr[b + 1] - qo0);
-    const int P_b = p.prefix_lens[b];
+    const int g = blockIdx.y;
     const int G = p.group;
-    const int rows_total = n_b * G;
-    const int row0 = blockIdx.x * 256;
-    if (row0 >= rows_total || n_b <= 0) return;   // uniform for the whole CTA
-    if (n_b > p.max_qo_len || P_b < 0 || (int64_t)P_b + n_b > p.stride) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.status, RX_DEV_BAD_LENGTH);
-        return;
+    // Extend: packed row R -> token R / G of request b (position P_b + R / G), head g*G + R % G.
+    // Shared-prefix: packed row R -> member R / G of group gid, head g*G + R % G, all keys.
+    int b = 0, n_b = 0, P_b = 0, rows_total, row0, kv_end, m0 = 0, k_lo = 0;
+    int64_t qo0 = 0;
+    const int32_t* slots_row;
+    if (!p.shared_mode) {
+        b = blockIdx.z;
+        qo0 = p.qo_indptr[b];
+        n_b = (int)(p.qo_indptr[b + 1] - qo0);
+        P_b = p.prefix_lens[b];
+        rows_total = n_b * G;
+        row0 = blockIdx.x * 256;
+        if (row0 >= rows_total || n_b <= 0) return;   // uniform for the whole CTA
+        if (n_b > p.max_qo_len || P_b < 0 || (int64_t)P_b + n_b > p.stride) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.status, RX_DEV_BAD_LENGTH);
+            return;
+        }
+        const int last_row = min(row0 + 256, rows_total) - 1;
+        kv_end = P_b + last_row / G + 1;              // keys needed by this CTA
+        slots_row = p.r2t + (int64_t)b * p.stride;
+    } else {
+        const int gid = blockIdx.z;
+        const int c = blockIdx.x % p.n_chunks;
+        m0 = p.grp_indptr[gid];
+        rows_total = (p.grp_indptr[gid + 1] - m0) * G;
+        row0 = (blockIdx.x / p.n_chunks) * 256;
+        const int len = p.grp_len[gid];
+        k_lo = c * p.chunk;
+        if (row0 >= rows_total || k_lo >= len) return;
+        if (len > p.stride) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.status, RX_DEV_BAD_LENGTH);
+            return;
+        }
+        kv_end = min(len, k_lo + p.chunk) - k_lo;     // keys of this chunk, relative to k_lo
+        slots_row = p.r2t + (int64_t)p.grp_members[m0] * p.stride + k_lo;
     }
     const int ntiles = rows_total - row0 > 128 ? 2 : 1;
-    const int last_row = min(row0 + 256, rows_total) - 1;
-    const int kv_end = P_b + last_row / G + 1;              // keys needed by this CTA
     const int nkv = (kv_end + EXT_BN - 1) / EXT_BN;
-    const int32_t* slots_row = p.r2t + (int64_t)b * p.stride;
+    // query row pointer of packed row R (clamped to the last valid row)
+    auto q_row = [&](int R) -> const __nv_bfloat16* {
+        if (!p.shared_mode) return p.q + ((qo0 + R / G) * p.hq + g * G + R % G) * D;
+        return p.q + ((int64_t)p.grp_members[m0 + R / G] * p.hq + g * G + R % G) * D;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(LY::BAR_Q), EXT_LOADERS);
@@ -157,8 +197,7 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             const int rr = qi / CPR, c = qi % CPR;
             const int t = rr >> 7, r = rr & 127;
             const int R = min(row0 + rr, rows_total - 1);
-            const int tok = R / G, h = g * G + R % G;
-            const __nv_bfloat16* src = p.q + ((qo0 + tok) * p.hq + h) * D + c * 8;
+            const __nv_bfloat16* src = q_row(R) + c * 8;
             const uint32_t dst = qs + (uint32_t)(t * LY::Q_TILE + (c >> 3) * 128 * 128 + r * 128 +
                                                  (((c & 7) ^ (r & 7)) << 4));
             cp_async_16(dst, src, 16);
@@ -283,7 +322,7 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             const bool valid = R < rows_total;
             const int Rc = min(R, rows_total - 1);
             const int tok = Rc / G;
-            const int pos = P_b + tok;   // attends keys 0..pos
+            const int pos = p.shared_mode ? kv_end - 1 : P_b + tok;   // attends keys 0..pos
             const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
             const uint32_t s_addr = tmem + lane_base + LY::COL_S0 + t * EXT_BN;
             const uint32_t p_addr = tmem + lane_base + LY::COL_P0 + t * (EXT_BN / 2);
@@ -351,6 +390,25 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             if (ok && warp_wait(bar(LY::BAR_O + t), (nkv - 1) & 1, abort_flag, p.status)) {
                 tc_fence_after();
                 const float inv = 1.f / l;
+                if (p.shared_mode) {
+                    // fp32 normalised partial and log2-domain lse for the decode merge
+                    const int64_t item = (int64_t)p.grp_members[m0 + tok] * p.hq + g * G + Rc % G;
+                    const int64_t slot = item * p.part_per + p.part_base + blockIdx.x % p.n_chunks;
+                    float* prow = p.part_o + slot * D;
+#pragma unroll
+                    for (int cc = 0; cc < D; cc += 32) {
+                        float ov[32];
+                        tmem_ld32(o_addr + cc, ov);
+                        tmem_wait_ld();
+                        if (valid) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                *reinterpret_cast<float4*>(prow + cc + e) =
+                                    make_float4(ov[e] * inv, ov[e + 1] * inv, ov[e + 2] * inv, ov[e + 3] * inv);
+                        }
+                    }
+                    if (valid) p.part_lse[slot] = m_ref + log2f(l);
+                } else {
                 __nv_bfloat16* orow = p.out + ((qo0 + tok) * p.hq + g * G + Rc % G) * D;
 #pragma unroll
                 for (int cc = 0; cc < D; cc += 32) {
@@ -370,6 +428,7 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                     }
                 }
                 if (valid && p.lse) p.lse[(qo0 + tok) * p.hq + g * G + Rc % G] = (m_ref + log2f(l)) * EXT_LN2;
+                }
             }
         }
     }
@@ -407,7 +466,7 @@ static int check_device() {
 }
 
 template <int D>
-static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t stream) {
+static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t stream, int gz) {
     static bool attr = false;
     const int smem = ExtLayout<D>::ALLOC;
     if (!attr) {
@@ -418,8 +477,51 @@ static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t strea
         }
         attr = true;
     }
-    dim3 grid((unsigned)tiles, (unsigned)p.hkv, (unsigned)p.batch);
+    dim3 grid((unsigned)tiles, (unsigned)p.hkv, (unsigned)gz);
     extend_tc_kernel<D><<<grid, EXT_THREADS, smem, stream>>>(p);
+    return RX_OK;
+}
+
+int launch_shared_prefix_tc(const SharedTcParams& sp, cudaStream_t stream) {
+    const int dc = check_device();
+    if (dc != RX_OK) return dc;
+    ExtendParams p{};
+    p.q = (const __nv_bfloat16*)sp.q;
+    p.r2t = sp.r2t;
+    p.stride = sp.stride;
+    p.k_pool = (const __nv_bfloat16*)sp.k_pool;
+    p.v_pool = (const __nv_bfloat16*)sp.v_pool;
+    p.num_slots = sp.num_slots;
+    p.batch = sp.batch;
+    p.hq = sp.hq;
+    p.hkv = sp.hkv;
+    p.group = sp.hq / sp.hkv;
+    p.scale_log2 = sp.scale * EXT_LOG2E;
+    p.status = sp.status;
+    p.shared_mode = 1;
+    p.grp_indptr = sp.grp_indptr;
+    p.grp_members = sp.grp_members;
+    p.grp_len = sp.grp_len;
+    p.chunk = sp.chunk;
+    p.n_chunks = sp.n_chunks;
+    p.part_o = sp.part_o;
+    p.part_lse = sp.part_lse;
+    p.part_per = sp.part_per;
+    p.part_base = sp.part_base;
+    const int64_t row_tiles = ((int64_t)sp.max_group_size * p.group + 255) / 256;
+    const int64_t gx = row_tiles * sp.n_chunks;
+    if (gx >= (1ll << 31) || sp.num_groups >= 65536) {
+        set_error("decode_attention: shared-prefix grid too large");
+        return RX_EINVAL;
+    }
+    const int rc = sp.head_dim == 128 ? launch_extend_tc<128>(p, (int)gx, stream, sp.num_groups)
+                                      : launch_extend_tc<64>(p, (int)gx, stream, sp.num_groups);
+    if (rc != RX_OK) return rc;
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("decode_attention: shared-prefix launch failed: %s", cudaGetErrorString(e));
+        return RX_ECUDA;
+    }
     return RX_OK;
 }
 
@@ -488,8 +590,8 @@ extern "C" int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch, 
     p.status = d_status;
     const int64_t tiles = ((int64_t)max_qo_len * group + 255) / 256;
     RX_REQUIRE(tiles < 65536 && batch < 65536, "prefix_extend_attention: grid too large");
-    const int rc = desc->head_dim == 128 ? launch_extend_tc<128>(p, (int)tiles, stream)
-                                         : launch_extend_tc<64>(p, (int)tiles, stream);
+    const int rc = desc->head_dim == 128 ? launch_extend_tc<128>(p, (int)tiles, stream, batch)
+                                         : launch_extend_tc<64>(p, (int)tiles, stream, batch);
     if (rc != RX_OK) return rc;
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {

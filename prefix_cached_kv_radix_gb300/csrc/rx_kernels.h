@@ -28,4 +28,29 @@ struct SimtParams {
 
 int launch_attn_simt(const SimtParams& p, int dtype, int head_dim, cudaStream_t stream);
 
+// Shared-prefix part of decode on the tcgen05 kernel: for every group, the members' query
+// rows (stacked) attend one chunk of the group's shared keys; fp32 normalised partials and
+// log2-domain lse go to part_o/part_lse at partial index part_base + chunk.
+struct SharedTcParams {
+    const void* q;                // [batch, hq, D] bf16
+    const int32_t* r2t;
+    int64_t stride;
+    const void* k_pool;
+    const void* v_pool;
+    int64_t num_slots;
+    int32_t batch, hq, hkv, head_dim;
+    float scale;
+    int32_t* status;
+    int32_t num_groups, max_group_size;
+    const int32_t* grp_indptr;
+    const int32_t* grp_members;
+    const int32_t* grp_len;
+    int32_t chunk, n_chunks;
+    float* part_o;
+    float* part_lse;
+    int32_t part_per, part_base;
+};
+
+int launch_shared_prefix_tc(const SharedTcParams& p, cudaStream_t stream);
+
 }  // namespace rx

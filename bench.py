@@ -207,8 +207,9 @@ def run_ours(args, rank, world, local_rank):
 
     def step(i, e2e=False, timed_att=False):
         toks, ind = step_inputs[i]
-        plan = eng.plan_concat(toks, ind, n_new)
+        plan = eng.plan_concat(toks, ind, n_new, groups=s.decode)
         d = eng.upload(plan)
+        grp = eng.groups(plan, d) if s.decode else None
         if e2e:
             qd.copy_(qh, non_blocking=True)
             kd.copy_(kh, non_blocking=True)
@@ -218,8 +219,6 @@ def run_ours(args, rank, world, local_rank):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
         if s.decode:
-            grp, keep = eng.groups(plan)
-            d["_keep"] = keep
             eng.decode(plan, d, qd, out, lse, groups=grp)
             # kv_pool_write + (group map, group fill, shared chunks) + private chunks + merge
             n_launch = 1 + (3 if grp is not None else 0) + 2

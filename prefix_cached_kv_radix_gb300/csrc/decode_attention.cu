@@ -340,12 +340,12 @@ __global__ void decode_group_fill_kernel(DecodeParams p, int32_t* group_of) {
 }
 
 static int dec_chunk_keys(int32_t batch, int32_t hkv, int32_t max_kv_len) {
-    // Enough CTAs to fill 152 SMs several times over; chunks of 256..1024 keys.
-    int chunk = 512;
-    const int64_t ctas = (int64_t)batch * hkv * ((max_kv_len + chunk - 1) / chunk);
-    if (ctas < 152 * 4) chunk = 256;
-    if (max_kv_len > 65536 && ctas > 152 * 64) chunk = 1024;
-    return chunk;
+    // Long chunks amortise each CTA's start (slot staging, Q fragments) and end (cross-warp
+    // merge, partial write) over more bytes; short ones keep enough CTAs to fill 152 SMs.
+    auto ctas = [&](int c) { return (int64_t)batch * hkv * ((max_kv_len + c - 1) / c); };
+    if (ctas(1024) >= 152 * 16) return 1024;
+    if (ctas(512) >= 152 * 4) return 512;
+    return 256;
 }
 
 struct DecodeLayout {

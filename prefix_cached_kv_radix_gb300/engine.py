@@ -44,6 +44,9 @@ class StepPlan:
     max_qo_len: int
     max_kv_len: int
     stride: int
+    grp_indptr: np.ndarray = None   # decode shared-prefix groups (optional)
+    grp_members: np.ndarray = None
+    grp_len: np.ndarray = None
 
 
 class PrefixCacheEngine:
@@ -104,15 +107,15 @@ class PrefixCacheEngine:
         return n
 
     # ------------------------------------------------------------------ step
-    def plan(self, prompts, n_new) -> StepPlan:
+    def plan(self, prompts, n_new, groups: bool = False, min_shared: int = 64) -> StepPlan:
         """a1 + a2 for a list of prompts (see plan_concat)."""
         b = len(prompts)
         lens = np.array([len(p) for p in prompts], np.int64)
         tok_indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
         tokens = np.concatenate(prompts).astype(np.int32) if b else np.zeros(0, np.int32)
-        return self.plan_concat(tokens, tok_indptr, n_new)
+        return self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)
 
-    def plan_concat(self, tokens, tok_indptr, n_new) -> StepPlan:
+    def plan_concat(self, tokens, tok_indptr, n_new, groups: bool = False, min_shared: int = 64) -> StepPlan:
         """a1 + a2: match every prompt (tokens[tok_indptr[b]:tok_indptr[b+1]]), check that
         exactly its last n_new[b] tokens are uncached, allocate their slots, pin the matched
         prefixes for the duration of the step."""
@@ -131,8 +134,19 @@ class PrefixCacheEngine:
         self.tree.lock_batch(last)          # in flight: the matched prefixes cannot be evicted
         qo = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int64)
         max_kv = int(lens.max()) if b else 1
-        return StepPlan(b, tokens, tok_indptr, ps, pind, P.astype(np.int32), new, qo, last,
+        plan = StepPlan(b, tokens, tok_indptr, ps, pind, P.astype(np.int32), new, qo, last,
                         int(n_new.max()) if b else 0, max_kv, ((max_kv + 7) // 8) * 8)
+        if groups and b:
+            # requests whose cached paths share a node: their shared run is read once per group
+            gof, glen = self.tree.shared_groups(last, min_shared)
+            if len(glen):
+                order = np.argsort(gof, kind="stable")
+                order = order[gof[order] >= 0]
+                counts = np.bincount(gof[order], minlength=len(glen))
+                plan.grp_members = order.astype(np.int32)
+                plan.grp_indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+                plan.grp_len = glen.astype(np.int32)
+        return plan
 
     def upload(self, plan: StepPlan, stream=None) -> dict:
         """Move the step's index arrays to the device: packed into one pinned host buffer and
@@ -144,6 +158,9 @@ class PrefixCacheEngine:
                  ("qo_indptr", plan.qo_indptr, np.int64),
                  ("prefix_lens", plan.prefix_lens, np.int32),
                  ("kv_lens", plan.prefix_lens.astype(np.int64) + np.diff(plan.qo_indptr), np.int32)]
+        if plan.grp_len is not None:
+            parts += [("grp_indptr", plan.grp_indptr, np.int32), ("grp_members", plan.grp_members, np.int32),
+                      ("grp_len", plan.grp_len, np.int32)]
         offs, total = [], 0
         for _, a, dt in parts:
             offs.append(total)
@@ -186,16 +203,13 @@ class PrefixCacheEngine:
         api.prefix_extend_attention(self.desc, plan.batch, q, dev["qo_indptr"], dev["prefix_lens"], dev["r2t"],
                                     self.k_pool, self.v_pool, out, lse, plan.max_qo_len, self.status, stream)
 
-    def groups(self, plan: StepPlan, min_shared: int = 64):
-        """Shared-prefix groups of a decode batch from the tree (host), as device arrays."""
-        gof, glen = self.tree.shared_groups(plan.last_nodes, min_shared)
-        if len(glen) == 0:
-            return None, None
-        members = [np.flatnonzero(gof == g) for g in range(len(glen))]
-        indptr = np.concatenate([[0], np.cumsum([len(m) for m in members])]).astype(np.int32)
-        keep = (self._i32(indptr), self._i32(np.concatenate(members)), self._i32(glen))
-        st = api.shared_groups_struct(len(glen), int(max(len(m) for m in members)), *keep, int(glen.max()))
-        return st, keep
+    def groups(self, plan: StepPlan, dev: dict):
+        """The plan's shared-prefix groups (computed by plan(..., groups=True) and uploaded with
+        the step's index arrays) as the ABI struct, or None."""
+        if plan.grp_len is None:
+            return None
+        return api.shared_groups_struct(len(plan.grp_len), int(np.diff(plan.grp_indptr).max()), dev["grp_indptr"],
+                                        dev["grp_members"], dev["grp_len"], int(plan.grp_len.max()))
 
     def decode_workspace(self, plan: StepPlan, groups=None):
         nbytes = api.decode_workspace_bytes(self.desc, plan.batch, plan.max_kv_len, groups)

@@ -50,7 +50,7 @@ def run_step(w, engine=None, groups=False, lse=True, poison=True):
     for i in range(len(s.histories)):
         k, v = w.history_kv(i)
         eng.populate(w.history_tokens(i), k, v)
-    plan = eng.plan([w.request_tokens(b) for b in range(w.batch)], s.req_new)
+    plan = eng.plan([w.request_tokens(b) for b in range(w.batch)], s.req_new, groups=groups and s.decode)
     dev = eng.upload(plan)
     q, kn, vn = w.stacked_new()
     qd, kd, vd = (_dev_from_host(x, s.dtype, eng.device) for x in (q, kn, vn))
@@ -59,9 +59,7 @@ def run_step(w, engine=None, groups=False, lse=True, poison=True):
     eng.write(plan, dev, kd, vd)
     grp = None
     if s.decode:
-        if groups:
-            grp, _keep = eng.groups(plan)
-            dev["_keep"] = _keep
+        grp = eng.groups(plan, dev) if groups else None
         eng.decode(plan, dev, qd, out, lse_t, groups=grp)
     else:
         eng.extend(plan, dev, qd, out, lse_t)

@@ -207,9 +207,9 @@ def run_ours(args, rank, world, local_rank):
 
     def step(i, e2e=False, timed_att=False):
         toks, ind = step_inputs[i]
-        plan = eng.plan_concat(toks, ind, n_new, groups=s.decode)
+        plan = eng.plan_concat(toks, ind, n_new, groups=True if s.decode else "auto")
         d = eng.upload(plan)
-        grp = eng.groups(plan, d) if s.decode else None
+        grp = eng.groups(plan, d)
         if e2e:
             qd.copy_(qh, non_blocking=True)
             kd.copy_(kh, non_blocking=True)
@@ -224,7 +224,8 @@ def run_ours(args, rank, world, local_rank):
             n_launch = 1 + (3 if grp is not None else 0) + 2
         else:
             eng.extend(plan, d, qd, out, lse)
-            n_launch = 2   # kv_pool_write + extend
+            # kv_pool_write + extend, or + (prep, shared tcgen05, private, merge) with groups
+            n_launch = 2 if grp is None else 5
         if timed_att or e2e:
             launches[0] += n_launch
         if timed_att:

@@ -164,6 +164,49 @@ int insert_batch_at(rx_radix* t, int32_t batch, const rx_node* nodes, const int3
                     const int64_t* tok_indptr, const int32_t* new_slots, const int64_t* new_indptr,
                     int64_t* out_dup_len, rx_node* out_last);
 
+/* ------------------------------------------------------------------ step runtime
+ * One serving step over a batch of prompts, with all host work native: rx_step_plan does
+ * a1/a2 (match, allocate, pin) and lays every index array the kernels need into a
+ * caller-provided staging buffer (pinned host memory, copied to the device with one
+ * transfer); rx_step_finish does a7/a8 (insert, evict) and unpins.  Offsets are bytes from
+ * the start of the staging buffer, each 256-byte aligned; the same offsets apply to the
+ * device copy.  Arrays: prefix_slots int32 [sum P_b], prefix_indptr int64 [batch+1],
+ * new_slots int32 [T], qo_indptr int64 [batch+1], prefix_lens int32 [batch], kv_lens int32
+ * [batch] (P_b + n_b), and with groups grp_indptr / grp_members / grp_len int32. */
+typedef struct {
+    int32_t batch;
+    int32_t max_qo_len, max_kv_len, stride;  /* stride = max_kv_len rounded up to 8 */
+    int64_t total_new;                       /* T */
+    int64_t total_prefix;                    /* sum P_b */
+    int64_t bytes;                           /* bytes of the staging buffer in use */
+    int64_t off_prefix_slots, off_prefix_indptr, off_new_slots, off_qo_indptr, off_prefix_lens, off_kv_lens;
+    int32_t num_groups, max_group_size, max_group_len, max_group_rows;
+    int64_t off_grp_indptr, off_grp_members, off_grp_len;
+} rx_step_layout;
+
+enum { RX_GROUPS_NONE = 0, RX_GROUPS_ALWAYS = 1, RX_GROUPS_AUTO = 2 };
+
+/* Upper bound of the staging bytes rx_step_plan needs for these prompts. */
+size_t rx_step_stage_bytes(int32_t batch, int64_t total_tokens);
+
+/* Plan one step: request b's prompt is tokens[tok_indptr[b] : tok_indptr[b+1]], of which the
+ * last n_new[b] tokens must be uncached (RX_EINVAL otherwise, nothing allocated); allocates
+ * their slots (RX_ENOMEM if short: evict and retry), locks each request's matched node
+ * (out_last[b], capacity batch) until rx_step_finish.  group_mode: RX_GROUPS_NONE, _ALWAYS
+ * (radix_shared_groups with min_shared) or _AUTO (only when every request is in a group, its
+ * remaining keys are <= 256 and a request's new rows times heads_per_kv stay below 128 --
+ * the shape where stacking rows pays). */
+int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
+                 const int32_t* n_new, int32_t group_mode, int32_t heads_per_kv, int64_t min_shared,
+                 void* h_stage, size_t stage_cap, rx_node* out_last, rx_step_layout* out);
+
+/* Finish the step planned into h_stage: insert every prompt from its matched node, return
+ * new slots that turned out cached to the free list, evict >= evict_tokens LRU tokens (0:
+ * none; *out_evicted receives the count, may be NULL) and unlock the matched nodes. */
+int rx_step_finish(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
+                   const rx_node* last_nodes, const void* h_stage, const rx_step_layout* layout,
+                   int64_t evict_tokens, int64_t* out_evicted);
+
 int radix_stats(const rx_radix* t, rx_stats* out);
 
 /* Check the tree's invariants (edges, parents, slot ownership, stamps, locks);
@@ -205,6 +248,21 @@ int kv_pool_write(const rx_attn_desc* desc, int32_t batch,
                   int32_t* d_req_to_token, int64_t r2t_stride, int64_t total_new,
                   int32_t* d_status, void* stream);
 
+/* Optional description of requests that share a leading run of KV (a cached prefix), for
+ * decode_attention and prefix_extend_attention.  Members of group g have identical
+ * req_to_token[b, 0:len_g] (e.g. radix_shared_groups on their matched nodes); the shared
+ * part is read once per group, for all members' query rows stacked, instead of once per
+ * member, and merged exactly with each member's private part. */
+typedef struct {
+    int32_t num_groups;
+    int32_t max_group_size;          /* host hint: largest group (members) */
+    const int32_t* d_group_indptr;   /* [num_groups+1] offsets into d_group_members */
+    const int32_t* d_group_members;  /* request ids; a request is in at most one group */
+    const int32_t* d_group_len;      /* [num_groups] shared leading tokens, >= 1 */
+    int32_t max_group_len;           /* host hint: largest d_group_len */
+    int32_t max_group_rows;          /* extend only, host hint: largest sum of new tokens over a group's members */
+} rx_shared_groups;
+
 /* Extend (prefill over the new tokens) attention with a cached prefix.
  * For request b with P_b = d_prefix_lens[b] cached tokens and n_b = qo_indptr[b+1]-qo_indptr[b]
  * new tokens, new row i (absolute position p = P_b + i) of query head h computes
@@ -216,25 +274,25 @@ int kv_pool_write(const rx_attn_desc* desc, int32_t batch,
  * d_q, d_out: [T, hq, head_dim]; d_lse: optional [T, hq] float32 natural-log log-sum-exp
  * of the scaled scores.  max_qo_len (host) must be >= every n_b (sizes the grid); rows of
  * a request with n_b > max_qo_len or P_b + n_b > r2t_stride are skipped with
- * RX_DEV_BAD_LENGTH.  bf16 runs on tcgen05 tensor cores (sm_103a); f32 on CUDA cores. */
+ * RX_DEV_BAD_LENGTH.  bf16 runs on tcgen05 tensor cores (sm_103a); f32 on CUDA cores.
+ * groups (optional, bf16): requests sharing a cached prefix.  Their new rows are stacked
+ * into dense tiles against one read of the shared run (tcgen05), each request's remaining
+ * keys (its private cached tokens and its new tokens, causally) are done per row on CUDA
+ * cores, and the two softmax parts are merged exactly.  Worth it when the new rows per
+ * request are few and the private parts short (e.g. many short questions on one system
+ * prompt).  d_workspace: >= extend_workspace_bytes(...) bytes, 256-byte aligned, needed only
+ * with groups (else NULL / 0). */
 int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch,
                             const void* d_q, const int64_t* d_qo_indptr, const int32_t* d_prefix_lens,
                             const int32_t* d_req_to_token, int64_t r2t_stride,
                             const void* d_k_pool, const void* d_v_pool,
                             void* d_out, float* d_lse, int32_t max_qo_len,
+                            const rx_shared_groups* groups, void* d_workspace, size_t ws_bytes,
                             int32_t* d_status, void* stream);
 
-/* Optional description of requests that share a leading run of KV (a cached prefix)
- * in a decode batch.  Members of group g have identical req_to_token[b, 0:len_g]; the
- * shared part is read once per group instead of once per member. */
-typedef struct {
-    int32_t num_groups;
-    int32_t max_group_size;          /* host hint: largest group */
-    const int32_t* d_group_indptr;   /* [num_groups+1] offsets into d_group_members */
-    const int32_t* d_group_members;  /* request ids; a request is in at most one group */
-    const int32_t* d_group_len;      /* [num_groups] shared leading tokens, >= 1 */
-    int32_t max_group_len;           /* host hint: largest d_group_len */
-} rx_shared_groups;
+/* Bytes of device workspace prefix_extend_attention needs with these groups (0 without). */
+size_t extend_workspace_bytes(const rx_attn_desc* desc, int32_t batch, int32_t max_qo_len,
+                              const rx_shared_groups* groups);
 
 /* Bytes of device workspace decode_attention needs for this batch (>= 0), or 0 on error. */
 size_t decode_workspace_bytes(const rx_attn_desc* desc, int32_t batch, int32_t max_kv_len,

@@ -24,7 +24,8 @@ EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "radix_lock", "radix
            "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "insert_batch_at", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups",
-           "kv_pool_write", "prefix_extend_attention", "decode_workspace_bytes", "decode_attention",
+           "kv_pool_write", "prefix_extend_attention", "extend_workspace_bytes", "decode_workspace_bytes",
+           "decode_attention",
            "decode_attention_noalloc",
            "rx_last_error", "rx_version")
 
@@ -49,7 +50,8 @@ class rx_stats(ctypes.Structure):
 class rx_shared_groups(ctypes.Structure):
     _fields_ = [("num_groups", ctypes.c_int32), ("max_group_size", ctypes.c_int32),
                 ("d_group_indptr", ctypes.c_void_p), ("d_group_members", ctypes.c_void_p),
-                ("d_group_len", ctypes.c_void_p), ("max_group_len", ctypes.c_int32)]
+                ("d_group_len", ctypes.c_void_p), ("max_group_len", ctypes.c_int32),
+                ("max_group_rows", ctypes.c_int32)]
 
 
 _lib = None
@@ -85,7 +87,8 @@ def load(path: str = LIB_PATH):
         "radix_check": (ctypes.c_int, [P]),
         "radix_shared_groups": (ctypes.c_int, [P, P, I32, I64, P, P, P]),
         "kv_pool_write": (ctypes.c_int, [P, I32, P, P, P, P, P, P, P, P, P, I64, I64, P, P]),
-        "prefix_extend_attention": (ctypes.c_int, [P, I32, P, P, P, P, I64, P, P, P, P, I32, P, P]),
+        "prefix_extend_attention": (ctypes.c_int, [P, I32, P, P, P, P, I64, P, P, P, P, I32, P, P, SZ, P, P]),
+        "extend_workspace_bytes": (SZ, [P, I32, I32, P]),
         "decode_workspace_bytes": (SZ, [P, I32, I32, P]),
         "decode_attention": (ctypes.c_int, [P, I32, P, P, I64, P, P, P, P, P, P, I32, P, SZ, P, P]),
         "decode_attention_noalloc": (ctypes.c_int, [P, I32, P, P, I64, P, P, P, P, P, P, I32, P, P]),
@@ -110,20 +113,22 @@ def _np_i32(a) -> np.ndarray:
 
 
 def _ptr(t):
-    """Device pointer of a tensor (None -> NULL)."""
+    """Device pointer of a tensor, or an integer device address (None -> NULL)."""
     if t is None:
         return None
+    if isinstance(t, int):
+        return t
     assert t.is_cuda and t.is_contiguous(), "device buffers must be contiguous CUDA tensors"
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _stream(stream):
     if stream is None:
         import torch
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
-        return ctypes.c_void_p(stream)
-    return ctypes.c_void_p(stream.cuda_stream)
+        return stream
+    return stream.cuda_stream
 
 
 def version() -> str:
@@ -211,12 +216,20 @@ def insert(tree, tokens, slots):
 
 
 def evict(tree, num_tokens: int, cap: int | None = None) -> np.ndarray:
-    """Frees LRU leaves until >= num_tokens are freed; returns the freed slots (up to cap)."""
-    cap = num_tokens + 1_000_000 if cap is None else cap
-    out = np.empty(max(cap, 1), np.int32)
+    """Frees LRU leaves until >= num_tokens are freed; returns the freed slots (the first
+    `cap` of them; default: all)."""
     n = I64()
-    _check("evict", load().evict(tree, num_tokens, out.ctypes.data, cap, ctypes.byref(n)))
-    return out[: min(n.value, cap)].copy()
+    c = radix_stats(tree)["cached_tokens"] if cap is None else cap   # at most everything cached
+    out = np.empty(max(c, 1), np.int32)
+    _check("evict", load().evict(tree, num_tokens, out.ctypes.data, c, ctypes.byref(n)))
+    return out[: min(n.value, c)].copy()
+
+
+def evict_count(tree, num_tokens: int) -> int:
+    """evict without collecting the freed slots; returns how many were freed."""
+    n = I64()
+    _check("evict", load().evict(tree, num_tokens, None, 0, ctypes.byref(n)))
+    return n.value
 
 
 def match_prefix_batch(tree, tokens, tok_indptr):
@@ -289,6 +302,9 @@ class RadixTree:
     def evict(self, n, cap=None):
         return evict(self.h, n, cap)
 
+    def evict_count(self, n):
+        return evict_count(self.h, n)
+
     def alloc_slots(self, n):
         return alloc_slots(self.h, n)
 
@@ -328,27 +344,38 @@ class RadixTree:
 
 # ============================================================================ kernels
 def kv_pool_write(desc, batch, prefix_slots, prefix_indptr, new_slots, qo_indptr, k_new, v_new, k_pool, v_pool,
-                  req_to_token, total_new, status, stream=None) -> None:
+                  req_to_token, total_new, status, stream=None, r2t_stride=None) -> None:
+    """req_to_token: a [batch, stride] tensor, or a device address with r2t_stride given."""
+    stride = req_to_token.shape[1] if r2t_stride is None else r2t_stride
     _check("kv_pool_write", load().kv_pool_write(
         ctypes.byref(desc), batch, _ptr(prefix_slots), _ptr(prefix_indptr), _ptr(new_slots), _ptr(qo_indptr),
-        _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(req_to_token), req_to_token.shape[1],
+        _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(req_to_token), stride,
         total_new, _ptr(status), _stream(stream)))
 
 
 def prefix_extend_attention(desc, batch, q, qo_indptr, prefix_lens, req_to_token, k_pool, v_pool, out, lse,
-                            max_qo_len, status, stream=None) -> None:
+                            max_qo_len, status, groups=None, workspace=None, stream=None, r2t_stride=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    stride = req_to_token.shape[1] if r2t_stride is None else r2t_stride
     _check("prefix_extend_attention", load().prefix_extend_attention(
         ctypes.byref(desc), batch, _ptr(q), _ptr(qo_indptr), _ptr(prefix_lens), _ptr(req_to_token),
-        req_to_token.shape[1], _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(lse), max_qo_len, _ptr(status),
+        stride, _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(lse), max_qo_len,
+        ctypes.byref(groups) if groups is not None else None, _ptr(workspace), ws_bytes, _ptr(status),
         _stream(stream)))
 
 
-def shared_groups_struct(num_groups, max_group_size, group_indptr, group_members, group_len, max_group_len):
-    """rx_shared_groups from device tensors (int32)."""
+def extend_workspace_bytes(desc, batch, max_qo_len, groups=None) -> int:
+    return int(load().extend_workspace_bytes(ctypes.byref(desc), batch, max_qo_len,
+                                             ctypes.byref(groups) if groups is not None else None))
+
+
+def shared_groups_struct(num_groups, max_group_size, group_indptr, group_members, group_len, max_group_len,
+                         max_group_rows=0):
+    """rx_shared_groups from device int32 arrays (tensors or device addresses)."""
     if num_groups == 0:
         return None
-    return rx_shared_groups(num_groups, max_group_size, group_indptr.data_ptr(), group_members.data_ptr(),
-                            group_len.data_ptr(), max_group_len)
+    return rx_shared_groups(num_groups, max_group_size, _ptr(group_indptr), _ptr(group_members),
+                            _ptr(group_len), max_group_len, max_group_rows)
 
 
 def decode_workspace_bytes(desc, batch, max_kv_len, groups=None) -> int:
@@ -357,10 +384,11 @@ def decode_workspace_bytes(desc, batch, max_kv_len, groups=None) -> int:
 
 
 def decode_attention(desc, batch, q, req_to_token, kv_lens, k_pool, v_pool, out, lse, max_kv_len, workspace,
-                     status, groups=None, stream=None) -> None:
+                     status, groups=None, stream=None, r2t_stride=None) -> None:
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    stride = req_to_token.shape[1] if r2t_stride is None else r2t_stride
     _check("decode_attention", load().decode_attention(
-        ctypes.byref(desc), batch, _ptr(q), _ptr(req_to_token), req_to_token.shape[1], _ptr(kv_lens),
+        ctypes.byref(desc), batch, _ptr(q), _ptr(req_to_token), stride, _ptr(kv_lens),
         ctypes.byref(groups) if groups is not None else None, _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(lse),
         max_kv_len, _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
 

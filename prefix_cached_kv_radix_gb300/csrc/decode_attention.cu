@@ -69,6 +69,7 @@ struct DecodeParams {
     int32_t grp_chunks;         // shared partial slots per (request, head)
     int32_t grp_rows_max;       // max stacked rows (members * group) of a group
     const int32_t* group_of;    // [batch] group id or -1 (workspace, filled by a prep kernel)
+    int32_t* group_src;         // [num_groups] first member (its slot-table row holds the shared slots)
 };
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(chunk ^ (row & 7)); }
@@ -331,12 +332,14 @@ __global__ void decode_group_of_kernel(DecodeParams p, int32_t* group_of) {
     for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < p.batch; b += gridDim.x * blockDim.x) group_of[b] = -1;
 }
 __global__ void decode_group_fill_kernel(DecodeParams p, int32_t* group_of) {
-    for (int gid = blockIdx.x; gid < p.num_groups; gid += gridDim.x)
+    for (int gid = blockIdx.x; gid < p.num_groups; gid += gridDim.x) {
+        if (threadIdx.x == 0) p.group_src[gid] = p.grp_members[p.grp_indptr[gid]];
         for (int i = p.grp_indptr[gid] + threadIdx.x; i < p.grp_indptr[gid + 1]; i += blockDim.x) {
             const int b = p.grp_members[i];
             if (b >= 0 && b < p.batch) group_of[b] = gid;
             else report(p.status, RX_DEV_BAD_LENGTH);
         }
+    }
 }
 
 static int dec_chunk_keys(int32_t batch, int32_t hkv, int32_t max_kv_len) {
@@ -350,7 +353,7 @@ static int dec_chunk_keys(int32_t batch, int32_t hkv, int32_t max_kv_len) {
 
 struct DecodeLayout {
     int chunk, max_chunks, grp_chunks;
-    size_t part_o_bytes, part_lse_bytes, group_of_bytes, total;
+    size_t part_o_bytes, part_lse_bytes, group_of_bytes, group_src_bytes, total;
 };
 
 static DecodeLayout dec_layout(const rx_attn_desc* d, int32_t batch, int32_t max_kv_len, const rx_shared_groups* grp) {
@@ -362,8 +365,9 @@ static DecodeLayout dec_layout(const rx_attn_desc* d, int32_t batch, int32_t max
     L.part_o_bytes = (size_t)batch * d->hq * per * d->head_dim * sizeof(float);
     L.part_lse_bytes = (size_t)batch * d->hq * per * sizeof(float);
     L.group_of_bytes = (grp && grp->num_groups > 0) ? (size_t)batch * sizeof(int32_t) : 0;
+    L.group_src_bytes = (grp && grp->num_groups > 0) ? (size_t)grp->num_groups * sizeof(int32_t) : 0;
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    L.total = up(L.part_o_bytes) + up(L.part_lse_bytes) + up(L.group_of_bytes);
+    L.total = up(L.part_o_bytes) + up(L.part_lse_bytes) + up(L.group_of_bytes) + up(L.group_src_bytes);
     return L;
 }
 
@@ -448,6 +452,7 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
     int32_t* group_of = nullptr;
     if (use_groups) {
         group_of = (int32_t*)(ws + up(lay.part_o_bytes) + up(lay.part_lse_bytes));
+        p.group_src = (int32_t*)(ws + up(lay.part_o_bytes) + up(lay.part_lse_bytes) + up(lay.group_of_bytes));
         p.num_groups = groups->num_groups;
         p.grp_indptr = groups->d_group_indptr;
         p.grp_members = groups->d_group_members;
@@ -488,9 +493,10 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
         sp.scale = desc->scale;
         sp.status = d_status;
         sp.num_groups = groups->num_groups;
-        sp.max_group_size = groups->max_group_size;
-        sp.grp_indptr = groups->d_group_indptr;
-        sp.grp_members = groups->d_group_members;
+        sp.max_group_rows = groups->max_group_size;     // one query row per member in decode
+        sp.grp_row_indptr = groups->d_group_indptr;
+        sp.grp_rows = groups->d_group_members;
+        sp.grp_src = p.group_src;
         sp.grp_len = groups->d_group_len;
         sp.chunk = lay.chunk;
         sp.n_chunks = lay.grp_chunks;

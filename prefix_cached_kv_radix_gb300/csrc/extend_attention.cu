@@ -70,13 +70,15 @@ struct ExtendParams {
     float scale_log2;
     int32_t max_qo_len;
     int32_t* status;
-    // Shared-prefix mode (decode groups): CTA (row tile * n_chunks + chunk, kv head, group).
-    // Rows are the members' decode queries (member-major, head fastest); keys are one chunk of
-    // the group's shared run, unmasked; outputs are fp32 normalised partials and log2-domain
-    // log-sum-exp written to part_o/part_lse at partial index part_base + chunk.
+    // Shared-prefix mode: CTA (row tile * n_chunks + chunk, kv head, group).  The rows of
+    // group gid are the query rows grp_rows[grp_row_indptr[gid] ..] (global row ids of q,
+    // head fastest within a row); keys are one chunk of the group's shared run, taken from
+    // the slot-table row grp_src[gid], unmasked; outputs are fp32 normalised partials and
+    // log2-domain log-sum-exp at partial index part_base + chunk of (row, head).
     int32_t shared_mode;
-    const int32_t* grp_indptr;
-    const int32_t* grp_members;
+    const int32_t* grp_row_indptr;
+    const int32_t* grp_rows;
+    const int32_t* grp_src;
     const int32_t* grp_len;
     int32_t chunk, n_chunks;
     float* part_o;
@@ -144,8 +146,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
     } else {
         const int gid = blockIdx.z;
         const int c = blockIdx.x % p.n_chunks;
-        m0 = p.grp_indptr[gid];
-        rows_total = (p.grp_indptr[gid + 1] - m0) * G;
+        m0 = p.grp_row_indptr[gid];
+        rows_total = (p.grp_row_indptr[gid + 1] - m0) * G;
         row0 = (blockIdx.x / p.n_chunks) * 256;
         const int len = p.grp_len[gid];
         k_lo = c * p.chunk;
@@ -155,14 +157,14 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             return;
         }
         kv_end = min(len, k_lo + p.chunk) - k_lo;     // keys of this chunk, relative to k_lo
-        slots_row = p.r2t + (int64_t)p.grp_members[m0] * p.stride + k_lo;
+        slots_row = p.r2t + (int64_t)p.grp_src[gid] * p.stride + k_lo;
     }
     const int ntiles = rows_total - row0 > 128 ? 2 : 1;
     const int nkv = (kv_end + EXT_BN - 1) / EXT_BN;
     // query row pointer of packed row R (clamped to the last valid row)
     auto q_row = [&](int R) -> const __nv_bfloat16* {
         if (!p.shared_mode) return p.q + ((qo0 + R / G) * p.hq + g * G + R % G) * D;
-        return p.q + ((int64_t)p.grp_members[m0 + R / G] * p.hq + g * G + R % G) * D;
+        return p.q + ((int64_t)p.grp_rows[m0 + R / G] * p.hq + g * G + R % G) * D;
     };
 
     if (threadIdx.x == 0) {
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                 const float inv = 1.f / l;
                 if (p.shared_mode) {
                     // fp32 normalised partial and log2-domain lse for the decode merge
-                    const int64_t item = (int64_t)p.grp_members[m0 + tok] * p.hq + g * G + Rc % G;
+                    const int64_t item = (int64_t)p.grp_rows[m0 + tok] * p.hq + g * G + Rc % G;
                     const int64_t slot = item * p.part_per + p.part_base + blockIdx.x % p.n_chunks;
                     float* prow = p.part_o + slot * D;
 #pragma unroll
@@ -482,6 +484,193 @@ static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t strea
     return RX_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+// Grouped extend (requests sharing a cached prefix): the shared run is processed once for
+// all members' stacked new rows on the tcgen05 kernel (partials per key chunk); each
+// request's own tail (its private cached tokens and its new tokens, causally) on CUDA
+// cores, merged exactly with the shared chunks:
+//   M = max_s lse_s, o = sum_s 2^(lse_s-M) o_s / sum_s 2^(lse_s-M).
+struct GroupedExtendWs {
+    float* part_o;        // [T * hq][per][D]
+    float* part_lse;      // [T * hq][per] (log2 domain)
+    int32_t* row_indptr;  // [num_groups + 1]
+    int32_t* rows;        // [T]
+    int32_t* src;         // [num_groups]
+    int32_t* shared_of;   // [batch] shared tokens of the request's group (0 outside groups)
+    int32_t per;          // 1 (private) + shared chunks
+};
+
+// One block of 1024 threads: per-request shared lengths, the groups' row lists (members' new
+// tokens, in member order) and source slot-table rows.  Members are processed 1024 at a time;
+// each thread takes one member, a block-wide scan places its rows.
+__global__ void __launch_bounds__(1024) grouped_prep_kernel(int32_t batch, const int64_t* qo_indptr, int32_t num_groups,
+                                                           const int32_t* grp_indptr, const int32_t* grp_members,
+                                                           const int32_t* grp_len, GroupedExtendWs ws, int32_t* status) {
+    __shared__ int32_t scan[1024];
+    __shared__ int32_t carry;
+    for (int b = threadIdx.x; b < batch; b += blockDim.x) ws.shared_of[b] = 0;
+    for (int gid = threadIdx.x; gid < num_groups; gid += blockDim.x)
+        ws.src[gid] = (grp_indptr[gid + 1] > grp_indptr[gid]) ? grp_members[grp_indptr[gid]] : 0;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int M = grp_indptr[num_groups];
+    for (int base = 0; base < M; base += 1024) {
+        const int i = base + threadIdx.x;
+        int b = -1, gid = 0, n = 0;
+        int64_t q0 = 0;
+        if (i < M) {
+            b = grp_members[i];
+            int lo = 0, hi = num_groups - 1;           // group of member i
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (grp_indptr[mid] <= i) lo = mid; else hi = mid - 1;
+            }
+            gid = lo;
+            if (b >= 0 && b < batch) {
+                q0 = qo_indptr[b];
+                n = (int)(qo_indptr[b + 1] - q0);
+            } else {
+                report(status, RX_DEV_BAD_LENGTH);
+                b = -1;
+            }
+        }
+        scan[threadIdx.x] = n;
+        __syncthreads();
+        for (int off = 1; off < 1024; off <<= 1) {     // inclusive scan
+            const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
+            __syncthreads();
+            scan[threadIdx.x] += v;
+            __syncthreads();
+        }
+        const int start = carry + scan[threadIdx.x] - n;
+        if (i < M) {
+            if (b >= 0) {
+                ws.shared_of[b] = grp_len[gid];
+                for (int t = 0; t < n; ++t) ws.rows[start + t] = (int32_t)(q0 + t);
+            }
+            if (i == grp_indptr[gid]) ws.row_indptr[gid] = start;   // first member of its group
+        }
+        __syncthreads();
+        if (threadIdx.x == 1023) carry = start + n;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        ws.row_indptr[num_groups] = carry;
+        for (int gid = num_groups - 1; gid >= 0; --gid)             // empty groups: empty row range
+            if (grp_indptr[gid + 1] == grp_indptr[gid]) ws.row_indptr[gid] = ws.row_indptr[gid + 1];
+    }
+}
+
+// Private part and merge: one warp per (new row, query head) attends keys
+// [shared_of[b], P_b + i] of its own request on CUDA cores (its private cached tokens and its
+// new tokens, causally), then merges that softmax part with the group's shared chunks.
+template <int D>
+__global__ void __launch_bounds__(128) grouped_private_merge_kernel(ExtendParams p, GroupedExtendWs ws,
+                                                                    int64_t total_rows, int32_t chunk) {
+    constexpr int E = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * 4 + warp;
+    if (item >= total_rows * p.hq) return;
+    const int64_t row = item / p.hq;
+    if (row >= p.qo_indptr[p.batch]) return;
+    const int h = (int)(item - row * p.hq);
+    const int g = h / p.group;
+    int lo = 0, hi = p.batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.qo_indptr[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int64_t i = row - p.qo_indptr[b];
+    const int64_t n = p.qo_indptr[b + 1] - p.qo_indptr[b];
+    const int64_t P = p.prefix_lens[b];
+    if (n > p.max_qo_len || P < 0 || P + n > p.stride) {
+        if (lane == 0 && h == 0 && i == 0) report(p.status, RX_DEV_BAD_LENGTH);
+        return;
+    }
+    const int32_t shared = ws.shared_of[b];
+    const int64_t pos = P + i;
+    const __nv_bfloat16* qr = p.q + item * D;
+    float qv[E], acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        qv[e] = __bfloat162float(qr[lane + 32 * e]) * p.scale_log2;
+        acc[e] = 0.f;
+    }
+    const int32_t* slots = p.r2t + (int64_t)b * p.stride;
+    float m = -INFINITY, l = 0.f;
+    for (int64_t j = shared; j <= pos; ++j) {
+        const int32_t sl = slots[j];
+        if (sl < 0 || sl >= p.num_slots) {
+            if (lane == 0) report(p.status, RX_DEV_BAD_SLOT);
+            continue;
+        }
+        const __nv_bfloat16* kr = p.k_pool + ((int64_t)sl * p.hkv + g) * D;
+        const __nv_bfloat16* vr = p.v_pool + ((int64_t)sl * p.hkv + g) * D;
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dot += qv[e] * __bfloat162float(kr[lane + 32 * e]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        const float mn = fmaxf(m, dot);
+        const float corr = exp2f(m - mn), w = exp2f(dot - mn);
+        l = l * corr + w;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = acc[e] * corr + w * __bfloat162float(vr[lane + 32 * e]);
+        m = mn;
+    }
+    // merge: private part (m, l, acc unnormalised) with the shared chunks (normalised, lse)
+    const int nsh = (shared + chunk - 1) / chunk;
+    const float* pl = ws.part_lse + item * ws.per;
+    const float* po = ws.part_o + item * ws.per * D;
+    const float lse_priv = m + log2f(l);              // -inf when the range was empty
+    float M = lse_priv;
+    for (int c = 0; c < nsh; ++c) M = fmaxf(M, pl[1 + c]);
+    const float wp = (l > 0.f) ? exp2f(lse_priv - M) : 0.f;
+    float W = wp, out[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = (l > 0.f) ? wp * acc[e] / l : 0.f;
+    for (int c = 0; c < nsh; ++c) {
+        const float w = exp2f(pl[1 + c] - M);
+        W += w;
+#pragma unroll
+        for (int e = 0; e < E; ++e) out[e] += w * po[(int64_t)(1 + c) * D + lane + 32 * e];
+    }
+    __nv_bfloat16* orow = p.out + item * D;
+#pragma unroll
+    for (int e = 0; e < E; ++e) orow[lane + 32 * e] = __float2bfloat16_rn(out[e] / W);
+    if (p.lse && lane == 0) p.lse[item] = (M + log2f(W)) * EXT_LN2;
+}
+
+static int grouped_chunk(int32_t max_group_len, int64_t row_tiles_x_heads) {
+    // enough shared-part CTAs to cover the SMs, chunks of at least 128 keys
+    int chunk = max_group_len;
+    while (chunk > 128 && row_tiles_x_heads * ((max_group_len + chunk - 1) / chunk) < 152) chunk = (chunk + 1) / 2;
+    return ((chunk + EXT_BN - 1) / EXT_BN) * EXT_BN;
+}
+
+struct GroupedLayout {
+    int chunk, n_chunks, per;
+    size_t o_bytes, lse_bytes, idx_bytes, total;
+};
+
+static GroupedLayout grouped_layout(const rx_attn_desc* d, int32_t batch, int64_t total_rows,
+                                    const rx_shared_groups* grp) {
+    GroupedLayout L{};
+    const int G = d->hq / d->hkv;
+    const int64_t row_tiles = ((int64_t)grp->max_group_rows * G + 255) / 256;
+    L.chunk = grouped_chunk(grp->max_group_len, row_tiles * d->hkv);
+    L.n_chunks = (grp->max_group_len + L.chunk - 1) / L.chunk;
+    L.per = 1 + L.n_chunks;
+    L.o_bytes = (size_t)total_rows * d->hq * L.per * d->head_dim * sizeof(float);
+    L.lse_bytes = (size_t)total_rows * d->hq * L.per * sizeof(float);
+    L.idx_bytes = ((size_t)(grp->num_groups + 1) + (size_t)total_rows + (size_t)grp->num_groups + (size_t)batch) *
+                  sizeof(int32_t);
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    L.total = up(L.o_bytes) + up(L.lse_bytes) + up(L.idx_bytes);
+    return L;
+}
+
 int launch_shared_prefix_tc(const SharedTcParams& sp, cudaStream_t stream) {
     const int dc = check_device();
     if (dc != RX_OK) return dc;
@@ -499,8 +688,9 @@ int launch_shared_prefix_tc(const SharedTcParams& sp, cudaStream_t stream) {
     p.scale_log2 = sp.scale * EXT_LOG2E;
     p.status = sp.status;
     p.shared_mode = 1;
-    p.grp_indptr = sp.grp_indptr;
-    p.grp_members = sp.grp_members;
+    p.grp_row_indptr = sp.grp_row_indptr;
+    p.grp_rows = sp.grp_rows;
+    p.grp_src = sp.grp_src;
     p.grp_len = sp.grp_len;
     p.chunk = sp.chunk;
     p.n_chunks = sp.n_chunks;
@@ -508,7 +698,7 @@ int launch_shared_prefix_tc(const SharedTcParams& sp, cudaStream_t stream) {
     p.part_lse = sp.part_lse;
     p.part_per = sp.part_per;
     p.part_base = sp.part_base;
-    const int64_t row_tiles = ((int64_t)sp.max_group_size * p.group + 255) / 256;
+    const int64_t row_tiles = ((int64_t)sp.max_group_rows * p.group + 255) / 256;
     const int64_t gx = row_tiles * sp.n_chunks;
     if (gx >= (1ll << 31) || sp.num_groups >= 65536) {
         set_error("decode_attention: shared-prefix grid too large");
@@ -529,10 +719,82 @@ int launch_shared_prefix_tc(const SharedTcParams& sp, cudaStream_t stream) {
 
 using namespace rx;
 
+extern "C" size_t extend_workspace_bytes(const rx_attn_desc* desc, int32_t batch, int32_t max_qo_len,
+                                         const rx_shared_groups* groups) {
+    if (!desc || batch < 0 || max_qo_len < 0 || desc->hkv <= 0 || desc->hq % desc->hkv != 0) return 0;
+    if (!groups || groups->num_groups <= 0) return 0;
+    return grouped_layout(desc, batch, (int64_t)batch * max_qo_len, groups).total;
+}
+
+static int grouped_extend(const rx_attn_desc* desc, const ExtendParams& p, const rx_shared_groups* groups,
+                          void* d_workspace, size_t ws_bytes, cudaStream_t stream) {
+    RX_REQUIRE(groups->d_group_indptr && groups->d_group_members && groups->d_group_len &&
+                   groups->max_group_rows >= 1 && groups->max_group_len >= 1,
+               "prefix_extend_attention: incomplete shared groups");
+    const int64_t rows_bound = (int64_t)p.batch * p.max_qo_len;
+    const GroupedLayout L = grouped_layout(desc, p.batch, rows_bound, groups);
+    RX_REQUIRE(d_workspace && ws_bytes >= L.total && ((uintptr_t)d_workspace & 255) == 0,
+               "prefix_extend_attention: grouped path needs a 256-byte aligned workspace of %zu bytes (got %zu)",
+               L.total, ws_bytes);
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    unsigned char* w = (unsigned char*)d_workspace;
+    GroupedExtendWs ws{};
+    ws.part_o = (float*)w;
+    ws.part_lse = (float*)(w + up(L.o_bytes));
+    int32_t* idx = (int32_t*)(w + up(L.o_bytes) + up(L.lse_bytes));
+    ws.row_indptr = idx;
+    ws.rows = idx + groups->num_groups + 1;
+    ws.src = ws.rows + rows_bound;
+    ws.shared_of = ws.src + groups->num_groups;
+    ws.per = L.per;
+    grouped_prep_kernel<<<1, 1024, 0, stream>>>(p.batch, p.qo_indptr, groups->num_groups, groups->d_group_indptr,
+                                                 groups->d_group_members, groups->d_group_len, ws, p.status);
+    SharedTcParams sp{};
+    sp.q = p.q;
+    sp.r2t = p.r2t;
+    sp.stride = p.stride;
+    sp.k_pool = p.k_pool;
+    sp.v_pool = p.v_pool;
+    sp.num_slots = p.num_slots;
+    sp.batch = p.batch;
+    sp.hq = p.hq;
+    sp.hkv = p.hkv;
+    sp.head_dim = desc->head_dim;
+    sp.scale = desc->scale;
+    sp.status = p.status;
+    sp.num_groups = groups->num_groups;
+    sp.max_group_rows = groups->max_group_rows;
+    sp.grp_row_indptr = ws.row_indptr;
+    sp.grp_rows = ws.rows;
+    sp.grp_src = ws.src;
+    sp.grp_len = groups->d_group_len;
+    sp.chunk = L.chunk;
+    sp.n_chunks = L.n_chunks;
+    sp.part_o = ws.part_o;
+    sp.part_lse = ws.part_lse;
+    sp.part_per = L.per;
+    sp.part_base = 1;
+    int rc = launch_shared_prefix_tc(sp, stream);
+    if (rc != RX_OK) return rc;
+    const int64_t items = rows_bound * p.hq;
+    const unsigned blocks = (unsigned)((items + 3) / 4);
+    if (desc->head_dim == 128)
+        grouped_private_merge_kernel<128><<<blocks, 128, 0, stream>>>(p, ws, rows_bound, L.chunk);
+    else
+        grouped_private_merge_kernel<64><<<blocks, 128, 0, stream>>>(p, ws, rows_bound, L.chunk);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("prefix_extend_attention: grouped launch failed: %s", cudaGetErrorString(e));
+        return RX_ECUDA;
+    }
+    return RX_OK;
+}
+
 extern "C" int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch, const void* d_q,
                                        const int64_t* d_qo_indptr, const int32_t* d_prefix_lens,
                                        const int32_t* d_req_to_token, int64_t r2t_stride, const void* d_k_pool,
                                        const void* d_v_pool, void* d_out, float* d_lse, int32_t max_qo_len,
+                                       const rx_shared_groups* groups, void* d_workspace, size_t ws_bytes,
                                        int32_t* d_status, void* stream_) {
     RX_REQUIRE(desc && batch >= 0 && max_qo_len >= 0 && r2t_stride >= 0, "prefix_extend_attention: bad arguments");
     RX_REQUIRE(desc->hq > 0 && desc->hkv > 0 && desc->hq % desc->hkv == 0,
@@ -588,6 +850,7 @@ extern "C" int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch, 
     p.scale_log2 = desc->scale * EXT_LOG2E;
     p.max_qo_len = max_qo_len;
     p.status = d_status;
+    if (groups && groups->num_groups > 0) return grouped_extend(desc, p, groups, d_workspace, ws_bytes, stream);
     const int64_t tiles = ((int64_t)max_qo_len * group + 255) / 256;
     RX_REQUIRE(tiles < 65536 && batch < 65536, "prefix_extend_attention: grid too large");
     const int rc = desc->head_dim == 128 ? launch_extend_tc<128>(p, (int)tiles, stream, batch)

@@ -445,6 +445,161 @@ int insert_batch_at(rx_radix* t, int32_t batch, const rx_node* nodes, const int3
     return RX_OK;
 }
 
+static inline int64_t up256(int64_t x) { return (x + 255) & ~(int64_t)255; }
+
+size_t rx_step_stage_bytes(int32_t batch, int64_t total_tokens) {
+    if (batch < 0 || total_tokens < 0) return 0;
+    const int64_t b1 = (int64_t)batch + 1;
+    return (size_t)(up256(4 * total_tokens) + up256(8 * b1) + up256(4 * total_tokens) + up256(8 * b1) +
+                    up256(4 * (int64_t)batch) + up256(4 * (int64_t)batch) + up256(4 * b1) + up256(4 * (int64_t)batch) +
+                    up256(4 * (int64_t)batch) + 256);
+}
+
+int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr, const int32_t* n_new,
+                 int32_t group_mode, int32_t heads_per_kv, int64_t min_shared, void* h_stage, size_t stage_cap,
+                 rx_node* out_last, rx_step_layout* out) {
+    RX_REQUIRE(t && batch >= 0 && tok_indptr && out && h_stage && (batch == 0 || (tokens && n_new && out_last)),
+               "rx_step_plan: bad arguments");
+    const int64_t total_tokens = tok_indptr[batch];
+    RX_REQUIRE(stage_cap >= rx_step_stage_bytes(batch, total_tokens), "rx_step_plan: staging buffer of %zu bytes, %zu needed",
+               stage_cap, rx_step_stage_bytes(batch, total_tokens));
+    unsigned char* st = (unsigned char*)h_stage;
+    rx_step_layout L{};
+    L.batch = batch;
+    // a1: matched slots straight into the staging buffer
+    L.off_prefix_slots = 0;
+    int32_t* ps = (int32_t*)(st + L.off_prefix_slots);
+    std::vector<int64_t> P((size_t)batch);
+    int64_t acc = 0, T = 0;
+    int32_t max_qo = 0, max_kv = 1;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t len = tok_indptr[b + 1] - tok_indptr[b];
+        RX_REQUIRE(len >= 0 && n_new[b] >= 0 && n_new[b] <= len, "rx_step_plan: request %d: %lld tokens, %d new", b,
+                   (long long)len, n_new[b]);
+        t->clock += 1;
+        rx::Node* last = nullptr;
+        const int64_t m = t->walk(tokens + tok_indptr[b], len, ps + acc, &last);
+        t->st.match_calls += 1;
+        t->st.match_query_tokens += len;
+        t->st.match_hit_tokens += m;
+        out_last[b] = last->id;
+        RX_REQUIRE(m + n_new[b] == len, "rx_step_plan: request %d: %lld tokens cached, %lld expected", b, (long long)m,
+                   (long long)(len - n_new[b]));
+        P[(size_t)b] = m;
+        acc += m;
+        T += n_new[b];
+        max_qo = std::max(max_qo, n_new[b]);
+        max_kv = std::max<int32_t>(max_kv, (int32_t)len);
+    }
+    L.total_prefix = acc;
+    L.total_new = T;
+    L.max_qo_len = max_qo;
+    L.max_kv_len = max_kv;
+    L.stride = (max_kv + 7) / 8 * 8;
+    L.off_prefix_indptr = up256(4 * acc);
+    L.off_new_slots = L.off_prefix_indptr + up256(8 * ((int64_t)batch + 1));
+    L.off_qo_indptr = L.off_new_slots + up256(4 * T);
+    L.off_prefix_lens = L.off_qo_indptr + up256(8 * ((int64_t)batch + 1));
+    L.off_kv_lens = L.off_prefix_lens + up256(4 * (int64_t)batch);
+    L.off_grp_indptr = L.off_kv_lens + up256(4 * (int64_t)batch);
+    L.off_grp_members = L.off_grp_indptr + up256(4 * ((int64_t)batch + 1));
+    L.off_grp_len = L.off_grp_members + up256(4 * (int64_t)batch);
+    L.bytes = L.off_kv_lens + up256(4 * (int64_t)batch);
+    // a2: allocate the new tokens' slots
+    int32_t* ns = (int32_t*)(st + L.off_new_slots);
+    {
+        const int rc = alloc_slots(t, T, ns);
+        if (rc != RX_OK) return rc;
+    }
+    int64_t* pind = (int64_t*)(st + L.off_prefix_indptr);
+    int64_t* qo = (int64_t*)(st + L.off_qo_indptr);
+    int32_t* pl = (int32_t*)(st + L.off_prefix_lens);
+    int32_t* kl = (int32_t*)(st + L.off_kv_lens);
+    pind[0] = 0;
+    qo[0] = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        pind[b + 1] = pind[b] + P[(size_t)b];
+        qo[b + 1] = qo[b] + n_new[b];
+        pl[b] = (int32_t)P[(size_t)b];
+        kl[b] = (int32_t)(P[(size_t)b] + n_new[b]);
+    }
+    // pin the matched prefixes for the step
+    for (int32_t b = 0; b < batch; ++b)
+        for (rx::Node* x = t->by_id[out_last[b]]; x != &t->root; x = x->parent) x->ref += 1;
+    // optional shared-prefix groups
+    if (group_mode != RX_GROUPS_NONE && batch > 0) {
+        std::vector<int32_t> gof((size_t)batch);
+        std::vector<int64_t> glen((size_t)batch);
+        int32_t ng = 0;
+        int rc = radix_shared_groups(t, out_last, batch, min_shared, gof.data(), glen.data(), &ng);
+        if (rc != RX_OK) return rc;
+        bool use = ng > 0;
+        if (use && group_mode == RX_GROUPS_AUTO) {
+            for (int32_t b = 0; b < batch && use; ++b) {
+                if (gof[(size_t)b] < 0) use = false;
+                else if (P[(size_t)b] + n_new[b] - glen[(size_t)gof[(size_t)b]] > 256) use = false;
+                else if ((int64_t)n_new[b] * heads_per_kv >= 128) use = false;
+            }
+        }
+        if (use) {
+            int32_t* gi = (int32_t*)(st + L.off_grp_indptr);
+            int32_t* gm = (int32_t*)(st + L.off_grp_members);
+            int32_t* gl = (int32_t*)(st + L.off_grp_len);
+            std::vector<int32_t> cnt((size_t)ng, 0);
+            std::vector<int64_t> rows((size_t)ng, 0);
+            for (int32_t b = 0; b < batch; ++b)
+                if (gof[(size_t)b] >= 0) {
+                    cnt[(size_t)gof[(size_t)b]] += 1;
+                    rows[(size_t)gof[(size_t)b]] += n_new[b];
+                }
+            gi[0] = 0;
+            for (int32_t g = 0; g < ng; ++g) gi[g + 1] = gi[g] + cnt[(size_t)g];
+            std::vector<int32_t> fill(gi, gi + ng);
+            for (int32_t b = 0; b < batch; ++b)
+                if (gof[(size_t)b] >= 0) gm[fill[(size_t)gof[(size_t)b]]++] = b;
+            for (int32_t g = 0; g < ng; ++g) {
+                gl[g] = (int32_t)glen[(size_t)g];
+                L.max_group_size = std::max(L.max_group_size, cnt[(size_t)g]);
+                L.max_group_len = std::max(L.max_group_len, gl[g]);
+                L.max_group_rows = std::max<int32_t>(L.max_group_rows, (int32_t)rows[(size_t)g]);
+            }
+            L.num_groups = ng;
+            L.bytes = L.off_grp_len + up256(4 * (int64_t)ng);
+        }
+    }
+    *out = L;
+    return RX_OK;
+}
+
+int rx_step_finish(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
+                   const rx_node* last_nodes, const void* h_stage, const rx_step_layout* L, int64_t evict_tokens,
+                   int64_t* out_evicted) {
+    RX_REQUIRE(t && L && h_stage && batch == L->batch && (batch == 0 || (tokens && tok_indptr && last_nodes)),
+               "rx_step_finish: bad arguments");
+    const unsigned char* st = (const unsigned char*)h_stage;
+    const int32_t* ns = (const int32_t*)(st + L->off_new_slots);
+    const int64_t* qo = (const int64_t*)(st + L->off_qo_indptr);
+    const int32_t* pl = (const int32_t*)(st + L->off_prefix_lens);
+    std::vector<int64_t> dup((size_t)std::max(batch, 1));
+    std::vector<rx_node> last((size_t)std::max(batch, 1));
+    int rc = insert_batch_at(t, batch, last_nodes, tokens, tok_indptr, ns, qo, dup.data(), last.data());
+    if (rc != RX_OK) return rc;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t over = dup[(size_t)b] - pl[b];   // new slots whose tokens were cached meanwhile
+        if (over > 0) {
+            rc = free_slots(t, ns + qo[b], over);
+            if (rc != RX_OK) return rc;
+        }
+    }
+    int64_t freed = 0;
+    if (evict_tokens > 0) {
+        rc = evict(t, evict_tokens, nullptr, 0, &freed);
+        if (rc != RX_OK) return rc;
+    }
+    if (out_evicted) *out_evicted = freed;
+    return radix_unlock_batch(t, last_nodes, batch);
+}
+
 int radix_stats(const rx_radix* t, rx_stats* out) {
     RX_REQUIRE(t && out, "radix_stats: bad arguments");
     *out = t->st;

@@ -28,9 +28,9 @@ struct SimtParams {
 
 int launch_attn_simt(const SimtParams& p, int dtype, int head_dim, cudaStream_t stream);
 
-// Shared-prefix part of decode on the tcgen05 kernel: for every group, the members' query
-// rows (stacked) attend one chunk of the group's shared keys; fp32 normalised partials and
-// log2-domain lse go to part_o/part_lse at partial index part_base + chunk.
+// Shared-prefix part on the tcgen05 kernel: for every group, its query rows (stacked) attend
+// one chunk of the group's shared keys (slot-table row grp_src[g]); fp32 normalised partials
+// and log2-domain lse go to part_o/part_lse at partial index part_base + chunk.
 struct SharedTcParams {
     const void* q;                // [batch, hq, D] bf16
     const int32_t* r2t;
@@ -41,9 +41,10 @@ struct SharedTcParams {
     int32_t batch, hq, hkv, head_dim;
     float scale;
     int32_t* status;
-    int32_t num_groups, max_group_size;
-    const int32_t* grp_indptr;
-    const int32_t* grp_members;
+    int32_t num_groups, max_group_rows;
+    const int32_t* grp_row_indptr;   // [num_groups+1] into grp_rows
+    const int32_t* grp_rows;         // global query-row ids (decode: request ids)
+    const int32_t* grp_src;          // [num_groups] slot-table row holding the shared slots
     const int32_t* grp_len;
     int32_t chunk, n_chunks;
     float* part_o;

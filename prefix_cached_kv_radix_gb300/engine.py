@@ -44,9 +44,10 @@ class StepPlan:
     max_qo_len: int
     max_kv_len: int
     stride: int
-    grp_indptr: np.ndarray = None   # decode shared-prefix groups (optional)
+    grp_indptr: np.ndarray = None   # shared-prefix groups (optional)
     grp_members: np.ndarray = None
     grp_len: np.ndarray = None
+    grp_rows: int = 0               # largest sum of new tokens over a group's members
 
 
 class PrefixCacheEngine:
@@ -68,11 +69,14 @@ class PrefixCacheEngine:
                                   1.0 / float(np.sqrt(head_dim)))
         self._ws = None
         # step index arrays travel in one pinned buffer (two, alternating) and one H2D copy
-        self._pin = [None, None]
-        self._pin_ev = [None, None]
+        self._pin = [None, None]        # pinned host staging (torch tensor, numpy view)
+        self._pin_np = [None, None]
+        self._pin_ev = [torch.cuda.Event(), torch.cuda.Event()]
+        self._pin_used = [False, False]
         self._pin_i = 0
         self._dev_idx = None
         self._r2t = None
+        self._stream = torch.cuda.current_stream(self.device)
 
     # ------------------------------------------------------------------ helpers
     def _i32(self, a):
@@ -139,6 +143,13 @@ class PrefixCacheEngine:
         if groups and b:
             # requests whose cached paths share a node: their shared run is read once per group
             gof, glen = self.tree.shared_groups(last, min_shared)
+            if len(glen) and groups == "auto":
+                # extend: stack rows only when each request's remaining keys are few (they run
+                # on CUDA cores) and the stacked rows beat the per-request 128-row tiles
+                shared = np.where(gof >= 0, glen[np.maximum(gof, 0)], 0)
+                private = P + n_new - shared
+                if (gof < 0).any() or private.max() > 256 or n_new.max() * (self.hq // self.hkv) >= 128:
+                    glen = glen[:0]
             if len(glen):
                 order = np.argsort(gof, kind="stable")
                 order = order[gof[order] >= 0]
@@ -146,6 +157,7 @@ class PrefixCacheEngine:
                 plan.grp_members = order.astype(np.int32)
                 plan.grp_indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
                 plan.grp_len = glen.astype(np.int32)
+                plan.grp_rows = int(np.bincount(gof[order], weights=n_new[order], minlength=len(glen)).max())
         return plan
 
     def upload(self, plan: StepPlan, stream=None) -> dict:
@@ -169,39 +181,48 @@ class PrefixCacheEngine:
         self._pin_i ^= 1
         if self._pin[i] is None or self._pin[i].numel() < total:
             self._pin[i] = torch.empty(max(total, 4096) * 2, dtype=torch.uint8).pin_memory()
-            self._pin_ev[i] = None
+            self._pin_np[i] = self._pin[i].numpy()
+            self._pin_used[i] = False
         if self._dev_idx is None or self._dev_idx.numel() < total:
             self._dev_idx = torch.empty(max(total, 4096) * 2, dtype=torch.uint8, device=self.device)
-        if self._pin_ev[i] is not None:
+        if self._pin_used[i]:
             self._pin_ev[i].synchronize()          # the copy that last read this buffer is done
-        host = self._pin[i].numpy()
+        host = self._pin_np[i]
         for (name, a, dt), o in zip(parts, offs):
             host[o:o + len(a) * np.dtype(dt).itemsize] = np.ascontiguousarray(a, dt).view(np.uint8)
-        st = torch.cuda.current_stream(self.device) if stream is None else stream
+        st = self._stream if stream is None else stream
         with torch.cuda.stream(st):
             self._dev_idx[:total].copy_(self._pin[i][:total], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(st)
-        self._pin_ev[i] = ev
-        out = {}
-        for (name, a, dt), o in zip(parts, offs):
-            nb = len(a) * np.dtype(dt).itemsize
-            out[name] = self._dev_idx[o:o + nb].view(torch.int32 if dt == np.int32 else torch.int64)
-        if self._r2t is None or self._r2t.numel() < max(B, 1) * plan.stride:
-            self._r2t = torch.empty(max(B, 1) * plan.stride * 2, dtype=torch.int32, device=self.device)
-        out["r2t"] = self._r2t[:max(B, 1) * plan.stride].view(max(B, 1), plan.stride)
+        self._pin_ev[i].record(st)
+        self._pin_used[i] = True
+        base = self._dev_idx.data_ptr()
+        out = {name: base + o for (name, a, dt), o in zip(parts, offs)}   # device addresses
+        if self._r2t is None or self._r2t.shape[1] != plan.stride or self._r2t.shape[0] < max(B, 1):
+            self._r2t = torch.empty(max(B, 1) * 2, plan.stride, dtype=torch.int32, device=self.device)
+        out["r2t"] = self._r2t
+        out["batch"] = B
+        out["stride"] = plan.stride
         return out
 
     def write(self, plan: StepPlan, dev: dict, k_new, v_new, stream=None) -> None:
         """a3: slot table + scatter of the new tokens' K/V."""
         api.kv_pool_write(self.desc, plan.batch, dev["prefix_slots"], dev["prefix_indptr"], dev["new_slots"],
                           dev["qo_indptr"], k_new, v_new, self.k_pool, self.v_pool, dev["r2t"],
-                          int(plan.qo_indptr[-1]), self.status, stream)
+                          int(plan.qo_indptr[-1]), self.status, stream or self._stream.cuda_stream)
 
     def extend(self, plan: StepPlan, dev: dict, q, out, lse=None, stream=None) -> None:
-        """a4: new tokens attend to their cached prefix and causally to themselves."""
+        """a4: new tokens attend to their cached prefix and causally to themselves (with the
+        plan's shared-prefix groups, if any: shared run once per group, stacked rows)."""
+        grp = self.groups(plan, dev)
+        ws = None
+        if grp is not None:
+            nbytes = api.extend_workspace_bytes(self.desc, plan.batch, plan.max_qo_len, grp)
+            if self._ws is None or self._ws.numel() < nbytes:
+                self._ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            ws = self._ws
         api.prefix_extend_attention(self.desc, plan.batch, q, dev["qo_indptr"], dev["prefix_lens"], dev["r2t"],
-                                    self.k_pool, self.v_pool, out, lse, plan.max_qo_len, self.status, stream)
+                                    self.k_pool, self.v_pool, out, lse, plan.max_qo_len, self.status,
+                                    groups=grp, workspace=ws, stream=stream or self._stream.cuda_stream)
 
     def groups(self, plan: StepPlan, dev: dict):
         """The plan's shared-prefix groups (computed by plan(..., groups=True) and uploaded with
@@ -209,7 +230,7 @@ class PrefixCacheEngine:
         if plan.grp_len is None:
             return None
         return api.shared_groups_struct(len(plan.grp_len), int(np.diff(plan.grp_indptr).max()), dev["grp_indptr"],
-                                        dev["grp_members"], dev["grp_len"], int(plan.grp_len.max()))
+                                        dev["grp_members"], dev["grp_len"], int(plan.grp_len.max()), plan.grp_rows)
 
     def decode_workspace(self, plan: StepPlan, groups=None):
         nbytes = api.decode_workspace_bytes(self.desc, plan.batch, plan.max_kv_len, groups)
@@ -221,7 +242,8 @@ class PrefixCacheEngine:
         """a5 + a6: one query token per request over all of its cached tokens."""
         ws = self.decode_workspace(plan, groups)
         api.decode_attention(self.desc, plan.batch, q, dev["r2t"], dev["kv_lens"], self.k_pool, self.v_pool, out,
-                             lse, plan.max_kv_len, ws, self.status, groups=groups, stream=stream)
+                             lse, plan.max_kv_len, ws, self.status, groups=groups,
+                             stream=stream or self._stream.cuda_stream)
 
     def commit(self, plan: StepPlan) -> np.ndarray:
         """a7: insert every prompt, continuing from the node its match ended at; frees new
@@ -238,9 +260,10 @@ class PrefixCacheEngine:
         """a8: evict least-recently-used unlocked leaves until num_tokens are freed."""
         return self.tree.evict(num_tokens)
 
-    def finish(self, plan: StepPlan, evict_tokens: int = 0) -> np.ndarray:
-        """End of a step: a7 insert, a8 evict (the step's prefixes still pinned), unpin."""
+    def finish(self, plan: StepPlan, evict_tokens: int = 0) -> int:
+        """End of a step: a7 insert, a8 evict (the step's prefixes still pinned), unpin.
+        Returns the number of slots evicted."""
         self.commit(plan)
-        freed = self.release(evict_tokens) if evict_tokens else np.zeros(0, np.int32)
+        freed = self.tree.evict_count(evict_tokens) if evict_tokens else 0
         self.tree.unlock_batch(plan.last_nodes)
         return freed

@@ -50,7 +50,7 @@ def run_step(w, engine=None, groups=False, lse=True, poison=True):
     for i in range(len(s.histories)):
         k, v = w.history_kv(i)
         eng.populate(w.history_tokens(i), k, v)
-    plan = eng.plan([w.request_tokens(b) for b in range(w.batch)], s.req_new, groups=groups and s.decode)
+    plan = eng.plan([w.request_tokens(b) for b in range(w.batch)], s.req_new, groups=groups)
     dev = eng.upload(plan)
     q, kn, vn = w.stacked_new()
     qd, kd, vd = (_dev_from_host(x, s.dtype, eng.device) for x in (q, kn, vn))
@@ -62,6 +62,7 @@ def run_step(w, engine=None, groups=False, lse=True, poison=True):
         grp = eng.groups(plan, dev) if groups else None
         eng.decode(plan, dev, qd, out, lse_t, groups=grp)
     else:
+        grp = eng.groups(plan, dev)
         eng.extend(plan, dev, qd, out, lse_t)
     torch.cuda.synchronize()
     return eng, plan, dev, out, lse_t, grp

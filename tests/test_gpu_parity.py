@@ -234,3 +234,49 @@ def test_step_then_evict_restores_cache():
     # the same step again sees the same hits (the prefix stayed cached)
     plan2 = eng.plan([w.request_tokens(b) for b in range(w.batch)], spec.req_new)
     assert np.array_equal(plan2.prefix_lens, plan.prefix_lens)
+
+
+# ---------------------------------------------------------------- grouped extend (shared prefix stacked)
+def run_grouped(spec, groups="auto", expect_grouped=True):
+    w = W.generate(spec)
+    eng, plan, dev, out, lse, grp = run_step(w, groups=groups)
+    assert eng.device_status() == 0
+    assert (grp is not None) == expect_grouped
+    check_tables(w, eng, plan, dev)
+    check_attention(w, out, lse)
+    return w, out, lse
+
+
+def test_grouped_extend_c2():
+    run_grouped(W.config("c2"))
+
+
+def test_grouped_extend_private_cached_tails():
+    # a shared 300-token root, 6 children of 40 tokens, 3 requests per child with 5 new tokens:
+    # the group shares the root; each request's child tokens and own tokens are private
+    spec = W.spec_branching("grp-tails", "bf16", 12, 12, 64, 1 << 14, W.GPT2_VOCAB, 41, root=300, n_children=6,
+                            child_len=40, leaves_per_child=3, n_new=5)
+    run_grouped(spec)
+
+
+def test_grouped_extend_gqa_d128():
+    spec = W.spec_shared_prompt("grp-gqa", "bf16", 32, 8, 128, 1 << 14, W.QWEN_VOCAB, 42, 700, [3, 9, 1, 16, 7, 12])
+    run_grouped(spec)
+
+
+def test_grouped_extend_forced_with_ungrouped_requests():
+    # two roots: requests under root A form a group, the single request on root B does not
+    spec = W.Spec("grp-mixed", "bf16", 8, 2, 128, 1 << 13, W.QWEN_VOCAB, 43, seg_parent=[-1, -1],
+                  seg_len=[260, 90], histories=[0, 1], req_seg=[0, 0, 0, 1], req_cached=[260, 260, 130, 90],
+                  req_new=[4, 6, 3, 5])
+    run_grouped(spec, groups=True)
+
+
+def test_grouped_equals_ungrouped_extend():
+    spec = W.config("c2")
+    w = W.generate(spec)
+    _, _, _, o1, l1, g1 = run_step(w, groups=False)
+    _, _, _, o2, l2, g2 = run_step(w, groups="auto")
+    assert g1 is None and g2 is not None
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1 - l2).abs().max().item() <= 1e-3

@@ -225,6 +225,47 @@ class PrefixCacheModel:
         return all(len({self.entries[x][1] for x in node}) == 1 for node in self.nodes())
 
 
+# --------------------------------------------------------------------------- shared groups
+def shared_groups(matched, min_shared: int = 1):
+    """Requests whose cached prefixes share their first node, and how long the common part is.
+
+    matched: each request's matched (cached) token prefix.  Requests with a non-empty match
+    are grouped by its first token (the root's child they go through), groups in order of
+    first appearance; a group of two or more whose members' longest common prefix is at
+    least min_shared keeps that length, the others are dropped (-1).  This is the reading
+    behind reading a shared prefix once per group (the "SGLang" page's shared-prefix reuse
+    across requests): the common prefix of cached paths ends at a node boundary, since a
+    divergence point is always cut."""
+    first, order = {}, []
+    for b, p in enumerate(matched):
+        if len(p) == 0:
+            continue
+        key = int(p[0])
+        if key not in first:
+            first[key] = []
+            order.append(key)
+        first[key].append(b)
+    group_of, lens = [-1] * len(matched), []
+    for key in order:
+        mem = first[key]
+        if len(mem) < 2:
+            continue
+        a = [int(t) for t in matched[mem[0]]]
+        lcp = len(a)
+        for b in mem[1:]:
+            o = [int(t) for t in matched[b]]
+            n = 0
+            while n < min(lcp, len(o)) and o[n] == a[n]:
+                n += 1
+            lcp = n
+        if lcp < min_shared:
+            continue
+        for b in mem:
+            group_of[b] = len(lens)
+        lens.append(lcp)
+    return np.array(group_of, np.int32), np.array(lens, np.int64)
+
+
 # --------------------------------------------------------------------------- slot table
 def req_to_token(prefix_slots, new_slots, stride: int) -> np.ndarray:
     """Row b = matched prefix slots of request b, then its new slots, padded with -1."""

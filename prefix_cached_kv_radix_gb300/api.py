@@ -23,7 +23,7 @@ RX_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20   # include/radix_attn.h
 EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "radix_lock", "radix_unlock", "alloc_slots",
            "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "insert_batch_at", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
-           "radix_shared_groups",
+           "radix_shared_groups", "rx_step_stage_bytes", "rx_step_plan", "rx_step_finish",
            "kv_pool_write", "prefix_extend_attention", "extend_workspace_bytes", "decode_workspace_bytes",
            "decode_attention",
            "decode_attention_noalloc",
@@ -53,6 +53,20 @@ class rx_shared_groups(ctypes.Structure):
                 ("d_group_len", ctypes.c_void_p), ("max_group_len", ctypes.c_int32),
                 ("max_group_rows", ctypes.c_int32)]
 
+
+class rx_step_layout(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("max_qo_len", ctypes.c_int32), ("max_kv_len", ctypes.c_int32),
+                ("stride", ctypes.c_int32), ("total_new", ctypes.c_int64), ("total_prefix", ctypes.c_int64),
+                ("bytes", ctypes.c_int64), ("off_prefix_slots", ctypes.c_int64), ("off_prefix_indptr", ctypes.c_int64),
+                ("off_new_slots", ctypes.c_int64), ("off_qo_indptr", ctypes.c_int64),
+                ("off_prefix_lens", ctypes.c_int64), ("off_kv_lens", ctypes.c_int64),
+                ("num_groups", ctypes.c_int32), ("max_group_size", ctypes.c_int32),
+                ("max_group_len", ctypes.c_int32), ("max_group_rows", ctypes.c_int32),
+                ("off_grp_indptr", ctypes.c_int64), ("off_grp_members", ctypes.c_int64),
+                ("off_grp_len", ctypes.c_int64)]
+
+
+RX_GROUPS_NONE, RX_GROUPS_ALWAYS, RX_GROUPS_AUTO = 0, 1, 2
 
 _lib = None
 P = ctypes.c_void_p
@@ -86,6 +100,9 @@ def load(path: str = LIB_PATH):
         "radix_stats": (ctypes.c_int, [P, P]),
         "radix_check": (ctypes.c_int, [P]),
         "radix_shared_groups": (ctypes.c_int, [P, P, I32, I64, P, P, P]),
+        "rx_step_stage_bytes": (SZ, [I32, I64]),
+        "rx_step_plan": (ctypes.c_int, [P, I32, P, P, P, I32, I32, I64, P, SZ, P, P]),
+        "rx_step_finish": (ctypes.c_int, [P, I32, P, P, P, P, P, I64, P]),
         "kv_pool_write": (ctypes.c_int, [P, I32, P, P, P, P, P, P, P, P, P, I64, I64, P, P]),
         "prefix_extend_attention": (ctypes.c_int, [P, I32, P, P, P, P, I64, P, P, P, P, I32, P, P, SZ, P, P]),
         "extend_workspace_bytes": (SZ, [P, I32, I32, P]),
@@ -279,6 +296,35 @@ def radix_shared_groups(tree, last_nodes, min_shared: int = 1):
     _check("radix_shared_groups", load().radix_shared_groups(tree, ln.ctypes.data, b, min_shared, gof.ctypes.data,
                                                              glen.ctypes.data, ctypes.byref(ng)))
     return gof[:b].copy(), glen[: ng.value].copy()
+
+
+def rx_step_stage_bytes(batch: int, total_tokens: int) -> int:
+    return int(load().rx_step_stage_bytes(batch, total_tokens))
+
+
+def rx_step_plan(tree, tokens: np.ndarray, tok_indptr: np.ndarray, n_new: np.ndarray, group_mode: int,
+                 heads_per_kv: int, min_shared: int, stage_addr: int, stage_cap: int, out_last: np.ndarray):
+    """tokens int32, tok_indptr int64 [batch+1], n_new int32 [batch], out_last int64 [batch]
+    (filled): all contiguous.  stage_addr: host address of the staging buffer.  Returns the
+    rx_step_layout."""
+    b = len(tok_indptr) - 1
+    lay = rx_step_layout()
+    _check("rx_step_plan", load().rx_step_plan(
+        tree, b, tokens.ctypes.data, tok_indptr.ctypes.data, n_new.ctypes.data if b else None,
+        group_mode, heads_per_kv, min_shared, stage_addr, stage_cap, out_last.ctypes.data if b else None,
+        ctypes.byref(lay)))
+    return lay
+
+
+def rx_step_finish(tree, tokens: np.ndarray, tok_indptr: np.ndarray, last_nodes: np.ndarray, stage_addr: int,
+                   layout, evict_tokens: int) -> int:
+    """Returns the number of slots evicted."""
+    n = I64()
+    _check("rx_step_finish", load().rx_step_finish(
+        tree, layout.batch, tokens.ctypes.data, tok_indptr.ctypes.data,
+        last_nodes.ctypes.data if layout.batch else None, stage_addr, ctypes.byref(layout), evict_tokens,
+        ctypes.byref(n)))
+    return n.value
 
 
 class RadixTree:

@@ -523,16 +523,16 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
         pl[b] = (int32_t)P[(size_t)b];
         kl[b] = (int32_t)(P[(size_t)b] + n_new[b]);
     }
-    // pin the matched prefixes for the step
-    for (int32_t b = 0; b < batch; ++b)
-        for (rx::Node* x = t->by_id[out_last[b]]; x != &t->root; x = x->parent) x->ref += 1;
     // optional shared-prefix groups
     if (group_mode != RX_GROUPS_NONE && batch > 0) {
         std::vector<int32_t> gof((size_t)batch);
         std::vector<int64_t> glen((size_t)batch);
         int32_t ng = 0;
         int rc = radix_shared_groups(t, out_last, batch, min_shared, gof.data(), glen.data(), &ng);
-        if (rc != RX_OK) return rc;
+        if (rc != RX_OK) {
+            free_slots(t, ns, T);
+            return rc;
+        }
         bool use = ng > 0;
         if (use && group_mode == RX_GROUPS_AUTO) {
             for (int32_t b = 0; b < batch && use; ++b) {
@@ -567,6 +567,9 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
             L.bytes = L.off_grp_len + up256(4 * (int64_t)ng);
         }
     }
+    // pin the matched prefixes for the step (last, so that a failure above leaves none pinned)
+    for (int32_t b = 0; b < batch; ++b)
+        for (rx::Node* x = t->by_id[out_last[b]]; x != &t->root; x = x->parent) x->ref += 1;
     *out = L;
     return RX_OK;
 }

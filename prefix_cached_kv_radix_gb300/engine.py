@@ -32,6 +32,9 @@ def _dev_from_host(a, dtype_bits, device):
 
 @dataclass
 class StepPlan:
+    """One planned step.  The index arrays are views of the pinned staging buffer the step's
+    device copy is made from (two buffers alternate: a plan stays valid until the plan after
+    next)."""
     batch: int
     tokens: np.ndarray          # concatenated full prompts (cached part + new tokens)
     tok_indptr: np.ndarray      # [batch+1]
@@ -40,7 +43,7 @@ class StepPlan:
     prefix_lens: np.ndarray     # [batch] int32 (P_b)
     new_slots: np.ndarray       # [T]
     qo_indptr: np.ndarray       # [batch+1]
-    last_nodes: np.ndarray      # [batch] node where each match ended
+    last_nodes: np.ndarray      # [batch] node where each match ended (pinned until finish)
     max_qo_len: int
     max_kv_len: int
     stride: int
@@ -48,6 +51,12 @@ class StepPlan:
     grp_members: np.ndarray = None
     grp_len: np.ndarray = None
     grp_rows: int = 0               # largest sum of new tokens over a group's members
+    layout: object = None           # rx_step_layout of the staging buffer
+    stage: int = -1                 # which staging buffer
+
+
+_GROUP_MODE = {False: api.RX_GROUPS_NONE, None: api.RX_GROUPS_NONE, True: api.RX_GROUPS_ALWAYS,
+               "auto": api.RX_GROUPS_AUTO}
 
 
 class PrefixCacheEngine:
@@ -119,84 +128,72 @@ class PrefixCacheEngine:
         tokens = np.concatenate(prompts).astype(np.int32) if b else np.zeros(0, np.int32)
         return self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)
 
-    def plan_concat(self, tokens, tok_indptr, n_new, groups: bool = False, min_shared: int = 64) -> StepPlan:
+    def _staging(self, nbytes: int) -> int:
+        """Next pinned staging buffer with room for nbytes, once the copy that last read it is done."""
+        i = self._pin_i
+        self._pin_i ^= 1
+        if self._pin[i] is None or self._pin[i].numel() < nbytes:
+            if self._pin_used[i]:
+                self._pin_ev[i].synchronize()
+            self._pin[i] = torch.empty(max(nbytes, 4096) * 2, dtype=torch.uint8).pin_memory()
+            self._pin_np[i] = self._pin[i].numpy()
+            self._pin_used[i] = False
+        if self._pin_used[i]:
+            self._pin_ev[i].synchronize()
+            self._pin_used[i] = False
+        return i
+
+    def plan_concat(self, tokens, tok_indptr, n_new, groups=False, min_shared: int = 64) -> StepPlan:
         """a1 + a2: match every prompt (tokens[tok_indptr[b]:tok_indptr[b+1]]), check that
         exactly its last n_new[b] tokens are uncached, allocate their slots, pin the matched
-        prefixes for the duration of the step."""
+        prefixes until finish; with groups (True, or "auto": only where stacking pays) the
+        shared-prefix groups too.  All in the library (rx_step_plan), written straight into a
+        pinned staging buffer."""
         tokens = np.ascontiguousarray(tokens, np.int32)
         tok_indptr = np.ascontiguousarray(tok_indptr, np.int64)
+        n_new = np.ascontiguousarray(n_new, np.int32)
         b = len(tok_indptr) - 1
-        lens = np.diff(tok_indptr)
-        ps, pind, last = self.tree.match_prefix_batch(tokens, tok_indptr)
-        P = np.diff(pind).astype(np.int64)
-        n_new = np.asarray(n_new, np.int64)
-        if not np.array_equal(P + n_new, lens):
-            bad = int(np.flatnonzero(P + n_new != lens)[0])
-            raise ValueError(f"request {bad}: {P[bad]} tokens cached, but {lens[bad] - n_new[bad]} expected")
-        T = int(n_new.sum())
-        new = self.tree.alloc_slots(T)
-        self.tree.lock_batch(last)          # in flight: the matched prefixes cannot be evicted
-        qo = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int64)
-        max_kv = int(lens.max()) if b else 1
-        plan = StepPlan(b, tokens, tok_indptr, ps, pind, P.astype(np.int32), new, qo, last,
-                        int(n_new.max()) if b else 0, max_kv, ((max_kv + 7) // 8) * 8)
-        if groups and b:
-            # requests whose cached paths share a node: their shared run is read once per group
-            gof, glen = self.tree.shared_groups(last, min_shared)
-            if len(glen) and groups == "auto":
-                # extend: stack rows only when each request's remaining keys are few (they run
-                # on CUDA cores) and the stacked rows beat the per-request 128-row tiles
-                shared = np.where(gof >= 0, glen[np.maximum(gof, 0)], 0)
-                private = P + n_new - shared
-                if (gof < 0).any() or private.max() > 256 or n_new.max() * (self.hq // self.hkv) >= 128:
-                    glen = glen[:0]
-            if len(glen):
-                order = np.argsort(gof, kind="stable")
-                order = order[gof[order] >= 0]
-                counts = np.bincount(gof[order], minlength=len(glen))
-                plan.grp_members = order.astype(np.int32)
-                plan.grp_indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
-                plan.grp_len = glen.astype(np.int32)
-                plan.grp_rows = int(np.bincount(gof[order], weights=n_new[order], minlength=len(glen)).max())
+        need = api.rx_step_stage_bytes(b, int(tok_indptr[-1]))
+        i = self._staging(need)
+        host = self._pin_np[i]
+        last = np.empty(max(b, 1), np.int64)
+        L = api.rx_step_plan(self.tree.h, tokens, tok_indptr, n_new, _GROUP_MODE[groups], self.hq // self.hkv,
+                             min_shared, self._pin[i].data_ptr(), host.nbytes, last)
+
+        def view(off, n, dt):
+            return host[off:off + n * np.dtype(dt).itemsize].view(dt)
+
+        plan = StepPlan(b, tokens, tok_indptr, view(L.off_prefix_slots, L.total_prefix, np.int32),
+                        view(L.off_prefix_indptr, b + 1, np.int64), view(L.off_prefix_lens, b, np.int32),
+                        view(L.off_new_slots, L.total_new, np.int32), view(L.off_qo_indptr, b + 1, np.int64),
+                        last[:b], L.max_qo_len, L.max_kv_len, L.stride, layout=L, stage=i)
+        if L.num_groups:
+            plan.grp_indptr = view(L.off_grp_indptr, L.num_groups + 1, np.int32)
+            plan.grp_members = view(L.off_grp_members, int(plan.grp_indptr[-1]), np.int32)
+            plan.grp_len = view(L.off_grp_len, L.num_groups, np.int32)
+            plan.grp_rows = L.max_group_rows
         return plan
 
     def upload(self, plan: StepPlan, stream=None) -> dict:
-        """Move the step's index arrays to the device: packed into one pinned host buffer and
-        copied with one asynchronous H2D transfer on the stream (device views returned)."""
-        B = plan.batch
-        parts = [("prefix_slots", plan.prefix_slots if len(plan.prefix_slots) else np.zeros(1, np.int32), np.int32),
-                 ("prefix_indptr", plan.prefix_indptr, np.int64),
-                 ("new_slots", plan.new_slots if len(plan.new_slots) else np.zeros(1, np.int32), np.int32),
-                 ("qo_indptr", plan.qo_indptr, np.int64),
-                 ("prefix_lens", plan.prefix_lens, np.int32),
-                 ("kv_lens", plan.prefix_lens.astype(np.int64) + np.diff(plan.qo_indptr), np.int32)]
-        if plan.grp_len is not None:
-            parts += [("grp_indptr", plan.grp_indptr, np.int32), ("grp_members", plan.grp_members, np.int32),
-                      ("grp_len", plan.grp_len, np.int32)]
-        offs, total = [], 0
-        for _, a, dt in parts:
-            offs.append(total)
-            total += (len(a) * np.dtype(dt).itemsize + 255) // 256 * 256
-        i = self._pin_i
-        self._pin_i ^= 1
-        if self._pin[i] is None or self._pin[i].numel() < total:
-            self._pin[i] = torch.empty(max(total, 4096) * 2, dtype=torch.uint8).pin_memory()
-            self._pin_np[i] = self._pin[i].numpy()
-            self._pin_used[i] = False
+        """Move the step's index arrays to the device: one asynchronous H2D copy of the staging
+        buffer on the stream.  Returns device addresses (same offsets as the staging buffer)."""
+        L, i = plan.layout, plan.stage
+        total = max(int(L.bytes), 256)
         if self._dev_idx is None or self._dev_idx.numel() < total:
             self._dev_idx = torch.empty(max(total, 4096) * 2, dtype=torch.uint8, device=self.device)
-        if self._pin_used[i]:
-            self._pin_ev[i].synchronize()          # the copy that last read this buffer is done
-        host = self._pin_np[i]
-        for (name, a, dt), o in zip(parts, offs):
-            host[o:o + len(a) * np.dtype(dt).itemsize] = np.ascontiguousarray(a, dt).view(np.uint8)
         st = self._stream if stream is None else stream
         with torch.cuda.stream(st):
             self._dev_idx[:total].copy_(self._pin[i][:total], non_blocking=True)
         self._pin_ev[i].record(st)
         self._pin_used[i] = True
         base = self._dev_idx.data_ptr()
-        out = {name: base + o for (name, a, dt), o in zip(parts, offs)}   # device addresses
+        out = {"prefix_slots": base + L.off_prefix_slots, "prefix_indptr": base + L.off_prefix_indptr,
+               "new_slots": base + L.off_new_slots, "qo_indptr": base + L.off_qo_indptr,
+               "prefix_lens": base + L.off_prefix_lens, "kv_lens": base + L.off_kv_lens}
+        if L.num_groups:
+            out.update(grp_indptr=base + L.off_grp_indptr, grp_members=base + L.off_grp_members,
+                       grp_len=base + L.off_grp_len)
+        B = plan.batch
         if self._r2t is None or self._r2t.shape[1] != plan.stride or self._r2t.shape[0] < max(B, 1):
             self._r2t = torch.empty(max(B, 1) * 2, plan.stride, dtype=torch.int32, device=self.device)
         out["r2t"] = self._r2t
@@ -227,10 +224,11 @@ class PrefixCacheEngine:
     def groups(self, plan: StepPlan, dev: dict):
         """The plan's shared-prefix groups (computed by plan(..., groups=True) and uploaded with
         the step's index arrays) as the ABI struct, or None."""
-        if plan.grp_len is None:
+        L = plan.layout
+        if not L.num_groups:
             return None
-        return api.shared_groups_struct(len(plan.grp_len), int(np.diff(plan.grp_indptr).max()), dev["grp_indptr"],
-                                        dev["grp_members"], dev["grp_len"], int(plan.grp_len.max()), plan.grp_rows)
+        return api.shared_groups_struct(L.num_groups, L.max_group_size, dev["grp_indptr"], dev["grp_members"],
+                                        dev["grp_len"], L.max_group_len, L.max_group_rows)
 
     def decode_workspace(self, plan: StepPlan, groups=None):
         nbytes = api.decode_workspace_bytes(self.desc, plan.batch, plan.max_kv_len, groups)
@@ -261,9 +259,7 @@ class PrefixCacheEngine:
         return self.tree.evict(num_tokens)
 
     def finish(self, plan: StepPlan, evict_tokens: int = 0) -> int:
-        """End of a step: a7 insert, a8 evict (the step's prefixes still pinned), unpin.
-        Returns the number of slots evicted."""
-        self.commit(plan)
-        freed = self.tree.evict_count(evict_tokens) if evict_tokens else 0
-        self.tree.unlock_batch(plan.last_nodes)
-        return freed
+        """End of a step: a7 insert, a8 evict (the step's prefixes still pinned), unpin -- one
+        library call (rx_step_finish).  Returns the number of slots evicted."""
+        return api.rx_step_finish(self.tree.h, plan.tokens, plan.tok_indptr, plan.last_nodes,
+                                  self._pin[plan.stage].data_ptr(), plan.layout, evict_tokens)

@@ -246,3 +246,19 @@ def test_exhaustive_small_scripts_keep_invariants():
                 m.evict(int(rng.integers(1, 4)))
             assert m.check_stamps_uniform()
             assert m.cached_tokens() + len(m.alloc.free) == 32
+
+
+def test_shared_groups_hand_worked():
+    """Groups by first token, common length = longest common prefix (worked by hand)."""
+    from oracle import shared_groups
+    shared = list(range(100, 140))
+    matched = [shared + [1000 + i] for i in range(5)] + [[9, 9, 9, 9]] + [shared[:10] + [55]] + [[]]
+    gof, glen = shared_groups(matched, 1)
+    assert gof.tolist() == [0, 0, 0, 0, 0, -1, 0, -1] and glen.tolist() == [10]
+    gof, glen = shared_groups(matched[:5], 1)
+    assert gof.tolist() == [0] * 5 and glen.tolist() == [40]
+    gof, glen = shared_groups(matched[:5], 41)
+    assert gof.tolist() == [-1] * 5 and glen.tolist() == []
+    # two separate groups, numbered in order of first appearance; a prefix of another counts
+    gof, glen = shared_groups([[5, 6, 7], [1, 2], [5, 6], [1, 2, 3], [8]], 1)
+    assert gof.tolist() == [0, 1, 0, 1, -1] and glen.tolist() == [2, 2]

@@ -1,0 +1,190 @@
+"""Native step runtime (rx_step_plan / rx_step_finish) against the oracle's prefix-cache model.
+
+Host code only: a step's match, allocation, pinning, index layout, shared-prefix groups,
+insert, free of duplicate slots, eviction and unpinning must equal the same operations
+replayed on the oracle, bit for bit, over multi-step scripts.
+"""
+import numpy as np
+import pytest
+
+from oracle import PrefixCacheModel, shared_groups
+from prefix_cached_kv_radix_gb300 import api
+
+api.load()
+
+
+def _stage(batch, total):
+    n = api.rx_step_stage_bytes(batch, total)
+    buf = np.zeros(n + 64, np.uint8)
+    addr = buf.ctypes.data
+    return buf, addr, n
+
+
+def _view(buf, off, n, dt):
+    return buf[off:off + n * np.dtype(dt).itemsize].view(dt)
+
+
+def _auto_ok(gof, glen, P, n_new, heads_per_kv):
+    if len(glen) == 0 or (gof < 0).any():
+        return False
+    shared = glen[gof]
+    return bool((P + n_new - shared).max() <= 256 and (n_new * heads_per_kv).max() < 128)
+
+
+def _step(t, m, prompts, n_new, mode, hpk, min_shared, evict_tokens):
+    b = len(prompts)
+    tok_indptr = np.concatenate([[0], np.cumsum([len(p) for p in prompts])]).astype(np.int64)
+    tokens = np.concatenate(prompts).astype(np.int32) if b else np.zeros(0, np.int32)
+    n_new = np.asarray(n_new, np.int32)
+    buf, addr, cap = _stage(b, int(tok_indptr[-1]))
+    last = np.empty(max(b, 1), np.int64)
+    L = api.rx_step_plan(t.h, tokens, tok_indptr, n_new, mode, hpk, min_shared, addr, cap, last)
+    # oracle: match every prompt, allocate, lock
+    P, pre = [], []
+    for p in prompts:
+        k, s = m.match(p)
+        P.append(k)
+        pre.append(s)
+    P = np.array(P, np.int64)
+    T = int(n_new.sum())
+    new = m.alloc.alloc(T)
+    for p, k in zip(prompts, P):
+        m.lock(p, int(k))
+    assert L.batch == b and L.total_new == T and L.total_prefix == int(P.sum())
+    assert L.max_qo_len == (int(n_new.max()) if b else 0)
+    assert L.max_kv_len == max([len(p) for p in prompts] + [1]) and L.stride % 8 == 0 and L.stride >= L.max_kv_len
+    for off in (L.off_prefix_slots, L.off_prefix_indptr, L.off_new_slots, L.off_qo_indptr, L.off_prefix_lens,
+                L.off_kv_lens, L.off_grp_indptr, L.off_grp_members, L.off_grp_len):
+        assert off % 256 == 0
+    assert L.bytes <= cap
+    assert _view(buf, L.off_prefix_slots, L.total_prefix, np.int32).tolist() == \
+        (np.concatenate(pre).tolist() if b else [])
+    assert _view(buf, L.off_prefix_indptr, b + 1, np.int64).tolist() == [0] + np.cumsum(P).tolist()
+    assert _view(buf, L.off_new_slots, T, np.int32).tolist() == new.tolist()
+    assert _view(buf, L.off_qo_indptr, b + 1, np.int64).tolist() == [0] + np.cumsum(n_new).tolist()
+    assert _view(buf, L.off_prefix_lens, b, np.int32).tolist() == P.tolist()
+    assert _view(buf, L.off_kv_lens, b, np.int32).tolist() == (P + n_new).tolist()
+    # groups
+    gof, glen = shared_groups([p[:k] for p, k in zip(prompts, P)], min_shared)
+    use = mode != api.RX_GROUPS_NONE and len(glen) > 0
+    if mode == api.RX_GROUPS_AUTO:
+        use = use and _auto_ok(gof, glen, P, n_new.astype(np.int64), hpk)
+    if use:
+        assert L.num_groups == len(glen)
+        gi = _view(buf, L.off_grp_indptr, L.num_groups + 1, np.int32)
+        gm = _view(buf, L.off_grp_members, int(gi[-1]), np.int32)
+        gl = _view(buf, L.off_grp_len, L.num_groups, np.int32)
+        assert gl.tolist() == glen.tolist()
+        for g in range(L.num_groups):
+            assert gm[gi[g]:gi[g + 1]].tolist() == np.flatnonzero(gof == g).tolist()
+        assert L.max_group_size == int(np.diff(gi).max()) and L.max_group_len == int(glen.max())
+        assert L.max_group_rows == max(int(n_new[gof == g].sum()) for g in range(len(glen)))
+    else:
+        assert L.num_groups == 0
+    # pinned: an eviction of everything leaves the matched prefixes
+    # finish on both
+    evicted = api.rx_step_finish(t.h, tokens, tok_indptr, last, addr, L, evict_tokens)
+    qo = np.concatenate([[0], np.cumsum(n_new)])
+    dups = []
+    for i, p in enumerate(prompts):
+        full = np.concatenate([pre[i], new[qo[i]:qo[i + 1]]]).astype(np.int32)
+        dups.append(m.insert(p, full))
+    for i in range(b):
+        over = dups[i] - P[i]
+        if over > 0:
+            m.alloc.release(new[qo[i]:qo[i] + over])
+    freed = m.evict(evict_tokens) if evict_tokens else np.zeros(0, np.int32)
+    for p, k in zip(prompts, P):
+        m.lock(p, int(k), -1)
+    assert evicted == len(freed)
+    st = t.stats()
+    assert st["cached_tokens"] == m.cached_tokens() and st["free_slots"] == len(m.alloc.free)
+    assert st["node_count"] == len(m.nodes())
+    t.check()
+
+
+def _random_prompts(rng, m, b, vocab, maxlen):
+    """Prompts whose last n_new tokens are exactly the uncached tail (distinct first new token
+    per divergence point, so that no earlier request of the batch caches a later one's tail)."""
+    prompts, n_new, used = [], [], set()
+    for _ in range(b):
+        for _try in range(50):
+            p = rng.integers(0, vocab, size=int(rng.integers(1, maxlen + 1))).tolist()
+            k = m._cached_len(p)
+            if k == len(p) and rng.random() < 0.7:
+                continue
+            key = (tuple(p[:k]), p[k] if k < len(p) else None)
+            if key in used:
+                continue
+            used.add(key)
+            prompts.append(np.array(p, np.int32))
+            n_new.append(len(p) - k)
+            break
+    return prompts, n_new
+
+
+@pytest.mark.parametrize("mode", [api.RX_GROUPS_NONE, api.RX_GROUPS_ALWAYS, api.RX_GROUPS_AUTO])
+def test_step_scripts_match_oracle(mode):
+    rng = np.random.default_rng(40 + mode)
+    for trial in range(6):
+        t = api.RadixTree(600, trial)
+        m = PrefixCacheModel(600, trial)
+        for step in range(8):
+            prompts, n_new = _random_prompts(rng, m, int(rng.integers(0, 7)), 3, 12)
+            if sum(n_new) > len(m.alloc.free):
+                break
+            _step(t, m, prompts, n_new, mode, int(rng.choice([1, 4, 16])), int(rng.integers(1, 4)),
+                  int(rng.integers(0, 10)))
+        n = t.stats()["free_slots"]
+        assert t.alloc_slots(n).tolist() == m.alloc.alloc(n).tolist()
+
+
+def test_step_plan_rejects_cached_tail_without_side_effects():
+    t = api.RadixTree(64, 2)
+    s = t.alloc_slots(4)
+    t.insert([1, 2, 3, 4], s)
+    before = t.stats()
+    tokens = np.array([1, 2, 3, 4, 5], np.int32)
+    ind = np.array([0, 5], np.int64)
+    buf, addr, cap = _stage(1, 5)
+    last = np.empty(1, np.int64)
+    with pytest.raises(api.RxError) as e:      # claims 2 new tokens; only 1 is uncached
+        api.rx_step_plan(t.h, tokens, ind, np.array([2], np.int32), 0, 1, 1, addr, cap, last)
+    assert e.value.code == api.RX_EINVAL
+    after = t.stats()
+    assert after["free_slots"] == before["free_slots"] and after["cached_tokens"] == before["cached_tokens"]
+    # nothing was pinned: everything is still evictable
+    assert len(t.evict(100)) == 4
+    t.check()
+
+
+def test_step_plan_out_of_slots_and_small_stage():
+    t = api.RadixTree(8, 0)
+    tokens = np.arange(10, dtype=np.int32)
+    ind = np.array([0, 10], np.int64)
+    buf, addr, cap = _stage(1, 10)
+    last = np.empty(1, np.int64)
+    with pytest.raises(api.RxError) as e:
+        api.rx_step_plan(t.h, tokens, ind, np.array([10], np.int32), 0, 1, 1, addr, cap, last)
+    assert e.value.code == api.RX_ENOMEM
+    assert t.stats()["free_slots"] == 8
+    with pytest.raises(api.RxError) as e:
+        api.rx_step_plan(t.h, tokens[:4], np.array([0, 4], np.int64), np.array([4], np.int32), 0, 1, 1, addr,
+                         16, last)
+    assert e.value.code == api.RX_EINVAL
+
+
+def test_step_pins_prefixes_until_finish():
+    t = api.RadixTree(64, 5)
+    s = t.alloc_slots(6)
+    t.insert([7, 7, 7, 7, 7, 7], s)
+    tokens = np.array([7, 7, 7, 7, 7, 7, 8, 9], np.int32)
+    ind = np.array([0, 8], np.int64)
+    buf, addr, cap = _stage(1, 8)
+    last = np.empty(1, np.int64)
+    L = api.rx_step_plan(t.h, tokens, ind, np.array([2], np.int32), 0, 1, 1, addr, cap, last)
+    assert len(t.evict(100)) == 0            # the matched prefix is pinned
+    ev = api.rx_step_finish(t.h, tokens, ind, last, addr, L, 100)
+    assert ev == 2 and t.stats()["cached_tokens"] == 6   # evicts before unpinning: only the new leaf
+    assert len(t.evict(100)) == 6                        # unpinned afterwards
+    t.check()

@@ -12,29 +12,28 @@
 // GB300 design.  One CTA per (request, kv head, 256 packed query rows).  The query heads
 // of a kv head (GQA group) are packed with the tokens, head fastest: packed row R ->
 // token R / G, head g*G + R % G, so every K/V tile feeds G heads and the tile stays a
-// dense contraction.  Two 128-row Q tiles share each K/V tile (halves L2->SM traffic per
-// FLOP).  Roles (384 threads, three warpgroups):
-//   warps 0-2  loaders: 16-byte cp.async gathers of Q once and of K/V tiles (64 keys)
-//              through the slot table into a 5-stage ring in the 128B-swizzled K-major
-//              layout tcgen05 reads.  A single warp cannot issue gathers fast enough to feed
-//              the tensor core, so three warps split every tile.  Each loader thread keeps
-//              two tiles of copies in flight, waits for its own oldest group, fences the
-//              generic->async proxy and arrives on the tile's barrier; slot ids are
-//              prefetched one tile ahead.
-//   warp 3     TMEM allocator and single-thread tcgen05.mma issuer:
-//              S_t = Q_t K^T (M=128, N=64, K=D, both operands from smem) and
-//              O_t += P_t V (M=128, N=D, K=64, P from TMEM, V an MN-major smem operand),
-//              completion via tcgen05.commit.
+// dense contraction.  Two 128-row Q tiles share each K/V tile of 128 keys.  Roles (512
+// threads, four warpgroups, registers split 88 / 168 / 168 / 88 with setmaxnreg):
+//   warps 0-3, 13-15  loaders: 16-byte cp.async gathers of Q once and of K and V tiles
+//              through the slot table into separate K (3-deep) and V (2-deep) rings in the
+//              128B-swizzled layouts tcgen05 reads.  Each thread's arrival on a tile's full
+//              barrier is made by the copy hardware when its copies land
+//              (cp.async.mbarrier.arrive), so loaders wait only for free slots; slot ids are
+//              prefetched a tile ahead.
+//   warp 12    TMEM allocator and single-thread tcgen05.mma issuer, per K/V tile j and
+//              Q tile t:  O_t += P_t(j) V(j)  (M=128, N=D, K=128, P from TMEM), then at once
+//              S_t(j+1) = Q_t K(j+1)^T  (M=128, N=128, K=D) into the same TMEM columns -- the
+//              tensor pipe runs one thread's MMAs in order, so P is read before it is
+//              overwritten.  Completion via tcgen05.commit.
 //   warps 4-7  softmax of Q tile 0; warps 8-11 softmax of Q tile 1: tcgen05.ld of a score
 //              row per thread, causal mask, online softmax in the exp2 domain with a lazy
 //              rescale (the reference max only moves when the row max grows by more than
-//              2^8, which keeps every P <= 256), P packed to bf16 and stored back to TMEM
-//              (tcgen05.st), O rescaled in TMEM only when the reference moved, O / l to
-//              global at the end.
-// TMEM columns: S0 [0,64) S1 [64,128) P0 [128,160) P1 [160,192) O0 [256,256+D) O1 after.
-// The two Q tiles ping-pong: while one tile's softmax runs, the tensor core works on the
-// other's GEMMs.  Every wait is bounded; on time-out the kernel records RX_DEV_TIMEOUT,
-// drains its async copies, frees TMEM and returns.
+//              2^8, which keeps every P <= 256), P packed to bf16 and stored over the row's
+//              scores in TMEM (tcgen05.st); fp32 pairs use the packed f32x2 forms.
+// TMEM columns: S0/P0 [0,128) S1/P1 [128,256) O0 [256,256+D) O1 after.  While one Q tile's
+// softmax runs, the tensor core works on the other's GEMMs.  Every wait is bounded; on
+// time-out the kernel records RX_DEV_TIMEOUT, drains its async copies, frees TMEM and
+// returns.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -45,12 +44,11 @@
 
 namespace rx {
 
-constexpr int EXT_BN = 64;        // keys per K/V tile
-constexpr int EXT_NS = 5;         // K/V ring depth (a loader runs EXT_NS-1-EXT_LAG tiles ahead)
-constexpr int EXT_LAG = 2;        // cp.async groups a loader thread keeps in flight (<= EXT_NS - 2)
-constexpr int EXT_LOADERS = 96;   // loader threads (warps 0-2)
-constexpr int EXT_MMA_WARP = 3;
-constexpr int EXT_THREADS = 384;  // 12 warps
+constexpr int EXT_BN = 128;       // keys per K/V tile
+constexpr int EXT_THREADS = 512;  // 16 warps
+constexpr int EXT_MMA_WARP = 12;
+constexpr int EXT_LOADERS = 224;  // warps 0-3 and 13-15
+constexpr uint32_t EXT_REGS_SOFTMAX = 168, EXT_REGS_OTHER = 88;   // 2*128*88 + 2*128*168 = 512*128
 constexpr float EXT_LOG2E = 1.4426950408889634f;
 constexpr float EXT_LN2 = 0.6931471805599453f;
 constexpr float EXT_RESCALE_THRESHOLD = 8.0f;   // log2 units
@@ -88,22 +86,25 @@ struct ExtendParams {
 
 template <int D>
 struct ExtLayout {
+    static constexpr int NK = D == 128 ? 3 : 4;    // K ring depth
+    static constexpr int NV = D == 128 ? 2 : 4;    // V ring depth
     static constexpr int Q_TILE = 128 * D * 2;
     static constexpr int KV_TILE = EXT_BN * D * 2;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
-    static constexpr int OFF_V = OFF_K + EXT_NS * KV_TILE;
-    static constexpr int OFF_BAR = OFF_V + EXT_NS * KV_TILE;
-    // q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], mma_done
-    static constexpr int BAR_Q = 0, BAR_KVF = 1, BAR_KVE = 1 + EXT_NS, BAR_S = 1 + 2 * EXT_NS,
-                         BAR_P = BAR_S + 2, BAR_O = BAR_P + 2, BAR_DONE = BAR_O + 2, NBAR = BAR_DONE + 1;
+    static constexpr int OFF_V = OFF_K + NK * KV_TILE;
+    static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
+    // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], mma_done
+    static constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 1 + NK, BAR_VF = 1 + 2 * NK, BAR_VE = 1 + 2 * NK + NV,
+                         BAR_S = 1 + 2 * NK + 2 * NV, BAR_P = BAR_S + 2, BAR_DONE = BAR_P + 2, NBAR = BAR_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;   // room to align the base to 1024 B
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S0 = 0, COL_P0 = 2 * EXT_BN, COL_O0 = 256;
+    static constexpr uint32_t COL_O0 = 256;
     static constexpr int CPR = D / 8;                                   // 16-byte chunks per row
     static constexpr int NX = (EXT_BN * CPR + EXT_LOADERS - 1) / EXT_LOADERS;   // chunks per loader thread per tile
+    static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
 template <int D>
@@ -111,6 +112,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
     using LY = ExtLayout<D>;
     constexpr int CPR = LY::CPR;
     constexpr int NX = LY::NX;
+    constexpr int NK = LY::NK;
+    constexpr int NV = LY::NV;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -169,14 +172,17 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
 
     if (threadIdx.x == 0) {
         mbar_init(bar(LY::BAR_Q), EXT_LOADERS);
-        for (int i = 0; i < EXT_NS; ++i) {
-            mbar_init(bar(LY::BAR_KVF + i), EXT_LOADERS);
-            mbar_init(bar(LY::BAR_KVE + i), 1);
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(bar(LY::BAR_KF + i), EXT_LOADERS);
+            mbar_init(bar(LY::BAR_KE + i), 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(bar(LY::BAR_VF + i), EXT_LOADERS);
+            mbar_init(bar(LY::BAR_VE + i), 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(LY::BAR_S + t), 1);
-            mbar_init(bar(LY::BAR_P + t), 128);
-            mbar_init(bar(LY::BAR_O + t), 1);
+            mbar_init(bar(LY::BAR_P + t), 4);          // one arrival per softmax warp
         }
         mbar_init(bar(LY::BAR_DONE), 1);
         *abort_flag = 0;
@@ -190,10 +196,15 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    const int wg = warp >> 2;
 
-    if (warp < EXT_LOADERS / 32) {
+    // Role dispatch on the warpgroup first, so that each register re-split dominates the
+    // code that relies on it (the compiler allocates each region to its own limit).
+    if (wg == 0 || wg == 3) {
+    regs_decrease<EXT_REGS_OTHER>();
+    if (warp != EXT_MMA_WARP) {
         // ------------------------------------------------------------ loaders
-        const int lt = threadIdx.x;
+        const int lt = warp < 4 ? (int)threadIdx.x : (int)threadIdx.x - (EXT_MMA_WARP + 1) * 32 + 128;
         const uint32_t qs = base + LY::OFF_Q;
         for (int qi = lt; qi < ntiles * 128 * CPR; qi += EXT_LOADERS) {
             const int rr = qi / CPR, c = qi % CPR;
@@ -204,7 +215,7 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                                                  (((c & 7) ^ (r & 7)) << 4));
             cp_async_16(dst, src, 16);
         }
-        cp_async_commit();                     // group 0: Q (completes with tile 0)
+        cp_async_arrive_noinc(bar(LY::BAR_Q));   // arrives once this thread's Q copies land
         int32_t slot_a[NX], slot_b[NX];      // slot ids, one tile ahead (two buffers)
         auto load_slots = [&](int j, int32_t* dst) {
 #pragma unroll
@@ -214,18 +225,10 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                 dst[x] = (q < EXT_BN * CPR && kk < kv_end) ? slots_row[kk] : -1;
             }
         };
-        auto publish = [&](int jt) {           // copies of tile jt (and Q) are complete
-            fence_proxy_async_smem();
-            if (jt == 0) mbar_arrive(bar(LY::BAR_Q));
-            mbar_arrive(bar(LY::BAR_KVF + jt % EXT_NS));
-        };
-        // Issue tile j from `cur`, then start loading the slots of tile j+1 into `nxt`.
-        auto step = [&](int j, const int32_t* cur, int32_t* nxt) -> bool {
-            const int st = j % EXT_NS;
-            if (j >= EXT_NS && !warp_wait(bar(LY::BAR_KVE + st), ((j / EXT_NS) - 1) & 1, abort_flag, p.status))
-                return false;
-            const uint32_t kb = base + LY::OFF_K + st * LY::KV_TILE;
-            const uint32_t vb = base + LY::OFF_V + st * LY::KV_TILE;
+        // Gather one K or V tile; the full barrier gets this thread's arrival when its copies
+        // have landed (cp.async.mbarrier.arrive), so a loader never waits for its own copies,
+        // only for free ring slots.
+        auto issue = [&](int j, uint32_t buf, const __nv_bfloat16* pool, const int32_t* cur, uint32_t full) {
 #pragma unroll
             for (int x = 0; x < NX; ++x) {
                 const int q = lt + EXT_LOADERS * x;
@@ -241,16 +244,19 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                     const int64_t off = ((int64_t)slot * p.hkv + g) * D + c * 8;
                     const uint32_t so =
                         (uint32_t)((c >> 3) * EXT_BN * 128 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
-                    cp_async_16(kb + so, p.k_pool + off, bytes);
-                    cp_async_16(vb + so, p.v_pool + off, bytes);
+                    cp_async_16(buf + so, pool + off, bytes);
                 }
             }
-            cp_async_commit();
+            cp_async_arrive_noinc(full);
+        };
+        // Issue K and V of tile j from `cur`, and load the slots of tile j+1 into `nxt`.
+        auto step = [&](int j, const int32_t* cur, int32_t* nxt) -> bool {
+            const int ks = j % NK, vs = j % NV;
+            if (j >= NK && !warp_wait(bar(LY::BAR_KE + ks), ((j / NK) - 1) & 1, abort_flag, p.status)) return false;
+            issue(j, base + LY::OFF_K + ks * LY::KV_TILE, p.k_pool, cur, bar(LY::BAR_KF + ks));
+            if (j >= NV && !warp_wait(bar(LY::BAR_VE + vs), ((j / NV) - 1) & 1, abort_flag, p.status)) return false;
+            issue(j, base + LY::OFF_V + vs * LY::KV_TILE, p.v_pool, cur, bar(LY::BAR_VF + vs));
             if (j + 1 < nkv) load_slots(j + 1, nxt);
-            if (j >= EXT_LAG) {
-                cp_async_wait<EXT_LAG>();
-                publish(j - EXT_LAG);
-            }
             return true;
         };
         load_slots(0, slot_a);
@@ -259,10 +265,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             ok = step(j, slot_a, slot_b);
             if (ok && j + 1 < nkv) ok = step(j + 1, slot_b, slot_a);
         }
-        cp_async_wait<0>();
-        if (ok)
-            for (int jt = max(0, nkv - EXT_LAG); jt < nkv; ++jt) publish(jt);
-    } else if (warp == EXT_MMA_WARP) {
+        cp_async_wait_all();                   // no copy may still be landing at teardown
+    } else {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, EXT_BN, 0, 0);
@@ -271,52 +275,68 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             const uint64_t kd0 = sdesc_sw128(base + LY::OFF_K, 16, 1024);
             const uint64_t vd0 = sdesc_sw128(base + LY::OFF_V, EXT_BN * 128, 1024);
             // descriptor start addresses advance in 16-byte units in the low bits
-            auto qdesc = [&](int t, int s) {
-                return qd0 + (uint64_t)((t * LY::Q_TILE + (s >> 2) * 128 * 128 + (s & 3) * 32) >> 4);
+            auto issue_s = [&](int t, int ks) {
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s)
+                    umma_f16_ss(tmem + t * EXT_BN,
+                                qd0 + (uint64_t)((t * LY::Q_TILE + (s >> 2) * 128 * 128 + (s & 3) * 32) >> 4),
+                                kd0 + (uint64_t)((ks * LY::KV_TILE + (s >> 2) * EXT_BN * 128 + (s & 3) * 32) >> 4),
+                                IDESC_S, s > 0 ? 1u : 0u);
+                umma_commit(bar(LY::BAR_S + t));
             };
-            auto kdesc = [&](int st, int s) {
-                return kd0 + (uint64_t)((st * LY::KV_TILE + (s >> 2) * EXT_BN * 128 + (s & 3) * 32) >> 4);
-            };
-            auto vdesc = [&](int st, int s) { return vd0 + (uint64_t)((st * LY::KV_TILE + s * 16 * 128) >> 4); };
-            bool ok = mbar_wait(bar(LY::BAR_Q), 0, abort_flag, p.status);
-            tc_fence_after();
-            auto issue_pv = [&](int t, int jj) {
-                const int pst = jj % EXT_NS;
+            auto issue_pv = [&](int t, int vs, int j) {
 #pragma unroll
                 for (int s = 0; s < EXT_BN / 16; ++s)
-                    umma_f16_ts(tmem + LY::COL_O0 + t * D, tmem + LY::COL_P0 + t * (EXT_BN / 2) + s * 8,
-                                vdesc(pst, s), IDESC_PV, (jj > 0 || s > 0) ? 1u : 0u);
-                umma_commit(bar(LY::BAR_O + t));
+                    umma_f16_ts(tmem + LY::COL_O0 + t * D, tmem + t * EXT_BN + s * 8,
+                                vd0 + (uint64_t)((vs * LY::KV_TILE + s * 16 * 128) >> 4), IDESC_PV,
+                                (j > 0 || s > 0) ? 1u : 0u);
             };
+            // The copies were made by the loaders' generic-proxy cp.async and are acquired
+            // through the full barriers; a proxy fence here orders them before the tensor
+            // core's (async-proxy) reads.
+            bool ok = mbar_wait(bar(LY::BAR_Q), 0, abort_flag, p.status) &&
+                      mbar_wait(bar(LY::BAR_KF), 0, abort_flag, p.status);
+            fence_proxy_async_smem();
+            tc_fence_after();
+            if (ok) {
+                for (int t = 0; t < ntiles; ++t) issue_s(t, 0);
+                umma_commit(bar(LY::BAR_KE));
+            }
             for (int j = 0; ok && j < nkv; ++j) {
-                const int st = j % EXT_NS;
-                if (!mbar_wait(bar(LY::BAR_KVF + st), (j / EXT_NS) & 1, abort_flag, p.status)) { ok = false; break; }
+                const int vs = j % NV;
+                if (!mbar_wait(bar(LY::BAR_VF + vs), (j / NV) & 1, abort_flag, p.status)) { ok = false; break; }
+                fence_proxy_async_smem();
                 tc_fence_after();
+                const bool more = j + 1 < nkv;
+                const int ks = (j + 1) % NK;
                 for (int t = 0; t < ntiles; ++t) {
-                    if (j > 0) {
-                        if (!mbar_wait(bar(LY::BAR_P + t), (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-                        tc_fence_after();
+                    if (!mbar_wait(bar(LY::BAR_P + t), j & 1, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(t, vs, j);
+                    if (t == ntiles - 1) umma_commit(bar(LY::BAR_VE + vs));   // V(j) read by every tile
+                    if (more) {
+                        if (t == 0) {
+                            if (!mbar_wait(bar(LY::BAR_KF + ks), ((j + 1) / NK) & 1, abort_flag, p.status)) {
+                                ok = false;
+                                break;
+                            }
+                            fence_proxy_async_smem();
+                            tc_fence_after();
+                        }
+                        issue_s(t, ks);
                     }
-#pragma unroll
-                    for (int s = 0; s < D / 16; ++s)
-                        umma_f16_ss(tmem + LY::COL_S0 + t * EXT_BN, qdesc(t, s), kdesc(st, s), IDESC_S, s > 0 ? 1u : 0u);
-                    umma_commit(bar(LY::BAR_S + t));
-                    if (j > 0) issue_pv(t, j - 1);
                 }
                 if (!ok) break;
-                if (j > 0) umma_commit(bar(LY::BAR_KVE + (j - 1) % EXT_NS));
-            }
-            for (int t = 0; ok && t < ntiles; ++t) {
-                if (!mbar_wait(bar(LY::BAR_P + t), (nkv - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-                tc_fence_after();
-                issue_pv(t, nkv - 1);
+                if (more) umma_commit(bar(LY::BAR_KE + ks));
             }
             umma_commit(bar(LY::BAR_DONE));
         }
         __syncwarp();
+    }
     } else {
         // ------------------------------------------------------------ softmax warpgroups
-        const int t = (warp - 4) >> 2;
+        regs_increase<EXT_REGS_SOFTMAX>();
+        const int t = wg - 1;
         if (t < ntiles) {
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
@@ -326,20 +346,21 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             const int tok = Rc / G;
             const int pos = p.shared_mode ? kv_end - 1 : P_b + tok;   // attends keys 0..pos
             const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-            const uint32_t s_addr = tmem + lane_base + LY::COL_S0 + t * EXT_BN;
-            const uint32_t p_addr = tmem + lane_base + LY::COL_P0 + t * (EXT_BN / 2);
+            const uint32_t s_addr = tmem + lane_base + t * EXT_BN;   // scores, then P over them
             const uint32_t o_addr = tmem + lane_base + LY::COL_O0 + t * D;
+            const float sl = p.scale_log2;
             float m_ref = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j < nkv; ++j) {
                 if (!warp_wait(bar(LY::BAR_S + t), j & 1, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
                 float s[EXT_BN];
-                tmem_ld32(s_addr, s);
-                tmem_ld32(s_addr + 32, s + 32);
+#pragma unroll
+                for (int c = 0; c < EXT_BN; c += 32) tmem_ld32(s_addr + c, s + c);
                 tmem_wait_ld();
                 const int k0 = j * EXT_BN;
-                if (k0 + EXT_BN - 1 > pos) {
+                const bool masked = k0 + EXT_BN - 1 > pos;
+                if (masked) {
 #pragma unroll
                     for (int c = 0; c < EXT_BN; ++c)
                         if (k0 + c > pos) s[c] = -INFINITY;
@@ -348,52 +369,64 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = s[i];
 #pragma unroll
-                for (int c = 8; c < EXT_BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-                mx *= p.scale_log2;
+                for (int c = 8; c + 16 <= EXT_BN; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[EXT_BN - 8 + i]);
+                float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                mx *= sl;
                 float m_new = m_ref;
                 if (m_ref == -INFINITY || mx > m_ref + EXT_RESCALE_THRESHOLD) m_new = fmaxf(m_ref, mx);
-                const float alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
-                float rs8[8];
+                const float alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
+                const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new != m_ref);
+                l *= alpha;
+                m_ref = m_new;
+                const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m_new, -m_new);
+                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+                // P in two halves of 64 keys (32 columns)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-                uint32_t pk[EXT_BN / 2];
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[EXT_BN / 4];
 #pragma unroll
-                for (int c = 0; c < EXT_BN; c += 2) {
-                    const float e0 = fast_exp2(fmaf(s[c], p.scale_log2, -m_new));
-                    const float e1 = fast_exp2(fmaf(s[c + 1], p.scale_log2, -m_new));
-                    rs8[(c >> 1) & 7] += e0 + e1;
-                    pk[c >> 1] = pack_bf16x2(e0, e1);
+                    for (int cc = 0; cc < EXT_BN / 2; cc += 2) {
+                        const int c = h * (EXT_BN / 2) + cc;
+                        const uint64_t x2 = f2_fma(f2_pack(s[c], s[c + 1]), sl2, nm2);
+                        float x0, x1;
+                        f2_unpack(x2, x0, x1);
+                        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                        acc2[(c >> 1) & 3] = f2_add(acc2[(c >> 1) & 3], f2_pack(e0, e1));
+                        pk[cc >> 1] = pack_bf16x2(e0, e1);
+                    }
+                    tmem_st32u(s_addr + h * 32, pk);
                 }
-                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-                l = l * alpha + rs;
-                if (j > 0) {
-                    if (!warp_wait(bar(LY::BAR_O + t), (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, m_new != m_ref)) {
+                const uint64_t a01 = f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3]));
+                float ra, rb;
+                f2_unpack(a01, ra, rb);
+                l += ra + rb;
+                if (rescale) {
+                    // PV_t(j-1) has completed (S_t(j) was issued after it and is complete), and
+                    // PV_t(j) waits for this warp's arrival below.
 #pragma unroll
-                        for (int cc = 0; cc < D; cc += 32) {
-                            float ov[32];
-                            tmem_ld32(o_addr + cc, ov);
-                            tmem_wait_ld();
+                    for (int cc = 0; cc < D; cc += 32) {
+                        float ov[32];
+                        tmem_ld32(o_addr + cc, ov);
+                        tmem_wait_ld();
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-                            tmem_st32(o_addr + cc, ov);
-                        }
+                        for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+                        tmem_st32(o_addr + cc, ov);
                     }
                 }
-                m_ref = m_new;
-                tmem_st32u(p_addr, pk);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(LY::BAR_P + t));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(LY::BAR_P + t));
             }
-            if (ok && warp_wait(bar(LY::BAR_O + t), (nkv - 1) & 1, abort_flag, p.status)) {
+            if (ok && warp_wait(bar(LY::BAR_DONE), 0, abort_flag, p.status)) {
                 tc_fence_after();
                 const float inv = 1.f / l;
                 if (p.shared_mode) {
-                    // fp32 normalised partial and log2-domain lse for the decode merge
+                    // fp32 normalised partial and log2-domain lse for the merge
                     const int64_t item = (int64_t)p.grp_rows[m0 + tok] * p.hq + g * G + Rc % G;
                     const int64_t slot = item * p.part_per + p.part_base + blockIdx.x % p.n_chunks;
                     float* prow = p.part_o + slot * D;
@@ -411,25 +444,25 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                     }
                     if (valid) p.part_lse[slot] = m_ref + log2f(l);
                 } else {
-                __nv_bfloat16* orow = p.out + ((qo0 + tok) * p.hq + g * G + Rc % G) * D;
+                    __nv_bfloat16* orow = p.out + ((qo0 + tok) * p.hq + g * G + Rc % G) * D;
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 32) {
-                    float ov[32];
-                    tmem_ld32(o_addr + cc, ov);
-                    tmem_wait_ld();
-                    if (valid) {
+                    for (int cc = 0; cc < D; cc += 32) {
+                        float ov[32];
+                        tmem_ld32(o_addr + cc, ov);
+                        tmem_wait_ld();
+                        if (valid) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 8) {
-                            uint4 v;
-                            v.x = pack_bf16x2(ov[e + 0] * inv, ov[e + 1] * inv);
-                            v.y = pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv);
-                            v.z = pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv);
-                            v.w = pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv);
-                            *reinterpret_cast<uint4*>(orow + cc + e) = v;
+                            for (int e = 0; e < 32; e += 8) {
+                                uint4 v;
+                                v.x = pack_bf16x2(ov[e + 0] * inv, ov[e + 1] * inv);
+                                v.y = pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv);
+                                v.z = pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv);
+                                v.w = pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv);
+                                *reinterpret_cast<uint4*>(orow + cc + e) = v;
+                            }
                         }
                     }
-                }
-                if (valid && p.lse) p.lse[(qo0 + tok) * p.hq + g * G + Rc % G] = (m_ref + log2f(l)) * EXT_LN2;
+                    if (valid && p.lse) p.lse[(qo0 + tok) * p.hq + g * G + Rc % G] = (m_ref + log2f(l)) * EXT_LN2;
                 }
             }
         }
@@ -475,6 +508,15 @@ static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t strea
         const cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) {
             set_error("prefix_extend_attention: cannot set shared memory size: %s", cudaGetErrorString(e));
+            return RX_ECUDA;
+        }
+        // The warpgroups re-split the registers the block is launched with (setmaxnreg); the
+        // shares must add up to no more than that, or the increasing warps would wait forever.
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, extend_tc_kernel<D>) != cudaSuccess ||
+            (int64_t)fa.numRegs * EXT_THREADS < 2 * 128 * (int64_t)EXT_REGS_OTHER + 2 * 128 * (int64_t)EXT_REGS_SOFTMAX) {
+            set_error("prefix_extend_attention: kernel built with %d registers per thread; the register split needs %d",
+                      fa.numRegs, (int)((2 * 128 * EXT_REGS_OTHER + 2 * 128 * EXT_REGS_SOFTMAX) / EXT_THREADS));
             return RX_ECUDA;
         }
         attr = true;

@@ -57,19 +57,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded wait on an mbarrier phase.  Gives up when *abort (shared, CTA-wide) is set or
 // after `limit_ns`; on time-out it sets *abort and reports RX_DEV_TIMEOUT.  Returns true
 // when the phase completed.
@@ -314,35 +301,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
-}
-
-// 2^x for a pair, on the FMA pipe (keeps the special-function unit free for the other
-// columns).  x = k + f with k = round(x) (the 1.5 * 2^23 shift) and f in [-1/2, 1/2];
-// 2^f by a cubic fitted here in relative error on that interval (iteratively reweighted
-// least squares on Chebyshev nodes; max relative error 7.5e-5, far below bf16's 2^-9);
-// 2^k added into the exponent field.  Inputs are clamped to >= -125 (the result is then
-// ~2^-125, not 0: callers use it only where no score is masked).
-__device__ __forceinline__ uint64_t f2_exp2_poly(uint64_t x) {
-    constexpr float SHIFT = 12582912.0f;   // 1.5 * 2^23
-    float x0, x1;
-    f2_unpack(x, x0, x1);
-    x0 = fmaxf(x0, -125.f);
-    x1 = fmaxf(x1, -125.f);
-    const uint64_t xc = f2_pack(x0, x1);
-    const uint64_t sh = f2_pack(SHIFT, SHIFT);
-    const uint64_t t = f2_add(xc, sh);                                   // k in the low mantissa bits
-    const uint64_t k = f2_add(t, f2_pack(-SHIFT, -SHIFT));               // k as a float
-    const uint64_t f = f2_fma(k, f2_pack(-1.f, -1.f), xc);              // x - k
-    uint64_t p = f2_fma(f, f2_pack(0.0551716685f, 0.0551716685f), f2_pack(0.24261114f, 0.24261114f));
-    p = f2_fma(p, f, f2_pack(0.69326097f, 0.69326097f));
-    p = f2_fma(p, f, f2_pack(0.99992806f, 0.99992806f));
-    float p0, p1, t0, t1;
-    f2_unpack(p, p0, p1);
-    f2_unpack(t, t0, t1);
-    // bits(t) << 23 == k << 23 (mod 2^32): the shift constant's own bits vanish
-    const float e0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-    const float e1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
-    return f2_pack(e0, e1);
 }
 
 // ------------------------------------------------------------------ register split

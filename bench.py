@@ -163,6 +163,22 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------------------- replicas
+def reduce_max(values, world: int, device="cpu"):
+    """Elementwise max over ranks (the timed region's slowest replica); identity at N = 1."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def replica_throughput(tokens_per_step: int, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job tokens/s: every replica processes the same batch each step (weak scaling)."""
+    return tokens_per_step * steps * world / (ms_max * 1e-3)
+
+
 # ---------------------------------------------------------------------------- our arm
 def fresh_prompts(w, step, used):
     """The workload's prompts with step-specific new-token ids.  Requests that diverge from
@@ -294,10 +310,7 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     if eng.device_status() != 0:
         raise RuntimeError(f"device status {eng.device_status()} after timed steps")
-    if world > 1:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+    ms, ms_e2e = reduce_max([ms, ms_e2e], world, dev)
     att_ms = [a.elapsed_time(b) for a, b in att_ev]
     work = algorithmic_work(w)
     hbm, bf16, bf16_s, src = load_peaks()
@@ -330,7 +343,7 @@ def run_ours(args, rank, world, local_rank):
                             "profiles/traffic.json)" if traffic is not None else
                             "null: no ncu capture recorded for these kernel sources")
     tokens = T * args.steps * world
-    value = tokens / (ms * 1e-3)
+    value = replica_throughput(T, args.steps, world, ms)
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = out_h.numel() * out_h.element_size()
     cpu = None
@@ -346,7 +359,8 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": replica_throughput(T, args.steps, world, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
         "gpu_launches": launches[0] // 2,   # per timed region (value); the e2e region launches as many
         "clocks": clk,
         "radix_stats": eng.tree.stats(),
@@ -380,6 +394,11 @@ def oracle_step(w, rows_per_request=None):
     return done, oracle.max_threads()
 
 
+# Rows per request in one reference step (None = every new row): full steps where the oracle
+# finishes one in about a second or two, a bounded sample of each request's rows otherwise.
+REF_ROWS = {"c3": 8, "c5": 2}
+
+
 def cpu_baseline(w, seconds):
     """Time the oracle (as it stands) on the host cores on a bounded sample of the step."""
     import oracle
@@ -388,8 +407,8 @@ def cpu_baseline(w, seconds):
     toks, reps = 0, 0
     rows = None
     s = w.spec
-    if s.name in ("c3", "c5"):
-        rows = 8            # a few rows per request: full rows would take minutes to hours
+    if s.name in REF_ROWS:
+        rows = REF_ROWS[s.name]   # a few rows per request: full rows would take minutes to hours
     while True:
         n, thr = oracle_step(w, rows)
         toks += n
@@ -403,29 +422,33 @@ def cpu_baseline(w, seconds):
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the oracle, as it stands, on the host cores (rank 0 only)."""
     if rank != 0:
         return
+    import oracle
+    oracle.build()
     spec = W.config(args.workload)
     w = W.generate(spec)
-    cb = cpu_baseline(w, args.cpu_seconds)
+    rows = REF_ROWS.get(spec.name)
     for _ in range(args.warmup):
-        pass
-    # the reference arm is the oracle: steps are bounded samples of the workload
+        oracle_step(w, rows)
     t0 = time.perf_counter()
     toks = 0
-    rows = 8 if spec.name in ("c3", "c5") else None
+    thr = 1
     for _ in range(args.steps):
-        n, _thr = oracle_step(w, rows)
+        n, thr = oracle_step(w, rows)
         toks += n
     dt = time.perf_counter() - t0
     v = toks / dt
+    sample = (f"{args.steps} oracle steps of {spec.name} (list matcher + fp64 attention of every new row)"
+              if rows is None else
+              f"{args.steps} oracle steps of {spec.name}, each the first {rows} new rows of every request")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": f"{spec.name}: {spec.note}", "batch": w.batch,
                        "sample": "full step" if rows is None else f"first {rows} new rows per request"},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
-                             "sample": cb["sample"]},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

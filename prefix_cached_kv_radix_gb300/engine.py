@@ -61,18 +61,23 @@ _GROUP_MODE = {False: api.RX_GROUPS_NONE, None: api.RX_GROUPS_NONE, True: api.RX
 
 class PrefixCacheEngine:
     def __init__(self, dtype: str, hq: int, hkv: int, head_dim: int, num_slots: int, seed: int,
-                 device: str = "cuda", poison: bool = True):
+                 device: str = "cuda", poison: bool = True, num_layers: int = 1):
+        """One radix tree over `num_layers` layers' KV pools: a cached token has one slot, and
+        every layer keeps that token's K/V at the same slot of its own pool (the tree, the
+        plan, the slot table and the index upload are shared by the layers of a step)."""
         self.dtype = dtype
         self.tdtype = torch.float32 if dtype == "f32" else torch.bfloat16
         self.hq, self.hkv, self.d = hq, hkv, head_dim
         self.num_slots = num_slots
         self.device = torch.device(device)
         self.tree = api.RadixTree(num_slots, seed)
-        self.k_pool = torch.empty(num_slots, hkv, head_dim, dtype=self.tdtype, device=self.device)
-        self.v_pool = torch.empty_like(self.k_pool)
+        self.num_layers = num_layers
+        self.k_pools = torch.empty(num_layers, num_slots, hkv, head_dim, dtype=self.tdtype, device=self.device)
+        self.v_pools = torch.empty_like(self.k_pools)
         if poison:   # unused slots hold NaN so that any stray gather shows up
-            self.k_pool.fill_(float("nan"))
-            self.v_pool.fill_(float("nan"))
+            self.k_pools.fill_(float("nan"))
+            self.v_pools.fill_(float("nan"))
+        self.k_pool, self.v_pool = self.k_pools[0], self.v_pools[0]   # layer 0 (single-layer use)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.desc = api.make_desc(api.RX_F32 if dtype == "f32" else api.RX_BF16, hq, hkv, head_dim, num_slots,
                                   1.0 / float(np.sqrt(head_dim)))
@@ -100,20 +105,24 @@ class PrefixCacheEngine:
     # ------------------------------------------------------------------ cached history
     def populate(self, tokens: np.ndarray, k, v) -> int:
         """Cache one earlier sequence: match, allocate the uncached tail, write its K/V,
-        insert.  k, v: [len, hkv, d] for the whole sequence (host arrays or device tensors).
-        Returns the number of tokens newly written."""
+        insert.  k, v: [len, hkv, d] for the whole sequence (host arrays or device tensors),
+        or lists of those, one per layer.  Returns the number of tokens newly written."""
         tokens = np.ascontiguousarray(tokens, np.int32)
         slots, m, _ = self.tree.match_prefix(tokens)
         n = len(tokens) - m
         if n == 0:
             return 0
         new = self.tree.alloc_slots(n)
-        kn = k[m:] if isinstance(k, torch.Tensor) else _dev_from_host(k[m:], self.dtype, self.device)
-        vn = v[m:] if isinstance(v, torch.Tensor) else _dev_from_host(v[m:], self.dtype, self.device)
+        ks = k if isinstance(k, (list, tuple)) else [k]
+        vs = v if isinstance(v, (list, tuple)) else [v]
+        assert len(ks) == len(vs) <= self.num_layers
         r2t = torch.empty(1, len(tokens), dtype=torch.int32, device=self.device)
-        api.kv_pool_write(self.desc, 1, self._i32(slots if m else [0]), self._i64([0, m]), self._i32(new),
-                          self._i64([0, n]), kn.contiguous(), vn.contiguous(), self.k_pool, self.v_pool, r2t, n,
-                          self.status)
+        ps, pi, ns, qi = self._i32(slots if m else [0]), self._i64([0, m]), self._i32(new), self._i64([0, n])
+        for layer, (kl, vl) in enumerate(zip(ks, vs)):
+            kn = kl[m:] if isinstance(kl, torch.Tensor) else _dev_from_host(kl[m:], self.dtype, self.device)
+            vn = vl[m:] if isinstance(vl, torch.Tensor) else _dev_from_host(vl[m:], self.dtype, self.device)
+            api.kv_pool_write(self.desc, 1, ps, pi, ns, qi, kn.contiguous(), vn.contiguous(), self.k_pools[layer],
+                              self.v_pools[layer], r2t, n, self.status)
         dup, _ = self.tree.insert(tokens, np.concatenate([slots, new]))
         if dup > m:
             self.tree.free_slots(new[: dup - m])
@@ -201,13 +210,13 @@ class PrefixCacheEngine:
         out["stride"] = plan.stride
         return out
 
-    def write(self, plan: StepPlan, dev: dict, k_new, v_new, stream=None) -> None:
-        """a3: slot table + scatter of the new tokens' K/V."""
+    def write(self, plan: StepPlan, dev: dict, k_new, v_new, stream=None, layer: int = 0) -> None:
+        """a3: slot table + scatter of the new tokens' K/V into `layer`'s pools."""
         api.kv_pool_write(self.desc, plan.batch, dev["prefix_slots"], dev["prefix_indptr"], dev["new_slots"],
-                          dev["qo_indptr"], k_new, v_new, self.k_pool, self.v_pool, dev["r2t"],
+                          dev["qo_indptr"], k_new, v_new, self.k_pools[layer], self.v_pools[layer], dev["r2t"],
                           int(plan.qo_indptr[-1]), self.status, stream or self._stream.cuda_stream)
 
-    def extend(self, plan: StepPlan, dev: dict, q, out, lse=None, stream=None) -> None:
+    def extend(self, plan: StepPlan, dev: dict, q, out, lse=None, stream=None, layer: int = 0) -> None:
         """a4: new tokens attend to their cached prefix and causally to themselves (with the
         plan's shared-prefix groups, if any: shared run once per group, stacked rows)."""
         grp = self.groups(plan, dev)
@@ -218,7 +227,7 @@ class PrefixCacheEngine:
                 self._ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
             ws = self._ws
         api.prefix_extend_attention(self.desc, plan.batch, q, dev["qo_indptr"], dev["prefix_lens"], dev["r2t"],
-                                    self.k_pool, self.v_pool, out, lse, plan.max_qo_len, self.status,
+                                    self.k_pools[layer], self.v_pools[layer], out, lse, plan.max_qo_len, self.status,
                                     groups=grp, workspace=ws, stream=stream or self._stream.cuda_stream)
 
     def groups(self, plan: StepPlan, dev: dict):
@@ -236,10 +245,11 @@ class PrefixCacheEngine:
             self._ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
         return self._ws
 
-    def decode(self, plan: StepPlan, dev: dict, q, out, lse=None, groups=None, stream=None) -> None:
+    def decode(self, plan: StepPlan, dev: dict, q, out, lse=None, groups=None, stream=None, layer: int = 0) -> None:
         """a5 + a6: one query token per request over all of its cached tokens."""
         ws = self.decode_workspace(plan, groups)
-        api.decode_attention(self.desc, plan.batch, q, dev["r2t"], dev["kv_lens"], self.k_pool, self.v_pool, out,
+        api.decode_attention(self.desc, plan.batch, q, dev["r2t"], dev["kv_lens"], self.k_pools[layer],
+                             self.v_pools[layer], out,
                              lse, plan.max_kv_len, ws, self.status, groups=groups,
                              stream=stream or self._stream.cuda_stream)
 

@@ -1,0 +1,146 @@
+"""A multi-layer causal model on the GPU through the library: prefill, extend and decode.
+
+"Prompt Caching" (Ultralytics glossary), "How prompt caching works": the GPT-2 example
+prefills a 409-token system prompt once, runs each question's tokens alone on top of the
+cached keys/values ("Computed 8 of 417 tokens", "Computed 7 of 416 tokens") and finds the
+last position's next-token scores equal to a full recomputation (allclose, atol 1e-3).
+
+Here the oracle's random-weight ToyCausalLM (2 layers, 4 heads of 64) runs on the GPU: torch
+for the dense parts (embeddings, layer norms, projections, MLP, head), the library for every
+layer's KV cache and attention (one radix tree, one K/V pool per layer, kv_pool_write,
+prefix_extend_attention, decode_attention).  Its scores are compared with an uncached GPU run
+of the same model and with the oracle's own fp64 forward.
+"""
+import copy
+import json
+import os
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "prompt_caching_gpt2_counts.json")
+VOCAB, D_MODEL, HEADS = 4096, 256, 4
+
+
+def _ln(x):
+    mu = x.mean(-1, keepdim=True)
+    var = ((x - mu) ** 2).mean(-1, keepdim=True)
+    return (x - mu) / torch.sqrt(var + 1e-5)
+
+
+def _gelu(x):
+    return 0.5 * x * (1.0 + torch.tanh(float(np.sqrt(2.0 / np.pi)) * (x + 0.044715 * x ** 3)))
+
+
+class GpuToyLM:
+    """ToyCausalLM's weights on the GPU; attention and the KV cache through the library."""
+
+    def __init__(self, oracle_model, dtype: str, num_slots: int = 8192, seed: int = 5):
+        from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine
+        dev = torch.device("cuda")
+        f = lambda a: torch.tensor(a, dtype=torch.float32, device=dev)
+        self.wte, self.wpe = f(oracle_model.wte), f(oracle_model.wpe)
+        self.layers = [{k: f(v) for k, v in L.items()} for L in oracle_model.layers]
+        self.h, self.dh = oracle_model.h, oracle_model.dh
+        self.adt = torch.float32 if dtype == "f32" else torch.bfloat16
+        self.eng = PrefixCacheEngine(dtype, self.h, self.h, self.dh, num_slots, seed, poison=True,
+                                     num_layers=len(self.layers))
+        self.computed = 0
+
+    def step(self, prompts, n_new, decode=False):
+        """One batch step: every prompt's last n_new[b] tokens are uncached and run now.
+        Returns the logits of those rows (concatenated) and the plan."""
+        eng = self.eng
+        plan = eng.plan(prompts, n_new)
+        dev = eng.upload(plan)
+        ids = np.concatenate([p[len(p) - n:] for p, n in zip(prompts, n_new)])
+        pos = np.concatenate([np.arange(len(p) - n, len(p)) for p, n in zip(prompts, n_new)])
+        x = self.wte[torch.as_tensor(ids, device="cuda")] + self.wpe[torch.as_tensor(pos, device="cuda")]
+        T = len(ids)
+        for li, L in enumerate(self.layers):
+            hdn = _ln(x)
+            q = (hdn @ L["wq"]).reshape(T, self.h, self.dh).to(self.adt).contiguous()
+            k = (hdn @ L["wk"]).reshape(T, self.h, self.dh).to(self.adt).contiguous()
+            v = (hdn @ L["wv"]).reshape(T, self.h, self.dh).to(self.adt).contiguous()
+            eng.write(plan, dev, k, v, layer=li)
+            out = torch.empty_like(q)
+            if decode:
+                eng.decode(plan, dev, q, out, layer=li)
+            else:
+                eng.extend(plan, dev, q, out, layer=li)
+            x = x + out.float().reshape(T, -1) @ L["wo"]
+            x = x + _gelu(_ln(x) @ L["w1"]) @ L["w2"]
+        logits = _ln(x) @ self.wte.T
+        eng.finish(plan, 0)
+        torch.cuda.synchronize()
+        assert eng.device_status() == 0
+        self.computed += T
+        return logits.double().cpu().numpy(), plan
+
+
+def _oracle():
+    from oracle.toy_model import ToyCausalLM
+    return ToyCausalLM(seed=409, vocab=VOCAB, d_model=D_MODEL, n_heads=HEADS, n_layers=2)
+
+
+@pytest.mark.parametrize("dtype,tol_oracle", [("f32", 1e-4), ("bf16", 2e-2)])
+def test_cached_prompt_scores_equal_full_recompute(dtype, tol_oracle):
+    g = json.load(open(GOLDEN))
+    om = _oracle()
+    rng = np.random.default_rng(2024)
+    prefix = rng.integers(0, VOCAB, size=g["prefix_tokens"]).astype(np.int32)
+    m = GpuToyLM(om, dtype)
+    m.step([prefix], [len(prefix)])                    # prefill: the system prompt is cached once
+    assert m.eng.tree.stats()["cached_tokens"] == len(prefix)
+    _, cache = om.forward(prefix)
+    for case in g["cases"]:
+        qtok = rng.integers(0, VOCAB, size=case["computed"]).astype(np.int32)
+        prompt = np.concatenate([prefix, qtok])
+        cached, plan = m.step([prompt], [len(qtok)])
+        # "Computed n of N tokens": only the question ran; the prefix came from the cache
+        assert int(plan.prefix_lens[0]) == len(prefix) and len(qtok) + len(prefix) == case["total"]
+        # uncached GPU run of the same model: a fresh cache, the whole prompt computed
+        fresh = GpuToyLM(om, dtype, seed=6)
+        full_gpu, _ = fresh.step([prompt], [len(prompt)])
+        same = bool(np.allclose(cached[-1], full_gpu[-1], atol=g["atol"]))
+        assert same == case["same_next_token_scores"]
+        np.testing.assert_allclose(cached, full_gpu[len(prefix):], atol=g["atol"], rtol=0)
+        # and the oracle's fp64 forward over the whole prompt
+        full_ref, _ = om.forward(prompt)
+        np.testing.assert_allclose(cached, full_ref[len(prefix):], atol=tol_oracle, rtol=0)
+        # the oracle's own cached run agrees with the GPU's cached run too
+        ref_cached, _ = om.forward(qtok, past=copy.deepcopy(cache))
+        np.testing.assert_allclose(cached, ref_cached, atol=tol_oracle, rtol=0)
+    m.eng.tree.check()
+
+
+@pytest.mark.parametrize("dtype,tol_oracle", [("f32", 1e-4), ("bf16", 2e-2)])
+def test_batched_decode_after_shared_prefill(dtype, tol_oracle):
+    """Three requests share a cached prompt, extend with their own questions in one batch,
+    then decode greedily token by token (decode_attention), all against the oracle."""
+    om = _oracle()
+    rng = np.random.default_rng(11)
+    prefix = rng.integers(0, VOCAB, size=200).astype(np.int32)
+    m = GpuToyLM(om, dtype)
+    m.step([prefix], [len(prefix)])
+    seqs = [np.concatenate([prefix, rng.integers(0, VOCAB, size=n).astype(np.int32)]) for n in (5, 9, 3)]
+    logits, plan = m.step(seqs, [5, 9, 3])
+    assert plan.prefix_lens.tolist() == [200, 200, 200]
+    ends = np.cumsum([5, 9, 3]) - 1
+    for step in range(4):
+        nxt = [int(np.argmax(logits[e])) for e in ends]
+        # compare this step's last-row scores with the oracle's full forward of each sequence
+        for b, s in enumerate(seqs):
+            ref, _ = om.forward(s)
+            np.testing.assert_allclose(logits[ends[b]], ref[-1], atol=tol_oracle, rtol=0)
+        seqs = [np.concatenate([s, [t]]).astype(np.int32) for s, t in zip(seqs, nxt)]
+        logits, plan = m.step(seqs, [1, 1, 1], decode=True)
+        ends = np.arange(3)
+    for b, s in enumerate(seqs):
+        ref, _ = om.forward(s)
+        np.testing.assert_allclose(logits[b], ref[-1], atol=tol_oracle, rtol=0)
+    m.eng.tree.check()

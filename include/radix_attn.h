@@ -108,6 +108,17 @@ void radix_destroy(rx_radix* t);
 int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slots,
                  int64_t* out_len, rx_node* out_last);
 
+/* Length of the longest cached prefix of tokens[0:n], read-only: no LRU stamp, no split, no
+ * statistics.  A scheduler uses it to order waiting requests by how much of each is cached
+ * (cache-aware scheduling, "SGLang: Efficient Execution of Structured Language Model
+ * Programs", results on cache hit rates).  *out_len = the length match_prefix would return now. */
+int match_prefix_len(const rx_radix* t, const int32_t* tokens, int64_t n, int64_t* out_len);
+
+/* match_prefix_len for `batch` requests: request b is tokens[tok_indptr[b] : tok_indptr[b+1]];
+ * out_len has capacity batch. */
+int match_prefix_len_batch(const rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
+                           int64_t* out_len);
+
 /* Pin / unpin the path from the root to a node so that evict never frees it
  * (reference counted along the whole path).  RX_ELOCKED if unlocking an unlocked node. */
 int radix_lock(rx_radix* t, rx_node node);

@@ -20,7 +20,7 @@ RX_DEV_OK, RX_DEV_BAD_SLOT, RX_DEV_BAD_LENGTH, RX_DEV_TIMEOUT = 0, 1, 2, 3
 RX_F32, RX_BF16 = 0, 1
 RX_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20   # include/radix_attn.h
 
-EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "radix_lock", "radix_unlock", "alloc_slots",
+EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "match_prefix_len", "match_prefix_len_batch", "radix_lock", "radix_unlock", "alloc_slots",
            "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "insert_batch_at", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups", "rx_step_stage_bytes", "rx_step_plan", "rx_step_finish",
@@ -86,6 +86,8 @@ def load(path: str = LIB_PATH):
         "radix_create": (ctypes.c_int, [I64, U64, P]),
         "radix_destroy": (None, [P]),
         "match_prefix": (ctypes.c_int, [P, P, I64, P, P, P]),
+        "match_prefix_len": (ctypes.c_int, [P, P, I64, P]),
+        "match_prefix_len_batch": (ctypes.c_int, [P, I32, P, P, P]),
         "radix_lock": (ctypes.c_int, [P, I64]),
         "radix_unlock": (ctypes.c_int, [P, I64]),
         "alloc_slots": (ctypes.c_int, [P, I64, P]),
@@ -175,6 +177,24 @@ def match_prefix(tree, tokens):
     _check("match_prefix", load().match_prefix(tree, tok.ctypes.data, len(tok), out.ctypes.data,
                                                ctypes.byref(n), ctypes.byref(last)))
     return out[: n.value].copy(), n.value, last.value
+
+
+def match_prefix_len(tree, tokens) -> int:
+    """Length of the longest cached prefix, without touching the tree (no stamp, no split)."""
+    tok = _np_i32(tokens)
+    n = I64()
+    _check("match_prefix_len", load().match_prefix_len(tree, tok.ctypes.data, len(tok), ctypes.byref(n)))
+    return n.value
+
+
+def match_prefix_len_batch(tree, tokens, tok_indptr) -> np.ndarray:
+    tok = _np_i32(tokens)
+    ind = np.ascontiguousarray(np.asarray(tok_indptr, np.int64))
+    b = len(ind) - 1
+    out = np.empty(max(b, 1), np.int64)
+    _check("match_prefix_len_batch", load().match_prefix_len_batch(tree, b, tok.ctypes.data, ind.ctypes.data,
+                                                                   out.ctypes.data))
+    return out[:b].copy()
 
 
 def radix_lock(tree, node: int) -> None:
@@ -344,6 +364,12 @@ class RadixTree:
 
     def insert(self, tokens, slots):
         return insert(self.h, tokens, slots)
+
+    def match_prefix_len(self, tokens):
+        return match_prefix_len(self.h, tokens)
+
+    def match_prefix_len_batch(self, tokens, tok_indptr):
+        return match_prefix_len_batch(self.h, tokens, tok_indptr)
 
     def evict(self, n, cap=None):
         return evict(self.h, n, cap)

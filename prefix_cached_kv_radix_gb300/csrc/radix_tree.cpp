@@ -221,6 +221,36 @@ int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slo
     return RX_OK;
 }
 
+int match_prefix_len(const rx_radix* t, const int32_t* tokens, int64_t n, int64_t* out_len) {
+    RX_REQUIRE(t && out_len && n >= 0 && (n == 0 || tokens), "match_prefix_len: bad arguments");
+    const rx::Node* x = &t->root;
+    int64_t pos = 0;
+    while (pos < n) {                       // the walk of match_prefix, without split or stamp
+        auto it = x->children.find(tokens[pos]);
+        if (it == x->children.end()) break;
+        const rx::Node* c = it->second;
+        const int64_t len = (int64_t)c->key.size();
+        const int64_t k = rx::common_prefix(c->key.data(), tokens + pos, 1, std::min<int64_t>(len, n - pos));
+        pos += k;
+        if (k < len) break;
+        x = c;
+    }
+    *out_len = pos;
+    return RX_OK;
+}
+
+int match_prefix_len_batch(const rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
+                           int64_t* out_len) {
+    RX_REQUIRE(t && batch >= 0 && tok_indptr && (batch == 0 || out_len), "match_prefix_len_batch: bad arguments");
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t n = tok_indptr[b + 1] - tok_indptr[b];
+        RX_REQUIRE(n >= 0, "match_prefix_len_batch: request %d has a negative length", b);
+        const int rc = match_prefix_len(t, tokens + tok_indptr[b], n, out_len + b);
+        if (rc != RX_OK) return rc;
+    }
+    return RX_OK;
+}
+
 int radix_lock(rx_radix* t, rx_node node) {
     RX_REQUIRE(t, "radix_lock: tree is NULL");
     auto it = t->by_id.find(node);

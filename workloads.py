@@ -330,3 +330,61 @@ def config(name: str) -> Spec:
 
 
 CONFIG_NAMES = ("c1", "c2", "c3", "c4", "c5")
+
+
+# ---------------------------------------------------------------------------- request traces
+@dataclass
+class Session:
+    """One conversation: a shared prefix (system prompt or few-shot block, by id), then turns
+    of (user tokens, reply tokens).  Turn t's request is prefix + every earlier turn's user and
+    reply tokens + turn t's user tokens; its reply is generated after it."""
+    prefix_id: int
+    start: int                       # arrival step of the first turn
+    turns: list = field(default_factory=list)
+
+
+@dataclass
+class Trace:
+    prefixes: list                   # token arrays, by prefix id
+    sessions: list                   # Session
+
+    def request(self, s: int, t: int) -> np.ndarray:
+        ses = self.sessions[s]
+        parts = [self.prefixes[ses.prefix_id]]
+        for u, r in ses.turns[:t]:
+            parts += [u, r]
+        parts.append(ses.turns[t][0])
+        return np.concatenate(parts).astype(np.int32)
+
+    def sequence(self, s: int, t: int) -> np.ndarray:
+        """The request followed by its reply: what the cache holds once the turn is done."""
+        return np.concatenate([self.request(s, t), self.sessions[s].turns[t][1]]).astype(np.int32)
+
+
+def chat_trace(seed: int, vocab: int = 151936, n_system: int = 4, n_fewshot: int = 3, n_chats: int = 48,
+               n_questions: int = 96, horizon: int = 64, scale: int = 1) -> Trace:
+    """Seeded request trace in the shape of the "SGLang" page's walk-through: chat sessions that
+    share a few system prompts and grow turn by turn (each turn's prompt holds the whole
+    conversation so far), and few-shot question sets that share a long examples block.  Token
+    ids are uniform; lengths are uniform in the ranges below; arrivals are uniform over
+    `horizon` steps; `scale` divides every length (small traces for exhaustive checks)."""
+    rng = _rng(seed, 31)
+
+    def n(lo, hi):
+        return int(rng.integers(max(lo // scale, 1), max(hi // scale, 1) + 1))
+
+    prefixes = [rng.integers(0, vocab, size=n(256, 1024)).astype(np.int32) for _ in range(n_system)]
+    prefixes += [rng.integers(0, vocab, size=n(512, 2048)).astype(np.int32) for _ in range(n_fewshot)]
+    sessions = []
+    for _ in range(n_chats):
+        s = Session(int(rng.integers(0, n_system)), int(rng.integers(0, horizon)))
+        for _t in range(int(rng.integers(2, 7))):
+            s.turns.append((rng.integers(0, vocab, size=n(16, 128)).astype(np.int32),
+                            rng.integers(0, vocab, size=n(32, 256)).astype(np.int32)))
+        sessions.append(s)
+    for _ in range(n_questions):
+        s = Session(n_system + int(rng.integers(0, n_fewshot)), int(rng.integers(0, horizon)))
+        s.turns.append((rng.integers(0, vocab, size=n(16, 64)).astype(np.int32),
+                        rng.integers(0, vocab, size=n(8, 32)).astype(np.int32)))
+        sessions.append(s)
+    return Trace(prefixes, sessions)

@@ -48,13 +48,13 @@ def load_peaks():
 
 # ---------------------------------------------------------------------------- ncu traffic
 def kernel_source_hash() -> str:
-    """Digest of the CUDA/C++ sources the library is built from: DRAM counters recorded for
-    one version of the kernels are reported only while the sources are unchanged."""
+    """Digest of the kernel sources (CUDA files and the headers they include): DRAM counters
+    recorded for one version of the kernels are reported only while those are unchanged."""
     import hashlib
     csrc = os.path.join(ROOT, "prefix_cached_kv_radix_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+        if f.endswith((".cu", ".cuh", ".h")):
             h.update(f.encode())
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]

@@ -114,6 +114,17 @@ int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slo
  * Programs", results on cache hit rates).  *out_len = the length match_prefix would return now. */
 int match_prefix_len(const rx_radix* t, const int32_t* tokens, int64_t n, int64_t* out_len);
 
+/* Reuse granularity (default 1 = token granular, as RadixAttention keeps it): with a page
+ * size p > 1, every match (match_prefix, match_prefix_batch, match_prefix_len, rx_step_plan)
+ * counts whole pages only -- the cached prefix cut down to a multiple of p, ending (split,
+ * stamped) at that page boundary -- as a cache of fixed-size pages can reuse only full pages
+ * (the aiezz OpenJev-on-SGLang tutorial, advanced serving tips, the tip on treating cache
+ * reuse as an opportunity: cache page boundaries are one of the things that cut hits).
+ * Storage stays token granular: the tail of a partly matched page is recomputed and its new
+ * slots are returned as duplicates when inserted.
+ * RX_EINVAL outside [1, 2^20]. */
+int radix_set_page_size(rx_radix* t, int64_t page_size);
+
 /* match_prefix_len for `batch` requests: request b is tokens[tok_indptr[b] : tok_indptr[b+1]];
  * out_len has capacity batch. */
 int match_prefix_len_batch(const rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,

@@ -20,7 +20,8 @@ RX_DEV_OK, RX_DEV_BAD_SLOT, RX_DEV_BAD_LENGTH, RX_DEV_TIMEOUT = 0, 1, 2, 3
 RX_F32, RX_BF16 = 0, 1
 RX_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20   # include/radix_attn.h
 
-EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "match_prefix_len", "match_prefix_len_batch", "radix_lock", "radix_unlock", "alloc_slots",
+EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "match_prefix_len", "match_prefix_len_batch", "radix_set_page_size",
+           "radix_lock", "radix_unlock", "alloc_slots",
            "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "insert_batch_at", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups", "rx_step_stage_bytes", "rx_step_plan", "rx_step_finish",
@@ -88,6 +89,7 @@ def load(path: str = LIB_PATH):
         "match_prefix": (ctypes.c_int, [P, P, I64, P, P, P]),
         "match_prefix_len": (ctypes.c_int, [P, P, I64, P]),
         "match_prefix_len_batch": (ctypes.c_int, [P, I32, P, P, P]),
+        "radix_set_page_size": (ctypes.c_int, [P, I64]),
         "radix_lock": (ctypes.c_int, [P, I64]),
         "radix_unlock": (ctypes.c_int, [P, I64]),
         "alloc_slots": (ctypes.c_int, [P, I64, P]),
@@ -195,6 +197,10 @@ def match_prefix_len_batch(tree, tokens, tok_indptr) -> np.ndarray:
     _check("match_prefix_len_batch", load().match_prefix_len_batch(tree, b, tok.ctypes.data, ind.ctypes.data,
                                                                    out.ctypes.data))
     return out[:b].copy()
+
+
+def radix_set_page_size(tree, page_size: int) -> None:
+    _check("radix_set_page_size", load().radix_set_page_size(tree, page_size))
 
 
 def radix_lock(tree, node: int) -> None:
@@ -350,9 +356,12 @@ def rx_step_finish(tree, tokens: np.ndarray, tok_indptr: np.ndarray, last_nodes:
 class RadixTree:
     """Owning wrapper of an rx_radix handle."""
 
-    def __init__(self, num_slots: int, seed: int):
+    def __init__(self, num_slots: int, seed: int, page_size: int = 1):
         self.h = radix_create(num_slots, seed)
         self.num_slots = num_slots
+        self.page_size = page_size
+        if page_size != 1:
+            radix_set_page_size(self.h, page_size)
 
     def __del__(self):
         if getattr(self, "h", None) is not None and _lib is not None:

@@ -88,6 +88,7 @@ struct rx_radix {
     rx::Node root;
     uint64_t clock = 0;
     int64_t next_id = 1;
+    int64_t page = 1;                  // reuse granularity: matches count whole pages only
     std::unordered_map<int64_t, rx::Node*> by_id;
     rx_stats st{};
 
@@ -141,6 +142,33 @@ struct rx_radix {
     // node on it, optionally collect slots.  Returns the matched length; *last = end node.
     int64_t walk(const int32_t* tokens, int64_t n, int32_t* out_slots, rx::Node** last) {
         return walk_from(&root, 0, tokens, n, out_slots, last);
+    }
+
+    // Length of the cached prefix of tokens[0:n], touching nothing.
+    int64_t cached_len(const int32_t* tokens, int64_t n) const {
+        const rx::Node* x = &root;
+        int64_t pos = 0;
+        while (pos < n) {
+            auto it = x->children.find(tokens[pos]);
+            if (it == x->children.end()) break;
+            const rx::Node* c = it->second;
+            const int64_t len = (int64_t)c->key.size();
+            const int64_t k = rx::common_prefix(c->key.data(), tokens + pos, 1, std::min<int64_t>(len, n - pos));
+            pos += k;
+            if (k < len) break;
+            x = c;
+        }
+        return pos;
+    }
+
+    // A request's reusable prefix: the cached prefix, cut down to whole pages when the page
+    // size is above one (the walk then ends, splits and stamps at that page boundary).
+    int64_t match(const int32_t* tokens, int64_t n, int32_t* out_slots, rx::Node** last) {
+        if (page > 1) {
+            const int64_t m = cached_len(tokens, n);
+            n = m - m % page;
+        }
+        return walk(tokens, n, out_slots, last);
     }
 
     // The walk continued from node x, which ends at token position pos of the sequence.
@@ -212,7 +240,7 @@ int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slo
                "match_prefix: bad arguments");
     t->clock += 1;
     rx::Node* last = nullptr;
-    const int64_t m = t->walk(tokens, n, out_slots, &last);
+    const int64_t m = t->match(tokens, n, out_slots, &last);
     t->st.match_calls += 1;
     t->st.match_query_tokens += n;
     t->st.match_hit_tokens += m;
@@ -223,19 +251,15 @@ int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slo
 
 int match_prefix_len(const rx_radix* t, const int32_t* tokens, int64_t n, int64_t* out_len) {
     RX_REQUIRE(t && out_len && n >= 0 && (n == 0 || tokens), "match_prefix_len: bad arguments");
-    const rx::Node* x = &t->root;
-    int64_t pos = 0;
-    while (pos < n) {                       // the walk of match_prefix, without split or stamp
-        auto it = x->children.find(tokens[pos]);
-        if (it == x->children.end()) break;
-        const rx::Node* c = it->second;
-        const int64_t len = (int64_t)c->key.size();
-        const int64_t k = rx::common_prefix(c->key.data(), tokens + pos, 1, std::min<int64_t>(len, n - pos));
-        pos += k;
-        if (k < len) break;
-        x = c;
-    }
-    *out_len = pos;
+    const int64_t m = t->cached_len(tokens, n);
+    *out_len = m - m % t->page;         // the length match_prefix would return now
+    return RX_OK;
+}
+
+int radix_set_page_size(rx_radix* t, int64_t page_size) {
+    RX_REQUIRE(t && page_size >= 1 && page_size <= (1 << 20), "radix_set_page_size: page size %lld out of range",
+               (long long)page_size);
+    t->page = page_size;
     return RX_OK;
 }
 
@@ -508,7 +532,7 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
                    (long long)len, n_new[b]);
         t->clock += 1;
         rx::Node* last = nullptr;
-        const int64_t m = t->walk(tokens + tok_indptr[b], len, ps + acc, &last);
+        const int64_t m = t->match(tokens + tok_indptr[b], len, ps + acc, &last);
         t->st.match_calls += 1;
         t->st.match_query_tokens += len;
         t->st.match_hit_tokens += m;

@@ -61,7 +61,7 @@ _GROUP_MODE = {False: api.RX_GROUPS_NONE, None: api.RX_GROUPS_NONE, True: api.RX
 
 class PrefixCacheEngine:
     def __init__(self, dtype: str, hq: int, hkv: int, head_dim: int, num_slots: int, seed: int,
-                 device: str = "cuda", poison: bool = True, num_layers: int = 1):
+                 device: str = "cuda", poison: bool = True, num_layers: int = 1, page_size: int = 1):
         """One radix tree over `num_layers` layers' KV pools: a cached token has one slot, and
         every layer keeps that token's K/V at the same slot of its own pool (the tree, the
         plan, the slot table and the index upload are shared by the layers of a step)."""
@@ -70,7 +70,7 @@ class PrefixCacheEngine:
         self.hq, self.hkv, self.d = hq, hkv, head_dim
         self.num_slots = num_slots
         self.device = torch.device(device)
-        self.tree = api.RadixTree(num_slots, seed)
+        self.tree = api.RadixTree(num_slots, seed, page_size=page_size)
         self.num_layers = num_layers
         self.k_pools = torch.empty(num_layers, num_slots, hkv, head_dim, dtype=self.tdtype, device=self.device)
         self.v_pools = torch.empty_like(self.k_pools)
@@ -129,6 +129,15 @@ class PrefixCacheEngine:
         return n
 
     # ------------------------------------------------------------------ step
+    def new_token_counts(self, prompts) -> np.ndarray:
+        """How many trailing tokens of each prompt must be computed now: those past its
+        reusable cached prefix (whole pages only when the tree has a page size above one)."""
+        if not len(prompts):
+            return np.zeros(0, np.int64)
+        ind = np.concatenate([[0], np.cumsum([len(p) for p in prompts])]).astype(np.int64)
+        m = self.tree.match_prefix_len_batch(np.concatenate(prompts).astype(np.int32), ind)
+        return np.diff(ind) - m
+
     def plan(self, prompts, n_new, groups: bool = False, min_shared: int = 64) -> StepPlan:
         """a1 + a2 for a list of prompts (see plan_concat)."""
         b = len(prompts)

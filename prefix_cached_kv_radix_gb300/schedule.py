@@ -52,11 +52,12 @@ class TraceResult:
 
 
 def simulate(trace, pool_slots: int, batch: int = 8, policy: str = "fifo", window: int = 64,
-             seed: int = 0) -> TraceResult:
+             seed: int = 0, page_size: int = 1) -> TraceResult:
     """Replay every turn of every session of `trace`; a session's next turn becomes ready the
-    step after its previous turn (its prompt holds that turn's reply)."""
+    step after its previous turn (its prompt holds that turn's reply).  With page_size > 1
+    only whole pages of a match are reused."""
     assert policy in ("fifo", "cache_aware")
-    tree = api.RadixTree(pool_slots, seed)
+    tree = api.RadixTree(pool_slots, seed, page_size=page_size)
     S = len(trace.sessions)
     nxt = [0] * S
     ready_at = [s.start for s in trace.sessions]
@@ -145,6 +146,7 @@ def main():
     longest = max(len(tr.sequence(s, t)) for s in range(len(tr.sessions)) for t in range(len(tr.sessions[s].turns)))
     print(f"trace: {len(tr.sessions)} sessions, {opt.requests} requests, {opt.prompt_tokens} prompt tokens, "
           f"{distinct} distinct tokens; optimal hit rate {opt.hit_rate:.4f}")
+    print()
     print("| pool (share of distinct tokens) | order | hit rate | % of optimal | evicted tokens |")
     print("|---|---|---|---|---|")
     for frac in (0.05, 0.1, 0.25, 0.5, 1.0):
@@ -153,6 +155,16 @@ def main():
             r = simulate(tr, pool, batch=a.batch, policy=pol, window=a.window)
             print(f"| {frac:.2f} ({pool} slots) | {pol} | {r.hit_rate:.4f} | {100 * r.hit_rate / opt.hit_rate:.1f} % | "
                   f"{r.evicted_tokens} |")
+    # reuse granularity: hits lost at page boundaries (cache-aware order)
+    print()
+    print("| page size | pool (share of distinct tokens) | hit rate | % of the token-granular optimum | computed tokens |")
+    print("|---|---|---|---|---|")
+    for frac in (0.5, 1.0):
+        pool = max(int(frac * distinct), a.batch * longest)
+        for page in (1, 4, 16, 64):
+            r = simulate(tr, pool, batch=a.batch, policy="cache_aware", window=a.window, page_size=page)
+            print(f"| {page} | {frac:.2f} | {r.hit_rate:.4f} | {100 * r.hit_rate / opt.hit_rate:.1f} % | "
+                  f"{r.computed_tokens} |")
 
 
 if __name__ == "__main__":

@@ -280,3 +280,59 @@ def test_grouped_equals_ungrouped_extend():
     assert g1 is None and g2 is not None
     assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
     assert (l1 - l2).abs().max().item() <= 1e-3
+
+
+# ---------------------------------------------------------------- page-granular reuse
+@pytest.mark.parametrize("name,page", [("c2", 16), ("c1", 48), ("c2", 64)])
+def test_page_granular_reuse_recomputes_the_partial_page(name, page):
+    """With a page size the cached prefix is reused in whole pages only: the tail of the
+    partly matched page is recomputed (its K/V written again to new slots, its rows
+    attended) and the outputs of every computed row still equal the oracle's."""
+    from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine, _dev_from_host
+    import oracle
+    spec = W.config(name)
+    w = W.generate(spec)
+    s = spec
+    eng = PrefixCacheEngine(s.dtype, s.hq, s.hkv, s.d, s.num_slots, s.seed, page_size=page)
+    for i in range(len(s.histories)):
+        k, v = w.history_kv(i)
+        eng.populate(w.history_tokens(i), k, v)
+    prompts = [w.request_tokens(b) for b in range(w.batch)]
+    n_new = eng.new_token_counts(prompts)
+    P_r = np.array([len(p) for p in prompts]) - n_new
+    assert (P_r % page == 0).all() and (P_r <= np.array(s.req_cached)).all()
+    assert (P_r < np.array(s.req_cached)).any()          # some prefix tails are recomputed
+    rng = np.random.default_rng(99)
+    qs, ks, vs, rows = [], [], [], []
+    for b in range(w.batch):
+        kf, vf = w.request_kv(b)
+        lo, P = int(P_r[b]), s.req_cached[b]
+        extra_q = rng.standard_normal((P - lo, s.hq, s.d)).astype(np.float32)
+        if s.dtype == "bf16":
+            extra_q = W.f32_to_bf16_bits(extra_q)
+        qs.append(np.concatenate([extra_q, w.req_q[b]]))
+        ks.append(kf[lo:])
+        vs.append(vf[lo:])
+        rows.append((lo, qs[-1]))
+    plan = eng.plan(prompts, n_new)
+    assert np.array_equal(plan.prefix_lens, P_r)
+    dev = eng.upload(plan)
+    qd, kd, vd = (_dev_from_host(np.concatenate(x), s.dtype, eng.device) for x in (qs, ks, vs))
+    out = torch.empty_like(qd)
+    eng.write(plan, dev, kd, vd)
+    eng.extend(plan, dev, qd, out, None)
+    free_before = eng.tree.stats()["free_slots"]
+    eng.finish(plan)
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
+    # the recomputed tail's new slots came back as duplicates
+    assert eng.tree.stats()["free_slots"] - free_before == int((np.array(s.req_cached) - P_r).sum())
+    got = to_host_f32(out)
+    qo = np.concatenate([[0], np.cumsum(n_new)])
+    for b in range(w.batch):
+        kf, vf = w.request_kv(b)
+        lo, qb = rows[b]
+        want, _ = oracle.attention_rows(f32(qb, s.dtype), lo + np.arange(len(qb)), f32(kf, s.dtype),
+                                        f32(vf, s.dtype), s.scale)
+        compare(got[qo[b]:qo[b + 1]], want, f"{name} page {page} request {b}")
+    eng.tree.check()

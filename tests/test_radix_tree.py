@@ -219,3 +219,38 @@ def test_insert_batch_at_equals_insert_batch():
             t1.check()
             k = int(rng.integers(1, 20))
             assert t1.evict(k).tolist() == t2.evict(k).tolist()
+
+
+def test_page_granular_matches_against_oracle():
+    """With a page size p the tree reuses whole pages only: every match is the oracle's cached
+    length cut down to a multiple of p, and inserts stay token granular."""
+    for p in (2, 4, 16):
+        rng = np.random.default_rng(30 + p)
+        t = api.RadixTree(2048, p, page_size=p)
+        m = PrefixCacheModel(2048, p)
+        for _ in range(60):
+            q = rng.integers(0, 3, size=int(rng.integers(1, 40))).astype(np.int32)
+            want = m._cached_len(list(q))
+            want -= want % p
+            assert t.match_prefix_len(q) == want
+            slots, k, _ = t.match_prefix(q)
+            assert k == want
+            k2, s2 = m.match(list(q)[:want])        # the oracle's match of the whole pages
+            assert k2 == want and slots.tolist() == s2.tolist()
+            if t.stats()["free_slots"] >= len(q):
+                new = t.alloc_slots(len(q) - k)
+                new2 = m.alloc.alloc(len(q) - k)
+                assert new.tolist() == new2.tolist()
+                d, _ = t.insert(q, np.concatenate([slots, new]))
+                d2 = m.insert(list(q), np.concatenate([s2, new2]))
+                assert d == d2 >= k
+                t.free_slots(new[: d - k])          # the recomputed tail of the partial page
+                m.alloc.release(new2[: d2 - k])
+            if rng.random() < 0.2:
+                k_ev = int(rng.integers(1, 20))
+                assert t.evict(k_ev).tolist() == m.evict(k_ev).tolist()
+            st = t.stats()
+            assert st["cached_tokens"] == m.cached_tokens() and st["free_slots"] == len(m.alloc.free)
+            t.check()
+    with pytest.raises(api.RxError):
+        api.radix_set_page_size(api.RadixTree(8, 0).h, 0)

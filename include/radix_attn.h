@@ -217,7 +217,8 @@ size_t rx_step_stage_bytes(int32_t batch, int64_t total_tokens);
  * (out_last[b], capacity batch) until rx_step_finish.  group_mode: RX_GROUPS_NONE, _ALWAYS
  * (radix_shared_groups with min_shared) or _AUTO (only when every request is in a group, its
  * remaining keys are <= 256 and a request's new rows times heads_per_kv stay below 128 --
- * the shape where stacking rows pays). */
+ * the shape where stacking rows pays -- and not when every request has at most 8 rows
+ * (new tokens x heads_per_kv) over at most 1024 keys, which the small-extend kernel serves). */
 int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
                  const int32_t* n_new, int32_t group_mode, int32_t heads_per_kv, int64_t min_shared,
                  void* h_stage, size_t stage_cap, rx_node* out_last, rx_step_layout* out);
@@ -364,6 +365,44 @@ int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
                              const void* d_k_pool, const void* d_v_pool,
                              void* d_out, float* d_lse, int32_t max_kv_len,
                              int32_t* d_status, void* stream);
+
+/* ------------------------------------------------------------------ one-call step launch
+ * Everything of a planned step that follows rx_step_plan, in one call: one H2D copy of the
+ * staging buffer (h_stage) to its device copy (io->d_stage), kv_pool_write (a3), the
+ * attention -- prefix_extend_attention (a4), or decode_attention (a5/a6) when io->decode --
+ * with the plan's shared-prefix groups, and rx_step_finish (a7/a8: insert, free duplicates,
+ * evict evict_tokens, unpin; host only, it does not wait for the GPU).  All device work is
+ * enqueued on `stream`.  Device buffers are the caller's: the rows of the step's new tokens
+ * (d_q, d_k_new, d_v_new: [T, hq|hkv, head_dim] in qo_indptr order), d_out (and optional
+ * d_lse), the pools, d_stage (>= layout bytes), d_r2t (>= batch * stride int32) and
+ * d_workspace (>= rx_step_workspace_bytes).  After the call the staging buffer is still
+ * being read by the copy: call rx_stage_wait(h_stage) before planning into it again.
+ * Returns RX_EINVAL (nothing launched, the plan still pinned) when a buffer is too small;
+ * a launch failure returns RX_ECUDA; *out_evicted (may be NULL) receives the evicted count. */
+typedef struct {
+    const void* d_q;
+    const void* d_k_new;
+    const void* d_v_new;
+    void* d_k_pool;
+    void* d_v_pool;
+    void* d_out;
+    float* d_lse;                 /* optional */
+    void* d_stage;
+    size_t d_stage_bytes;
+    int32_t* d_r2t;
+    int64_t r2t_elems;
+    void* d_workspace;
+    size_t ws_bytes;
+    int32_t* d_status;
+    int32_t decode;               /* 1: one new token per request, decode_attention */
+} rx_step_io;
+
+size_t rx_step_workspace_bytes(const rx_attn_desc* desc, const rx_step_layout* layout, int32_t decode);
+int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32_t* tokens, const int64_t* tok_indptr,
+                   const rx_node* last_nodes, void* h_stage, const rx_step_layout* layout, const rx_step_io* io,
+                   int64_t evict_tokens, int64_t* out_evicted, void* stream);
+/* Block until the last rx_step_launch copy out of h_stage is complete (no-op if none). */
+int rx_stage_wait(const void* h_stage);
 
 /* Thread-local message describing the last failure in this thread ("" if none). */
 const char* rx_last_error(void);

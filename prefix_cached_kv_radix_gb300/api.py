@@ -25,6 +25,7 @@ EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "match_prefix_len", 
            "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "insert_batch_at", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups", "rx_step_stage_bytes", "rx_step_plan", "rx_step_finish",
+           "rx_step_workspace_bytes", "rx_step_launch", "rx_stage_wait",
            "kv_pool_write", "prefix_extend_attention", "extend_workspace_bytes", "decode_workspace_bytes",
            "decode_attention",
            "decode_attention_noalloc",
@@ -69,6 +70,14 @@ class rx_step_layout(ctypes.Structure):
 
 RX_GROUPS_NONE, RX_GROUPS_ALWAYS, RX_GROUPS_AUTO = 0, 1, 2
 
+
+class rx_step_io(ctypes.Structure):
+    _fields_ = [("d_q", ctypes.c_void_p), ("d_k_new", ctypes.c_void_p), ("d_v_new", ctypes.c_void_p),
+                ("d_k_pool", ctypes.c_void_p), ("d_v_pool", ctypes.c_void_p), ("d_out", ctypes.c_void_p),
+                ("d_lse", ctypes.c_void_p), ("d_stage", ctypes.c_void_p), ("d_stage_bytes", ctypes.c_size_t),
+                ("d_r2t", ctypes.c_void_p), ("r2t_elems", ctypes.c_int64), ("d_workspace", ctypes.c_void_p),
+                ("ws_bytes", ctypes.c_size_t), ("d_status", ctypes.c_void_p), ("decode", ctypes.c_int32)]
+
 _lib = None
 P = ctypes.c_void_p
 I32, I64, U64, SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
@@ -107,6 +116,9 @@ def load(path: str = LIB_PATH):
         "rx_step_stage_bytes": (SZ, [I32, I64]),
         "rx_step_plan": (ctypes.c_int, [P, I32, P, P, P, I32, I32, I64, P, SZ, P, P]),
         "rx_step_finish": (ctypes.c_int, [P, I32, P, P, P, P, P, I64, P]),
+        "rx_step_workspace_bytes": (SZ, [P, P, I32]),
+        "rx_step_launch": (ctypes.c_int, [P, P, P, P, P, P, P, P, I64, P, P]),
+        "rx_stage_wait": (ctypes.c_int, [P]),
         "kv_pool_write": (ctypes.c_int, [P, I32, P, P, P, P, P, P, P, P, P, I64, I64, P, P]),
         "prefix_extend_attention": (ctypes.c_int, [P, I32, P, P, P, P, I64, P, P, P, P, I32, P, P, SZ, P, P]),
         "extend_workspace_bytes": (SZ, [P, I32, I32, P]),
@@ -351,6 +363,26 @@ def rx_step_finish(tree, tokens: np.ndarray, tok_indptr: np.ndarray, last_nodes:
         last_nodes.ctypes.data if layout.batch else None, stage_addr, ctypes.byref(layout), evict_tokens,
         ctypes.byref(n)))
     return n.value
+
+
+def rx_step_workspace_bytes(desc, layout, decode: bool) -> int:
+    return int(load().rx_step_workspace_bytes(ctypes.byref(desc), ctypes.byref(layout), 1 if decode else 0))
+
+
+def rx_step_launch(tree, desc, tokens: np.ndarray, tok_indptr: np.ndarray, last_nodes: np.ndarray, stage_addr: int,
+                   layout, io, evict_tokens: int, stream) -> int:
+    """Copy, kv_pool_write, attention and finish of a planned step in one call; returns the
+    number of slots evicted."""
+    n = I64()
+    _check("rx_step_launch", load().rx_step_launch(
+        tree, ctypes.byref(desc), tokens.ctypes.data, tok_indptr.ctypes.data,
+        last_nodes.ctypes.data if layout.batch else None, stage_addr, ctypes.byref(layout), ctypes.byref(io),
+        evict_tokens, ctypes.byref(n), _stream(stream)))
+    return n.value
+
+
+def rx_stage_wait(stage_addr: int) -> None:
+    _check("rx_stage_wait", load().rx_stage_wait(stage_addr))
 
 
 class RadixTree:

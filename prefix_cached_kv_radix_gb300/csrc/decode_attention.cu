@@ -34,7 +34,7 @@ namespace rx {
 constexpr int DEC_THREADS = 128;   // 4 warps
 constexpr int DEC_STAGE_KEYS = 64; // 16 keys per warp per stage
 constexpr int DEC_NS = 3;          // cp.async ring depth
-constexpr int DEC_MAX_CHUNK = 1024;   // keys per split (the slot list is staged in smem)
+constexpr int DEC_MAX_CHUNK = SMALL_EXT_MAX_KEYS;   // keys per split (the slot list is staged in smem)
 constexpr float LOG2E = 1.4426950408889634f;
 
 __host__ __device__ constexpr int dec_ring_bytes(int D) {
@@ -102,14 +102,23 @@ __device__ __forceinline__ void dec_load_stage(const DecodeParams& p, const int3
     }
 }
 
+// Causal limits of the rows of a small extend tile: row n may see keys <= pos0 + n / group.
+struct ExtRows {
+    int pos0, group;
+    __nv_bfloat16* out;   // final output rows (out_slot[n] = row index into [T * hq])
+    float* lse;           // optional natural-log lse per output row
+};
+
 // Attention of up to 8 query rows (packed into N of m16n8k16) over keys [k_begin, k_end)
-// of one slot-table row; writes normalised partial outputs and log2-domain lse.
-// Row n of the tile reads the query at q_off[n] and writes partial slot out_slot[n]
-// (rows = the query heads of one kv head of one request).
-template <int D>
+// of one slot-table row.  Decode (EXT = false): rows are the query heads of one kv head of
+// one request, all keys visible; writes normalised partial outputs and log2-domain lse at
+// partial slot out_slot[n].  Small extend (EXT = true): rows are (new token, head) pairs of
+// one request with causal limits (ExtRows), the chunk covers every key, and the final bf16
+// output row out_slot[n] (and its lse) is written directly.  Row n reads its query at q_off[n].
+template <int D, bool EXT = false>
 __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* slots_row, int k_begin, int k_end,
                                           int g, const int64_t* q_off, const int64_t* out_slot, int nrows,
-                                          unsigned char* smem, int32_t* slot_s) {
+                                          unsigned char* smem, int32_t* slot_s, ExtRows ext = ExtRows{}) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;                        // m-tiles of O^T
     constexpr int ROWB = D * 2;
@@ -170,21 +179,33 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
                 mma_bf16_16816(sacc, a, qb[s][0], qb[s][1]);
             }
         }
-        // scale, mask keys beyond the chunk, online softmax per query row (column)
-        const bool ok_lo = key0 + r8 < k_end, ok_hi = key0 + r8 + 8 < k_end;
-        float x0 = ok_lo ? sacc[0] * p.scale_log2 : -INFINITY;
-        float x1 = ok_lo ? sacc[1] * p.scale_log2 : -INFINITY;
-        float x2 = ok_hi ? sacc[2] * p.scale_log2 : -INFINITY;
-        float x3 = ok_hi ? sacc[3] * p.scale_log2 : -INFINITY;
+        // scale, mask keys beyond the chunk (and, extending, beyond each row's position),
+        // online softmax per query row (column)
+        bool ok_lo0 = key0 + r8 < k_end, ok_hi0 = key0 + r8 + 8 < k_end;
+        bool ok_lo1 = ok_lo0, ok_hi1 = ok_hi0;
+        if (EXT) {
+            const int lim0 = ext.pos0 + (2 * t4) / ext.group, lim1 = ext.pos0 + (2 * t4 + 1) / ext.group;
+            ok_lo0 = ok_lo0 && key0 + r8 <= lim0;
+            ok_hi0 = ok_hi0 && key0 + r8 + 8 <= lim0;
+            ok_lo1 = ok_lo1 && key0 + r8 <= lim1;
+            ok_hi1 = ok_hi1 && key0 + r8 + 8 <= lim1;
+        }
+        float x0 = ok_lo0 ? sacc[0] * p.scale_log2 : -INFINITY;
+        float x1 = ok_lo1 ? sacc[1] * p.scale_log2 : -INFINITY;
+        float x2 = ok_hi0 ? sacc[2] * p.scale_log2 : -INFINITY;
+        float x3 = ok_hi1 ? sacc[3] * p.scale_log2 : -INFINITY;
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);   // finite: key0 < k_end
-        const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
-        const float p0 = exp2f(x0 - n0), p1 = exp2f(x1 - n1), p2 = exp2f(x2 - n0), p3 = exp2f(x3 - n1);
+        float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);   // decode: finite, as key0 < k_end
+        // extending, a row may have seen no key yet: keep a finite reference so that the
+        // rescale and the weights below are 0 rather than NaN
+        const float r0 = EXT && n0 == -INFINITY ? 0.f : n0, r1 = EXT && n1 == -INFINITY ? 0.f : n1;
+        const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
+        const float p0 = exp2f(x0 - r0), p1 = exp2f(x1 - r1), p2 = exp2f(x2 - r0), p3 = exp2f(x3 - r1);
         l0 = l0 * a0 + p0 + p2;
         l1 = l1 * a1 + p1 + p3;
         m0 = n0;
@@ -250,8 +271,13 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
             acc += sc * red_o[(w * 8 + n) * D + d];
         }
         const int64_t slot = out_slot[n];
-        p.part_o[slot * D + d] = acc / L;
-        if (d == 0) p.part_lse[slot] = M + log2f(L);
+        if (EXT) {
+            ext.out[slot * D + d] = __float2bfloat16_rn(acc / L);
+            if (d == 0 && ext.lse) ext.lse[slot] = (M + log2f(L)) * LN2;
+        } else {
+            p.part_o[slot * D + d] = acc / L;
+            if (d == 0) p.part_lse[slot] = M + log2f(L);
+        }
     }
     __syncthreads();
 }
@@ -284,6 +310,77 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_private_kernel(DecodeParam
     }
     dec_chunk<D>(p, p.r2t + (int64_t)b * p.stride, k_begin, k_end, g, q_off, out_slot, p.group, smem,
                  reinterpret_cast<int32_t*>(smem + dec_ring_bytes(D)));
+}
+
+// Small extend: blockIdx = (kv head, request).  A request's n_b new tokens times the query
+// heads of a kv head (<= 8 rows) attend causally over all of its P_b + n_b keys in one
+// chunk, and write the final output rows.
+template <int D>
+__global__ void __launch_bounds__(DEC_THREADS) extend_small_kernel(DecodeParams p, const int64_t* qo_indptr,
+                                                                   const int32_t* prefix_lens, int32_t max_qo_len,
+                                                                   __nv_bfloat16* out, float* lse) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int g = blockIdx.x, b = blockIdx.y;
+    const int64_t qo0 = qo_indptr[b];
+    const int n = (int)(qo_indptr[b + 1] - qo0);
+    const int P = prefix_lens[b];
+    if (n <= 0) return;
+    if (n > max_qo_len || n * p.group > 8 || P < 0 || (int64_t)P + n > p.stride || P + n > DEC_MAX_CHUNK) {
+        if (g == 0 && threadIdx.x == 0) report(p.status, RX_DEV_BAD_LENGTH);
+        return;
+    }
+    const int rows = n * p.group;
+    int64_t q_off[8], out_row[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int rr = r < rows ? r : 0;
+        out_row[r] = (qo0 + rr / p.group) * p.hq + g * p.group + rr % p.group;
+        q_off[r] = out_row[r] * D;
+    }
+    ExtRows ext{P, p.group, out, lse};
+    dec_chunk<D, true>(p, p.r2t + (int64_t)b * p.stride, 0, P + n, g, q_off, out_row, rows, smem,
+                       reinterpret_cast<int32_t*>(smem + dec_ring_bytes(D)), ext);
+}
+
+int launch_extend_small(const SmallExtendArgs& a, cudaStream_t stream) {
+    DecodeParams p{};
+    p.q = (const __nv_bfloat16*)a.q;
+    p.r2t = a.r2t;
+    p.stride = a.stride;
+    p.k_pool = (const __nv_bfloat16*)a.k_pool;
+    p.v_pool = (const __nv_bfloat16*)a.v_pool;
+    p.num_slots = a.num_slots;
+    p.batch = a.batch;
+    p.hq = a.hq;
+    p.hkv = a.hkv;
+    p.group = a.hq / a.hkv;
+    p.scale_log2 = a.scale * LOG2E;
+    p.status = a.status;
+    const int smem = dec_ring_bytes(a.head_dim) + DEC_MAX_CHUNK * 4;
+    dim3 grid((unsigned)a.hkv, (unsigned)a.batch);
+    if (a.head_dim == 128) {
+        static bool attr = false;
+        if (!attr) {
+            cudaFuncSetAttribute(extend_small_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            attr = true;
+        }
+        extend_small_kernel<128><<<grid, DEC_THREADS, smem, stream>>>(p, a.qo_indptr, a.prefix_lens, a.max_qo_len,
+                                                                      (__nv_bfloat16*)a.out, a.lse);
+    } else {
+        static bool attr = false;
+        if (!attr) {
+            cudaFuncSetAttribute(extend_small_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            attr = true;
+        }
+        extend_small_kernel<64><<<grid, DEC_THREADS, smem, stream>>>(p, a.qo_indptr, a.prefix_lens, a.max_qo_len,
+                                                                     (__nv_bfloat16*)a.out, a.lse);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("prefix_extend_attention: small-extend launch failed: %s", cudaGetErrorString(e));
+        return RX_ECUDA;
+    }
+    return RX_OK;
 }
 
 // Merge the private and shared partials of each (request, head).

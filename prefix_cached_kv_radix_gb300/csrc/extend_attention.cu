@@ -893,6 +893,30 @@ extern "C" int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch, 
     p.max_qo_len = max_qo_len;
     p.status = d_status;
     if (groups && groups->num_groups > 0) return grouped_extend(desc, p, groups, d_workspace, ws_bytes, stream);
+    if ((int64_t)group * max_qo_len <= SMALL_EXT_MAX_ROWS && r2t_stride <= SMALL_EXT_MAX_KEYS) {
+        // a handful of rows per (request, kv head) over at most 1024 keys: the decode-shaped
+        // kernel (keys in M of mma.sync, the rows in N) in one chunk, final rows written directly
+        SmallExtendArgs a{};
+        a.q = d_q;
+        a.qo_indptr = d_qo_indptr;
+        a.prefix_lens = d_prefix_lens;
+        a.r2t = d_req_to_token;
+        a.stride = r2t_stride;
+        a.k_pool = d_k_pool;
+        a.v_pool = d_v_pool;
+        a.num_slots = desc->num_slots;
+        a.out = d_out;
+        a.lse = d_lse;
+        a.batch = batch;
+        a.hq = desc->hq;
+        a.hkv = desc->hkv;
+        a.head_dim = desc->head_dim;
+        a.max_qo_len = max_qo_len;
+        a.scale = desc->scale;
+        a.status = d_status;
+        RX_REQUIRE(batch < 65536, "prefix_extend_attention: grid too large");
+        return launch_extend_small(a, stream);
+    }
     const int64_t tiles = ((int64_t)max_qo_len * group + 255) / 256;
     RX_REQUIRE(tiles < 65536 && batch < 65536, "prefix_extend_attention: grid too large");
     const int rc = desc->head_dim == 128 ? launch_extend_tc<128>(p, (int)tiles, stream, batch)

@@ -588,6 +588,9 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
             return rc;
         }
         bool use = ng > 0;
+        // auto: not when every request fits the small-extend shape (a handful of rows over at
+        // most 1024 keys), which needs no stacking
+        if (use && group_mode == RX_GROUPS_AUTO && (int64_t)max_qo * heads_per_kv <= 8 && max_kv <= 1024) use = false;
         if (use && group_mode == RX_GROUPS_AUTO) {
             for (int32_t b = 0; b < batch && use; ++b) {
                 if (gof[(size_t)b] < 0) use = false;

@@ -54,4 +54,25 @@ struct SharedTcParams {
 
 int launch_shared_prefix_tc(const SharedTcParams& p, cudaStream_t stream);
 
+// Small extend (decode_attention.cu): every request's new tokens times the query heads of a kv
+// head fit 8 rows and its keys one 1024-key chunk (guaranteed by r2t_stride <= 1024).
+constexpr int SMALL_EXT_MAX_ROWS = 8;
+constexpr int SMALL_EXT_MAX_KEYS = 1024;
+struct SmallExtendArgs {
+    const void* q;
+    const int64_t* qo_indptr;
+    const int32_t* prefix_lens;
+    const int32_t* r2t;
+    int64_t stride;
+    const void* k_pool;
+    const void* v_pool;
+    int64_t num_slots;
+    void* out;
+    float* lse;
+    int32_t batch, hq, hkv, head_dim, max_qo_len;
+    float scale;
+    int32_t* status;
+};
+int launch_extend_small(const SmallExtendArgs& a, cudaStream_t stream);
+
 }  // namespace rx

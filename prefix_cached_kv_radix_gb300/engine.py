@@ -90,6 +90,8 @@ class PrefixCacheEngine:
         self._pin_i = 0
         self._dev_idx = None
         self._r2t = None
+        self._r2t_flat = None     # the one-call path's slot table ([batch, stride] in a flat buffer)
+        self._io = None
         self._stream = torch.cuda.current_stream(self.device)
 
     # ------------------------------------------------------------------ helpers
@@ -150,6 +152,8 @@ class PrefixCacheEngine:
         """Next pinned staging buffer with room for nbytes, once the copy that last read it is done."""
         i = self._pin_i
         self._pin_i ^= 1
+        if self._pin[i] is not None:
+            api.rx_stage_wait(self._pin[i].data_ptr())     # a native step's copy out of it is done
         if self._pin[i] is None or self._pin[i].numel() < nbytes:
             if self._pin_used[i]:
                 self._pin_ev[i].synchronize()
@@ -190,6 +194,40 @@ class PrefixCacheEngine:
             plan.grp_members = view(L.off_grp_members, int(plan.grp_indptr[-1]), np.int32)
             plan.grp_len = view(L.off_grp_len, L.num_groups, np.int32)
             plan.grp_rows = L.max_group_rows
+        return plan
+
+    def step(self, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse=None, decode: bool = False,
+             groups=False, min_shared: int = 64, evict_tokens: int = 0, stream=None) -> StepPlan:
+        """A whole step in two library calls: rx_step_plan (a1, a2, groups, pinning, into a
+        pinned staging buffer) and rx_step_launch (the one H2D copy, a3, a4 or a5/a6, then
+        a7/a8 and unpinning).  q/k_new/v_new are the step's new rows in request order; out
+        receives the attention output.  Returns the plan (its index arrays stay readable until
+        the plan after next)."""
+        plan = self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)
+        L = plan.layout
+        st = self._stream if stream is None else stream
+        total = max(int(L.bytes), 256)
+        if self._dev_idx is None or self._dev_idx.numel() < total:
+            self._dev_idx = torch.empty(max(total, 4096) * 2, dtype=torch.uint8, device=self.device)
+        r2t_need = max(plan.batch, 1) * plan.stride
+        if self._r2t_flat is None or self._r2t_flat.numel() < r2t_need:
+            self._r2t_flat = torch.empty(r2t_need * 2, dtype=torch.int32, device=self.device)
+        ws_need = api.rx_step_workspace_bytes(self.desc, L, decode)
+        if ws_need and (self._ws is None or self._ws.numel() < ws_need):
+            self._ws = torch.empty(ws_need, dtype=torch.uint8, device=self.device)
+        io = self._io
+        if io is None:
+            io = self._io = api.rx_step_io()
+        io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
+        io.d_k_pool, io.d_v_pool = self.k_pool.data_ptr(), self.v_pool.data_ptr()
+        io.d_out, io.d_lse = out.data_ptr(), (lse.data_ptr() if lse is not None else None)
+        io.d_stage, io.d_stage_bytes = self._dev_idx.data_ptr(), self._dev_idx.numel()
+        io.d_r2t, io.r2t_elems = self._r2t_flat.data_ptr(), self._r2t_flat.numel()
+        io.d_workspace = self._ws.data_ptr() if self._ws is not None else None
+        io.ws_bytes = self._ws.numel() if self._ws is not None else 0
+        io.d_status, io.decode = self.status.data_ptr(), 1 if decode else 0
+        api.rx_step_launch(self.tree.h, self.desc, plan.tokens, plan.tok_indptr, plan.last_nodes,
+                           self._pin[plan.stage].data_ptr(), L, io, evict_tokens, st.cuda_stream)
         return plan
 
     def upload(self, plan: StepPlan, stream=None) -> dict:

@@ -248,7 +248,13 @@ def run_grouped(spec, groups="auto", expect_grouped=True):
 
 
 def test_grouped_extend_c2():
-    run_grouped(W.config("c2"))
+    run_grouped(W.config("c2"), groups=True)
+
+
+def test_auto_grouping_leaves_small_extend_ungrouped():
+    # c2's 7-8 rows per (request, head) over 417 keys fit the small-extend kernel: "auto"
+    # does not stack them, and the outputs are the oracle's either way
+    run_grouped(W.config("c2"), groups="auto", expect_grouped=False)
 
 
 def test_grouped_extend_private_cached_tails():
@@ -256,7 +262,7 @@ def test_grouped_extend_private_cached_tails():
     # the group shares the root; each request's child tokens and own tokens are private
     spec = W.spec_branching("grp-tails", "bf16", 12, 12, 64, 1 << 14, W.GPT2_VOCAB, 41, root=300, n_children=6,
                             child_len=40, leaves_per_child=3, n_new=5)
-    run_grouped(spec)
+    run_grouped(spec, groups=True)
 
 
 def test_grouped_extend_gqa_d128():
@@ -276,8 +282,8 @@ def test_grouped_equals_ungrouped_extend():
     spec = W.config("c2")
     w = W.generate(spec)
     _, _, _, o1, l1, g1 = run_step(w, groups=False)
-    _, _, _, o2, l2, g2 = run_step(w, groups="auto")
-    assert g1 is None and g2 is not None
+    _, _, _, o2, l2, g2 = run_step(w, groups=True)
+    assert g1 is None and g2 is not None      # small-extend kernel vs the grouped path
     assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
     assert (l1 - l2).abs().max().item() <= 1e-3
 
@@ -336,3 +342,65 @@ def test_page_granular_reuse_recomputes_the_partial_page(name, page):
                                         f32(vf, s.dtype), s.scale)
         compare(got[qo[b]:qo[b + 1]], want, f"{name} page {page} request {b}")
     eng.tree.check()
+
+
+# ---------------------------------------------------------------- one-call step
+@pytest.mark.parametrize("name", ["c1", "c2", "c4"])
+def test_one_call_step_matches_oracle(name):
+    """engine.step: rx_step_plan then rx_step_launch (copy, kv_pool_write, attention with the
+    plan's groups, insert/evict/unpin) gives the oracle's slots and attention; a second step
+    planned into the other staging buffer while the first may still run stays correct."""
+    from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine, _dev_from_host
+    spec = W.config(name)
+    w = W.generate(spec)
+    s = spec
+    eng = PrefixCacheEngine(s.dtype, s.hq, s.hkv, s.d, s.num_slots, s.seed)
+    for i in range(len(s.histories)):
+        k, v = w.history_kv(i)
+        eng.populate(w.history_tokens(i), k, v)
+    prompts = [w.request_tokens(b) for b in range(w.batch)]
+    ind = np.concatenate([[0], np.cumsum([len(p) for p in prompts])]).astype(np.int64)
+    toks = np.concatenate(prompts).astype(np.int32)
+    q, kn, vn = w.stacked_new()
+    qd, kd, vd = (_dev_from_host(x, s.dtype, eng.device) for x in (q, kn, vn))
+    out = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[0], s.hq, dtype=torch.float32, device=eng.device)
+    pre, new, P = expected_slots(w)
+    plan = eng.step(toks, ind, s.req_new, qd, kd, vd, out, lse, decode=s.decode,
+                    groups=True if s.decode else "auto")
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
+    assert np.array_equal(plan.prefix_lens, P)
+    for b in range(w.batch):
+        assert plan.prefix_slots[plan.prefix_indptr[b]:plan.prefix_indptr[b + 1]].tolist() == pre[b].tolist()
+        assert plan.new_slots[plan.qo_indptr[b]:plan.qo_indptr[b + 1]].tolist() == new[b].tolist()
+    got, got_lse = to_host_f32(out), lse.cpu().numpy()
+    qo = np.concatenate([[0], np.cumsum(s.req_new)])
+    for b in range(w.batch):
+        want, want_lse = oracle_rows(w, b)
+        compare(got[qo[b]:qo[b + 1]], want, f"{name} request {b}")
+        assert np.abs(got_lse[qo[b]:qo[b + 1]] - want_lse).max() <= TOL_LSE
+    # the step inserted its new tokens: the same prompts are now fully cached
+    assert eng.new_token_counts(prompts).tolist() == [0] * w.batch
+    eng.tree.check()
+
+
+# ---------------------------------------------------------------- small extend (decode-shaped)
+@pytest.mark.parametrize("hq,hkv,d,new_lens,prefix", [(32, 8, 128, [1, 2, 2, 1, 2, 1], 600),
+                                                       (8, 8, 64, [8, 7, 3, 8, 1], 1000),
+                                                       (16, 2, 128, [1, 1, 1], 37)])
+def test_small_extend_rows(hq, hkv, d, new_lens, prefix):
+    """A few new tokens per request (new tokens x heads per kv head <= 8) over at most 1024
+    keys run on the decode-shaped kernel with per-row causal limits; every row equals the
+    oracle's (ragged lengths, GQA, D 64 and 128, the 1024-key edge)."""
+    spec = W.spec_shared_prompt("small", "bf16", hq, hkv, d, 8192, 50257, 17, prefix, new_lens)
+    w = W.generate(spec)
+    eng, plan, dev, out, lse, _ = run_step(w)
+    assert plan.layout.num_groups == 0 and max(new_lens) * (hq // hkv) <= 8 and plan.stride <= 1024
+    check_tables(w, eng, plan, dev)
+    got, got_lse = to_host_f32(out), lse.cpu().numpy()
+    qo = w.qo_indptr()
+    for b in range(w.batch):
+        want, want_lse = oracle_rows(w, b)
+        compare(got[qo[b]:qo[b + 1]], want, f"small extend request {b}")
+        assert np.abs(got_lse[qo[b]:qo[b + 1]] - want_lse).max() <= TOL_LSE

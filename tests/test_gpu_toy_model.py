@@ -106,9 +106,13 @@ def test_cached_prompt_scores_equal_full_recompute(dtype, tol_oracle):
         # uncached GPU run of the same model: a fresh cache, the whole prompt computed
         fresh = GpuToyLM(om, dtype, seed=6)
         full_gpu, _ = fresh.step([prompt], [len(prompt)])
-        same = bool(np.allclose(cached[-1], full_gpu[-1], atol=g["atol"]))
+        # the page's atol 1e-3 is for fp32 scores; with bf16 attention the cached rows (a few
+        # tokens: the small-extend kernel) and the full recompute (the tcgen05 kernel) round
+        # P to bf16 at different points, so the bf16 bar (2e-2) applies
+        atol = g["atol"] if dtype == "f32" else tol_oracle
+        same = bool(np.allclose(cached[-1], full_gpu[-1], atol=atol))
         assert same == case["same_next_token_scores"]
-        np.testing.assert_allclose(cached, full_gpu[len(prefix):], atol=g["atol"], rtol=0)
+        np.testing.assert_allclose(cached, full_gpu[len(prefix):], atol=atol, rtol=0)
         # and the oracle's fp64 forward over the whole prompt
         full_ref, _ = om.forward(prompt)
         np.testing.assert_allclose(cached, full_ref[len(prefix):], atol=tol_oracle, rtol=0)

@@ -24,8 +24,10 @@ def _view(buf, off, n, dt):
     return buf[off:off + n * np.dtype(dt).itemsize].view(dt)
 
 
-def _auto_ok(gof, glen, P, n_new, heads_per_kv):
+def _auto_ok(gof, glen, P, n_new, heads_per_kv, max_kv):
     if len(glen) == 0 or (gof < 0).any():
+        return False
+    if n_new.max() * heads_per_kv <= 8 and max_kv <= 1024:     # the small-extend shape: no stacking
         return False
     shared = glen[gof]
     return bool((P + n_new - shared).max() <= 256 and (n_new * heads_per_kv).max() < 128)
@@ -68,7 +70,7 @@ def _step(t, m, prompts, n_new, mode, hpk, min_shared, evict_tokens):
     gof, glen = shared_groups([p[:k] for p, k in zip(prompts, P)], min_shared)
     use = mode != api.RX_GROUPS_NONE and len(glen) > 0
     if mode == api.RX_GROUPS_AUTO:
-        use = use and _auto_ok(gof, glen, P, n_new.astype(np.int64), hpk)
+        use = use and _auto_ok(gof, glen, P, n_new.astype(np.int64), hpk, max([len(p) for p in prompts] + [1]))
     if use:
         assert L.num_groups == len(glen)
         gi = _view(buf, L.off_grp_indptr, L.num_groups + 1, np.int32)

@@ -276,6 +276,10 @@ def run_ours(args, rank, world, local_rank):
         d = eng.upload(plan)
         grp = eng.groups(plan, d)
         eng.write(plan, d, kd, vd)
+        if hasattr(torch.cuda, "_sleep"):
+            # keep the GPU busy while the host records the start event and issues the call, so
+            # that only the attention kernels fall between the events
+            torch.cuda._sleep(100_000)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         if s.decode:
@@ -320,9 +324,8 @@ def run_ours(args, rank, world, local_rank):
     ms_e2e, _ = timed(True)
     clk = clocks.stop()
     for i in range(args.steps):                # attention-only timing for the roofline (untimed above)
-        flush.zero_()
-        torch.cuda.synchronize()
-        step_att(args.warmup + 2 * args.steps + i)
+        flush.zero_()                          # no synchronize: the host prepares the call while the
+        step_att(args.warmup + 2 * args.steps + i)   # flush runs, so only the kernels fall between the events
     torch.cuda.synchronize()
     if eng.device_status() != 0:
         raise RuntimeError(f"device status {eng.device_status()} after timed steps")

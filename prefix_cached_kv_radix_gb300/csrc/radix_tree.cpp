@@ -577,8 +577,10 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
         pl[b] = (int32_t)P[(size_t)b];
         kl[b] = (int32_t)(P[(size_t)b] + n_new[b]);
     }
-    // optional shared-prefix groups
-    if (group_mode != RX_GROUPS_NONE && batch > 0) {
+    // optional shared-prefix groups ("auto": not for the small-extend shape -- a few rows per
+    // (request, kv head) over at most 1024 keys -- which needs no stacking)
+    const bool small_shape = (int64_t)max_qo * heads_per_kv <= 8 && max_kv <= 1024;
+    if (group_mode != RX_GROUPS_NONE && batch > 0 && !(group_mode == RX_GROUPS_AUTO && small_shape)) {
         std::vector<int32_t> gof((size_t)batch);
         std::vector<int64_t> glen((size_t)batch);
         int32_t ng = 0;
@@ -588,9 +590,6 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
             return rc;
         }
         bool use = ng > 0;
-        // auto: not when every request fits the small-extend shape (a handful of rows over at
-        // most 1024 keys), which needs no stacking
-        if (use && group_mode == RX_GROUPS_AUTO && (int64_t)max_qo * heads_per_kv <= 8 && max_kv <= 1024) use = false;
         if (use && group_mode == RX_GROUPS_AUTO) {
             for (int32_t b = 0; b < batch && use; ++b) {
                 if (gof[(size_t)b] < 0) use = false;

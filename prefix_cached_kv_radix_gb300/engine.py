@@ -92,6 +92,7 @@ class PrefixCacheEngine:
         self._r2t = None
         self._r2t_flat = None     # the one-call path's slot table ([batch, stride] in a flat buffer)
         self._io = None
+        self._stage_need = {}     # (batch, total tokens) -> staging bytes
         self._stream = torch.cuda.current_stream(self.device)
 
     # ------------------------------------------------------------------ helpers
@@ -175,7 +176,10 @@ class PrefixCacheEngine:
         tok_indptr = np.ascontiguousarray(tok_indptr, np.int64)
         n_new = np.ascontiguousarray(n_new, np.int32)
         b = len(tok_indptr) - 1
-        need = api.rx_step_stage_bytes(b, int(tok_indptr[-1]))
+        key = (b, int(tok_indptr[-1]))
+        need = self._stage_need.get(key)
+        if need is None:
+            need = self._stage_need[key] = api.rx_step_stage_bytes(*key)
         i = self._staging(need)
         host = self._pin_np[i]
         last = np.empty(max(b, 1), np.int64)

@@ -80,12 +80,12 @@ def oracle_rows(w, b, rows=None, threads=0):
     return o, l
 
 
-def compare(got, want, what=""):
+def compare(got, want, what="", max_abs=TOL_MAX_ABS):
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     assert np.isfinite(got).all(), f"{what}: non-finite output"
     err = np.abs(got - want)
-    assert err.max() <= TOL_MAX_ABS, f"{what}: max abs err {err.max():.3e}"
+    assert err.max() <= max_abs, f"{what}: max abs err {err.max():.3e}"
     assert err.mean() <= TOL_MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
     # relative Frobenius per head (last axis = head_dim, second to last = head)
     num = np.sqrt((err ** 2).sum(axis=(0, -1)))

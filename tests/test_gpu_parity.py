@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads as W
-from tests.gpu_cases import (TOL_LSE, compare, expected_slots, f32, oracle_rows, run_step, to_host_f32)
+from tests.gpu_cases import (TOL_LSE, TOL_MAX_ABS, compare, expected_slots, f32, oracle_rows, run_step, to_host_f32)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +43,7 @@ def check_tables(w, eng, plan, dev):
             assert np.array_equal(kp.numpy(), kn) and np.array_equal(vp.numpy(), vn)
 
 
-def check_attention(w, out, lse, rows=None):
+def check_attention(w, out, lse, rows=None, max_abs=TOL_MAX_ABS):
     got = to_host_f32(out)
     got_lse = lse.cpu().numpy() if lse is not None else None
     qo = w.qo_indptr()
@@ -53,17 +53,17 @@ def check_attention(w, out, lse, rows=None):
         idx = None if rows is None else rows[b]
         want, wl = oracle_rows(w, b, idx)
         sel = np.arange(qo[b], qo[b + 1]) if idx is None else qo[b] + np.asarray(idx)
-        compare(got[sel], want, f"request {b}")
+        compare(got[sel], want, f"request {b}", max_abs)
         if got_lse is not None:
             assert np.abs(got_lse[sel] - wl).max() <= TOL_LSE, f"request {b}: lse"
 
 
-def run_and_check(spec, groups=False):
-    w = W.generate(spec)
+def run_and_check(spec, groups=False, workload=None, max_abs=TOL_MAX_ABS):
+    w = workload if workload is not None else W.generate(spec)
     eng, plan, dev, out, lse, _ = run_step(w, groups=groups)
     assert eng.device_status() == 0
     check_tables(w, eng, plan, dev)
-    check_attention(w, out, lse)
+    check_attention(w, out, lse, max_abs=max_abs)
     eng.tree.check()
     return w, eng
 
@@ -110,6 +110,39 @@ def test_extend_fp32_gqa():
     run_and_check(spec)
 
 
+def grow_keys(w, rate):
+    """Scale every key by 1 + rate * (its position in the context), in place: later key tiles
+    raise the running row max by more than the lazy-rescale threshold again and again, so the
+    kernels' rescale of the partial output (after the previous PV has completed) runs often.
+    Position = offset along the segment path for cached keys, P_b + i for new ones."""
+    s = w.spec
+    start = {}
+    for seg in range(len(s.seg_parent)):
+        path = w.seg_path(seg)
+        start[seg] = sum(s.seg_len[x] for x in path[:-1])
+    def scaled(a, p0):
+        f = f32(a, s.dtype) * (1.0 + rate * (p0 + np.arange(len(a), dtype=np.float32)))[:, None, None]
+        return W.f32_to_bf16_bits(f) if s.dtype == "bf16" else f.astype(np.float32)
+    w.seg_k = [scaled(k, start[i]) for i, k in enumerate(w.seg_k)]
+    w.req_k = [scaled(k, s.req_cached[b]) for b, k in enumerate(w.req_k)]
+    return w
+
+
+def peaked_max_abs(w):
+    """Max-abs bound when attention concentrates on single keys: P is rounded to bf16 before
+    PV and the output to bf16 after it, each within 2^-8 relative, so a row that is nearly one
+    value row v is off by up to about 2^-7 max|v| (mean-abs and relative bounds stay)."""
+    vmax = max(np.abs(f32(v, w.spec.dtype)).max() for v in w.seg_v + w.req_v)
+    return max(TOL_MAX_ABS, 2.0 ** -7 * vmax)
+
+
+def test_extend_rescales_as_scores_grow():
+    spec = W.spec_multiturn("grow", "bf16", 64, 8, 128, 1 << 14, W.QWEN_VOCAB, 16, branches=2, branch_len=1200,
+                            hit_len=1000, n_new=100)
+    w = grow_keys(W.generate(spec), 0.02)
+    run_and_check(spec, workload=w, max_abs=peaked_max_abs(w))
+
+
 # ---------------------------------------------------------------- decode
 def small_decode(dtype="bf16", hq=32, hkv=8, d=128, seed=21):
     return W.spec_decode("dec-small", dtype, hq, hkv, d, 1 << 16, W.QWEN_VOCAB, seed, batch=24, share_frac=0.6,
@@ -122,6 +155,12 @@ def test_decode_split_kv():
 
 def test_decode_shared_prefix_groups():
     w, eng = run_and_check(small_decode(), groups=True)
+
+
+def test_decode_shared_prefix_groups_rescale():
+    spec = small_decode(seed=26)
+    w = grow_keys(W.generate(spec), 0.01)
+    run_and_check(spec, groups=True, workload=w, max_abs=peaked_max_abs(w))
 
 
 def test_decode_groups_equal_no_groups():

@@ -21,7 +21,8 @@
 //              (cp.async.mbarrier.arrive), so loaders wait only for free slots; slot ids are
 //              prefetched a tile ahead.
 //   warp 12    TMEM allocator and single-thread tcgen05.mma issuer, per K/V tile j and
-//              Q tile t:  O_t += P_t(j) V(j)  (M=128, N=D, K=128, P from TMEM), then at once
+//              Q tile t:  O_t += P_t(j) V(j)  (M=128, N=D, K=128, P from TMEM, in two halves of
+//              64 keys as the softmax publishes them), then at once
 //              S_t(j+1) = Q_t K(j+1)^T  (M=128, N=128, K=D) into the same TMEM columns -- the
 //              tensor pipe runs one thread's MMAs in order, so P is read before it is
 //              overwritten.  Completion via tcgen05.commit.
@@ -29,7 +30,8 @@
 //              row per thread, causal mask, online softmax in the exp2 domain with a lazy
 //              rescale (the reference max only moves when the row max grows by more than
 //              2^8, which keeps every P <= 256), P packed to bf16 and stored over the row's
-//              scores in TMEM (tcgen05.st); fp32 pairs use the packed f32x2 forms.
+//              scores in TMEM (tcgen05.st) in two halves, each released to the tensor core at
+//              once; fp32 pairs use the packed f32x2 forms.
 // TMEM columns: S0/P0 [0,128) S1/P1 [128,256) O0 [256,256+D) O1 after.  While one Q tile's
 // softmax runs, the tensor core works on the other's GEMMs.  Every wait is bounded; on
 // time-out the kernel records RX_DEV_TIMEOUT, drains its async copies, frees TMEM and
@@ -94,9 +96,9 @@ struct ExtLayout {
     static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + NK * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
-    // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], mma_done
+    // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[half][2], mma_done
     static constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 1 + NK, BAR_VF = 1 + 2 * NK, BAR_VE = 1 + 2 * NK + NV,
-                         BAR_S = 1 + 2 * NK + 2 * NV, BAR_P = BAR_S + 2, BAR_DONE = BAR_P + 2, NBAR = BAR_DONE + 1;
+                         BAR_S = 1 + 2 * NK + 2 * NV, BAR_P = BAR_S + 2, BAR_DONE = BAR_P + 4, NBAR = BAR_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;   // room to align the base to 1024 B
@@ -182,7 +184,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(LY::BAR_S + t), 1);
-            mbar_init(bar(LY::BAR_P + t), 4);          // one arrival per softmax warp
+            mbar_init(bar(LY::BAR_P + t), 4);          // one arrival per softmax warp, keys 0-63
+            mbar_init(bar(LY::BAR_P + 2 + t), 4);      // keys 64-127
         }
         mbar_init(bar(LY::BAR_DONE), 1);
         *abort_flag = 0;
@@ -284,9 +287,9 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                                 IDESC_S, s > 0 ? 1u : 0u);
                 umma_commit(bar(LY::BAR_S + t));
             };
-            auto issue_pv = [&](int t, int vs, int j) {
+            auto issue_pv = [&](int t, int vs, int j, int h) {   // keys 64h .. 64h+63 of the tile
 #pragma unroll
-                for (int s = 0; s < EXT_BN / 16; ++s)
+                for (int s = h * (EXT_BN / 32); s < (h + 1) * (EXT_BN / 32); ++s)
                     umma_f16_ts(tmem + LY::COL_O0 + t * D, tmem + t * EXT_BN + s * 8,
                                 vd0 + (uint64_t)((vs * LY::KV_TILE + s * 16 * 128) >> 4), IDESC_PV,
                                 (j > 0 || s > 0) ? 1u : 0u);
@@ -310,9 +313,14 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                 const bool more = j + 1 < nkv;
                 const int ks = (j + 1) % NK;
                 for (int t = 0; t < ntiles; ++t) {
+                    // P arrives in two halves: PV over keys 0-63 runs while the softmax warps
+                    // still compute keys 64-127
                     if (!mbar_wait(bar(LY::BAR_P + t), j & 1, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv(t, vs, j);
+                    issue_pv(t, vs, j, 0);
+                    if (!mbar_wait(bar(LY::BAR_P + 2 + t), j & 1, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(t, vs, j, 1);
                     if (t == ntiles - 1) umma_commit(bar(LY::BAR_VE + vs));   // V(j) read by every tile
                     if (more) {
                         if (t == 0) {
@@ -384,7 +392,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                 m_ref = m_new;
                 const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m_new, -m_new);
                 uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-                // P in two halves of 64 keys (32 columns)
+                // P in two halves of 64 keys (32 columns), each published as soon as it is
+                // stored, so that the tensor core starts PV on the first half
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pk[EXT_BN / 4];
@@ -399,28 +408,28 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                         pk[cc >> 1] = pack_bf16x2(e0, e1);
                     }
                     tmem_st32u(s_addr + h * 32, pk);
+                    if (h == 0 && rescale) {
+                        // PV_t(j-1) has completed (S_t(j) was issued after it and is complete),
+                        // and PV_t(j) waits for the arrival below.
+#pragma unroll
+                        for (int cc = 0; cc < D; cc += 32) {
+                            float ov[32];
+                            tmem_ld32(o_addr + cc, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+                            tmem_st32(o_addr + cc, ov);
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(LY::BAR_P + 2 * h + t));
                 }
                 const uint64_t a01 = f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3]));
                 float ra, rb;
                 f2_unpack(a01, ra, rb);
                 l += ra + rb;
-                if (rescale) {
-                    // PV_t(j-1) has completed (S_t(j) was issued after it and is complete), and
-                    // PV_t(j) waits for this warp's arrival below.
-#pragma unroll
-                    for (int cc = 0; cc < D; cc += 32) {
-                        float ov[32];
-                        tmem_ld32(o_addr + cc, ov);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-                        tmem_st32(o_addr + cc, ov);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(LY::BAR_P + t));
             }
             if (ok && warp_wait(bar(LY::BAR_DONE), 0, abort_flag, p.status)) {
                 tc_fence_after();

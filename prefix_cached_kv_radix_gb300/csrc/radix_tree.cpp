@@ -17,16 +17,23 @@
 // held along the whole root path.  The allocator is a FIFO ring of free slots whose
 // initial order sorts slot ids by SplitMix64 (Steele, Lea & Flood, OOPSLA 2014).
 #include <algorithm>
+#include <atomic>
+#include <condition_variable>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <memory>
+#include <mutex>
 #include <new>
 #include <queue>
 #include <string>
+#include <thread>
 #include <tuple>
 #include <unordered_map>
 #include <unordered_set>
 #include <vector>
+
+#include <unistd.h>
 
 #include "rx_common.h"
 
@@ -62,6 +69,82 @@ static uint64_t splitmix64_at(uint64_t seed, uint64_t counter) {
     z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
     return z ^ (z >> 31);
 }
+
+// A small persistent pool for the data-parallel parts of a step's host work: reading every
+// prompt against the tree and copying matched slots.  Those tasks only read the tree, one
+// per request.  run(n, fn) calls fn(i) for every i in [0, n) on the workers and the calling
+// thread and returns when all calls are done; one parallel region runs at a time (a
+// concurrent caller runs its loop alone), and a process forked after the workers started
+// (which has none of them) runs every loop alone.
+class Pool {
+  public:
+    static Pool& get() {
+        static Pool* p = new Pool();   // never destroyed: idle workers just wait
+        return *p;
+    }
+    void run(int64_t n, const std::function<void(int64_t)>& fn) {
+        std::unique_lock<std::mutex> region(call_, std::try_to_lock);
+        if (!region.owns_lock() || workers_.empty() || n < 2 || getpid() != owner_) {
+            for (int64_t i = 0; i < n; ++i) fn(i);
+            return;
+        }
+        {
+            std::lock_guard<std::mutex> g(m_);
+            fn_ = &fn;
+            n_ = n;
+            next_.store(0);
+            busy_ = (int)workers_.size();
+            ++gen_;
+        }
+        cv_.notify_all();
+        drain();
+        std::unique_lock<std::mutex> g(m_);
+        done_cv_.wait(g, [&] { return busy_ == 0; });
+        fn_ = nullptr;
+    }
+
+  private:
+    Pool() : owner_(getpid()) {
+        const unsigned hc = std::thread::hardware_concurrency();
+        const unsigned nw = hc > 1 ? std::min(7u, hc - 1) : 0u;
+        for (unsigned i = 0; i < nw; ++i) {
+            try {
+                workers_.emplace_back([this] { loop(); });
+            } catch (...) {
+                break;                 // fewer workers (the caller always takes part)
+            }
+        }
+        for (auto& w : workers_) w.detach();
+    }
+    void drain() {
+        for (int64_t i = next_.fetch_add(1); i < n_; i = next_.fetch_add(1)) (*fn_)(i);
+    }
+    void loop() {
+        uint64_t seen = 0;
+        for (;;) {
+            {
+                std::unique_lock<std::mutex> g(m_);
+                cv_.wait(g, [&] { return gen_ != seen; });
+                seen = gen_;
+            }
+            drain();
+            std::lock_guard<std::mutex> g(m_);
+            if (--busy_ == 0) done_cv_.notify_one();
+        }
+    }
+    const pid_t owner_;
+    std::vector<std::thread> workers_;
+    std::mutex call_, m_;
+    std::condition_variable cv_, done_cv_;
+    const std::function<void(int64_t)>* fn_ = nullptr;
+    int64_t n_ = 0;
+    std::atomic<int64_t> next_{0};
+    int busy_ = 0;
+    uint64_t gen_ = 0;
+};
+
+// Prompts shorter than this in total are read on the calling thread alone.
+constexpr int64_t kParallelTokens = 1 << 15;
 
 // Length of the common prefix of a[0:n] and b[0:n], starting the search at `from`.  Blocks
 // of 16 are OR-reduced first so the compiler can vectorise the common case of equal runs.
@@ -171,6 +254,35 @@ struct rx_radix {
         return walk(tokens, n, out_slots, last);
     }
 
+    // The walk along a path already known to be cached for its first m tokens (a cached_len
+    // result; splits since then move node boundaries, never what is cached): split where it
+    // ends inside an edge and stamp every node on it, without comparing tokens again.
+    // Returns the end node, or nullptr if the path is not there.
+    rx::Node* walk_known(const int32_t* tokens, int64_t m) {
+        rx::Node* x = &root;
+        int64_t pos = 0;
+        while (pos < m) {
+            auto it = x->children.find(tokens[pos]);
+            if (it == x->children.end()) return nullptr;
+            rx::Node* c = it->second;
+            const size_t len = c->key.size();
+            const int64_t k = std::min<int64_t>((int64_t)len, m - pos);
+            if ((size_t)k < len) c = split(c, (size_t)k);
+            c->stamp = clock;
+            pos += k;
+            x = c;
+        }
+        return x;
+    }
+
+    // The slots of the whole root path ending at node x (which ends at depth x->depth).
+    static void path_slots(const rx::Node* x, int32_t* out) {
+        for (; x->parent != nullptr; x = x->parent) {
+            const int64_t k = (int64_t)x->key.size();
+            std::memcpy(out + (x->depth - k), x->slots.data(), sizeof(int32_t) * (size_t)k);
+        }
+    }
+
     // The walk continued from node x, which ends at token position pos of the sequence.
     int64_t walk_from(rx::Node* x, int64_t pos, const int32_t* tokens, int64_t n, int32_t* out_slots,
                       rx::Node** last) {
@@ -266,12 +378,16 @@ int radix_set_page_size(rx_radix* t, int64_t page_size) {
 int match_prefix_len_batch(const rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
                            int64_t* out_len) {
     RX_REQUIRE(t && batch >= 0 && tok_indptr && (batch == 0 || out_len), "match_prefix_len_batch: bad arguments");
-    for (int32_t b = 0; b < batch; ++b) {
-        const int64_t n = tok_indptr[b + 1] - tok_indptr[b];
-        RX_REQUIRE(n >= 0, "match_prefix_len_batch: request %d has a negative length", b);
-        const int rc = match_prefix_len(t, tokens + tok_indptr[b], n, out_len + b);
-        if (rc != RX_OK) return rc;
-    }
+    for (int32_t b = 0; b < batch; ++b)
+        RX_REQUIRE(tok_indptr[b + 1] >= tok_indptr[b], "match_prefix_len_batch: request %d has a negative length", b);
+    RX_REQUIRE(batch == 0 || tokens || tok_indptr[batch] == tok_indptr[0], "match_prefix_len_batch: tokens is NULL");
+    auto one = [&](int64_t b) {
+        const int64_t m = t->cached_len(tokens + tok_indptr[b], tok_indptr[b + 1] - tok_indptr[b]);
+        out_len[b] = m - m % t->page;
+    };
+    if (batch > 0 && tok_indptr[batch] - tok_indptr[0] >= rx::kParallelTokens) rx::Pool::get().run(batch, one);
+    else
+        for (int32_t b = 0; b < batch; ++b) one(b);
     return RX_OK;
 }
 
@@ -530,20 +646,51 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
         const int64_t len = tok_indptr[b + 1] - tok_indptr[b];
         RX_REQUIRE(len >= 0 && n_new[b] >= 0 && n_new[b] <= len, "rx_step_plan: request %d: %lld tokens, %d new", b,
                    (long long)len, n_new[b]);
+    }
+    // Every prompt is read against the tree first (in parallel: the reads are independent and
+    // nothing changes the tree meanwhile); the match lengths are checked before anything is
+    // stamped, split or allocated.
+    const bool par = batch > 0 && total_tokens - tok_indptr[0] >= rx::kParallelTokens;
+    {
+        auto one = [&](int64_t b) {
+            const int64_t m = t->cached_len(tokens + tok_indptr[b], tok_indptr[b + 1] - tok_indptr[b]);
+            P[(size_t)b] = m - m % t->page;
+        };
+        if (par) rx::Pool::get().run(batch, one);
+        else
+            for (int32_t b = 0; b < batch; ++b) one(b);
+    }
+    std::vector<int64_t> off((size_t)batch + 1, 0);
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t len = tok_indptr[b + 1] - tok_indptr[b];
+        RX_REQUIRE(P[(size_t)b] + n_new[b] == len, "rx_step_plan: request %d: %lld tokens cached, %lld expected", b,
+                   (long long)P[(size_t)b], (long long)(len - n_new[b]));
+        off[(size_t)b + 1] = off[(size_t)b] + P[(size_t)b];
+    }
+    // Then, in request order, each walk splits at its match end and stamps its path (one
+    // clock tick per request), without comparing tokens again.
+    std::vector<rx::Node*> lastn((size_t)batch);
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t len = tok_indptr[b + 1] - tok_indptr[b];
         t->clock += 1;
-        rx::Node* last = nullptr;
-        const int64_t m = t->match(tokens + tok_indptr[b], len, ps + acc, &last);
+        rx::Node* last = t->walk_known(tokens + tok_indptr[b], P[(size_t)b]);
+        RX_REQUIRE(last != nullptr, "rx_step_plan: request %d: cached path changed during the plan", b);
+        lastn[(size_t)b] = last;
         t->st.match_calls += 1;
         t->st.match_query_tokens += len;
-        t->st.match_hit_tokens += m;
+        t->st.match_hit_tokens += P[(size_t)b];
         out_last[b] = last->id;
-        RX_REQUIRE(m + n_new[b] == len, "rx_step_plan: request %d: %lld tokens cached, %lld expected", b, (long long)m,
-                   (long long)(len - n_new[b]));
-        P[(size_t)b] = m;
-        acc += m;
+        acc += P[(size_t)b];
         T += n_new[b];
         max_qo = std::max(max_qo, n_new[b]);
         max_kv = std::max<int32_t>(max_kv, (int32_t)len);
+    }
+    // The matched slots, copied along each final path (in parallel: no split happens now).
+    {
+        auto one = [&](int64_t b) { rx_radix::path_slots(lastn[(size_t)b], ps + off[(size_t)b]); };
+        if (par) rx::Pool::get().run(batch, one);
+        else
+            for (int32_t b = 0; b < batch; ++b) one(b);
     }
     L.total_prefix = acc;
     L.total_new = T;

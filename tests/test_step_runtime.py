@@ -190,3 +190,75 @@ def test_step_pins_prefixes_until_finish():
     assert ev == 2 and t.stats()["cached_tokens"] == 6   # evicts before unpinning: only the new leaf
     assert len(t.evict(100)) == 6                        # unpinned afterwards
     t.check()
+
+
+def test_long_prompt_step_equals_per_call_replay():
+    """Prompts long enough (here ~130 K tokens a step) for rx_step_plan to read them against the
+    tree on its worker threads.  The matched slots must equal the oracle's list matcher, and the
+    whole step -- stamps, splits, node ids, allocation, insert, eviction order -- must equal the
+    same step replayed through the single-call entry points (match_prefix per request, lock,
+    insert_batch_at, evict, unlock) on a twin tree."""
+    from oracle import ListMatcher
+    rng = np.random.default_rng(77)
+    vocab = 50000
+    root = rng.integers(0, vocab, size=4000).astype(np.int32)
+    branches = [np.concatenate([root, rng.integers(0, vocab, size=3000).astype(np.int32)]) for _ in range(4)]
+    t1, t2 = api.RadixTree(1 << 16, 5), api.RadixTree(1 << 16, 5)
+    lm = ListMatcher()
+    for br in branches:
+        for t in (t1, t2):
+            k = t.match_prefix_len(br)
+            sl = t.alloc_slots(len(br) - k)
+            full = np.concatenate([np.zeros(k, np.int32), sl]).astype(np.int32)
+            d, _ = t.insert(br, full)
+        k, pre = lm.match(br)
+        lm.add(br, np.concatenate([pre, sl]).astype(np.int32))
+    for step in range(3):
+        prompts, n_new = [], []
+        for b in range(24):
+            br = branches[b % 4]
+            cached = t1.match_prefix_len(br)            # eviction trims the branches step by step
+            cut = int(rng.integers(1, cached + 1))
+            n = int(rng.integers(1, 4))
+            tail = rng.integers(vocab, vocab + 10 ** 6, size=n).astype(np.int32)   # never cached
+            prompts.append(np.concatenate([br[:cut], tail]))
+            n_new.append(n)
+        tok_indptr = np.concatenate([[0], np.cumsum([len(p) for p in prompts])]).astype(np.int64)
+        tokens = np.concatenate(prompts).astype(np.int32)
+        assert tok_indptr[-1] > (1 << 15)
+        nn = np.asarray(n_new, np.int32)
+        T = int(nn.sum())
+        buf, addr, cap = _stage(len(prompts), int(tok_indptr[-1]))
+        last = np.empty(len(prompts), np.int64)
+        L = api.rx_step_plan(t1.h, tokens, tok_indptr, nn, api.RX_GROUPS_NONE, 1, 1, addr, cap, last)
+        got = _view(buf, L.off_prefix_slots, L.total_prefix, np.int32)
+        P = _view(buf, L.off_prefix_lens, len(prompts), np.int32).copy()
+        want = [lm.match(p) for p in prompts]
+        assert P.tolist() == [k for k, _ in want]
+        assert got.tolist() == np.concatenate([s for _, s in want]).tolist()
+        evicted1 = api.rx_step_finish(t1.h, tokens, tok_indptr, last, addr, L, T)
+        # the same step through the single-call entry points
+        lasts, slots2 = [], []
+        for p in prompts:
+            s2, k2, n2 = t2.match_prefix(p)
+            lasts.append(n2)
+            slots2.append(s2)
+        assert lasts == last.tolist()
+        assert np.concatenate(slots2).tolist() == got.tolist()
+        new = t2.alloc_slots(T)
+        assert new.tolist() == _view(buf, L.off_new_slots, T, np.int32).tolist()
+        api.radix_lock_batch(t2.h, lasts)
+        qo = np.concatenate([[0], np.cumsum(nn)]).astype(np.int64)
+        dups, _ = api.insert_batch_at(t2.h, lasts, tokens, tok_indptr, new, qo)
+        for b, d in enumerate(dups):
+            if d > P[b]:
+                t2.free_slots(new[qo[b]:qo[b] + d - P[b]])
+        freed2 = t2.evict(T)
+        api.radix_unlock_batch(t2.h, lasts)
+        assert evicted1 == len(freed2)
+        assert t1.stats() == t2.stats()
+        for p in prompts:
+            lm.add(p, np.concatenate([lm.match(p)[1], np.zeros(len(p) - lm.match(p)[0], np.int32)]))
+        t1.check()
+    # identical stamps and structure: everything evicts in the same order
+    assert t1.evict(10 ** 7).tolist() == t2.evict(10 ** 7).tolist()

@@ -8,8 +8,9 @@ the attention kernel(s) (extend, or split-KV decode + merge), insert of the new 
 and LRU eviction of as many cached tokens (so the cache stays at a steady size).  Every
 step's requests carry fresh new-token ids, so each step is a new batch of requests that
 hits the cached prefix.  Inputs (Q and the new K/V) are resident in HBM when the timed
-region starts; the e2e figure repeats the step through the same public calls with the
-inputs in pinned host memory, copying them in and the outputs back inside the timed region.
+region starts; the e2e figure repeats the step through the same public call with the inputs
+in pinned host memory: the library copies them in and the output back inside the timed
+region (a pipeline of request ranges whose copies run behind the kernels).
 
 Prints one JSON line.  With N > 1 (torchrun) every rank runs its own replica of the
 workload on its own GPU (the path shards over independent requests; no collective is
@@ -256,16 +257,13 @@ def run_ours(args, rank, world, local_rank):
         return 2 if not grouped else 4
 
     def step(i, e2e=False):
-        """One step through the library's one-call path (plan, then copy + kernels + finish)."""
+        """One step through the library's one-call path (plan, then copy + kernels + finish);
+        e2e: the new rows come from and the output goes to pinned host memory, through the
+        library's own copies."""
         toks, ind = step_inputs[i]
-        if e2e:
-            qd.copy_(qh, non_blocking=True)
-            kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-        plan = eng.step(toks, ind, n_new, qd, kd, vd, out, lse, decode=s.decode, groups=group_mode, evict_tokens=T)
+        plan = eng.step(toks, ind, n_new, qd, kd, vd, out, lse, decode=s.decode, groups=group_mode, evict_tokens=T,
+                        host=(qh, kh, vh, out_h) if e2e else None, chunks=args.chunks)
         launches[0] += n_launch(plan.layout.num_groups > 0)
-        if e2e:
-            out_h.copy_(out, non_blocking=True)
         return plan
 
     def step_att(i):
@@ -481,6 +479,8 @@ def main():
     ap.add_argument("--workload", default="c2", choices=list(W.CONFIG_NAMES))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunks", type=int, default=0,
+                    help="request ranges of the e2e copy pipeline (0: chosen by the library)")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="override the KV pool size (profiling captures keep the device footprint small)")
     args = ap.parse_args()

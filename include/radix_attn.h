@@ -367,8 +367,9 @@ int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
                              int32_t* d_status, void* stream);
 
 /* ------------------------------------------------------------------ one-call step launch
- * Everything of a planned step that follows rx_step_plan, in one call: one H2D copy of the
- * staging buffer (h_stage) to its device copy (io->d_stage), kv_pool_write (a3), the
+ * Everything of a planned step that follows rx_step_plan, in one call: the staging buffer
+ * (h_stage) to its device copy (io->d_stage) -- read by a kernel through the device mapping
+ * of pinned memory, or by a copy-engine transfer when it is not mapped --, kv_pool_write (a3), the
  * attention -- prefix_extend_attention (a4), or decode_attention (a5/a6) when io->decode --
  * with the plan's shared-prefix groups, and rx_step_finish (a7/a8: insert, free duplicates,
  * evict evict_tokens, unpin; host only, it does not wait for the GPU).  All device work is
@@ -377,6 +378,14 @@ int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
  * d_lse), the pools, d_stage (>= layout bytes), d_r2t (>= batch * stride int32) and
  * d_workspace (>= rx_step_workspace_bytes).  After the call the staging buffer is still
  * being read by the copy: call rx_stage_wait(h_stage) before planning into it again.
+ * Host-buffer mode (h_q set): the step's new rows come from host memory -- h_q, h_k_new,
+ * h_v_new in the layout of d_q, d_k_new, d_v_new (pinned, for the copies to run
+ * asynchronously) -- and the output goes back to h_out (and h_lse, optional).  The requests
+ * are cut into `chunks` ranges of about equal token counts (0: chosen from the bytes moved;
+ * 1 with shared-prefix groups) that run as a pipeline on two internal copy streams: the rows
+ * of range c+1 are copied in while range c computes on `stream` and the output of range c-1
+ * is copied out.  `stream` waits for the last copy, so the host buffers are complete (and
+ * may be reused) once `stream` is.  The device buffers are still the caller's.
  * Returns RX_EINVAL (nothing launched, the plan still pinned) when a buffer is too small;
  * a launch failure returns RX_ECUDA; *out_evicted (may be NULL) receives the evicted count. */
 typedef struct {
@@ -395,12 +404,31 @@ typedef struct {
     size_t ws_bytes;
     int32_t* d_status;
     int32_t decode;               /* 1: one new token per request, decode_attention */
+    const void* h_q;              /* host-buffer mode: NULL for device rows already filled */
+    const void* h_k_new;
+    const void* h_v_new;
+    void* h_out;
+    float* h_lse;                 /* optional */
+    int32_t chunks;               /* host-buffer mode: request ranges of the pipeline (0: auto) */
 } rx_step_io;
 
 size_t rx_step_workspace_bytes(const rx_attn_desc* desc, const rx_step_layout* layout, int32_t decode);
 int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32_t* tokens, const int64_t* tok_indptr,
                    const rx_node* last_nodes, void* h_stage, const rx_step_layout* layout, const rx_step_io* io,
                    int64_t evict_tokens, int64_t* out_evicted, void* stream);
+/* Host-buffer mode: start the copies of a step's new rows (io->h_q, h_k_new, h_v_new into
+ * io->d_q, d_k_new, d_v_new) before the step is planned, so that they overlap the plan: the
+ * rows of the pipeline's first request range (rx_step_launch copies the others after the
+ * step's index arrays, which would otherwise queue behind them).
+ * Request b's rows are n_new[b] consecutive rows after those of requests 0..b-1 (the plan's
+ * qo order), so the pipeline's request ranges (io->chunks, 0: automatic) follow from n_new
+ * alone.  The copies run after the work already on `stream`.  The next host-buffer
+ * rx_step_launch on this device with the same h_q and d_q uses them instead of copying again
+ * (RX_EINVAL if its plan has other row counts); no other host-buffer step may run on the
+ * device in between. */
+int rx_step_prefetch(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, const rx_step_io* io,
+                     void* stream);
+
 /* Block until the last rx_step_launch copy out of h_stage is complete (no-op if none). */
 int rx_stage_wait(const void* h_stage);
 

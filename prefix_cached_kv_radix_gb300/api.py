@@ -25,7 +25,7 @@ EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "match_prefix_len", 
            "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "insert_batch_at", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups", "rx_step_stage_bytes", "rx_step_plan", "rx_step_finish",
-           "rx_step_workspace_bytes", "rx_step_launch", "rx_stage_wait",
+           "rx_step_workspace_bytes", "rx_step_launch", "rx_step_prefetch", "rx_stage_wait",
            "kv_pool_write", "prefix_extend_attention", "extend_workspace_bytes", "decode_workspace_bytes",
            "decode_attention",
            "decode_attention_noalloc",
@@ -76,7 +76,9 @@ class rx_step_io(ctypes.Structure):
                 ("d_k_pool", ctypes.c_void_p), ("d_v_pool", ctypes.c_void_p), ("d_out", ctypes.c_void_p),
                 ("d_lse", ctypes.c_void_p), ("d_stage", ctypes.c_void_p), ("d_stage_bytes", ctypes.c_size_t),
                 ("d_r2t", ctypes.c_void_p), ("r2t_elems", ctypes.c_int64), ("d_workspace", ctypes.c_void_p),
-                ("ws_bytes", ctypes.c_size_t), ("d_status", ctypes.c_void_p), ("decode", ctypes.c_int32)]
+                ("ws_bytes", ctypes.c_size_t), ("d_status", ctypes.c_void_p), ("decode", ctypes.c_int32),
+                ("h_q", ctypes.c_void_p), ("h_k_new", ctypes.c_void_p), ("h_v_new", ctypes.c_void_p),
+                ("h_out", ctypes.c_void_p), ("h_lse", ctypes.c_void_p), ("chunks", ctypes.c_int32)]
 
 _lib = None
 P = ctypes.c_void_p
@@ -118,6 +120,7 @@ def load(path: str = LIB_PATH):
         "rx_step_finish": (ctypes.c_int, [P, I32, P, P, P, P, P, I64, P]),
         "rx_step_workspace_bytes": (SZ, [P, P, I32]),
         "rx_step_launch": (ctypes.c_int, [P, P, P, P, P, P, P, P, I64, P, P]),
+        "rx_step_prefetch": (ctypes.c_int, [P, I32, P, P, P]),
         "rx_stage_wait": (ctypes.c_int, [P]),
         "kv_pool_write": (ctypes.c_int, [P, I32, P, P, P, P, P, P, P, P, P, I64, I64, P, P]),
         "prefix_extend_attention": (ctypes.c_int, [P, I32, P, P, P, P, I64, P, P, P, P, I32, P, P, SZ, P, P]),
@@ -367,6 +370,13 @@ def rx_step_finish(tree, tokens: np.ndarray, tok_indptr: np.ndarray, last_nodes:
 
 def rx_step_workspace_bytes(desc, layout, decode: bool) -> int:
     return int(load().rx_step_workspace_bytes(ctypes.byref(desc), ctypes.byref(layout), 1 if decode else 0))
+
+
+def rx_step_prefetch(desc, n_new: np.ndarray, io, stream) -> None:
+    """Start the host-buffer copies of a step's new rows before it is planned."""
+    nn = np.ascontiguousarray(np.asarray(n_new, np.int32))
+    _check("rx_step_prefetch", load().rx_step_prefetch(ctypes.byref(desc), len(nn), nn.ctypes.data if len(nn) else None,
+                                                       ctypes.byref(io), _stream(stream)))
 
 
 def rx_step_launch(tree, desc, tokens: np.ndarray, tok_indptr: np.ndarray, last_nodes: np.ndarray, stage_addr: int,

@@ -15,6 +15,7 @@
 #include "radix_attn.h"
 #include "rx_common.h"
 #include "rx_device.cuh"
+#include "rx_kernels.h"
 
 namespace rx {
 
@@ -22,14 +23,14 @@ __global__ void __launch_bounds__(256) kv_pool_write_kernel(
     int32_t batch, const int32_t* __restrict__ prefix_slots, const int64_t* __restrict__ prefix_indptr,
     const int32_t* __restrict__ new_slots, const int64_t* __restrict__ qo_indptr, const uint4* __restrict__ k_new,
     const uint4* __restrict__ v_new, uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
-    int32_t* __restrict__ r2t, int64_t stride, int64_t num_slots, int32_t row_vecs, int64_t total_new,
+    int32_t* __restrict__ r2t, int64_t stride, int64_t num_slots, int32_t row_vecs, int64_t t_begin, int64_t t_end,
     int32_t* status) {
     if ((int)blockIdx.x < batch) {
         const int b = blockIdx.x;
         const int64_t p0 = prefix_indptr[b], P = prefix_indptr[b + 1] - p0;
         const int64_t q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0;
         int32_t* row = r2t + (int64_t)b * stride;
-        const bool bad_len = P < 0 || n < 0 || P + n > stride || q0 + n > total_new;
+        const bool bad_len = P < 0 || n < 0 || P + n > stride || q0 < t_begin || q0 + n > t_end;
         if (bad_len && threadIdx.x == 0) report(status, RX_DEV_BAD_LENGTH);
         for (int64_t j = threadIdx.x; j < stride; j += blockDim.x) {
             int32_t s = -1;
@@ -47,9 +48,11 @@ __global__ void __launch_bounds__(256) kv_pool_write_kernel(
         }
         return;
     }
-    const int64_t nvec = total_new * row_vecs;
+    // new tokens t_begin .. t_end-1 (the rows of this call's requests)
+    const int64_t nvec = (t_end - t_begin) * row_vecs;
     const int64_t step = (int64_t)(gridDim.x - batch) * blockDim.x;
-    for (int64_t i = (int64_t)(blockIdx.x - batch) * blockDim.x + threadIdx.x; i < nvec; i += step) {
+    for (int64_t j = (int64_t)(blockIdx.x - batch) * blockDim.x + threadIdx.x; j < nvec; j += step) {
+        const int64_t i = t_begin * row_vecs + j;
         const int64_t t = i / row_vecs;
         const int32_t v = (int32_t)(i - t * row_vecs);
         const int32_t s = new_slots[t];
@@ -65,12 +68,13 @@ __global__ void __launch_bounds__(256) kv_pool_write_kernel(
 
 }  // namespace rx
 
-extern "C" int kv_pool_write(const rx_attn_desc* desc, int32_t batch, const int32_t* d_prefix_slots,
-                             const int64_t* d_prefix_indptr, const int32_t* d_new_slots,
-                             const int64_t* d_qo_indptr, const void* d_k_new, const void* d_v_new, void* d_k_pool,
-                             void* d_v_pool, int32_t* d_req_to_token, int64_t r2t_stride, int64_t total_new,
-                             int32_t* d_status, void* stream) {
-    RX_REQUIRE(desc && batch >= 0 && r2t_stride >= 0 && total_new >= 0, "kv_pool_write: bad arguments");
+namespace rx {
+
+int kv_pool_write_rows(const rx_attn_desc* desc, int32_t batch, const int32_t* d_prefix_slots,
+                       const int64_t* d_prefix_indptr, const int32_t* d_new_slots, const int64_t* d_qo_indptr,
+                       const void* d_k_new, const void* d_v_new, void* d_k_pool, void* d_v_pool, int32_t* d_req_to_token,
+                       int64_t r2t_stride, int64_t t_begin, int64_t t_end, int32_t* d_status, cudaStream_t stream) {
+    RX_REQUIRE(desc && batch >= 0 && r2t_stride >= 0 && t_begin >= 0 && t_end >= t_begin, "kv_pool_write: bad arguments");
     RX_REQUIRE(desc->dtype == RX_F32 || desc->dtype == RX_BF16, "kv_pool_write: unknown dtype %d", desc->dtype);
     RX_REQUIRE(desc->hkv > 0 && desc->head_dim > 0 && desc->num_slots > 0, "kv_pool_write: bad shape");
     const int64_t row_bytes = (int64_t)desc->hkv * desc->head_dim * (desc->dtype == RX_F32 ? 4 : 2);
@@ -78,25 +82,38 @@ extern "C" int kv_pool_write(const rx_attn_desc* desc, int32_t batch, const int3
                (long long)row_bytes);
     if (batch == 0) return RX_OK;
     RX_REQUIRE(d_prefix_indptr && d_qo_indptr && d_req_to_token, "kv_pool_write: null device pointer");
-    RX_REQUIRE(total_new == 0 || (d_new_slots && d_k_new && d_v_new && d_k_pool && d_v_pool),
+    RX_REQUIRE(t_end == t_begin || (d_new_slots && d_k_new && d_v_new && d_k_pool && d_v_pool),
                "kv_pool_write: null device pointer");
     for (const void* p : {d_k_new, d_v_new, (const void*)d_k_pool, (const void*)d_v_pool})
         RX_REQUIRE(((uintptr_t)p & 15) == 0, "kv_pool_write: K/V buffers must be 16-byte aligned");
     const int32_t row_vecs = (int32_t)(row_bytes / 16);
-    const int64_t nvec = total_new * row_vecs;
+    const int64_t nvec = (t_end - t_begin) * row_vecs;
     int64_t copy_blocks = (nvec + 255) / 256;
     if (copy_blocks > 152 * 16) copy_blocks = 152 * 16;
     if (copy_blocks < 1) copy_blocks = 1;
     const int64_t grid = (int64_t)batch + copy_blocks;
     RX_REQUIRE(grid < (1ll << 31), "kv_pool_write: batch too large");
-    rx::kv_pool_write_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
+    kv_pool_write_kernel<<<(unsigned)grid, 256, 0, stream>>>(
         batch, d_prefix_slots, d_prefix_indptr, d_new_slots, d_qo_indptr, (const uint4*)d_k_new,
         (const uint4*)d_v_new, (uint4*)d_k_pool, (uint4*)d_v_pool, d_req_to_token, r2t_stride, desc->num_slots,
-        row_vecs, total_new, d_status);
+        row_vecs, t_begin, t_end, d_status);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
-        rx::set_error("kv_pool_write: launch failed: %s", cudaGetErrorString(e));
+        set_error("kv_pool_write: launch failed: %s", cudaGetErrorString(e));
         return RX_ECUDA;
     }
     return RX_OK;
+}
+
+}  // namespace rx
+
+extern "C" int kv_pool_write(const rx_attn_desc* desc, int32_t batch, const int32_t* d_prefix_slots,
+                             const int64_t* d_prefix_indptr, const int32_t* d_new_slots,
+                             const int64_t* d_qo_indptr, const void* d_k_new, const void* d_v_new, void* d_k_pool,
+                             void* d_v_pool, int32_t* d_req_to_token, int64_t r2t_stride, int64_t total_new,
+                             int32_t* d_status, void* stream) {
+    RX_REQUIRE(total_new >= 0, "kv_pool_write: bad arguments");
+    return rx::kv_pool_write_rows(desc, batch, d_prefix_slots, d_prefix_indptr, d_new_slots, d_qo_indptr, d_k_new,
+                                  d_v_new, d_k_pool, d_v_pool, d_req_to_token, r2t_stride, 0, total_new, d_status,
+                                  (cudaStream_t)stream);
 }

@@ -8,18 +8,136 @@
 // The staging buffer a step was planned into is read by an asynchronous copy; each staging
 // buffer has an event (recorded after its copy) that rx_stage_wait synchronises, so the next
 // plan into the same buffer cannot overwrite it early.
+//
+// With host buffers the step's rows cross the host link inside the call, as a pipeline of
+// request ranges: range c+1's rows are copied in (copy-in stream) while range c runs
+// kv_pool_write and attention (the caller's stream) and range c-1's output is copied out
+// (copy-out stream), so the transfers hide behind the kernels instead of adding to them.
+// Ranges need no other synchronisation: a request's prefix slots were all written by earlier
+// steps, and its own new K/V by its own range.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 #include "radix_attn.h"
 #include "rx_common.h"
+#include "rx_kernels.h"
 
 namespace {
 
 std::mutex g_ev_mu;
 std::unordered_map<const void*, cudaEvent_t> g_stage_events;   // staging buffer -> event of its last copy
+
+// The index arrays of a step, read by the GPU straight from the pinned staging buffer (mapped
+// into the device's address space) instead of by a copy engine, so that they never wait
+// behind the bulk row copies queued on the engines.  16-byte vectors, grid-stride.
+__global__ void __launch_bounds__(256) stage_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+// Copy streams and events of the host-buffer pipeline, per device (created on first use),
+// and the input copies a rx_step_prefetch has started for the next rx_step_launch.
+struct Pipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    std::vector<cudaEvent_t> ev;      // start, end, then per range: in, done
+    std::mutex use;                   // one step enqueues on a device's pipe at a time
+    bool pending = false;             // copies started by rx_step_prefetch, not yet used
+    const void* p_hq = nullptr;
+    const void* p_dq = nullptr;
+    int64_t p_T = 0;
+    std::vector<int32_t> p_cut;       // the request ranges they were cut into
+};
+std::mutex g_pipe_mu;
+std::unordered_map<int, Pipe> g_pipes;
+
+int pipe_for(int nev, Pipe** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        rx::set_error("rx_step_launch: cannot query the device");
+        return RX_ECUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_pipe_mu);
+    Pipe& p = g_pipes[dev];
+    if (!p.in && (cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) != cudaSuccess ||
+                  cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) != cudaSuccess)) {
+        rx::set_error("rx_step_launch: cannot create the copy streams");
+        return RX_ECUDA;
+    }
+    while ((int)p.ev.size() < nev) {
+        cudaEvent_t e;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            rx::set_error("rx_step_launch: cannot create an event");
+            return RX_ECUDA;
+        }
+        p.ev.push_back(e);
+    }
+    *out = &p;
+    return RX_OK;
+}
+
+// Row bytes of the step's tensors: q/out rows (hq heads) and k/v rows (hkv heads).
+struct RowBytes {
+    int64_t q, kv;
+};
+RowBytes row_bytes(const rx_attn_desc* d) {
+    const int64_t elt = d->dtype == RX_F32 ? 4 : 2;
+    return {(int64_t)d->hq * d->head_dim * elt, (int64_t)d->hkv * d->head_dim * elt};
+}
+
+// The pipeline's request ranges: `chunks` (0: one per 64 MB moved, at most 4) ranges of about
+// equal token counts, cut at request boundaries of the row index qo (host, batch+1 entries).
+std::vector<int32_t> range_cuts(const rx_attn_desc* d, const int64_t* qo, int32_t B, int32_t chunks) {
+    const int64_t T = qo[B] - qo[0];
+    const RowBytes rb = row_bytes(d);
+    int nc = chunks > 0 ? chunks : (int)std::min<int64_t>(4, std::max<int64_t>(1, (T * (2 * rb.q + 2 * rb.kv)) >> 26));
+    nc = std::max(1, std::min<int>(nc, std::max(B, 1)));
+    std::vector<int32_t> cut((size_t)nc + 1, 0);
+    cut[(size_t)nc] = B;
+    for (int c = 1; c < nc; ++c) {   // first request whose rows start at or after c/nc of the tokens
+        const int64_t target = qo[0] + T * c / nc;
+        cut[(size_t)c] = std::max((int32_t)(std::lower_bound(qo, qo + B, target) - qo), cut[(size_t)c - 1]);
+    }
+    return cut;
+}
+
+// The input copies of ranges c_begin .. c_end-1: on `stream` itself for a single range, else
+// on the copy-in stream, each range's completion recorded in its event.  `start`: the copy
+// streams first wait for the work already on `stream` (the first copies of a step).
+int copy_in(Pipe* pp, const rx_attn_desc* d, const rx_step_io* io, const int64_t* qo, const std::vector<int32_t>& cut,
+            int c_begin, int c_end, bool start, cudaStream_t stream) {
+    const RowBytes rb = row_bytes(d);
+    const int nc = (int)cut.size() - 1;
+    cudaStream_t s_in = nc > 1 ? pp->in : stream;
+    cudaError_t e = cudaSuccess;
+    if (nc > 1 && start) {
+        e = cudaEventRecord(pp->ev[0], stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, pp->ev[0], 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(pp->out, pp->ev[0], 0);
+    }
+    for (int c = c_begin; c < c_end && e == cudaSuccess; ++c) {
+        const int64_t t0 = qo[cut[(size_t)c]], t1 = qo[cut[(size_t)c + 1]];
+        if (t1 > t0) {
+            e = cudaMemcpyAsync((char*)io->d_q + t0 * rb.q, (const char*)io->h_q + t0 * rb.q, (size_t)((t1 - t0) * rb.q),
+                                cudaMemcpyHostToDevice, s_in);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync((char*)io->d_k_new + t0 * rb.kv, (const char*)io->h_k_new + t0 * rb.kv,
+                                    (size_t)((t1 - t0) * rb.kv), cudaMemcpyHostToDevice, s_in);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync((char*)io->d_v_new + t0 * rb.kv, (const char*)io->h_v_new + t0 * rb.kv,
+                                    (size_t)((t1 - t0) * rb.kv), cudaMemcpyHostToDevice, s_in);
+        }
+        if (e == cudaSuccess && nc > 1) e = cudaEventRecord(pp->ev[2 + 2 * c], s_in);
+    }
+    if (e != cudaSuccess) {
+        rx::set_error("rx_step_launch: input copy failed: %s", cudaGetErrorString(e));
+        return RX_ECUDA;
+    }
+    return RX_OK;
+}
 
 rx_shared_groups groups_of(const rx_step_layout* L, unsigned char* d_stage) {
     rx_shared_groups g{};
@@ -94,12 +212,6 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
                 ev = it->second;
             }
         }
-        cudaError_t e = cudaMemcpyAsync(io->d_stage, h_stage, (size_t)L->bytes, cudaMemcpyHostToDevice, stream);
-        if (e == cudaSuccess) e = cudaEventRecord(ev, stream);
-        if (e != cudaSuccess) {
-            set_error("rx_step_launch: staging copy failed: %s", cudaGetErrorString(e));
-            return RX_ECUDA;
-        }
         unsigned char* ds = (unsigned char*)io->d_stage;
         const int32_t* prefix_slots = (const int32_t*)(ds + L->off_prefix_slots);
         const int64_t* prefix_indptr = (const int64_t*)(ds + L->off_prefix_indptr);
@@ -107,23 +219,138 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
         const int64_t* qo_indptr = (const int64_t*)(ds + L->off_qo_indptr);
         const int32_t* prefix_lens = (const int32_t*)(ds + L->off_prefix_lens);
         const int32_t* kv_lens = (const int32_t*)(ds + L->off_kv_lens);
-        int rc = kv_pool_write(desc, B, prefix_slots, prefix_indptr, new_slots, qo_indptr, io->d_k_new, io->d_v_new,
-                               io->d_k_pool, io->d_v_pool, io->d_r2t, L->stride, L->total_new, io->d_status, stream);
-        if (rc != RX_OK) return rc;
         rx_shared_groups g{};
         const rx_shared_groups* gp = nullptr;
         if (L->num_groups > 0) {
             g = groups_of(L, ds);
             gp = &g;
         }
-        if (io->decode)
-            rc = decode_attention(desc, B, io->d_q, io->d_r2t, L->stride, kv_lens, gp, io->d_k_pool, io->d_v_pool,
-                                  io->d_out, io->d_lse, L->max_kv_len, io->d_workspace, io->ws_bytes, io->d_status, stream);
-        else
-            rc = prefix_extend_attention(desc, B, io->d_q, qo_indptr, prefix_lens, io->d_r2t, L->stride, io->d_k_pool,
-                                         io->d_v_pool, io->d_out, io->d_lse, L->max_qo_len, gp, io->d_workspace,
-                                         io->ws_bytes, io->d_status, stream);
-        if (rc != RX_OK) return rc;
+        const bool host = io->h_q != nullptr;
+        if (host)
+            RX_REQUIRE(io->h_k_new && io->h_v_new && io->h_out, "rx_step_launch: host-buffer mode needs h_k_new, h_v_new, h_out");
+        const RowBytes rb = row_bytes(desc);
+        const int64_t* h_qo = (const int64_t*)((const unsigned char*)h_stage + L->off_qo_indptr);
+        // the index arrays, on the compute stream: read by a kernel through the mapping of the
+        // pinned staging buffer when it has one (never behind the rows' copies), else copied
+        void* h_dev = nullptr;
+        if (cudaHostGetDevicePointer(&h_dev, h_stage, 0) != cudaSuccess) {
+            cudaGetLastError();   // not mapped (pageable): clear the error, copy instead
+            h_dev = nullptr;
+        }
+        cudaError_t e = cudaSuccess;
+        if (h_dev && ((uintptr_t)h_dev & 15) == 0 && ((uintptr_t)io->d_stage & 15) == 0 && L->bytes % 16 == 0) {
+            const int64_t n = L->bytes / 16;
+            const int blocks = (int)std::min<int64_t>(152 * 2, (n + 255) / 256);
+            stage_copy_kernel<<<std::max(blocks, 1), 256, 0, stream>>>((const uint4*)h_dev, (uint4*)io->d_stage, n);
+            e = cudaGetLastError();
+        } else {
+            e = cudaMemcpyAsync(io->d_stage, h_stage, (size_t)L->bytes, cudaMemcpyHostToDevice, stream);
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(ev, stream);
+        if (e != cudaSuccess) {
+            set_error("rx_step_launch: staging copy failed: %s", cudaGetErrorString(e));
+            return RX_ECUDA;
+        }
+        std::vector<int32_t> cut{0, B};
+        Pipe* pp = nullptr;
+        std::unique_lock<std::mutex> pipe_lock;
+        if (host) {
+            int rc = pipe_for(2, &pp);
+            if (rc != RX_OK) return rc;
+            pipe_lock = std::unique_lock<std::mutex>(pp->use);
+            if (pp->pending && pp->p_hq == io->h_q && pp->p_dq == io->d_q) {
+                // the first range is already on its way (rx_step_prefetch, same ranges cut from
+                // n_new): the rest follow the index arrays
+                RX_REQUIRE(pp->p_T == L->total_new && pp->p_cut.back() == B,
+                           "rx_step_launch: the prefetched rows are not this step's (%lld rows, %lld prefetched)",
+                           (long long)L->total_new, (long long)pp->p_T);
+                cut = pp->p_cut;
+                rc = copy_in(pp, desc, io, h_qo, cut, 1, (int)cut.size() - 1, false, stream);
+            } else {
+                cut = range_cuts(desc, h_qo, B, io->chunks);
+                rc = pipe_for(2 + 2 * ((int)cut.size() - 1), &pp);
+                if (rc == RX_OK) rc = copy_in(pp, desc, io, h_qo, cut, 0, (int)cut.size() - 1, true, stream);
+            }
+            if (rc != RX_OK) return rc;
+            pp->pending = false;
+        }
+        const int nc = (int)cut.size() - 1;
+        // shared-prefix groups span ranges: then one compute over all rows once every range is in
+        const bool ranged = nc > 1 && gp == nullptr;
+        if (nc > 1 && !ranged)
+            for (int c = 0; c < nc && e == cudaSuccess; ++c) e = cudaStreamWaitEvent(stream, pp->ev[2 + 2 * c], 0);
+        const int nk = ranged ? nc : 1;
+        for (int c = 0; c < nk && e == cudaSuccess; ++c) {
+            const int32_t b0 = ranged ? cut[(size_t)c] : 0, b1 = ranged ? cut[(size_t)c + 1] : B;
+            if (b1 == b0) continue;
+            if (ranged) e = cudaStreamWaitEvent(stream, pp->ev[2 + 2 * c], 0);
+            if (e != cudaSuccess) break;
+            const int64_t t0 = h_qo[b0], t1 = h_qo[b1];
+            const int32_t nb = b1 - b0;
+            int32_t* r2t_c = io->d_r2t + (int64_t)b0 * L->stride;
+            int rc = rx::kv_pool_write_rows(desc, nb, prefix_slots, prefix_indptr + b0, new_slots, qo_indptr + b0,
+                                            io->d_k_new, io->d_v_new, io->d_k_pool, io->d_v_pool, r2t_c, L->stride,
+                                            t0, t1, io->d_status, stream);
+            if (rc != RX_OK) return rc;
+            if (io->decode)   // decode rows are the requests themselves (one new token each)
+                rc = decode_attention(desc, nb, (const char*)io->d_q + t0 * rb.q, r2t_c, L->stride, kv_lens + b0, gp,
+                                      io->d_k_pool, io->d_v_pool, (char*)io->d_out + t0 * rb.q,
+                                      io->d_lse ? io->d_lse + t0 * desc->hq : nullptr, L->max_kv_len, io->d_workspace,
+                                      io->ws_bytes, io->d_status, stream);
+            else
+                rc = prefix_extend_attention(desc, nb, io->d_q, qo_indptr + b0, prefix_lens + b0, r2t_c, L->stride,
+                                             io->d_k_pool, io->d_v_pool, io->d_out, io->d_lse, L->max_qo_len, gp,
+                                             io->d_workspace, io->ws_bytes, io->d_status, stream);
+            if (rc != RX_OK) return rc;
+            if (!host) continue;
+            // the output of these rows back to the host: behind the compute on the copy-out
+            // stream when the step is ranged, else on `stream` itself
+            cudaStream_t s_out = ranged ? pp->out : stream;
+            if (ranged) {
+                e = cudaEventRecord(pp->ev[3 + 2 * c], stream);
+                if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, pp->ev[3 + 2 * c], 0);
+            }
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync((char*)io->h_out + t0 * rb.q, (const char*)io->d_out + t0 * rb.q,
+                                    (size_t)((t1 - t0) * rb.q), cudaMemcpyDeviceToHost, s_out);
+            if (e == cudaSuccess && io->h_lse && io->d_lse)
+                e = cudaMemcpyAsync(io->h_lse + t0 * desc->hq, io->d_lse + t0 * desc->hq, (size_t)((t1 - t0) * desc->hq * 4),
+                                    cudaMemcpyDeviceToHost, s_out);
+        }
+        if (e == cudaSuccess && host && ranged) {   // `stream` completes only after the last output copy
+            e = cudaEventRecord(pp->ev[1], pp->out);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, pp->ev[1], 0);
+        }
+        if (e != cudaSuccess) {
+            set_error("rx_step_launch: %s", cudaGetErrorString(e));
+            return RX_ECUDA;
+        }
     }
     return rx_step_finish(t, B, tokens, tok_indptr, last_nodes, h_stage, L, evict_tokens, out_evicted);
+}
+
+extern "C" int rx_step_prefetch(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, const rx_step_io* io,
+                                void* stream_) {
+    RX_REQUIRE(desc && io && batch >= 0 && (batch == 0 || n_new), "rx_step_prefetch: bad arguments");
+    RX_REQUIRE(io->h_q && io->h_k_new && io->h_v_new && io->d_q && io->d_k_new && io->d_v_new,
+               "rx_step_prefetch: needs the host and device rows");
+    std::vector<int64_t> qo((size_t)batch + 1, 0);
+    for (int32_t b = 0; b < batch; ++b) {
+        RX_REQUIRE(n_new[b] >= 0, "rx_step_prefetch: request %d has %d new tokens", b, n_new[b]);
+        qo[(size_t)b + 1] = qo[(size_t)b] + n_new[b];
+    }
+    const std::vector<int32_t> cut = range_cuts(desc, qo.data(), batch, io->chunks);
+    Pipe* pp = nullptr;
+    int rc = pipe_for(2 + 2 * ((int)cut.size() - 1), &pp);
+    if (rc != RX_OK) return rc;
+    std::lock_guard<std::mutex> lk(pp->use);
+    // the first range only: further copies would queue the step's index arrays behind them
+    rc = copy_in(pp, desc, io, qo.data(), cut, 0, 1, true, (cudaStream_t)stream_);
+    if (rc != RX_OK) return rc;
+    pp->pending = true;
+    pp->p_hq = io->h_q;
+    pp->p_dq = io->d_q;
+    pp->p_T = qo[(size_t)batch];
+    pp->p_cut = cut;
+    return RX_OK;
 }

@@ -201,15 +201,33 @@ class PrefixCacheEngine:
         return plan
 
     def step(self, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse=None, decode: bool = False,
-             groups=False, min_shared: int = 64, evict_tokens: int = 0, stream=None) -> StepPlan:
+             groups=False, min_shared: int = 64, evict_tokens: int = 0, stream=None, host=None,
+             chunks: int = 0) -> StepPlan:
         """A whole step in two library calls: rx_step_plan (a1, a2, groups, pinning, into a
         pinned staging buffer) and rx_step_launch (the one H2D copy, a3, a4 or a5/a6, then
         a7/a8 and unpinning).  q/k_new/v_new are the step's new rows in request order; out
-        receives the attention output.  Returns the plan (its index arrays stay readable until
-        the plan after next)."""
+        receives the attention output.  With host=(q_h, k_h, v_h, out_h[, lse_h]) (pinned host
+        tensors of the same shapes) the rows come from and the output goes to host memory,
+        copied by the library as a pipeline of `chunks` request ranges (0: automatic): the
+        input copies start before the plan (rx_step_prefetch) and run behind the kernels with
+        the output copies; they are complete when the stream is.  Returns the plan (its index arrays
+        stay readable until the plan after next)."""
+        st = self._stream if stream is None else stream
+        io = self._io
+        if io is None:
+            io = self._io = api.rx_step_io()
+        if host is not None:
+            # the rows start crossing the host link before the plan is made
+            io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
+            io.h_q, io.h_k_new, io.h_v_new, io.h_out = (x.data_ptr() for x in host[:4])
+            io.h_lse = host[4].data_ptr() if len(host) > 4 and host[4] is not None else None
+            io.chunks = int(chunks)
+            api.rx_step_prefetch(self.desc, n_new, io, st.cuda_stream)
+        else:
+            io.h_q = io.h_k_new = io.h_v_new = io.h_out = io.h_lse = None
+            io.chunks = 0
         plan = self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)
         L = plan.layout
-        st = self._stream if stream is None else stream
         total = max(int(L.bytes), 256)
         if self._dev_idx is None or self._dev_idx.numel() < total:
             self._dev_idx = torch.empty(max(total, 4096) * 2, dtype=torch.uint8, device=self.device)
@@ -219,9 +237,6 @@ class PrefixCacheEngine:
         ws_need = api.rx_step_workspace_bytes(self.desc, L, decode)
         if ws_need and (self._ws is None or self._ws.numel() < ws_need):
             self._ws = torch.empty(ws_need, dtype=torch.uint8, device=self.device)
-        io = self._io
-        if io is None:
-            io = self._io = api.rx_step_io()
         io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
         io.d_k_pool, io.d_v_pool = self.k_pool.data_ptr(), self.v_pool.data_ptr()
         io.d_out, io.d_lse = out.data_ptr(), (lse.data_ptr() if lse is not None else None)

@@ -443,3 +443,83 @@ def test_small_extend_rows(hq, hkv, d, new_lens, prefix):
         want, want_lse = oracle_rows(w, b)
         compare(got[qo[b]:qo[b + 1]], want, f"small extend request {b}")
         assert np.abs(got_lse[qo[b]:qo[b + 1]] - want_lse).max() <= TOL_LSE
+
+
+# ---------------------------------------------------------------- host-buffer step (e2e path)
+def _engine_for(w):
+    from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine
+    s = w.spec
+    eng = PrefixCacheEngine(s.dtype, s.hq, s.hkv, s.d, s.num_slots, s.seed)
+    for i in range(len(s.histories)):
+        k, v = w.history_kv(i)
+        eng.populate(w.history_tokens(i), k, v)
+    return eng
+
+
+@pytest.mark.parametrize("chunks", [1, 3, 0])
+def test_host_buffer_step_equals_device_step(chunks):
+    """rx_step_launch in host-buffer mode (rows copied in and the output out by the library, as
+    a pipeline of request ranges) gives exactly the device-buffer step's output and lse."""
+    from prefix_cached_kv_radix_gb300.engine import _dev_from_host
+    spec = W.Spec("gqa4-ragged-host", "bf16", 32, 8, 128, 1 << 14, W.QWEN_VOCAB, 31,
+                  seg_parent=[-1, 0], seg_len=[300, 77], histories=[1],
+                  req_seg=[1, 0, 0, 1, 0, 1], req_cached=[377, 150, 0, 377, 300, 200],
+                  req_new=[130, 200, 37, 1, 0, 64])
+    w = W.generate(spec)
+    prompts = [w.request_tokens(b) for b in range(w.batch)]
+    ind = np.concatenate([[0], np.cumsum([len(p) for p in prompts])]).astype(np.int64)
+    toks = np.concatenate(prompts).astype(np.int32)
+    q, kn, vn = w.stacked_new()
+    outs = []
+    for host in (False, True):
+        eng = _engine_for(w)
+        qd, kd, vd = (_dev_from_host(x, spec.dtype, eng.device) for x in (q, kn, vn))
+        out = torch.empty_like(qd)
+        lse = torch.empty(qd.shape[0], spec.hq, dtype=torch.float32, device=eng.device)
+        if host:
+            hq_, hk_, hv_ = (x.cpu().pin_memory() for x in (qd, kd, vd))
+            for x in (qd, kd, vd):
+                x.zero_()                           # the library must fill them from the host copies
+            out_h = torch.full(out.shape, float("nan"), dtype=out.dtype).pin_memory()
+            lse_h = torch.full(lse.shape, float("nan"), dtype=torch.float32).pin_memory()
+            eng.step(toks, ind, spec.req_new, qd, kd, vd, out, lse, host=(hq_, hk_, hv_, out_h, lse_h), chunks=chunks)
+            torch.cuda.synchronize()
+            outs.append((out_h.float().numpy(), lse_h.numpy()))
+        else:
+            eng.step(toks, ind, spec.req_new, qd, kd, vd, out, lse)
+            torch.cuda.synchronize()
+            outs.append((to_host_f32(out), lse.cpu().numpy()))
+        assert eng.device_status() == 0
+        eng.tree.check()
+    (o_d, l_d), (o_h, l_h) = outs
+    assert np.array_equal(o_d, o_h) and np.array_equal(l_d, l_h)
+    qo = w.qo_indptr()
+    for b in range(w.batch):
+        if spec.req_new[b]:
+            want, _ = oracle_rows(w, b)
+            compare(o_h[qo[b]:qo[b + 1]], want, f"request {b}")
+
+
+def test_host_buffer_decode_chunks_match_oracle():
+    from prefix_cached_kv_radix_gb300.engine import _dev_from_host
+    spec = small_decode(seed=27)
+    w = W.generate(spec)
+    prompts = [w.request_tokens(b) for b in range(w.batch)]
+    ind = np.concatenate([[0], np.cumsum([len(p) for p in prompts])]).astype(np.int64)
+    toks = np.concatenate(prompts).astype(np.int32)
+    q, kn, vn = w.stacked_new()
+    eng = _engine_for(w)
+    qd, kd, vd = (_dev_from_host(x, spec.dtype, eng.device) for x in (q, kn, vn))
+    hq_, hk_, hv_ = (x.cpu().pin_memory() for x in (qd, kd, vd))
+    out = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[0], spec.hq, dtype=torch.float32, device=eng.device)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    eng.step(toks, ind, spec.req_new, qd, kd, vd, out, lse, decode=True, host=(hq_, hk_, hv_, out_h, lse_h), chunks=4)
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
+    got, got_lse = out_h.float().numpy(), lse_h.numpy()
+    for b in range(w.batch):
+        want, wl = oracle_rows(w, b)
+        compare(got[b:b + 1], want, f"request {b}")
+        assert np.abs(got_lse[b:b + 1] - wl).max() <= TOL_LSE

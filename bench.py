@@ -251,10 +251,12 @@ def run_ours(args, rank, world, local_rank):
     group_mode = True if s.decode else "auto"
 
     def n_launch(grouped: bool) -> int:
-        if s.decode:   # kv_pool_write + (group map, group fill, shared chunks) + private chunks + merge
-            return 1 + (3 if grouped else 0) + 2
-        # kv_pool_write + extend, or + (prep, shared tcgen05, private + merge) with groups
-        return 2 if not grouped else 4
+        # index-array copy + kv_pool_write, then for decode: (group map, group fill, shared
+        # chunks) + private chunks + merge; for extend: extend, or (prep, shared tcgen05,
+        # private + merge) with groups
+        if s.decode:
+            return 2 + (3 if grouped else 0) + 2
+        return 3 if not grouped else 5
 
     def step(i, e2e=False):
         """One step through the library's one-call path (plan, then copy + kernels + finish);

@@ -251,11 +251,11 @@ def run_ours(args, rank, world, local_rank):
     group_mode = True if s.decode else "auto"
 
     def n_launch(grouped: bool) -> int:
-        # index-array copy + kv_pool_write, then for decode: (group map, group fill, shared
-        # chunks) + private chunks + merge; for extend: extend, or (prep, shared tcgen05,
-        # private + merge) with groups
+        # index-array copy + kv_pool_write, then for decode: (group map, shared chunks) +
+        # private chunks + merge; for extend: extend, or (prep, shared tcgen05, private +
+        # merge) with groups
         if s.decode:
-            return 2 + (3 if grouped else 0) + 2
+            return 2 + (2 if grouped else 0) + 2
         return 3 if not grouped else 5
 
     def step(i, e2e=False):

@@ -23,6 +23,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include "radix_attn.h"
 #include "rx_common.h"
@@ -425,18 +426,49 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, __nv_
 }
 
 // group_of[b] from the member lists; -1 for requests outside every group.
-__global__ void decode_group_of_kernel(DecodeParams p, int32_t* group_of) {
-    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < p.batch; b += gridDim.x * blockDim.x) group_of[b] = -1;
+// Each request's group (or -1), and each group's source slot-table row (its first member):
+// one block, every request cleared before the groups' members are written.
+__global__ void __launch_bounds__(512) decode_group_map_kernel(DecodeParams p, int32_t* group_of) {
+    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) group_of[b] = -1;
+    __syncthreads();
+    for (int gid = threadIdx.x; gid < p.num_groups; gid += blockDim.x) p.group_src[gid] = p.grp_members[p.grp_indptr[gid]];
+    const int n = p.num_groups > 0 ? p.grp_indptr[p.num_groups] : 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int lo = 0, hi = p.num_groups - 1;       // the group of member i
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.grp_indptr[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        const int b = p.grp_members[i];
+        if (b >= 0 && b < p.batch) group_of[b] = lo;
+        else report(p.status, RX_DEV_BAD_LENGTH);
+    }
 }
-__global__ void decode_group_fill_kernel(DecodeParams p, int32_t* group_of) {
-    for (int gid = blockIdx.x; gid < p.num_groups; gid += gridDim.x) {
-        if (threadIdx.x == 0) p.group_src[gid] = p.grp_members[p.grp_indptr[gid]];
-        for (int i = p.grp_indptr[gid] + threadIdx.x; i < p.grp_indptr[gid + 1]; i += blockDim.x) {
-            const int b = p.grp_members[i];
-            if (b >= 0 && b < p.batch) group_of[b] = gid;
-            else report(p.status, RX_DEV_BAD_LENGTH);
+
+// A side stream per device and two events: the shared-prefix part runs there, concurrently
+// with the private part on the caller's stream (they only meet in the merge).
+struct DecodeFork {
+    cudaStream_t side = nullptr;
+    cudaEvent_t ready = nullptr, shared_done = nullptr;
+    std::mutex use;
+};
+static std::mutex g_fork_mu;
+static std::unordered_map<int, DecodeFork> g_forks;
+
+static DecodeFork* decode_fork() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lk(g_fork_mu);
+    DecodeFork& f = g_forks[dev];
+    if (!f.side) {
+        if (cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&f.ready, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&f.shared_done, cudaEventDisableTiming) != cudaSuccess) {
+            f.side = nullptr;
+            return nullptr;
         }
     }
+    return &f;
 }
 
 static int dec_chunk_keys(int32_t batch, int32_t hkv, int32_t max_kv_len) {
@@ -571,11 +603,23 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
         }
         attr_set[di] = true;
     }
+    DecodeFork* fork = nullptr;
+    std::unique_lock<std::mutex> fork_lock;
     if (use_groups) {
-        decode_group_of_kernel<<<(batch + 255) / 256, 256, 0, stream>>>(p, group_of);
-        decode_group_fill_kernel<<<groups->num_groups, 128, 0, stream>>>(p, group_of);
+        decode_group_map_kernel<<<1, 512, 0, stream>>>(p, group_of);
         // The shared runs go through the tcgen05 kernel: a group's stacked query rows read
-        // each shared K/V row once per 256 rows.
+        // each shared K/V row once per 256 rows.  On the side stream, concurrently with the
+        // private part (both need only the group map); the merge waits for both.
+        fork = decode_fork();
+        cudaStream_t shared_stream = stream;
+        if (fork) {
+            fork_lock = std::unique_lock<std::mutex>(fork->use);
+            if (cudaEventRecord(fork->ready, stream) == cudaSuccess &&
+                cudaStreamWaitEvent(fork->side, fork->ready, 0) == cudaSuccess)
+                shared_stream = fork->side;
+            else
+                fork = nullptr;
+        }
         SharedTcParams sp{};
         sp.q = d_q;
         sp.r2t = d_req_to_token;
@@ -601,12 +645,20 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
         sp.part_lse = p.part_lse;
         sp.part_per = lay.max_chunks + lay.grp_chunks;
         sp.part_base = lay.max_chunks;
-        const int rc = launch_shared_prefix_tc(sp, stream);
+        const int rc = launch_shared_prefix_tc(sp, shared_stream);
         if (rc != RX_OK) return rc;
+        if (fork && cudaEventRecord(fork->shared_done, fork->side) != cudaSuccess) {
+            set_error("decode_attention: cannot record the shared part's event");
+            return RX_ECUDA;
+        }
     }
     dim3 grid((unsigned)lay.max_chunks, (unsigned)desc->hkv, (unsigned)batch);
     if (D == 128) decode_private_kernel<128><<<grid, DEC_THREADS, smem, stream>>>(p);
     else decode_private_kernel<64><<<grid, DEC_THREADS, smem, stream>>>(p);
+    if (fork && cudaStreamWaitEvent(stream, fork->shared_done, 0) != cudaSuccess) {
+        set_error("decode_attention: cannot join the shared part");
+        return RX_ECUDA;
+    }
     const int64_t items = (int64_t)batch * desc->hq;
     const unsigned mblocks = (unsigned)((items + 3) / 4);
     if (D == 128) decode_merge_kernel<128><<<mblocks, 128, 0, stream>>>(p, (__nv_bfloat16*)d_out, d_lse);

@@ -13,7 +13,6 @@ strings library calls together and moves the step's small index arrays to the de
 """
 from __future__ import annotations
 
-from dataclasses import dataclass
 
 import numpy as np
 import torch
@@ -30,29 +29,79 @@ def _dev_from_host(a, dtype_bits, device):
     return t.to(device, non_blocking=False)
 
 
-@dataclass
+def _contig(a, dt):
+    """a as a C-contiguous array of dtype dt (the array itself when it already is one)."""
+    if isinstance(a, np.ndarray) and a.dtype == dt and a.flags.c_contiguous:
+        return a
+    return np.ascontiguousarray(a, dt)
+
+
 class StepPlan:
     """One planned step.  The index arrays are views of the pinned staging buffer the step's
     device copy is made from (two buffers alternate: a plan stays valid until the plan after
-    next)."""
-    batch: int
-    tokens: np.ndarray          # concatenated full prompts (cached part + new tokens)
-    tok_indptr: np.ndarray      # [batch+1]
-    prefix_slots: np.ndarray    # packed matched slots
-    prefix_indptr: np.ndarray   # [batch+1]
-    prefix_lens: np.ndarray     # [batch] int32 (P_b)
-    new_slots: np.ndarray       # [T]
-    qo_indptr: np.ndarray       # [batch+1]
-    last_nodes: np.ndarray      # [batch] node where each match ended (pinned until finish)
-    max_qo_len: int
-    max_kv_len: int
-    stride: int
-    grp_indptr: np.ndarray = None   # shared-prefix groups (optional)
-    grp_members: np.ndarray = None
-    grp_len: np.ndarray = None
-    grp_rows: int = 0               # largest sum of new tokens over a group's members
-    layout: object = None           # rx_step_layout of the staging buffer
-    stage: int = -1                 # which staging buffer
+    next); each is made on first use."""
+    __slots__ = ("batch", "tokens", "tok_indptr", "last_nodes", "max_qo_len", "max_kv_len", "stride", "layout",
+                 "stage", "_host", "_views")
+
+    def __init__(self, batch, tokens, tok_indptr, last_nodes, layout, stage, host):
+        self.batch = batch
+        self.tokens = tokens            # concatenated full prompts (cached part + new tokens)
+        self.tok_indptr = tok_indptr    # [batch+1]
+        self.last_nodes = last_nodes    # [batch] node where each match ended (pinned until finish)
+        self.max_qo_len = layout.max_qo_len
+        self.max_kv_len = layout.max_kv_len
+        self.stride = layout.stride
+        self.layout = layout            # rx_step_layout of the staging buffer
+        self.stage = stage              # which staging buffer
+        self._host = host
+        self._views = {}
+
+    def _view(self, name, off, n, dt):
+        v = self._views.get(name)
+        if v is None:
+            v = self._views[name] = self._host[off:off + n * np.dtype(dt).itemsize].view(dt)
+        return v
+
+    @property
+    def prefix_slots(self):             # packed matched slots
+        L = self.layout
+        return self._view("ps", L.off_prefix_slots, L.total_prefix, np.int32)
+
+    @property
+    def prefix_indptr(self):            # [batch+1]
+        return self._view("pi", self.layout.off_prefix_indptr, self.batch + 1, np.int64)
+
+    @property
+    def prefix_lens(self):              # [batch] int32 (P_b)
+        return self._view("pl", self.layout.off_prefix_lens, self.batch, np.int32)
+
+    @property
+    def new_slots(self):                # [T]
+        L = self.layout
+        return self._view("ns", L.off_new_slots, L.total_new, np.int32)
+
+    @property
+    def qo_indptr(self):                # [batch+1]
+        return self._view("qo", self.layout.off_qo_indptr, self.batch + 1, np.int64)
+
+    @property
+    def grp_indptr(self):               # shared-prefix groups (None without)
+        L = self.layout
+        return self._view("gi", L.off_grp_indptr, L.num_groups + 1, np.int32) if L.num_groups else None
+
+    @property
+    def grp_members(self):
+        L = self.layout
+        return self._view("gm", L.off_grp_members, int(self.grp_indptr[-1]), np.int32) if L.num_groups else None
+
+    @property
+    def grp_len(self):
+        L = self.layout
+        return self._view("gl", L.off_grp_len, L.num_groups, np.int32) if L.num_groups else None
+
+    @property
+    def grp_rows(self):                 # largest sum of new tokens over a group's members
+        return self.layout.max_group_rows if self.layout.num_groups else 0
 
 
 _GROUP_MODE = {False: api.RX_GROUPS_NONE, None: api.RX_GROUPS_NONE, True: api.RX_GROUPS_ALWAYS,
@@ -83,8 +132,11 @@ class PrefixCacheEngine:
                                   1.0 / float(np.sqrt(head_dim)))
         self._ws = None
         # step index arrays travel in one pinned buffer (two, alternating) and one H2D copy
-        self._pin = [None, None]        # pinned host staging (torch tensor, numpy view)
+        self._pin = [None, None]        # pinned host staging (torch tensor, numpy view, address)
         self._pin_np = [None, None]
+        self._pin_addr = [0, 0]
+        self._io_static = None          # the io whose buffer addresses are current
+        self._ws_need = {}
         self._pin_ev = [torch.cuda.Event(), torch.cuda.Event()]
         self._pin_used = [False, False]
         self._pin_i = 0
@@ -154,12 +206,13 @@ class PrefixCacheEngine:
         i = self._pin_i
         self._pin_i ^= 1
         if self._pin[i] is not None:
-            api.rx_stage_wait(self._pin[i].data_ptr())     # a native step's copy out of it is done
+            api.rx_stage_wait(self._pin_addr[i])            # a native step's copy out of it is done
         if self._pin[i] is None or self._pin[i].numel() < nbytes:
             if self._pin_used[i]:
                 self._pin_ev[i].synchronize()
             self._pin[i] = torch.empty(max(nbytes, 4096) * 2, dtype=torch.uint8).pin_memory()
             self._pin_np[i] = self._pin[i].numpy()
+            self._pin_addr[i] = self._pin[i].data_ptr()
             self._pin_used[i] = False
         if self._pin_used[i]:
             self._pin_ev[i].synchronize()
@@ -172,9 +225,9 @@ class PrefixCacheEngine:
         prefixes until finish; with groups (True, or "auto": only where stacking pays) the
         shared-prefix groups too.  All in the library (rx_step_plan), written straight into a
         pinned staging buffer."""
-        tokens = np.ascontiguousarray(tokens, np.int32)
-        tok_indptr = np.ascontiguousarray(tok_indptr, np.int64)
-        n_new = np.ascontiguousarray(n_new, np.int32)
+        tokens = _contig(tokens, np.int32)
+        tok_indptr = _contig(tok_indptr, np.int64)
+        n_new = _contig(n_new, np.int32)
         b = len(tok_indptr) - 1
         key = (b, int(tok_indptr[-1]))
         need = self._stage_need.get(key)
@@ -184,21 +237,8 @@ class PrefixCacheEngine:
         host = self._pin_np[i]
         last = np.empty(max(b, 1), np.int64)
         L = api.rx_step_plan(self.tree.h, tokens, tok_indptr, n_new, _GROUP_MODE[groups], self.hq // self.hkv,
-                             min_shared, self._pin[i].data_ptr(), host.nbytes, last)
-
-        def view(off, n, dt):
-            return host[off:off + n * np.dtype(dt).itemsize].view(dt)
-
-        plan = StepPlan(b, tokens, tok_indptr, view(L.off_prefix_slots, L.total_prefix, np.int32),
-                        view(L.off_prefix_indptr, b + 1, np.int64), view(L.off_prefix_lens, b, np.int32),
-                        view(L.off_new_slots, L.total_new, np.int32), view(L.off_qo_indptr, b + 1, np.int64),
-                        last[:b], L.max_qo_len, L.max_kv_len, L.stride, layout=L, stage=i)
-        if L.num_groups:
-            plan.grp_indptr = view(L.off_grp_indptr, L.num_groups + 1, np.int32)
-            plan.grp_members = view(L.off_grp_members, int(plan.grp_indptr[-1]), np.int32)
-            plan.grp_len = view(L.off_grp_len, L.num_groups, np.int32)
-            plan.grp_rows = L.max_group_rows
-        return plan
+                             min_shared, self._pin_addr[i], host.nbytes, last)
+        return StepPlan(b, tokens, tok_indptr, last[:b], L, i, host)
 
     def step(self, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse=None, decode: bool = False,
              groups=False, min_shared: int = 64, evict_tokens: int = 0, stream=None, host=None,
@@ -228,25 +268,37 @@ class PrefixCacheEngine:
             io.chunks = 0
         plan = self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)
         L = plan.layout
+        # the step's device buffers: grown when needed; their addresses go into io only then
+        fresh = self._io_static is not io
         total = max(int(L.bytes), 256)
         if self._dev_idx is None or self._dev_idx.numel() < total:
             self._dev_idx = torch.empty(max(total, 4096) * 2, dtype=torch.uint8, device=self.device)
+            fresh = True
         r2t_need = max(plan.batch, 1) * plan.stride
         if self._r2t_flat is None or self._r2t_flat.numel() < r2t_need:
             self._r2t_flat = torch.empty(r2t_need * 2, dtype=torch.int32, device=self.device)
-        ws_need = api.rx_step_workspace_bytes(self.desc, L, decode)
+            fresh = True
+        wkey = (decode, L.batch, L.max_qo_len, L.max_kv_len, L.num_groups, L.max_group_size, L.max_group_len,
+                L.max_group_rows)
+        ws_need = self._ws_need.get(wkey)
+        if ws_need is None:
+            ws_need = self._ws_need[wkey] = api.rx_step_workspace_bytes(self.desc, L, decode)
         if ws_need and (self._ws is None or self._ws.numel() < ws_need):
             self._ws = torch.empty(ws_need, dtype=torch.uint8, device=self.device)
+            fresh = True
+        if fresh:
+            io.d_k_pool, io.d_v_pool = self.k_pool.data_ptr(), self.v_pool.data_ptr()
+            io.d_stage, io.d_stage_bytes = self._dev_idx.data_ptr(), self._dev_idx.numel()
+            io.d_r2t, io.r2t_elems = self._r2t_flat.data_ptr(), self._r2t_flat.numel()
+            io.d_workspace = self._ws.data_ptr() if self._ws is not None else None
+            io.ws_bytes = self._ws.numel() if self._ws is not None else 0
+            io.d_status = self.status.data_ptr()
+            self._io_static = io
         io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
-        io.d_k_pool, io.d_v_pool = self.k_pool.data_ptr(), self.v_pool.data_ptr()
         io.d_out, io.d_lse = out.data_ptr(), (lse.data_ptr() if lse is not None else None)
-        io.d_stage, io.d_stage_bytes = self._dev_idx.data_ptr(), self._dev_idx.numel()
-        io.d_r2t, io.r2t_elems = self._r2t_flat.data_ptr(), self._r2t_flat.numel()
-        io.d_workspace = self._ws.data_ptr() if self._ws is not None else None
-        io.ws_bytes = self._ws.numel() if self._ws is not None else 0
-        io.d_status, io.decode = self.status.data_ptr(), 1 if decode else 0
+        io.decode = 1 if decode else 0
         api.rx_step_launch(self.tree.h, self.desc, plan.tokens, plan.tok_indptr, plan.last_nodes,
-                           self._pin[plan.stage].data_ptr(), L, io, evict_tokens, st.cuda_stream)
+                           self._pin_addr[plan.stage], L, io, evict_tokens, st.cuda_stream)
         return plan
 
     def upload(self, plan: StepPlan, stream=None) -> dict:

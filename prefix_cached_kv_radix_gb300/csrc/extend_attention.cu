@@ -12,9 +12,11 @@
 // GB300 design.  One CTA per (request, kv head, 256 packed query rows).  The query heads
 // of a kv head (GQA group) are packed with the tokens, head fastest: packed row R ->
 // token R / G, head g*G + R % G, so every K/V tile feeds G heads and the tile stays a
-// dense contraction.  Two 128-row Q tiles share each K/V tile of 128 keys.  Roles (512
+// dense contraction.  Two 128-row Q tiles share each K/V tile of 128 keys.  A full Q tile
+// is one TMA box per 64 columns (q seen as [token][head][D], box 64 x G x 128/G), loaded at
+// entry; a full output tile leaves the same way (TMA store from shared memory).  Roles (512
 // threads, four warpgroups, registers split 88 / 168 / 168 / 88 with setmaxnreg):
-//   warps 0-3, 13-15  loaders: 16-byte cp.async gathers of Q once and of K and V tiles
+//   warps 0-3, 13-15  loaders: 16-byte cp.async gathers of a ragged Q tile and of K and V tiles
 //              through the slot table into separate K (3-deep) and V (2-deep) rings in the
 //              128B-swizzled layouts tcgen05 reads.  Each thread's arrival on a tile's full
 //              barrier is made by the copy hardware when its copies land
@@ -36,8 +38,10 @@
 // softmax runs, the tensor core works on the other's GEMMs.  Every wait is bounded; on
 // time-out the kernel records RX_DEV_TIMEOUT, drains its async copies, frees TMEM and
 // returns.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "radix_attn.h"
 #include "rx_common.h"
@@ -84,6 +88,11 @@ struct ExtendParams {
     float* part_o;
     float* part_lse;
     int32_t part_per, part_base;
+    // Extend mode: tiled tensor maps of q and out seen as [rows][hq][D] (box 64 x G x 128/G
+    // elements, 128-byte swizzle), set by the host when G divides 128 and the buffers allow
+    // it.  Full 128-row Q tiles are then loaded, and full output tiles stored, by TMA.
+    int32_t q_map_ok, o_map_ok;
+    CUtensorMap q_map, o_map;
 };
 
 template <int D>
@@ -110,7 +119,7 @@ struct ExtLayout {
 };
 
 template <int D>
-__global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams p) {
+__global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_constant__ ExtendParams p) {
     using LY = ExtLayout<D>;
     constexpr int CPR = LY::CPR;
     constexpr int NX = LY::NX;
@@ -165,6 +174,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
         slots_row = p.r2t + (int64_t)p.grp_src[gid] * p.stride + k_lo;
     }
     const int ntiles = rows_total - row0 > 128 ? 2 : 1;
+    // full tiles of the extend mode go through the tensor maps (token coordinates are 31-bit)
+    const bool map_rows = !p.shared_mode && qo0 + n_b <= INT32_MAX;
     const int nkv = (kv_end + EXT_BN - 1) / EXT_BN;
     // query row pointer of packed row R (clamped to the last valid row)
     auto q_row = [&](int R) -> const __nv_bfloat16* {
@@ -173,7 +184,7 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
     };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(LY::BAR_Q), EXT_LOADERS);
+        mbar_init(bar(LY::BAR_Q), EXT_LOADERS + 1);   // + the TMA issuer's expect-tx arrival
         for (int i = 0; i < NK; ++i) {
             mbar_init(bar(LY::BAR_KF + i), EXT_LOADERS);
             mbar_init(bar(LY::BAR_KE + i), 1);
@@ -190,6 +201,16 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
         mbar_init(bar(LY::BAR_DONE), 1);
         *abort_flag = 0;
         fence_mbar_init();
+        // Full 128-row Q tiles of the extend mode by TMA, one box per 64 columns, in the
+        // swizzled layout the MMA reads.  Issued here, before the register re-split, where
+        // its few values cost the role loops nothing.
+        const int n_full_q = (p.q_map_ok && map_rows) ? min(ntiles, (rows_total - row0) >> 7) : 0;
+        mbar_arrive_expect_tx(bar(LY::BAR_Q), (uint32_t)(n_full_q * LY::Q_TILE));
+        const int tok0 = (int)(qo0 + row0 / G);
+        for (int t = 0; t < n_full_q; ++t)
+            for (int h = 0; h < D / 64; ++h)
+                tma_load_3d(base + LY::OFF_Q + (uint32_t)(t * LY::Q_TILE + h * 128 * 128), &p.q_map, h * 64, g * G,
+                            tok0 + t * (128 / G), bar(LY::BAR_Q));
     }
     if (warp == EXT_MMA_WARP) {
         tmem_alloc(base + LY::OFF_MISC, LY::TMEM_COLS);
@@ -209,7 +230,11 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
         // ------------------------------------------------------------ loaders
         const int lt = warp < 4 ? (int)threadIdx.x : (int)threadIdx.x - (EXT_MMA_WARP + 1) * 32 + 128;
         const uint32_t qs = base + LY::OFF_Q;
-        for (int qi = lt; qi < ntiles * 128 * CPR; qi += EXT_LOADERS) {
+        // The full Q tiles come by TMA (issued at entry); a ragged last tile, and every tile
+        // of the shared-prefix mode, is gathered row by row (rows past the end clamped to the
+        // last one).
+        const int n_full_q = (p.q_map_ok && map_rows) ? min(ntiles, (rows_total - row0) >> 7) : 0;
+        for (int qi = n_full_q * 128 * CPR + lt; qi < ntiles * 128 * CPR; qi += EXT_LOADERS) {
             const int rr = qi / CPR, c = qi % CPR;
             const int t = rr >> 7, r = rr & 127;
             const int R = min(row0 + rr, rows_total - 1);
@@ -219,54 +244,56 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             cp_async_16(dst, src, 16);
         }
         cp_async_arrive_noinc(bar(LY::BAR_Q));   // arrives once this thread's Q copies land
-        int32_t slot_a[NX], slot_b[NX];      // slot ids, one tile ahead (two buffers)
-        auto load_slots = [&](int j, int32_t* dst) {
-#pragma unroll
-            for (int x = 0; x < NX; ++x) {
-                const int q = lt + EXT_LOADERS * x;
-                const int kk = j * EXT_BN + q / CPR;
-                dst[x] = (q < EXT_BN * CPR && kk < kv_end) ? slots_row[kk] : -1;
-            }
+        // Slot ids of one tile (this thread's keys), loaded a tile ahead: the loads of tile
+        // j+1 are issued once tile j's copies are, and first read after the next ring wait.
+        // A key inside the context whose id is outside [0, num_slots) is reported and, like a
+        // key past the context, zero-filled.  The hot loop is kept short (one tile per
+        // iteration, no per-copy branch): its code competes with the softmax loop's for the
+        // instruction cache.
+        int32_t sl[NX];
+        const uint32_t nslots = (uint32_t)min(p.num_slots, (int64_t)1 << 31);
+        auto inside = [&](int j, int x) {
+            const int q = lt + EXT_LOADERS * x;
+            return q < EXT_BN * CPR && j * EXT_BN + q / CPR < kv_end;
         };
-        // Gather one K or V tile; the full barrier gets this thread's arrival when its copies
-        // have landed (cp.async.mbarrier.arrive), so a loader never waits for its own copies,
-        // only for free ring slots.
-        auto issue = [&](int j, uint32_t buf, const __nv_bfloat16* pool, const int32_t* cur, uint32_t full) {
+        auto load_slots = [&](int j) {
+#pragma unroll
+            for (int x = 0; x < NX; ++x)
+                sl[x] = inside(j, x) ? slots_row[j * EXT_BN + (lt + EXT_LOADERS * x) / CPR] : -1;
+        };
+        // Gather one K or V tile (zero fill where sl < 0); the full barrier gets this thread's
+        // arrival when its copies have landed (cp.async.mbarrier.arrive), so a loader never
+        // waits for its own copies, only for free ring slots.
+        auto issue = [&](uint32_t buf, const __nv_bfloat16* pool, uint32_t full) {
 #pragma unroll
             for (int x = 0; x < NX; ++x) {
                 const int q = lt + EXT_LOADERS * x;
                 if (q < EXT_BN * CPR) {
                     const int key = q / CPR, c = q % CPR;
-                    int32_t slot = cur[x];
-                    uint32_t bytes = 16;
-                    if (slot < 0 || slot >= p.num_slots) {
-                        if (slot != -1 || j * EXT_BN + key < kv_end) report(p.status, RX_DEV_BAD_SLOT);
-                        slot = 0;
-                        bytes = 0;             // zero fill: beyond the context or a bad slot
-                    }
-                    const int64_t off = ((int64_t)slot * p.hkv + g) * D + c * 8;
+                    const int64_t off = ((int64_t)max(sl[x], 0) * p.hkv + g) * D + c * 8;
                     const uint32_t so =
                         (uint32_t)((c >> 3) * EXT_BN * 128 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
-                    cp_async_16(buf + so, pool + off, bytes);
+                    cp_async_16(buf + so, pool + off, sl[x] >= 0 ? 16u : 0u);
                 }
             }
             cp_async_arrive_noinc(full);
         };
-        // Issue K and V of tile j from `cur`, and load the slots of tile j+1 into `nxt`.
-        auto step = [&](int j, const int32_t* cur, int32_t* nxt) -> bool {
+        load_slots(0);
+        for (int j = 0; j < nkv; ++j) {
             const int ks = j % NK, vs = j % NV;
-            if (j >= NK && !warp_wait(bar(LY::BAR_KE + ks), ((j / NK) - 1) & 1, abort_flag, p.status)) return false;
-            issue(j, base + LY::OFF_K + ks * LY::KV_TILE, p.k_pool, cur, bar(LY::BAR_KF + ks));
-            if (j >= NV && !warp_wait(bar(LY::BAR_VE + vs), ((j / NV) - 1) & 1, abort_flag, p.status)) return false;
-            issue(j, base + LY::OFF_V + vs * LY::KV_TILE, p.v_pool, cur, bar(LY::BAR_VF + vs));
-            if (j + 1 < nkv) load_slots(j + 1, nxt);
-            return true;
-        };
-        load_slots(0, slot_a);
-        bool ok = true;
-        for (int j = 0; ok && j < nkv; j += 2) {
-            ok = step(j, slot_a, slot_b);
-            if (ok && j + 1 < nkv) ok = step(j + 1, slot_b, slot_a);
+            if (j >= NK && !warp_wait(bar(LY::BAR_KE + ks), ((j / NK) - 1) & 1, abort_flag, p.status)) break;
+            bool bad = false;
+#pragma unroll
+            for (int x = 0; x < NX; ++x) {
+                const bool in = inside(j, x), valid = (uint32_t)sl[x] < nslots;
+                bad |= in && !valid;
+                sl[x] = (in && valid) ? sl[x] : -1;
+            }
+            if (bad) report(p.status, RX_DEV_BAD_SLOT);
+            issue(base + LY::OFF_K + ks * LY::KV_TILE, p.k_pool, bar(LY::BAR_KF + ks));
+            if (j >= NV && !warp_wait(bar(LY::BAR_VE + vs), ((j / NV) - 1) & 1, abort_flag, p.status)) break;
+            issue(base + LY::OFF_V + vs * LY::KV_TILE, p.v_pool, bar(LY::BAR_VF + vs));
+            if (j + 1 < nkv) load_slots(j + 1);
         }
         cp_async_wait_all();                   // no copy may still be landing at teardown
     } else {
@@ -362,17 +389,27 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
             for (int j = 0; j < nkv; ++j) {
                 if (!warp_wait(bar(LY::BAR_S + t), j & 1, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
+                const int lim = pos - j * EXT_BN;   // columns past lim are masked
+                if (__any_sync(0xffffffffu, lim < EXT_BN - 1)) {
+                    // the diagonal tiles only: mask in TMEM, 32 columns at a time (rolled, to
+                    // keep the loop's code small).  The whole warp enters (tcgen05.ld/st are
+                    // warp-collective); a lane whose row sees the whole tile masks nothing.
+#pragma unroll 1
+                    for (int c0 = 0; c0 < EXT_BN; c0 += 32) {
+                        float v[32];
+                        tmem_ld32(s_addr + c0, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c0 + e > lim) v[e] = -INFINITY;
+                        tmem_st32(s_addr + c0, v);
+                    }
+                    tmem_wait_st();
+                }
                 float s[EXT_BN];
 #pragma unroll
                 for (int c = 0; c < EXT_BN; c += 32) tmem_ld32(s_addr + c, s + c);
                 tmem_wait_ld();
-                const int k0 = j * EXT_BN;
-                const bool masked = k0 + EXT_BN - 1 > pos;
-                if (masked) {
-#pragma unroll
-                    for (int c = 0; c < EXT_BN; ++c)
-                        if (k0 + c > pos) s[c] = -INFINITY;
-                }
                 float mx8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = s[i];
@@ -410,8 +447,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                     tmem_st32u(s_addr + h * 32, pk);
                     if (h == 0 && rescale) {
                         // PV_t(j-1) has completed (S_t(j) was issued after it and is complete),
-                        // and PV_t(j) waits for the arrival below.
-#pragma unroll
+                        // and PV_t(j) waits for the arrival below.  Rare: rolled.
+#pragma unroll 1
                         for (int cc = 0; cc < D; cc += 32) {
                             float ov[32];
                             tmem_ld32(o_addr + cc, ov);
@@ -431,10 +468,11 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                 f2_unpack(a01, ra, rb);
                 l += ra + rb;
             }
-            if (ok && warp_wait(bar(LY::BAR_DONE), 0, abort_flag, p.status)) {
-                tc_fence_after();
-                const float inv = 1.f / l;
-                if (p.shared_mode) {
+            const bool done = ok && warp_wait(bar(LY::BAR_DONE), 0, abort_flag, p.status);
+            if (done) tc_fence_after();
+            const float inv = 1.f / l;
+            if (p.shared_mode) {
+                if (done) {
                     // fp32 normalised partial and log2-domain lse for the merge
                     const int64_t item = (int64_t)p.grp_rows[m0 + tok] * p.hq + g * G + Rc % G;
                     const int64_t slot = item * p.part_per + p.part_base + blockIdx.x % p.n_chunks;
@@ -452,7 +490,43 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                         }
                     }
                     if (valid) p.part_lse[slot] = m_ref + log2f(l);
-                } else {
+                }
+            } else {
+                // A full tile (uniform in the warpgroup) is written by TMA: each thread puts its
+                // normalised bf16 row into the tile's Q buffer (no longer read: every MMA has
+                // completed) in the swizzled layout, then one thread stores the boxes.  The
+                // first barrier also agrees that every warp got here with its rows.
+                bool staged = false;
+                if (p.o_map_ok && map_rows && row0 + (t + 1) * 128 <= rows_total) {
+                    const uint32_t stg = base + LY::OFF_Q + (uint32_t)(t * LY::Q_TILE);
+                    if (done) {
+#pragma unroll
+                        for (int cc = 0; cc < D; cc += 32) {
+                            float ov[32];
+                            tmem_ld32(o_addr + cc, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; e += 8) {
+                                const int c = (cc + e) >> 3;
+                                st_shared_v4(stg + (uint32_t)((c >> 3) * 128 * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
+                                             pack_bf16x2(ov[e + 0] * inv, ov[e + 1] * inv),
+                                             pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv),
+                                             pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv),
+                                             pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv));
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    staged = named_bar_and(1 + t, 128, done);
+                    if (staged && r == 0) {
+                        const int tok_first = (int)(qo0 + (row0 + t * 128) / G);
+                        for (int h = 0; h < D / 64; ++h)
+                            tma_store_3d(&p.o_map, stg + (uint32_t)(h * 128 * 128), h * 64, g * G, tok_first);
+                        bulk_commit();
+                        bulk_wait_read_all();   // the buffer is read before the CTA may exit
+                    }
+                }
+                if (done && !staged) {
                     __nv_bfloat16* orow = p.out + ((qo0 + tok) * p.hq + g * G + Rc % G) * D;
 #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
@@ -471,8 +545,8 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(ExtendParams 
                             }
                         }
                     }
-                    if (valid && p.lse) p.lse[(qo0 + tok) * p.hq + g * G + Rc % G] = (m_ref + log2f(l)) * EXT_LN2;
                 }
+                if (done && valid && p.lse) p.lse[(qo0 + tok) * p.hq + g * G + Rc % G] = (m_ref + log2f(l)) * EXT_LN2;
             }
         }
     }
@@ -507,6 +581,37 @@ static int check_device() {
         return RX_EDEVICE;
     }
     return RX_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver, resolved once through the runtime (no -lcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// Tensor map of a bf16 [rows][hq][D] buffer for the extend kernel's 128-row tiles: box
+// 64 columns x G heads x 128/G tokens (a tile of packed rows, head fastest), 128-byte swizzle
+// (the layout tcgen05 reads).  `rows` is the token extent of the map.  Returns false where the
+// shape or address does not allow it (the kernel then gathers and stores row by row).
+static bool rows_tensor_map(CUtensorMap* m, const void* ptr, int hq, int D, int G, int64_t rows) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || G <= 0 || 128 % G != 0 || (D != 64 && D != 128) || ((uintptr_t)ptr & 15u) != 0 || rows <= 0 ||
+        rows > INT32_MAX)
+        return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)hq, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)hq * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D>
@@ -928,6 +1033,13 @@ extern "C" int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch, 
     }
     const int64_t tiles = ((int64_t)max_qo_len * group + 255) / 256;
     RX_REQUIRE(tiles < 65536 && batch < 65536, "prefix_extend_attention: grid too large");
+    // The rows of q and out are located through qo_indptr, whose first entry need not be 0,
+    // so the host knows no tighter bound than the 31-bit coordinate range: the maps never
+    // clip, and the kernel addresses through them only full tiles of one request's rows
+    // (the rows the row-by-row path would touch as well).
+    const int64_t row_bound = INT32_MAX;
+    p.q_map_ok = rows_tensor_map(&p.q_map, d_q, desc->hq, desc->head_dim, group, row_bound) ? 1 : 0;
+    p.o_map_ok = rows_tensor_map(&p.o_map, d_out, desc->hq, desc->head_dim, group, row_bound) ? 1 : 0;
     const int rc = desc->head_dim == 128 ? launch_extend_tc<128>(p, (int)tiles, stream, batch)
                                          : launch_extend_tc<64>(p, (int)tiles, stream, batch);
     if (rc != RX_OK) return rc;

@@ -86,6 +86,17 @@ def test_extend_gqa4_d128_ragged():
     run_and_check(spec)
 
 
+@pytest.mark.parametrize("hq,hkv", [(12, 4), (32, 2)])
+def test_extend_group_sizes(hq, hkv):
+    # 3 query heads per kv head do not tile 128 packed rows by whole tokens, so every Q and
+    # output tile goes row by row; 16 per kv head make TMA boxes of 16 heads x 8 tokens.
+    # Full tiles, a ragged last tile beside a full one, and a single token per request.
+    spec = W.Spec(f"group{hq // hkv}", "bf16", hq, hkv, 128, 1 << 14, W.QWEN_VOCAB, 19,
+                  seg_parent=[-1, 0], seg_len=[257, 64], histories=[1],
+                  req_seg=[1, 0, 1], req_cached=[321, 100, 321], req_new=[150, 64, 1])
+    run_and_check(spec)
+
+
 def test_extend_gqa8_d128_many_tiles():
     spec = W.spec_multiturn("gqa8", "bf16", 64, 8, 128, 1 << 14, W.QWEN_VOCAB, 12, branches=2, branch_len=1200,
                             hit_len=1000, n_new=100)

@@ -7,8 +7,8 @@
 //
 // Design (GB300): the step is HBM-bound (each K/V byte is used by the hq/hkv query heads of
 // one kv head only), so the kernel is built around streaming: one CTA per (request, kv head,
-// chunk of keys); 16-byte cp.async gathers of 64-key stages into a 3-stage 128B-swizzled
-// ring; each warp owns 16 keys of a stage and computes S^T = K Q^T with keys in the M
+// chunk of keys); 16-byte cp.async gathers of 64-key stages into a 2-stage 128B-swizzled
+// ring, three CTAs per SM; each warp owns 16 keys of a stage and computes S^T = K Q^T with keys in the M
 // dimension of m16n8k16 (the <= 8 query heads of the group fill N, so only half of each
 // tile is padding), then O^T += V^T P^T with V^T fragments from ldmatrix.trans and P^T
 // moved into B-fragment layout by movmatrix.  Online softmax in the exp2 domain.  Each CTA
@@ -34,7 +34,11 @@ namespace rx {
 
 constexpr int DEC_THREADS = 128;   // 4 warps
 constexpr int DEC_STAGE_KEYS = 64; // 16 keys per warp per stage
-constexpr int DEC_NS = 3;          // cp.async ring depth
+// cp.async ring depth.  Two 32 KB stages per CTA keep the shared memory at ~69 KB, so three
+// CTAs share an SM (192 KB in flight) and cover one another's prologue (length, group and slot
+// loads) and epilogue (cross-warp merge): with three stages and two CTAs per SM those phases
+// left the SM half idle for ~22 % of each CTA's life.
+constexpr int DEC_NS = 2;
 constexpr int DEC_MAX_CHUNK = SMALL_EXT_MAX_KEYS;   // keys per split (the slot list is staged in smem)
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -156,7 +160,8 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
         cp_async_commit();
     }
     for (int it = 0; it < nstages; ++it) {
-        cp_async_wait<DEC_NS - 2>();
+        // Every warp is done with stage it-1, whose buffer takes stage it+DEC_NS-1; issuing it
+        // before waiting for stage it keeps all DEC_NS stages in flight.
         __syncthreads();
         {
             const int nx = it + DEC_NS - 1;
@@ -164,6 +169,8 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
                 dec_load_stage<D>(p, slot_s, nx * DEC_STAGE_KEYS, nk, g, kbuf(nx % DEC_NS), vbuf(nx % DEC_NS), tid);
             cp_async_commit();
         }
+        cp_async_wait<DEC_NS - 1>();   // stage it has landed (this thread's copies) ...
+        __syncthreads();               // ... and every thread's
         const int st = it % DEC_NS;
         const int key0 = k_begin + it * DEC_STAGE_KEYS + warp * 16;   // first key of this warp
         if (key0 >= k_end) continue;                                   // nothing for this warp
@@ -289,15 +296,12 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_private_kernel(DecodeParam
     extern __shared__ __align__(1024) unsigned char smem[];
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int32_t L = p.kv_lens[b];
+    const int gid = p.group_of ? p.group_of[b] : -1;   // loaded together with L
     if (L < 1 || L > p.max_len || L > p.stride) {
         if (c == 0 && g == 0 && threadIdx.x == 0) report(p.status, RX_DEV_BAD_LENGTH);
         return;
     }
-    int shared = 0;
-    if (p.group_of) {
-        const int gid = p.group_of[b];
-        if (gid >= 0) shared = min(p.grp_len[gid], L);
-    }
+    const int shared = gid >= 0 ? min(p.grp_len[gid], L) : 0;
     const int k_begin = shared + c * p.chunk;
     if (k_begin >= L) return;
     const int k_end = min(L, k_begin + p.chunk);
@@ -597,6 +601,9 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
         const cudaError_t e1 =
             D == 128 ? cudaFuncSetAttribute(decode_private_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
                      : cudaFuncSetAttribute(decode_private_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e1 == cudaSuccess)   // the whole unified L1 as shared memory: three CTAs per SM
+            (void)(D == 128 ? cudaFuncSetAttribute(decode_private_kernel<128>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)
+                            : cudaFuncSetAttribute(decode_private_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100));
         if (e1 != cudaSuccess) {
             set_error("decode_attention: cannot set shared memory size: %s", cudaGetErrorString(e1));
             return RX_ECUDA;

@@ -388,7 +388,10 @@ int launch_extend_small(const SmallExtendArgs& a, cudaStream_t stream) {
     return RX_OK;
 }
 
-// Merge the private and shared partials of each (request, head).
+// Merge the private and shared partials of each (request, head): one warp per item.  The
+// loads are laid out to overlap (length and group id together; one partial's lse per lane,
+// reduced by shuffles; the partial rows four at a time): the kernel is a short chain of
+// dependent global round trips, not a bandwidth problem.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, __nv_bfloat16* out, float* lse) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -396,33 +399,32 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, __nv_
     if (item >= (int64_t)p.batch * p.hq) return;
     const int b = (int)(item / p.hq);
     const int32_t L = p.kv_lens[b];
+    const int gid = p.group_of ? p.group_of[b] : -1;
     if (L < 1 || L > p.max_len || L > p.stride) return;
-    int shared = 0;
-    if (p.group_of) {
-        const int gid = p.group_of[b];
-        if (gid >= 0) shared = min(p.grp_len[gid], L);
-    }
+    const int shared = gid >= 0 ? min(p.grp_len[gid], L) : 0;
     const int npriv = (L - shared + p.chunk - 1) / p.chunk;
-    const int nsh = (shared + p.chunk - 1) / p.chunk;
+    const int n = npriv + (shared + p.chunk - 1) / p.chunk;   // private chunks, then shared ones
     const int per = p.max_chunks + p.grp_chunks;
     const float* po = p.part_o + item * per * D;
     const float* pl = p.part_lse + item * per;
+    auto idx = [&](int s) { return s < npriv ? s : p.max_chunks + (s - npriv); };
     float M = -INFINITY;
-    for (int s = 0; s < npriv; ++s) M = fmaxf(M, pl[s]);
-    for (int s = 0; s < nsh; ++s) M = fmaxf(M, pl[p.max_chunks + s]);
+    for (int s = lane; s < n; s += 32) M = fmaxf(M, pl[idx(s)]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     constexpr int E = D / 32;
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     float W = 0.f;
-    auto add = [&](int s) {
-        const float w = exp2f(pl[s] - M);
+#pragma unroll 4
+    for (int s = 0; s < n; ++s) {
+        const int i = idx(s);
+        const float w = exp2f(pl[i] - M);
         W += w;
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] += w * po[(int64_t)s * D + lane + 32 * e];
-    };
-    for (int s = 0; s < npriv; ++s) add(s);
-    for (int s = 0; s < nsh; ++s) add(p.max_chunks + s);
+        for (int e = 0; e < E; ++e) acc[e] += w * po[(int64_t)i * D + lane + 32 * e];
+    }
     __nv_bfloat16* orow = out + item * D;
 #pragma unroll
     for (int e = 0; e < E; ++e) orow[lane + 32 * e] = __float2bfloat16_rn(acc[e] / W);

@@ -31,12 +31,21 @@ namespace {
 std::mutex g_ev_mu;
 std::unordered_map<const void*, cudaEvent_t> g_stage_events;   // staging buffer -> event of its last copy
 
-// The index arrays of a step, read by the GPU straight from the pinned staging buffer (mapped
-// into the device's address space) instead of by a copy engine, so that they never wait
-// behind the bulk row copies queued on the engines.  16-byte vectors, grid-stride.
+// The index arrays of a host-buffer step, read by the GPU straight from the pinned staging
+// buffer (mapped into the device's address space) instead of by a copy engine, so that they
+// never wait behind the bulk row copies queued on the engines.  16-byte vectors, four
+// independent loads per thread in flight (reads across the host link are latency-bound).
 __global__ void __launch_bounds__(256) stage_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        dst[i] = src[i];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {
+        const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = d;
+    }
+    for (; i < n; i += stride) dst[i] = src[i];
 }
 
 // Copy streams and events of the host-buffer pipeline, per device (created on first use),
@@ -230,10 +239,12 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
             RX_REQUIRE(io->h_k_new && io->h_v_new && io->h_out, "rx_step_launch: host-buffer mode needs h_k_new, h_v_new, h_out");
         const RowBytes rb = row_bytes(desc);
         const int64_t* h_qo = (const int64_t*)((const unsigned char*)h_stage + L->off_qo_indptr);
-        // the index arrays, on the compute stream: read by a kernel through the mapping of the
-        // pinned staging buffer when it has one (never behind the rows' copies), else copied
+        // the index arrays, on the compute stream: in host-buffer mode read by a kernel through
+        // the mapping of the pinned staging buffer when it has one (never behind the rows'
+        // copies); otherwise one copy-engine transfer (about twice the kernel's rate over the
+        // host link)
         void* h_dev = nullptr;
-        if (cudaHostGetDevicePointer(&h_dev, h_stage, 0) != cudaSuccess) {
+        if (host && cudaHostGetDevicePointer(&h_dev, h_stage, 0) != cudaSuccess) {
             cudaGetLastError();   // not mapped (pageable): clear the error, copy instead
             h_dev = nullptr;
         }

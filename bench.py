@@ -37,6 +37,7 @@ import workloads as W  # noqa: E402
 METRIC = "prefix-cached attention tokens/s; % HBM (decode) / % bf16 TC peak (extend)"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 << 20           # GB300 L2
 
 
 def load_peaks():
@@ -241,7 +242,7 @@ def run_ours(args, rank, world, local_rank):
     launches = [0]
 
     # every step's prompts are prepared before timing (inputs resident when timing starts)
-    n_total = 2 * args.warmup + 3 * args.steps     # warm-up (both paths), value, e2e, attention
+    n_total = 2 * args.warmup + 4 * args.steps     # warm-up (both paths), value, e2e, attention, isolated
     step_inputs = []
     for i in range(n_total):
         prompts = fresh_prompts(w, i, used)
@@ -300,11 +301,29 @@ def run_ours(args, rank, world, local_rank):
     if eng.device_status() != 0:
         raise RuntimeError(f"device status {eng.device_status()} after warm-up")
 
-    def timed(e2e):
+    work = algorithmic_work(w)
+    # A step that touches far more than L2 holds is timed as K steps back to back in one event
+    # region (the host's plan of step i+1 overlaps the GPU's step i, as the engine is built to
+    # do: double-buffered staging, host finish right after the launch).  A step that fits in
+    # L2 is timed alone after an L2 flush and a synchronize.
+    back_to_back = work["bytes"] >= 2 * L2_BYTES
+
+    def timed(e2e, isolated=not back_to_back, first=None):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
         launches[0] = 0
+        first = args.warmup + (args.steps if e2e else 0) if first is None else first
+        if not isolated:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(args.steps):
+                step(first + i, e2e=e2e)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            return e0.elapsed_time(e1), launches[0]
         times = []
         for i in range(args.steps):
             flush.zero_()                      # untimed: evict L2 between timed steps
@@ -313,7 +332,7 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            step(args.warmup + (args.steps if e2e else 0) + i, e2e=e2e)
+            step(first + i, e2e=e2e)
             e1.record(stream)
             times.append((e0, e1))
         torch.cuda.synchronize()
@@ -327,6 +346,9 @@ def run_ours(args, rank, world, local_rank):
     ms, n_launches = timed(False)
     ms_e2e, _ = timed(True)
     clk = clocks.stop()
+    ms_iso = None
+    if back_to_back:   # the same steps once more, each alone after a flush, for comparison
+        ms_iso, _ = timed(False, isolated=True, first=args.warmup + 3 * args.steps + args.warmup)
     for i in range(args.steps):                # attention-only timing for the roofline (untimed above)
         flush.zero_()                          # no synchronize: the host prepares the call while the
         step_att(args.warmup + 2 * args.steps + i)   # flush runs, so only the kernels fall between the events
@@ -335,7 +357,6 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {eng.device_status()} after timed steps")
     ms, ms_e2e = reduce_max([ms, ms_e2e], world, dev)
     att_ms = [a.elapsed_time(b) for a, b in att_ev]
-    work = algorithmic_work(w)
     hbm, bf16, bf16_s, src = load_peaks()
     att = statistics.mean(att_ms) if att_ms else float("nan")
     # the bound follows the step's arithmetic intensity against the ridge of the two peaks
@@ -378,13 +399,17 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "f32" if s.dtype == "f32" else "bf16", "data": "synthetic (seeded N(0,1) Q/K/V, uniform token ids)",
         "config": {"workload": f"{s.name}: {s.note}", "batch": w.batch, "new_tokens_per_step": T,
                    "cached_prefix_tokens": int(sum(s.req_cached)), "heads": f"{s.hq}/{s.hkv}x{s.d}",
-                   "kv_pool_slots": s.num_slots, "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "kv_pool_slots": s.num_slots,
+                   "l2": (f"not flushed: a step touches {work['bytes'] / 1e9:.2f} GB (L2 {L2_BYTES >> 20} MiB); "
+                          f"{args.steps} steps back to back in one timed region" if back_to_back else
+                          f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write), each step timed alone"),
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": replica_throughput(T, args.steps, world, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": n_launches,   # library kernels in the timed region (value); the e2e region adds one per step
+        "isolated_step_ms": ms_iso / args.steps if ms_iso is not None else None,
         "clocks": clk,
         "radix_stats": eng.tree.stats(),
     }

@@ -231,8 +231,10 @@ def run_ours(args, rank, world, local_rank):
     qd, kd, vd = (_dev_from_host(x, s.dtype, dev) for x in (q, kn, vn))
     out = torch.empty_like(qd)
     lse = torch.empty(qd.shape[0], s.hq, dtype=torch.float32, device=dev)
-    # pinned host copies for the end-to-end variant
+    # pinned host copies for the end-to-end variant, and a second set of device rows for it: the
+    # steps use the two in turn, so a step's input copies run under the previous step's kernels
     qh, kh, vh = (x.cpu().pin_memory() for x in (qd, kd, vd))
+    rows_e2e = [(qd, kd, vd), tuple(torch.empty_like(x) for x in (qd, kd, vd))]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     T = w.total_new()
@@ -266,8 +268,9 @@ def run_ours(args, rank, world, local_rank):
         e2e: the new rows come from and the output goes to pinned host memory, through the
         library's own copies."""
         toks, ind = step_inputs[i]
-        plan = eng.step(toks, ind, n_new, qd, kd, vd, out, lse, decode=s.decode, groups=group_mode, evict_tokens=T,
-                        host=(qh, kh, vh, out_h) if e2e else None, chunks=args.chunks)
+        q_, k_, v_ = rows_e2e[i % 2] if e2e else (qd, kd, vd)
+        plan = eng.step(toks, ind, n_new, q_, k_, v_, out, lse, decode=s.decode, groups=group_mode, evict_tokens=T,
+                        host=(qh, kh, vh, out_h) if e2e else None, chunks=args.chunks, overlap=e2e)
         launches[0] += n_launch(plan.layout.num_groups > 0, e2e)
         return plan
 

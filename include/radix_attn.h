@@ -368,8 +368,8 @@ int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
 
 /* ------------------------------------------------------------------ one-call step launch
  * Everything of a planned step that follows rx_step_plan, in one call: the staging buffer
- * (h_stage) to its device copy (io->d_stage) -- read by a kernel through the device mapping
- * of pinned memory, or by a copy-engine transfer when it is not mapped --, kv_pool_write (a3), the
+ * (h_stage) to its device copy (io->d_stage) -- a copy-engine transfer, or in host-buffer
+ * mode a kernel reading the device mapping of the pinned buffer --, kv_pool_write (a3), the
  * attention -- prefix_extend_attention (a4), or decode_attention (a5/a6) when io->decode --
  * with the plan's shared-prefix groups, and rx_step_finish (a7/a8: insert, free duplicates,
  * evict evict_tokens, unpin; host only, it does not wait for the GPU).  All device work is
@@ -385,7 +385,13 @@ int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
  * 1 with shared-prefix groups) that run as a pipeline on two internal copy streams: the rows
  * of range c+1 are copied in while range c computes on `stream` and the output of range c-1
  * is copied out.  `stream` waits for the last copy, so the host buffers are complete (and
- * may be reused) once `stream` is.  The device buffers are still the caller's.
+ * may be reused) once `stream` is.  The device buffers are still the caller's.  The input
+ * copies wait for all work already on `stream`, or, with io->overlap set, only for the
+ * kernels of the last host-buffer step whose d_q was this step's d_q (when the library still
+ * tracks it: it keeps the last four; an untracked d_q waits for all work on `stream`).  With
+ * overlap the caller must have no other reads of d_q, d_k_new or d_v_new pending on `stream`;
+ * a caller that uses two sets of device input rows in turn then gets the copies of a step
+ * running under the kernels of the previous one.
  * Returns RX_EINVAL (nothing launched, the plan still pinned) when a buffer is too small;
  * a launch failure returns RX_ECUDA; *out_evicted (may be NULL) receives the evicted count. */
 typedef struct {
@@ -410,6 +416,8 @@ typedef struct {
     void* h_out;
     float* h_lse;                 /* optional */
     int32_t chunks;               /* host-buffer mode: request ranges of the pipeline (0: auto) */
+    int32_t overlap;              /* host-buffer mode: 1 = input copies wait only for the last
+                                     step that read the same d_q (see above) */
 } rx_step_io;
 
 size_t rx_step_workspace_bytes(const rx_attn_desc* desc, const rx_step_layout* layout, int32_t decode);
@@ -422,7 +430,8 @@ int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32_t* tokens,
  * step's index arrays, which would otherwise queue behind them).
  * Request b's rows are n_new[b] consecutive rows after those of requests 0..b-1 (the plan's
  * qo order), so the pipeline's request ranges (io->chunks, 0: automatic) follow from n_new
- * alone.  The copies run after the work already on `stream`.  The next host-buffer
+ * alone.  The copies run after the work already on `stream` (with io->overlap: after the
+ * kernels of the last step that read io->d_q, as in rx_step_launch).  The next host-buffer
  * rx_step_launch on this device with the same h_q and d_q uses them instead of copying again
  * (RX_EINVAL if its plan has other row counts); no other host-buffer step may run on the
  * device in between. */

@@ -78,7 +78,8 @@ class rx_step_io(ctypes.Structure):
                 ("d_r2t", ctypes.c_void_p), ("r2t_elems", ctypes.c_int64), ("d_workspace", ctypes.c_void_p),
                 ("ws_bytes", ctypes.c_size_t), ("d_status", ctypes.c_void_p), ("decode", ctypes.c_int32),
                 ("h_q", ctypes.c_void_p), ("h_k_new", ctypes.c_void_p), ("h_v_new", ctypes.c_void_p),
-                ("h_out", ctypes.c_void_p), ("h_lse", ctypes.c_void_p), ("chunks", ctypes.c_int32)]
+                ("h_out", ctypes.c_void_p), ("h_lse", ctypes.c_void_p), ("chunks", ctypes.c_int32),
+                ("overlap", ctypes.c_int32)]
 
 _lib = None
 P = ctypes.c_void_p

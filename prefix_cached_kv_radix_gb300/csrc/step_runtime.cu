@@ -59,6 +59,14 @@ struct Pipe {
     const void* p_dq = nullptr;
     int64_t p_T = 0;
     std::vector<int32_t> p_cut;       // the request ranges they were cut into
+    // Release events of device input rows: recorded on the compute stream after the kernels of
+    // the last host-buffer step that read the rows at d_q (the last four buffers).
+    struct Release {
+        const void* d_q = nullptr;
+        cudaEvent_t ev = nullptr;
+    };
+    Release rel[4];
+    int rel_next = 0;
 };
 std::mutex g_pipe_mu;
 std::unordered_map<int, Pipe> g_pipes;
@@ -115,7 +123,8 @@ std::vector<int32_t> range_cuts(const rx_attn_desc* d, const int64_t* qo, int32_
 
 // The input copies of ranges c_begin .. c_end-1: on `stream` itself for a single range, else
 // on the copy-in stream, each range's completion recorded in its event.  `start`: the copy
-// streams first wait for the work already on `stream` (the first copies of a step).
+// streams first wait for the work already on `stream` (the first copies of a step) -- with
+// io->overlap, only for the kernels of the last step that read io->d_q, when it is tracked.
 int copy_in(Pipe* pp, const rx_attn_desc* d, const rx_step_io* io, const int64_t* qo, const std::vector<int32_t>& cut,
             int c_begin, int c_end, bool start, cudaStream_t stream) {
     const RowBytes rb = row_bytes(d);
@@ -123,9 +132,16 @@ int copy_in(Pipe* pp, const rx_attn_desc* d, const rx_step_io* io, const int64_t
     cudaStream_t s_in = nc > 1 ? pp->in : stream;
     cudaError_t e = cudaSuccess;
     if (nc > 1 && start) {
-        e = cudaEventRecord(pp->ev[0], stream);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, pp->ev[0], 0);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(pp->out, pp->ev[0], 0);
+        cudaEvent_t w = nullptr;
+        if (io->overlap)
+            for (const Pipe::Release& r : pp->rel)
+                if (r.ev && r.d_q == io->d_q) w = r.ev;
+        if (!w) {
+            w = pp->ev[0];
+            e = cudaEventRecord(w, stream);
+        }
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, w, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(pp->out, w, 0);
     }
     for (int c = c_begin; c < c_end && e == cudaSuccess; ++c) {
         const int64_t t0 = qo[cut[(size_t)c]], t1 = qo[cut[(size_t)c + 1]];
@@ -327,6 +343,18 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
             if (e == cudaSuccess && io->h_lse && io->d_lse)
                 e = cudaMemcpyAsync(io->h_lse + t0 * desc->hq, io->d_lse + t0 * desc->hq, (size_t)((t1 - t0) * desc->hq * 4),
                                     cudaMemcpyDeviceToHost, s_out);
+        }
+        if (e == cudaSuccess && host) {   // the step's kernels are done with its input rows
+            Pipe::Release* r = nullptr;
+            for (Pipe::Release& x : pp->rel)
+                if (x.ev && x.d_q == io->d_q) r = &x;
+            if (!r) {
+                r = &pp->rel[pp->rel_next];
+                pp->rel_next = (pp->rel_next + 1) % 4;
+                if (!r->ev) e = cudaEventCreateWithFlags(&r->ev, cudaEventDisableTiming);
+                r->d_q = io->d_q;
+            }
+            if (e == cudaSuccess) e = cudaEventRecord(r->ev, stream);
         }
         if (e == cudaSuccess && host && ranged) {   // `stream` completes only after the last output copy
             e = cudaEventRecord(pp->ev[1], pp->out);

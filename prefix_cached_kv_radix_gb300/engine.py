@@ -242,7 +242,7 @@ class PrefixCacheEngine:
 
     def step(self, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse=None, decode: bool = False,
              groups=False, min_shared: int = 64, evict_tokens: int = 0, stream=None, host=None,
-             chunks: int = 0) -> StepPlan:
+             chunks: int = 0, overlap: bool = False) -> StepPlan:
         """A whole step in two library calls: rx_step_plan (a1, a2, groups, pinning, into a
         pinned staging buffer) and rx_step_launch (the one H2D copy, a3, a4 or a5/a6, then
         a7/a8 and unpinning).  q/k_new/v_new are the step's new rows in request order; out
@@ -250,8 +250,11 @@ class PrefixCacheEngine:
         tensors of the same shapes) the rows come from and the output goes to host memory,
         copied by the library as a pipeline of `chunks` request ranges (0: automatic): the
         input copies start before the plan (rx_step_prefetch) and run behind the kernels with
-        the output copies; they are complete when the stream is.  Returns the plan (its index arrays
-        stay readable until the plan after next)."""
+        the output copies; they are complete when the stream is.  overlap=True (host mode): the
+        input copies wait only for the kernels of the last step that read the same q buffer, not
+        for all work on the stream -- with two sets of device rows used in turn, a step's copies
+        run under the previous step's kernels (nothing else may still read q/k_new/v_new).
+        Returns the plan (its index arrays stay readable until the plan after next)."""
         st = self._stream if stream is None else stream
         io = self._io
         if io is None:
@@ -262,10 +265,11 @@ class PrefixCacheEngine:
             io.h_q, io.h_k_new, io.h_v_new, io.h_out = (x.data_ptr() for x in host[:4])
             io.h_lse = host[4].data_ptr() if len(host) > 4 and host[4] is not None else None
             io.chunks = int(chunks)
+            io.overlap = 1 if overlap else 0
             api.rx_step_prefetch(self.desc, n_new, io, st.cuda_stream)
         else:
             io.h_q = io.h_k_new = io.h_v_new = io.h_out = io.h_lse = None
-            io.chunks = 0
+            io.chunks = io.overlap = 0
         plan = self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)
         L = plan.layout
         # the step's device buffers: grown when needed; their addresses go into io only then

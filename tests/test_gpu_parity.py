@@ -511,6 +511,51 @@ def test_host_buffer_step_equals_device_step(chunks):
             compare(o_h[qo[b]:qo[b + 1]], want, f"request {b}")
 
 
+def test_host_buffer_steps_overlap_back_to_back():
+    """Host-buffer steps back to back with overlap: two sets of device rows used in turn, each
+    step's input copies waiting only for the kernels of the last step that read the same rows
+    (so they run under the previous step's kernels), no synchronize between steps.  Every
+    step's output equals, bit for bit, the same step run one at a time on device rows."""
+    from prefix_cached_kv_radix_gb300.engine import _dev_from_host
+    spec = W.Spec("gqa4-ragged-overlap", "bf16", 32, 8, 128, 1 << 14, W.QWEN_VOCAB, 33,
+                  seg_parent=[-1, 0], seg_len=[300, 77], histories=[1],
+                  req_seg=[1, 0, 0, 1, 0, 1], req_cached=[377, 150, 0, 377, 300, 200],
+                  req_new=[130, 200, 37, 1, 0, 64])
+    w = W.generate(spec)
+    rng = np.random.default_rng(5)
+    q, kn, vn = w.stacked_new()
+    steps = []
+    for j in range(4):   # fresh new tokens and different rows at every step
+        prompts = [np.concatenate([w.request_prefix_tokens(b),
+                                   rng.integers(1, spec.vocab, size=spec.req_new[b])]).astype(np.int32)
+                   for b in range(w.batch)]
+        ind = np.concatenate([[0], np.cumsum([len(x) for x in prompts])]).astype(np.int64)
+        steps.append((np.concatenate(prompts).astype(np.int32), ind, 1.0 + 0.25 * j))
+    ref = []
+    eng = _engine_for(w)
+    base = [_dev_from_host(x, spec.dtype, eng.device) for x in (q, kn, vn)]
+    out = torch.empty_like(base[0])
+    for toks, ind, sc in steps:
+        rows = [x * sc for x in base]
+        eng.step(toks, ind, spec.req_new, *rows, out)
+        torch.cuda.synchronize()
+        ref.append(to_host_f32(out))
+    assert eng.device_status() == 0
+    eng = _engine_for(w)
+    sets = [[torch.zeros_like(x) for x in base] for _ in range(2)]
+    out = torch.empty_like(base[0])
+    host_rows = [[(x * sc).cpu().pin_memory() for x in base] for _, _, sc in steps]
+    outs_h = [torch.full(out.shape, float("nan"), dtype=out.dtype).pin_memory() for _ in steps]
+    for j, (toks, ind, _) in enumerate(steps):
+        eng.step(toks, ind, spec.req_new, *sets[j % 2], out, host=(*host_rows[j], outs_h[j]), chunks=3,
+                 overlap=True)
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
+    eng.tree.check()
+    for j in range(len(steps)):
+        assert np.array_equal(outs_h[j].float().numpy(), ref[j]), f"step {j}"
+
+
 def test_host_buffer_decode_chunks_match_oracle():
     from prefix_cached_kv_radix_gb300.engine import _dev_from_host
     spec = small_decode(seed=27)

@@ -49,16 +49,20 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------------------- ncu traffic
+# the sources of the attention call's kernels (the ones the recorded counters cover)
+ATTENTION_SOURCES = ("attention_simt.cu", "decode_attention.cu", "extend_attention.cu", "rx_common.h",
+                     "rx_device.cuh", "rx_kernels.h")
+
+
 def kernel_source_hash() -> str:
-    """Digest of the kernel sources (CUDA files and the headers they include): DRAM counters
-    recorded for one version of the kernels are reported only while those are unchanged."""
+    """Digest of the attention kernels' sources (CUDA files and the headers they include): DRAM
+    counters recorded for one version of those kernels are reported only while it is unchanged."""
     import hashlib
     csrc = os.path.join(ROOT, "prefix_cached_kv_radix_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in ATTENTION_SOURCES:
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 

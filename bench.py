@@ -223,6 +223,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     spec = W.config(args.workload)
+    if args.requests:
+        spec = W.take_requests(spec, args.requests)
     if args.pool_slots:
         spec.num_slots = args.pool_slots
     w = W.generate(spec)
@@ -519,6 +521,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunks", type=int, default=0,
                     help="request ranges of the e2e copy pipeline (0: chosen by the library)")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="profiling only: the workload's first N requests (same per-request shapes)")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="override the KV pool size (profiling captures keep the device footprint small)")
     args = ap.parse_args()

@@ -332,6 +332,28 @@ def config(name: str) -> Spec:
 CONFIG_NAMES = ("c1", "c2", "c3", "c4", "c5")
 
 
+def take_requests(spec: Spec, n: int) -> Spec:
+    """The first n requests of ``spec`` with the segments on their paths (renumbered, parents
+    kept) and only those histories: the same per-request shapes at a smaller footprint, for
+    profiling captures.  Token and tensor values differ from the full workload's (they are
+    drawn per segment and request index)."""
+    n = max(0, min(n, len(spec.req_seg)))
+    keep = set()
+    for sg in spec.req_seg[:n]:
+        while sg >= 0 and sg not in keep:
+            keep.add(sg)
+            sg = spec.seg_parent[sg]
+    order = sorted(keep)
+    new_id = {old: i for i, old in enumerate(order)}
+    remap = lambda sg: new_id[sg] if sg >= 0 else -1
+    return Spec(f"{spec.name}-first{n}", spec.dtype, spec.hq, spec.hkv, spec.d, spec.num_slots, spec.vocab, spec.seed,
+                seg_parent=[remap(spec.seg_parent[o]) for o in order], seg_len=[spec.seg_len[o] for o in order],
+                histories=[new_id[h] for h in spec.histories if h in keep],
+                req_seg=[remap(x) for x in spec.req_seg[:n]], req_cached=list(spec.req_cached[:n]),
+                req_new=list(spec.req_new[:n]), decode=spec.decode,
+                note=f"{spec.note}, first {n} requests")
+
+
 # ---------------------------------------------------------------------------- request traces
 @dataclass
 class Session:

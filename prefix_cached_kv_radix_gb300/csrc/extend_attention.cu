@@ -264,16 +264,21 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
         // Gather one K or V tile (zero fill where sl < 0); the full barrier gets this thread's
         // arrival when its copies have landed (cp.async.mbarrier.arrive), so a loader never
         // waits for its own copies, only for free ring slots.
-        auto issue = [&](uint32_t buf, const __nv_bfloat16* pool, uint32_t full) {
+        // This thread copies the same 16-byte chunk (lt % CPR) of every key row it handles
+        // (EXT_LOADERS is a multiple of CPR): its pool addresses differ by slot * row pitch only.
+        static_assert(EXT_LOADERS % CPR == 0, "loader chunk per thread");
+        const uint32_t pitch = (uint32_t)(p.hkv * D * 2);
+        const char* kb = reinterpret_cast<const char*>(p.k_pool + (size_t)g * D + (lt % CPR) * 8);
+        const char* vb = reinterpret_cast<const char*>(p.v_pool + (size_t)g * D + (lt % CPR) * 8);
+        auto issue = [&](uint32_t buf, const char* pb, uint32_t full) {
 #pragma unroll
             for (int x = 0; x < NX; ++x) {
                 const int q = lt + EXT_LOADERS * x;
                 if (q < EXT_BN * CPR) {
                     const int key = q / CPR, c = q % CPR;
-                    const int64_t off = ((int64_t)max(sl[x], 0) * p.hkv + g) * D + c * 8;
                     const uint32_t so =
                         (uint32_t)((c >> 3) * EXT_BN * 128 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
-                    cp_async_16(buf + so, pool + off, sl[x] >= 0 ? 16u : 0u);
+                    cp_async_16(buf + so, pb + (size_t)(uint32_t)max(sl[x], 0) * pitch, sl[x] >= 0 ? 16u : 0u);
                 }
             }
             cp_async_arrive_noinc(full);
@@ -290,9 +295,9 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
                 sl[x] = (in && valid) ? sl[x] : -1;
             }
             if (bad) report(p.status, RX_DEV_BAD_SLOT);
-            issue(base + LY::OFF_K + ks * LY::KV_TILE, p.k_pool, bar(LY::BAR_KF + ks));
+            issue(base + LY::OFF_K + ks * LY::KV_TILE, kb, bar(LY::BAR_KF + ks));
             if (j >= NV && !warp_wait(bar(LY::BAR_VE + vs), ((j / NV) - 1) & 1, abort_flag, p.status)) break;
-            issue(base + LY::OFF_V + vs * LY::KV_TILE, p.v_pool, bar(LY::BAR_VF + vs));
+            issue(base + LY::OFF_V + vs * LY::KV_TILE, vb, bar(LY::BAR_VF + vs));
             if (j + 1 < nkv) load_slots(j + 1);
         }
         cp_async_wait_all();                   // no copy may still be landing at teardown

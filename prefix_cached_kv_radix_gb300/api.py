@@ -149,6 +149,16 @@ def _np_i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 
+def _addr(a: np.ndarray) -> int:
+    """Host address of a contiguous numpy array.  Through a ctypes view of its buffer: about a
+    third of the cost of `_addr(a)` per call, which adds up on the per-step calls (the
+    array's own `ctypes` path for read-only arrays, which cannot be viewed that way)."""
+    try:
+        return ctypes.addressof(ctypes.c_char.from_buffer(a))
+    except (TypeError, ValueError):
+        return a.ctypes.data
+
+
 def _ptr(t):
     """Device pointer of a tensor, or an integer device address (None -> NULL)."""
     if t is None:
@@ -192,7 +202,7 @@ def match_prefix(tree, tokens):
     tok = _np_i32(tokens)
     out = np.empty(max(len(tok), 1), np.int32)
     n, last = I64(), I64()
-    _check("match_prefix", load().match_prefix(tree, tok.ctypes.data, len(tok), out.ctypes.data,
+    _check("match_prefix", load().match_prefix(tree, _addr(tok), len(tok), _addr(out),
                                                ctypes.byref(n), ctypes.byref(last)))
     return out[: n.value].copy(), n.value, last.value
 
@@ -201,7 +211,7 @@ def match_prefix_len(tree, tokens) -> int:
     """Length of the longest cached prefix, without touching the tree (no stamp, no split)."""
     tok = _np_i32(tokens)
     n = I64()
-    _check("match_prefix_len", load().match_prefix_len(tree, tok.ctypes.data, len(tok), ctypes.byref(n)))
+    _check("match_prefix_len", load().match_prefix_len(tree, _addr(tok), len(tok), ctypes.byref(n)))
     return n.value
 
 
@@ -210,8 +220,8 @@ def match_prefix_len_batch(tree, tokens, tok_indptr) -> np.ndarray:
     ind = np.ascontiguousarray(np.asarray(tok_indptr, np.int64))
     b = len(ind) - 1
     out = np.empty(max(b, 1), np.int64)
-    _check("match_prefix_len_batch", load().match_prefix_len_batch(tree, b, tok.ctypes.data, ind.ctypes.data,
-                                                                   out.ctypes.data))
+    _check("match_prefix_len_batch", load().match_prefix_len_batch(tree, b, _addr(tok), _addr(ind),
+                                                                   _addr(out)))
     return out[:b].copy()
 
 
@@ -236,31 +246,31 @@ def insert_batch_at(tree, nodes, tokens, tok_indptr, new_slots, new_indptr):
     b = len(nd)
     dup = np.empty(max(b, 1), np.int64)
     last = np.empty(max(b, 1), np.int64)
-    _check("insert_batch_at", load().insert_batch_at(tree, b, nd.ctypes.data, tok.ctypes.data, ind.ctypes.data,
-                                                     sl.ctypes.data if len(sl) else None, nind.ctypes.data,
-                                                     dup.ctypes.data, last.ctypes.data))
+    _check("insert_batch_at", load().insert_batch_at(tree, b, _addr(nd), _addr(tok), _addr(ind),
+                                                     _addr(sl) if len(sl) else None, _addr(nind),
+                                                     _addr(dup), _addr(last)))
     return dup[:b].copy(), last[:b].copy()
 
 
 def radix_lock_batch(tree, nodes) -> None:
     a = np.ascontiguousarray(np.asarray(nodes, np.int64))
-    _check("radix_lock_batch", load().radix_lock_batch(tree, a.ctypes.data if len(a) else None, len(a)))
+    _check("radix_lock_batch", load().radix_lock_batch(tree, _addr(a) if len(a) else None, len(a)))
 
 
 def radix_unlock_batch(tree, nodes) -> None:
     a = np.ascontiguousarray(np.asarray(nodes, np.int64))
-    _check("radix_unlock_batch", load().radix_unlock_batch(tree, a.ctypes.data if len(a) else None, len(a)))
+    _check("radix_unlock_batch", load().radix_unlock_batch(tree, _addr(a) if len(a) else None, len(a)))
 
 
 def alloc_slots(tree, n: int) -> np.ndarray:
     out = np.empty(max(n, 1), np.int32)
-    _check("alloc_slots", load().alloc_slots(tree, n, out.ctypes.data))
+    _check("alloc_slots", load().alloc_slots(tree, n, _addr(out)))
     return out[:n].copy()
 
 
 def free_slots(tree, slots) -> None:
     s = _np_i32(slots)
-    _check("free_slots", load().free_slots(tree, s.ctypes.data if len(s) else None, len(s)))
+    _check("free_slots", load().free_slots(tree, _addr(s) if len(s) else None, len(s)))
 
 
 def insert(tree, tokens, slots):
@@ -268,8 +278,8 @@ def insert(tree, tokens, slots):
     tok, sl = _np_i32(tokens), _np_i32(slots)
     assert len(tok) == len(sl)
     dup, last = I64(), I64()
-    _check("insert", load().insert(tree, tok.ctypes.data if len(tok) else None,
-                                   sl.ctypes.data if len(sl) else None, len(tok),
+    _check("insert", load().insert(tree, _addr(tok) if len(tok) else None,
+                                   _addr(sl) if len(sl) else None, len(tok),
                                    ctypes.byref(dup), ctypes.byref(last)))
     return dup.value, last.value
 
@@ -280,7 +290,7 @@ def evict(tree, num_tokens: int, cap: int | None = None) -> np.ndarray:
     n = I64()
     c = radix_stats(tree)["cached_tokens"] if cap is None else cap   # at most everything cached
     out = np.empty(max(c, 1), np.int32)
-    _check("evict", load().evict(tree, num_tokens, out.ctypes.data, c, ctypes.byref(n)))
+    _check("evict", load().evict(tree, num_tokens, _addr(out), c, ctypes.byref(n)))
     return out[: min(n.value, c)].copy()
 
 
@@ -300,8 +310,8 @@ def match_prefix_batch(tree, tokens, tok_indptr):
     out = np.empty(max(len(tok), 1), np.int32)
     oind = np.empty(b + 1, np.int64)
     last = np.empty(max(b, 1), np.int64)
-    _check("match_prefix_batch", load().match_prefix_batch(tree, b, tok.ctypes.data, ind.ctypes.data, out.ctypes.data,
-                                                           oind.ctypes.data, last.ctypes.data))
+    _check("match_prefix_batch", load().match_prefix_batch(tree, b, _addr(tok), _addr(ind), _addr(out),
+                                                           _addr(oind), _addr(last)))
     return out[: oind[b]].copy(), oind, last[:b].copy()
 
 
@@ -313,8 +323,8 @@ def insert_batch(tree, tokens, tok_indptr, slots):
     assert len(tok) == len(sl) == ind[b]
     dup = np.empty(max(b, 1), np.int64)
     last = np.empty(max(b, 1), np.int64)
-    _check("insert_batch", load().insert_batch(tree, b, tok.ctypes.data, ind.ctypes.data, sl.ctypes.data,
-                                               dup.ctypes.data, last.ctypes.data))
+    _check("insert_batch", load().insert_batch(tree, b, _addr(tok), _addr(ind), _addr(sl),
+                                               _addr(dup), _addr(last)))
     return dup[:b].copy(), last[:b].copy()
 
 
@@ -335,8 +345,8 @@ def radix_shared_groups(tree, last_nodes, min_shared: int = 1):
     gof = np.empty(max(b, 1), np.int32)
     glen = np.empty(max(b, 1), np.int64)
     ng = I32()
-    _check("radix_shared_groups", load().radix_shared_groups(tree, ln.ctypes.data, b, min_shared, gof.ctypes.data,
-                                                             glen.ctypes.data, ctypes.byref(ng)))
+    _check("radix_shared_groups", load().radix_shared_groups(tree, _addr(ln), b, min_shared, _addr(gof),
+                                                             _addr(glen), ctypes.byref(ng)))
     return gof[:b].copy(), glen[: ng.value].copy()
 
 
@@ -352,8 +362,8 @@ def rx_step_plan(tree, tokens: np.ndarray, tok_indptr: np.ndarray, n_new: np.nda
     b = len(tok_indptr) - 1
     lay = rx_step_layout()
     _check("rx_step_plan", load().rx_step_plan(
-        tree, b, tokens.ctypes.data, tok_indptr.ctypes.data, n_new.ctypes.data if b else None,
-        group_mode, heads_per_kv, min_shared, stage_addr, stage_cap, out_last.ctypes.data if b else None,
+        tree, b, _addr(tokens), _addr(tok_indptr), _addr(n_new) if b else None,
+        group_mode, heads_per_kv, min_shared, stage_addr, stage_cap, _addr(out_last) if b else None,
         ctypes.byref(lay)))
     return lay
 
@@ -363,8 +373,8 @@ def rx_step_finish(tree, tokens: np.ndarray, tok_indptr: np.ndarray, last_nodes:
     """Returns the number of slots evicted."""
     n = I64()
     _check("rx_step_finish", load().rx_step_finish(
-        tree, layout.batch, tokens.ctypes.data, tok_indptr.ctypes.data,
-        last_nodes.ctypes.data if layout.batch else None, stage_addr, ctypes.byref(layout), evict_tokens,
+        tree, layout.batch, _addr(tokens), _addr(tok_indptr),
+        _addr(last_nodes) if layout.batch else None, stage_addr, ctypes.byref(layout), evict_tokens,
         ctypes.byref(n)))
     return n.value
 
@@ -376,7 +386,7 @@ def rx_step_workspace_bytes(desc, layout, decode: bool) -> int:
 def rx_step_prefetch(desc, n_new: np.ndarray, io, stream) -> None:
     """Start the host-buffer copies of a step's new rows before it is planned."""
     nn = np.ascontiguousarray(np.asarray(n_new, np.int32))
-    _check("rx_step_prefetch", load().rx_step_prefetch(ctypes.byref(desc), len(nn), nn.ctypes.data if len(nn) else None,
+    _check("rx_step_prefetch", load().rx_step_prefetch(ctypes.byref(desc), len(nn), _addr(nn) if len(nn) else None,
                                                        ctypes.byref(io), _stream(stream)))
 
 
@@ -386,8 +396,8 @@ def rx_step_launch(tree, desc, tokens: np.ndarray, tok_indptr: np.ndarray, last_
     number of slots evicted."""
     n = I64()
     _check("rx_step_launch", load().rx_step_launch(
-        tree, ctypes.byref(desc), tokens.ctypes.data, tok_indptr.ctypes.data,
-        last_nodes.ctypes.data if layout.batch else None, stage_addr, ctypes.byref(layout), ctypes.byref(io),
+        tree, ctypes.byref(desc), _addr(tokens), _addr(tok_indptr),
+        _addr(last_nodes) if layout.batch else None, stage_addr, ctypes.byref(layout), ctypes.byref(io),
         evict_tokens, ctypes.byref(n), _stream(stream)))
     return n.value
 

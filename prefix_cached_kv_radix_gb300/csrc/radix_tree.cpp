@@ -175,7 +175,16 @@ struct rx_radix {
     std::unordered_map<int64_t, rx::Node*> by_id;
     rx_stats st{};
 
-    ~rx_radix() { destroy_children(&root); }
+    // Evicted nodes, kept for reuse: a node's edge vectors and child map keep their capacity,
+    // so the steady state of insert and evict (a step's leaves in, an older step's out)
+    // allocates nothing.  At most kSpareNodes are kept.
+    static constexpr size_t kSpareNodes = 4096;
+    std::vector<rx::Node*> spare;
+
+    ~rx_radix() {
+        destroy_children(&root);
+        for (rx::Node* n : spare) delete n;
+    }
 
     void destroy_children(rx::Node* x) {
         std::vector<rx::Node*> stack;
@@ -196,7 +205,20 @@ struct rx_radix {
     }
 
     rx::Node* new_node() {
-        rx::Node* n = new rx::Node();
+        rx::Node* n;
+        if (!spare.empty()) {
+            n = spare.back();
+            spare.pop_back();
+            n->parent = nullptr;
+            n->key.clear();
+            n->slots.clear();
+            n->children.clear();
+            n->stamp = 0;
+            n->ref = 0;
+            n->depth = 0;
+        } else {
+            n = new rx::Node();
+        }
         n->id = next_id++;
         by_id[n->id] = n;
         ++st.node_count;
@@ -536,7 +558,8 @@ int evict(rx_radix* t, int64_t num_tokens, int32_t* out_freed, int64_t cap, int6
         t->st.cached_tokens -= (int64_t)x->key.size();
         t->by_id.erase(x->id);
         --t->st.node_count;
-        delete x;
+        if (t->spare.size() < rx_radix::kSpareNodes) t->spare.push_back(x);
+        else delete x;
         if (p != &t->root && p->children.empty() && p->ref == 0) heap.emplace(p->stamp, p->id, p);
     }
     t->st.evicted_tokens += freed;

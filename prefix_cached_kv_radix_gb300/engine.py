@@ -267,7 +267,7 @@ class PrefixCacheEngine:
             io.chunks = int(chunks)
             io.overlap = 1 if overlap else 0
             api.rx_step_prefetch(self.desc, n_new, io, st.cuda_stream)
-        else:
+        elif io.h_q:
             io.h_q = io.h_k_new = io.h_v_new = io.h_out = io.h_lse = None
             io.chunks = io.overlap = 0
         plan = self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)

@@ -66,6 +66,32 @@ def test_lock_semantics():
     t.check()
 
 
+def test_recycled_nodes_get_new_handles():
+    """Evicted nodes are recycled for later inserts (their storage, not their handles): the
+    handle of an evicted node stays unknown after its memory holds a new node, new handles
+    never repeat, and the tree checks out over many insert/evict rounds."""
+    t = api.RadixTree(512, 3)
+    rng = np.random.default_rng(7)
+    dead, seen = [], set()
+    for rnd in range(30):
+        live = []
+        for i in range(8):                       # eight fresh leaves under distinct first tokens
+            toks = [1000 * rnd + i] + rng.integers(0, 9, size=int(rng.integers(1, 6))).tolist()
+            sl = t.alloc_slots(len(toks))
+            dup, node = t.insert(toks, sl)
+            assert dup == 0 and node not in seen
+            seen.add(node)
+            live.append(node)
+        t.check()
+        for node in dead[-16:]:                  # handles of nodes whose storage may now be reused
+            with pytest.raises(api.RxError):
+                t.lock(node)
+        assert len(t.evict(10 ** 6)) > 0         # everything goes: the next round reuses it
+        dead.extend(live)
+        t.check()
+    assert t.stats()["node_count"] == 0
+
+
 def _run_script(ops, num_slots, seed):
     """Apply the same operations to the C++ tree and the oracle model; compare everything."""
     t = api.RadixTree(num_slots, seed)

@@ -5,12 +5,16 @@
 // written once into their pool slots, and each request's slot table lists its matched
 // (shared) slots followed by its new slots, so attention can gather the whole context.
 //
-// One launch, two kinds of blocks: the first `batch` blocks each fill one table row
-// (coalesced int32 stores); the rest copy 16-byte vectors of the new K/V rows to their
-// slots (consecutive threads copy consecutive vectors of a row: coalesced reads, and
-// full 32-byte sectors on the scattered writes).  HBM-bound: the algorithmic bytes are
-// 2 * T * hkv * head_dim * elt read + the same written + the table.
+// One launch, two kinds of blocks: the first batch * tiles blocks each fill one tile of
+// KPW_TILE entries of a table row (coalesced int32 stores; each thread has KPW_PER
+// independent loads in flight, so a long row is not one block's chain of dependent round
+// trips); the rest copy 16-byte vectors of the new K/V rows to their slots (consecutive
+// threads copy consecutive vectors of a row: coalesced reads, and full 32-byte sectors on
+// the scattered writes).  HBM-bound: the algorithmic bytes are 2 * T * hkv * head_dim * elt
+// read + the same written + the table.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "radix_attn.h"
 #include "rx_common.h"
@@ -19,39 +23,51 @@
 
 namespace rx {
 
-__global__ void __launch_bounds__(256) kv_pool_write_kernel(
-    int32_t batch, const int32_t* __restrict__ prefix_slots, const int64_t* __restrict__ prefix_indptr,
+constexpr int KPW_THREADS = 256;
+constexpr int KPW_PER = 4;                           // table entries per thread
+constexpr int KPW_TILE = KPW_THREADS * KPW_PER;      // table entries per block
+
+__global__ void __launch_bounds__(KPW_THREADS) kv_pool_write_kernel(
+    int32_t batch, int32_t tiles, const int32_t* __restrict__ prefix_slots, const int64_t* __restrict__ prefix_indptr,
     const int32_t* __restrict__ new_slots, const int64_t* __restrict__ qo_indptr, const uint4* __restrict__ k_new,
     const uint4* __restrict__ v_new, uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
     int32_t* __restrict__ r2t, int64_t stride, int64_t num_slots, int32_t row_vecs, int64_t t_begin, int64_t t_end,
     int32_t* status) {
-    if ((int)blockIdx.x < batch) {
-        const int b = blockIdx.x;
+    const int64_t table_blocks = (int64_t)batch * tiles;
+    if ((int64_t)blockIdx.x < table_blocks) {
+        const int b = (int)(blockIdx.x / tiles);
+        const int64_t j0 = (int64_t)(blockIdx.x % tiles) * KPW_TILE;
         const int64_t p0 = prefix_indptr[b], P = prefix_indptr[b + 1] - p0;
         const int64_t q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0;
         int32_t* row = r2t + (int64_t)b * stride;
         const bool bad_len = P < 0 || n < 0 || P + n > stride || q0 < t_begin || q0 + n > t_end;
-        if (bad_len && threadIdx.x == 0) report(status, RX_DEV_BAD_LENGTH);
-        for (int64_t j = threadIdx.x; j < stride; j += blockDim.x) {
-            int32_t s = -1;
-            if (!bad_len) {
-                if (j < P)
-                    s = prefix_slots[p0 + j];
-                else if (j < P + n)
-                    s = new_slots[q0 + (j - P)];
-                if (s < -1 || s >= num_slots || (s == -1 && j < P + n)) {
-                    report(status, RX_DEV_BAD_SLOT);
-                    s = -1;
-                }
+        if (bad_len && j0 == 0 && threadIdx.x == 0) report(status, RX_DEV_BAD_LENGTH);
+        int32_t s[KPW_PER];
+#pragma unroll
+        for (int u = 0; u < KPW_PER; ++u) {          // the loads first, all in flight together
+            const int64_t j = j0 + threadIdx.x + (int64_t)u * KPW_THREADS;
+            s[u] = -1;
+            if (!bad_len && j < P)
+                s[u] = prefix_slots[p0 + j];
+            else if (!bad_len && j < P + n)
+                s[u] = new_slots[q0 + (j - P)];
+        }
+#pragma unroll
+        for (int u = 0; u < KPW_PER; ++u) {
+            const int64_t j = j0 + threadIdx.x + (int64_t)u * KPW_THREADS;
+            if (j >= stride) break;
+            if (s[u] < -1 || s[u] >= num_slots || (s[u] == -1 && !bad_len && j < P + n)) {
+                report(status, RX_DEV_BAD_SLOT);
+                s[u] = -1;
             }
-            row[j] = s;
+            row[j] = s[u];
         }
         return;
     }
     // new tokens t_begin .. t_end-1 (the rows of this call's requests)
     const int64_t nvec = (t_end - t_begin) * row_vecs;
-    const int64_t step = (int64_t)(gridDim.x - batch) * blockDim.x;
-    for (int64_t j = (int64_t)(blockIdx.x - batch) * blockDim.x + threadIdx.x; j < nvec; j += step) {
+    const int64_t step = (int64_t)(gridDim.x - table_blocks) * blockDim.x;
+    for (int64_t j = (int64_t)(blockIdx.x - table_blocks) * blockDim.x + threadIdx.x; j < nvec; j += step) {
         const int64_t i = t_begin * row_vecs + j;
         const int64_t t = i / row_vecs;
         const int32_t v = (int32_t)(i - t * row_vecs);
@@ -88,13 +104,14 @@ int kv_pool_write_rows(const rx_attn_desc* desc, int32_t batch, const int32_t* d
         RX_REQUIRE(((uintptr_t)p & 15) == 0, "kv_pool_write: K/V buffers must be 16-byte aligned");
     const int32_t row_vecs = (int32_t)(row_bytes / 16);
     const int64_t nvec = (t_end - t_begin) * row_vecs;
-    int64_t copy_blocks = (nvec + 255) / 256;
+    int64_t copy_blocks = (nvec + KPW_THREADS - 1) / KPW_THREADS;
     if (copy_blocks > 152 * 16) copy_blocks = 152 * 16;
     if (copy_blocks < 1) copy_blocks = 1;
-    const int64_t grid = (int64_t)batch + copy_blocks;
-    RX_REQUIRE(grid < (1ll << 31), "kv_pool_write: batch too large");
-    kv_pool_write_kernel<<<(unsigned)grid, 256, 0, stream>>>(
-        batch, d_prefix_slots, d_prefix_indptr, d_new_slots, d_qo_indptr, (const uint4*)d_k_new,
+    const int64_t tiles = std::max<int64_t>(1, (r2t_stride + KPW_TILE - 1) / KPW_TILE);
+    const int64_t grid = (int64_t)batch * tiles + copy_blocks;
+    RX_REQUIRE(grid < (1ll << 31) && tiles < (1ll << 31), "kv_pool_write: batch or stride too large");
+    kv_pool_write_kernel<<<(unsigned)grid, KPW_THREADS, 0, stream>>>(
+        batch, (int32_t)tiles, d_prefix_slots, d_prefix_indptr, d_new_slots, d_qo_indptr, (const uint4*)d_k_new,
         (const uint4*)d_v_new, (uint4*)d_k_pool, (uint4*)d_v_pool, d_req_to_token, r2t_stride, desc->num_slots,
         row_vecs, t_begin, t_end, d_status);
     const cudaError_t e = cudaGetLastError();

@@ -750,7 +750,13 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
     // optional shared-prefix groups ("auto": not for the small-extend shape -- a few rows per
     // (request, kv head) over at most 1024 keys -- which needs no stacking)
     const bool small_shape = (int64_t)max_qo * heads_per_kv <= 8 && max_kv <= 1024;
-    if (group_mode != RX_GROUPS_NONE && batch > 0 && !(group_mode == RX_GROUPS_AUTO && small_shape)) {
+    bool want_groups = group_mode != RX_GROUPS_NONE && batch > 0 && !(group_mode == RX_GROUPS_AUTO && small_shape);
+    // "auto" never stacks a request with 128 or more new rows per kv head: decided from n_new
+    // alone, before the groups are derived from the tree (which would be discarded)
+    if (want_groups && group_mode == RX_GROUPS_AUTO)
+        for (int32_t b = 0; b < batch && want_groups; ++b)
+            if ((int64_t)n_new[b] * heads_per_kv >= 128) want_groups = false;
+    if (want_groups) {
         std::vector<int32_t> gof((size_t)batch);
         std::vector<int64_t> glen((size_t)batch);
         int32_t ng = 0;

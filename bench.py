@@ -276,7 +276,7 @@ def run_ours(args, rank, world, local_rank):
         toks, ind = step_inputs[i]
         q_, k_, v_ = rows_e2e[i % 2] if e2e else (qd, kd, vd)
         plan = eng.step(toks, ind, n_new, q_, k_, v_, out, lse, decode=s.decode, groups=group_mode, evict_tokens=T,
-                        host=(qh, kh, vh, out_h) if e2e else None, chunks=args.chunks, overlap=e2e)
+                        host=(qh, kh, vh, out_h) if e2e else None, chunks=args.chunks, overlap=True)
         launches[0] += n_launch(plan.layout.num_groups > 0, e2e)
         return plan
 

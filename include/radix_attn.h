@@ -416,8 +416,13 @@ typedef struct {
     void* h_out;
     float* h_lse;                 /* optional */
     int32_t chunks;               /* host-buffer mode: request ranges of the pipeline (0: auto) */
-    int32_t overlap;              /* host-buffer mode: 1 = input copies wait only for the last
-                                     step that read the same d_q (see above) */
+    int32_t overlap;              /* 1: host-buffer mode, the input copies wait only for the last
+                                     step that read the same d_q (see above); device rows, the
+                                     index arrays are copied on an internal copy stream after
+                                     the kernels of the last step that read the same d_stage
+                                     (tracked as for d_q), and `stream` waits for the copy --
+                                     with two d_stage buffers in turn, under the previous
+                                     step's kernels */
 } rx_step_io;
 
 size_t rx_step_workspace_bytes(const rx_attn_desc* desc, const rx_step_layout* layout, int32_t decode);

@@ -67,7 +67,36 @@ struct Pipe {
     };
     Release rel[4];
     int rel_next = 0;
+    // The same for device staging buffers (d_stage) of device-row steps with overlap, whose
+    // index-array copy runs on the copy-in stream; `staged` marks the copy's completion.
+    Release srel[4];
+    int srel_next = 0;
+    cudaEvent_t staged = nullptr;
 };
+
+// The release event of `buf` in table r (n entries, round robin), created on first use.
+cudaError_t release_slot(Pipe::Release* r, int n, int* next, const void* buf, cudaEvent_t* out) {
+    for (int i = 0; i < n; ++i)
+        if (r[i].ev && r[i].d_q == buf) {
+            *out = r[i].ev;
+            return cudaSuccess;
+        }
+    Pipe::Release& x = r[*next];
+    *next = (*next + 1) % n;
+    if (!x.ev) {
+        const cudaError_t e = cudaEventCreateWithFlags(&x.ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+    }
+    x.d_q = buf;
+    *out = x.ev;
+    return cudaSuccess;
+}
+
+cudaEvent_t release_of(const Pipe::Release* r, int n, const void* buf) {
+    for (int i = 0; i < n; ++i)
+        if (r[i].ev && r[i].d_q == buf) return r[i].ev;
+    return nullptr;
+}
 std::mutex g_pipe_mu;
 std::unordered_map<int, Pipe> g_pipes;
 
@@ -132,10 +161,7 @@ int copy_in(Pipe* pp, const rx_attn_desc* d, const rx_step_io* io, const int64_t
     cudaStream_t s_in = nc > 1 ? pp->in : stream;
     cudaError_t e = cudaSuccess;
     if (nc > 1 && start) {
-        cudaEvent_t w = nullptr;
-        if (io->overlap)
-            for (const Pipe::Release& r : pp->rel)
-                if (r.ev && r.d_q == io->d_q) w = r.ev;
+        cudaEvent_t w = io->overlap ? release_of(pp->rel, 4, io->d_q) : nullptr;
         if (!w) {
             w = pp->ev[0];
             e = cudaEventRecord(w, stream);
@@ -265,15 +291,36 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
             h_dev = nullptr;
         }
         cudaError_t e = cudaSuccess;
-        if (h_dev && ((uintptr_t)h_dev & 15) == 0 && ((uintptr_t)io->d_stage & 15) == 0 && L->bytes % 16 == 0) {
+        // device rows with overlap: the copy runs on the copy-in stream, after the kernels that
+        // last read this d_stage (when tracked; else after all work on `stream`), and `stream`
+        // waits for it -- under the previous step's kernels when the caller alternates d_stage
+        Pipe* sp = nullptr;
+        std::unique_lock<std::mutex> stage_lock;
+        if (!host && io->overlap) {
+            int rc = pipe_for(2, &sp);
+            if (rc != RX_OK) return rc;
+            stage_lock = std::unique_lock<std::mutex>(sp->use);
+            if (!sp->staged) e = cudaEventCreateWithFlags(&sp->staged, cudaEventDisableTiming);
+            cudaEvent_t w = release_of(sp->srel, 4, io->d_stage);
+            if (e == cudaSuccess && !w) {
+                w = sp->ev[0];
+                e = cudaEventRecord(w, stream);
+            }
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(sp->in, w, 0);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(io->d_stage, h_stage, (size_t)L->bytes, cudaMemcpyHostToDevice, sp->in);
+            if (e == cudaSuccess) e = cudaEventRecord(ev, sp->in);
+            if (e == cudaSuccess) e = cudaEventRecord(sp->staged, sp->in);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, sp->staged, 0);
+        } else if (h_dev && ((uintptr_t)h_dev & 15) == 0 && ((uintptr_t)io->d_stage & 15) == 0 && L->bytes % 16 == 0) {
             const int64_t n = L->bytes / 16;
             const int blocks = (int)std::min<int64_t>(152 * 2, (n + 255) / 256);
             stage_copy_kernel<<<std::max(blocks, 1), 256, 0, stream>>>((const uint4*)h_dev, (uint4*)io->d_stage, n);
             e = cudaGetLastError();
+            if (e == cudaSuccess) e = cudaEventRecord(ev, stream);
         } else {
             e = cudaMemcpyAsync(io->d_stage, h_stage, (size_t)L->bytes, cudaMemcpyHostToDevice, stream);
+            if (e == cudaSuccess) e = cudaEventRecord(ev, stream);
         }
-        if (e == cudaSuccess) e = cudaEventRecord(ev, stream);
         if (e != cudaSuccess) {
             set_error("rx_step_launch: staging copy failed: %s", cudaGetErrorString(e));
             return RX_ECUDA;
@@ -345,16 +392,14 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
                                     cudaMemcpyDeviceToHost, s_out);
         }
         if (e == cudaSuccess && host) {   // the step's kernels are done with its input rows
-            Pipe::Release* r = nullptr;
-            for (Pipe::Release& x : pp->rel)
-                if (x.ev && x.d_q == io->d_q) r = &x;
-            if (!r) {
-                r = &pp->rel[pp->rel_next];
-                pp->rel_next = (pp->rel_next + 1) % 4;
-                if (!r->ev) e = cudaEventCreateWithFlags(&r->ev, cudaEventDisableTiming);
-                r->d_q = io->d_q;
-            }
-            if (e == cudaSuccess) e = cudaEventRecord(r->ev, stream);
+            cudaEvent_t r = nullptr;
+            e = release_slot(pp->rel, 4, &pp->rel_next, io->d_q, &r);
+            if (e == cudaSuccess) e = cudaEventRecord(r, stream);
+        }
+        if (e == cudaSuccess && sp) {     // ... and with its device staging buffer
+            cudaEvent_t r = nullptr;
+            e = release_slot(sp->srel, 4, &sp->srel_next, io->d_stage, &r);
+            if (e == cudaSuccess) e = cudaEventRecord(r, stream);
         }
         if (e == cudaSuccess && host && ranged) {   // `stream` completes only after the last output copy
             e = cudaEventRecord(pp->ev[1], pp->out);

@@ -141,6 +141,7 @@ class PrefixCacheEngine:
         self._pin_used = [False, False]
         self._pin_i = 0
         self._dev_idx = None
+        self._dev_stage = [None, None]  # the one-call path's device copies of the staging buffers
         self._r2t = None
         self._r2t_flat = None     # the one-call path's slot table ([batch, stride] in a flat buffer)
         self._io = None
@@ -250,10 +251,12 @@ class PrefixCacheEngine:
         tensors of the same shapes) the rows come from and the output goes to host memory,
         copied by the library as a pipeline of `chunks` request ranges (0: automatic): the
         input copies start before the plan (rx_step_prefetch) and run behind the kernels with
-        the output copies; they are complete when the stream is.  overlap=True (host mode): the
+        the output copies; they are complete when the stream is.  overlap=True: in host mode the
         input copies wait only for the kernels of the last step that read the same q buffer, not
         for all work on the stream -- with two sets of device rows used in turn, a step's copies
-        run under the previous step's kernels (nothing else may still read q/k_new/v_new).
+        run under the previous step's kernels (nothing else may still read q/k_new/v_new); with
+        device rows the index arrays' copy runs on a copy stream under the previous step's
+        kernels (the engine alternates two device copies of the staging buffer).
         Returns the plan (its index arrays stay readable until the plan after next)."""
         st = self._stream if stream is None else stream
         io = self._io
@@ -267,17 +270,22 @@ class PrefixCacheEngine:
             io.chunks = int(chunks)
             io.overlap = 1 if overlap else 0
             api.rx_step_prefetch(self.desc, n_new, io, st.cuda_stream)
-        elif io.h_q:
-            io.h_q = io.h_k_new = io.h_v_new = io.h_out = io.h_lse = None
-            io.chunks = io.overlap = 0
+        else:
+            if io.h_q:
+                io.h_q = io.h_k_new = io.h_v_new = io.h_out = io.h_lse = None
+                io.chunks = 0
+            io.overlap = 1 if overlap else 0
         plan = self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)
         L = plan.layout
         # the step's device buffers: grown when needed; their addresses go into io only then
         fresh = self._io_static is not io
         total = max(int(L.bytes), 256)
-        if self._dev_idx is None or self._dev_idx.numel() < total:
-            self._dev_idx = torch.empty(max(total, 4096) * 2, dtype=torch.uint8, device=self.device)
-            fresh = True
+        # the device copy of the index arrays alternates with the pinned staging buffer, so that
+        # with overlap a step's copy can run while the previous step's kernels read the other
+        ds = self._dev_stage[plan.stage]
+        if ds is None or ds.numel() < total:
+            ds = self._dev_stage[plan.stage] = torch.empty(max(total, 4096) * 2, dtype=torch.uint8, device=self.device)
+        io.d_stage, io.d_stage_bytes = ds.data_ptr(), ds.numel()
         r2t_need = max(plan.batch, 1) * plan.stride
         if self._r2t_flat is None or self._r2t_flat.numel() < r2t_need:
             self._r2t_flat = torch.empty(r2t_need * 2, dtype=torch.int32, device=self.device)
@@ -292,7 +300,6 @@ class PrefixCacheEngine:
             fresh = True
         if fresh:
             io.d_k_pool, io.d_v_pool = self.k_pool.data_ptr(), self.v_pool.data_ptr()
-            io.d_stage, io.d_stage_bytes = self._dev_idx.data_ptr(), self._dev_idx.numel()
             io.d_r2t, io.r2t_elems = self._r2t_flat.data_ptr(), self._r2t_flat.numel()
             io.d_workspace = self._ws.data_ptr() if self._ws is not None else None
             io.ws_bytes = self._ws.numel() if self._ws is not None else 0

@@ -556,6 +556,44 @@ def test_host_buffer_steps_overlap_back_to_back():
         assert np.array_equal(outs_h[j].float().numpy(), ref[j]), f"step {j}"
 
 
+def test_device_steps_overlap_back_to_back():
+    """Device-row steps back to back with overlap (the index arrays copied on a copy stream
+    under the previous step's kernels, into the engine's two device staging buffers in turn),
+    no synchronize between steps: every step's output equals, bit for bit, the same step run
+    one at a time."""
+    from prefix_cached_kv_radix_gb300.engine import _dev_from_host
+    spec = W.Spec("gqa4-ragged-overlap-dev", "bf16", 32, 8, 128, 1 << 14, W.QWEN_VOCAB, 35,
+                  seg_parent=[-1, 0], seg_len=[300, 77], histories=[1],
+                  req_seg=[1, 0, 0, 1, 0, 1], req_cached=[377, 150, 0, 377, 300, 200],
+                  req_new=[130, 200, 37, 1, 0, 64])
+    w = W.generate(spec)
+    rng = np.random.default_rng(6)
+    q, kn, vn = w.stacked_new()
+    steps = []
+    for j in range(5):
+        prompts = [np.concatenate([w.request_prefix_tokens(b),
+                                   rng.integers(1, spec.vocab, size=spec.req_new[b])]).astype(np.int32)
+                   for b in range(w.batch)]
+        ind = np.concatenate([[0], np.cumsum([len(x) for x in prompts])]).astype(np.int64)
+        steps.append((np.concatenate(prompts).astype(np.int32), ind, 1.0 + 0.25 * j))
+    results = []
+    for overlap in (False, True):
+        eng = _engine_for(w)
+        base = [_dev_from_host(x, spec.dtype, eng.device) for x in (q, kn, vn)]
+        rows = [[x * sc for x in base] for _, _, sc in steps]
+        outs = [torch.empty_like(base[0]) for _ in steps]
+        for j, (toks, ind, _) in enumerate(steps):
+            eng.step(toks, ind, spec.req_new, *rows[j], outs[j], overlap=overlap)
+            if not overlap:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert eng.device_status() == 0
+        eng.tree.check()
+        results.append([to_host_f32(o) for o in outs])
+    for j in range(len(steps)):
+        assert np.array_equal(results[0][j], results[1][j]), f"step {j}"
+
+
 def test_host_buffer_decode_chunks_match_oracle():
     from prefix_cached_kv_radix_gb300.engine import _dev_from_host
     spec = small_decode(seed=27)

@@ -123,7 +123,8 @@ struct ExtRows {
 template <int D, bool EXT = false>
 __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* slots_row, int k_begin, int k_end,
                                           int g, const int64_t* q_off, const int64_t* out_slot, int nrows,
-                                          unsigned char* smem, int32_t* slot_s, ExtRows ext = ExtRows{}) {
+                                          unsigned char* smem, int32_t* slot_s, ExtRows ext = ExtRows{},
+                                          bool slots_staged = false) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;                        // m-tiles of O^T
     constexpr int ROWB = D * 2;
@@ -152,7 +153,8 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
 
     const int nstages = (k_end - k_begin + DEC_STAGE_KEYS - 1) / DEC_STAGE_KEYS;
     const int nk = k_end - k_begin;                  // <= DEC_MAX_CHUNK
-    for (int i = tid; i < nk; i += DEC_THREADS) slot_s[i] = slots_row[k_begin + i];
+    if (!slots_staged)
+        for (int i = tid; i < nk; i += DEC_THREADS) slot_s[i] = slots_row[k_begin + i];
     __syncthreads();
 #pragma unroll
     for (int s = 0; s < DEC_NS - 1; ++s) {
@@ -326,6 +328,19 @@ __global__ void __launch_bounds__(DEC_THREADS) extend_small_kernel(DecodeParams 
                                                                    __nv_bfloat16* out, float* lse) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int g = blockIdx.x, b = blockIdx.y;
+    // The request's slot-table row is loaded first, up to the table's stride (a launch
+    // parameter): its loads are in flight together with the request's offsets instead of
+    // waiting for them (one dependent round trip fewer before the first K/V stage).
+    int32_t* slot_s = reinterpret_cast<int32_t*>(smem + dec_ring_bytes(D));
+    constexpr int PRE = DEC_MAX_CHUNK / DEC_THREADS;
+    const int lim = (int)min(p.stride, (int64_t)DEC_MAX_CHUNK);
+    const int32_t* row = p.r2t + (int64_t)b * p.stride;
+    int32_t pre[PRE];
+#pragma unroll
+    for (int u = 0; u < PRE; ++u) {
+        const int i = (int)threadIdx.x + u * DEC_THREADS;
+        pre[u] = i < lim ? row[i] : -1;
+    }
     const int64_t qo0 = qo_indptr[b];
     const int n = (int)(qo_indptr[b + 1] - qo0);
     const int P = prefix_lens[b];
@@ -342,9 +357,13 @@ __global__ void __launch_bounds__(DEC_THREADS) extend_small_kernel(DecodeParams 
         out_row[r] = (qo0 + rr / p.group) * p.hq + g * p.group + rr % p.group;
         q_off[r] = out_row[r] * D;
     }
+#pragma unroll
+    for (int u = 0; u < PRE; ++u) {
+        const int i = (int)threadIdx.x + u * DEC_THREADS;
+        if (i < lim) slot_s[i] = pre[u];
+    }
     ExtRows ext{P, p.group, out, lse};
-    dec_chunk<D, true>(p, p.r2t + (int64_t)b * p.stride, 0, P + n, g, q_off, out_row, rows, smem,
-                       reinterpret_cast<int32_t*>(smem + dec_ring_bytes(D)), ext);
+    dec_chunk<D, true>(p, row, 0, P + n, g, q_off, out_row, rows, smem, slot_s, ext, true);
 }
 
 int launch_extend_small(const SmallExtendArgs& a, cudaStream_t stream) {

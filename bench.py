@@ -367,7 +367,7 @@ def run_ours(args, rank, world, local_rank):
     ms, ms_e2e = reduce_max([ms, ms_e2e], world, dev)
     att_ms = [a.elapsed_time(b) for a, b in att_ev]
     hbm, bf16, bf16_s, src = load_peaks()
-    att = statistics.mean(att_ms) if att_ms else float("nan")
+    att = statistics.median(att_ms) if att_ms else float("nan")
     # the bound follows the step's arithmetic intensity against the ridge of the two peaks
     intensity = work["flops"] / work["bytes"]
     ridge = bf16 * 1e12 / (hbm * 1e9)

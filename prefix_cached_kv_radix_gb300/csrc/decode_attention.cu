@@ -73,7 +73,8 @@ struct DecodeParams {
     const int32_t* grp_len;
     int32_t grp_chunks;         // shared partial slots per (request, head)
     int32_t grp_rows_max;       // max stacked rows (members * group) of a group
-    const int32_t* group_of;    // [batch] group id or -1 (workspace, filled by a prep kernel)
+    const int32_t* shared_of;   // [batch] keys each request takes from its group's shared run
+                                // (0 outside groups; workspace, filled by the group-map kernel)
     int32_t* group_src;         // [num_groups] first member (its slot-table row holds the shared slots)
 };
 
@@ -298,12 +299,11 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_private_kernel(DecodeParam
     extern __shared__ __align__(1024) unsigned char smem[];
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int32_t L = p.kv_lens[b];
-    const int gid = p.group_of ? p.group_of[b] : -1;   // loaded together with L
+    const int shared = p.shared_of ? p.shared_of[b] : 0;   // loaded together with L
     if (L < 1 || L > p.max_len || L > p.stride) {
         if (c == 0 && g == 0 && threadIdx.x == 0) report(p.status, RX_DEV_BAD_LENGTH);
         return;
     }
-    const int shared = gid >= 0 ? min(p.grp_len[gid], L) : 0;
     const int k_begin = shared + c * p.chunk;
     if (k_begin >= L) return;
     const int k_end = min(L, k_begin + p.chunk);
@@ -418,9 +418,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, __nv_
     if (item >= (int64_t)p.batch * p.hq) return;
     const int b = (int)(item / p.hq);
     const int32_t L = p.kv_lens[b];
-    const int gid = p.group_of ? p.group_of[b] : -1;
+    const int shared = p.shared_of ? p.shared_of[b] : 0;
     if (L < 1 || L > p.max_len || L > p.stride) return;
-    const int shared = gid >= 0 ? min(p.grp_len[gid], L) : 0;
     const int npriv = (L - shared + p.chunk - 1) / p.chunk;
     const int n = npriv + (shared + p.chunk - 1) / p.chunk;   // private chunks, then shared ones
     const int per = p.max_chunks + p.grp_chunks;
@@ -450,11 +449,12 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeParams p, __nv_
     if (lse && lane == 0) lse[item] = (M + log2f(W)) * LN2;
 }
 
-// group_of[b] from the member lists; -1 for requests outside every group.
-// Each request's group (or -1), and each group's source slot-table row (its first member):
-// one block, every request cleared before the groups' members are written.
-__global__ void __launch_bounds__(512) decode_group_map_kernel(DecodeParams p, int32_t* group_of) {
-    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) group_of[b] = -1;
+// Each request's count of shared keys (its group's shared run, cut to its own length; 0 outside
+// every group), and each group's source slot-table row (its first member): one block, every
+// request cleared before the groups' members are written.  The decode kernels then learn where
+// a request's private keys start from one load, beside its length.
+__global__ void __launch_bounds__(512) decode_group_map_kernel(DecodeParams p, int32_t* shared_of) {
+    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) shared_of[b] = 0;
     __syncthreads();
     for (int gid = threadIdx.x; gid < p.num_groups; gid += blockDim.x) p.group_src[gid] = p.grp_members[p.grp_indptr[gid]];
     const int n = p.num_groups > 0 ? p.grp_indptr[p.num_groups] : 0;
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(512) decode_group_map_kernel(DecodeParams p, i
             if (p.grp_indptr[mid] <= i) lo = mid; else hi = mid - 1;
         }
         const int b = p.grp_members[i];
-        if (b >= 0 && b < p.batch) group_of[b] = lo;
+        if (b >= 0 && b < p.batch) shared_of[b] = min(p.grp_len[lo], p.kv_lens[b]);
         else report(p.status, RX_DEV_BAD_LENGTH);
     }
 }
@@ -507,7 +507,7 @@ static int dec_chunk_keys(int32_t batch, int32_t hkv, int32_t max_kv_len) {
 
 struct DecodeLayout {
     int chunk, max_chunks, grp_chunks;
-    size_t part_o_bytes, part_lse_bytes, group_of_bytes, group_src_bytes, total;
+    size_t part_o_bytes, part_lse_bytes, shared_of_bytes, group_src_bytes, total;
 };
 
 static DecodeLayout dec_layout(const rx_attn_desc* d, int32_t batch, int32_t max_kv_len, const rx_shared_groups* grp) {
@@ -518,10 +518,10 @@ static DecodeLayout dec_layout(const rx_attn_desc* d, int32_t batch, int32_t max
     const size_t per = (size_t)(L.max_chunks + L.grp_chunks);
     L.part_o_bytes = (size_t)batch * d->hq * per * d->head_dim * sizeof(float);
     L.part_lse_bytes = (size_t)batch * d->hq * per * sizeof(float);
-    L.group_of_bytes = (grp && grp->num_groups > 0) ? (size_t)batch * sizeof(int32_t) : 0;
+    L.shared_of_bytes = (grp && grp->num_groups > 0) ? (size_t)batch * sizeof(int32_t) : 0;
     L.group_src_bytes = (grp && grp->num_groups > 0) ? (size_t)grp->num_groups * sizeof(int32_t) : 0;
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    L.total = up(L.part_o_bytes) + up(L.part_lse_bytes) + up(L.group_of_bytes) + up(L.group_src_bytes);
+    L.total = up(L.part_o_bytes) + up(L.part_lse_bytes) + up(L.shared_of_bytes) + up(L.group_src_bytes);
     return L;
 }
 
@@ -603,16 +603,16 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
     p.part_lse = (float*)(ws + up(lay.part_o_bytes));
     p.status = d_status;
     p.grp_chunks = lay.grp_chunks;
-    int32_t* group_of = nullptr;
+    int32_t* shared_of = nullptr;
     if (use_groups) {
-        group_of = (int32_t*)(ws + up(lay.part_o_bytes) + up(lay.part_lse_bytes));
-        p.group_src = (int32_t*)(ws + up(lay.part_o_bytes) + up(lay.part_lse_bytes) + up(lay.group_of_bytes));
+        shared_of = (int32_t*)(ws + up(lay.part_o_bytes) + up(lay.part_lse_bytes));
+        p.group_src = (int32_t*)(ws + up(lay.part_o_bytes) + up(lay.part_lse_bytes) + up(lay.shared_of_bytes));
         p.num_groups = groups->num_groups;
         p.grp_indptr = groups->d_group_indptr;
         p.grp_members = groups->d_group_members;
         p.grp_len = groups->d_group_len;
         p.grp_rows_max = groups->max_group_size * group;
-        p.group_of = group_of;
+        p.shared_of = shared_of;
     }
     const int D = desc->head_dim;
     const size_t smem = dec_smem_bytes(D);
@@ -634,7 +634,7 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
     DecodeFork* fork = nullptr;
     std::unique_lock<std::mutex> fork_lock;
     if (use_groups) {
-        decode_group_map_kernel<<<1, 512, 0, stream>>>(p, group_of);
+        decode_group_map_kernel<<<1, 512, 0, stream>>>(p, shared_of);
         // The shared runs go through the tcgen05 kernel: a group's stacked query rows read
         // each shared K/V row once per 256 rows.  On the side stream, concurrently with the
         // private part (both need only the group map); the merge waits for both.

@@ -452,6 +452,13 @@ const char* rx_last_error(void);
 /* Library version string. */
 const char* rx_version(void);
 
+/* Self-test of the bounded waits inside the kernels: one CTA waits on an mbarrier that no
+ * thread arrives at; after limit_ns (clamped to [1 us, 100 ms]) the wait gives up and sets
+ * *d_status (device int32, caller-owned) to RX_DEV_TIMEOUT unless it already holds a code, and
+ * the kernel ends.  The device stays usable.  Asynchronous on `stream`; RX_ECUDA if the launch
+ * fails. */
+int rx_wait_selftest(int32_t* d_status, uint64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,7 @@ EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "match_prefix_len", 
            "kv_pool_write", "prefix_extend_attention", "extend_workspace_bytes", "decode_workspace_bytes",
            "decode_attention",
            "decode_attention_noalloc",
-           "rx_last_error", "rx_version")
+           "rx_last_error", "rx_version", "rx_wait_selftest")
 
 
 class RxError(RuntimeError):
@@ -131,6 +131,7 @@ def load(path: str = LIB_PATH):
         "decode_attention_noalloc": (ctypes.c_int, [P, I32, P, P, I64, P, P, P, P, P, P, I32, P, P]),
         "rx_last_error": (ctypes.c_char_p, []),
         "rx_version": (ctypes.c_char_p, []),
+        "rx_wait_selftest": (ctypes.c_int, [P, U64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -400,6 +401,12 @@ def rx_step_launch(tree, desc, tokens: np.ndarray, tok_indptr: np.ndarray, last_
         _addr(last_nodes) if layout.batch else None, stage_addr, ctypes.byref(layout), ctypes.byref(io),
         evict_tokens, ctypes.byref(n), _stream(stream)))
     return n.value
+
+
+def rx_wait_selftest(status, limit_ns: int, stream=None) -> None:
+    """The kernels' bounded wait run out on purpose (a barrier nobody arrives at): *status
+    becomes RX_DEV_TIMEOUT once the stream reaches it (see include/radix_attn.h)."""
+    _check("rx_wait_selftest", load().rx_wait_selftest(_ptr(status), int(limit_ns), _stream(stream)))
 
 
 def rx_stage_wait(stage_addr: int) -> None:

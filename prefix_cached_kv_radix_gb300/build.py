@@ -22,7 +22,8 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libradixattn.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
-CU_SOURCES = ["kv_pool_write.cu", "attention_simt.cu", "extend_attention.cu", "decode_attention.cu", "step_runtime.cu"]
+CU_SOURCES = ["kv_pool_write.cu", "attention_simt.cu", "extend_attention.cu", "decode_attention.cu", "step_runtime.cu",
+              "wait_selftest.cu"]
 CPP_SOURCES = ["radix_tree.cpp"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 

@@ -4,6 +4,8 @@ Small and medium cases that span several tiles and ragged tails, plus edge cases
 Slot tables are bit-exact; attention is within max-abs 2e-2, mean-abs 2e-3, relative
 Frobenius 1e-2 per head, and log-sum-exp within 1e-3.
 """
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -257,6 +259,24 @@ def test_bad_slot_sets_status_decode():
     api.decode_attention(eng.desc, 1, qd, r2t, lens, eng.k_pool, eng.v_pool, od, None, 40, ws, eng.status)
     torch.cuda.synchronize()
     assert eng.device_status() == api.RX_DEV_BAD_SLOT
+
+
+def test_bounded_wait_times_out_and_device_stays_usable():
+    """A kernel's bounded wait on a barrier that nothing arrives at gives up after its limit,
+    records RX_DEV_TIMEOUT in the status word and ends; the device then runs a normal step."""
+    from prefix_cached_kv_radix_gb300 import api
+    api.load()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    api.rx_wait_selftest(status, 5_000_000)          # 5 ms
+    torch.cuda.synchronize()
+    assert int(status.item()) == api.RX_DEV_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    # a second call leaves a recorded code in place
+    api.rx_wait_selftest(status, 1_000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == api.RX_DEV_TIMEOUT
+    run_and_check(W.config("c1"))
 
 
 def test_workspace_too_small_is_rejected_on_host():

@@ -35,3 +35,17 @@ def test_host_calls_need_no_gpu():
     assert api.version().startswith("radixattn")
     t = api.RadixTree(8, 1)
     assert t.stats()["free_slots"] == 8
+
+
+def test_array_addresses_for_the_binding():
+    """The binding's array address helper: the buffer address for writable arrays, the
+    array's own for read-only and empty ones (all handed to the library as plain pointers)."""
+    import numpy as np
+    a = np.arange(10, dtype=np.int32)
+    assert api._addr(a) == a.ctypes.data
+    ro = np.frombuffer(np.arange(4, dtype=np.int64).tobytes(), np.int64)
+    assert not ro.flags.writeable and api._addr(ro) == ro.ctypes.data
+    e = np.zeros(0, np.int64)
+    assert api._addr(e) == e.ctypes.data
+    v = a[2:]                                  # a contiguous view starts where it says
+    assert api._addr(v) == a.ctypes.data + 8

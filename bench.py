@@ -259,12 +259,12 @@ def run_ours(args, rank, world, local_rank):
     n_new = np.asarray(s.req_new, np.int64)
     group_mode = True if s.decode else "auto"
 
-    def n_launch(grouped: bool, e2e: bool) -> int:
-        # kv_pool_write (plus, through host buffers, the index-array copy kernel; device-resident
-        # steps copy the index arrays with the copy engine), then for decode: (group map, shared
-        # chunks) + private chunks + merge; for extend: extend, or (prep, shared tcgen05,
-        # private + merge) with groups
-        base = 2 if e2e else 1
+    def n_launch(grouped: bool, e2e: bool, stage_bytes: int) -> int:
+        # kv_pool_write (plus the index-array copy kernel for host-buffer steps and for index
+        # arrays of at most 1 MiB; larger ones of device-row steps go by the copy engine), then
+        # for decode: (group map, shared chunks) + private chunks + merge; for extend: extend,
+        # or (prep, shared tcgen05, private + merge) with groups
+        base = 2 if (e2e or stage_bytes <= (1 << 20)) else 1
         if s.decode:
             return base + (2 if grouped else 0) + 2
         return base + (1 if not grouped else 3)
@@ -277,7 +277,7 @@ def run_ours(args, rank, world, local_rank):
         q_, k_, v_ = rows_e2e[i % 2] if e2e else (qd, kd, vd)
         plan = eng.step(toks, ind, n_new, q_, k_, v_, out, lse, decode=s.decode, groups=group_mode, evict_tokens=T,
                         host=(qh, kh, vh, out_h) if e2e else None, chunks=args.chunks, overlap=True)
-        launches[0] += n_launch(plan.layout.num_groups > 0, e2e)
+        launches[0] += n_launch(plan.layout.num_groups > 0, e2e, int(plan.layout.bytes))
         return plan
 
     def step_att(i):

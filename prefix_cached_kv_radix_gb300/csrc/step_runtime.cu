@@ -281,12 +281,14 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
             RX_REQUIRE(io->h_k_new && io->h_v_new && io->h_out, "rx_step_launch: host-buffer mode needs h_k_new, h_v_new, h_out");
         const RowBytes rb = row_bytes(desc);
         const int64_t* h_qo = (const int64_t*)((const unsigned char*)h_stage + L->off_qo_indptr);
-        // the index arrays, on the compute stream: in host-buffer mode read by a kernel through
-        // the mapping of the pinned staging buffer when it has one (never behind the rows'
-        // copies); otherwise one copy-engine transfer (about twice the kernel's rate over the
-        // host link)
+        // the index arrays: read by a kernel through the mapping of the pinned staging buffer
+        // when it has one -- in host-buffer mode (never behind the rows' copies) and for small
+        // arrays (a copy-engine transfer costs more in fixed latency there) -- otherwise one
+        // copy-engine transfer (about twice the kernel's rate over the host link)
+        constexpr int64_t kSmallStage = 1 << 20;
+        const bool by_kernel = host || L->bytes <= kSmallStage;
         void* h_dev = nullptr;
-        if (host && cudaHostGetDevicePointer(&h_dev, h_stage, 0) != cudaSuccess) {
+        if (by_kernel && cudaHostGetDevicePointer(&h_dev, h_stage, 0) != cudaSuccess) {
             cudaGetLastError();   // not mapped (pageable): clear the error, copy instead
             h_dev = nullptr;
         }
@@ -296,7 +298,7 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
         // waits for it -- under the previous step's kernels when the caller alternates d_stage
         Pipe* sp = nullptr;
         std::unique_lock<std::mutex> stage_lock;
-        if (!host && io->overlap) {
+        if (!by_kernel && io->overlap) {
             int rc = pipe_for(2, &sp);
             if (rc != RX_OK) return rc;
             stage_lock = std::unique_lock<std::mutex>(sp->use);

@@ -5,7 +5,7 @@ import workloads as W
 
 
 def test_take_requests_keeps_shapes_and_paths():
-    for name in ("c2", "c3", "c5"):
+    for name in ("c2", "c3", "c4", "c5"):
         full = W.config(name)
         sub = W.take_requests(full, 3)
         assert sub.req_cached == full.req_cached[:3] and sub.req_new == full.req_new[:3]

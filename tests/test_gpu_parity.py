@@ -99,6 +99,16 @@ def test_extend_group_sizes(hq, hkv):
     run_and_check(spec)
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4)])
+def test_extend_d64_tensor_core_tiles(hq, hkv):
+    # head dim 64 on the tcgen05 kernel (more than 8 rows per request and kv head): one TMA box
+    # per tile row (64 columns), 1 or 2 query heads per kv head; full tiles beside ragged ones
+    spec = W.Spec(f"d64-g{hq // hkv}", "bf16", hq, hkv, 64, 1 << 13, W.QWEN_VOCAB, 21,
+                  seg_parent=[-1, 0], seg_len=[200, 90], histories=[1],
+                  req_seg=[1, 0, 1], req_cached=[290, 57, 0], req_new=[256, 130, 41])
+    run_and_check(spec)
+
+
 def test_extend_gqa8_d128_many_tiles():
     spec = W.spec_multiturn("gqa8", "bf16", 64, 8, 128, 1 << 14, W.QWEN_VOCAB, 12, branches=2, branch_len=1200,
                             hit_len=1000, n_new=100)

@@ -180,6 +180,51 @@ struct rx_radix {
     // allocates nothing.  At most kSpareNodes are kept.
     static constexpr size_t kSpareNodes = 4096;
     std::vector<rx::Node*> spare;
+    // evict's scratch (the walk's stack and the heap of evictable leaves), kept between calls
+    using EvictItem = std::tuple<uint64_t, int64_t, rx::Node*>;
+    std::vector<rx::Node*> ev_stack;
+    std::vector<EvictItem> ev_heap;
+    // Hash-map nodes of evicted entries (child links and handles), reused through node handles
+    // for the entries of later nodes, so that inserting and evicting leaves allocates nothing.
+    using ChildMap = decltype(rx::Node::children);
+    using IdMap = std::unordered_map<int64_t, rx::Node*>;
+    std::vector<ChildMap::node_type> spare_child;
+    std::vector<IdMap::node_type> spare_id;
+
+    void add_child(rx::Node* parent, int32_t tok, rx::Node* c) {
+        if (spare_child.empty()) {
+            parent->children[tok] = c;
+            return;
+        }
+        ChildMap::node_type nh = std::move(spare_child.back());
+        spare_child.pop_back();
+        nh.key() = tok;
+        nh.mapped() = c;
+        auto r = parent->children.insert(std::move(nh));
+        if (!r.inserted) {          // the token already had a child: replace it, keep the handle
+            r.position->second = c;
+            spare_child.push_back(std::move(r.node));
+        }
+    }
+    void drop_child(rx::Node* parent, int32_t tok) {
+        ChildMap::node_type nh = parent->children.extract(tok);
+        if (nh && spare_child.size() < kSpareNodes) spare_child.push_back(std::move(nh));
+    }
+    void add_id(int64_t id, rx::Node* n) {
+        if (spare_id.empty()) {
+            by_id[id] = n;
+            return;
+        }
+        IdMap::node_type nh = std::move(spare_id.back());
+        spare_id.pop_back();
+        nh.key() = id;
+        nh.mapped() = n;
+        by_id.insert(std::move(nh));    // ids are never reused: always a new key
+    }
+    void drop_id(int64_t id) {
+        IdMap::node_type nh = by_id.extract(id);
+        if (nh && spare_id.size() < kSpareNodes) spare_id.push_back(std::move(nh));
+    }
 
     ~rx_radix() {
         destroy_children(&root);
@@ -220,7 +265,7 @@ struct rx_radix {
             n = new rx::Node();
         }
         n->id = next_id++;
-        by_id[n->id] = n;
+        add_id(n->id, n);
         ++st.node_count;
         return n;
     }
@@ -238,7 +283,7 @@ struct rx_radix {
         c->key.erase(c->key.begin(), c->key.begin() + k);
         c->slots.erase(c->slots.begin(), c->slots.begin() + k);
         c->parent->children[top->key[0]] = top;
-        top->children[c->key[0]] = c;
+        add_child(top, c->key[0], c);
         c->parent = top;
         return top;
     }
@@ -521,7 +566,7 @@ int insert(rx_radix* t, const int32_t* tokens, const int32_t* slots, int64_t n, 
         leaf->slots.assign(slots + dup, slots + n);
         leaf->stamp = t->clock;
         leaf->depth = x->depth + (n - dup);
-        x->children[tokens[dup]] = leaf;
+        t->add_child(x, tokens[dup], leaf);
         x = leaf;
         t->st.cached_tokens += n - dup;
         t->st.inserted_tokens += n - dup;
@@ -534,33 +579,45 @@ int insert(rx_radix* t, const int32_t* tokens, const int32_t* slots, int64_t n, 
 
 int evict(rx_radix* t, int64_t num_tokens, int32_t* out_freed, int64_t cap, int64_t* out_n) {
     RX_REQUIRE(t && out_n && num_tokens >= 0 && cap >= 0, "evict: bad arguments");
-    using Item = std::tuple<uint64_t, int64_t, rx::Node*>;
-    std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
-    // Collect the evictable leaves.
-    std::vector<rx::Node*> stack{&t->root};
+    if (num_tokens == 0) {
+        *out_n = 0;
+        return RX_OK;
+    }
+    // Collect the evictable leaves into a min-heap on (stamp, id).
+    auto& heap = t->ev_heap;
+    auto& stack = t->ev_stack;
+    const std::greater<rx_radix::EvictItem> later;
+    heap.clear();
+    stack.clear();
+    stack.push_back(&t->root);
     while (!stack.empty()) {
         rx::Node* x = stack.back();
         stack.pop_back();
-        if (x != &t->root && x->children.empty() && x->ref == 0) heap.emplace(x->stamp, x->id, x);
+        if (x != &t->root && x->children.empty() && x->ref == 0) heap.emplace_back(x->stamp, x->id, x);
         for (auto& kv : x->children) stack.push_back(kv.second);
     }
+    std::make_heap(heap.begin(), heap.end(), later);
     int64_t freed = 0;
     while (freed < num_tokens && !heap.empty()) {
-        rx::Node* x = std::get<2>(heap.top());
-        heap.pop();
+        std::pop_heap(heap.begin(), heap.end(), later);
+        rx::Node* x = std::get<2>(heap.back());
+        heap.pop_back();
         for (int32_t s : x->slots) {
             if (out_freed && freed < cap) out_freed[freed] = s;
             t->push_free(s);
             ++freed;
         }
         rx::Node* p = x->parent;
-        p->children.erase(x->key[0]);
+        t->drop_child(p, x->key[0]);
         t->st.cached_tokens -= (int64_t)x->key.size();
-        t->by_id.erase(x->id);
+        t->drop_id(x->id);
         --t->st.node_count;
         if (t->spare.size() < rx_radix::kSpareNodes) t->spare.push_back(x);
         else delete x;
-        if (p != &t->root && p->children.empty() && p->ref == 0) heap.emplace(p->stamp, p->id, p);
+        if (p != &t->root && p->children.empty() && p->ref == 0) {
+            heap.emplace_back(p->stamp, p->id, p);
+            std::push_heap(heap.begin(), heap.end(), later);
+        }
     }
     t->st.evicted_tokens += freed;
     *out_n = freed;
@@ -626,7 +683,7 @@ int insert_batch_at(rx_radix* t, int32_t batch, const rx_node* nodes, const int3
             leaf->slots.assign(sl + (dup - d), sl + m);
             leaf->stamp = t->clock;
             leaf->depth = end->depth + (n - dup);
-            end->children[tok[dup]] = leaf;
+            t->add_child(end, tok[dup], leaf);
             end = leaf;
             t->st.cached_tokens += n - dup;
             t->st.inserted_tokens += n - dup;

@@ -246,8 +246,15 @@ struct rx_radix {
         }
     }
 
+    // The free list is a ring of num_slots entries from `head`; positions wrap without a
+    // division per slot.
+    int64_t ring_pos(int64_t i) const {
+        const int64_t p = head + i;
+        return p < num_slots ? p : p - num_slots;
+    }
+
     void push_free(int32_t s) {
-        ring[(head + count) % num_slots] = s;
+        ring[(size_t)ring_pos(count)] = s;
         ++count;
         is_free[s] = 1;
     }
@@ -505,12 +512,13 @@ int alloc_slots(rx_radix* t, int64_t n, int32_t* out_slots) {
         set_error("alloc_slots: %lld slots requested, %lld free", (long long)n, (long long)t->count);
         return RX_ENOMEM;
     }
-    for (int64_t i = 0; i < n; ++i) {
-        const int32_t s = t->ring[(size_t)((t->head + i) % t->num_slots)];
-        out_slots[i] = s;
-        t->is_free[(size_t)s] = 0;
-    }
-    t->head = (t->head + n) % t->num_slots;
+    // at most two contiguous runs of the ring: from head to its end, then from its start
+    if (n == 0) return RX_OK;
+    const int64_t first = std::min<int64_t>(n, t->num_slots - t->head);
+    std::memcpy(out_slots, t->ring.data() + t->head, sizeof(int32_t) * (size_t)first);
+    if (n > first) std::memcpy(out_slots + first, t->ring.data(), sizeof(int32_t) * (size_t)(n - first));
+    for (int64_t i = 0; i < n; ++i) t->is_free[(size_t)out_slots[i]] = 0;
+    t->head = t->ring_pos(n);
     t->count -= n;
     return RX_OK;
 }
@@ -530,7 +538,7 @@ int free_slots(rx_radix* t, const int32_t* slots, int64_t n) {
         return RX_EINVAL;
     }
     for (i = 0; i < n; ++i) {
-        t->ring[(size_t)((t->head + t->count) % t->num_slots)] = slots[i];
+        t->ring[(size_t)t->ring_pos(t->count)] = slots[i];
         t->count += 1;
     }
     return RX_OK;

@@ -66,6 +66,23 @@ def test_lock_semantics():
     t.check()
 
 
+def test_long_edge_matches_up_to_every_divergence_point():
+    """Reading a prompt along a long cached edge (compared in blocks of 64 and 16 tokens, then
+    token by token) stops exactly at the first differing token, wherever it falls relative to
+    the blocks; the read-only and the splitting match agree."""
+    edge = np.arange(1, 1001, dtype=np.int32)
+    for cut in [0, 1, 2, 15, 16, 17, 63, 64, 65, 79, 80, 127, 128, 129, 500, 998, 999, 1000]:
+        t = api.RadixTree(4096, 5)
+        sl = t.alloc_slots(len(edge))
+        t.insert(edge, sl)
+        prompt = np.concatenate([edge[:cut], [-7], edge[cut + 1:]]).astype(np.int32) if cut < 1000 \
+            else np.concatenate([edge, [5, 6, 7]]).astype(np.int32)
+        assert t.match_prefix_len(prompt) == cut
+        got, n, _ = t.match_prefix(prompt)
+        assert n == cut and got.tolist() == sl[:cut].tolist()
+        t.check()
+
+
 def test_recycled_nodes_get_new_handles():
     """Evicted nodes are recycled for later inserts (their storage, not their handles): the
     handle of an evicted node stays unknown after its memory holds a new node, new handles

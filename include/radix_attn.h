@@ -368,8 +368,9 @@ int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
 
 /* ------------------------------------------------------------------ one-call step launch
  * Everything of a planned step that follows rx_step_plan, in one call: the staging buffer
- * (h_stage) to its device copy (io->d_stage) -- a copy-engine transfer, or in host-buffer
- * mode a kernel reading the device mapping of the pinned buffer --, kv_pool_write (a3), the
+ * (h_stage) to its device copy (io->d_stage) -- a kernel reading the device mapping of the
+ * pinned buffer in host-buffer mode and for at most 1 MiB, else a copy-engine transfer --,
+ * kv_pool_write (a3), the
  * attention -- prefix_extend_attention (a4), or decode_attention (a5/a6) when io->decode --
  * with the plan's shared-prefix groups, and rx_step_finish (a7/a8: insert, free duplicates,
  * evict evict_tokens, unpin; host only, it does not wait for the GPU).  All device work is

@@ -10,12 +10,14 @@ pool of bounded size: each step takes a batch of waiting requests (in arrival or
 cache-aware: longest cached prefix first within a window of waiting requests), evicts LRU leaves
 when the batch's new tokens do not fit, plans the step (match, allocate, pin) and finishes it
 (insert the request and its reply, unpin), exactly as a serving step does, but allocates slots
-only: no K/V is computed.  The optimal hit rate is that of an unbounded cache: every distinct
-prefix token computed once, whatever the order.
+only: no K/V is computed.  Two references: the hit rate of an unbounded cache (every distinct
+prefix token computed once, whatever the order: no policy reaches it under a bounded pool), and
+an offline replay of the arrival order at the same pool size that evicts by furthest next use
+(Belady's rule, knowing the future requests: `offline_optimal`).
 
     python -m prefix_cached_kv_radix_gb300.schedule [--seed 1] [--batch 8] [--chats 400] [--questions 800]
 
-prints the hit rates of both orders at several pool sizes against the optimal one.
+prints the hit rates of both orders at several pool sizes against both references.
 """
 from __future__ import annotations
 
@@ -120,6 +122,139 @@ def simulate(trace, pool_slots: int, batch: int = 8, policy: str = "fifo", windo
     return res
 
 
+def fifo_batches(trace, batch: int) -> list:
+    """The batches of (session, turn) that simulate(policy="fifo") runs when no batch has to
+    shrink for lack of room (the arrival order does not depend on the cache's contents)."""
+    S = len(trace.sessions)
+    nxt = [0] * S
+    ready_at = [s.start for s in trace.sessions]
+    total = sum(len(s.turns) for s in trace.sessions)
+    out, done, step = [], 0, 0
+    while done < total:
+        ready = sorted((ready_at[s], s) for s in range(S) if nxt[s] < len(trace.sessions[s].turns)
+                       and ready_at[s] <= step)
+        if not ready:
+            step = min(ready_at[s] for s in range(S) if nxt[s] < len(trace.sessions[s].turns))
+            continue
+        chosen = [s for _, s in ready][:batch]
+        out.append([(s, nxt[s]) for s in chosen])
+        for s in chosen:
+            nxt[s] += 1
+            ready_at[s] = step + 1
+            done += 1
+        step += 1
+    return out
+
+
+def furthest_next_use_replay(steps, pool_slots: int) -> TraceResult:
+    """Offline replay of a fixed sequence of steps under a pool of `pool_slots` token slots,
+    evicting by furthest next use (Belady's rule for paging, applied to cached tokens).
+
+    steps: list of steps, each a list of (request_tokens, sequence_tokens) where the sequence is
+    the request followed by its reply (what the cache holds after the step).  Each cached token
+    is one prefix (a node of the trie of all sequences).  Per step, as in `simulate`: every
+    sequence's cached prefix is looked up before the step, hits = cached tokens of the request
+    part, the uncached tokens are computed; when they do not fit in the free slots, cached
+    tokens are evicted one at a time from the ends of cached paths (a token with no cached
+    extension), the one whose next use (the first step at or after this one whose sequence
+    contains it) is furthest first -- never used again counts as infinitely far; ties go to the
+    deeper token, then to the later-created one.  Then every sequence is inserted (tokens two
+    sequences of a step share are computed by both and stored once)."""
+    import bisect
+    import heapq
+    ids_of = []               # per step, per sequence: the prefix ids of its tokens
+    node = {}                 # (parent id, token) -> prefix id
+    parent, depth = [], []
+    uses = []                 # prefix id -> steps whose sequences contain it (ascending)
+    for t, st in enumerate(steps):
+        per = []
+        for _, seq in st:
+            ids = np.empty(len(seq), np.int64)
+            p = -1
+            for i, tok in enumerate(seq.tolist() if hasattr(seq, "tolist") else seq):
+                key = (p, tok)
+                q = node.get(key)
+                if q is None:
+                    q = node[key] = len(parent)
+                    parent.append(p)
+                    depth.append(i + 1)
+                    uses.append([])
+                if not uses[q] or uses[q][-1] != t:
+                    uses[q].append(t)
+                ids[i] = q
+                p = q
+            per.append(ids)
+        ids_of.append(per)
+    n = len(parent)
+    cached = np.zeros(n, bool)
+    nchild = np.zeros(n, np.int64)
+    leaves = set()
+    free = pool_slots
+    res = TraceResult()
+    INF = len(steps) + 1
+
+    def cached_len(ids):
+        k = 0
+        while k < len(ids) and cached[ids[k]]:
+            k += 1
+        return k
+
+    def key(q, t):
+        u = uses[q]
+        i = bisect.bisect_left(u, t)
+        nu = u[i] if i < len(u) else INF
+        return (-nu, -depth[q], -q, q)
+
+    for t, st in enumerate(steps):
+        m = [cached_len(ids) for ids in ids_of[t]]
+        need = sum(len(ids) - k for ids, k in zip(ids_of[t], m))
+        if free < need:
+            heap = [key(q, t) for q in leaves]
+            heapq.heapify(heap)
+            while free < need and heap:
+                q = heapq.heappop(heap)[3]
+                cached[q] = False
+                leaves.discard(q)
+                free += 1
+                res.evicted_tokens += 1
+                p = parent[q]
+                if p >= 0:
+                    nchild[p] -= 1
+                    if nchild[p] == 0:
+                        leaves.add(p)
+                        heapq.heappush(heap, key(p, t))
+            m = [cached_len(ids) for ids in ids_of[t]]
+            need = sum(len(ids) - k for ids, k in zip(ids_of[t], m))
+        newly = 0
+        for ids, k in zip(ids_of[t], m):
+            for q in ids[k:].tolist():
+                if not cached[q]:
+                    cached[q] = True
+                    newly += 1
+                    leaves.add(q)
+                    p = parent[q]
+                    if p >= 0:
+                        if nchild[p] == 0:
+                            leaves.discard(p)
+                        nchild[p] += 1
+        free -= newly
+        assert free >= 0, "pool smaller than one step's new tokens"
+        for (req, _), k in zip(st, m):
+            res.prompt_tokens += len(req)
+            res.hit_tokens += min(k, len(req))
+            res.requests += 1
+        res.computed_tokens += need
+        res.steps += 1
+    return res
+
+
+def offline_optimal(trace, pool_slots: int, batch: int = 8) -> TraceResult:
+    """The arrival-order schedule replayed offline at the same pool size with furthest-next-use
+    eviction: the reference that the LRU replays' hit rates are compared with at that size."""
+    steps = [[(trace.request(s, t), trace.sequence(s, t)) for s, t in b] for b in fifo_batches(trace, batch)]
+    return furthest_next_use_replay(steps, pool_slots)
+
+
 def optimal(trace) -> TraceResult:
     """Hit counts of an unbounded cache (one request at a time): the most any order can reuse."""
     tot = sum(len(trace.sequence(s, t)) for s in range(len(trace.sessions))
@@ -147,14 +282,19 @@ def main():
     print(f"trace: {len(tr.sessions)} sessions, {opt.requests} requests, {opt.prompt_tokens} prompt tokens, "
           f"{distinct} distinct tokens; optimal hit rate {opt.hit_rate:.4f}")
     print()
-    print("| pool (share of distinct tokens) | order | hit rate | % of optimal | evicted tokens |")
-    print("|---|---|---|---|---|")
+    print("| pool (share of distinct tokens) | order / eviction | hit rate | % of unbounded | "
+          "% of offline at this pool | evicted tokens |")
+    print("|---|---|---|---|---|---|")
     for frac in (0.05, 0.1, 0.25, 0.5, 1.0):
         pool = max(int(frac * distinct), a.batch * longest)
+        off = offline_optimal(tr, pool, batch=a.batch)
+        print(f"| {frac:.2f} ({pool} slots) | arrival / offline furthest next use | {off.hit_rate:.4f} | "
+              f"{100 * off.hit_rate / opt.hit_rate:.1f} % | 100 % | {off.evicted_tokens} |")
         for pol in ("fifo", "cache_aware"):
             r = simulate(tr, pool, batch=a.batch, policy=pol, window=a.window)
-            print(f"| {frac:.2f} ({pool} slots) | {pol} | {r.hit_rate:.4f} | {100 * r.hit_rate / opt.hit_rate:.1f} % | "
-                  f"{r.evicted_tokens} |")
+            print(f"| {frac:.2f} ({pool} slots) | {'arrival' if pol == 'fifo' else 'cache-aware'} / LRU | "
+                  f"{r.hit_rate:.4f} | {100 * r.hit_rate / opt.hit_rate:.1f} % | "
+                  f"{100 * r.hit_rate / off.hit_rate:.1f} % | {r.evicted_tokens} |")
     # reuse granularity: hits lost at page boundaries (cache-aware order)
     print()
     print("| page size | pool (share of distinct tokens) | hit rate | % of the token-granular optimum | computed tokens |")

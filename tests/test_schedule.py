@@ -143,3 +143,65 @@ def test_cache_aware_order_and_hit_bounds():
     t.insert([1, 2, 3, 4, 5, 6], sl)
     assert schedule.cache_aware_order(t, [np.array([9, 9]), np.array([1, 2, 7]), np.array([1, 2, 3, 4]),
                                           np.array([1, 5])]) == [2, 1, 3, 0]
+
+
+# ---------------------------------------------------------------- offline reference at the same pool
+def _steps(*seqs):
+    """One request per step, no reply: (request, sequence) pairs from token lists."""
+    return [[(np.array(q, np.int32), np.array(q, np.int32))] for q in seqs]
+
+
+def test_furthest_next_use_hand_worked():
+    # pool 4: s0 [1,2] and s1 [3,4] fill it; s2 [5,6] needs 2 slots.  LRU would evict [1,2]
+    # (least recent) and miss it at s3; furthest next use evicts 34 (never used again), then its
+    # parent 3 (a leaf now, never used again), and s3 [1,2] hits both tokens.
+    steps = _steps([1, 2], [3, 4], [5, 6], [1, 2])
+    r = schedule.furthest_next_use_replay(steps, 4)
+    assert (r.prompt_tokens, r.hit_tokens, r.computed_tokens, r.evicted_tokens) == (8, 2, 6, 2)
+    # the library's LRU tree on the same steps: s2 evicts [1,2], s3 misses
+    t = api.RadixTree(4, 0)
+    hits = 0
+    for ((q, _),) in steps:
+        slots, m, _ = t.match_prefix(q)
+        hits += m
+        free = t.stats()["free_slots"]
+        if free < len(q) - m:
+            t.evict_count(len(q) - m - free)
+            slots, m, _ = t.match_prefix(q)
+        t.insert(q, np.concatenate([slots[:m], t.alloc_slots(len(q) - m)]).astype(np.int32))
+    assert hits == 0
+
+
+def test_furthest_next_use_token_granular_hand_worked():
+    # pool 5.  s0 [1,2,3] computes 3; s1 [1,4] hits 1 (token 1), computes 1 -> cache {1,12,123,14}.
+    # s2 [7,8] needs 2, 1 free -> evict 1: the leaves are 123 (depth 3) and 14 (depth 2); the
+    # future is s3 [1,2,9] (uses 1 and 12 only), so both leaves are never used again and the
+    # deeper one goes: 123.  s3 [1,2,9] hits 2, needs 1, 0 free -> evict 1 among the leaves 14
+    # (never again), 78 (never again), 12 (now): equal next use for 14 and 78, equal depth, the
+    # later-created one (78) goes.  s4 [1,4] hits 2.
+    steps = _steps([1, 2, 3], [1, 4], [7, 8], [1, 2, 9], [1, 4])
+    r = schedule.furthest_next_use_replay(steps, 5)
+    assert r.prompt_tokens == 3 + 2 + 2 + 3 + 2
+    assert r.hit_tokens == 0 + 1 + 0 + 2 + 2
+    assert r.computed_tokens == 3 + 1 + 2 + 1 + 0
+    assert r.evicted_tokens == 2
+
+
+def test_offline_reference_bounds():
+    tr = W.chat_trace(1, n_chats=60, n_questions=120, horizon=8, scale=4)
+    opt = schedule.optimal(tr)
+    longest = max(len(tr.sequence(s, t)) for s in range(len(tr.sessions)) for t in range(len(tr.sessions[s].turns)))
+    # with room for everything: no eviction, and the same hits as the arrival-order replay in the
+    # library (the batches are the same, within-batch duplicates count alike)
+    big = opt.computed_tokens * 2
+    off = schedule.offline_optimal(tr, big, batch=8)
+    lru = schedule.simulate(tr, big, batch=8, policy="fifo")
+    assert off.evicted_tokens == 0 and lru.evicted_tokens == 0
+    assert (off.requests, off.prompt_tokens, off.hit_tokens, off.computed_tokens) == \
+        (lru.requests, lru.prompt_tokens, lru.hit_tokens, lru.computed_tokens)
+    # under pressure: never above the unbounded cache, and the batches are the arrival order's
+    pool = max(int(0.3 * opt.computed_tokens), 8 * longest)
+    off = schedule.offline_optimal(tr, pool, batch=8)
+    assert off.evicted_tokens > 0 and off.hit_tokens <= opt.hit_tokens
+    assert off.requests == opt.requests and off.prompt_tokens == opt.prompt_tokens
+    assert sum(len(b) for b in schedule.fifo_batches(tr, 8)) == opt.requests

@@ -1,6 +1,7 @@
 """Benchmark: prefix-cached attention steps on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload c2]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload c5] [--subs c3,c4,c2]
 
 One step is one pass of the whole hot path over one batch: host radix match and slot
 allocation, upload of the step's index arrays, kv_pool_write (slot table + K/V scatter),
@@ -12,6 +13,11 @@ region starts; the e2e figure repeats the step through the same public call with
 in pinned host memory: the library copies them in and the output back inside the timed
 region (a pipeline of request ranges whose copies run behind the kernels).
 
+The headline line is the long multi-turn chat workload (c5: 32 requests x 1024 new tokens over
+29,491 cached, GQA 64/8 x 128), the largest single-GPU one; the few-shot tree (c3), the batched
+decode (c4), the shared system prompt (c2) and the tiny fp32 case (c1) are measured in the same
+run and reported under "sub_results" with the same keys.
+
 Prints one JSON line.  With N > 1 (torchrun) every rank runs its own replica of the
 workload on its own GPU (the path shards over independent requests; no collective is
 needed), value = all ranks' tokens / max over ranks of the time.
@@ -19,6 +25,7 @@ needed), value = all ranks' tokens / max over ranks of the time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -38,6 +45,8 @@ METRIC = "prefix-cached attention tokens/s; % HBM (decode) / % bf16 TC peak (ext
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 129 << 20           # GB300 L2
+DEFAULT_WORKLOAD = "c5"
+DEFAULT_SUBS = {"c5": ("c3", "c4", "c2", "c1")}
 
 
 def load_peaks():
@@ -111,48 +120,131 @@ def algorithmic_work(w):
     qo_bytes = 2 * w.total_new() * s.hq * s.d * elt
     idx_bytes = 4 * tot_ctx
     return dict(flops=flops, pairs=pairs, kv_unique_bytes=uniq_tokens * row,
-                bytes=uniq_tokens * row + qo_bytes + idx_bytes, kv_naive_bytes=tot_ctx * row)
+                bytes=uniq_tokens * row + qo_bytes + idx_bytes, kv_naive_bytes=tot_ctx * row,
+                naive_bytes=tot_ctx * row + qo_bytes + idx_bytes)
+
+
+def pool_write_bytes(w, stride: int) -> int:
+    """kv_pool_write's algorithmic bytes: the new rows' K and V read and written once each, the
+    slot table written in full ([batch, stride] int32), the prefix and new slot lists read."""
+    s = w.spec
+    elt = 4 if s.dtype == "f32" else 2
+    T = w.total_new()
+    return 4 * T * s.hkv * s.d * elt + 4 * w.batch * stride + 4 * (int(sum(s.req_cached)) + T)
 
 
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    """SM clock and throttle reasons of this process's GPU, sampled through NVML (read only)
+    every few milliseconds from a background thread while a timed region runs, and on demand
+    with sample().  Falls back to `nvidia-smi -lms 200` when NVML cannot be loaded."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
-        self.t = None
+    def __init__(self, device_index: int, period_s: float = 0.001):
+        self.period = period_s
+        self.samples = []             # (sm_mhz, max_mhz, reasons bitmask)
+        self.lock = threading.Lock()
+        self.running = False
+        self.thread = None
+        self.nvml = None
+        self.handle = None
+        self.smi = None
+        self.smi_lines = []
+        self._open(device_index)
+
+    def _open(self, device_index):
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            got = False
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(device_index)
+                bus = f"{getattr(pr, 'pci_domain_id', 0):08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+                got = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                got = False
+            if not got:
+                n = ctypes.c_uint()
+                lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+                idx = 0 if n.value == 1 else device_index
+                got = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) == 0
+            if got:
+                self.nvml, self.handle = lib, h
+                self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                    getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except (OSError, AttributeError):
+            self.nvml = None
+
+    def sample(self):
+        if self.nvml is None:
+            return
+        sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if (self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(sm)) == 0 and
+                self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0):
+            self.reasons_fn(self.handle, ctypes.byref(rs))
+            with self.lock:
+                self.samples.append((sm.value, mx.value, rs.value))
+
+    def _loop(self):
+        while self.running:
+            self.sample()
+            time.sleep(self.period)
 
     def start(self):
+        """Sample in the background (NVML) until pause() or stop()."""
+        if self.nvml is not None:
+            if not self.running:
+                self.running = True
+                self.thread = threading.Thread(target=self._loop, daemon=True)
+                self.thread.start()
+            return
+        if self.smi is not None:
+            return
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            self.smi = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                         "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=lambda: self.smi_lines.extend(ln.strip() for ln in self.smi.stdout),
+                                           daemon=True)
+            self.thread.start()
+        except OSError:
+            self.smi = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def pause(self):
+        if self.nvml is not None and self.running:
+            self.running = False
+            self.thread.join(timeout=2)
 
     def stop(self):
-        if self.proc is None:
+        """Stop sampling; returns {sm_mhz (median), sm_max_mhz, reasons, samples, source} or None."""
+        if self.nvml is not None:
+            self.pause()
+            with self.lock:
+                smp = list(self.samples)
+            if not smp:
+                return None
+            reasons = sorted({name for _, _, r in smp for bit, name in self.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(x[0] for x in smp), "sm_max_mhz": max(x[1] for x in smp),
+                    "sm_min_mhz": min(x[0] for x in smp), "reasons": reasons, "samples": len(smp),
+                    "source": (f"NVML: every {self.period * 1e3:.0f} ms during back-to-back timed regions, "
+                               "before every step timed alone")}
+        if self.smi is None:
             return None
-        self.proc.terminate()
+        self.smi.terminate()
         try:
-            self.proc.wait(timeout=5)
+            self.smi.wait(timeout=5)
         except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.t.join(timeout=2)
+            self.smi.kill()
+        self.thread.join(timeout=2)
         sm, mx, reasons = [], 0.0, set()
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.smi_lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -161,12 +253,13 @@ class ClockSampler:
                 mx = max(mx, float(f[2]))
             except ValueError:
                 continue
-            for name, val in zip(names[1:], f[5:9]):
+            for name, val in zip(names, f[5:9]):
                 if val.lower() in ("active", "1", "yes"):
                     reasons.add(name)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvidia-smi every 200 ms"}
 
 
 # ---------------------------------------------------------------------------- replicas
@@ -216,13 +309,55 @@ def fresh_prompts(w, step, used):
     return prompts
 
 
-def run_ours(args, rank, world, local_rank):
+def link_rates(pairs, reps: int = 5):
+    """Attainable host-link rates on this machine: one large cudaMemcpyAsync per direction from/to
+    the same pinned buffers the e2e steps use (H2D alone, D2H alone, both at once on two
+    streams), timed with CUDA events; GB/s (1e9 B/s), best of `reps`."""
+    import torch
+    h2d_src, h2d_dst, d2h_src, d2h_dst = pairs
+    nb_in = h2d_src.numel() * h2d_src.element_size()
+    nb_out = d2h_src.numel() * d2h_src.element_size()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn, streams):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in streams]
+            for (a, _), st in zip(ev, streams):
+                a.record(st)
+            fn()
+            for (_, b), st in zip(ev, streams):
+                b.record(st)
+            torch.cuda.synchronize()
+            best = min(best, max(a.elapsed_time(b) for a, b in ev))
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s_in):
+            h2d_dst.copy_(h2d_src, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s_out):
+            d2h_dst.copy_(d2h_src, non_blocking=True)
+
+    t_in = timed(h2d, [s_in])
+    t_out = timed(d2h, [s_out])
+    t_both = timed(lambda: (h2d(), d2h()), [s_in, s_out])
+    return {"h2d_gbs": nb_in / (t_in * 1e-3) / 1e9, "d2h_gbs": nb_out / (t_out * 1e-3) / 1e9,
+            "both_gbs": (nb_in + nb_out) / (t_both * 1e-3) / 1e9, "h2d_bytes": nb_in, "d2h_bytes": nb_out,
+            "how": "one cudaMemcpyAsync per direction between the e2e steps' pinned host buffers and device "
+                   "rows, best of 5, CUDA events"}
+
+
+def measure(name, args, rank, world, local_rank, cpu: bool):
+    """Every figure of one workload: the step (value), the e2e step through host buffers, the
+    attention call and kv_pool_write alone (rooflines), clocks, host link, CPU baseline."""
     import torch
     from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine, _dev_from_host
 
-    torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    spec = W.config(args.workload)
+    spec = W.config(name)
     if args.requests:
         spec = W.take_requests(spec, args.requests)
     if args.pool_slots:
@@ -246,8 +381,9 @@ def run_ours(args, rank, world, local_rank):
     T = w.total_new()
     used = {}
     stream = torch.cuda.current_stream()
-    att_ev = []
+    att_ev, write_ev = [], []
     launches = [0]
+    strides = []
 
     # every step's prompts are prepared before timing (inputs resident when timing starts)
     n_total = 2 * args.warmup + 4 * args.steps     # warm-up (both paths), value, e2e, attention, isolated
@@ -281,24 +417,29 @@ def run_ours(args, rank, world, local_rank):
         return plan
 
     def step_att(i):
-        """The same step through the per-operation calls, with CUDA events around the attention
-        call alone (the roofline's kernel time)."""
+        """The same step through the per-operation calls, with CUDA events around kv_pool_write
+        alone and around the attention call alone (the rooflines' kernel times)."""
         toks, ind = step_inputs[i]
         plan = eng.plan_concat(toks, ind, n_new, groups=group_mode)
+        strides.append(plan.stride)
         d = eng.upload(plan)
         grp = eng.groups(plan, d)
-        eng.write(plan, d, kd, vd)
         if hasattr(torch.cuda, "_sleep"):
-            # keep the GPU busy while the host records the start event and issues the call, so
-            # that only the attention kernels fall between the events
-            torch.cuda._sleep(100_000)
+            # keep the GPU busy while the host records the start event and issues the calls, so
+            # that only the kernels fall between the events
+            torch.cuda._sleep(200_000)
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        eng.write(plan, d, kd, vd)
+        w1.record(stream)
         e0.record(stream)
         if s.decode:
             eng.decode(plan, d, qd, out, lse, groups=grp)
         else:
             eng.extend(plan, d, qd, out, lse)
         e1.record(stream)
+        write_ev.append((w0, w1))
         att_ev.append((e0, e1))
         eng.finish(plan, evict_tokens=T)
 
@@ -316,6 +457,7 @@ def run_ours(args, rank, world, local_rank):
     # do: double-buffered staging, host finish right after the launch).  A step that fits in
     # L2 is timed alone after an L2 flush and a synchronize.
     back_to_back = work["bytes"] >= 2 * L2_BYTES
+    clocks = ClockSampler(local_rank)
 
     def timed(e2e, isolated=not back_to_back, first=None):
         if world > 1:
@@ -325,20 +467,25 @@ def run_ours(args, rank, world, local_rank):
         first = args.warmup + (args.steps if e2e else 0) if first is None else first
         if not isolated:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            clocks.start()
             e0.record(stream)
             for i in range(args.steps):
                 step(first + i, e2e=e2e)
             e1.record(stream)
             torch.cuda.synchronize()
+            clocks.pause()
             if world > 1:
                 torch.distributed.barrier()
             return e0.elapsed_time(e1), launches[0]
         times = []
+        if clocks.nvml is None:
+            clocks.start()
         for i in range(args.steps):
             flush.zero_()                      # untimed: evict L2 between timed steps
             # the flush completes before the timed region opens, so the step's host work
             # (planning, launches, finish) cannot hide behind it: the region holds the whole step
             torch.cuda.synchronize()
+            clocks.sample()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             step(first + i, e2e=e2e)
@@ -350,24 +497,23 @@ def run_ours(args, rank, world, local_rank):
         ms = sum(a.elapsed_time(b) for a, b in times)
         return ms, launches[0]
 
-    clocks = ClockSampler(local_rank)
-    clocks.start()
     ms, n_launches = timed(False)
     ms_e2e, _ = timed(True)
     clk = clocks.stop()
     ms_iso = None
     if back_to_back:   # the same steps once more, each alone after a flush, for comparison
         ms_iso, _ = timed(False, isolated=True, first=args.warmup + 3 * args.steps + args.warmup)
-    for i in range(args.steps):                # attention-only timing for the roofline (untimed above)
-        flush.zero_()                          # no synchronize: the host prepares the call while the
+    for i in range(args.steps):                # kernel-only timing for the rooflines (untimed above)
+        flush.zero_()                          # no synchronize: the host prepares the calls while the
         step_att(args.warmup + 2 * args.steps + i)   # flush runs, so only the kernels fall between the events
     torch.cuda.synchronize()
     if eng.device_status() != 0:
         raise RuntimeError(f"device status {eng.device_status()} after timed steps")
+    link = link_rates((qh, rows_e2e[1][0], out, out_h))
     ms, ms_e2e = reduce_max([ms, ms_e2e], world, dev)
-    att_ms = [a.elapsed_time(b) for a, b in att_ev]
     hbm, bf16, bf16_s, src = load_peaks()
-    att = statistics.median(att_ms) if att_ms else float("nan")
+    att = statistics.median(a.elapsed_time(b) for a, b in att_ev)
+    wr = statistics.median(a.elapsed_time(b) for a, b in write_ev)
     # the bound follows the step's arithmetic intensity against the ridge of the two peaks
     intensity = work["flops"] / work["bytes"]
     ridge = bf16 * 1e12 / (hbm * 1e9)
@@ -379,29 +525,33 @@ def run_ours(args, rank, world, local_rank):
                 "kernel": "decode_attention (split-KV + merge)" if s.decode else "prefix_extend_attention",
                 "algorithmic": f"{work['bytes'] / 1e9:.4f} GB unique (KV {work['kv_unique_bytes'] / 1e9:.4f} GB + Q/O + indices) per launch",
                 "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
-                "launch_ms": att, "peak_source": f"{src} hbm_gbs"}
+                "launch_ms": att, "peak_source": f"{src} hbm_gbs (copy)"}
+        if s.decode:
+            naive = work["naive_bytes"] / (att * 1e-3) / 1e9
+            roof["naive"] = {"achieved": naive, "frac": naive / hbm,
+                             "algorithmic": f"{work['naive_bytes'] / 1e9:.4f} GB: every request's whole context "
+                                            "read as if nothing were shared (labelled, not the headline fraction)"}
     else:
+        # the attention call is timed alone (after an L2 flush, with nothing else running): the
+        # burst peak applies; the fraction of the sustained peak is given beside it
         achieved = work["flops"] / (att * 1e-3) / 1e12
-        # a kernel timed inside long steps runs under the power cap: the sustained peak applies
-        long_steps = ms / args.steps >= 5.0
-        peak = bf16_s if long_steps and bf16_s else bf16
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
                 "traffic": traffic, "kernel": "prefix_extend_attention (tcgen05)",
                 "algorithmic": f"{work['flops'] / 1e9:.3f} GFLOP per launch (4*D per causal pair per q head)",
                 "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
-                "launch_ms": att,
-                "peak_source": f"{src} " + ("bf16_tflops_sustained (steps of >= 5 ms)" if peak == bf16_s and long_steps
-                                            else "bf16_tflops (burst)")}
+                "launch_ms": att, "peak_source": f"{src} bf16_tflops (burst: the kernel is timed alone)",
+                "frac_of_sustained": achieved / bf16_s if bf16_s else None}
     roof["traffic_note"] = ("dram read+write bytes of the attention call's kernels for one step (ncu, "
                             "profiles/traffic.json)" if traffic is not None else
                             "null: no ncu capture recorded for these kernel sources")
-    tokens = T * args.steps * world
+    wbytes = pool_write_bytes(w, int(statistics.median(strides)))
+    wach = wbytes / (wr * 1e-3) / 1e9
+    pool_roof = {"bound": "hbm", "achieved": wach, "peak": hbm, "unit": "GB/s", "frac": wach / hbm, "launch_ms": wr,
+                 "algorithmic": f"{wbytes / 1e6:.2f} MB per launch (new K/V read + written, slot table, slot lists)"}
     value = replica_throughput(T, args.steps, world, ms)
     h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
     d2h = out_h.numel() * out_h.element_size()
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds)
+    e2e_copy = (h2d + d2h) / (ms_e2e / args.steps * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -414,68 +564,160 @@ def run_ours(args, rank, world, local_rank):
                           f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write), each step timed alone"),
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
-        "cpu_baseline": cpu,
+        "kv_pool_write_roofline": pool_roof,
+        "cpu_baseline": cpu_baseline(w, args.cpu_seconds) if (cpu and rank == 0) else None,
         "e2e": {"value": replica_throughput(T, args.steps, world, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "copy_gbs": e2e_copy,
+                "frac_of_link": e2e_copy / link["both_gbs"] if link["both_gbs"] else None},
+        "host_link": link,
         "gpu_launches": n_launches,   # library kernels in the timed region (value); the e2e region adds one per step
         "isolated_step_ms": ms_iso / args.steps if ms_iso is not None else None,
         "clocks": clk,
         "radix_stats": eng.tree.stats(),
     }
+    return line
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    import gc
+
+    def one(name):
+        r = measure(name, args, rank, world, local_rank, cpu=not args.no_cpu_baseline)
+        gc.collect()                   # the workload's pools and rows go before the next one's
+        torch.cuda.empty_cache()
+        return r
+
+    line = one(args.workload)
+    subs = {}
+    for name in args.subs:
+        if name != args.workload:
+            subs[name] = one(name)
+            for k in ("metric", "unit", "n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline",
+                      "data"):
+                subs[name].pop(k, None)
+    if subs:
+        line["sub_results"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------------------- oracle timing
-def oracle_step(w, rows_per_request=None):
+def _f32(a, dtype):
+    return W.bf16_bits_to_f32(a) if dtype == "bf16" else np.asarray(a, np.float32)
+
+
+def oracle_step(w, rows_of=None, threads: int = 0, full: bool = False):
     """The oracle's own version of one step: list matcher + slot allocator replay for the
-    table, fp64 attention for the output rows.  Returns (tokens computed, threads)."""
+    table, fp64 attention for the output rows.  rows_of(b) gives the row indices of request b
+    to compute (None: every new row); full=True computes every row of the whole prompt, as an
+    uncached recompute must.  Returns (new tokens output, threads, keys attended per head,
+    seconds in the matcher)."""
     import oracle
     s = w.spec
     lm = oracle.ListMatcher()
     for i in range(len(s.histories)):
         lm.add(w.history_tokens(i), np.zeros(len(w.history_tokens(i)), np.int32))
-    done = 0
+    done, keys, t_match = 0, 0, 0.0
     for b in range(w.batch):
+        t0 = time.perf_counter()
         lm.match(w.request_tokens(b))
-        n = s.req_new[b]
-        idx = np.arange(n) if rows_per_request is None else np.arange(min(n, rows_per_request))
-        if len(idx) == 0:
+        t_match += time.perf_counter() - t0
+        n, P = s.req_new[b], s.req_cached[b]
+        idx = np.arange(n) if rows_of is None else np.asarray(rows_of(b), np.int64)
+        if len(idx) == 0 and not full:
             continue
         k, v = w.request_kv(b)
-        k = W.bf16_bits_to_f32(k) if s.dtype == "bf16" else k
-        v = W.bf16_bits_to_f32(v) if s.dtype == "bf16" else v
-        q = W.bf16_bits_to_f32(w.req_q[b]) if s.dtype == "bf16" else w.req_q[b]
-        oracle.attention_rows(q[idx], s.req_cached[b] + idx, k, v, s.scale)
+        k, v = _f32(k, s.dtype), _f32(v, s.dtype)
+        q = _f32(w.req_q[b], s.dtype)
+        if full:
+            # no cache: every position of the prompt is computed (the prefix rows' queries are
+            # seeded draws of the same distribution; only the work matters here)
+            qp = np.random.default_rng([s.seed, 77, b]).standard_normal((P, s.hq, s.d), dtype=np.float32)
+            qa = np.concatenate([_f32(W.f32_to_bf16_bits(qp), "bf16") if s.dtype == "bf16" else qp, q])
+            pos = np.arange(P + n)
+            oracle.attention_rows(qa, pos, k, v, s.scale, threads)
+            keys += int((pos + 1).sum())
+        else:
+            oracle.attention_rows(q[idx], P + idx, k, v, s.scale, threads)
+            keys += int((P + idx + 1).sum())
         done += len(idx)
-    return done, oracle.max_threads()
+    return done, (threads or oracle.max_threads()), keys, t_match
 
 
-# Rows per request in one reference step (None = every new row): full steps where the oracle
-# finishes one in about a second or two, a bounded sample of each request's rows otherwise.
-REF_ROWS = {"c3": 8, "c5": 2}
+# Rows per request in one baseline step where a full step would take minutes: c5's 32
+# requests x 1024 rows over ~30 K keys (32 TFLOP) are sampled.  The reference arm, which runs
+# --steps oracle steps, also samples c3 (its full step takes tens of seconds on the host).
+def sample_rows(name, reference: bool = False):
+    if name.startswith("c5"):
+        return lambda b: np.array([0, 1023])
+    if reference and name.startswith("c3"):
+        return lambda b: np.arange(8)
+    return None
+
+
+def sample_note(name, reference: bool = False):
+    if name.startswith("c5"):
+        return "new rows {0, 1023} of every request"
+    if reference and name.startswith("c3"):
+        return "the first 8 new rows of every request"
+    return None
+
+
+def _timed_loop(fn, seconds, min_reps=1):
+    t0 = time.perf_counter()
+    reps, acc = 0, []
+    while True:
+        acc.append(fn())
+        reps += 1
+        if reps >= min_reps and time.perf_counter() - t0 > seconds:
+            break
+    return time.perf_counter() - t0, reps, acc
 
 
 def cpu_baseline(w, seconds):
-    """Time the oracle (as it stands) on the host cores on a bounded sample of the step."""
+    """Time the oracle (as it stands) on the host cores on a bounded sample of the step: the rows
+    mode on all cores (the headline baseline), plus for the small workloads a 1-core run and the
+    uncached full recompute, the list matcher alone, and for the sampled workload the full step
+    extrapolated from the sample (labelled as such)."""
     import oracle
     oracle.build()
-    t0 = time.perf_counter()
-    toks, reps = 0, 0
-    rows = None
     s = w.spec
-    if s.name in REF_ROWS:
-        rows = REF_ROWS[s.name]   # a few rows per request: full rows would take minutes to hours
-    while True:
-        n, thr = oracle_step(w, rows)
-        toks += n
-        reps += 1
-        if time.perf_counter() - t0 > seconds:
-            break
-    dt = time.perf_counter() - t0
+    rows_of = sample_rows(s.name)
+    dt, reps, acc = _timed_loop(lambda: oracle_step(w, rows_of), seconds)
+    toks = sum(a[0] for a in acc)
+    thr = acc[0][1]
     sample = (f"{reps} full oracle step(s) of {s.name} (list matcher + fp64 attention of every new row)"
-              if rows is None else f"{reps} oracle pass(es) of {s.name} with the first {rows} new rows per request")
-    return {"value": toks / dt, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample, "seconds": dt}
+              if rows_of is None else
+              f"{reps} oracle pass(es) of {s.name} with {sample_note(s.name)}")
+    res = {"value": toks / dt, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample, "seconds": dt,
+           "mode": "rows (the rows the method outputs, over logical-order K/V)"}
+    # the list matcher alone: one step's prompts against the cached sequences
+    t_match = sum(a[3] for a in acc) / reps
+    ptoks = sum(len(w.request_tokens(b)) for b in range(w.batch))
+    res["matcher"] = {"seconds_per_step": t_match, "prompt_tokens_per_s": ptoks / t_match if t_match else None,
+                      "what": "oracle list matcher (longest common prefix over the cached sequences), one step"}
+    if rows_of is not None:
+        keys_s = sum(a[2] for a in acc)
+        t_att = dt - t_match * reps
+        keys_full = sum(s.req_new[b] * (s.req_cached[b] + 1) + s.req_new[b] * (s.req_new[b] - 1) // 2
+                        for b in range(w.batch))
+        est = t_att / keys_s * keys_full + t_match
+        res["extrapolated_full_step"] = {
+            "label": "EXTRAPOLATION, not a measurement: the sampled rows' time per attended key scaled to every new "
+                     "row of the step, plus the matcher",
+            "seconds_per_step": est, "value": w.total_new() / est, "unit": UNIT}
+    if s.name in ("c1", "c2"):
+        d1, r1, a1 = _timed_loop(lambda: oracle_step(w, rows_of, threads=1), seconds / 2)
+        res["one_core"] = {"value": sum(a[0] for a in a1) / d1, "unit": UNIT, "cores": 1, "seconds": d1,
+                           "sample": f"{r1} full oracle step(s) on one thread"}
+        df, rf, af = _timed_loop(lambda: oracle_step(w, full=True), seconds / 2)
+        res["full_mode"] = {"value": sum(a[0] for a in af) / df, "unit": UNIT, "cores": thr, "seconds": df,
+                            "rows_per_step": int(sum(s.req_cached) + w.total_new()),
+                            "sample": f"{rf} uncached step(s): every row of every prompt recomputed; value counts "
+                                      "the new tokens delivered"}
+    return res
 
 
 def run_reference(args, rank, world):
@@ -486,25 +728,26 @@ def run_reference(args, rank, world):
     oracle.build()
     spec = W.config(args.workload)
     w = W.generate(spec)
-    rows = REF_ROWS.get(spec.name)
+    rows_of = sample_rows(spec.name, reference=True)
+    note = sample_note(spec.name, reference=True)
     for _ in range(args.warmup):
-        oracle_step(w, rows)
+        oracle_step(w, rows_of)
     t0 = time.perf_counter()
     toks = 0
     thr = 1
     for _ in range(args.steps):
-        n, thr = oracle_step(w, rows)
+        n, thr, _, _ = oracle_step(w, rows_of)
         toks += n
     dt = time.perf_counter() - t0
     v = toks / dt
     sample = (f"{args.steps} oracle steps of {spec.name} (list matcher + fp64 attention of every new row)"
-              if rows is None else
-              f"{args.steps} oracle steps of {spec.name}, each the first {rows} new rows of every request")
+              if rows_of is None else
+              f"{args.steps} oracle steps of {spec.name}, each {note}")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": f"{spec.name}: {spec.note}", "batch": w.batch,
-                       "sample": "full step" if rows is None else f"first {rows} new rows per request"},
+                       "sample": "full step" if rows_of is None else note},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -513,11 +756,14 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c2", choices=list(W.CONFIG_NAMES))
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.CONFIG_NAMES))
+    ap.add_argument("--subs", default=None,
+                    help="comma-separated workloads measured in the same run (default: c3,c4,c2,c1 with c5; "
+                         "none otherwise); 'none' for none")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunks", type=int, default=0,
                     help="request ranges of the e2e copy pipeline (0: chosen by the library)")
@@ -527,6 +773,17 @@ def main():
                     help="override the KV pool size (profiling captures keep the device footprint small)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.subs is None:
+        args.subs = list(DEFAULT_SUBS.get(args.workload, ()))
+    elif args.subs in ("", "none"):
+        args.subs = []
+    else:
+        args.subs = [x for x in args.subs.split(",") if x]
+        for x in args.subs:
+            if x not in W.CONFIG_NAMES:
+                ap.error(f"unknown workload {x}")
+    if args.requests or args.pool_slots:
+        args.subs = []                  # profiling captures: one workload
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

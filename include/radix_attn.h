@@ -352,9 +352,10 @@ int decode_attention(const rx_attn_desc* desc, int32_t batch,
  *    caller's buffers).
  *  - A batch whose decode_workspace_bytes(...) exceeds RX_DECODE_NOALLOC_SCRATCH_BYTES is
  *    rejected with RX_EINVAL and a message; split the batch or use decode_attention.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make that first call
- *    before any stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress, a host-side lookup), so the address stays right after a
+ *    cudaDeviceReset or on another device.  The first call on a device may load the
+ *    library's device code there; make that first call before any stream capture.
  *  - All calls share the one array (it keeps the last call's contents; every call writes
  *    the scratch before reading it): calls that overlap on the GPU -- on different streams,
  *    or from different host threads -- race and give wrong results.  Serialise them. */
@@ -452,6 +453,14 @@ const char* rx_last_error(void);
 
 /* Library version string. */
 const char* rx_version(void);
+
+/* Tracing (the pages have no counterpart; a profiling aid): on != 0 puts an NVTX range named
+ * after the entry point around every call that does work (the tree operations, the step
+ * runtime's plan/launch/finish/prefetch/stage wait, kv_pool_write and the attention calls), so
+ * that a profiler's timeline shows the library's host and GPU work per call.  Off by default;
+ * RX_NVTX=1 in the environment when the library is loaded turns it on from the start.  While
+ * off, a call pays one relaxed atomic load.  Process-wide; returns the previous setting. */
+int rx_set_tracing(int on);
 
 /* Self-test of the bounded waits inside the kernels: one CTA waits on an mbarrier that no
  * thread arrives at; after limit_ns (clamped to [1 us, 100 ms]) the wait gives up and sets

@@ -29,7 +29,7 @@ EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "match_prefix_len", 
            "kv_pool_write", "prefix_extend_attention", "extend_workspace_bytes", "decode_workspace_bytes",
            "decode_attention",
            "decode_attention_noalloc",
-           "rx_last_error", "rx_version", "rx_wait_selftest")
+           "rx_last_error", "rx_version", "rx_wait_selftest", "rx_set_tracing")
 
 
 class RxError(RuntimeError):
@@ -132,6 +132,7 @@ def load(path: str = LIB_PATH):
         "rx_last_error": (ctypes.c_char_p, []),
         "rx_version": (ctypes.c_char_p, []),
         "rx_wait_selftest": (ctypes.c_int, [P, U64, P]),
+        "rx_set_tracing": (ctypes.c_int, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -181,6 +182,11 @@ def _stream(stream):
 
 def version() -> str:
     return load().rx_version().decode()
+
+
+def set_tracing(on: bool) -> bool:
+    """NVTX ranges around the library's calls (off by default); returns the previous setting."""
+    return bool(load().rx_set_tracing(1 if on else 0))
 
 
 def make_desc(dtype: int, hq: int, hkv: int, head_dim: int, num_slots: int, scale: float) -> rx_attn_desc:
@@ -535,10 +541,12 @@ def decode_attention(desc, batch, q, req_to_token, kv_lens, k_pool, v_pool, out,
 
 
 def decode_attention_noalloc(desc, batch, q, req_to_token, kv_lens, k_pool, v_pool, out, lse, max_kv_len, status,
-                             groups=None, stream=None) -> None:
+                             groups=None, stream=None, r2t_stride=None) -> None:
     """decode_attention with the library's static scratch instead of a workspace: for callers
-    that cannot allocate device memory per call.  Overlapping calls race (one shared array)."""
+    that cannot allocate device memory per call.  Overlapping calls race (one shared array).
+    req_to_token is a [batch, stride] tensor, or a device address with r2t_stride given."""
+    stride = req_to_token.shape[1] if r2t_stride is None else r2t_stride
     _check("decode_attention_noalloc", load().decode_attention_noalloc(
-        ctypes.byref(desc), batch, _ptr(q), _ptr(req_to_token), req_to_token.shape[1], _ptr(kv_lens),
+        ctypes.byref(desc), batch, _ptr(q), _ptr(req_to_token), stride, _ptr(kv_lens),
         ctypes.byref(groups) if groups is not None else None, _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(lse),
         max_kv_len, _ptr(status), _stream(stream)))

@@ -382,23 +382,26 @@ int launch_extend_small(const SmallExtendArgs& a, cudaStream_t stream) {
     p.status = a.status;
     const int smem = dec_ring_bytes(a.head_dim) + DEC_MAX_CHUNK * 4;
     dim3 grid((unsigned)a.hkv, (unsigned)a.batch);
-    if (a.head_dim == 128) {
-        static bool attr = false;
-        if (!attr) {
-            cudaFuncSetAttribute(extend_small_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            attr = true;
+    static PerDeviceOnce attr[2];
+    const int rc = per_device_once(attr[a.head_dim == 128 ? 1 : 0], [&] {
+        const cudaError_t e =
+            a.head_dim == 128
+                ? cudaFuncSetAttribute(extend_small_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                : cudaFuncSetAttribute(extend_small_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) {
+            set_error("prefix_extend_attention: cannot set the small-extend shared memory size: %s",
+                      cudaGetErrorString(e));
+            return (int)RX_ECUDA;
         }
+        return (int)RX_OK;
+    });
+    if (rc != RX_OK) return rc;
+    if (a.head_dim == 128)
         extend_small_kernel<128><<<grid, DEC_THREADS, smem, stream>>>(p, a.qo_indptr, a.prefix_lens, a.max_qo_len,
                                                                       (__nv_bfloat16*)a.out, a.lse);
-    } else {
-        static bool attr = false;
-        if (!attr) {
-            cudaFuncSetAttribute(extend_small_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            attr = true;
-        }
+    else
         extend_small_kernel<64><<<grid, DEC_THREADS, smem, stream>>>(p, a.qo_indptr, a.prefix_lens, a.max_qo_len,
                                                                      (__nv_bfloat16*)a.out, a.lse);
-    }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("prefix_extend_attention: small-extend launch failed: %s", cudaGetErrorString(e));
@@ -533,7 +536,9 @@ using namespace rx;
 
 extern "C" size_t decode_workspace_bytes(const rx_attn_desc* desc, int32_t batch, int32_t max_kv_len,
                                          const rx_shared_groups* groups) {
-    if (!desc || batch < 0 || max_kv_len < 1) return 0;
+    if (!desc || batch < 0 || max_kv_len < 1 || desc->hkv <= 0 || desc->hq <= 0) return 0;
+    // the CUDA-core path (fp32, or more than 8 query heads per kv head) takes no workspace
+    if (desc->dtype == RX_F32 || desc->hq / desc->hkv > 8) return 0;
     return dec_layout(desc, batch, max_kv_len, groups).total;
 }
 
@@ -542,6 +547,7 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
                                 const rx_shared_groups* groups, const void* d_k_pool, const void* d_v_pool,
                                 void* d_out, float* d_lse, int32_t max_kv_len, void* d_workspace,
                                 size_t ws_bytes, int32_t* d_status, void* stream_) {
+    RX_TRACE("decode_attention");
     RX_REQUIRE(desc && batch >= 0 && max_kv_len >= 1 && r2t_stride >= 0, "decode_attention: bad arguments");
     RX_REQUIRE(desc->hq > 0 && desc->hkv > 0 && desc->hq % desc->hkv == 0, "decode_attention: bad head counts");
     RX_REQUIRE(desc->head_dim == 64 || desc->head_dim == 128, "decode_attention: head_dim must be 64 or 128");
@@ -616,9 +622,8 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
     }
     const int D = desc->head_dim;
     const size_t smem = dec_smem_bytes(D);
-    static bool attr_set[2] = {false, false};
-    const int di = D == 128 ? 1 : 0;
-    if (!attr_set[di]) {
+    static PerDeviceOnce attr_set[2];
+    const int arc = per_device_once(attr_set[D == 128 ? 1 : 0], [&] {
         const cudaError_t e1 =
             D == 128 ? cudaFuncSetAttribute(decode_private_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
                      : cudaFuncSetAttribute(decode_private_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -627,10 +632,11 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
                             : cudaFuncSetAttribute(decode_private_kernel<64>, cudaFuncAttributePreferredSharedMemoryCarveout, 100));
         if (e1 != cudaSuccess) {
             set_error("decode_attention: cannot set shared memory size: %s", cudaGetErrorString(e1));
-            return RX_ECUDA;
+            return (int)RX_ECUDA;
         }
-        attr_set[di] = true;
-    }
+        return (int)RX_OK;
+    });
+    if (arc != RX_OK) return arc;
     DecodeFork* fork = nullptr;
     std::unique_lock<std::mutex> fork_lock;
     if (use_groups) {
@@ -709,15 +715,13 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
 // allocator of its own to provide the split-KV workspace.  For them this entry point keeps
 // the workspace in one file-scope device array of RX_DECODE_NOALLOC_SCRATCH_BYTES, which
 // every GPU that loads the library holds until the process exits.  Host code cannot use
-// the array's name as a device address, so the address is looked up once per device with
-// cudaGetSymbolAddress (on that device's first call, with the device current) and cached.
+// the array's name as a device address: every call looks the address up with
+// cudaGetSymbolAddress on the current device (a host-side lookup; the device code is loaded
+// on a device's first call), so the address follows the current context, also after a
+// cudaDeviceReset.
 namespace rx {
 
 static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[RX_DECODE_NOALLOC_SCRATCH_BYTES];
-
-constexpr int NOALLOC_MAX_DEVICES = 64;
-static std::mutex g_noalloc_mu;
-static void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
 
 }  // namespace rx
 
@@ -726,6 +730,7 @@ extern "C" int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
                                         const int32_t* d_kv_lens, const rx_shared_groups* groups,
                                         const void* d_k_pool, const void* d_v_pool, void* d_out, float* d_lse,
                                         int32_t max_kv_len, int32_t* d_status, void* stream) {
+    RX_TRACE("decode_attention_noalloc");
     RX_REQUIRE(desc && batch >= 0 && max_kv_len >= 1, "decode_attention_noalloc: bad arguments");
     if (batch == 0) return RX_OK;
     const size_t need = decode_workspace_bytes(desc, batch, max_kv_len, groups);
@@ -733,28 +738,11 @@ extern "C" int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
                "decode_attention_noalloc: this batch needs %zu bytes of scratch, the static scratch holds %zu "
                "(use decode_attention with a caller-provided workspace, or split the batch)",
                need, (size_t)RX_DECODE_NOALLOC_SCRATCH_BYTES);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        set_error("decode_attention_noalloc: cudaGetDevice failed: %s", cudaGetErrorString(e));
-        return RX_ECUDA;
-    }
-    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) {
-        set_error("decode_attention_noalloc: device %d beyond the %d supported", dev, NOALLOC_MAX_DEVICES);
-        return RX_EDEVICE;
-    }
     void* scratch = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(g_noalloc_mu);
-        if (!g_noalloc_ptr[dev]) {
-            e = cudaGetSymbolAddress(&scratch, g_decode_noalloc_scratch);
-            if (e != cudaSuccess) {
-                set_error("decode_attention_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
-                return RX_ECUDA;
-            }
-            g_noalloc_ptr[dev] = scratch;
-        }
-        scratch = g_noalloc_ptr[dev];
+    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_decode_noalloc_scratch);
+    if (e != cudaSuccess || !scratch) {
+        set_error("decode_attention_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+        return RX_ECUDA;
     }
     // The split-KV partials and the group map are fully written before they are read in
     // every call, so the scratch needs no clearing between calls.

@@ -568,24 +568,24 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
     }
 }
 
-static int g_cc_checked = 0;   // 1 = sm_103, -1 = other
-
+// The current device must be an sm_103 (GB300): checked once per device (a device that fails
+// the check is checked again on the next call and fails again).
 static int check_device() {
-    if (g_cc_checked == 0) {
+    static PerDeviceOnce checked;
+    return per_device_once(checked, [] {
         int dev = 0, major = 0, minor = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
             set_error("prefix_extend_attention: cannot query the device");
-            return RX_ECUDA;
+            return (int)RX_ECUDA;
         }
-        g_cc_checked = (major == 10 && minor == 3) ? 1 : -1;
-    }
-    if (g_cc_checked != 1) {
-        set_error("prefix_extend_attention: the tcgen05 kernel needs an sm_103 (GB300) device");
-        return RX_EDEVICE;
-    }
-    return RX_OK;
+        if (major != 10 || minor != 3) {
+            set_error("prefix_extend_attention: the tcgen05 kernel needs an sm_103 (GB300) device");
+            return (int)RX_EDEVICE;
+        }
+        return (int)RX_OK;
+    });
 }
 
 // cuTensorMapEncodeTiled from the driver, resolved once through the runtime (no -lcuda).
@@ -621,13 +621,13 @@ static bool rows_tensor_map(CUtensorMap* m, const void* ptr, int hq, int D, int 
 
 template <int D>
 static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t stream, int gz) {
-    static bool attr = false;
+    static PerDeviceOnce attr;
     const int smem = ExtLayout<D>::ALLOC;
-    if (!attr) {
+    const int rc = per_device_once(attr, [&] {
         const cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) {
             set_error("prefix_extend_attention: cannot set shared memory size: %s", cudaGetErrorString(e));
-            return RX_ECUDA;
+            return (int)RX_ECUDA;
         }
         // The warpgroups re-split the registers the block is launched with (setmaxnreg); the
         // shares must add up to no more than that, or the increasing warps would wait forever.
@@ -636,10 +636,11 @@ static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t strea
             (int64_t)fa.numRegs * EXT_THREADS < 2 * 128 * (int64_t)EXT_REGS_OTHER + 2 * 128 * (int64_t)EXT_REGS_SOFTMAX) {
             set_error("prefix_extend_attention: kernel built with %d registers per thread; the register split needs %d",
                       fa.numRegs, (int)((2 * 128 * EXT_REGS_OTHER + 2 * 128 * EXT_REGS_SOFTMAX) / EXT_THREADS));
-            return RX_ECUDA;
+            return (int)RX_ECUDA;
         }
-        attr = true;
-    }
+        return (int)RX_OK;
+    });
+    if (rc != RX_OK) return rc;
     dim3 grid((unsigned)tiles, (unsigned)p.hkv, (unsigned)gz);
     extend_tc_kernel<D><<<grid, EXT_THREADS, smem, stream>>>(p);
     return RX_OK;
@@ -957,6 +958,7 @@ extern "C" int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch, 
                                        const void* d_v_pool, void* d_out, float* d_lse, int32_t max_qo_len,
                                        const rx_shared_groups* groups, void* d_workspace, size_t ws_bytes,
                                        int32_t* d_status, void* stream_) {
+    RX_TRACE("prefix_extend_attention");
     RX_REQUIRE(desc && batch >= 0 && max_qo_len >= 0 && r2t_stride >= 0, "prefix_extend_attention: bad arguments");
     RX_REQUIRE(desc->hq > 0 && desc->hkv > 0 && desc->hq % desc->hkv == 0,
                "prefix_extend_attention: bad head counts");

@@ -129,6 +129,7 @@ extern "C" int kv_pool_write(const rx_attn_desc* desc, int32_t batch, const int3
                              const int64_t* d_qo_indptr, const void* d_k_new, const void* d_v_new, void* d_k_pool,
                              void* d_v_pool, int32_t* d_req_to_token, int64_t r2t_stride, int64_t total_new,
                              int32_t* d_status, void* stream) {
+    RX_TRACE("kv_pool_write");
     RX_REQUIRE(total_new >= 0, "kv_pool_write: bad arguments");
     return rx::kv_pool_write_rows(desc, batch, d_prefix_slots, d_prefix_indptr, d_new_slots, d_qo_indptr, d_k_new,
                                   d_v_new, d_k_pool, d_v_pool, d_req_to_token, r2t_stride, 0, total_new, d_status,

@@ -20,6 +20,7 @@
 #include <atomic>
 #include <condition_variable>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <functional>
 #include <memory>
@@ -40,6 +41,12 @@
 namespace rx {
 
 static thread_local std::string g_last_error;
+
+static int trace_from_env() {
+    const char* e = std::getenv("RX_NVTX");
+    return (e && e[0] == '1') ? 1 : 0;
+}
+std::atomic<int> g_trace{trace_from_env()};
 
 void set_error(const char* fmt, ...) {
     char buf[512];
@@ -390,6 +397,8 @@ const char* rx_last_error(void) { return rx::g_last_error.c_str(); }
 
 const char* rx_version(void) { return "radixattn 0.1 (sm_103a)"; }
 
+int rx_set_tracing(int on) { return rx::g_trace.exchange(on ? 1 : 0); }
+
 int radix_create(int64_t num_slots, uint64_t slot_perm_seed, rx_radix** out) {
     RX_REQUIRE(out != nullptr, "radix_create: out is NULL");
     RX_REQUIRE(num_slots >= 1 && num_slots <= INT32_MAX, "radix_create: num_slots %lld out of range",
@@ -425,6 +434,7 @@ void radix_destroy(rx_radix* t) { delete t; }
 
 int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slots, int64_t* out_len,
                  rx_node* out_last) {
+    RX_TRACE("match_prefix");
     RX_REQUIRE(t && out_len && out_last && n >= 0 && (n == 0 || (tokens && out_slots)),
                "match_prefix: bad arguments");
     t->clock += 1;
@@ -439,6 +449,7 @@ int match_prefix(rx_radix* t, const int32_t* tokens, int64_t n, int32_t* out_slo
 }
 
 int match_prefix_len(const rx_radix* t, const int32_t* tokens, int64_t n, int64_t* out_len) {
+    RX_TRACE("match_prefix_len");
     RX_REQUIRE(t && out_len && n >= 0 && (n == 0 || tokens), "match_prefix_len: bad arguments");
     const int64_t m = t->cached_len(tokens, n);
     *out_len = m - m % t->page;         // the length match_prefix would return now
@@ -454,6 +465,7 @@ int radix_set_page_size(rx_radix* t, int64_t page_size) {
 
 int match_prefix_len_batch(const rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
                            int64_t* out_len) {
+    RX_TRACE("match_prefix_len_batch");
     RX_REQUIRE(t && batch >= 0 && tok_indptr && (batch == 0 || out_len), "match_prefix_len_batch: bad arguments");
     for (int32_t b = 0; b < batch; ++b)
         RX_REQUIRE(tok_indptr[b + 1] >= tok_indptr[b], "match_prefix_len_batch: request %d has a negative length", b);
@@ -469,6 +481,7 @@ int match_prefix_len_batch(const rx_radix* t, int32_t batch, const int32_t* toke
 }
 
 int radix_lock(rx_radix* t, rx_node node) {
+    RX_TRACE("radix_lock");
     RX_REQUIRE(t, "radix_lock: tree is NULL");
     auto it = t->by_id.find(node);
     RX_REQUIRE(it != t->by_id.end(), "radix_lock: unknown node %lld", (long long)node);
@@ -477,6 +490,7 @@ int radix_lock(rx_radix* t, rx_node node) {
 }
 
 int radix_unlock(rx_radix* t, rx_node node) {
+    RX_TRACE("radix_unlock");
     RX_REQUIRE(t, "radix_unlock: tree is NULL");
     auto it = t->by_id.find(node);
     RX_REQUIRE(it != t->by_id.end(), "radix_unlock: unknown node %lld", (long long)node);
@@ -490,6 +504,7 @@ int radix_unlock(rx_radix* t, rx_node node) {
 }
 
 int radix_lock_batch(rx_radix* t, const rx_node* nodes, int32_t n) {
+    RX_TRACE("radix_lock_batch");
     RX_REQUIRE(t && n >= 0 && (n == 0 || nodes), "radix_lock_batch: bad arguments");
     for (int32_t i = 0; i < n; ++i)
         RX_REQUIRE(t->by_id.count(nodes[i]), "radix_lock_batch: unknown node %lld", (long long)nodes[i]);
@@ -498,6 +513,7 @@ int radix_lock_batch(rx_radix* t, const rx_node* nodes, int32_t n) {
 }
 
 int radix_unlock_batch(rx_radix* t, const rx_node* nodes, int32_t n) {
+    RX_TRACE("radix_unlock_batch");
     RX_REQUIRE(t && n >= 0 && (n == 0 || nodes), "radix_unlock_batch: bad arguments");
     for (int32_t i = 0; i < n; ++i) {
         const int rc = radix_unlock(t, nodes[i]);
@@ -507,6 +523,7 @@ int radix_unlock_batch(rx_radix* t, const rx_node* nodes, int32_t n) {
 }
 
 int alloc_slots(rx_radix* t, int64_t n, int32_t* out_slots) {
+    RX_TRACE("alloc_slots");
     RX_REQUIRE(t && n >= 0 && (n == 0 || out_slots), "alloc_slots: bad arguments");
     if (n > t->count) {
         set_error("alloc_slots: %lld slots requested, %lld free", (long long)n, (long long)t->count);
@@ -524,6 +541,7 @@ int alloc_slots(rx_radix* t, int64_t n, int32_t* out_slots) {
 }
 
 int free_slots(rx_radix* t, const int32_t* slots, int64_t n) {
+    RX_TRACE("free_slots");
     RX_REQUIRE(t && n >= 0 && (n == 0 || slots), "free_slots: bad arguments");
     int64_t i = 0;
     for (; i < n; ++i) {
@@ -546,6 +564,7 @@ int free_slots(rx_radix* t, const int32_t* slots, int64_t n) {
 
 int insert(rx_radix* t, const int32_t* tokens, const int32_t* slots, int64_t n, int64_t* out_dup_len,
            rx_node* out_last) {
+    RX_TRACE("insert");
     RX_REQUIRE(t && out_dup_len && out_last && n >= 0 && (n == 0 || (tokens && slots)),
                "insert: bad arguments");
     // Validate the slots the tree would take before changing anything.
@@ -589,6 +608,7 @@ int insert(rx_radix* t, const int32_t* tokens, const int32_t* slots, int64_t n, 
 }
 
 int evict(rx_radix* t, int64_t num_tokens, int32_t* out_freed, int64_t cap, int64_t* out_n) {
+    RX_TRACE("evict");
     RX_REQUIRE(t && out_n && num_tokens >= 0 && cap >= 0, "evict: bad arguments");
     if (num_tokens == 0) {
         *out_n = 0;
@@ -637,6 +657,7 @@ int evict(rx_radix* t, int64_t num_tokens, int32_t* out_freed, int64_t cap, int6
 
 int match_prefix_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
                        int32_t* out_slots, int64_t* out_indptr, rx_node* out_last) {
+    RX_TRACE("match_prefix_batch");
     RX_REQUIRE(t && batch >= 0 && tok_indptr && out_indptr && (batch == 0 || out_last),
                "match_prefix_batch: bad arguments");
     out_indptr[0] = 0;
@@ -653,6 +674,7 @@ int match_prefix_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const 
 
 int insert_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
                  const int32_t* slots, int64_t* out_dup_len, rx_node* out_last) {
+    RX_TRACE("insert_batch");
     RX_REQUIRE(t && batch >= 0 && tok_indptr && (batch == 0 || (out_dup_len && out_last)),
                "insert_batch: bad arguments");
     for (int32_t b = 0; b < batch; ++b) {
@@ -667,6 +689,7 @@ int insert_batch(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
 int insert_batch_at(rx_radix* t, int32_t batch, const rx_node* nodes, const int32_t* tokens,
                     const int64_t* tok_indptr, const int32_t* new_slots, const int64_t* new_indptr,
                     int64_t* out_dup_len, rx_node* out_last) {
+    RX_TRACE("insert_batch_at");
     RX_REQUIRE(t && batch >= 0 && (batch == 0 || (nodes && tokens && tok_indptr && new_indptr && out_dup_len && out_last)),
                "insert_batch_at: bad arguments");
     for (int32_t b = 0; b < batch; ++b) {
@@ -719,6 +742,7 @@ size_t rx_step_stage_bytes(int32_t batch, int64_t total_tokens) {
 int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr, const int32_t* n_new,
                  int32_t group_mode, int32_t heads_per_kv, int64_t min_shared, void* h_stage, size_t stage_cap,
                  rx_node* out_last, rx_step_layout* out) {
+    RX_TRACE("rx_step_plan");
     RX_REQUIRE(t && batch >= 0 && tok_indptr && out && h_stage && (batch == 0 || (tokens && n_new && out_last)),
                "rx_step_plan: bad arguments");
     const int64_t total_tokens = tok_indptr[batch];
@@ -877,6 +901,7 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
 int rx_step_finish(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_t* tok_indptr,
                    const rx_node* last_nodes, const void* h_stage, const rx_step_layout* L, int64_t evict_tokens,
                    int64_t* out_evicted) {
+    RX_TRACE("rx_step_finish");
     RX_REQUIRE(t && L && h_stage && batch == L->batch && (batch == 0 || (tokens && tok_indptr && last_nodes)),
                "rx_step_finish: bad arguments");
     const unsigned char* st = (const unsigned char*)h_stage;
@@ -912,6 +937,7 @@ int radix_stats(const rx_radix* t, rx_stats* out) {
 }
 
 int radix_check(const rx_radix* t) {
+    RX_TRACE("radix_check");
     RX_REQUIRE(t, "radix_check: tree is NULL");
     std::vector<uint8_t> owned((size_t)t->num_slots, 0);
     int64_t nodes = 0, tokens = 0;
@@ -968,6 +994,7 @@ int radix_check(const rx_radix* t) {
 
 int radix_shared_groups(const rx_radix* t, const rx_node* last_nodes, int32_t batch, int64_t min_shared,
                         int32_t* out_group_of, int64_t* out_group_len, int32_t* out_num_groups) {
+    RX_TRACE("radix_shared_groups");
     RX_REQUIRE(t && batch >= 0 && out_num_groups && (batch == 0 || (last_nodes && out_group_of && out_group_len)),
                "radix_shared_groups: bad arguments");
     // Root paths of every request's end node (root excluded), shallow to deep.

@@ -4,9 +4,34 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "radix_attn.h"
 
 namespace rx {
+
+// Set-up that a CUDA context keeps per device (a kernel's dynamic shared-memory limit and
+// carve-out, a device capability check): done once on each device, under a lock, so that a
+// process driving several GPUs from several threads sets it on every device it launches on.
+// Devices 0..63; a later context on the same device (after cudaDeviceReset) is not tracked.
+struct PerDeviceOnce {
+    std::mutex mu;
+    uint64_t done = 0;        // bit d: set-up succeeded on device d
+};
+
+// Runs f() (returning an RX_* status) the first time it is called with device `dev` current;
+// later calls on that device return RX_OK without running it.  A failed f() is retried on the
+// next call.
+template <class F>
+int per_device_once(PerDeviceOnce& o, F&& f) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return f();
+    std::lock_guard<std::mutex> lk(o.mu);
+    if (o.done & (1ull << dev)) return RX_OK;
+    const int rc = f();
+    if (rc == RX_OK) o.done |= 1ull << dev;
+    return rc;
+}
 
 // Generic CUDA-core causal attention (one warp per row and head).
 struct SimtParams {

@@ -16,6 +16,7 @@
 // Ranges need no other synchronisation: a request's prefix slots were all written by earlier
 // steps, and its own new K/V by its own range.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <mutex>
@@ -25,6 +26,15 @@
 #include "radix_attn.h"
 #include "rx_common.h"
 #include "rx_kernels.h"
+
+namespace rx {
+
+// NVTX ranges of the ABI calls (only reached when tracing is on): NVTX's header-only dispatch
+// forwards them to an attached profiler and ignores them otherwise.
+void trace_push(const char* name) { nvtxRangePushA(name); }
+void trace_pop() { nvtxRangePop(); }
+
+}  // namespace rx
 
 namespace {
 
@@ -219,6 +229,7 @@ extern "C" size_t rx_step_workspace_bytes(const rx_attn_desc* desc, const rx_ste
 }
 
 extern "C" int rx_stage_wait(const void* h_stage) {
+    RX_TRACE("rx_stage_wait");
     cudaEvent_t ev = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_ev_mu);
@@ -237,6 +248,7 @@ extern "C" int rx_stage_wait(const void* h_stage) {
 extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32_t* tokens, const int64_t* tok_indptr,
                               const rx_node* last_nodes, void* h_stage, const rx_step_layout* L, const rx_step_io* io,
                               int64_t evict_tokens, int64_t* out_evicted, void* stream_) {
+    RX_TRACE("rx_step_launch");
     RX_REQUIRE(t && desc && L && io && h_stage && tok_indptr, "rx_step_launch: bad arguments");
     const int32_t B = L->batch;
     cudaStream_t stream = (cudaStream_t)stream_;
@@ -417,6 +429,7 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
 
 extern "C" int rx_step_prefetch(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, const rx_step_io* io,
                                 void* stream_) {
+    RX_TRACE("rx_step_prefetch");
     RX_REQUIRE(desc && io && batch >= 0 && (batch == 0 || n_new), "rx_step_prefetch: bad arguments");
     RX_REQUIRE(io->h_q && io->h_k_new && io->h_v_new && io->d_q && io->d_k_new && io->d_v_new,
                "rx_step_prefetch: needs the host and device rows");

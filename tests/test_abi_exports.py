@@ -33,6 +33,15 @@ def test_every_declared_symbol_is_exported():
 
 def test_host_calls_need_no_gpu():
     assert api.version().startswith("radixattn")
+    # tracing is off unless asked for; with it on the calls still work (NVTX ranges go nowhere
+    # without a profiler) and the setting comes back
+    import numpy as np
+    assert api.set_tracing(True) is False or os.environ.get("RX_NVTX") == "1"
+    t = api.RadixTree(16, 2)
+    sl = t.alloc_slots(3)
+    t.insert(np.array([5, 6, 7], np.int32), sl)
+    assert t.match_prefix_len(np.array([5, 6, 9], np.int32)) == 2
+    assert api.set_tracing(False) is True
     t = api.RadixTree(8, 1)
     assert t.stats()["free_slots"] == 8
 

@@ -369,9 +369,9 @@ int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
 
 /* ------------------------------------------------------------------ one-call step launch
  * Everything of a planned step that follows rx_step_plan, in one call: the staging buffer
- * (h_stage) to its device copy (io->d_stage) -- a kernel reading the device mapping of the
- * pinned buffer in host-buffer mode and for at most 1 MiB, else a copy-engine transfer --,
- * kv_pool_write (a3), the
+ * (h_stage) to its device copy (io->d_stage) -- for at most 1 MiB of device-row step, by
+ * kv_pool_write's own launch reading the device mapping of the pinned buffer; in host-buffer
+ * mode a kernel reading that mapping; else a copy-engine transfer --, kv_pool_write (a3), the
  * attention -- prefix_extend_attention (a4), or decode_attention (a5/a6) when io->decode --
  * with the plan's shared-prefix groups, and rx_step_finish (a7/a8: insert, free duplicates,
  * evict evict_tokens, unpin; host only, it does not wait for the GPU).  All device work is
@@ -447,6 +447,23 @@ int rx_step_prefetch(const rx_attn_desc* desc, int32_t batch, const int32_t* n_n
 
 /* Block until the last rx_step_launch copy out of h_stage is complete (no-op if none). */
 int rx_stage_wait(const void* h_stage);
+
+/* A whole step in one call, for a serving loop that crosses the library boundary once per
+ * step (the pages' serving step: match the cached prefix, compute only the new tokens,
+ * insert them -- "SGLang: Efficient Execution of Structured Language Model Programs",
+ * RadixAttention and the nine-step walk-through).  In order: in host-buffer mode (io->h_q
+ * set) rx_step_prefetch; rx_stage_wait(h_stage); rx_step_plan into h_stage (its arguments and
+ * outputs: out_last, *out); then, when io's device buffers hold the plan -- d_stage_bytes >=
+ * out->bytes, r2t_elems >= batch * out->stride, ws_bytes >= rx_step_workspace_bytes(desc, out,
+ * io->decode) -- rx_step_launch with evict_tokens (*out_evicted, may be NULL, gets the evicted
+ * count).  When a device buffer is too small it returns RX_ENOMEM with the plan made and
+ * pinned and nothing launched: the caller grows the buffer (sizes from *out) and completes the
+ * step with rx_step_launch on that plan.  Any other failure is returned as the failing call
+ * returns it. */
+int rx_step_run(rx_radix* t, const rx_attn_desc* desc, int32_t batch, const int32_t* tokens,
+                const int64_t* tok_indptr, const int32_t* n_new, int32_t group_mode, int32_t heads_per_kv,
+                int64_t min_shared, void* h_stage, size_t stage_cap, const rx_step_io* io, int64_t evict_tokens,
+                rx_node* out_last, rx_step_layout* out, int64_t* out_evicted, void* stream);
 
 /* Thread-local message describing the last failure in this thread ("" if none). */
 const char* rx_last_error(void);

@@ -25,7 +25,7 @@ EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "match_prefix_len", 
            "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "insert_batch_at", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups", "rx_step_stage_bytes", "rx_step_plan", "rx_step_finish",
-           "rx_step_workspace_bytes", "rx_step_launch", "rx_step_prefetch", "rx_stage_wait",
+           "rx_step_workspace_bytes", "rx_step_launch", "rx_step_prefetch", "rx_stage_wait", "rx_step_run",
            "kv_pool_write", "prefix_extend_attention", "extend_workspace_bytes", "decode_workspace_bytes",
            "decode_attention",
            "decode_attention_noalloc",
@@ -121,6 +121,7 @@ def load(path: str = LIB_PATH):
         "rx_step_finish": (ctypes.c_int, [P, I32, P, P, P, P, P, I64, P]),
         "rx_step_workspace_bytes": (SZ, [P, P, I32]),
         "rx_step_launch": (ctypes.c_int, [P, P, P, P, P, P, P, P, I64, P, P]),
+        "rx_step_run": (ctypes.c_int, [P, P, I32, P, P, P, I32, I32, I64, P, SZ, P, I64, P, P, P, P]),
         "rx_step_prefetch": (ctypes.c_int, [P, I32, P, P, P]),
         "rx_stage_wait": (ctypes.c_int, [P]),
         "kv_pool_write": (ctypes.c_int, [P, I32, P, P, P, P, P, P, P, P, P, I64, I64, P, P]),
@@ -407,6 +408,23 @@ def rx_step_launch(tree, desc, tokens: np.ndarray, tok_indptr: np.ndarray, last_
         _addr(last_nodes) if layout.batch else None, stage_addr, ctypes.byref(layout), ctypes.byref(io),
         evict_tokens, ctypes.byref(n), _stream(stream)))
     return n.value
+
+
+def rx_step_run(tree, desc, tokens: np.ndarray, tok_indptr: np.ndarray, n_new: np.ndarray, group_mode: int,
+                heads_per_kv: int, min_shared: int, stage_addr: int, stage_cap: int, io, evict_tokens: int,
+                out_last: np.ndarray, layout, evicted, stream) -> int:
+    """Plan and launch a step in one call (tokens int32, tok_indptr int64, n_new int32, out_last
+    int64 [batch]: contiguous; layout: an rx_step_layout to fill; evicted: a ctypes int64 or
+    None).  Returns RX_OK, or RX_ENOMEM when io's device buffers are too small for the plan
+    (planned and pinned, not launched: grow them and call rx_step_launch); raises otherwise."""
+    b = len(tok_indptr) - 1
+    rc = load().rx_step_run(tree, ctypes.byref(desc), b, _addr(tokens), _addr(tok_indptr), _addr(n_new) if b else None,
+                            group_mode, heads_per_kv, min_shared, stage_addr, stage_cap, ctypes.byref(io), evict_tokens,
+                            _addr(out_last) if b else None, ctypes.byref(layout),
+                            ctypes.byref(evicted) if evicted is not None else None, _stream(stream))
+    if rc != RX_OK and rc != RX_ENOMEM:
+        _check("rx_step_run", rc)
+    return rc
 
 
 def rx_wait_selftest(status, limit_ns: int, stream=None) -> None:

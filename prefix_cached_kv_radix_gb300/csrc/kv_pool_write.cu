@@ -5,7 +5,11 @@
 // written once into their pool slots, and each request's slot table lists its matched
 // (shared) slots followed by its new slots, so attention can gather the whole context.
 //
-// One launch, two kinds of blocks: the first batch * tiles blocks each fill one tile of
+// One launch, three kinds of blocks: optionally, a few blocks first copy a step's staging
+// buffer (its index arrays, read through the device mapping of pinned host memory) to its
+// device copy for the kernels that follow -- the step runtime's small device-row steps, where
+// the table blocks read the slot lists from the mapped buffer themselves -- then batch * tiles
+// blocks each fill one tile of
 // KPW_TILE entries of a table row (coalesced int32 stores; each thread has KPW_PER
 // independent loads in flight, so a long row is not one block's chain of dependent round
 // trips); the rest copy 16-byte vectors of the new K/V rows to their slots (consecutive
@@ -32,11 +36,26 @@ __global__ void __launch_bounds__(KPW_THREADS) kv_pool_write_kernel(
     const int32_t* __restrict__ new_slots, const int64_t* __restrict__ qo_indptr, const uint4* __restrict__ k_new,
     const uint4* __restrict__ v_new, uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
     int32_t* __restrict__ r2t, int64_t stride, int64_t num_slots, int32_t row_vecs, int64_t t_begin, int64_t t_end,
-    int32_t* status) {
+    int32_t* status, const uint4* __restrict__ stage_src, uint4* __restrict__ stage_dst, int64_t stage_vecs,
+    int32_t stage_blocks) {
+    if ((int32_t)blockIdx.x < stage_blocks) {          // the staging buffer to its device copy
+        const int64_t step = (int64_t)stage_blocks * blockDim.x;
+        int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        for (; i + 3 * step < stage_vecs; i += 4 * step) {   // four loads in flight per thread
+            const uint4 a = stage_src[i], b = stage_src[i + step], c = stage_src[i + 2 * step], d = stage_src[i + 3 * step];
+            stage_dst[i] = a;
+            stage_dst[i + step] = b;
+            stage_dst[i + 2 * step] = c;
+            stage_dst[i + 3 * step] = d;
+        }
+        for (; i < stage_vecs; i += step) stage_dst[i] = stage_src[i];
+        return;
+    }
+    const int32_t bid = (int32_t)blockIdx.x - stage_blocks;
     const int64_t table_blocks = (int64_t)batch * tiles;
-    if ((int64_t)blockIdx.x < table_blocks) {
-        const int b = (int)(blockIdx.x / tiles);
-        const int64_t j0 = (int64_t)(blockIdx.x % tiles) * KPW_TILE;
+    if ((int64_t)bid < table_blocks) {
+        const int b = (int)(bid / tiles);
+        const int64_t j0 = (int64_t)(bid % tiles) * KPW_TILE;
         const int64_t p0 = prefix_indptr[b], P = prefix_indptr[b + 1] - p0;
         const int64_t q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0;
         int32_t* row = r2t + (int64_t)b * stride;
@@ -66,8 +85,8 @@ __global__ void __launch_bounds__(KPW_THREADS) kv_pool_write_kernel(
     }
     // new tokens t_begin .. t_end-1 (the rows of this call's requests)
     const int64_t nvec = (t_end - t_begin) * row_vecs;
-    const int64_t step = (int64_t)(gridDim.x - table_blocks) * blockDim.x;
-    for (int64_t j = (int64_t)(blockIdx.x - table_blocks) * blockDim.x + threadIdx.x; j < nvec; j += step) {
+    const int64_t step = (int64_t)(gridDim.x - stage_blocks - table_blocks) * blockDim.x;
+    for (int64_t j = (int64_t)(bid - table_blocks) * blockDim.x + threadIdx.x; j < nvec; j += step) {
         const int64_t i = t_begin * row_vecs + j;
         const int64_t t = i / row_vecs;
         const int32_t v = (int32_t)(i - t * row_vecs);
@@ -89,7 +108,8 @@ namespace rx {
 int kv_pool_write_rows(const rx_attn_desc* desc, int32_t batch, const int32_t* d_prefix_slots,
                        const int64_t* d_prefix_indptr, const int32_t* d_new_slots, const int64_t* d_qo_indptr,
                        const void* d_k_new, const void* d_v_new, void* d_k_pool, void* d_v_pool, int32_t* d_req_to_token,
-                       int64_t r2t_stride, int64_t t_begin, int64_t t_end, int32_t* d_status, cudaStream_t stream) {
+                       int64_t r2t_stride, int64_t t_begin, int64_t t_end, int32_t* d_status, cudaStream_t stream,
+                       const void* stage_src, void* stage_dst, int64_t stage_bytes) {
     RX_REQUIRE(desc && batch >= 0 && r2t_stride >= 0 && t_begin >= 0 && t_end >= t_begin, "kv_pool_write: bad arguments");
     RX_REQUIRE(desc->dtype == RX_F32 || desc->dtype == RX_BF16, "kv_pool_write: unknown dtype %d", desc->dtype);
     RX_REQUIRE(desc->hkv > 0 && desc->head_dim > 0 && desc->num_slots > 0, "kv_pool_write: bad shape");
@@ -108,12 +128,18 @@ int kv_pool_write_rows(const rx_attn_desc* desc, int32_t batch, const int32_t* d
     if (copy_blocks > 152 * 16) copy_blocks = 152 * 16;
     if (copy_blocks < 1) copy_blocks = 1;
     const int64_t tiles = std::max<int64_t>(1, (r2t_stride + KPW_TILE - 1) / KPW_TILE);
-    const int64_t grid = (int64_t)batch * tiles + copy_blocks;
+    RX_REQUIRE(stage_bytes == 0 || (stage_src && stage_dst && stage_bytes % 16 == 0 && ((uintptr_t)stage_src & 15) == 0 &&
+                                    ((uintptr_t)stage_dst & 15) == 0),
+               "kv_pool_write: staging copy must be 16-byte aligned whole vectors");
+    const int64_t stage_vecs = stage_bytes / 16;
+    const int32_t stage_blocks =
+        stage_vecs > 0 ? (int32_t)std::min<int64_t>(64, (stage_vecs + KPW_THREADS * 4 - 1) / (KPW_THREADS * 4)) : 0;
+    const int64_t grid = stage_blocks + (int64_t)batch * tiles + copy_blocks;
     RX_REQUIRE(grid < (1ll << 31) && tiles < (1ll << 31), "kv_pool_write: batch or stride too large");
     kv_pool_write_kernel<<<(unsigned)grid, KPW_THREADS, 0, stream>>>(
         batch, (int32_t)tiles, d_prefix_slots, d_prefix_indptr, d_new_slots, d_qo_indptr, (const uint4*)d_k_new,
         (const uint4*)d_v_new, (uint4*)d_k_pool, (uint4*)d_v_pool, d_req_to_token, r2t_stride, desc->num_slots,
-        row_vecs, t_begin, t_end, d_status);
+        row_vecs, t_begin, t_end, d_status, (const uint4*)stage_src, (uint4*)stage_dst, stage_vecs, stage_blocks);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("kv_pool_write: launch failed: %s", cudaGetErrorString(e));

@@ -39,7 +39,12 @@ void trace_pop() { nvtxRangePop(); }
 namespace {
 
 std::mutex g_ev_mu;
-std::unordered_map<const void*, cudaEvent_t> g_stage_events;   // staging buffer -> event of its last copy
+struct StageInfo {
+    cudaEvent_t ev = nullptr;         // recorded after the last reads of the staging buffer
+    void* h_dev = nullptr;            // its device mapping (null: not mapped)
+    bool mapped_known = false;
+};
+std::unordered_map<const void*, StageInfo> g_stage_events;   // staging buffer -> its event and mapping
 
 // The index arrays of a host-buffer step, read by the GPU straight from the pinned staging
 // buffer (mapped into the device's address space) instead of by a copy engine, so that they
@@ -234,7 +239,7 @@ extern "C" int rx_stage_wait(const void* h_stage) {
     {
         std::lock_guard<std::mutex> lk(g_ev_mu);
         auto it = g_stage_events.find(h_stage);
-        if (it != g_stage_events.end()) ev = it->second;
+        if (it != g_stage_events.end()) ev = it->second.ev;
     }
     if (!ev) return RX_OK;
     const cudaError_t e = cudaEventSynchronize(ev);
@@ -261,19 +266,26 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
         const size_t ws = rx_step_workspace_bytes(desc, L, io->decode);
         RX_REQUIRE(ws == 0 || (io->d_workspace && io->ws_bytes >= ws), "rx_step_launch: workspace of %zu bytes, %zu needed",
                    io->ws_bytes, ws);
+        // the staging buffer's event and device mapping, looked up once per buffer
         cudaEvent_t ev = nullptr;
+        void* h_map = nullptr;
         {
             std::lock_guard<std::mutex> lk(g_ev_mu);
-            auto it = g_stage_events.find(h_stage);
-            if (it == g_stage_events.end()) {
-                if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
-                    set_error("rx_step_launch: cannot create an event");
-                    return RX_ECUDA;
-                }
-                g_stage_events[h_stage] = ev;
-            } else {
-                ev = it->second;
+            StageInfo& si = g_stage_events[h_stage];
+            if (!si.ev && cudaEventCreateWithFlags(&si.ev, cudaEventDisableTiming) != cudaSuccess) {
+                si.ev = nullptr;
+                set_error("rx_step_launch: cannot create an event");
+                return RX_ECUDA;
             }
+            if (!si.mapped_known) {
+                if (cudaHostGetDevicePointer(&si.h_dev, h_stage, 0) != cudaSuccess) {
+                    cudaGetLastError();   // not mapped (pageable): clear the error, copy instead
+                    si.h_dev = nullptr;
+                }
+                si.mapped_known = true;
+            }
+            ev = si.ev;
+            h_map = si.h_dev;
         }
         unsigned char* ds = (unsigned char*)io->d_stage;
         const int32_t* prefix_slots = (const int32_t*)(ds + L->off_prefix_slots);
@@ -299,12 +311,12 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
         // copy-engine transfer (about twice the kernel's rate over the host link)
         constexpr int64_t kSmallStage = 1 << 20;
         const bool by_kernel = host || L->bytes <= kSmallStage;
-        void* h_dev = nullptr;
-        if (by_kernel && cudaHostGetDevicePointer(&h_dev, h_stage, 0) != cudaSuccess) {
-            cudaGetLastError();   // not mapped (pageable): clear the error, copy instead
-            h_dev = nullptr;
-        }
+        void* h_dev = by_kernel ? h_map : nullptr;
         cudaError_t e = cudaSuccess;
+        // device rows, small arrays: kv_pool_write reads the slot lists from the mapping itself
+        // and copies the whole buffer for the attention kernels in the same launch (one launch
+        // fewer); the event follows it
+        bool fused_stage = false;
         // device rows with overlap: the copy runs on the copy-in stream, after the kernels that
         // last read this d_stage (when tracked; else after all work on `stream`), and `stream`
         // waits for it -- under the previous step's kernels when the caller alternates d_stage
@@ -325,6 +337,9 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
             if (e == cudaSuccess) e = cudaEventRecord(ev, sp->in);
             if (e == cudaSuccess) e = cudaEventRecord(sp->staged, sp->in);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, sp->staged, 0);
+        } else if (h_dev && ((uintptr_t)h_dev & 15) == 0 && ((uintptr_t)io->d_stage & 15) == 0 && L->bytes % 16 == 0 &&
+                   !host) {
+            fused_stage = true;
         } else if (h_dev && ((uintptr_t)h_dev & 15) == 0 && ((uintptr_t)io->d_stage & 15) == 0 && L->bytes % 16 == 0) {
             const int64_t n = L->bytes / 16;
             const int blocks = (int)std::min<int64_t>(152 * 2, (n + 255) / 256);
@@ -376,9 +391,23 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
             const int64_t t0 = h_qo[b0], t1 = h_qo[b1];
             const int32_t nb = b1 - b0;
             int32_t* r2t_c = io->d_r2t + (int64_t)b0 * L->stride;
-            int rc = rx::kv_pool_write_rows(desc, nb, prefix_slots, prefix_indptr + b0, new_slots, qo_indptr + b0,
-                                            io->d_k_new, io->d_v_new, io->d_k_pool, io->d_v_pool, r2t_c, L->stride,
-                                            t0, t1, io->d_status, stream);
+            int rc;
+            if (fused_stage) {   // one range (device rows): the index arrays from the mapping
+                const unsigned char* hm = (const unsigned char*)h_dev;
+                rc = rx::kv_pool_write_rows(desc, nb, (const int32_t*)(hm + L->off_prefix_slots),
+                                            (const int64_t*)(hm + L->off_prefix_indptr),
+                                            (const int32_t*)(hm + L->off_new_slots), (const int64_t*)(hm + L->off_qo_indptr),
+                                            io->d_k_new, io->d_v_new, io->d_k_pool, io->d_v_pool, r2t_c, L->stride, t0, t1,
+                                            io->d_status, stream, h_dev, io->d_stage, L->bytes);
+                if (rc == RX_OK && cudaEventRecord(ev, stream) != cudaSuccess) {
+                    set_error("rx_step_launch: cannot record the staging event");
+                    return RX_ECUDA;
+                }
+            } else {
+                rc = rx::kv_pool_write_rows(desc, nb, prefix_slots, prefix_indptr + b0, new_slots, qo_indptr + b0,
+                                            io->d_k_new, io->d_v_new, io->d_k_pool, io->d_v_pool, r2t_c, L->stride, t0,
+                                            t1, io->d_status, stream);
+            }
             if (rc != RX_OK) return rc;
             if (io->decode)   // decode rows are the requests themselves (one new token each)
                 rc = decode_attention(desc, nb, (const char*)io->d_q + t0 * rb.q, r2t_c, L->stride, kv_lens + b0, gp,
@@ -425,6 +454,37 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
         }
     }
     return rx_step_finish(t, B, tokens, tok_indptr, last_nodes, h_stage, L, evict_tokens, out_evicted);
+}
+
+extern "C" int rx_step_run(rx_radix* t, const rx_attn_desc* desc, int32_t batch, const int32_t* tokens,
+                           const int64_t* tok_indptr, const int32_t* n_new, int32_t group_mode, int32_t heads_per_kv,
+                           int64_t min_shared, void* h_stage, size_t stage_cap, const rx_step_io* io,
+                           int64_t evict_tokens, rx_node* out_last, rx_step_layout* out, int64_t* out_evicted,
+                           void* stream) {
+    RX_TRACE("rx_step_run");
+    RX_REQUIRE(t && desc && io && h_stage && out && tok_indptr && batch >= 0, "rx_step_run: bad arguments");
+    int rc = RX_OK;
+    if (io->h_q && batch > 0) {           // the first range's rows start crossing the link now
+        rc = rx_step_prefetch(desc, batch, n_new, io, stream);
+        if (rc != RX_OK) return rc;
+    }
+    rc = rx_stage_wait(h_stage);
+    if (rc != RX_OK) return rc;
+    rc = rx_step_plan(t, batch, tokens, tok_indptr, n_new, group_mode, heads_per_kv, min_shared, h_stage, stage_cap,
+                      out_last, out);
+    if (rc != RX_OK) return rc;
+    if (out->batch > 0 && out->total_new > 0) {
+        const size_t ws = rx_step_workspace_bytes(desc, out, io->decode);
+        if (!io->d_stage || io->d_stage_bytes < (size_t)out->bytes || !io->d_r2t ||
+            io->r2t_elems < (int64_t)out->batch * out->stride || (ws > 0 && (!io->d_workspace || io->ws_bytes < ws))) {
+            set_error("rx_step_run: device buffers too small for this plan (staging %zu of %lld, slot table %lld of "
+                      "%lld, workspace %zu of %zu): planned, not launched",
+                      io->d_stage_bytes, (long long)out->bytes, (long long)io->r2t_elems,
+                      (long long)out->batch * out->stride, io->ws_bytes, ws);
+            return RX_ENOMEM;
+        }
+    }
+    return rx_step_launch(t, desc, tokens, tok_indptr, out_last, h_stage, out, io, evict_tokens, out_evicted, stream);
 }
 
 extern "C" int rx_step_prefetch(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, const rx_step_io* io,

@@ -136,6 +136,7 @@ class PrefixCacheEngine:
         self._pin_np = [None, None]
         self._pin_addr = [0, 0]
         self._io_static = None          # the io whose buffer addresses are current
+        self._bound = None              # (slot table, workspace) addresses bound into it
         self._ws_need = {}
         self._pin_ev = [torch.cuda.Event(), torch.cuda.Event()]
         self._pin_used = [False, False]
@@ -144,6 +145,7 @@ class PrefixCacheEngine:
         self._dev_stage = [None, None]  # the one-call path's device copies of the staging buffers
         self._r2t = None
         self._r2t_flat = None     # the one-call path's slot table ([batch, stride] in a flat buffer)
+        self._last = [None, None]  # the one-call path's match-end nodes, per staging buffer
         self._io = None
         self._stage_need = {}     # (batch, total tokens) -> staging bytes
         self._stream = torch.cuda.current_stream(self.device)
@@ -202,11 +204,13 @@ class PrefixCacheEngine:
         tokens = np.concatenate(prompts).astype(np.int32) if b else np.zeros(0, np.int32)
         return self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)
 
-    def _staging(self, nbytes: int) -> int:
-        """Next pinned staging buffer with room for nbytes, once the copy that last read it is done."""
+    def _staging(self, nbytes: int, native_wait: bool = True) -> int:
+        """Next pinned staging buffer with room for nbytes, once the copy that last read it is done
+        (native_wait=False: the caller's native call waits for a native step's copy itself, unless
+        the buffer has to be replaced here)."""
         i = self._pin_i
         self._pin_i ^= 1
-        if self._pin[i] is not None:
+        if self._pin[i] is not None and (native_wait or self._pin[i].numel() < nbytes):
             api.rx_stage_wait(self._pin_addr[i])            # a native step's copy out of it is done
         if self._pin[i] is None or self._pin[i].numel() < nbytes:
             if self._pin_used[i]:
@@ -244,73 +248,93 @@ class PrefixCacheEngine:
     def step(self, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse=None, decode: bool = False,
              groups=False, min_shared: int = 64, evict_tokens: int = 0, stream=None, host=None,
              chunks: int = 0, overlap: bool = False) -> StepPlan:
-        """A whole step in two library calls: rx_step_plan (a1, a2, groups, pinning, into a
-        pinned staging buffer) and rx_step_launch (the one H2D copy, a3, a4 or a5/a6, then
-        a7/a8 and unpinning).  q/k_new/v_new are the step's new rows in request order; out
-        receives the attention output.  With host=(q_h, k_h, v_h, out_h[, lse_h]) (pinned host
-        tensors of the same shapes) the rows come from and the output goes to host memory,
-        copied by the library as a pipeline of `chunks` request ranges (0: automatic): the
-        input copies start before the plan (rx_step_prefetch) and run behind the kernels with
-        the output copies; they are complete when the stream is.  overlap=True: in host mode the
-        input copies wait only for the kernels of the last step that read the same q buffer, not
-        for all work on the stream -- with two sets of device rows used in turn, a step's copies
-        run under the previous step's kernels (nothing else may still read q/k_new/v_new); with
-        device rows the index arrays' copy runs on a copy stream under the previous step's
-        kernels (the engine alternates two device copies of the staging buffer).
-        Returns the plan (its index arrays stay readable until the plan after next)."""
+        """A whole step in one library call, rx_step_run: rx_step_plan (a1, a2, groups, pinning,
+        into a pinned staging buffer) then rx_step_launch (the index arrays to the device, a3,
+        a4 or a5/a6, then a7/a8 and unpinning).  q/k_new/v_new are the step's new rows in request
+        order; out receives the attention output.  With host=(q_h, k_h, v_h, out_h[, lse_h])
+        (pinned host tensors of the same shapes) the rows come from and the output goes to host
+        memory, copied by the library as a pipeline of `chunks` request ranges (0: automatic):
+        the input copies start before the plan is made (inside the same call) and run behind the
+        kernels with the output copies; they are complete when the stream is.  overlap=True: in
+        host mode the input copies wait only for the kernels of the last step that read the same
+        q buffer, not for all work on the stream -- with two sets of device rows used in turn, a
+        step's copies run under the previous step's kernels (nothing else may still read
+        q/k_new/v_new); with device rows the index arrays' copy runs on a copy stream under the
+        previous step's kernels (the engine alternates two device copies of the staging buffer).
+        When a device buffer turns out too small for the plan, it is grown and the planned step
+        launched with rx_step_launch.  Returns the plan (its index arrays stay readable until the
+        plan after next)."""
         st = self._stream if stream is None else stream
         io = self._io
         if io is None:
             io = self._io = api.rx_step_io()
         if host is not None:
-            # the rows start crossing the host link before the plan is made
-            io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
             io.h_q, io.h_k_new, io.h_v_new, io.h_out = (x.data_ptr() for x in host[:4])
             io.h_lse = host[4].data_ptr() if len(host) > 4 and host[4] is not None else None
             io.chunks = int(chunks)
-            io.overlap = 1 if overlap else 0
-            api.rx_step_prefetch(self.desc, n_new, io, st.cuda_stream)
-        else:
-            if io.h_q:
-                io.h_q = io.h_k_new = io.h_v_new = io.h_out = io.h_lse = None
-                io.chunks = 0
-            io.overlap = 1 if overlap else 0
-        plan = self.plan_concat(tokens, tok_indptr, n_new, groups, min_shared)
-        L = plan.layout
-        # the step's device buffers: grown when needed; their addresses go into io only then
-        fresh = self._io_static is not io
-        total = max(int(L.bytes), 256)
-        # the device copy of the index arrays alternates with the pinned staging buffer, so that
-        # with overlap a step's copy can run while the previous step's kernels read the other
-        ds = self._dev_stage[plan.stage]
-        if ds is None or ds.numel() < total:
-            ds = self._dev_stage[plan.stage] = torch.empty(max(total, 4096) * 2, dtype=torch.uint8, device=self.device)
-        io.d_stage, io.d_stage_bytes = ds.data_ptr(), ds.numel()
-        r2t_need = max(plan.batch, 1) * plan.stride
-        if self._r2t_flat is None or self._r2t_flat.numel() < r2t_need:
-            self._r2t_flat = torch.empty(r2t_need * 2, dtype=torch.int32, device=self.device)
-            fresh = True
-        wkey = (decode, L.batch, L.max_qo_len, L.max_kv_len, L.num_groups, L.max_group_size, L.max_group_len,
-                L.max_group_rows)
-        ws_need = self._ws_need.get(wkey)
-        if ws_need is None:
-            ws_need = self._ws_need[wkey] = api.rx_step_workspace_bytes(self.desc, L, decode)
-        if ws_need and (self._ws is None or self._ws.numel() < ws_need):
-            self._ws = torch.empty(ws_need, dtype=torch.uint8, device=self.device)
-            fresh = True
-        if fresh:
-            io.d_k_pool, io.d_v_pool = self.k_pool.data_ptr(), self.v_pool.data_ptr()
-            io.d_r2t, io.r2t_elems = self._r2t_flat.data_ptr(), self._r2t_flat.numel()
-            io.d_workspace = self._ws.data_ptr() if self._ws is not None else None
-            io.ws_bytes = self._ws.numel() if self._ws is not None else 0
-            io.d_status = self.status.data_ptr()
-            self._io_static = io
+        elif io.h_q:
+            io.h_q = io.h_k_new = io.h_v_new = io.h_out = io.h_lse = None
+            io.chunks = 0
+        io.overlap = 1 if overlap else 0
         io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
         io.d_out, io.d_lse = out.data_ptr(), (lse.data_ptr() if lse is not None else None)
         io.decode = 1 if decode else 0
-        api.rx_step_launch(self.tree.h, self.desc, plan.tokens, plan.tok_indptr, plan.last_nodes,
-                           self._pin_addr[plan.stage], L, io, evict_tokens, st.cuda_stream)
-        return plan
+        tokens = _contig(tokens, np.int32)
+        tok_indptr = _contig(tok_indptr, np.int64)
+        n_new = _contig(n_new, np.int32)
+        b = len(tok_indptr) - 1
+        key = (b, int(tok_indptr[-1]))
+        need = self._stage_need.get(key)
+        if need is None:
+            need = self._stage_need[key] = api.rx_step_stage_bytes(*key)
+        i = self._staging(need, native_wait=False)
+        hbuf = self._pin_np[i]
+        # the device copy of the index arrays alternates with the pinned staging buffer, so that
+        # with overlap a step's copy can run while the previous step's kernels read the other;
+        # the plan's arrays never take more than the staging buffer's bound
+        ds = self._dev_stage[i]
+        if ds is None or ds.numel() < need:
+            ds = self._dev_stage[i] = torch.empty(max(need, 4096) * 2, dtype=torch.uint8, device=self.device)
+        io.d_stage, io.d_stage_bytes = ds.data_ptr(), ds.numel()
+        if self._r2t_flat is None:
+            self._r2t_flat = torch.empty(max(b, 1) * 1024, dtype=torch.int32, device=self.device)
+        # rebind when a buffer was replaced (here, or the workspace by a per-operation call)
+        if self._io_static is not io or self._bound != (self._r2t_flat.data_ptr(),
+                                                        self._ws.data_ptr() if self._ws is not None else 0):
+            self._bind_io(io)
+        last = self._last[i]
+        if last is None or len(last) < max(b, 1):
+            last = self._last[i] = np.empty(max(b, 1) * 2, np.int64)
+        L = api.rx_step_layout()
+        rc = api.rx_step_run(self.tree.h, self.desc, tokens, tok_indptr, n_new, _GROUP_MODE[groups],
+                             self.hq // self.hkv, min_shared, self._pin_addr[i], hbuf.nbytes, io, evict_tokens, last,
+                             L, None, st.cuda_stream)
+        if rc == api.RX_ENOMEM:
+            # planned and pinned, not launched: grow the slot table or the workspace, then launch
+            r2t_need = max(L.batch, 1) * L.stride
+            if self._r2t_flat.numel() < r2t_need:
+                self._r2t_flat = torch.empty(r2t_need * 2, dtype=torch.int32, device=self.device)
+            wkey = (decode, L.batch, L.max_qo_len, L.max_kv_len, L.num_groups, L.max_group_size, L.max_group_len,
+                    L.max_group_rows)
+            ws_need = self._ws_need.get(wkey)
+            if ws_need is None:
+                ws_need = self._ws_need[wkey] = api.rx_step_workspace_bytes(self.desc, L, decode)
+            if ws_need and (self._ws is None or self._ws.numel() < ws_need):
+                self._ws = torch.empty(ws_need, dtype=torch.uint8, device=self.device)
+            self._bind_io(io)
+            api.rx_step_launch(self.tree.h, self.desc, tokens, tok_indptr, last, self._pin_addr[i], L, io,
+                               evict_tokens, st.cuda_stream)
+        return StepPlan(b, tokens, tok_indptr, last[:b], L, i, hbuf)
+
+    def _bind_io(self, io) -> None:
+        """The step io's long-lived buffer addresses (pools, slot table, workspace, status)."""
+        io.d_k_pool, io.d_v_pool = self.k_pool.data_ptr(), self.v_pool.data_ptr()
+        io.d_r2t, io.r2t_elems = self._r2t_flat.data_ptr(), self._r2t_flat.numel()
+        io.d_workspace = self._ws.data_ptr() if self._ws is not None else None
+        io.ws_bytes = self._ws.numel() if self._ws is not None else 0
+        io.d_status = self.status.data_ptr()
+        self._io_static = io
+        self._bound = (self._r2t_flat.data_ptr(), self._ws.data_ptr() if self._ws is not None else 0)
 
     def upload(self, plan: StepPlan, stream=None) -> dict:
         """Move the step's index arrays to the device: one asynchronous H2D copy of the staging

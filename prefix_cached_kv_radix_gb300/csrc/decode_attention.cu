@@ -44,9 +44,10 @@ constexpr float LOG2E = 1.4426950408889634f;
 
 __host__ __device__ constexpr int dec_ring_bytes(int D) {
     // K/V ring, or the cross-warp merge buffer that reuses it, whichever is larger
-    return (DEC_NS * 2 * DEC_STAGE_KEYS * D * 2) > (4 * 8 * D * 4 + 4 * 8 * 2 * 4)
+    // (the merge buffer: partial rows, running max and sum, merge weights, row lse)
+    return (DEC_NS * 2 * DEC_STAGE_KEYS * D * 2) > (4 * 8 * D * 4 + 4 * 8 * 2 * 4 + 4 * 8 * 4 + 8 * 4)
                ? (DEC_NS * 2 * DEC_STAGE_KEYS * D * 2)
-               : (4 * 8 * D * 4 + 4 * 8 * 2 * 4);
+               : (4 * 8 * D * 4 + 4 * 8 * 2 * 4 + 4 * 8 * 4 + 8 * 4);
 }
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -82,50 +83,75 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(
 
 // Gather one stage of K and V (64 keys starting at chunk-relative key k0) into smem.
 // Slot ids come from the chunk's slot list staged in shared memory (slot_s): reading them
-// from global memory here would put one dependent round trip before every copy.
+// from global memory here would put one dependent round trip before every copy.  The list
+// is checked when it is staged and padded with -1 (no key: past the chunk's end, or a bad
+// slot, already reported) to the end of the last stage, so that no copy repeats the check:
+// a -1 slot copies zeros.  col = g * D + this thread's 16-byte column * 8, the same for
+// every key.
 template <int D>
-__device__ __forceinline__ void dec_load_stage(const DecodeParams& p, const int32_t* slot_s, int k0, int k_end,
-                                               int g, uint32_t kbuf, uint32_t vbuf, int tid) {
+__device__ __forceinline__ void dec_load_stage(const DecodeParams& p, const int32_t* slot_s, int k0, int64_t col,
+                                               uint32_t kbuf, uint32_t vbuf, int tid) {
     constexpr int CPR = D / 8;                       // 16-byte chunks per row
     constexpr int PER = DEC_STAGE_KEYS * CPR / DEC_THREADS;
     const int c = tid % CPR;
+    const int64_t row_elems = (int64_t)p.hkv * D;
 #pragma unroll
     for (int x = 0; x < PER; ++x) {
         const int key = tid / CPR + x * (DEC_THREADS / CPR);
-        const int kk = k0 + key;
-        int32_t s = kk < k_end ? slot_s[kk] : 0;
-        uint32_t bytes = 16;
-        if (kk >= k_end) bytes = 0;
-        else if (s < 0 || s >= p.num_slots) {
-            report(p.status, RX_DEV_BAD_SLOT);
-            s = 0;
-            bytes = 0;
-        }
-        const int64_t off = ((int64_t)s * p.hkv + g) * D + c * 8;
+        const int32_t s = slot_s[k0 + key];
+        const int64_t off = (int64_t)max(s, 0) * row_elems + col;
         const uint32_t so = (uint32_t)(key * D * 2) + swz(key, c) * 16;
+        const uint32_t bytes = s >= 0 ? 16u : 0u;
         cp_async_16(kbuf + so, p.k_pool + off, bytes);
         cp_async_16(vbuf + so, p.v_pool + off, bytes);
     }
 }
 
+// A slot from a slot-table row, checked against the pool: out of range, it is reported and
+// becomes -1 (its key reads as zeros).
+__device__ __forceinline__ int32_t checked_slot(const DecodeParams& p, int32_t s) {
+    if (s < 0 || s >= p.num_slots) {
+        report(p.status, RX_DEV_BAD_SLOT);
+        return -1;
+    }
+    return s;
+}
+
+// Where the rows of a tile live (row indices into [rows, D] arrays).  Decode: row n is query
+// head g*group + n of request b (head0 = b*hq + g*group), and its partial goes to slot
+// (head0 + n)*per + chunk.  Small extend: row n is new token n / group, head g*group +
+// n % group (head0 = g*group) of a request whose first new token is qo0, and its final
+// output row is its query row.
+struct DecRowMap {
+    int64_t head0, per, chunk;
+    __device__ __forceinline__ int64_t q_row(int n) const { return head0 + n; }
+    __device__ __forceinline__ int64_t out_row(int n) const { return (head0 + n) * per + chunk; }
+};
+struct ExtRowMap {
+    int64_t qo0;
+    int hq, head0, group;
+    __device__ __forceinline__ int64_t q_row(int n) const { return (qo0 + n / group) * hq + head0 + n % group; }
+    __device__ __forceinline__ int64_t out_row(int n) const { return q_row(n); }
+};
+
 // Causal limits of the rows of a small extend tile: row n may see keys <= pos0 + n / group.
 struct ExtRows {
     int pos0, group;
-    __nv_bfloat16* out;   // final output rows (out_slot[n] = row index into [T * hq])
+    __nv_bfloat16* out;   // final output rows ([T * hq, D])
     float* lse;           // optional natural-log lse per output row
+    bool pair_store;      // out is 4-byte aligned: two bf16 per store
 };
 
 // Attention of up to 8 query rows (packed into N of m16n8k16) over keys [k_begin, k_end)
 // of one slot-table row.  Decode (EXT = false): rows are the query heads of one kv head of
 // one request, all keys visible; writes normalised partial outputs and log2-domain lse at
-// partial slot out_slot[n].  Small extend (EXT = true): rows are (new token, head) pairs of
-// one request with causal limits (ExtRows), the chunk covers every key, and the final bf16
-// output row out_slot[n] (and its lse) is written directly.  Row n reads its query at q_off[n].
-template <int D, bool EXT = false>
+// partial slot rows.out_row(n).  Small extend (EXT = true): rows are (new token, head) pairs
+// of one request with causal limits (ExtRows), the chunk covers every key, and the final
+// bf16 output row rows.out_row(n) (and its lse) is written directly.
+template <int D, bool EXT = false, class RowMap>
 __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* slots_row, int k_begin, int k_end,
-                                          int g, const int64_t* q_off, const int64_t* out_slot, int nrows,
-                                          unsigned char* smem, int32_t* slot_s, ExtRows ext = ExtRows{},
-                                          bool slots_staged = false) {
+                                          int g, const RowMap& rows, int nrows, unsigned char* smem, int32_t* slot_s,
+                                          ExtRows ext = ExtRows{}, bool slots_staged = false) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;                        // m-tiles of O^T
     constexpr int ROWB = D * 2;
@@ -136,11 +162,11 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
     auto kbuf = [&](int st) { return sbase + (uint32_t)(st * 2 * STAGE_B); };
     auto vbuf = [&](int st) { return sbase + (uint32_t)(st * 2 * STAGE_B + STAGE_B); };
 
-    // Q^T fragments (B operand of S^T = K Q^T): head n = r8, dims 16s + 2*t4 (+1), (+8).
+    // Q^T fragments (B operand of S^T = K Q^T): row n = r8, dims 16s + 2*t4 (+1), (+8).
     uint32_t qb[KSTEPS][2];
     {
         const bool valid = r8 < nrows;
-        const __nv_bfloat16* qr = p.q + (valid ? q_off[r8] : 0);
+        const __nv_bfloat16* qr = p.q + (valid ? rows.q_row(r8) * D : 0);
 #pragma unroll
         for (int s = 0; s < KSTEPS; ++s) {
             qb[s][0] = valid ? *reinterpret_cast<const uint32_t*>(qr + 16 * s + 2 * t4) : 0u;
@@ -150,16 +176,25 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
     float o[MT][4];
 #pragma unroll
     for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2*t4, 2*t4+1
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows 2*t4, 2*t4+1
 
-    const int nstages = (k_end - k_begin + DEC_STAGE_KEYS - 1) / DEC_STAGE_KEYS;
     const int nk = k_end - k_begin;                  // <= DEC_MAX_CHUNK
+    const int nstages = (nk + DEC_STAGE_KEYS - 1) / DEC_STAGE_KEYS;
     if (!slots_staged)
-        for (int i = tid; i < nk; i += DEC_THREADS) slot_s[i] = slots_row[k_begin + i];
+        for (int i = tid; i < nstages * DEC_STAGE_KEYS; i += DEC_THREADS)
+            slot_s[i] = i < nk ? checked_slot(p, slots_row[k_begin + i]) : -1;
+    // the last key each of this lane's two rows may see, plus one: the chunk's end, and
+    // extending, the row's own position
+    int end0 = k_end, end1 = k_end;
+    if (EXT) {
+        end0 = min(k_end, ext.pos0 + (2 * t4) / ext.group + 1);
+        end1 = min(k_end, ext.pos0 + (2 * t4 + 1) / ext.group + 1);
+    }
+    const int64_t col = (int64_t)g * D + (tid % (D / 8)) * 8;
     __syncthreads();
 #pragma unroll
     for (int s = 0; s < DEC_NS - 1; ++s) {
-        if (s < nstages) dec_load_stage<D>(p, slot_s, s * DEC_STAGE_KEYS, nk, g, kbuf(s), vbuf(s), tid);
+        if (s < nstages) dec_load_stage<D>(p, slot_s, s * DEC_STAGE_KEYS, col, kbuf(s), vbuf(s), tid);
         cp_async_commit();
     }
     for (int it = 0; it < nstages; ++it) {
@@ -169,7 +204,7 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
         {
             const int nx = it + DEC_NS - 1;
             if (nx < nstages)
-                dec_load_stage<D>(p, slot_s, nx * DEC_STAGE_KEYS, nk, g, kbuf(nx % DEC_NS), vbuf(nx % DEC_NS), tid);
+                dec_load_stage<D>(p, slot_s, nx * DEC_STAGE_KEYS, col, kbuf(nx % DEC_NS), vbuf(nx % DEC_NS), tid);
             cp_async_commit();
         }
         cp_async_wait<DEC_NS - 1>();   // stage it has landed (this thread's copies) ...
@@ -190,21 +225,12 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
                 mma_bf16_16816(sacc, a, qb[s][0], qb[s][1]);
             }
         }
-        // scale, mask keys beyond the chunk (and, extending, beyond each row's position),
-        // online softmax per query row (column)
-        bool ok_lo0 = key0 + r8 < k_end, ok_hi0 = key0 + r8 + 8 < k_end;
-        bool ok_lo1 = ok_lo0, ok_hi1 = ok_hi0;
-        if (EXT) {
-            const int lim0 = ext.pos0 + (2 * t4) / ext.group, lim1 = ext.pos0 + (2 * t4 + 1) / ext.group;
-            ok_lo0 = ok_lo0 && key0 + r8 <= lim0;
-            ok_hi0 = ok_hi0 && key0 + r8 + 8 <= lim0;
-            ok_lo1 = ok_lo1 && key0 + r8 <= lim1;
-            ok_hi1 = ok_hi1 && key0 + r8 + 8 <= lim1;
-        }
-        float x0 = ok_lo0 ? sacc[0] * p.scale_log2 : -INFINITY;
-        float x1 = ok_lo1 ? sacc[1] * p.scale_log2 : -INFINITY;
-        float x2 = ok_hi0 ? sacc[2] * p.scale_log2 : -INFINITY;
-        float x3 = ok_hi1 ? sacc[3] * p.scale_log2 : -INFINITY;
+        // scale, mask keys past each row's limit, online softmax per query row (column)
+        const int kl = key0 + r8, kh = key0 + r8 + 8;
+        float x0 = kl < end0 ? sacc[0] * p.scale_log2 : -INFINITY;
+        float x1 = kl < end1 ? sacc[1] * p.scale_log2 : -INFINITY;
+        float x2 = kh < end0 ? sacc[2] * p.scale_log2 : -INFINITY;
+        float x3 = kh < end1 ? sacc[3] * p.scale_log2 : -INFINITY;
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -213,10 +239,10 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
         }
         float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);   // decode: finite, as key0 < k_end
         // extending, a row may have seen no key yet: keep a finite reference so that the
-        // rescale and the weights below are 0 rather than NaN
+        // rescale and the weights below are 0 rather than NaN (2^-inf is +0 on the SFU)
         const float r0 = EXT && n0 == -INFINITY ? 0.f : n0, r1 = EXT && n1 == -INFINITY ? 0.f : n1;
-        const float a0 = exp2f(m0 - r0), a1 = exp2f(m1 - r1);
-        const float p0 = exp2f(x0 - r0), p1 = exp2f(x1 - r1), p2 = exp2f(x2 - r0), p3 = exp2f(x3 - r1);
+        const float a0 = fast_exp2(m0 - r0), a1 = fast_exp2(m1 - r1);
+        const float p0 = fast_exp2(x0 - r0), p1 = fast_exp2(x1 - r1), p2 = fast_exp2(x2 - r0), p3 = fast_exp2(x3 - r1);
         l0 = l0 * a0 + p0 + p2;
         l1 = l1 * a1 + p1 + p3;
         m0 = n0;
@@ -253,6 +279,8 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
     }
     float* red_o = reinterpret_cast<float*>(smem);                 // [4 warps][8 rows][D]
     float* red_ml = red_o + 4 * 8 * D;                             // [4 warps][8 rows][2]
+    float* red_w = red_ml + 4 * 8 * 2;                             // [4 warps][8 rows]
+    float* row_lse = red_w + 4 * 8;                                // [8 rows] (log2 domain)
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
         const int d = 16 * i + r8;
@@ -268,26 +296,50 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
         red_ml[(warp * 8 + 2 * t4 + 1) * 2 + 1] = l1;
     }
     __syncthreads();
-    for (int idx = tid; idx < nrows * D; idx += DEC_THREADS) {
-        const int n = idx / D, d = idx - n * D;
+    // each row's merge weights, once: warp w's part counts 2^(m_w - M) / L, where M is the
+    // largest running maximum and L = sum_w 2^(m_w - M) l_w
+    if (tid < 8) {
+        const int n = tid;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < 4; ++w) M = fmaxf(M, red_ml[(w * 8 + n) * 2]);
-        float L = 0.f, acc = 0.f;
+        float sc[4], L = 0.f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const float mw = red_ml[(w * 8 + n) * 2];
-            const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
-            L += sc * red_ml[(w * 8 + n) * 2 + 1];
-            acc += sc * red_o[(w * 8 + n) * D + d];
+            sc[w] = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            L += sc[w] * red_ml[(w * 8 + n) * 2 + 1];
         }
-        const int64_t slot = out_slot[n];
+        const float inv = 1.f / L;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) red_w[w * 8 + n] = sc[w] * inv;
+        row_lse[n] = M + log2f(L);
+    }
+    __syncthreads();
+    constexpr int HALF = D / 2;                                    // two dims per thread and pass
+    for (int idx = tid; idx < nrows * HALF; idx += DEC_THREADS) {
+        const int n = idx / HALF, d = 2 * (idx - n * HALF);
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float wt = red_w[w * 8 + n];
+            const float2 v = *reinterpret_cast<const float2*>(red_o + (w * 8 + n) * D + d);
+            acc0 += wt * v.x;
+            acc1 += wt * v.y;
+        }
+        const int64_t slot = rows.out_row(n);
         if (EXT) {
-            ext.out[slot * D + d] = __float2bfloat16_rn(acc / L);
-            if (d == 0 && ext.lse) ext.lse[slot] = (M + log2f(L)) * LN2;
+            __nv_bfloat16* dst = ext.out + slot * D + d;
+            if (ext.pair_store) {
+                *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc0, acc1);
+            } else {
+                dst[0] = __float2bfloat16_rn(acc0);
+                dst[1] = __float2bfloat16_rn(acc1);
+            }
+            if (d == 0 && ext.lse) ext.lse[slot] = row_lse[n] * LN2;
         } else {
-            p.part_o[slot * D + d] = acc / L;
-            if (d == 0) p.part_lse[slot] = M + log2f(L);
+            *reinterpret_cast<float2*>(p.part_o + slot * D + d) = make_float2(acc0, acc1);
+            if (d == 0) p.part_lse[slot] = row_lse[n];
         }
     }
     __syncthreads();
@@ -307,15 +359,8 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_private_kernel(DecodeParam
     const int k_begin = shared + c * p.chunk;
     if (k_begin >= L) return;
     const int k_end = min(L, k_begin + p.chunk);
-    int64_t q_off[8], out_slot[8];
-    const int per = p.max_chunks + p.grp_chunks;
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-        const int h = g * p.group + (n < p.group ? n : 0);
-        q_off[n] = ((int64_t)b * p.hq + h) * D;
-        out_slot[n] = ((int64_t)b * p.hq + h) * per + c;
-    }
-    dec_chunk<D>(p, p.r2t + (int64_t)b * p.stride, k_begin, k_end, g, q_off, out_slot, p.group, smem,
+    const DecRowMap rows{(int64_t)b * p.hq + (int64_t)g * p.group, (int64_t)p.max_chunks + p.grp_chunks, c};
+    dec_chunk<D>(p, p.r2t + (int64_t)b * p.stride, k_begin, k_end, g, rows, p.group, smem,
                  reinterpret_cast<int32_t*>(smem + dec_ring_bytes(D)));
 }
 
@@ -325,7 +370,7 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_private_kernel(DecodeParam
 template <int D>
 __global__ void __launch_bounds__(DEC_THREADS) extend_small_kernel(DecodeParams p, const int64_t* qo_indptr,
                                                                    const int32_t* prefix_lens, int32_t max_qo_len,
-                                                                   __nv_bfloat16* out, float* lse) {
+                                                                   __nv_bfloat16* out, float* lse, int pair_store) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int g = blockIdx.x, b = blockIdx.y;
     // The request's slot-table row is loaded first, up to the table's stride (a launch
@@ -349,21 +394,15 @@ __global__ void __launch_bounds__(DEC_THREADS) extend_small_kernel(DecodeParams 
         if (g == 0 && threadIdx.x == 0) report(p.status, RX_DEV_BAD_LENGTH);
         return;
     }
-    const int rows = n * p.group;
-    int64_t q_off[8], out_row[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int rr = r < rows ? r : 0;
-        out_row[r] = (qo0 + rr / p.group) * p.hq + g * p.group + rr % p.group;
-        q_off[r] = out_row[r] * D;
-    }
+    // the staged list: checked slots for the request's P + n keys, -1 after them
 #pragma unroll
     for (int u = 0; u < PRE; ++u) {
         const int i = (int)threadIdx.x + u * DEC_THREADS;
-        if (i < lim) slot_s[i] = pre[u];
+        slot_s[i] = i < P + n ? checked_slot(p, pre[u]) : -1;
     }
-    ExtRows ext{P, p.group, out, lse};
-    dec_chunk<D, true>(p, row, 0, P + n, g, q_off, out_row, rows, smem, slot_s, ext, true);
+    const ExtRowMap rows{qo0, p.hq, g * p.group, p.group};
+    ExtRows ext{P, p.group, out, lse, pair_store != 0};
+    dec_chunk<D, true>(p, row, 0, P + n, g, rows, n * p.group, smem, slot_s, ext, true);
 }
 
 int launch_extend_small(const SmallExtendArgs& a, cudaStream_t stream) {
@@ -396,12 +435,13 @@ int launch_extend_small(const SmallExtendArgs& a, cudaStream_t stream) {
         return (int)RX_OK;
     });
     if (rc != RX_OK) return rc;
+    const int pair_store = ((uintptr_t)a.out & 3) == 0 ? 1 : 0;   // bf16 pairs in one store
     if (a.head_dim == 128)
         extend_small_kernel<128><<<grid, DEC_THREADS, smem, stream>>>(p, a.qo_indptr, a.prefix_lens, a.max_qo_len,
-                                                                      (__nv_bfloat16*)a.out, a.lse);
+                                                                      (__nv_bfloat16*)a.out, a.lse, pair_store);
     else
         extend_small_kernel<64><<<grid, DEC_THREADS, smem, stream>>>(p, a.qo_indptr, a.prefix_lens, a.max_qo_len,
-                                                                     (__nv_bfloat16*)a.out, a.lse);
+                                                                     (__nv_bfloat16*)a.out, a.lse, pair_store);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("prefix_extend_attention: small-extend launch failed: %s", cudaGetErrorString(e));

@@ -134,132 +134,129 @@ def pool_write_bytes(w, stride: int) -> int:
 
 
 # ---------------------------------------------------------------------------- clocks
+# A separate process samples the clocks, so that the queries run on another core and never on
+# the benchmark's own thread: an NVML query made by the benchmark's thread next to a short step
+# (before it, after it, or during the L2 flush before it) was measured to add 7-15 us to a step.
+_SAMPLER = r"""
+import ctypes, sys, time
+lib = ctypes.CDLL("libnvidia-ml.so.1")
+assert lib.nvmlInit_v2() == 0
+h = ctypes.c_void_p()
+bus = sys.argv[1].encode()
+if not bus or lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+    n = ctypes.c_uint()
+    lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+    idx = 0 if n.value == 1 else int(sys.argv[2])
+    assert lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) == 0
+fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+period = float(sys.argv[3])
+sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm))   # the first queries are the slow ones
+lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+fn(h, ctypes.byref(rs))
+print("ready", flush=True)
+while True:   # the maximum clock is fixed: queried once above
+    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and fn(h, ctypes.byref(rs)) == 0:
+        print(sm.value, mx.value, rs.value, flush=True)
+    time.sleep(period)
+"""
+
+
 class ClockSampler:
-    """SM clock and throttle reasons of this process's GPU, sampled through NVML (read only)
-    every few milliseconds from a background thread while a timed region runs, and on demand
-    with sample().  Falls back to `nvidia-smi -lms 200` when NVML cannot be loaded."""
+    """SM clock and throttle reasons of this process's GPU (read only), sampled every
+    0.2 ms (plus the query's own time) by a separate process through NVML while the timed regions run (start/pause
+    around each region); falls back to `nvidia-smi -lms 200` when NVML cannot be used."""
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index: int, period_s: float = 0.001):
+    def __init__(self, device_index: int, period_s: float = 0.0002):
         self.period = period_s
+        self.dev = device_index
         self.samples = []             # (sm_mhz, max_mhz, reasons bitmask)
-        self.lock = threading.Lock()
-        self.running = False
+        self.proc = None
         self.thread = None
-        self.nvml = None
-        self.handle = None
-        self.smi = None
+        self.smi = False
         self.smi_lines = []
-        self._open(device_index)
-
-    def _open(self, device_index):
+        self.bus = ""
         try:
-            lib = ctypes.CDLL("libnvidia-ml.so.1")
-            if lib.nvmlInit_v2() != 0:
-                return
-            h = ctypes.c_void_p()
-            got = False
-            try:
-                import torch
-                pr = torch.cuda.get_device_properties(device_index)
-                bus = f"{getattr(pr, 'pci_domain_id', 0):08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
-                got = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
-            except Exception:
-                got = False
-            if not got:
-                n = ctypes.c_uint()
-                lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
-                idx = 0 if n.value == 1 else device_index
-                got = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) == 0
-            if got:
-                self.nvml, self.handle = lib, h
-                self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                    getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        except (OSError, AttributeError):
-            self.nvml = None
+            import torch
+            pr = torch.cuda.get_device_properties(device_index)
+            self.bus = f"{getattr(pr, 'pci_domain_id', 0):08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        except Exception:
+            self.bus = ""
 
-    def sample(self):
-        if self.nvml is None:
-            return
-        sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
-        if (self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(sm)) == 0 and
-                self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0):
-            self.reasons_fn(self.handle, ctypes.byref(rs))
-            with self.lock:
-                self.samples.append((sm.value, mx.value, rs.value))
-
-    def _loop(self):
-        while self.running:
-            self.sample()
-            time.sleep(self.period)
+    def _reader(self, proc, sink):
+        for ln in proc.stdout:
+            sink.append(ln.strip())
 
     def start(self):
-        """Sample in the background (NVML) until pause() or stop()."""
-        if self.nvml is not None:
-            if not self.running:
-                self.running = True
-                self.thread = threading.Thread(target=self._loop, daemon=True)
-                self.thread.start()
+        """Start sampling (a no-op while sampling)."""
+        if self.proc is not None:
             return
-        if self.smi is not None:
-            return
+        lines = []
         try:
-            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-            self.smi = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                                         "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=lambda: self.smi_lines.extend(ln.strip() for ln in self.smi.stdout),
-                                           daemon=True)
-            self.thread.start()
-        except OSError:
-            self.smi = None
+            self.proc = subprocess.Popen([sys.executable, "-c", _SAMPLER, self.bus, str(self.dev), str(self.period)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self.proc.stdout.readline().strip()
+            if first != "ready":
+                raise OSError("sampler did not start")
+            self.smi = False
+        except (OSError, ValueError):
+            if self.proc is not None:
+                self.proc.kill()
+            try:
+                q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                     "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+                self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.bus or self.dev}", f"--query-gpu={q}",
+                                              "--format=csv,noheader,nounits", "-lms", "200"],
+                                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.smi = True
+            except OSError:
+                self.proc = None
+                return
+        self.thread = threading.Thread(target=self._reader, args=(self.proc, lines), daemon=True)
+        self.thread.start()
+        self._lines = lines
 
     def pause(self):
-        if self.nvml is not None and self.running:
-            self.running = False
-            self.thread.join(timeout=2)
+        """Stop sampling and keep what was sampled."""
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        for ln in self._lines:
+            f = ln.replace(",", " ").split()
+            try:
+                if self.smi:
+                    if len(f) < 9:
+                        continue
+                    bits = 0
+                    for name, val in zip((0x8, 0x40, 0x20, 0x4), f[5:9]):
+                        if val.lower() in ("active", "1", "yes"):
+                            bits |= name
+                    self.samples.append((float(f[1]), float(f[2]), bits))
+                else:
+                    self.samples.append((float(f[0]), float(f[1]), int(f[2])))
+            except (ValueError, IndexError):
+                continue
+        self.proc = None
 
     def stop(self):
-        """Stop sampling; returns {sm_mhz (median), sm_max_mhz, reasons, samples, source} or None."""
-        if self.nvml is not None:
-            self.pause()
-            with self.lock:
-                smp = list(self.samples)
-            if not smp:
-                return None
-            reasons = sorted({name for _, _, r in smp for bit, name in self.REASONS.items() if r & bit})
-            return {"sm_mhz": statistics.median(x[0] for x in smp), "sm_max_mhz": max(x[1] for x in smp),
-                    "sm_min_mhz": min(x[0] for x in smp), "reasons": reasons, "samples": len(smp),
-                    "source": (f"NVML: every {self.period * 1e3:.0f} ms during back-to-back timed regions, "
-                               "before every step timed alone")}
-        if self.smi is None:
+        """Stop sampling; returns {sm_mhz (median), sm_max_mhz, sm_min_mhz, reasons, samples, source} or None."""
+        self.pause()
+        if not self.samples:
             return None
-        self.smi.terminate()
-        try:
-            self.smi.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.smi.kill()
-        self.thread.join(timeout=2)
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.smi_lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = max(mx, float(f[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, f[5:9]):
-                if val.lower() in ("active", "1", "yes"):
-                    reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
-                "source": "nvidia-smi every 200 ms"}
+        smp = self.samples
+        reasons = sorted({name for _, _, r in smp for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(x[0] for x in smp), "sm_max_mhz": max(x[1] for x in smp),
+                "sm_min_mhz": min(x[0] for x in smp), "reasons": reasons, "samples": len(smp),
+                "source": ("nvidia-smi every 200 ms during the timed regions" if self.smi else
+                           f"NVML from a separate process, one query per {self.period * 1e3:.1f} ms sleep, during the timed regions")}
 
 
 # ---------------------------------------------------------------------------- replicas
@@ -396,11 +393,11 @@ def measure(name, args, rank, world, local_rank, cpu: bool):
     group_mode = True if s.decode else "auto"
 
     def n_launch(grouped: bool, e2e: bool, stage_bytes: int) -> int:
-        # kv_pool_write (plus the index-array copy kernel for host-buffer steps and for index
-        # arrays of at most 1 MiB; larger ones of device-row steps go by the copy engine), then
-        # for decode: (group map, shared chunks) + private chunks + merge; for extend: extend,
-        # or (prep, shared tcgen05, private + merge) with groups
-        base = 2 if (e2e or stage_bytes <= (1 << 20)) else 1
+        # kv_pool_write (plus the index-array copy kernel for host-buffer steps; device-row
+        # steps copy arrays of at most 1 MiB inside kv_pool_write's launch and larger ones by
+        # the copy engine), then for decode: (group map, shared chunks) + private chunks +
+        # merge; for extend: extend, or (prep, shared tcgen05, private + merge) with groups
+        base = 2 if e2e else 1
         if s.decode:
             return base + (2 if grouped else 0) + 2
         return base + (1 if not grouped else 3)
@@ -478,20 +475,19 @@ def measure(name, args, rank, world, local_rank, cpu: bool):
                 torch.distributed.barrier()
             return e0.elapsed_time(e1), launches[0]
         times = []
-        if clocks.nvml is None:
-            clocks.start()
+        clocks.start()
         for i in range(args.steps):
             flush.zero_()                      # untimed: evict L2 between timed steps
             # the flush completes before the timed region opens, so the step's host work
             # (planning, launches, finish) cannot hide behind it: the region holds the whole step
             torch.cuda.synchronize()
-            clocks.sample()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             step(first + i, e2e=e2e)
             e1.record(stream)
             times.append((e0, e1))
         torch.cuda.synchronize()
+        clocks.pause()
         if world > 1:
             torch.distributed.barrier()
         ms = sum(a.elapsed_time(b) for a, b in times)

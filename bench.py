@@ -389,7 +389,7 @@ def measure(name, args, rank, world, local_rank, cpu: bool):
         prompts = fresh_prompts(w, i, used)
         ind = np.concatenate([[0], np.cumsum([len(x) for x in prompts])]).astype(np.int64)
         step_inputs.append((np.concatenate(prompts).astype(np.int32), ind))
-    n_new = np.asarray(s.req_new, np.int64)
+    n_new = np.asarray(s.req_new, np.int32)   # the library's own type: no conversion per step
     group_mode = True if s.decode else "auto"
 
     def n_launch(grouped: bool, e2e: bool, stage_bytes: int) -> int:
@@ -464,6 +464,9 @@ def measure(name, args, rank, world, local_rank, cpu: bool):
         first = args.warmup + (args.steps if e2e else 0) if first is None else first
         if not isolated:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)                  # created before timing starts (see below)
+            e1.record(stream)
+            torch.cuda.synchronize()
             clocks.start()
             e0.record(stream)
             for i in range(args.steps):
@@ -474,18 +477,22 @@ def measure(name, args, rank, world, local_rank, cpu: bool):
             if world > 1:
                 torch.distributed.barrier()
             return e0.elapsed_time(e1), launches[0]
-        times = []
+        # the events exist before timing starts (an event's first record creates it, which would
+        # otherwise fall inside the timed region)
+        times = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for e0, e1 in times:
+            e0.record(stream)
+            e1.record(stream)
         clocks.start()
         for i in range(args.steps):
             flush.zero_()                      # untimed: evict L2 between timed steps
             # the flush completes before the timed region opens, so the step's host work
             # (planning, launches, finish) cannot hide behind it: the region holds the whole step
             torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0, e1 = times[i]
             e0.record(stream)
             step(first + i, e2e=e2e)
             e1.record(stream)
-            times.append((e0, e1))
         torch.cuda.synchronize()
         clocks.pause()
         if world > 1:

@@ -445,25 +445,50 @@ int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32_t* tokens,
 int rx_step_prefetch(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, const rx_step_io* io,
                      void* stream);
 
-/* Block until the last rx_step_launch copy out of h_stage is complete (no-op if none). */
+/* Block until the last rx_step_launch that read h_stage is done with it (no-op if none): by
+ * its CUDA event, or, for a small device-row step (index arrays read by kv_pool_write itself
+ * through the buffer's device mapping), by a sequence number that launch writes to pinned host
+ * memory when its last block is done -- read here without a CUDA call while the GPU is ahead;
+ * after that, with short sleeps, returning RX_ECUDA on a context fault or after 60 s. */
 int rx_stage_wait(const void* h_stage);
 
 /* A whole step in one call, for a serving loop that crosses the library boundary once per
  * step (the pages' serving step: match the cached prefix, compute only the new tokens,
  * insert them -- "SGLang: Efficient Execution of Structured Language Model Programs",
- * RadixAttention and the nine-step walk-through).  In order: in host-buffer mode (io->h_q
- * set) rx_step_prefetch; rx_stage_wait(h_stage); rx_step_plan into h_stage (its arguments and
- * outputs: out_last, *out); then, when io's device buffers hold the plan -- d_stage_bytes >=
- * out->bytes, r2t_elems >= batch * out->stride, ws_bytes >= rx_step_workspace_bytes(desc, out,
- * io->decode) -- rx_step_launch with evict_tokens (*out_evicted, may be NULL, gets the evicted
- * count).  When a device buffer is too small it returns RX_ENOMEM with the plan made and
- * pinned and nothing launched: the caller grows the buffer (sizes from *out) and completes the
- * step with rx_step_launch on that plan.  Any other failure is returned as the failing call
- * returns it. */
-int rx_step_run(rx_radix* t, const rx_attn_desc* desc, int32_t batch, const int32_t* tokens,
-                const int64_t* tok_indptr, const int32_t* n_new, int32_t group_mode, int32_t heads_per_kv,
-                int64_t min_shared, void* h_stage, size_t stage_cap, const rx_step_io* io, int64_t evict_tokens,
-                rx_node* out_last, rx_step_layout* out, int64_t* out_evicted, void* stream);
+ * RadixAttention and the nine-step walk-through).  The arguments sit in one struct, so that a
+ * loop keeps one per staging buffer and changes only the step's inputs (batch, tokens,
+ * tok_indptr, n_new) between calls.  In order: in host-buffer mode (io->h_q set)
+ * rx_step_prefetch; rx_stage_wait(h_stage); rx_step_plan(tree, batch, tokens, tok_indptr,
+ * n_new, group_mode, heads_per_kv, min_shared, h_stage, stage_cap, out_last, out); then, when
+ * io's device buffers hold the plan -- d_stage_bytes >= out->bytes, r2t_elems >= batch *
+ * out->stride, ws_bytes >= rx_step_workspace_bytes(desc, out, io->decode) -- rx_step_launch
+ * with evict_tokens (*out_evicted, may be NULL, gets the evicted count) on `stream`.  When a
+ * device buffer is too small it returns RX_ENOMEM with the plan made and pinned and nothing
+ * launched: the caller grows the buffer (sizes from *out) and completes the step with
+ * rx_step_launch on that plan.  Any other failure is returned as the failing call returns it.
+ * The struct is only read; *out, out_last and *out_evicted are written. */
+typedef struct {
+    rx_radix* tree;
+    const rx_attn_desc* desc;
+    int32_t batch;
+    int32_t group_mode;           /* RX_GROUPS_NONE / _ALWAYS / _AUTO */
+    const int32_t* tokens;        /* host, the prompts concatenated */
+    const int64_t* tok_indptr;    /* host, [batch + 1] */
+    const int32_t* n_new;         /* host, [batch] */
+    int32_t heads_per_kv;
+    int32_t pad0;
+    int64_t min_shared;
+    void* h_stage;                /* pinned staging buffer and its size in bytes */
+    size_t stage_cap;
+    const rx_step_io* io;
+    int64_t evict_tokens;
+    rx_node* out_last;            /* host, [batch] */
+    rx_step_layout* out;
+    int64_t* out_evicted;         /* optional */
+    void* stream;                 /* cudaStream_t */
+} rx_step_args;
+
+int rx_step_run(const rx_step_args* args);
 
 /* Thread-local message describing the last failure in this thread ("" if none). */
 const char* rx_last_error(void);

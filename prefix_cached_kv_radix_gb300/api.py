@@ -81,6 +81,15 @@ class rx_step_io(ctypes.Structure):
                 ("h_out", ctypes.c_void_p), ("h_lse", ctypes.c_void_p), ("chunks", ctypes.c_int32),
                 ("overlap", ctypes.c_int32)]
 
+class rx_step_args(ctypes.Structure):
+    _fields_ = [("tree", ctypes.c_void_p), ("desc", ctypes.c_void_p), ("batch", ctypes.c_int32),
+                ("group_mode", ctypes.c_int32), ("tokens", ctypes.c_void_p), ("tok_indptr", ctypes.c_void_p),
+                ("n_new", ctypes.c_void_p), ("heads_per_kv", ctypes.c_int32), ("pad0", ctypes.c_int32),
+                ("min_shared", ctypes.c_int64), ("h_stage", ctypes.c_void_p), ("stage_cap", ctypes.c_size_t),
+                ("io", ctypes.c_void_p), ("evict_tokens", ctypes.c_int64), ("out_last", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("out_evicted", ctypes.c_void_p), ("stream", ctypes.c_void_p)]
+
+
 _lib = None
 P = ctypes.c_void_p
 I32, I64, U64, SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
@@ -121,7 +130,7 @@ def load(path: str = LIB_PATH):
         "rx_step_finish": (ctypes.c_int, [P, I32, P, P, P, P, P, I64, P]),
         "rx_step_workspace_bytes": (SZ, [P, P, I32]),
         "rx_step_launch": (ctypes.c_int, [P, P, P, P, P, P, P, P, I64, P, P]),
-        "rx_step_run": (ctypes.c_int, [P, P, I32, P, P, P, I32, I32, I64, P, SZ, P, I64, P, P, P, P]),
+        "rx_step_run": (ctypes.c_int, [P]),
         "rx_step_prefetch": (ctypes.c_int, [P, I32, P, P, P]),
         "rx_stage_wait": (ctypes.c_int, [P]),
         "kv_pool_write": (ctypes.c_int, [P, I32, P, P, P, P, P, P, P, P, P, I64, I64, P, P]),
@@ -410,18 +419,13 @@ def rx_step_launch(tree, desc, tokens: np.ndarray, tok_indptr: np.ndarray, last_
     return n.value
 
 
-def rx_step_run(tree, desc, tokens: np.ndarray, tok_indptr: np.ndarray, n_new: np.ndarray, group_mode: int,
-                heads_per_kv: int, min_shared: int, stage_addr: int, stage_cap: int, io, evict_tokens: int,
-                out_last: np.ndarray, layout, evicted, stream) -> int:
-    """Plan and launch a step in one call (tokens int32, tok_indptr int64, n_new int32, out_last
-    int64 [batch]: contiguous; layout: an rx_step_layout to fill; evicted: a ctypes int64 or
-    None).  Returns RX_OK, or RX_ENOMEM when io's device buffers are too small for the plan
-    (planned and pinned, not launched: grow them and call rx_step_launch); raises otherwise."""
-    b = len(tok_indptr) - 1
-    rc = load().rx_step_run(tree, ctypes.byref(desc), b, _addr(tokens), _addr(tok_indptr), _addr(n_new) if b else None,
-                            group_mode, heads_per_kv, min_shared, stage_addr, stage_cap, ctypes.byref(io), evict_tokens,
-                            _addr(out_last) if b else None, ctypes.byref(layout),
-                            ctypes.byref(evicted) if evicted is not None else None, _stream(stream))
+def rx_step_run(args) -> int:
+    """Plan and launch a step in one call.  args: an rx_step_args (tokens int32, tok_indptr
+    int64, n_new int32, out_last int64 [batch]: host addresses of contiguous arrays; out: the
+    address of an rx_step_layout to fill), or its address as an int.  Returns RX_OK, or
+    RX_ENOMEM when io's device buffers are too small for the plan (planned and pinned, not
+    launched: grow them and call rx_step_launch); raises otherwise."""
+    rc = load().rx_step_run(args if isinstance(args, int) else ctypes.addressof(args))
     if rc != RX_OK and rc != RX_ENOMEM:
         _check("rx_step_run", rc)
     return rc

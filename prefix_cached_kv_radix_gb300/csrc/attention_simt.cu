@@ -5,8 +5,8 @@
 // cached keys/values stand in for recomputing the prefix.  Row i of request b (position
 // p = P_b + i) of query head h attends keys 0..p gathered through req_to_token[b, :].
 //
-// One warp per (row, head); lanes split the head dimension; keys are streamed one at a
-// time with an online softmax.  This path serves fp32 (the tiny correctness workload),
+// One warp per (row, head); lanes split the head dimension; keys are streamed with an online
+// softmax, their slots and K/V rows fetched ahead of use.  This path serves fp32 (the tiny correctness workload),
 // where tensor cores would change the arithmetic; bf16 goes through the tcgen05 extend
 // kernel and the mma.sync decode kernel.
 #include <cuda_bf16.h>
@@ -78,27 +78,49 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtParams p) {
     }
     const int32_t* slots = p.r2t + (int64_t)b * p.stride;
     float m = -INFINITY, l = 0.f;
-    for (int64_t j = 0; j <= pos; ++j) {
-        const int32_t s = slots[j];
-        if (s < 0 || s >= p.num_slots) {
-            if (lane == 0) report(p.status, RX_DEV_BAD_SLOT);
-            continue;
+    // Keys in runs of 32: one coalesced load of the run's slots (a lane each), then four keys'
+    // K and V rows requested together before the first is used, so that a key costs a
+    // fraction of a memory round trip instead of two dependent ones.  The online softmax still
+    // takes the keys one by one in order, with the same arithmetic as a key-at-a-time loop.
+    const int64_t nkeys = pos + 1;
+    for (int64_t j0 = 0; j0 < nkeys; j0 += 32) {
+        const int cnt = (int)(nkeys - j0 < 32 ? nkeys - j0 : 32);
+        const int32_t s_lane = lane < cnt ? slots[j0 + lane] : 0;
+        if (lane < cnt && (s_lane < 0 || s_lane >= p.num_slots)) report(p.status, RX_DEV_BAD_SLOT);
+        for (int k0 = 0; k0 < cnt; k0 += 4) {
+            float kv[4][E], vv[4][E];
+            bool ok[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int32_t s = __shfl_sync(0xffffffffu, s_lane, (k0 + u) & 31);   // the same in every lane
+                ok[u] = k0 + u < cnt && s >= 0 && s < p.num_slots;
+                const int64_t base = ((int64_t)(ok[u] ? s : 0) * p.hkv + g) * D;
+                const T* kr = (const T*)p.k_pool + base;
+                const T* vr = (const T*)p.v_pool + base;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    kv[u][e] = ok[u] ? to_f<T>(kr[lane + 32 * e]) : 0.f;
+                    vv[u][e] = ok[u] ? to_f<T>(vr[lane + 32 * e]) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (!ok[u]) continue;       // a bad slot (reported) or past the row's last key
+                float dot = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) dot += qv[e] * kv[u][e];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                const float sc = dot * p.scale;
+                const float mn = fmaxf(m, sc);
+                const float corr = expf(m - mn);
+                const float w = expf(sc - mn);
+                l = l * corr + w;
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = acc[e] * corr + w * vv[u][e];
+                m = mn;
+            }
         }
-        const T* kr = (const T*)p.k_pool + ((int64_t)s * p.hkv + g) * D;
-        const T* vr = (const T*)p.v_pool + ((int64_t)s * p.hkv + g) * D;
-        float dot = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) dot += qv[e] * to_f<T>(kr[lane + 32 * e]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        const float sc = dot * p.scale;
-        const float mn = fmaxf(m, sc);
-        const float corr = expf(m - mn);
-        const float w = expf(sc - mn);
-        l = l * corr + w;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = acc[e] * corr + w * to_f<T>(vr[lane + 32 * e]);
-        m = mn;
     }
     T* orow = (T*)p.out + (row * p.hq + h) * D;
     const float inv = l > 0.f ? 1.f / l : 0.f;

@@ -102,6 +102,7 @@ struct SmallExtendArgs {
 };
 int launch_extend_small(const SmallExtendArgs& a, cudaStream_t stream);
 
+
 // kv_pool_write for the requests of one call whose new tokens are t_begin .. t_end-1 (index
 // arrays absolute: a slice of a step's requests passes its offset pointers).  With stage_bytes
 // > 0 the same launch also copies stage_src (16-byte aligned, any device-readable address, e.g.
@@ -111,6 +112,7 @@ int kv_pool_write_rows(const rx_attn_desc* desc, int32_t batch, const int32_t* d
                        const int64_t* d_prefix_indptr, const int32_t* d_new_slots, const int64_t* d_qo_indptr,
                        const void* d_k_new, const void* d_v_new, void* d_k_pool, void* d_v_pool, int32_t* d_req_to_token,
                        int64_t r2t_stride, int64_t t_begin, int64_t t_end, int32_t* d_status, cudaStream_t stream,
-                       const void* stage_src = nullptr, void* stage_dst = nullptr, int64_t stage_bytes = 0);
+                       const void* stage_src = nullptr, void* stage_dst = nullptr, int64_t stage_bytes = 0,
+                       unsigned* done_ctr = nullptr, uint32_t* done_flag = nullptr, uint32_t done_seq = 0);
 
 }  // namespace rx

@@ -19,7 +19,9 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <chrono>
 #include <mutex>
+#include <thread>
 #include <unordered_map>
 #include <vector>
 
@@ -43,6 +45,16 @@ struct StageInfo {
     cudaEvent_t ev = nullptr;         // recorded after the last reads of the staging buffer
     void* h_dev = nullptr;            // its device mapping (null: not mapped)
     bool mapped_known = false;
+    // Small device-row steps: kv_pool_write is the staging buffer's only reader, and its last
+    // block writes `seq` to flag_host (pinned, mapped; flag_dev on the device) when the launch
+    // is done with the buffer, counting its blocks in ctr_dev (device memory on `dev`).  Then
+    // no event is recorded, and waiting is reading host memory.
+    uint32_t* flag_host = nullptr;
+    uint32_t* flag_dev = nullptr;
+    unsigned* ctr_dev = nullptr;
+    int dev = -1;
+    uint32_t seq = 0;
+    int mode = 0;                     // the last launch's reads end at: 0 nothing, 1 ev, 2 flag == seq
 };
 std::unordered_map<const void*, StageInfo> g_stage_events;   // staging buffer -> its event and mapping
 
@@ -233,14 +245,76 @@ extern "C" size_t rx_step_workspace_bytes(const rx_attn_desc* desc, const rx_ste
                   : extend_workspace_bytes(desc, L->batch, L->max_qo_len, gp);
 }
 
+// The staging buffer's completion flag and block counter on the current device, made on the
+// buffer's first small device-row launch there (the counter is cleared on `stream`, ahead of
+// that launch).  RX_OK when the buffer can use them on this device.
+static int stage_flag(StageInfo* si, cudaStream_t stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RX_ECUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_ev_mu);
+    if (si->flag_host) return si->dev == dev ? RX_OK : RX_EINVAL;
+    void* h = nullptr;
+    void* d = nullptr;
+    void* c = nullptr;
+    if (cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess ||
+        cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess || cudaMalloc(&c, 64) != cudaSuccess ||
+        cudaMemsetAsync(c, 0, 64, stream) != cudaSuccess) {
+        cudaGetLastError();
+        if (c) cudaFree(c);
+        if (h) cudaFreeHost(h);
+        return RX_ECUDA;
+    }
+    si->flag_host = (uint32_t*)h;
+    *si->flag_host = 0;
+    si->flag_dev = (uint32_t*)d;
+    si->ctr_dev = (unsigned*)c;
+    si->dev = dev;
+    si->seq = 0;
+    return RX_OK;
+}
+
+// Wait until *flag == seq: first by reading it (the GPU is usually done by the time the host
+// gets here), then with short sleeps while checking the context for a fault, for at most a
+// minute.  The acquire load orders the caller's later writes to the staging buffer after it.
+static int wait_stage_flag(const uint32_t* flag, uint32_t seq) {
+    for (int i = 0; i < 4096; ++i)
+        if (__atomic_load_n(flag, __ATOMIC_ACQUIRE) == seq) return RX_OK;
+    const auto t0 = std::chrono::steady_clock::now();
+    while (__atomic_load_n(flag, __ATOMIC_ACQUIRE) != seq) {
+        const cudaError_t e = cudaStreamQuery(0);   // reports an earlier fault; does not wait
+        if (e != cudaSuccess && e != cudaErrorNotReady) {
+            set_error("rx_stage_wait: %s", cudaGetErrorString(e));
+            return RX_ECUDA;
+        }
+        if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(60)) {
+            set_error("rx_stage_wait: the staging buffer's last launch has not finished after 60 s");
+            return RX_ECUDA;
+        }
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+    }
+    return RX_OK;
+}
+
 extern "C" int rx_stage_wait(const void* h_stage) {
     RX_TRACE("rx_stage_wait");
     cudaEvent_t ev = nullptr;
+    const uint32_t* flag = nullptr;
+    uint32_t seq = 0;
     {
         std::lock_guard<std::mutex> lk(g_ev_mu);
         auto it = g_stage_events.find(h_stage);
-        if (it != g_stage_events.end()) ev = it->second.ev;
+        if (it != g_stage_events.end()) {
+            if (it->second.mode == 1) ev = it->second.ev;
+            if (it->second.mode == 2) {
+                flag = it->second.flag_host;
+                seq = it->second.seq;
+            }
+        }
     }
+    if (flag) return wait_stage_flag(flag, seq);
     if (!ev) return RX_OK;
     const cudaError_t e = cudaEventSynchronize(ev);
     if (e != cudaSuccess) {
@@ -269,9 +343,11 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
         // the staging buffer's event and device mapping, looked up once per buffer
         cudaEvent_t ev = nullptr;
         void* h_map = nullptr;
+        StageInfo* sinfo = nullptr;
         {
             std::lock_guard<std::mutex> lk(g_ev_mu);
             StageInfo& si = g_stage_events[h_stage];
+            sinfo = &si;   // entries are never erased: the reference stays valid
             if (!si.ev && cudaEventCreateWithFlags(&si.ev, cudaEventDisableTiming) != cudaSuccess) {
                 si.ev = nullptr;
                 set_error("rx_step_launch: cannot create an event");
@@ -354,6 +430,10 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
             set_error("rx_step_launch: staging copy failed: %s", cudaGetErrorString(e));
             return RX_ECUDA;
         }
+        if (!fused_stage) {   // the event just recorded marks the end of the buffer's reads
+            std::lock_guard<std::mutex> lk(g_ev_mu);
+            sinfo->mode = 1;
+        }
         std::vector<int32_t> cut{0, B};
         Pipe* pp = nullptr;
         std::unique_lock<std::mutex> pipe_lock;
@@ -394,14 +474,30 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
             int rc;
             if (fused_stage) {   // one range (device rows): the index arrays from the mapping
                 const unsigned char* hm = (const unsigned char*)h_dev;
+                // the launch's end is signalled in host memory when this buffer has a flag on
+                // this device, else by the event
+                const bool by_flag = stage_flag(sinfo, stream) == RX_OK;
+                uint32_t seq = 0;
+                if (by_flag) {
+                    std::lock_guard<std::mutex> lk(g_ev_mu);
+                    seq = ++sinfo->seq;
+                }
                 rc = rx::kv_pool_write_rows(desc, nb, (const int32_t*)(hm + L->off_prefix_slots),
                                             (const int64_t*)(hm + L->off_prefix_indptr),
                                             (const int32_t*)(hm + L->off_new_slots), (const int64_t*)(hm + L->off_qo_indptr),
                                             io->d_k_new, io->d_v_new, io->d_k_pool, io->d_v_pool, r2t_c, L->stride, t0, t1,
-                                            io->d_status, stream, h_dev, io->d_stage, L->bytes);
-                if (rc == RX_OK && cudaEventRecord(ev, stream) != cudaSuccess) {
-                    set_error("rx_step_launch: cannot record the staging event");
-                    return RX_ECUDA;
+                                            io->d_status, stream, h_dev, io->d_stage, L->bytes,
+                                            by_flag ? sinfo->ctr_dev : nullptr, by_flag ? sinfo->flag_dev : nullptr, seq);
+                if (rc == RX_OK && by_flag) {
+                    std::lock_guard<std::mutex> lk(g_ev_mu);
+                    sinfo->mode = 2;
+                } else if (rc == RX_OK) {
+                    if (cudaEventRecord(ev, stream) != cudaSuccess) {
+                        set_error("rx_step_launch: cannot record the staging event");
+                        return RX_ECUDA;
+                    }
+                    std::lock_guard<std::mutex> lk(g_ev_mu);
+                    sinfo->mode = 1;
                 }
             } else {
                 rc = rx::kv_pool_write_rows(desc, nb, prefix_slots, prefix_indptr + b0, new_slots, qo_indptr + b0,
@@ -456,12 +552,20 @@ extern "C" int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32
     return rx_step_finish(t, B, tokens, tok_indptr, last_nodes, h_stage, L, evict_tokens, out_evicted);
 }
 
-extern "C" int rx_step_run(rx_radix* t, const rx_attn_desc* desc, int32_t batch, const int32_t* tokens,
-                           const int64_t* tok_indptr, const int32_t* n_new, int32_t group_mode, int32_t heads_per_kv,
-                           int64_t min_shared, void* h_stage, size_t stage_cap, const rx_step_io* io,
-                           int64_t evict_tokens, rx_node* out_last, rx_step_layout* out, int64_t* out_evicted,
-                           void* stream) {
+extern "C" int rx_step_run(const rx_step_args* a) {
     RX_TRACE("rx_step_run");
+    RX_REQUIRE(a, "rx_step_run: bad arguments");
+    rx_radix* t = a->tree;
+    const rx_attn_desc* desc = a->desc;
+    const int32_t batch = a->batch;
+    const int32_t* tokens = a->tokens;
+    const int64_t* tok_indptr = a->tok_indptr;
+    const int32_t* n_new = a->n_new;
+    void* h_stage = a->h_stage;
+    const rx_step_io* io = a->io;
+    rx_node* out_last = a->out_last;
+    rx_step_layout* out = a->out;
+    void* stream = a->stream;
     RX_REQUIRE(t && desc && io && h_stage && out && tok_indptr && batch >= 0, "rx_step_run: bad arguments");
     int rc = RX_OK;
     if (io->h_q && batch > 0) {           // the first range's rows start crossing the link now
@@ -470,8 +574,8 @@ extern "C" int rx_step_run(rx_radix* t, const rx_attn_desc* desc, int32_t batch,
     }
     rc = rx_stage_wait(h_stage);
     if (rc != RX_OK) return rc;
-    rc = rx_step_plan(t, batch, tokens, tok_indptr, n_new, group_mode, heads_per_kv, min_shared, h_stage, stage_cap,
-                      out_last, out);
+    rc = rx_step_plan(t, batch, tokens, tok_indptr, n_new, a->group_mode, a->heads_per_kv, a->min_shared, h_stage,
+                      a->stage_cap, out_last, out);
     if (rc != RX_OK) return rc;
     if (out->batch > 0 && out->total_new > 0) {
         const size_t ws = rx_step_workspace_bytes(desc, out, io->decode);
@@ -484,7 +588,8 @@ extern "C" int rx_step_run(rx_radix* t, const rx_attn_desc* desc, int32_t batch,
             return RX_ENOMEM;
         }
     }
-    return rx_step_launch(t, desc, tokens, tok_indptr, out_last, h_stage, out, io, evict_tokens, out_evicted, stream);
+    return rx_step_launch(t, desc, tokens, tok_indptr, out_last, h_stage, out, io, a->evict_tokens, a->out_evicted,
+                          stream);
 }
 
 extern "C" int rx_step_prefetch(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, const rx_step_io* io,

@@ -14,6 +14,8 @@ strings library calls together and moves the step's small index arrays to the de
 from __future__ import annotations
 
 
+import ctypes
+
 import numpy as np
 import torch
 
@@ -31,7 +33,7 @@ def _dev_from_host(a, dtype_bits, device):
 
 def _contig(a, dt):
     """a as a C-contiguous array of dtype dt (the array itself when it already is one)."""
-    if isinstance(a, np.ndarray) and a.dtype == dt and a.flags.c_contiguous:
+    if type(a) is np.ndarray and a.dtype == dt and a.flags.c_contiguous:
         return a
     return np.ascontiguousarray(a, dt)
 
@@ -40,23 +42,33 @@ class StepPlan:
     """One planned step.  The index arrays are views of the pinned staging buffer the step's
     device copy is made from (two buffers alternate: a plan stays valid until the plan after
     next); each is made on first use."""
-    __slots__ = ("batch", "tokens", "tok_indptr", "last_nodes", "max_qo_len", "max_kv_len", "stride", "layout",
-                 "stage", "_host", "_views")
+    __slots__ = ("batch", "tokens", "tok_indptr", "last_nodes", "layout", "stage", "_host", "_views")
 
     def __init__(self, batch, tokens, tok_indptr, last_nodes, layout, stage, host):
         self.batch = batch
         self.tokens = tokens            # concatenated full prompts (cached part + new tokens)
         self.tok_indptr = tok_indptr    # [batch+1]
         self.last_nodes = last_nodes    # [batch] node where each match ended (pinned until finish)
-        self.max_qo_len = layout.max_qo_len
-        self.max_kv_len = layout.max_kv_len
-        self.stride = layout.stride
         self.layout = layout            # rx_step_layout of the staging buffer
         self.stage = stage              # which staging buffer
         self._host = host
-        self._views = {}
+        self._views = None
+
+    @property
+    def max_qo_len(self):
+        return self.layout.max_qo_len
+
+    @property
+    def max_kv_len(self):
+        return self.layout.max_kv_len
+
+    @property
+    def stride(self):
+        return self.layout.stride
 
     def _view(self, name, off, n, dt):
+        if self._views is None:
+            self._views = {}
         v = self._views.get(name)
         if v is None:
             v = self._views[name] = self._host[off:off + n * np.dtype(dt).itemsize].view(dt)
@@ -136,7 +148,6 @@ class PrefixCacheEngine:
         self._pin_np = [None, None]
         self._pin_addr = [0, 0]
         self._io_static = None          # the io whose buffer addresses are current
-        self._bound = None              # (slot table, workspace) addresses bound into it
         self._ws_need = {}
         self._pin_ev = [torch.cuda.Event(), torch.cuda.Event()]
         self._pin_used = [False, False]
@@ -146,6 +157,14 @@ class PrefixCacheEngine:
         self._r2t = None
         self._r2t_flat = None     # the one-call path's slot table ([batch, stride] in a flat buffer)
         self._last = [None, None]  # the one-call path's match-end nodes, per staging buffer
+        self._args = [None, None]  # the one-call path's rx_step_args and layout, per staging buffer
+        self._args_addr = [0, 0]
+        self._args_set = [None, None]  # the per-buffer fields last written into each
+        self._layout = [None, None]
+        self._dev_stage_cap = [0, 0]
+        self._bound_bufs = (None, None)  # the slot table and workspace objects bound into the io
+        self._io_flags = None            # (overlap, decode) last written into the io
+        self._io_host = False            # the io holds host-buffer addresses
         self._io = None
         self._stage_need = {}     # (batch, total tokens) -> staging bytes
         self._stream = torch.cuda.current_stream(self.device)
@@ -272,13 +291,17 @@ class PrefixCacheEngine:
             io.h_q, io.h_k_new, io.h_v_new, io.h_out = (x.data_ptr() for x in host[:4])
             io.h_lse = host[4].data_ptr() if len(host) > 4 and host[4] is not None else None
             io.chunks = int(chunks)
-        elif io.h_q:
+            self._io_host = True
+        elif self._io_host:
             io.h_q = io.h_k_new = io.h_v_new = io.h_out = io.h_lse = None
             io.chunks = 0
-        io.overlap = 1 if overlap else 0
+            self._io_host = False
+        flags = (1 if overlap else 0, 1 if decode else 0)
+        if flags != self._io_flags:
+            io.overlap, io.decode = flags
+            self._io_flags = flags
         io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
         io.d_out, io.d_lse = out.data_ptr(), (lse.data_ptr() if lse is not None else None)
-        io.decode = 1 if decode else 0
         tokens = _contig(tokens, np.int32)
         tok_indptr = _contig(tok_indptr, np.int64)
         n_new = _contig(n_new, np.int32)
@@ -287,28 +310,46 @@ class PrefixCacheEngine:
         need = self._stage_need.get(key)
         if need is None:
             need = self._stage_need[key] = api.rx_step_stage_bytes(*key)
-        i = self._staging(need, native_wait=False)
+        i = self._pin_i
+        if self._pin[i] is not None and not self._pin_used[i] and self._pin_np[i].nbytes >= need:
+            self._pin_i = i ^ 1           # the buffer fits; the library waits for its last reader
+        else:
+            i = self._staging(need, native_wait=False)
         hbuf = self._pin_np[i]
         # the device copy of the index arrays alternates with the pinned staging buffer, so that
         # with overlap a step's copy can run while the previous step's kernels read the other;
         # the plan's arrays never take more than the staging buffer's bound
-        ds = self._dev_stage[i]
-        if ds is None or ds.numel() < need:
+        if self._dev_stage_cap[i] < need:
             ds = self._dev_stage[i] = torch.empty(max(need, 4096) * 2, dtype=torch.uint8, device=self.device)
-        io.d_stage, io.d_stage_bytes = ds.data_ptr(), ds.numel()
+            self._dev_stage_cap[i] = ds.numel()
         if self._r2t_flat is None:
             self._r2t_flat = torch.empty(max(b, 1) * 1024, dtype=torch.int32, device=self.device)
         # rebind when a buffer was replaced (here, or the workspace by a per-operation call)
-        if self._io_static is not io or self._bound != (self._r2t_flat.data_ptr(),
-                                                        self._ws.data_ptr() if self._ws is not None else 0):
+        if self._io_static is not io or self._bound_bufs[0] is not self._r2t_flat or self._bound_bufs[1] is not self._ws:
             self._bind_io(io)
+        a = self._args[i]
+        if a is None:
+            a = self._args[i] = api.rx_step_args()
+            self._args_addr[i] = ctypes.addressof(a)
+            L = self._layout[i] = api.rx_step_layout()
+            a.tree, a.desc, a.io, a.out = self.tree.h, ctypes.addressof(self.desc), ctypes.addressof(io), \
+                ctypes.addressof(L)
+        L = self._layout[i]
         last = self._last[i]
         if last is None or len(last) < max(b, 1):
             last = self._last[i] = np.empty(max(b, 1) * 2, np.int64)
-        L = api.rx_step_layout()
-        rc = api.rx_step_run(self.tree.h, self.desc, tokens, tok_indptr, n_new, _GROUP_MODE[groups],
-                             self.hq // self.hkv, min_shared, self._pin_addr[i], hbuf.nbytes, io, evict_tokens, last,
-                             L, None, st.cuda_stream)
+            a.out_last = api._addr(last)
+        # the step's inputs; the rest of the struct only when it changes
+        a.batch, a.tokens, a.tok_indptr, a.n_new = b, api._addr(tokens), api._addr(tok_indptr), api._addr(n_new)
+        per = (_GROUP_MODE[groups], min_shared, evict_tokens, st.cuda_stream, self._pin_addr[i], hbuf.nbytes,
+               self._dev_stage[i])
+        if per != self._args_set[i]:
+            a.group_mode, a.heads_per_kv, a.min_shared, a.evict_tokens = per[0], self.hq // self.hkv, per[1], per[2]
+            a.stream, a.h_stage, a.stage_cap = per[3], per[4], per[5]
+            self._args_set[i] = per
+        # the device staging copy that goes with this buffer
+        io.d_stage, io.d_stage_bytes = self._dev_stage_addr(i), self._dev_stage_cap[i]
+        rc = api.rx_step_run(self._args_addr[i])
         if rc == api.RX_ENOMEM:
             # planned and pinned, not launched: grow the slot table or the workspace, then launch
             r2t_need = max(L.batch, 1) * L.stride
@@ -326,6 +367,9 @@ class PrefixCacheEngine:
                                evict_tokens, st.cuda_stream)
         return StepPlan(b, tokens, tok_indptr, last[:b], L, i, hbuf)
 
+    def _dev_stage_addr(self, i: int) -> int:
+        return self._dev_stage[i].data_ptr()
+
     def _bind_io(self, io) -> None:
         """The step io's long-lived buffer addresses (pools, slot table, workspace, status)."""
         io.d_k_pool, io.d_v_pool = self.k_pool.data_ptr(), self.v_pool.data_ptr()
@@ -334,7 +378,7 @@ class PrefixCacheEngine:
         io.ws_bytes = self._ws.numel() if self._ws is not None else 0
         io.d_status = self.status.data_ptr()
         self._io_static = io
-        self._bound = (self._r2t_flat.data_ptr(), self._ws.data_ptr() if self._ws is not None else 0)
+        self._bound_bufs = (self._r2t_flat, self._ws)
 
     def upload(self, plan: StepPlan, stream=None) -> dict:
         """Move the step's index arrays to the device: one asynchronous H2D copy of the staging

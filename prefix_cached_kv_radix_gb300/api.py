@@ -81,6 +81,7 @@ class rx_step_io(ctypes.Structure):
                 ("h_out", ctypes.c_void_p), ("h_lse", ctypes.c_void_p), ("chunks", ctypes.c_int32),
                 ("overlap", ctypes.c_int32)]
 
+
 class rx_step_args(ctypes.Structure):
     _fields_ = [("tree", ctypes.c_void_p), ("desc", ctypes.c_void_p), ("batch", ctypes.c_int32),
                 ("group_mode", ctypes.c_int32), ("tokens", ctypes.c_void_p), ("tok_indptr", ctypes.c_void_p),
@@ -429,6 +430,30 @@ def rx_step_run(args) -> int:
     if rc != RX_OK and rc != RX_ENOMEM:
         _check("rx_step_run", rc)
     return rc
+
+
+_step_ext = None
+
+
+def step_ext():
+    """The _rxstep extension (the per-step marshalling of rx_step_run in C, built next to the
+    library where the Python headers are installed), bound to the loaded library's rx_step_run;
+    None when it was not built (the ctypes path then makes the same call)."""
+    global _step_ext
+    if _step_ext is None:
+        from .build import pystep_path
+        path = pystep_path()
+        _step_ext = False
+        if os.path.exists(path):
+            import importlib.machinery
+            import importlib.util
+            loader = importlib.machinery.ExtensionFileLoader("_rxstep", path)
+            spec = importlib.util.spec_from_file_location("_rxstep", path, loader=loader)
+            m = importlib.util.module_from_spec(spec)
+            loader.exec_module(m)
+            m.bind(ctypes.cast(load().rx_step_run, ctypes.c_void_p).value)
+            _step_ext = m
+    return _step_ext or None
 
 
 def rx_wait_selftest(status, limit_ns: int, stream=None) -> None:

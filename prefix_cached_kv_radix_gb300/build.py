@@ -3,7 +3,9 @@
     python -m prefix_cached_kv_radix_gb300.build [--force] [-v]
 
 Translation units compile in parallel; the result is prefix_cached_kv_radix_gb300/_build/
-libradixattn.so (git-ignored).  nvcc: -gencode arch=compute_103a,code=sm_103a -O3 -lineinfo.
+libradixattn.so (git-ignored).  nvcc: -gencode arch=compute_103a,code=sm_103a -O3 -lineinfo.  Also
+_build/_rxstep*.so, the per-step call's marshalling as a CPython extension, where the Python
+headers are installed.
 """
 from __future__ import annotations
 
@@ -26,6 +28,13 @@ CU_SOURCES = ["kv_pool_write.cu", "attention_simt.cu", "extend_attention.cu", "d
               "wait_selftest.cu"]
 CPP_SOURCES = ["radix_tree.cpp"]
 GENCODE = "arch=compute_103a,code=sm_103a"
+# the per-step marshalling as a CPython extension (optional: the ctypes binding does the same)
+PYSTEP_SRC = "pystep.c"
+
+
+def pystep_path() -> str:
+    import sysconfig
+    return os.path.join(OUT_DIR, "_rxstep" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
 
 
 def nvcc() -> str:
@@ -92,7 +101,22 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         _run([nv, "-shared", "-gencode", GENCODE, "-o", tmp, *objs, "-lcudart_static", "-lrt", "-lpthread",
               "-ldl"], verbose)
         os.replace(tmp, LIB_PATH)
+    build_pystep(force, verbose)
     return LIB_PATH
+
+
+def build_pystep(force: bool = False, verbose: bool = False) -> str | None:
+    """The _rxstep extension next to the library, when the Python headers are installed."""
+    import sysconfig
+    inc = sysconfig.get_paths().get("include")
+    if not inc or not os.path.exists(os.path.join(inc, "Python.h")):
+        return None
+    src, out = os.path.join(CSRC, PYSTEP_SRC), pystep_path()
+    if force or _stale(out, src):
+        tmp = out + f".tmp{os.getpid()}"
+        _run(["gcc", "-O2", "-shared", "-fPIC", "-Wall", "-I", inc, "-I", INCLUDE, src, "-o", tmp], verbose)
+        os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

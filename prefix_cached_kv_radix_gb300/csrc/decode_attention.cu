@@ -44,10 +44,10 @@ constexpr float LOG2E = 1.4426950408889634f;
 
 __host__ __device__ constexpr int dec_ring_bytes(int D) {
     // K/V ring, or the cross-warp merge buffer that reuses it, whichever is larger
-    // (the merge buffer: partial rows, running max and sum, merge weights, row lse)
-    return (DEC_NS * 2 * DEC_STAGE_KEYS * D * 2) > (4 * 8 * D * 4 + 4 * 8 * 2 * 4 + 4 * 8 * 4 + 8 * 4)
+    // (the merge buffer: partial rows of D + 4 floats, running max and sum, merge weights, row lse)
+    return (DEC_NS * 2 * DEC_STAGE_KEYS * D * 2) > (4 * 8 * (D + 4) * 4 + 4 * 8 * 2 * 4 + 4 * 8 * 4 + 8 * 4)
                ? (DEC_NS * 2 * DEC_STAGE_KEYS * D * 2)
-               : (4 * 8 * D * 4 + 4 * 8 * 2 * 4 + 4 * 8 * 4 + 8 * 4);
+               : (4 * 8 * (D + 4) * 4 + 4 * 8 * 2 * 4 + 4 * 8 * 4 + 8 * 4);
 }
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -247,12 +247,16 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
         l1 = l1 * a1 + p1 + p3;
         m0 = n0;
         m1 = n1;
+        // the accumulators change only where a running maximum moved (most stages, once the
+        // first keys are in, move none: then the warp skips the multiplies)
+        if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            o[i][0] *= a0;
-            o[i][1] *= a1;
-            o[i][2] *= a0;
-            o[i][3] *= a1;
+            for (int i = 0; i < MT; ++i) {
+                o[i][0] *= a0;
+                o[i][1] *= a1;
+                o[i][2] *= a0;
+                o[i][3] *= a1;
+            }
         }
         const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
         const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
@@ -277,17 +281,20 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    float* red_o = reinterpret_cast<float*>(smem);                 // [4 warps][8 rows][D]
-    float* red_ml = red_o + 4 * 8 * D;                             // [4 warps][8 rows][2]
+    // rows padded to D + 4 floats: the four lanes of a quad (t4) store rows 2*t4 (+1) of the
+    // same columns, which a D-float row stride would put in one bank
+    constexpr int RS = D + 4;
+    float* red_o = reinterpret_cast<float*>(smem);                 // [4 warps][8 rows][RS]
+    float* red_ml = red_o + 4 * 8 * RS;                            // [4 warps][8 rows][2]
     float* red_w = red_ml + 4 * 8 * 2;                             // [4 warps][8 rows]
     float* row_lse = red_w + 4 * 8;                                // [8 rows] (log2 domain)
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
         const int d = 16 * i + r8;
-        red_o[(warp * 8 + 2 * t4) * D + d] = o[i][0];
-        red_o[(warp * 8 + 2 * t4 + 1) * D + d] = o[i][1];
-        red_o[(warp * 8 + 2 * t4) * D + d + 8] = o[i][2];
-        red_o[(warp * 8 + 2 * t4 + 1) * D + d + 8] = o[i][3];
+        red_o[(warp * 8 + 2 * t4) * RS + d] = o[i][0];
+        red_o[(warp * 8 + 2 * t4 + 1) * RS + d] = o[i][1];
+        red_o[(warp * 8 + 2 * t4) * RS + d + 8] = o[i][2];
+        red_o[(warp * 8 + 2 * t4 + 1) * RS + d + 8] = o[i][3];
     }
     if (r8 == 0) {
         red_ml[(warp * 8 + 2 * t4) * 2 + 0] = m0;
@@ -323,7 +330,7 @@ __device__ __forceinline__ void dec_chunk(const DecodeParams& p, const int32_t* 
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const float wt = red_w[w * 8 + n];
-            const float2 v = *reinterpret_cast<const float2*>(red_o + (w * 8 + n) * D + d);
+            const float2 v = *reinterpret_cast<const float2*>(red_o + (w * 8 + n) * RS + d);
             acc0 += wt * v.x;
             acc1 += wt * v.y;
         }
@@ -373,6 +380,10 @@ __global__ void __launch_bounds__(DEC_THREADS) extend_small_kernel(DecodeParams 
                                                                    __nv_bfloat16* out, float* lse, int pair_store) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int g = blockIdx.x, b = blockIdx.y;
+    // Launched with programmatic serialization: the block may start while the kernel before it
+    // in the stream (kv_pool_write, in a step) finishes, and waits for that kernel before it
+    // reads anything (in a step, the offsets, the lengths and the table are all its output).
+    pdl_wait();
     // The request's slot-table row is loaded first, up to the table's stride (a launch
     // parameter): its loads are in flight together with the request's offsets instead of
     // waiting for them (one dependent round trip fewer before the first K/V stage).
@@ -436,13 +447,24 @@ int launch_extend_small(const SmallExtendArgs& a, cudaStream_t stream) {
     });
     if (rc != RX_OK) return rc;
     const int pair_store = ((uintptr_t)a.out & 3) == 0 ? 1 : 0;   // bf16 pairs in one store
-    if (a.head_dim == 128)
-        extend_small_kernel<128><<<grid, DEC_THREADS, smem, stream>>>(p, a.qo_indptr, a.prefix_lens, a.max_qo_len,
-                                                                      (__nv_bfloat16*)a.out, a.lse, pair_store);
-    else
-        extend_small_kernel<64><<<grid, DEC_THREADS, smem, stream>>>(p, a.qo_indptr, a.prefix_lens, a.max_qo_len,
-                                                                     (__nv_bfloat16*)a.out, a.lse, pair_store);
-    const cudaError_t e = cudaGetLastError();
+    // programmatic serialization: the kernel may start while the kernel before it in the stream
+    // (kv_pool_write, in a step) finishes, and waits for it before reading the table or pools
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(DEC_THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr_pdl[1];
+    attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr_pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = a.head_dim == 128
+                        ? cudaLaunchKernelEx(&cfg, extend_small_kernel<128>, p, a.qo_indptr, a.prefix_lens,
+                                             (int32_t)a.max_qo_len, (__nv_bfloat16*)a.out, a.lse, pair_store)
+                        : cudaLaunchKernelEx(&cfg, extend_small_kernel<64>, p, a.qo_indptr, a.prefix_lens,
+                                             (int32_t)a.max_qo_len, (__nv_bfloat16*)a.out, a.lse, pair_store);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("prefix_extend_attention: small-extend launch failed: %s", cudaGetErrorString(e));
         return RX_ECUDA;

@@ -122,6 +122,10 @@ __global__ void __launch_bounds__(KPW_THREADS) kv_pool_write_kernel(
     int32_t* __restrict__ r2t, int64_t stride, int64_t num_slots, int32_t row_vecs, int64_t t_begin, int64_t t_end,
     int32_t* status, const uint4* __restrict__ stage_src, uint4* __restrict__ stage_dst, int64_t stage_vecs,
     int32_t stage_blocks, unsigned* done_ctr, uint32_t* done_flag, uint32_t done_seq) {
+    // a kernel launched after this one with programmatic serialization (the small-extend
+    // attention) may start its own set-up now; it waits for this grid before it reads the
+    // table or the pools
+    pdl_launch_dependents();
     const int32_t bid = (int32_t)blockIdx.x - stage_blocks;
     const int64_t table_blocks = (int64_t)batch * tiles;
     if ((int32_t)blockIdx.x < stage_blocks) {          // the staging buffer to its device copy

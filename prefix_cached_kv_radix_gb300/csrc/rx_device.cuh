@@ -310,6 +310,14 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while the kernel before
+// it in the stream still runs, once that kernel's blocks have all called pdl_launch_dependents
+// (or exited); pdl_wait then blocks until that kernel has completed and its writes are visible.
+// Without such a launch both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 2^x on the special-function unit (ex2.approx.ftz.f32); arguments here are <= 8, and
 // very negative ones (masked scores) flush to 0.
 __device__ __forceinline__ float fast_exp2(float x) {

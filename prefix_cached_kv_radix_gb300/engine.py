@@ -300,8 +300,6 @@ class PrefixCacheEngine:
         if flags != self._io_flags:
             io.overlap, io.decode = flags
             self._io_flags = flags
-        io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
-        io.d_out, io.d_lse = out.data_ptr(), (lse.data_ptr() if lse is not None else None)
         tokens = _contig(tokens, np.int32)
         tok_indptr = _contig(tok_indptr, np.int64)
         n_new = _contig(n_new, np.int32)
@@ -339,8 +337,7 @@ class PrefixCacheEngine:
         if last is None or len(last) < max(b, 1):
             last = self._last[i] = np.empty(max(b, 1) * 2, np.int64)
             a.out_last = api._addr(last)
-        # the step's inputs; the rest of the struct only when it changes
-        a.batch, a.tokens, a.tok_indptr, a.n_new = b, api._addr(tokens), api._addr(tok_indptr), api._addr(n_new)
+        # the struct's per-buffer fields, only when they change
         per = (_GROUP_MODE[groups], min_shared, evict_tokens, st.cuda_stream, self._pin_addr[i], hbuf.nbytes,
                self._dev_stage[i])
         if per != self._args_set[i]:
@@ -349,7 +346,18 @@ class PrefixCacheEngine:
             self._args_set[i] = per
         # the device staging copy that goes with this buffer
         io.d_stage, io.d_stage_bytes = self._dev_stage_addr(i), self._dev_stage_cap[i]
-        rc = api.rx_step_run(self._args_addr[i])
+        # the step's inputs, and the call
+        ext = api.step_ext()
+        if ext is not None:
+            rc = ext.run(self._args_addr[i], ctypes.addressof(io), b, tokens, tok_indptr, n_new, q, k_new, v_new, out,
+                         lse)
+            if rc != api.RX_OK and rc != api.RX_ENOMEM:
+                api._check("rx_step_run", rc)
+        else:
+            io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
+            io.d_out, io.d_lse = out.data_ptr(), (lse.data_ptr() if lse is not None else None)
+            a.batch, a.tokens, a.tok_indptr, a.n_new = b, api._addr(tokens), api._addr(tok_indptr), api._addr(n_new)
+            rc = api.rx_step_run(self._args_addr[i])
         if rc == api.RX_ENOMEM:
             # planned and pinned, not launched: grow the slot table or the workspace, then launch
             r2t_need = max(L.batch, 1) * L.stride

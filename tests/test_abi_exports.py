@@ -58,3 +58,33 @@ def test_array_addresses_for_the_binding():
     assert api._addr(e) == e.ctypes.data
     v = a[2:]                                  # a contiguous view starts where it says
     assert api._addr(v) == a.ctypes.data + 8
+
+
+def test_step_extension_marshals_like_ctypes():
+    """The _rxstep extension writes the step's inputs into the same structs the ctypes path
+    writes and returns rx_step_run's code (here RX_EINVAL: no tree, so nothing runs)."""
+    import numpy as np
+    import pytest
+    ext = api.step_ext()
+    if ext is None:
+        pytest.skip("the Python headers are not installed: the step extension was not built")
+
+    class Dev:   # stands in for a device tensor: only data_ptr() is read
+        def __init__(self, p):
+            self.p = p
+
+        def data_ptr(self):
+            return self.p
+
+    a, io = api.rx_step_args(), api.rx_step_io()
+    toks = np.arange(10, dtype=np.int32)
+    ind = np.array([0, 4, 10], np.int64)
+    nn = np.array([1, 2], np.int32)
+    rc = ext.run(ctypes.addressof(a), ctypes.addressof(io), 2, toks, ind, nn, Dev(0x1000), Dev(0x2000), Dev(0x3000),
+                 Dev(0x4000), None)
+    assert rc == api.RX_EINVAL
+    assert "rx_step_run" in api.load().rx_last_error().decode()
+    assert (a.batch, a.tokens, a.tok_indptr, a.n_new) == (2, toks.ctypes.data, ind.ctypes.data, nn.ctypes.data)
+    assert (io.d_q, io.d_k_new, io.d_v_new, io.d_out, io.d_lse) == (0x1000, 0x2000, 0x3000, 0x4000, None)
+    with pytest.raises(TypeError):
+        ext.run(ctypes.addressof(a), ctypes.addressof(io), 2, toks)

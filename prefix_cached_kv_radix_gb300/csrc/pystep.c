@@ -6,11 +6,14 @@
  * arithmetic happens here.
  *
  *   bind(rx_step_run_address)
- *   run(args_addr, io_addr, batch, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse) -> rc
+ *   run(args_addr, io_addr, batch, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse, d_stage,
+ *       d_stage_bytes) -> rc
  *
  * tokens / tok_indptr / n_new: C-contiguous host arrays (int32 / int64 / int32; checked by the
  * caller), read through the buffer protocol; q, k_new, v_new, out, lse (or None): objects with
- * a data_ptr() method (device tensors).  The GIL is released during the native call. */
+ * a data_ptr() method (device tensors); d_stage, d_stage_bytes: the device staging copy that goes
+ * with this step's staging buffer (int address and size).  The GIL is released during the
+ * native call. */
 #define PY_SSIZE_T_CLEAN
 #include <Python.h>
 
@@ -54,8 +57,8 @@ static PyObject* py_bind(PyObject* self, PyObject* arg) {
 
 static PyObject* py_run(PyObject* self, PyObject* const* a, Py_ssize_t n) {
     (void)self;
-    if (n != 11) {
-        PyErr_SetString(PyExc_TypeError, "run: 11 arguments expected");
+    if (n != 13) {
+        PyErr_SetString(PyExc_TypeError, "run: 13 arguments expected");
         return NULL;
     }
     if (!g_run) {
@@ -65,6 +68,8 @@ static PyObject* py_run(PyObject* self, PyObject* const* a, Py_ssize_t n) {
     rx_step_args* args = (rx_step_args*)PyLong_AsVoidPtr(a[0]);
     rx_step_io* io = (rx_step_io*)PyLong_AsVoidPtr(a[1]);
     const long batch = PyLong_AsLong(a[2]);
+    void* d_stage = PyLong_AsVoidPtr(a[11]);
+    const size_t d_stage_bytes = PyLong_AsSize_t(a[12]);
     if (PyErr_Occurred()) return NULL;
     if (!args || !io || batch < 0 || batch > INT32_MAX) {
         PyErr_SetString(PyExc_ValueError, "run: bad struct address or batch");
@@ -80,6 +85,8 @@ static PyObject* py_run(PyObject* self, PyObject* const* a, Py_ssize_t n) {
     io->d_v_new = v;
     io->d_out = out;
     io->d_lse = (float*)lse;
+    io->d_stage = d_stage;
+    io->d_stage_bytes = d_stage_bytes;
     args->batch = (int32_t)batch;
     args->tokens = (const int32_t*)tokens;
     args->tok_indptr = (const int64_t*)tok_indptr;
@@ -94,7 +101,7 @@ static PyObject* py_run(PyObject* self, PyObject* const* a, Py_ssize_t n) {
 static PyMethodDef methods[] = {
     {"bind", (PyCFunction)py_bind, METH_O, "bind(address of rx_step_run)"},
     {"run", (PyCFunction)(void (*)(void))py_run, METH_FASTCALL,
-     "run(args_addr, io_addr, batch, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse) -> rc"},
+     "run(args_addr, io_addr, batch, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse, d_stage, d_stage_bytes) -> rc"},
     {NULL, NULL, 0, NULL},
 };
 

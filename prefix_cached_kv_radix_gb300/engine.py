@@ -31,9 +31,12 @@ def _dev_from_host(a, dtype_bits, device):
     return t.to(device, non_blocking=False)
 
 
+_DTYPES = {np.int32: np.dtype(np.int32), np.int64: np.dtype(np.int64)}
+
+
 def _contig(a, dt):
     """a as a C-contiguous array of dtype dt (the array itself when it already is one)."""
-    if type(a) is np.ndarray and a.dtype == dt and a.flags.c_contiguous:
+    if type(a) is np.ndarray and a.dtype is _DTYPES.get(dt) and a.flags.c_contiguous:
         return a
     return np.ascontiguousarray(a, dt)
 
@@ -162,6 +165,10 @@ class PrefixCacheEngine:
         self._args_set = [None, None]  # the per-buffer fields last written into each
         self._layout = [None, None]
         self._dev_stage_cap = [0, 0]
+        self._dev_stage_ptr = [0, 0]
+        self._io_addr = 0
+        self._stream_handle = 0
+        self._ext = None
         self._bound_bufs = (None, None)  # the slot table and workspace objects bound into the io
         self._io_flags = None            # (overlap, decode) last written into the io
         self._io_host = False            # the io holds host-buffer addresses
@@ -283,10 +290,12 @@ class PrefixCacheEngine:
         When a device buffer turns out too small for the plan, it is grown and the planned step
         launched with rx_step_launch.  Returns the plan (its index arrays stay readable until the
         plan after next)."""
-        st = self._stream if stream is None else stream
         io = self._io
         if io is None:
             io = self._io = api.rx_step_io()
+            self._io_addr = ctypes.addressof(io)
+            self._stream_handle = self._stream.cuda_stream
+            self._ext = api.step_ext()
         if host is not None:
             io.h_q, io.h_k_new, io.h_v_new, io.h_out = (x.data_ptr() for x in host[:4])
             io.h_lse = host[4].data_ptr() if len(host) > 4 and host[4] is not None else None
@@ -319,7 +328,7 @@ class PrefixCacheEngine:
         # the plan's arrays never take more than the staging buffer's bound
         if self._dev_stage_cap[i] < need:
             ds = self._dev_stage[i] = torch.empty(max(need, 4096) * 2, dtype=torch.uint8, device=self.device)
-            self._dev_stage_cap[i] = ds.numel()
+            self._dev_stage_cap[i], self._dev_stage_ptr[i] = ds.numel(), ds.data_ptr()
         if self._r2t_flat is None:
             self._r2t_flat = torch.empty(max(b, 1) * 1024, dtype=torch.int32, device=self.device)
         # rebind when a buffer was replaced (here, or the workspace by a per-operation call)
@@ -338,22 +347,21 @@ class PrefixCacheEngine:
             last = self._last[i] = np.empty(max(b, 1) * 2, np.int64)
             a.out_last = api._addr(last)
         # the struct's per-buffer fields, only when they change
-        per = (_GROUP_MODE[groups], min_shared, evict_tokens, st.cuda_stream, self._pin_addr[i], hbuf.nbytes,
-               self._dev_stage[i])
+        per = (_GROUP_MODE[groups], min_shared, evict_tokens,
+               self._stream_handle if stream is None else api._stream(stream), self._pin_addr[i], hbuf.nbytes)
         if per != self._args_set[i]:
             a.group_mode, a.heads_per_kv, a.min_shared, a.evict_tokens = per[0], self.hq // self.hkv, per[1], per[2]
             a.stream, a.h_stage, a.stage_cap = per[3], per[4], per[5]
             self._args_set[i] = per
-        # the device staging copy that goes with this buffer
-        io.d_stage, io.d_stage_bytes = self._dev_stage_addr(i), self._dev_stage_cap[i]
-        # the step's inputs, and the call
-        ext = api.step_ext()
+        # the step's inputs (and the device staging copy that goes with this buffer), and the call
+        ext = self._ext
         if ext is not None:
-            rc = ext.run(self._args_addr[i], ctypes.addressof(io), b, tokens, tok_indptr, n_new, q, k_new, v_new, out,
-                         lse)
+            rc = ext.run(self._args_addr[i], self._io_addr, b, tokens, tok_indptr, n_new, q, k_new, v_new, out, lse,
+                         self._dev_stage_ptr[i], self._dev_stage_cap[i])
             if rc != api.RX_OK and rc != api.RX_ENOMEM:
                 api._check("rx_step_run", rc)
         else:
+            io.d_stage, io.d_stage_bytes = self._dev_stage_ptr[i], self._dev_stage_cap[i]
             io.d_q, io.d_k_new, io.d_v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
             io.d_out, io.d_lse = out.data_ptr(), (lse.data_ptr() if lse is not None else None)
             a.batch, a.tokens, a.tok_indptr, a.n_new = b, api._addr(tokens), api._addr(tok_indptr), api._addr(n_new)
@@ -372,11 +380,8 @@ class PrefixCacheEngine:
                 self._ws = torch.empty(ws_need, dtype=torch.uint8, device=self.device)
             self._bind_io(io)
             api.rx_step_launch(self.tree.h, self.desc, tokens, tok_indptr, last, self._pin_addr[i], L, io,
-                               evict_tokens, st.cuda_stream)
+                               evict_tokens, self._stream_handle if stream is None else api._stream(stream))
         return StepPlan(b, tokens, tok_indptr, last[:b], L, i, hbuf)
-
-    def _dev_stage_addr(self, i: int) -> int:
-        return self._dev_stage[i].data_ptr()
 
     def _bind_io(self, io) -> None:
         """The step io's long-lived buffer addresses (pools, slot table, workspace, status)."""

@@ -81,10 +81,11 @@ def test_step_extension_marshals_like_ctypes():
     ind = np.array([0, 4, 10], np.int64)
     nn = np.array([1, 2], np.int32)
     rc = ext.run(ctypes.addressof(a), ctypes.addressof(io), 2, toks, ind, nn, Dev(0x1000), Dev(0x2000), Dev(0x3000),
-                 Dev(0x4000), None)
+                 Dev(0x4000), None, 0x5000, 4096)
     assert rc == api.RX_EINVAL
     assert "rx_step_run" in api.load().rx_last_error().decode()
     assert (a.batch, a.tokens, a.tok_indptr, a.n_new) == (2, toks.ctypes.data, ind.ctypes.data, nn.ctypes.data)
     assert (io.d_q, io.d_k_new, io.d_v_new, io.d_out, io.d_lse) == (0x1000, 0x2000, 0x3000, 0x4000, None)
+    assert (io.d_stage, io.d_stage_bytes) == (0x5000, 4096)
     with pytest.raises(TypeError):
         ext.run(ctypes.addressof(a), ctypes.addressof(io), 2, toks)

@@ -138,7 +138,10 @@ def pool_write_bytes(w, stride: int) -> int:
 # the benchmark's own thread: an NVML query made by the benchmark's thread next to a short step
 # (before it, after it, or during the L2 flush before it) was measured to add 7-15 us to a step.
 _SAMPLER = r"""
-import ctypes, sys, time
+import ctypes, os, sys, time
+cores = os.sched_getaffinity(0)
+if len(cores) > 1 and int(sys.argv[4]) in cores:   # off the core a step timed alone runs on
+    os.sched_setaffinity(0, cores - {int(sys.argv[4])})
 lib = ctypes.CDLL("libnvidia-ml.so.1")
 assert lib.nvmlInit_v2() == 0
 h = ctypes.c_void_p()
@@ -169,9 +172,10 @@ class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index: int, period_s: float = 0.0002):
+    def __init__(self, device_index: int, period_s: float = 0.0002, avoid_core: int = -1):
         self.period = period_s
         self.dev = device_index
+        self.avoid = avoid_core
         self.samples = []             # (sm_mhz, max_mhz, reasons bitmask)
         self.proc = None
         self.thread = None
@@ -195,7 +199,8 @@ class ClockSampler:
             return
         lines = []
         try:
-            self.proc = subprocess.Popen([sys.executable, "-c", _SAMPLER, self.bus, str(self.dev), str(self.period)],
+            self.proc = subprocess.Popen([sys.executable, "-c", _SAMPLER, self.bus, str(self.dev), str(self.period),
+                                          str(self.avoid)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             first = self.proc.stdout.readline().strip()
             if first != "ready":
@@ -454,9 +459,23 @@ def measure(name, args, rank, world, local_rank, cpu: bool):
     # do: double-buffered staging, host finish right after the launch).  A step that fits in
     # L2 is timed alone after an L2 flush and a synchronize.
     back_to_back = work["bytes"] >= 2 * L2_BYTES
-    clocks = ClockSampler(local_rank)
+    cores = sorted(os.sched_getaffinity(0))
+    pin_core = cores[-1 - local_rank % len(cores)]   # a core per rank, from the top
+    clocks = ClockSampler(local_rank, avoid_core=pin_core)
 
     def timed(e2e, isolated=not back_to_back, first=None):
+        # a step timed alone is host-bound: its thread stays on one core for the region (the
+        # clock sampler keeps off that core), instead of resuming on another one, cold, after
+        # each synchronize
+        allowed = os.sched_getaffinity(0)
+        if isolated and len(allowed) > 1:
+            os.sched_setaffinity(0, {pin_core})
+        try:
+            return timed_region(e2e, isolated, first)
+        finally:
+            os.sched_setaffinity(0, allowed)
+
+    def timed_region(e2e, isolated, first):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()

@@ -59,12 +59,97 @@ void set_error(const char* fmt, ...) {
 
 void clear_error() { g_last_error.clear(); }
 
+struct Node;
+
+// Map from an integer key to a node (a null node marks an empty cell): open addressing with
+// linear probing over a power-of-two table kept at most 3/4 full, a multiplicative hash, and
+// deletion by backward shift (no tombstones).  Clearing keeps the table, so a reused node's
+// child map allocates nothing.  The tree's child links (by first token) and node handles
+// (by id) live in these: a lookup is one multiply and, mostly, one cache line.
+template <class K>
+class NodeMap {
+  public:
+    Node* find(K k) const {
+        if (n_ == 0) return nullptr;
+        for (size_t i = home(k);; i = (i + 1) & mask_) {
+            const Cell& c = cells_[i];
+            if (!c.val) return nullptr;
+            if (c.key == k) return c.val;
+        }
+    }
+    void set(K k, Node* v) {   // insert, or replace the node of k
+        if ((n_ + 1) * 4 > cells_.size() * 3) grow();
+        size_t i = home(k);
+        for (; cells_[i].val; i = (i + 1) & mask_)
+            if (cells_[i].key == k) {
+                cells_[i].val = v;
+                return;
+            }
+        cells_[i] = Cell{k, v};
+        ++n_;
+    }
+    bool erase(K k) {
+        if (n_ == 0) return false;
+        size_t i = home(k);
+        for (; cells_[i].val; i = (i + 1) & mask_)
+            if (cells_[i].key == k) break;
+        if (!cells_[i].val) return false;
+        // backward shift: an entry after the hole moves into it unless its home lies in the
+        // cyclic range (hole, entry]
+        for (size_t j = (i + 1) & mask_; cells_[j].val; j = (j + 1) & mask_) {
+            const size_t h = home(cells_[j].key);
+            const bool stays = i <= j ? (i < h && h <= j) : (i < h || h <= j);
+            if (!stays) {
+                cells_[i] = cells_[j];
+                i = j;
+            }
+        }
+        cells_[i].val = nullptr;
+        --n_;
+        return true;
+    }
+    size_t size() const { return n_; }
+    bool empty() const { return n_ == 0; }
+    void clear() {
+        if (n_ == 0) return;
+        for (Cell& c : cells_) c.val = nullptr;
+        n_ = 0;
+    }
+    template <class F>
+    void for_each(F&& f) const {
+        for (const Cell& c : cells_)
+            if (c.val) f(c.key, c.val);
+    }
+
+  private:
+    struct Cell {
+        K key;
+        Node* val;
+    };
+    size_t home(K k) const { return (size_t)(((uint64_t)k * 0x9E3779B97F4A7C15ull) >> shift_); }
+    void grow() {
+        std::vector<Cell> old;
+        old.swap(cells_);
+        const size_t cap = old.empty() ? 4 : old.size() * 2;
+        cells_.assign(cap, Cell{K(), nullptr});
+        mask_ = cap - 1;
+        shift_ = 64;
+        for (size_t c = cap; c > 1; c >>= 1) --shift_;
+        n_ = 0;
+        for (const Cell& c : old)
+            if (c.val) set(c.key, c.val);
+    }
+    std::vector<Cell> cells_;
+    size_t mask_ = 0, n_ = 0;
+    unsigned shift_ = 64;
+};
+
 struct Node {
     int64_t id = 0;
     Node* parent = nullptr;
     std::vector<int32_t> key;     // edge tokens
     std::vector<int32_t> slots;   // pool slot of each edge token
-    std::unordered_map<int32_t, Node*> children;  // by first token
+    NodeMap<int32_t> children;    // by first token
     uint64_t stamp = 0;
     int64_t ref = 0;
     int64_t depth = 0;            // tokens from the root to the END of this node
@@ -182,7 +267,7 @@ struct rx_radix {
     uint64_t clock = 0;
     int64_t next_id = 1;
     int64_t page = 1;                  // reuse granularity: matches count whole pages only
-    std::unordered_map<int64_t, rx::Node*> by_id;
+    rx::NodeMap<int64_t> by_id;        // node handles
     rx_stats st{};
 
     // Evicted nodes, kept for reuse: a node's edge vectors and child map keep their capacity,
@@ -194,47 +279,10 @@ struct rx_radix {
     using EvictItem = std::tuple<uint64_t, int64_t, rx::Node*>;
     std::vector<rx::Node*> ev_stack;
     std::vector<EvictItem> ev_heap;
-    // Hash-map nodes of evicted entries (child links and handles), reused through node handles
-    // for the entries of later nodes, so that inserting and evicting leaves allocates nothing.
-    using ChildMap = decltype(rx::Node::children);
-    using IdMap = std::unordered_map<int64_t, rx::Node*>;
-    std::vector<ChildMap::node_type> spare_child;
-    std::vector<IdMap::node_type> spare_id;
-
-    void add_child(rx::Node* parent, int32_t tok, rx::Node* c) {
-        if (spare_child.empty()) {
-            parent->children[tok] = c;
-            return;
-        }
-        ChildMap::node_type nh = std::move(spare_child.back());
-        spare_child.pop_back();
-        nh.key() = tok;
-        nh.mapped() = c;
-        auto r = parent->children.insert(std::move(nh));
-        if (!r.inserted) {          // the token already had a child: replace it, keep the handle
-            r.position->second = c;
-            spare_child.push_back(std::move(r.node));
-        }
-    }
-    void drop_child(rx::Node* parent, int32_t tok) {
-        ChildMap::node_type nh = parent->children.extract(tok);
-        if (nh && spare_child.size() < kSpareNodes) spare_child.push_back(std::move(nh));
-    }
-    void add_id(int64_t id, rx::Node* n) {
-        if (spare_id.empty()) {
-            by_id[id] = n;
-            return;
-        }
-        IdMap::node_type nh = std::move(spare_id.back());
-        spare_id.pop_back();
-        nh.key() = id;
-        nh.mapped() = n;
-        by_id.insert(std::move(nh));    // ids are never reused: always a new key
-    }
-    void drop_id(int64_t id) {
-        IdMap::node_type nh = by_id.extract(id);
-        if (nh && spare_id.size() < kSpareNodes) spare_id.push_back(std::move(nh));
-    }
+    void add_child(rx::Node* parent, int32_t tok, rx::Node* c) { parent->children.set(tok, c); }
+    void drop_child(rx::Node* parent, int32_t tok) { parent->children.erase(tok); }
+    void add_id(int64_t id, rx::Node* n) { by_id.set(id, n); }
+    void drop_id(int64_t id) { by_id.erase(id); }
 
     ~rx_radix() {
         destroy_children(&root);
@@ -243,12 +291,12 @@ struct rx_radix {
 
     void destroy_children(rx::Node* x) {
         std::vector<rx::Node*> stack;
-        for (auto& kv : x->children) stack.push_back(kv.second);
+        x->children.for_each([&](int32_t, rx::Node* c) { stack.push_back(c); });
         x->children.clear();
         while (!stack.empty()) {
             rx::Node* n = stack.back();
             stack.pop_back();
-            for (auto& kv : n->children) stack.push_back(kv.second);
+            n->children.for_each([&](int32_t, rx::Node* c) { stack.push_back(c); });
             delete n;
         }
     }
@@ -299,7 +347,7 @@ struct rx_radix {
         top->depth = c->depth - (int64_t)(c->key.size() - k);
         c->key.erase(c->key.begin(), c->key.begin() + k);
         c->slots.erase(c->slots.begin(), c->slots.begin() + k);
-        c->parent->children[top->key[0]] = top;
+        c->parent->children.set(top->key[0], top);
         add_child(top, c->key[0], c);
         c->parent = top;
         return top;
@@ -316,9 +364,8 @@ struct rx_radix {
         const rx::Node* x = &root;
         int64_t pos = 0;
         while (pos < n) {
-            auto it = x->children.find(tokens[pos]);
-            if (it == x->children.end()) break;
-            const rx::Node* c = it->second;
+            const rx::Node* c = x->children.find(tokens[pos]);
+            if (!c) break;
             const int64_t len = (int64_t)c->key.size();
             const int64_t k = rx::common_prefix(c->key.data(), tokens + pos, 1, std::min<int64_t>(len, n - pos));
             pos += k;
@@ -346,9 +393,8 @@ struct rx_radix {
         rx::Node* x = &root;
         int64_t pos = 0;
         while (pos < m) {
-            auto it = x->children.find(tokens[pos]);
-            if (it == x->children.end()) return nullptr;
-            rx::Node* c = it->second;
+            rx::Node* c = x->children.find(tokens[pos]);
+            if (!c) return nullptr;
             const size_t len = c->key.size();
             const int64_t k = std::min<int64_t>((int64_t)len, m - pos);
             if ((size_t)k < len) c = split(c, (size_t)k);
@@ -371,9 +417,8 @@ struct rx_radix {
     int64_t walk_from(rx::Node* x, int64_t pos, const int32_t* tokens, int64_t n, int32_t* out_slots,
                       rx::Node** last) {
         while (pos < n) {
-            auto it = x->children.find(tokens[pos]);
-            if (it == x->children.end()) break;
-            rx::Node* c = it->second;
+            rx::Node* c = x->children.find(tokens[pos]);
+            if (!c) break;
             const size_t len = c->key.size();
             const int64_t lim = std::min<int64_t>((int64_t)len, n - pos);
             const int64_t k = rx::common_prefix(c->key.data(), tokens + pos, 1, lim);
@@ -424,7 +469,7 @@ int radix_create(int64_t num_slots, uint64_t slot_perm_seed, rx_radix** out) {
         return RX_ENOMEM;
     }
     t->root.id = 0;
-    t->by_id[0] = &t->root;
+    t->by_id.set(0, &t->root);
     t->st.num_slots = num_slots;
     *out = t;
     return RX_OK;
@@ -483,23 +528,23 @@ int match_prefix_len_batch(const rx_radix* t, int32_t batch, const int32_t* toke
 int radix_lock(rx_radix* t, rx_node node) {
     RX_TRACE("radix_lock");
     RX_REQUIRE(t, "radix_lock: tree is NULL");
-    auto it = t->by_id.find(node);
-    RX_REQUIRE(it != t->by_id.end(), "radix_lock: unknown node %lld", (long long)node);
-    for (rx::Node* x = it->second; x != &t->root; x = x->parent) x->ref += 1;
+    rx::Node* const at = t->by_id.find(node);
+    RX_REQUIRE(at, "radix_lock: unknown node %lld", (long long)node);
+    for (rx::Node* x = at; x != &t->root; x = x->parent) x->ref += 1;
     return RX_OK;
 }
 
 int radix_unlock(rx_radix* t, rx_node node) {
     RX_TRACE("radix_unlock");
     RX_REQUIRE(t, "radix_unlock: tree is NULL");
-    auto it = t->by_id.find(node);
-    RX_REQUIRE(it != t->by_id.end(), "radix_unlock: unknown node %lld", (long long)node);
-    for (rx::Node* x = it->second; x != &t->root; x = x->parent)
+    rx::Node* const at = t->by_id.find(node);
+    RX_REQUIRE(at, "radix_unlock: unknown node %lld", (long long)node);
+    for (rx::Node* x = at; x != &t->root; x = x->parent)
         if (x->ref <= 0) {
             set_error("radix_unlock: node %lld is not locked", (long long)node);
             return RX_ELOCKED;
         }
-    for (rx::Node* x = it->second; x != &t->root; x = x->parent) x->ref -= 1;
+    for (rx::Node* x = at; x != &t->root; x = x->parent) x->ref -= 1;
     return RX_OK;
 }
 
@@ -507,7 +552,7 @@ int radix_lock_batch(rx_radix* t, const rx_node* nodes, int32_t n) {
     RX_TRACE("radix_lock_batch");
     RX_REQUIRE(t && n >= 0 && (n == 0 || nodes), "radix_lock_batch: bad arguments");
     for (int32_t i = 0; i < n; ++i)
-        RX_REQUIRE(t->by_id.count(nodes[i]), "radix_lock_batch: unknown node %lld", (long long)nodes[i]);
+        RX_REQUIRE(t->by_id.find(nodes[i]), "radix_lock_batch: unknown node %lld", (long long)nodes[i]);
     for (int32_t i = 0; i < n; ++i) radix_lock(t, nodes[i]);
     return RX_OK;
 }
@@ -572,9 +617,8 @@ int insert(rx_radix* t, const int32_t* tokens, const int32_t* slots, int64_t n, 
         rx::Node* x = &t->root;
         int64_t pos = 0;   // non-mutating walk to find dup_len
         while (pos < n) {
-            auto it = x->children.find(tokens[pos]);
-            if (it == x->children.end()) break;
-            rx::Node* c = it->second;
+            rx::Node* c = x->children.find(tokens[pos]);
+            if (!c) break;
             const int64_t lim = std::min<int64_t>((int64_t)c->key.size(), n - pos);
             int64_t k = 1;
             while (k < lim && c->key[k] == tokens[pos + k]) ++k;
@@ -625,7 +669,7 @@ int evict(rx_radix* t, int64_t num_tokens, int32_t* out_freed, int64_t cap, int6
         rx::Node* x = stack.back();
         stack.pop_back();
         if (x != &t->root && x->children.empty() && x->ref == 0) heap.emplace_back(x->stamp, x->id, x);
-        for (auto& kv : x->children) stack.push_back(kv.second);
+        x->children.for_each([&](int32_t, rx::Node* c) { stack.push_back(c); });
     }
     std::make_heap(heap.begin(), heap.end(), later);
     int64_t freed = 0;
@@ -693,9 +737,8 @@ int insert_batch_at(rx_radix* t, int32_t batch, const rx_node* nodes, const int3
     RX_REQUIRE(t && batch >= 0 && (batch == 0 || (nodes && tokens && tok_indptr && new_indptr && out_dup_len && out_last)),
                "insert_batch_at: bad arguments");
     for (int32_t b = 0; b < batch; ++b) {
-        auto it = t->by_id.find(nodes[b]);
-        RX_REQUIRE(it != t->by_id.end(), "insert_batch_at: unknown node %lld", (long long)nodes[b]);
-        rx::Node* x = it->second;
+        rx::Node* x = t->by_id.find(nodes[b]);
+        RX_REQUIRE(x, "insert_batch_at: unknown node %lld", (long long)nodes[b]);
         const int64_t n = tok_indptr[b + 1] - tok_indptr[b];
         const int64_t d = x->depth;
         const int64_t m = new_indptr[b + 1] - new_indptr[b];
@@ -893,7 +936,7 @@ int rx_step_plan(rx_radix* t, int32_t batch, const int32_t* tokens, const int64_
     }
     // pin the matched prefixes for the step (last, so that a failure above leaves none pinned)
     for (int32_t b = 0; b < batch; ++b)
-        for (rx::Node* x = t->by_id[out_last[b]]; x != &t->root; x = x->parent) x->ref += 1;
+        for (rx::Node* x = t->by_id.find(out_last[b]); x != &t->root; x = x->parent) x->ref += 1;
     *out = L;
     return RX_OK;
 }
@@ -946,7 +989,9 @@ int radix_check(const rx_radix* t) {
         const rx::Node* x = stack.back();
         stack.pop_back();
         int64_t child_ref = 0;
-        for (auto& kv : x->children) {
+        std::vector<std::pair<int32_t, const rx::Node*>> kids;
+        x->children.for_each([&](int32_t tok, const rx::Node* c) { kids.emplace_back(tok, c); });
+        for (const auto& kv : kids) {
             const rx::Node* c = kv.second;
             RX_REQUIRE(c->parent == x, "radix_check: node %lld has a wrong parent", (long long)c->id);
             RX_REQUIRE(!c->key.empty() && c->key.size() == c->slots.size(),
@@ -958,9 +1003,7 @@ int radix_check(const rx_radix* t) {
             RX_REQUIRE(x == &t->root || c->stamp <= x->stamp,
                        "radix_check: node %lld is more recent than its parent", (long long)c->id);
             RX_REQUIRE(c->ref >= 0, "radix_check: node %lld has a negative lock count", (long long)c->id);
-            auto it = t->by_id.find(c->id);
-            RX_REQUIRE(it != t->by_id.end() && it->second == c, "radix_check: handle of node %lld",
-                       (long long)c->id);
+            RX_REQUIRE(t->by_id.find(c->id) == c, "radix_check: handle of node %lld", (long long)c->id);
             child_ref += c->ref;
             stack.push_back(c);
         }
@@ -1000,9 +1043,9 @@ int radix_shared_groups(const rx_radix* t, const rx_node* last_nodes, int32_t ba
     // Root paths of every request's end node (root excluded), shallow to deep.
     std::vector<std::vector<const rx::Node*>> paths((size_t)batch);
     for (int32_t b = 0; b < batch; ++b) {
-        auto it = t->by_id.find(last_nodes[b]);
-        RX_REQUIRE(it != t->by_id.end(), "radix_shared_groups: unknown node %lld", (long long)last_nodes[b]);
-        for (const rx::Node* x = it->second; x != &t->root; x = x->parent) paths[(size_t)b].push_back(x);
+        const rx::Node* const at = t->by_id.find(last_nodes[b]);
+        RX_REQUIRE(at, "radix_shared_groups: unknown node %lld", (long long)last_nodes[b]);
+        for (const rx::Node* x = at; x != &t->root; x = x->parent) paths[(size_t)b].push_back(x);
         std::reverse(paths[(size_t)b].begin(), paths[(size_t)b].end());
     }
     std::unordered_map<const rx::Node*, std::vector<int32_t>> by_top;

@@ -78,20 +78,21 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtParams p) {
     }
     const int32_t* slots = p.r2t + (int64_t)b * p.stride;
     float m = -INFINITY, l = 0.f;
-    // Keys in runs of 32: one coalesced load of the run's slots (a lane each), then four keys'
+    // Keys in runs of 32: one coalesced load of the run's slots (a lane each), then KG keys'
     // K and V rows requested together before the first is used, so that a key costs a
     // fraction of a memory round trip instead of two dependent ones.  The online softmax still
     // takes the keys one by one in order, with the same arithmetic as a key-at-a-time loop.
+    constexpr int KG = 8;
     const int64_t nkeys = pos + 1;
     for (int64_t j0 = 0; j0 < nkeys; j0 += 32) {
         const int cnt = (int)(nkeys - j0 < 32 ? nkeys - j0 : 32);
         const int32_t s_lane = lane < cnt ? slots[j0 + lane] : 0;
         if (lane < cnt && (s_lane < 0 || s_lane >= p.num_slots)) report(p.status, RX_DEV_BAD_SLOT);
-        for (int k0 = 0; k0 < cnt; k0 += 4) {
-            float kv[4][E], vv[4][E];
-            bool ok[4];
+        for (int k0 = 0; k0 < cnt; k0 += KG) {
+            float kv[KG][E], vv[KG][E];
+            bool ok[KG];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < KG; ++u) {
                 const int32_t s = __shfl_sync(0xffffffffu, s_lane, (k0 + u) & 31);   // the same in every lane
                 ok[u] = k0 + u < cnt && s >= 0 && s < p.num_slots;
                 const int64_t base = ((int64_t)(ok[u] ? s : 0) * p.hkv + g) * D;
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtParams p) {
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < KG; ++u) {
                 if (!ok[u]) continue;       // a bad slot (reported) or past the row's last key
                 float dot = 0.f;
 #pragma unroll

@@ -624,6 +624,51 @@ def test_device_steps_overlap_back_to_back():
         assert np.array_equal(results[0][j], results[1][j]), f"step {j}"
 
 
+@pytest.mark.gpu
+def test_small_extend_steps_back_to_back():
+    """Small-extend steps (a few rows per request and kv head: the small-extend kernel, launched
+    behind kv_pool_write with programmatic serialization, the index arrays read by kv_pool_write
+    through the staging buffer's mapping and the buffer's reuse signalled in host memory) run
+    back to back with no synchronize: every step's output equals, bit for bit, the same step run
+    one at a time, and the first equals the oracle."""
+    from prefix_cached_kv_radix_gb300.engine import _dev_from_host
+    spec = W.spec_shared_prompt("small-b2b", "bf16", 12, 12, 64, 1 << 14, W.GPT2_VOCAB, 41, 200,
+                                [7, 8, 5, 8, 1, 6, 8, 3, 7, 2, 8, 4])
+    w = W.generate(spec)
+    rng = np.random.default_rng(9)
+    q, kn, vn = w.stacked_new()
+    steps = []
+    for j in range(6):
+        prompts = [np.concatenate([w.request_prefix_tokens(b),
+                                   rng.integers(1, spec.vocab, size=spec.req_new[b])]).astype(np.int32)
+                   for b in range(w.batch)]
+        ind = np.concatenate([[0], np.cumsum([len(x) for x in prompts])]).astype(np.int64)
+        steps.append((np.concatenate(prompts).astype(np.int32), ind, 1.0 + 0.25 * j))
+    T = int(sum(spec.req_new))
+    results = []
+    for serial in (True, False):
+        eng = _engine_for(w)
+        base = [_dev_from_host(x, spec.dtype, eng.device) for x in (q, kn, vn)]
+        rows = [[x * sc for x in base] for _, _, sc in steps]
+        outs = [torch.empty_like(base[0]) for _ in steps]
+        for j, (toks, ind, _) in enumerate(steps):
+            eng.step(toks, ind, np.asarray(spec.req_new, np.int32), *rows[j], outs[j], groups="auto",
+                     evict_tokens=T, overlap=True)
+            if serial:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        assert eng.device_status() == 0
+        eng.tree.check()
+        results.append([to_host_f32(o) for o in outs])
+    for j in range(len(steps)):
+        assert np.array_equal(results[0][j], results[1][j]), f"step {j}"
+    got = results[1][0]
+    for b in range(w.batch):
+        want, _ = oracle_rows(w, b)
+        lo, hi = int(sum(spec.req_new[:b])), int(sum(spec.req_new[:b + 1]))
+        compare(got[lo:hi], want, f"request {b}")
+
+
 def test_host_buffer_decode_chunks_match_oracle():
     from prefix_cached_kv_radix_gb300.engine import _dev_from_host
     spec = small_decode(seed=27)

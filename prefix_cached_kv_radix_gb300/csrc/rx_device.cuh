@@ -45,11 +45,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One wait on an mbarrier phase: the thread is suspended until the phase completes or about
+// 100 us pass (the suspend-time hint; without it the hardware's own, shorter, limit applies and
+// a waiting warp comes back to spin more often, taking issue slots from the warps doing work:
+// 3 % of the tcgen05 extend kernel's time at c3).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, 100000;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -68,7 +72,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if ((++spins & 255u) == 0) {
+        if ((++spins & 15u) == 0) {
             if (global_ns() - t0 > limit_ns || peek_status(status) == RX_DEV_TIMEOUT) {
                 *abort = 1;
                 report(status, RX_DEV_TIMEOUT);

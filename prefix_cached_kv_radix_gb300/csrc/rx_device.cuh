@@ -82,15 +82,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the result is broadcast, and the warp is
-// re-converged (so warp-collective tcgen05.ld/st/alloc can follow).
+// Warp-uniform bounded wait: every lane waits on the barrier (the warp never splits into a
+// polling lane and 31 lanes parked at a reconvergence point, which cost the tcgen05 extend
+// kernel 5 % at c3 in branch resolution), and the lanes agree on the result, so the warp leaves
+// converged (warp-collective tcgen05.ld/st/alloc can follow).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status,
                                           uint64_t limit_ns = 2000000000ull) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, limit_ns) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
+    const bool ok = mbar_wait(bar, parity, abort, status, limit_ns);
+    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

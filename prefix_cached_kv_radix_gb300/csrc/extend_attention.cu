@@ -9,16 +9,21 @@
 // "SGLang: Efficient Execution of Structured Language Model Programs", RadixAttention:
 // the prefix's KV is reused across requests rather than recomputed.
 //
-// GB300 design.  One CTA per (request, kv head, 256 packed query rows).  The query heads
-// of a kv head (GQA group) are packed with the tokens, head fastest: packed row R ->
-// token R / G, head g*G + R % G, so every K/V tile feeds G heads and the tile stays a
-// dense contraction.  Two 128-row Q tiles share each K/V tile of 128 keys.  A full Q tile
-// is one TMA box per 64 columns (q seen as [token][head][D], box 64 x G x 128/G), loaded at
-// entry; a full output tile leaves the same way (TMA store from shared memory).  Roles (512
-// threads, four warpgroups, registers split 88 / 168 / 168 / 88 with setmaxnreg):
-//   warps 0-3, 13-15  loaders: 16-byte cp.async gathers of a ragged Q tile and of K and V tiles
-//              through the slot table into separate K (3-deep) and V (2-deep) rings in the
-//              128B-swizzled layouts tcgen05 reads.  Each thread's arrival on a tile's full
+// GB300 design.  The work items are (request, kv head, 256 packed query rows): the query
+// heads of a kv head (GQA group) are packed with the tokens, head fastest: packed row R ->
+// token R / G, head g*G + R % G, so every K/V tile feeds G heads and the tile stays a dense
+// contraction.  Two 128-row Q tiles share each K/V tile of 128 keys.  The grid is persistent:
+// one CTA per SM walks the items round-robin (item c, c + gridDim.x, ...), its rings, barriers
+// and TMEM running on across items, so an item's set-up and output overlap the neighbouring
+// items' work instead of each CTA starting and draining on its own.  Roles (512 threads, four
+// warpgroups, registers split 88 / 168 / 168 / 88 with setmaxnreg):
+//   warp 0     Q loads: per item, once the previous item's last S has read a Q buffer, the
+//              full 128-row tiles by TMA (one box per 64 columns, q seen as [token][head][D],
+//              box 64 x G x 128/G, 128-byte swizzle), a ragged tile and every tile of the
+//              shared-prefix mode row by row.
+//   warps 1-3, 13-15  K/V loaders: 16-byte cp.async gathers of K and V tiles through the slot
+//              table into separate K (3-deep) and V (2-deep) rings in the 128B-swizzled layouts
+//              tcgen05 reads, on across item boundaries.  Each thread's arrival on a tile's full
 //              barrier is made by the copy hardware when its copies land
 //              (cp.async.mbarrier.arrive), so loaders wait only for free slots; slot ids are
 //              prefetched a tile ahead.
@@ -27,13 +32,16 @@
 //              64 keys as the softmax publishes them), then at once
 //              S_t(j+1) = Q_t K(j+1)^T  (M=128, N=128, K=D) into the same TMEM columns -- the
 //              tensor pipe runs one thread's MMAs in order, so P is read before it is
-//              overwritten.  Completion via tcgen05.commit.
+//              overwritten.  Completion via tcgen05.commit; after an item's last PV on a tile a
+//              commit tells the softmax warps its O is complete.
 //   warps 4-7  softmax of Q tile 0; warps 8-11 softmax of Q tile 1: tcgen05.ld of a score
 //              row per thread, causal mask, online softmax in the exp2 domain with a lazy
 //              rescale (the reference max only moves when the row max grows by more than
 //              2^8, which keeps every P <= 256), P packed to bf16 and stored over the row's
 //              scores in TMEM (tcgen05.st) in two halves, each released to the tensor core at
-//              once; fp32 pairs use the packed f32x2 forms.
+//              once; fp32 pairs use the packed f32x2 forms.  At an item's end each thread
+//              writes its normalised row straight from TMEM while the tensor core already
+//              works on the next item's scores.
 // TMEM columns: S0/P0 [0,128) S1/P1 [128,256) O0 [256,256+D) O1 after.  While one Q tile's
 // softmax runs, the tensor core works on the other's GEMMs.  Every wait is bounded; on
 // time-out the kernel records RX_DEV_TIMEOUT, drains its async copies, frees TMEM and
@@ -42,6 +50,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 #include "radix_attn.h"
 #include "rx_common.h"
@@ -53,7 +63,8 @@ namespace rx {
 constexpr int EXT_BN = 128;       // keys per K/V tile
 constexpr int EXT_THREADS = 512;  // 16 warps
 constexpr int EXT_MMA_WARP = 12;
-constexpr int EXT_LOADERS = 224;  // warps 0-3 and 13-15
+constexpr int EXT_Q_WARP = 0;      // loads every item's Q tiles (TMA, or row gathers for ragged tiles)
+constexpr int EXT_LOADERS = 192;  // K/V gathers: warps 1-3 and 13-15
 constexpr uint32_t EXT_REGS_SOFTMAX = 168, EXT_REGS_OTHER = 88;   // 2*128*88 + 2*128*168 = 512*128
 constexpr float EXT_LOG2E = 1.4426950408889634f;
 constexpr float EXT_LN2 = 0.6931471805599453f;
@@ -88,11 +99,14 @@ struct ExtendParams {
     float* part_o;
     float* part_lse;
     int32_t part_per, part_base;
-    // Extend mode: tiled tensor maps of q and out seen as [rows][hq][D] (box 64 x G x 128/G
-    // elements, 128-byte swizzle), set by the host when G divides 128 and the buffers allow
-    // it.  Full 128-row Q tiles are then loaded, and full output tiles stored, by TMA.
-    int32_t q_map_ok, o_map_ok;
-    CUtensorMap q_map, o_map;
+    // Extend mode: tiled tensor map of q seen as [rows][hq][D] (box 64 x G x 128/G elements,
+    // 128-byte swizzle), set by the host when G divides 128 and the buffer allows it.  Full
+    // 128-row Q tiles are then loaded by TMA.
+    int32_t q_map_ok;
+    CUtensorMap q_map;
+    // Persistent grid: the work items are the cells (x, kv head, request or group) of a
+    // grid_x x hkv x (batch or groups) grid, x fastest; CTA c takes items c, c + gridDim.x, ...
+    int32_t grid_x, n_items;
 };
 
 template <int D>
@@ -105,9 +119,11 @@ struct ExtLayout {
     static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + NK * KV_TILE;
     static constexpr int OFF_BAR = OFF_V + NV * KV_TILE;
-    // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[half][2], mma_done
+    // q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[half][2],
+    // q_empty[2], o_ready[2], mma_done
     static constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 1 + NK, BAR_VF = 1 + 2 * NK, BAR_VE = 1 + 2 * NK + NV,
-                         BAR_S = 1 + 2 * NK + 2 * NV, BAR_P = BAR_S + 2, BAR_DONE = BAR_P + 4, NBAR = BAR_DONE + 1;
+                         BAR_S = 1 + 2 * NK + 2 * NV, BAR_P = BAR_S + 2, BAR_QE = BAR_P + 4, BAR_OR = BAR_QE + 2,
+                         BAR_DONE = BAR_OR + 2, NBAR = BAR_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;   // room to align the base to 1024 B
@@ -117,6 +133,68 @@ struct ExtLayout {
     static constexpr int NX = (EXT_BN * CPR + EXT_LOADERS - 1) / EXT_LOADERS;   // chunks per loader thread per tile
     static_assert(ALLOC <= 232448, "shared memory budget");
 };
+
+// One work item: a CTA's worth of rows of the grid (x, y, z) the kernel was written for.
+// Extend: packed row R -> token R / G of request b (position P_b + R / G), head g*G + R % G.
+// Shared-prefix: packed row R -> member R / G of group gid, head g*G + R % G, all keys.
+struct ExtItem {
+    bool valid;
+    int g, b, n_b, P_b, rows_total, row0, kv_end, m0, x, ntiles, nkv;
+    int64_t qo0;
+    bool map_rows;
+    const int32_t* slots_row;
+};
+
+// Decodes item index `it` (x fastest, then kv head, then request or group) and checks its
+// lengths; an item with no rows, or with a length the table cannot hold (reported once per
+// request or group, by its first item's thread 0), is not valid.  Every role of the CTA
+// decodes the same items in the same order, so they agree on which are skipped.
+__device__ __forceinline__ ExtItem ext_item(const ExtendParams& p, int it) {
+    ExtItem r{};
+    const int gx = p.grid_x;
+    r.x = it % gx;
+    r.g = (it / gx) % p.hkv;
+    const int z = it / (gx * p.hkv);
+    const int G = p.group;
+    r.valid = false;
+    if (!p.shared_mode) {
+        r.b = z;
+        r.qo0 = p.qo_indptr[r.b];
+        r.n_b = (int)(p.qo_indptr[r.b + 1] - r.qo0);
+        r.P_b = p.prefix_lens[r.b];
+        r.rows_total = r.n_b * G;
+        r.row0 = r.x * 256;
+        if (r.row0 >= r.rows_total || r.n_b <= 0) return r;
+        if (r.n_b > p.max_qo_len || r.P_b < 0 || (int64_t)r.P_b + r.n_b > p.stride) {
+            if (threadIdx.x == 0 && r.x == 0 && r.g == 0) report(p.status, RX_DEV_BAD_LENGTH);
+            return r;
+        }
+        const int last_row = min(r.row0 + 256, r.rows_total) - 1;
+        r.kv_end = r.P_b + last_row / G + 1;              // keys needed by this item
+        r.slots_row = p.r2t + (int64_t)r.b * p.stride;
+    } else {
+        const int gid = z;
+        const int c = r.x % p.n_chunks;
+        r.m0 = p.grp_row_indptr[gid];
+        r.rows_total = (p.grp_row_indptr[gid + 1] - r.m0) * G;
+        r.row0 = (r.x / p.n_chunks) * 256;
+        const int len = p.grp_len[gid];
+        const int k_lo = c * p.chunk;
+        if (r.row0 >= r.rows_total || k_lo >= len) return r;
+        if (len > p.stride) {
+            if (threadIdx.x == 0 && r.x == 0 && r.g == 0) report(p.status, RX_DEV_BAD_LENGTH);
+            return r;
+        }
+        r.kv_end = min(len, k_lo + p.chunk) - k_lo;       // keys of this chunk, relative to k_lo
+        r.slots_row = p.r2t + (int64_t)p.grp_src[gid] * p.stride + k_lo;
+    }
+    r.ntiles = r.rows_total - r.row0 > 128 ? 2 : 1;
+    // full tiles of the extend mode go through the tensor map (token coordinates are 31-bit)
+    r.map_rows = !p.shared_mode && r.qo0 + r.n_b <= INT32_MAX;
+    r.nkv = (r.kv_end + EXT_BN - 1) / EXT_BN;
+    r.valid = true;
+    return r;
+}
 
 template <int D>
 __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_constant__ ExtendParams p) {
@@ -135,56 +213,15 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + LY::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.y;
     const int G = p.group;
-    // Extend: packed row R -> token R / G of request b (position P_b + R / G), head g*G + R % G.
-    // Shared-prefix: packed row R -> member R / G of group gid, head g*G + R % G, all keys.
-    int b = 0, n_b = 0, P_b = 0, rows_total, row0, kv_end, m0 = 0, k_lo = 0;
-    int64_t qo0 = 0;
-    const int32_t* slots_row;
-    if (!p.shared_mode) {
-        b = blockIdx.z;
-        qo0 = p.qo_indptr[b];
-        n_b = (int)(p.qo_indptr[b + 1] - qo0);
-        P_b = p.prefix_lens[b];
-        rows_total = n_b * G;
-        row0 = blockIdx.x * 256;
-        if (row0 >= rows_total || n_b <= 0) return;   // uniform for the whole CTA
-        if (n_b > p.max_qo_len || P_b < 0 || (int64_t)P_b + n_b > p.stride) {
-            if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.status, RX_DEV_BAD_LENGTH);
-            return;
-        }
-        const int last_row = min(row0 + 256, rows_total) - 1;
-        kv_end = P_b + last_row / G + 1;              // keys needed by this CTA
-        slots_row = p.r2t + (int64_t)b * p.stride;
-    } else {
-        const int gid = blockIdx.z;
-        const int c = blockIdx.x % p.n_chunks;
-        m0 = p.grp_row_indptr[gid];
-        rows_total = (p.grp_row_indptr[gid + 1] - m0) * G;
-        row0 = (blockIdx.x / p.n_chunks) * 256;
-        const int len = p.grp_len[gid];
-        k_lo = c * p.chunk;
-        if (row0 >= rows_total || k_lo >= len) return;
-        if (len > p.stride) {
-            if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) report(p.status, RX_DEV_BAD_LENGTH);
-            return;
-        }
-        kv_end = min(len, k_lo + p.chunk) - k_lo;     // keys of this chunk, relative to k_lo
-        slots_row = p.r2t + (int64_t)p.grp_src[gid] * p.stride + k_lo;
-    }
-    const int ntiles = rows_total - row0 > 128 ? 2 : 1;
-    // full tiles of the extend mode go through the tensor maps (token coordinates are 31-bit)
-    const bool map_rows = !p.shared_mode && qo0 + n_b <= INT32_MAX;
-    const int nkv = (kv_end + EXT_BN - 1) / EXT_BN;
-    // query row pointer of packed row R (clamped to the last valid row)
-    auto q_row = [&](int R) -> const __nv_bfloat16* {
-        if (!p.shared_mode) return p.q + ((qo0 + R / G) * p.hq + g * G + R % G) * D;
-        return p.q + ((int64_t)p.grp_rows[m0 + R / G] * p.hq + g * G + R % G) * D;
+    // query row pointer of packed row R of an item (clamped to its last valid row by the caller)
+    auto q_row = [&](int64_t qo0, int m0, int gh, int R) -> const __nv_bfloat16* {
+        if (!p.shared_mode) return p.q + ((qo0 + R / G) * p.hq + gh * G + R % G) * D;
+        return p.q + ((int64_t)p.grp_rows[m0 + R / G] * p.hq + gh * G + R % G) * D;
     };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(LY::BAR_Q), EXT_LOADERS + 1);   // + the TMA issuer's expect-tx arrival
+        mbar_init(bar(LY::BAR_Q), 32 + 1);   // per item: the Q warp's lanes + lane 0's expect-tx arrival
         for (int i = 0; i < NK; ++i) {
             mbar_init(bar(LY::BAR_KF + i), EXT_LOADERS);
             mbar_init(bar(LY::BAR_KE + i), 1);
@@ -197,20 +234,12 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
             mbar_init(bar(LY::BAR_S + t), 1);
             mbar_init(bar(LY::BAR_P + t), 4);          // one arrival per softmax warp, keys 0-63
             mbar_init(bar(LY::BAR_P + 2 + t), 4);      // keys 64-127
+            mbar_init(bar(LY::BAR_QE + t), 1);         // Q buffer t read by its item's last S
+            mbar_init(bar(LY::BAR_OR + t), 1);         // O_t of an item complete
         }
         mbar_init(bar(LY::BAR_DONE), 1);
         *abort_flag = 0;
         fence_mbar_init();
-        // Full 128-row Q tiles of the extend mode by TMA, one box per 64 columns, in the
-        // swizzled layout the MMA reads.  Issued here, before the register re-split, where
-        // its few values cost the role loops nothing.
-        const int n_full_q = (p.q_map_ok && map_rows) ? min(ntiles, (rows_total - row0) >> 7) : 0;
-        mbar_arrive_expect_tx(bar(LY::BAR_Q), (uint32_t)(n_full_q * LY::Q_TILE));
-        const int tok0 = (int)(qo0 + row0 / G);
-        for (int t = 0; t < n_full_q; ++t)
-            for (int h = 0; h < D / 64; ++h)
-                tma_load_3d(base + LY::OFF_Q + (uint32_t)(t * LY::Q_TILE + h * 128 * 128), &p.q_map, h * 64, g * G,
-                            tok0 + t * (128 / G), bar(LY::BAR_Q));
     }
     if (warp == EXT_MMA_WARP) {
         tmem_alloc(base + LY::OFF_MISC, LY::TMEM_COLS);
@@ -227,80 +256,119 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
     if (wg == 0 || wg == 3) {
     regs_decrease<EXT_REGS_OTHER>();
     if (warp != EXT_MMA_WARP) {
-        // ------------------------------------------------------------ loaders
-        const int lt = warp < 4 ? (int)threadIdx.x : (int)threadIdx.x - (EXT_MMA_WARP + 1) * 32 + 128;
+        if (warp == EXT_Q_WARP) {
+        // ------------------------------------------------------------ Q loads
+        // Per item: each Q buffer is refilled once the previous item that used it has had its
+        // last S read it; full 128-row tiles of the extend mode by TMA (lane 0, one box per 64
+        // columns, in the swizzled layout the MMA reads), a ragged last tile and every tile of
+        // the shared-prefix mode row by row (rows past the end clamped to the last one).  A
+        // warp of its own, so that the K/V loaders run on into the next item meanwhile.
         const uint32_t qs = base + LY::OFF_Q;
-        // The full Q tiles come by TMA (issued at entry); a ragged last tile, and every tile
-        // of the shared-prefix mode, is gathered row by row (rows past the end clamped to the
-        // last one).
-        const int n_full_q = (p.q_map_ok && map_rows) ? min(ntiles, (rows_total - row0) >> 7) : 0;
-        for (int qi = n_full_q * 128 * CPR + lt; qi < ntiles * 128 * CPR; qi += EXT_LOADERS) {
-            const int rr = qi / CPR, c = qi % CPR;
-            const int t = rr >> 7, r = rr & 127;
-            const int R = min(row0 + rr, rows_total - 1);
-            const __nv_bfloat16* src = q_row(R) + c * 8;
-            const uint32_t dst = qs + (uint32_t)(t * LY::Q_TILE + (c >> 3) * 128 * 128 + r * 128 +
-                                                 (((c & 7) ^ (r & 7)) << 4));
-            cp_async_16(dst, src, 16);
-        }
-        cp_async_arrive_noinc(bar(LY::BAR_Q));   // arrives once this thread's Q copies land
-        // Slot ids of one tile (this thread's keys), loaded a tile ahead: the loads of tile
-        // j+1 are issued once tile j's copies are, and first read after the next ring wait.
-        // A key inside the context whose id is outside [0, num_slots) is reported and, like a
-        // key past the context, zero-filled.  The hot loop is kept short (one tile per
-        // iteration, no per-copy branch): its code competes with the softmax loop's for the
-        // instruction cache.
-        int32_t sl[NX];
-        const uint32_t nslots = (uint32_t)min(p.num_slots, (int64_t)1 << 31);
-        auto inside = [&](int j, int x) {
-            const int q = lt + EXT_LOADERS * x;
-            return q < EXT_BN * CPR && j * EXT_BN + q / CPR < kv_end;
-        };
-        auto load_slots = [&](int j) {
+        int quse0 = 0, quse1 = 0;         // items so far that used Q buffer 0 / 1
+        for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+            const ExtItem it = ext_item(p, item);
+            if (!it.valid) continue;
+            if (quse0 > 0 && !warp_wait(bar(LY::BAR_QE), (quse0 - 1) & 1, abort_flag, p.status)) break;
+            if (it.ntiles > 1 && quse1 > 0 && !warp_wait(bar(LY::BAR_QE + 1), (quse1 - 1) & 1, abort_flag, p.status))
+                break;
+            quse0 += 1;
+            quse1 += it.ntiles > 1 ? 1 : 0;
+            const int n_full_q = (p.q_map_ok && it.map_rows) ? min(it.ntiles, (it.rows_total - it.row0) >> 7) : 0;
+            if (lane == 0) {
+                fence_proxy_async_smem();     // earlier generic-proxy writes of the buffers first
+                mbar_arrive_expect_tx(bar(LY::BAR_Q), (uint32_t)(n_full_q * LY::Q_TILE));
+                const int tok0 = (int)(it.qo0 + it.row0 / G);
+                for (int t = 0; t < n_full_q; ++t)
+                    for (int h = 0; h < D / 64; ++h)
+                        tma_load_3d(qs + (uint32_t)(t * LY::Q_TILE + h * 128 * 128), &p.q_map, h * 64, it.g * G,
+                                    tok0 + t * (128 / G), bar(LY::BAR_Q));
+            }
+            // The rows the TMA does not bring, two lanes per row: the row's source is found once
+            // (in the shared-prefix mode through the group's row list) and the pair copies
+            // neighbouring 16-byte chunks, so every 32-byte sector is read whole.
+            for (int rr = n_full_q * 128 + (lane >> 1); rr < it.ntiles * 128; rr += 16) {
+                const int t = rr >> 7, r = rr & 127;
+                const int R = min(it.row0 + rr, it.rows_total - 1);
+                const __nv_bfloat16* src = q_row(it.qo0, it.m0, it.g, R);
+                const uint32_t rowb = qs + (uint32_t)(t * LY::Q_TILE + r * 128);
 #pragma unroll
-            for (int x = 0; x < NX; ++x)
-                sl[x] = inside(j, x) ? slots_row[j * EXT_BN + (lt + EXT_LOADERS * x) / CPR] : -1;
-        };
-        // Gather one K or V tile (zero fill where sl < 0); the full barrier gets this thread's
-        // arrival when its copies have landed (cp.async.mbarrier.arrive), so a loader never
-        // waits for its own copies, only for free ring slots.
+                for (int k = 0; k < CPR / 2; ++k) {
+                    const int c = 2 * k + (lane & 1);
+                    cp_async_16(rowb + (uint32_t)((c >> 3) * 128 * 128 + (((c & 7) ^ (r & 7)) << 4)), src + c * 8, 16);
+                }
+            }
+            cp_async_arrive_noinc(bar(LY::BAR_Q));   // arrives once this lane's Q copies land
+        }
+        cp_async_wait_all();
+        } else {
+        // ------------------------------------------------------------ K/V loaders
+        const int lt = warp < 4 ? (int)threadIdx.x - 32 : (int)threadIdx.x - (EXT_MMA_WARP + 1) * 32 + 96;
+        const uint32_t nslots = (uint32_t)min(p.num_slots, (int64_t)1 << 31);
         // This thread copies the same 16-byte chunk (lt % CPR) of every key row it handles
         // (EXT_LOADERS is a multiple of CPR): its pool addresses differ by slot * row pitch only.
         static_assert(EXT_LOADERS % CPR == 0, "loader chunk per thread");
         const uint32_t pitch = (uint32_t)(p.hkv * D * 2);
-        const char* kb = reinterpret_cast<const char*>(p.k_pool + (size_t)g * D + (lt % CPR) * 8);
-        const char* vb = reinterpret_cast<const char*>(p.v_pool + (size_t)g * D + (lt % CPR) * 8);
-        auto issue = [&](uint32_t buf, const char* pb, uint32_t full) {
-#pragma unroll
-            for (int x = 0; x < NX; ++x) {
+        int gt = 0;                       // K/V tiles gathered so far (all items): ring position
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            const ExtItem it = ext_item(p, item);
+            if (!it.valid) continue;
+            // Slot ids of one tile (this thread's keys), loaded a tile ahead: the loads of tile
+            // j+1 are issued once tile j's copies are, and first read after the next ring wait.
+            // A key inside the context whose id is outside [0, num_slots) is reported and, like a
+            // key past the context, zero-filled.
+            int32_t sl[NX];
+            const int kv_end = it.kv_end, nkv = it.nkv;
+            const int32_t* slots_row = it.slots_row;
+            auto inside = [&](int j, int x) {
                 const int q = lt + EXT_LOADERS * x;
-                if (q < EXT_BN * CPR) {
-                    const int key = q / CPR, c = q % CPR;
-                    const uint32_t so =
-                        (uint32_t)((c >> 3) * EXT_BN * 128 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
-                    cp_async_16(buf + so, pb + (size_t)(uint32_t)max(sl[x], 0) * pitch, sl[x] >= 0 ? 16u : 0u);
-                }
-            }
-            cp_async_arrive_noinc(full);
-        };
-        load_slots(0);
-        for (int j = 0; j < nkv; ++j) {
-            const int ks = j % NK, vs = j % NV;
-            if (j >= NK && !warp_wait(bar(LY::BAR_KE + ks), ((j / NK) - 1) & 1, abort_flag, p.status)) break;
-            bool bad = false;
+                return q < EXT_BN * CPR && j * EXT_BN + q / CPR < kv_end;
+            };
+            auto load_slots = [&](int j) {
 #pragma unroll
-            for (int x = 0; x < NX; ++x) {
-                const bool in = inside(j, x), valid = (uint32_t)sl[x] < nslots;
-                bad |= in && !valid;
-                sl[x] = (in && valid) ? sl[x] : -1;
+                for (int x = 0; x < NX; ++x)
+                    sl[x] = inside(j, x) ? slots_row[j * EXT_BN + (lt + EXT_LOADERS * x) / CPR] : -1;
+            };
+            const char* kb = reinterpret_cast<const char*>(p.k_pool + (size_t)it.g * D + (lt % CPR) * 8);
+            const char* vb = reinterpret_cast<const char*>(p.v_pool + (size_t)it.g * D + (lt % CPR) * 8);
+            // Gather one K or V tile (zero fill where sl < 0); the full barrier gets this
+            // thread's arrival when its copies have landed (cp.async.mbarrier.arrive), so a
+            // loader never waits for its own copies, only for free ring slots.
+            auto issue = [&](uint32_t buf, const char* pb, uint32_t full) {
+#pragma unroll
+                for (int x = 0; x < NX; ++x) {
+                    const int q = lt + EXT_LOADERS * x;
+                    if (q < EXT_BN * CPR) {
+                        const int key = q / CPR, c = q % CPR;
+                        const uint32_t so =
+                            (uint32_t)((c >> 3) * EXT_BN * 128 + key * 128 + (((c & 7) ^ (key & 7)) << 4));
+                        cp_async_16(buf + so, pb + (size_t)(uint32_t)max(sl[x], 0) * pitch, sl[x] >= 0 ? 16u : 0u);
+                    }
+                }
+                cp_async_arrive_noinc(full);
+            };
+            load_slots(0);
+            for (int j = 0; j < nkv; ++j) {
+                const int u = gt + j;                 // ring position of this tile
+                const int ks = u % NK, vs = u % NV;
+                if (u >= NK && !warp_wait(bar(LY::BAR_KE + ks), ((u / NK) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                bool bad = false;
+#pragma unroll
+                for (int x = 0; x < NX; ++x) {
+                    const bool in = inside(j, x), valid = (uint32_t)sl[x] < nslots;
+                    bad |= in && !valid;
+                    sl[x] = (in && valid) ? sl[x] : -1;
+                }
+                if (bad) report(p.status, RX_DEV_BAD_SLOT);
+                issue(base + LY::OFF_K + ks * LY::KV_TILE, kb, bar(LY::BAR_KF + ks));
+                if (u >= NV && !warp_wait(bar(LY::BAR_VE + vs), ((u / NV) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                issue(base + LY::OFF_V + vs * LY::KV_TILE, vb, bar(LY::BAR_VF + vs));
+                if (j + 1 < nkv) load_slots(j + 1);
             }
-            if (bad) report(p.status, RX_DEV_BAD_SLOT);
-            issue(base + LY::OFF_K + ks * LY::KV_TILE, kb, bar(LY::BAR_KF + ks));
-            if (j >= NV && !warp_wait(bar(LY::BAR_VE + vs), ((j / NV) - 1) & 1, abort_flag, p.status)) break;
-            issue(base + LY::OFF_V + vs * LY::KV_TILE, vb, bar(LY::BAR_VF + vs));
-            if (j + 1 < nkv) load_slots(j + 1);
+            gt += nkv;
         }
         cp_async_wait_all();                   // no copy may still be landing at teardown
+        }
     } else {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -326,48 +394,67 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
                                 vd0 + (uint64_t)((vs * LY::KV_TILE + s * 16 * 128) >> 4), IDESC_PV,
                                 (j > 0 || s > 0) ? 1u : 0u);
             };
-            // The copies were made by the loaders' generic-proxy cp.async and are acquired
-            // through the full barriers; a proxy fence here orders them before the tensor
+            // The copies were made by the loaders' generic-proxy cp.async (and TMA) and are
+            // acquired through the full barriers; a proxy fence orders them before the tensor
             // core's (async-proxy) reads.
-            bool ok = mbar_wait(bar(LY::BAR_Q), 0, abort_flag, p.status) &&
-                      mbar_wait(bar(LY::BAR_KF), 0, abort_flag, p.status);
-            fence_proxy_async_smem();
-            tc_fence_after();
-            if (ok) {
-                for (int t = 0; t < ntiles; ++t) issue_s(t, 0);
-                umma_commit(bar(LY::BAR_KE));
-            }
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int vs = j % NV;
-                if (!mbar_wait(bar(LY::BAR_VF + vs), (j / NV) & 1, abort_flag, p.status)) { ok = false; break; }
+            int gt = 0, ic = 0;               // K/V tiles and items consumed so far
+            int sc0 = 0, sc1 = 0;             // score steps of Q tile 0 / 1 so far (barrier phases)
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+                const ExtItem it = ext_item(p, item);
+                if (!it.valid) continue;
+                const int nt = it.ntiles, nkv = it.nkv;
+                ok = mbar_wait(bar(LY::BAR_Q), ic & 1, abort_flag, p.status) &&
+                     mbar_wait(bar(LY::BAR_KF + gt % NK), (gt / NK) & 1, abort_flag, p.status);
+                ic += 1;
+                if (!ok) break;
                 fence_proxy_async_smem();
                 tc_fence_after();
-                const bool more = j + 1 < nkv;
-                const int ks = (j + 1) % NK;
-                for (int t = 0; t < ntiles; ++t) {
-                    // P arrives in two halves: PV over keys 0-63 runs while the softmax warps
-                    // still compute keys 64-127
-                    if (!mbar_wait(bar(LY::BAR_P + t), j & 1, abort_flag, p.status)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(t, vs, j, 0);
-                    if (!mbar_wait(bar(LY::BAR_P + 2 + t), j & 1, abort_flag, p.status)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(t, vs, j, 1);
-                    if (t == ntiles - 1) umma_commit(bar(LY::BAR_VE + vs));   // V(j) read by every tile
-                    if (more) {
-                        if (t == 0) {
-                            if (!mbar_wait(bar(LY::BAR_KF + ks), ((j + 1) / NK) & 1, abort_flag, p.status)) {
-                                ok = false;
-                                break;
-                            }
-                            fence_proxy_async_smem();
-                            tc_fence_after();
-                        }
-                        issue_s(t, ks);
-                    }
+                for (int t = 0; t < nt; ++t) {
+                    issue_s(t, gt % NK);
+                    if (nkv == 1) umma_commit(bar(LY::BAR_QE + t));   // Q_t read by this item's last S
                 }
-                if (!ok) break;
-                if (more) umma_commit(bar(LY::BAR_KE + ks));
+                umma_commit(bar(LY::BAR_KE + gt % NK));
+                for (int j = 0; ok && j < nkv; ++j) {
+                    const int u = gt + j;
+                    const int vs = u % NV;
+                    if (!mbar_wait(bar(LY::BAR_VF + vs), (u / NV) & 1, abort_flag, p.status)) { ok = false; break; }
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    const bool more = j + 1 < nkv;
+                    const int ks = (u + 1) % NK;
+                    for (int t = 0; t < nt; ++t) {
+                        const int ph = ((t == 0 ? sc0 : sc1) + j) & 1;
+                        // P arrives in two halves: PV over keys 0-63 runs while the softmax warps
+                        // still compute keys 64-127
+                        if (!mbar_wait(bar(LY::BAR_P + t), ph, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(t, vs, j, 0);
+                        if (!mbar_wait(bar(LY::BAR_P + 2 + t), ph, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(t, vs, j, 1);
+                        if (t == nt - 1) umma_commit(bar(LY::BAR_VE + vs));   // V(u) read by every tile
+                        if (more) {
+                            if (t == 0) {
+                                if (!mbar_wait(bar(LY::BAR_KF + ks), ((u + 1) / NK) & 1, abort_flag, p.status)) {
+                                    ok = false;
+                                    break;
+                                }
+                                fence_proxy_async_smem();
+                                tc_fence_after();
+                            }
+                            issue_s(t, ks);
+                            if (j + 2 == nkv) umma_commit(bar(LY::BAR_QE + t));   // the item's last S_t
+                        } else {
+                            umma_commit(bar(LY::BAR_OR + t));   // O_t of this item complete
+                        }
+                    }
+                    if (!ok) break;
+                    if (more) umma_commit(bar(LY::BAR_KE + ks));
+                }
+                sc0 += nkv;
+                sc1 += nt > 1 ? nkv : 0;
+                gt += nkv;
             }
             umma_commit(bar(LY::BAR_DONE));
         }
@@ -377,22 +464,28 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
         // ------------------------------------------------------------ softmax warpgroups
         regs_increase<EXT_REGS_SOFTMAX>();
         const int t = wg - 1;
-        if (t < ntiles) {
-            const int quarter = warp & 3;
-            const int r = quarter * 32 + lane;
-            const int R = row0 + t * 128 + r;
-            const bool valid = R < rows_total;
-            const int Rc = min(R, rows_total - 1);
-            const int tok = Rc / G;
-            const int pos = p.shared_mode ? kv_end - 1 : P_b + tok;   // attends keys 0..pos
-            const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-            const uint32_t s_addr = tmem + lane_base + t * EXT_BN;   // scores, then P over them
-            const uint32_t o_addr = tmem + lane_base + LY::COL_O0 + t * D;
-            const float sl = p.scale_log2;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + t * EXT_BN;   // scores, then P over them
+        const uint32_t o_addr = tmem + lane_base + LY::COL_O0 + t * D;
+        const float sl = p.scale_log2;
+        int sc = 0, oc = 0;                   // score steps and items of this Q tile so far
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            int pos, nkv;
+            {
+                // only what the score loop needs stays live through it; the epilogue decodes
+                // the item again
+                const ExtItem it = ext_item(p, item);
+                if (!it.valid || t >= it.ntiles) continue;
+                const int Rc = min(it.row0 + t * 128 + r, it.rows_total - 1);
+                pos = p.shared_mode ? it.kv_end - 1 : it.P_b + Rc / G;   // attends keys 0..pos
+                nkv = it.nkv;
+            }
             float m_ref = -INFINITY, l = 0.f;
-            bool ok = true;
             for (int j = 0; j < nkv; ++j) {
-                if (!warp_wait(bar(LY::BAR_S + t), j & 1, abort_flag, p.status)) { ok = false; break; }
+                if (!warp_wait(bar(LY::BAR_S + t), (sc + j) & 1, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const int lim = pos - j * EXT_BN;   // columns past lim are masked
                 if (__any_sync(0xffffffffu, lim < EXT_BN - 1)) {
@@ -473,86 +566,61 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
                 f2_unpack(a01, ra, rb);
                 l += ra + rb;
             }
-            const bool done = ok && warp_wait(bar(LY::BAR_DONE), 0, abort_flag, p.status);
-            if (done) tc_fence_after();
+            if (!ok) break;
+            sc += nkv;
+            const ExtItem it = ext_item(p, item);
+            const int R = it.row0 + t * 128 + r;
+            const bool valid = R < it.rows_total;
+            const int Rc = min(R, it.rows_total - 1);
+            const int tok = Rc / G;
+            // The item's O_t is complete once its last PV has: the epilogue reads it while the
+            // tensor core already works on the next item's scores; the next item's first PV
+            // (which overwrites O_t) waits for P that this warpgroup publishes after the reads.
+            if (!warp_wait(bar(LY::BAR_OR + t), oc & 1, abort_flag, p.status)) { ok = false; break; }
+            oc += 1;
+            tc_fence_after();
             const float inv = 1.f / l;
             if (p.shared_mode) {
-                if (done) {
-                    // fp32 normalised partial and log2-domain lse for the merge
-                    const int64_t item = (int64_t)p.grp_rows[m0 + tok] * p.hq + g * G + Rc % G;
-                    const int64_t slot = item * p.part_per + p.part_base + blockIdx.x % p.n_chunks;
-                    float* prow = p.part_o + slot * D;
+                // fp32 normalised partial and log2-domain lse for the merge
+                const int64_t row_item = (int64_t)p.grp_rows[it.m0 + tok] * p.hq + it.g * G + Rc % G;
+                const int64_t slot = row_item * p.part_per + p.part_base + it.x % p.n_chunks;
+                float* prow = p.part_o + slot * D;
 #pragma unroll
-                    for (int cc = 0; cc < D; cc += 32) {
-                        float ov[32];
-                        tmem_ld32(o_addr + cc, ov);
-                        tmem_wait_ld();
-                        if (valid) {
+                for (int cc = 0; cc < D; cc += 32) {
+                    float ov[32];
+                    tmem_ld32(o_addr + cc, ov);
+                    tmem_wait_ld();
+                    if (valid) {
 #pragma unroll
-                            for (int e = 0; e < 32; e += 4)
-                                *reinterpret_cast<float4*>(prow + cc + e) =
-                                    make_float4(ov[e] * inv, ov[e + 1] * inv, ov[e + 2] * inv, ov[e + 3] * inv);
-                        }
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4*>(prow + cc + e) =
+                                make_float4(ov[e] * inv, ov[e + 1] * inv, ov[e + 2] * inv, ov[e + 3] * inv);
                     }
-                    if (valid) p.part_lse[slot] = m_ref + log2f(l);
                 }
+                if (valid) p.part_lse[slot] = m_ref + log2f(l);
             } else {
-                // A full tile (uniform in the warpgroup) is written by TMA: each thread puts its
-                // normalised bf16 row into the tile's Q buffer (no longer read: every MMA has
-                // completed) in the swizzled layout, then one thread stores the boxes.  The
-                // first barrier also agrees that every warp got here with its rows.
-                bool staged = false;
-                if (p.o_map_ok && map_rows && row0 + (t + 1) * 128 <= rows_total) {
-                    const uint32_t stg = base + LY::OFF_Q + (uint32_t)(t * LY::Q_TILE);
-                    if (done) {
+                // each thread writes its own normalised bf16 row (16-byte stores)
+                __nv_bfloat16* orow = p.out + ((it.qo0 + tok) * p.hq + it.g * G + Rc % G) * D;
 #pragma unroll
-                        for (int cc = 0; cc < D; cc += 32) {
-                            float ov[32];
-                            tmem_ld32(o_addr + cc, ov);
-                            tmem_wait_ld();
+                for (int cc = 0; cc < D; cc += 32) {
+                    float ov[32];
+                    tmem_ld32(o_addr + cc, ov);
+                    tmem_wait_ld();
+                    if (valid) {
 #pragma unroll
-                            for (int e = 0; e < 32; e += 8) {
-                                const int c = (cc + e) >> 3;
-                                st_shared_v4(stg + (uint32_t)((c >> 3) * 128 * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
-                                             pack_bf16x2(ov[e + 0] * inv, ov[e + 1] * inv),
-                                             pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv),
-                                             pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv),
-                                             pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv));
-                            }
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    staged = named_bar_and(1 + t, 128, done);
-                    if (staged && r == 0) {
-                        const int tok_first = (int)(qo0 + (row0 + t * 128) / G);
-                        for (int h = 0; h < D / 64; ++h)
-                            tma_store_3d(&p.o_map, stg + (uint32_t)(h * 128 * 128), h * 64, g * G, tok_first);
-                        bulk_commit();
-                        bulk_wait_read_all();   // the buffer is read before the CTA may exit
-                    }
-                }
-                if (done && !staged) {
-                    __nv_bfloat16* orow = p.out + ((qo0 + tok) * p.hq + g * G + Rc % G) * D;
-#pragma unroll
-                    for (int cc = 0; cc < D; cc += 32) {
-                        float ov[32];
-                        tmem_ld32(o_addr + cc, ov);
-                        tmem_wait_ld();
-                        if (valid) {
-#pragma unroll
-                            for (int e = 0; e < 32; e += 8) {
-                                uint4 v;
-                                v.x = pack_bf16x2(ov[e + 0] * inv, ov[e + 1] * inv);
-                                v.y = pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv);
-                                v.z = pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv);
-                                v.w = pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv);
-                                *reinterpret_cast<uint4*>(orow + cc + e) = v;
-                            }
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(ov[e + 0] * inv, ov[e + 1] * inv);
+                            v.y = pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv);
+                            v.z = pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv);
+                            v.w = pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv);
+                            *reinterpret_cast<uint4*>(orow + cc + e) = v;
                         }
                     }
                 }
-                if (done && valid && p.lse) p.lse[(qo0 + tok) * p.hq + g * G + Rc % G] = (m_ref + log2f(l)) * EXT_LN2;
+                if (valid && p.lse) p.lse[(it.qo0 + tok) * p.hq + it.g * G + Rc % G] = (m_ref + log2f(l)) * EXT_LN2;
             }
+            tc_fence_before();
         }
     }
     // ---------------------------------------------------------------- teardown
@@ -619,8 +687,25 @@ static bool rows_tensor_map(CUtensorMap* m, const void* ptr, int hq, int D, int 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Streaming multiprocessors of the current device (one persistent CTA each), read once per device.
+static int sm_count() {
+    static PerDeviceOnce once;
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    per_device_once(once, [&] {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return (int)RX_ECUDA;
+        counts[dev] = n;
+        return (int)RX_OK;
+    });
+    return counts[dev];
+}
+
+// Launches the kernel over the tiles x hkv x gz grid of work items as a persistent grid: one
+// CTA per SM (at most one per item), each walking the items round-robin.
 template <int D>
-static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t stream, int gz) {
+static int launch_extend_tc(ExtendParams p, int tiles, cudaStream_t stream, int gz) {
     static PerDeviceOnce attr;
     const int smem = ExtLayout<D>::ALLOC;
     const int rc = per_device_once(attr, [&] {
@@ -641,8 +726,21 @@ static int launch_extend_tc(const ExtendParams& p, int tiles, cudaStream_t strea
         return (int)RX_OK;
     });
     if (rc != RX_OK) return rc;
-    dim3 grid((unsigned)tiles, (unsigned)p.hkv, (unsigned)gz);
-    extend_tc_kernel<D><<<grid, EXT_THREADS, smem, stream>>>(p);
+    const int64_t items = (int64_t)tiles * p.hkv * gz;
+    if (items <= 0) return RX_OK;
+    if (items >= (1ll << 31)) {
+        set_error("prefix_extend_attention: too many work items (%lld)", (long long)items);
+        return RX_EINVAL;
+    }
+    const int sms = sm_count();
+    if (sms <= 0) {
+        set_error("prefix_extend_attention: cannot read the device's SM count");
+        return RX_ECUDA;
+    }
+    p.grid_x = tiles;
+    p.n_items = (int32_t)items;
+    const unsigned ctas = (unsigned)std::min<int64_t>(items, sms);
+    extend_tc_kernel<D><<<ctas, EXT_THREADS, smem, stream>>>(p);
     return RX_OK;
 }
 
@@ -1046,7 +1144,6 @@ extern "C" int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch, 
     // (the rows the row-by-row path would touch as well).
     const int64_t row_bound = INT32_MAX;
     p.q_map_ok = rows_tensor_map(&p.q_map, d_q, desc->hq, desc->head_dim, group, row_bound) ? 1 : 0;
-    p.o_map_ok = rows_tensor_map(&p.o_map, d_out, desc->hq, desc->head_dim, group, row_bound) ? 1 : 0;
     const int rc = desc->head_dim == 128 ? launch_extend_tc<128>(p, (int)tiles, stream, batch)
                                          : launch_extend_tc<64>(p, (int)tiles, stream, batch);
     if (rc != RX_OK) return rc;

@@ -52,6 +52,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <mutex>
+#include <unordered_map>
 
 #include "radix_attn.h"
 #include "rx_common.h"
@@ -65,6 +67,10 @@ constexpr int EXT_THREADS = 512;  // 16 warps
 constexpr int EXT_MMA_WARP = 12;
 constexpr int EXT_Q_WARP = 0;      // loads every item's Q tiles (TMA, or row gathers for ragged tiles)
 constexpr int EXT_LOADERS = 192;  // K/V gathers: warps 1-3 and 13-15
+constexpr int EXT_RING = 4;        // items handed from the Q warp to the other roles, in flight
+// warps that take items from the ring besides the Q warp that fills it: six loader warps, the
+// MMA warp and eight softmax warps (one arrival each per item)
+constexpr int EXT_ITEM_CONSUMERS = 15;
 constexpr uint32_t EXT_REGS_SOFTMAX = 168, EXT_REGS_OTHER = 88;   // 2*128*88 + 2*128*168 = 512*128
 constexpr float EXT_LOG2E = 1.4426950408889634f;
 constexpr float EXT_LN2 = 0.6931471805599453f;
@@ -105,8 +111,12 @@ struct ExtendParams {
     int32_t q_map_ok;
     CUtensorMap q_map;
     // Persistent grid: the work items are the cells (x, kv head, request or group) of a
-    // grid_x x hkv x (batch or groups) grid, x fastest; CTA c takes items c, c + gridDim.x, ...
+    // grid_x x hkv x (batch or groups) grid, x fastest.  With `work` (two counters: the next
+    // item, and the CTAs done; zero at launch) the CTAs take items in order as they free up, so
+    // the items in flight stay a compact window and share L2 (one CTA per item of the window
+    // touches the same requests' K/V); without it CTA c takes items c, c + gridDim.x, ...
     int32_t grid_x, n_items;
+    unsigned int* work;
 };
 
 template <int D>
@@ -123,9 +133,10 @@ struct ExtLayout {
     // q_empty[2], o_ready[2], mma_done
     static constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 1 + NK, BAR_VF = 1 + 2 * NK, BAR_VE = 1 + 2 * NK + NV,
                          BAR_S = 1 + 2 * NK + 2 * NV, BAR_P = BAR_S + 2, BAR_QE = BAR_P + 4, BAR_OR = BAR_QE + 2,
-                         BAR_DONE = BAR_OR + 2, NBAR = BAR_DONE + 1;
+                         BAR_IF = BAR_OR + 2, BAR_IE = BAR_IF + EXT_RING, BAR_DONE = BAR_IE + EXT_RING,
+                         NBAR = BAR_DONE + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int BYTES = OFF_MISC + 16 + 4 * EXT_RING;   // TMEM address, abort flag, item ring
     static constexpr int ALLOC = BYTES + 1024;   // room to align the base to 1024 B
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_O0 = 256;
@@ -211,6 +222,33 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
     auto bar = [&](int i) { return bar0 + (uint32_t)(8 * i); };
     volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + LY::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + LY::OFF_MISC + 4);
+    volatile int32_t* item_ring = reinterpret_cast<volatile int32_t*>(gbase + LY::OFF_MISC + 16);
+    // This CTA's k-th item (-1: none left).  Round-robin without a work counter; with one, the
+    // entry the Q warp wrote into the ring (a whole warp waits; lane 0 releases the entry).
+    auto take_item_warp = [&](int k) -> int {
+        if (!p.work) {
+            const int64_t it = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+            return it < p.n_items ? (int)it : -1;
+        }
+        const int e = k % EXT_RING;
+        if (!warp_wait(bar(LY::BAR_IF + e), (k / EXT_RING) & 1, abort_flag, p.status)) return -1;
+        const int item = item_ring[e];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(bar(LY::BAR_IE + e));
+        return item;
+    };
+    // the same for the single MMA-issuing thread
+    auto take_item_thread = [&](int k) -> int {
+        if (!p.work) {
+            const int64_t it = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+            return it < p.n_items ? (int)it : -1;
+        }
+        const int e = k % EXT_RING;
+        if (!mbar_wait(bar(LY::BAR_IF + e), (k / EXT_RING) & 1, abort_flag, p.status)) return -1;
+        const int item = item_ring[e];
+        mbar_arrive(bar(LY::BAR_IE + e));
+        return item;
+    };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
@@ -236,6 +274,10 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
             mbar_init(bar(LY::BAR_P + 2 + t), 4);      // keys 64-127
             mbar_init(bar(LY::BAR_QE + t), 1);         // Q buffer t read by its item's last S
             mbar_init(bar(LY::BAR_OR + t), 1);         // O_t of an item complete
+        }
+        for (int i = 0; i < EXT_RING; ++i) {
+            mbar_init(bar(LY::BAR_IF + i), 1);                        // entry i written
+            mbar_init(bar(LY::BAR_IE + i), EXT_ITEM_CONSUMERS);       // entry i read by every role
         }
         mbar_init(bar(LY::BAR_DONE), 1);
         *abort_flag = 0;
@@ -265,7 +307,26 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
         // warp of its own, so that the K/V loaders run on into the next item meanwhile.
         const uint32_t qs = base + LY::OFF_Q;
         int quse0 = 0, quse1 = 0;         // items so far that used Q buffer 0 / 1
-        for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+        for (int k = 0;; ++k) {
+            // the next item: from the work counter into the ring (once every role has read the
+            // entry it replaces), or round-robin
+            int item;
+            if (p.work) {
+                const int e = k % EXT_RING;
+                if (k >= EXT_RING && !warp_wait(bar(LY::BAR_IE + e), ((k / EXT_RING) - 1) & 1, abort_flag, p.status))
+                    break;
+                if (lane == 0) {
+                    const unsigned t = atomicAdd(&p.work[0], 1u);
+                    item = t < (unsigned)p.n_items ? (int)t : -1;
+                    item_ring[e] = item;
+                    mbar_arrive(bar(LY::BAR_IF + e));   // release: the entry is visible to the waiters
+                }
+                item = __shfl_sync(0xffffffffu, item, 0);
+            } else {
+                const int64_t it = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+                item = it < p.n_items ? (int)it : -1;
+            }
+            if (item < 0) break;
             const ExtItem it = ext_item(p, item);
             if (!it.valid) continue;
             if (quse0 > 0 && !warp_wait(bar(LY::BAR_QE), (quse0 - 1) & 1, abort_flag, p.status)) break;
@@ -310,7 +371,9 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
         const uint32_t pitch = (uint32_t)(p.hkv * D * 2);
         int gt = 0;                       // K/V tiles gathered so far (all items): ring position
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int item = take_item_warp(k);
+            if (item < 0) break;
             const ExtItem it = ext_item(p, item);
             if (!it.valid) continue;
             // Slot ids of one tile (this thread's keys), loaded a tile ahead: the loads of tile
@@ -400,7 +463,9 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
             int gt = 0, ic = 0;               // K/V tiles and items consumed so far
             int sc0 = 0, sc1 = 0;             // score steps of Q tile 0 / 1 so far (barrier phases)
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            for (int k = 0; ok; ++k) {
+                const int item = take_item_thread(k);
+                if (item < 0) break;
                 const ExtItem it = ext_item(p, item);
                 if (!it.valid) continue;
                 const int nt = it.ntiles, nkv = it.nkv;
@@ -472,7 +537,9 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
         const float sl = p.scale_log2;
         int sc = 0, oc = 0;                   // score steps and items of this Q tile so far
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int item = take_item_warp(k);
+            if (item < 0) break;
             int pos, nkv;
             {
                 // only what the score loop needs stays live through it; the epilogue decodes
@@ -626,6 +693,15 @@ __global__ void __launch_bounds__(EXT_THREADS, 1) extend_tc_kernel(const __grid_
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
+    // The last CTA out resets the work counters for the next launch that uses them (launches
+    // on one stream run one after another; every fetch of this CTA precedes its count).
+    if (p.work && threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&p.work[1], 1u) == gridDim.x - 1) {
+            atomicExch(&p.work[0], 0u);
+            atomicExch(&p.work[1], 0u);
+        }
+    }
     if (warp == EXT_MMA_WARP) {
         tc_fence_after();
         // Every MMA this CTA issued has completed before TMEM is released; this wait does
@@ -702,8 +778,47 @@ static int sm_count() {
     return counts[dev];
 }
 
+// Work counters of the persistent grid, a pair per stream (launches on one stream run one after
+// another and each launch's last CTA leaves its pair at zero; launches on different streams may
+// overlap, so each stream has its own pair).  Zero when the module loads.
+constexpr int EXT_WORK_SLOTS = 256;
+__device__ unsigned int g_ext_work[EXT_WORK_SLOTS][2];
+
+// The counter pair of `stream` on the current device, or null when every pair is taken (the
+// kernel then walks its items round-robin).
+static unsigned int* work_counters(cudaStream_t stream) {
+    static PerDeviceOnce once;
+    static unsigned int* base[64] = {};
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> slot_of;   // (device, stream) -> pair
+    static int used[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    per_device_once(once, [&] {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_ext_work) != cudaSuccess || !a) {
+            cudaGetLastError();
+            return (int)RX_ECUDA;
+        }
+        base[dev] = (unsigned int*)a;
+        return (int)RX_OK;
+    });
+    if (!base[dev]) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    const uint64_t key = ((uint64_t)dev << 56) ^ (uint64_t)(uintptr_t)stream;
+    auto it = slot_of.find(key);
+    if (it == slot_of.end()) {
+        if (used[dev] >= EXT_WORK_SLOTS) return nullptr;
+        it = slot_of.emplace(key, used[dev]++).first;
+    }
+    return base[dev] + 2 * it->second;
+}
+
 // Launches the kernel over the tiles x hkv x gz grid of work items as a persistent grid: one
-// CTA per SM (at most one per item), each walking the items round-robin.
+// CTA per SM (at most one per item), taking the items in order from the stream's work counter.
 template <int D>
 static int launch_extend_tc(ExtendParams p, int tiles, cudaStream_t stream, int gz) {
     static PerDeviceOnce attr;
@@ -739,6 +854,9 @@ static int launch_extend_tc(ExtendParams p, int tiles, cudaStream_t stream, int 
     }
     p.grid_x = tiles;
     p.n_items = (int32_t)items;
+    // the counter only where a CTA walks several items: with at most one item per CTA (the
+    // decode's shared-prefix part, launched beside the private part) each CTA takes its own
+    p.work = items > sms ? work_counters(stream) : nullptr;
     const unsigned ctas = (unsigned)std::min<int64_t>(items, sms);
     extend_tc_kernel<D><<<ctas, EXT_THREADS, smem, stream>>>(p);
     return RX_OK;

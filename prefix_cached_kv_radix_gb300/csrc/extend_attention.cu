@@ -13,9 +13,11 @@
 // heads of a kv head (GQA group) are packed with the tokens, head fastest: packed row R ->
 // token R / G, head g*G + R % G, so every K/V tile feeds G heads and the tile stays a dense
 // contraction.  Two 128-row Q tiles share each K/V tile of 128 keys.  The grid is persistent:
-// one CTA per SM walks the items round-robin (item c, c + gridDim.x, ...), its rings, barriers
-// and TMEM running on across items, so an item's set-up and output overlap the neighbouring
-// items' work instead of each CTA starting and draining on its own.  Roles (512 threads, four
+// one CTA per SM, its rings, barriers and TMEM running on across items, so an item's set-up and
+// output overlap the neighbouring items' work instead of each CTA starting and draining on its
+// own.  The CTAs take the items in order from a per-stream work counter (the Q warp fetches the
+// next item and hands its id to the other roles through a small ring in shared memory), so the
+// items in flight stay a compact window whose K/V the L2 holds.  Roles (512 threads, four
 // warpgroups, registers split 88 / 168 / 168 / 88 with setmaxnreg):
 //   warp 0     Q loads: per item, once the previous item's last S has read a Q buffer, the
 //              full 128-row tiles by TMA (one box per 64 columns, q seen as [token][head][D],

@@ -692,3 +692,37 @@ def test_host_buffer_decode_chunks_match_oracle():
         want, wl = oracle_rows(w, b)
         compare(got[b:b + 1], want, f"request {b}")
         assert np.abs(got_lse[b:b + 1] - wl).max() <= TOL_LSE
+
+
+@pytest.mark.gpu
+def test_extend_persistent_grid_on_two_streams():
+    """The extend kernel's persistent grid takes its items in order from a work counter per
+    stream: the same extend call launched on two streams at once (more items than SMs, so the
+    counters are used) gives, on each stream and on a third call after them, the output of the
+    first call bit for bit, and that output matches the oracle."""
+    spec = W.Spec("persist-2streams", "bf16", 32, 8, 128, 1 << 16, W.QWEN_VOCAB, 45,
+                  seg_parent=[-1], seg_len=[300], histories=[0],
+                  req_seg=[0] * 24, req_cached=[300] * 24, req_new=[128] * 24)
+    w = W.generate(spec)
+    eng, plan, dev, out, lse, _ = run_step(w)
+    want = to_host_f32(out)
+    q, _, _ = w.stacked_new()
+    from prefix_cached_kv_radix_gb300.engine import _dev_from_host
+    qd = _dev_from_host(q, spec.dtype, eng.device)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty_like(out) for _ in streams]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for st, o in zip(streams, outs):
+            eng.extend(plan, dev, qd, o, stream=st.cuda_stream)
+    torch.cuda.synchronize()
+    again = torch.empty_like(out)
+    eng.extend(plan, dev, qd, again)
+    torch.cuda.synchronize()
+    assert eng.device_status() == 0
+    for o in outs + [again]:
+        assert np.array_equal(to_host_f32(o), want)
+    for b in (0, 11, 23):
+        lo, hi = b * 128, (b + 1) * 128
+        o_want, _ = oracle_rows(w, b, rows=[0, 63, 127])
+        compare(want[lo:hi][[0, 63, 127]], o_want, f"request {b}")

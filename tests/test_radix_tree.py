@@ -161,6 +161,25 @@ def test_random_scripts_match_oracle(vocab):
         _run_script(ops, 48, trial)
 
 
+def test_wide_fanout_scripts_match_oracle():
+    """Hundreds of children under one node (the child links' open-addressing table grows, and
+    evictions delete from it with backward shifts, among long probe runs): the tree still
+    equals the oracle model op for op."""
+    rng = np.random.default_rng(77)
+    for trial in range(3):
+        ops = []
+        for _ in range(400):
+            r = rng.random()
+            seq = [int(rng.integers(0, 500))] + rng.integers(0, 3, size=rng.integers(0, 5)).tolist()
+            if r < 0.3:
+                ops.append(("match", seq))
+            elif r < 0.85:
+                ops.append(("insert", seq))
+            else:
+                ops.append(("evict", int(rng.integers(1, 40))))
+        _run_script(ops, 2000, 50 + trial)
+
+
 def test_exhaustive_short_sequences():
     seqs = [list(s) for L in range(1, 4) for s in itertools.product([0, 1], repeat=L)]
     ops = []

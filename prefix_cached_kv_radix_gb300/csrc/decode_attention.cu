@@ -699,6 +699,11 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
         return (int)RX_OK;
     });
     if (arc != RX_OK) return arc;
+    dim3 grid((unsigned)lay.max_chunks, (unsigned)desc->hkv, (unsigned)batch);
+    auto launch_private = [&] {
+        if (D == 128) decode_private_kernel<128><<<grid, DEC_THREADS, smem, stream>>>(p);
+        else decode_private_kernel<64><<<grid, DEC_THREADS, smem, stream>>>(p);
+    };
     DecodeFork* fork = nullptr;
     std::unique_lock<std::mutex> fork_lock;
     if (use_groups) {
@@ -716,6 +721,10 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
             else
                 fork = nullptr;
         }
+        // The private part is launched first: its CTAs fill the GPU at once, and the shared
+        // part's CTAs (a whole SM each) take SMs as the private part's last wave drains,
+        // instead of holding SMs from the private part's start.
+        launch_private();
         SharedTcParams sp{};
         sp.q = d_q;
         sp.r2t = d_req_to_token;
@@ -748,9 +757,7 @@ extern "C" int decode_attention(const rx_attn_desc* desc, int32_t batch, const v
             return RX_ECUDA;
         }
     }
-    dim3 grid((unsigned)lay.max_chunks, (unsigned)desc->hkv, (unsigned)batch);
-    if (D == 128) decode_private_kernel<128><<<grid, DEC_THREADS, smem, stream>>>(p);
-    else decode_private_kernel<64><<<grid, DEC_THREADS, smem, stream>>>(p);
+    if (!use_groups) launch_private();
     if (fork && cudaStreamWaitEvent(stream, fork->shared_done, 0) != cudaSuccess) {
         set_error("decode_attention: cannot join the shared part");
         return RX_ECUDA;

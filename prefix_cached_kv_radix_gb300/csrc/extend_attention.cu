@@ -787,10 +787,10 @@ constexpr int EXT_WORK_SLOTS = 256;
 __device__ unsigned int g_ext_work[EXT_WORK_SLOTS][2];
 
 // The counter pair of `stream` on the current device, or null when every pair is taken (the
-// kernel then walks its items round-robin).
+// kernel then walks its items round-robin).  The array's address is looked up on every call (a
+// host-side lookup in the current context), so a context created after cudaDeviceReset, which
+// loads the module at a new address with the counters at zero again, gets its own.
 static unsigned int* work_counters(cudaStream_t stream) {
-    static PerDeviceOnce once;
-    static unsigned int* base[64] = {};
     static std::mutex mu;
     static std::unordered_map<uint64_t, int> slot_of;   // (device, stream) -> pair
     static int used[64] = {};
@@ -799,16 +799,11 @@ static unsigned int* work_counters(cudaStream_t stream) {
         cudaGetLastError();
         return nullptr;
     }
-    per_device_once(once, [&] {
-        void* a = nullptr;
-        if (cudaGetSymbolAddress(&a, g_ext_work) != cudaSuccess || !a) {
-            cudaGetLastError();
-            return (int)RX_ECUDA;
-        }
-        base[dev] = (unsigned int*)a;
-        return (int)RX_OK;
-    });
-    if (!base[dev]) return nullptr;
+    void* base = nullptr;
+    if (cudaGetSymbolAddress(&base, g_ext_work) != cudaSuccess || !base) {
+        cudaGetLastError();
+        return nullptr;
+    }
     std::lock_guard<std::mutex> lk(mu);
     const uint64_t key = ((uint64_t)dev << 56) ^ (uint64_t)(uintptr_t)stream;
     auto it = slot_of.find(key);
@@ -816,7 +811,7 @@ static unsigned int* work_counters(cudaStream_t stream) {
         if (used[dev] >= EXT_WORK_SLOTS) return nullptr;
         it = slot_of.emplace(key, used[dev]++).first;
     }
-    return base[dev] + 2 * it->second;
+    return (unsigned int*)base + 2 * it->second;
 }
 
 // Launches the kernel over the tiles x hkv x gz grid of work items as a persistent grid: one

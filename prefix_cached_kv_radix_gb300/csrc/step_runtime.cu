@@ -161,8 +161,11 @@ RowBytes row_bytes(const rx_attn_desc* d) {
     return {(int64_t)d->hq * d->head_dim * elt, (int64_t)d->hkv * d->head_dim * elt};
 }
 
-// The pipeline's request ranges: `chunks` (0: one per 64 MB moved, at most 4) ranges of about
-// equal token counts, cut at request boundaries of the row index qo (host, batch+1 entries).
+// The pipeline's request ranges, cut at request boundaries of the row index qo (host, batch+1
+// entries): `chunks` ranges of about equal token counts; or, for chunks = 0, one range per 64 MB
+// moved (at most 4), with the last eighth of the last range's tokens (at least one request) cut
+// off as a range of its own when there are several: the output copy of the step's last range is
+// the one copy that no later kernel of the step hides, so it is kept short.
 std::vector<int32_t> range_cuts(const rx_attn_desc* d, const int64_t* qo, int32_t B, int32_t chunks) {
     const int64_t T = qo[B] - qo[0];
     const RowBytes rb = row_bytes(d);
@@ -173,6 +176,15 @@ std::vector<int32_t> range_cuts(const rx_attn_desc* d, const int64_t* qo, int32_
     for (int c = 1; c < nc; ++c) {   // first request whose rows start at or after c/nc of the tokens
         const int64_t target = qo[0] + T * c / nc;
         cut[(size_t)c] = std::max((int32_t)(std::lower_bound(qo, qo + B, target) - qo), cut[(size_t)c - 1]);
+    }
+    if (chunks <= 0 && nc > 1) {
+        const int32_t b0 = cut[(size_t)nc - 1];
+        if (B - b0 >= 2) {             // the first request whose rows start in the last eighth
+            const int64_t target = qo[B] - (qo[B] - qo[b0]) / 8;
+            int32_t s = (int32_t)(std::lower_bound(qo + b0 + 1, qo + B, target) - qo);
+            s = std::min(s, B - 1);
+            cut.insert(cut.end() - 1, s);
+        }
     }
     return cut;
 }

@@ -155,10 +155,10 @@ def test_benchmark_path_matches_oracle(name):
     """The benchmark's step at full size, three ways: (A) device rows, overlap, groups "auto";
     (B) right after A with no synchronize, on a second set of device rows holding other values
     (its index-array copy runs under A's kernels); (C) host-buffer mode with four request ranges
-    and overlap, on A's rows.  Every step has fresh new-token ids, inserts them and evicts as
-    many tokens, as in the benchmark.  Slots are the oracle's bit for bit; A and B match the
-    oracle (c3: every row; c5: the survey's sample for A, eight rows per request for B); C equals
-    A bit for bit."""
+    and overlap, on A's rows; (D) the same with the library's automatic ranges, as the benchmark
+    runs it.  Every step has fresh new-token ids, inserts them and evicts as many tokens, as in
+    the benchmark.  Slots are the oracle's bit for bit; A and B match the oracle (c3: every row;
+    c5: the survey's sample for A, eight rows per request for B); C and D equal A bit for bit."""
     import bench
     from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine, _dev_from_host
     spec = W.config(name)
@@ -172,7 +172,7 @@ def test_benchmark_path_matches_oracle(name):
     n_new = np.asarray(s.req_new, np.int64)
     used = {}
     inputs = []
-    for j in range(3):
+    for j in range(4):
         prompts = bench.fresh_prompts(w, j, used)
         ind = np.concatenate([[0], np.cumsum([len(x) for x in prompts])]).astype(np.int64)
         inputs.append((np.concatenate(prompts).astype(np.int32), ind))
@@ -190,7 +190,7 @@ def test_benchmark_path_matches_oracle(name):
     torch.cuda.synchronize()
     assert eng.device_status() == 0
     eng.tree.check()
-    want_new = step_slots(s, w, 3)
+    want_new = step_slots(s, w, 4)
     assert np.array_equal(np.concatenate(new_a), want_new[0])
     for j in range(2):          # both plans' index arrays stay readable until the plan after next
         _check_plan(plans[j], w, pre, want_new[j], P)
@@ -205,23 +205,28 @@ def test_benchmark_path_matches_oracle(name):
         rows_b_of = {b: np.sort(np.concatenate([[0, 1023], rng.choice(np.arange(1, 1023), 6, replace=False)]))
                      for b in range(w.batch)}
         _check_sampled(w2, outs[1], lses[1], rows_b_of.get, f"{name} step B")
-    # (C) host buffers, four request ranges, overlap; A's rows from pinned host memory
+    # (C) host buffers, four request ranges, overlap; A's rows from pinned host memory; (D) the
+    # same with the automatic ranges (a short last range of its own)
     host = [x.cpu().pin_memory() for x in rows_a]
     dev_rows = [torch.zeros_like(x) for x in rows_a]
     out_c = torch.empty_like(outs[0])
     lse_c = torch.empty_like(lses[0])
-    out_h = torch.full(out_c.shape, float("nan"), dtype=out_c.dtype).pin_memory()
-    lse_h = torch.full(lse_c.shape, float("nan"), dtype=torch.float32).pin_memory()
-    toks, ind = inputs[2]
-    plan_c = eng.step(toks, ind, n_new, *dev_rows, out_c, lse_c, groups="auto", evict_tokens=T,
-                      host=(*host, out_h, lse_h), chunks=4, overlap=True)
-    torch.cuda.synchronize()
-    assert eng.device_status() == 0
-    eng.tree.check()
-    _check_plan(plan_c, w, pre, want_new[2], P)
-    assert np.array_equal(out_h.view(torch.int16).numpy(), outs[0].view(torch.int16).cpu().numpy()), \
-        "host-buffer step differs from the device-row step"
-    assert np.array_equal(lse_h.numpy(), lses[0].cpu().numpy())
+    for j, chunks in ((2, 4), (3, 0)):
+        for x in dev_rows:
+            x.zero_()                               # the library must fill them from the host copies
+        torch.cuda.synchronize()                    # (with overlap the copies do not wait for this)
+        out_h = torch.full(out_c.shape, float("nan"), dtype=out_c.dtype).pin_memory()
+        lse_h = torch.full(lse_c.shape, float("nan"), dtype=torch.float32).pin_memory()
+        toks, ind = inputs[j]
+        plan_c = eng.step(toks, ind, n_new, *dev_rows, out_c, lse_c, groups="auto", evict_tokens=T,
+                          host=(*host, out_h, lse_h), chunks=chunks, overlap=True)
+        torch.cuda.synchronize()
+        assert eng.device_status() == 0
+        eng.tree.check()
+        _check_plan(plan_c, w, pre, want_new[j], P)
+        assert np.array_equal(out_h.view(torch.int16).numpy(), outs[0].view(torch.int16).cpu().numpy()), \
+            f"host-buffer step (chunks={chunks}) differs from the device-row step"
+        assert np.array_equal(lse_h.numpy(), lses[0].cpu().numpy())
 
 
 def step_slots(s, w, k):

@@ -383,10 +383,12 @@ int decode_attention_noalloc(const rx_attn_desc* desc, int32_t batch,
  * Host-buffer mode (h_q set): the step's new rows come from host memory -- h_q, h_k_new,
  * h_v_new in the layout of d_q, d_k_new, d_v_new (pinned, for the copies to run
  * asynchronously) -- and the output goes back to h_out (and h_lse, optional).  The requests
- * are cut into `chunks` ranges of about equal token counts (0: chosen from the bytes moved;
- * 1 with shared-prefix groups) that run as a pipeline on two internal copy streams: the rows
- * of range c+1 are copied in while range c computes on `stream` and the output of range c-1
- * is copied out.  `stream` waits for the last copy, so the host buffers are complete (and
+ * are cut into `chunks` ranges of about equal token counts (0: chosen from the bytes moved, and
+ * with several ranges the last eighth of the last range's tokens becomes a range of its own, so
+ * that the one output copy no later kernel hides is short) that run as a pipeline on two
+ * internal copy streams: the rows of range c+1 are copied in while range c computes on
+ * `stream` and the output of range c-1 is copied out (with shared-prefix groups the rows still
+ * cross in ranges, and one computation over all of them starts once every range is in).  `stream` waits for the last copy, so the host buffers are complete (and
  * may be reused) once `stream` is.  The device buffers are still the caller's.  The input
  * copies wait for all work already on `stream`, or, with io->overlap set, only for the
  * kernels of the last host-buffer step whose d_q was this step's d_q (when the library still

@@ -2,9 +2,9 @@
 attention) is compared in full at c1-c4 and on sampled rows at c5.  The path the benchmark
 times -- PrefixCacheEngine.step (rx_step_plan + rx_step_launch) with cross-step overlap,
 "auto" shared-prefix grouping, back-to-back steps on alternating device rows, and the
-host-buffer pipeline of four request ranges -- is compared at c3 in full and at c5 on the
-survey's sample: all 64 heads, rows {0, 127, 128, 511, 1023} plus 27 seeded random rows of
-every request, and every row of requests 0 and 31."""
+host-buffer pipeline of request ranges -- is compared at c3 in full and at c5 on a fixed
+sample: all 64 heads, rows {0, 127, 128, 511, 1023} plus 27 seeded random rows of every
+request, and every row of requests 0 and 31."""
 import copy
 
 import numpy as np
@@ -135,7 +135,7 @@ def _check_sampled(w, out, lse, rows_of, what):
 
 
 def c5_sample(w, seed=55):
-    """The survey's c5 sample: rows {0, 127, 128, 511, 1023} plus 27 seeded random rows of every
+    """The c5 sample: rows {0, 127, 128, 511, 1023} plus 27 seeded random rows of every
     request (32 rows each, all heads), and every row of requests 0 and 31."""
     rng = np.random.default_rng(seed)
     fixed = np.array([0, 127, 128, 511, 1023])
@@ -158,7 +158,7 @@ def test_benchmark_path_matches_oracle(name):
     and overlap, on A's rows; (D) the same with the library's automatic ranges, as the benchmark
     runs it.  Every step has fresh new-token ids, inserts them and evicts as many tokens, as in
     the benchmark.  Slots are the oracle's bit for bit; A and B match the oracle (c3: every row;
-    c5: the survey's sample for A, eight rows per request for B); C and D equal A bit for bit."""
+    c5: the fixed sample for A, eight rows per request for B); C and D equal A bit for bit."""
     import bench
     from prefix_cached_kv_radix_gb300.engine import PrefixCacheEngine, _dev_from_host
     spec = W.config(name)

@@ -541,6 +541,55 @@ def test_host_buffer_step_equals_device_step(chunks):
             compare(o_h[qo[b]:qo[b + 1]], want, f"request {b}")
 
 
+def test_host_buffer_automatic_ranges_end_with_an_empty_request():
+    """The automatic range split on a step large enough for several ranges (147 MB of rows):
+    the last eighth of the last range runs on its own, which here is a request with no new
+    tokens (its range copies and computes nothing but still writes its slot-table row).  The
+    host-buffer step equals the device-row step bit for bit, and sampled rows the oracle."""
+    from prefix_cached_kv_radix_gb300.engine import _dev_from_host
+    n = 800
+    spec = W.Spec("gqa4-auto-ranges", "bf16", 32, 8, 128, 1 << 14, W.QWEN_VOCAB, 37,
+                  seg_parent=[-1], seg_len=[300], histories=[0],
+                  req_seg=[0] * 10, req_cached=[300, 0, 300, 120, 300, 0, 300, 300, 64, 300],
+                  req_new=[n] * 9 + [0])
+    w = W.generate(spec)
+    prompts = [w.request_tokens(b) for b in range(w.batch)]
+    ind = np.concatenate([[0], np.cumsum([len(p) for p in prompts])]).astype(np.int64)
+    toks = np.concatenate(prompts).astype(np.int32)
+    q, kn, vn = w.stacked_new()
+    outs = []
+    for host in (False, True):
+        eng = _engine_for(w)
+        qd, kd, vd = (_dev_from_host(x, spec.dtype, eng.device) for x in (q, kn, vn))
+        out = torch.empty_like(qd)
+        lse = torch.empty(qd.shape[0], spec.hq, dtype=torch.float32, device=eng.device)
+        if host:
+            hq_, hk_, hv_ = (x.cpu().pin_memory() for x in (qd, kd, vd))
+            for x in (qd, kd, vd):
+                x.zero_()
+            torch.cuda.synchronize()
+            out_h = torch.full(out.shape, float("nan"), dtype=out.dtype).pin_memory()
+            lse_h = torch.full(lse.shape, float("nan"), dtype=torch.float32).pin_memory()
+            plan = eng.step(toks, ind, spec.req_new, qd, kd, vd, out, lse, host=(hq_, hk_, hv_, out_h, lse_h), chunks=0)
+            torch.cuda.synchronize()
+            outs.append((out_h.float().numpy(), lse_h.numpy()))
+        else:
+            plan = eng.step(toks, ind, spec.req_new, qd, kd, vd, out, lse)
+            torch.cuda.synchronize()
+            outs.append((to_host_f32(out), lse.cpu().numpy()))
+        assert eng.device_status() == 0
+        eng.tree.check()
+        assert np.array_equal(plan.prefix_lens, np.asarray(spec.req_cached, np.int32))
+    (o_d, l_d), (o_h, l_h) = outs
+    assert np.array_equal(o_d, o_h) and np.array_equal(l_d, l_h)
+    qo = w.qo_indptr()
+    for b in (0, 3, 8):
+        idx = np.array([0, 1, n // 2, n - 1])
+        want, want_lse = oracle_rows(w, b, idx)
+        compare(o_h[qo[b] + idx], want, f"request {b}")
+        assert np.abs(l_h[qo[b] + idx] - want_lse).max() <= TOL_LSE
+
+
 def test_host_buffer_steps_overlap_back_to_back():
     """Host-buffer steps back to back with overlap: two sets of device rows used in turn, each
     step's input copies waiting only for the kernels of the last step that read the same rows

@@ -447,6 +447,15 @@ int rx_step_launch(rx_radix* t, const rx_attn_desc* desc, const int32_t* tokens,
 int rx_step_prefetch(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, const rx_step_io* io,
                      void* stream);
 
+/* The request ranges a host-buffer step with these new-token counts is cut into (the same
+ * cuts rx_step_prefetch and rx_step_launch make; a host computation, no device needed; no
+ * counterpart on the pages: it exposes the pipeline's sizing for callers and tests).  Writes
+ * the n+1 cut points (request indices, first 0, last batch) to out_cuts (capacity cap) and n
+ * to *out_n.  n_new: host, [batch], each >= 0; chunks as rx_step_io.chunks.  RX_EINVAL on bad
+ * arguments or too small a capacity (max(chunks, 4) + 2 entries always suffice). */
+int rx_step_ranges(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, int32_t chunks, int32_t* out_cuts,
+                   int32_t cap, int32_t* out_n);
+
 /* Block until the last rx_step_launch that read h_stage is done with it (no-op if none): by
  * its CUDA event, or, for a small device-row step (index arrays read by kv_pool_write itself
  * through the buffer's device mapping), by a sequence number that launch writes to pinned host

@@ -25,7 +25,7 @@ EXPORTS = ("radix_create", "radix_destroy", "match_prefix", "match_prefix_len", 
            "free_slots", "insert", "evict", "match_prefix_batch", "insert_batch", "insert_batch_at", "radix_lock_batch",
            "radix_unlock_batch", "radix_stats", "radix_check",
            "radix_shared_groups", "rx_step_stage_bytes", "rx_step_plan", "rx_step_finish",
-           "rx_step_workspace_bytes", "rx_step_launch", "rx_step_prefetch", "rx_stage_wait", "rx_step_run",
+           "rx_step_workspace_bytes", "rx_step_launch", "rx_step_prefetch", "rx_step_ranges", "rx_stage_wait", "rx_step_run",
            "kv_pool_write", "prefix_extend_attention", "extend_workspace_bytes", "decode_workspace_bytes",
            "decode_attention",
            "decode_attention_noalloc",
@@ -133,6 +133,7 @@ def load(path: str = LIB_PATH):
         "rx_step_launch": (ctypes.c_int, [P, P, P, P, P, P, P, P, I64, P, P]),
         "rx_step_run": (ctypes.c_int, [P]),
         "rx_step_prefetch": (ctypes.c_int, [P, I32, P, P, P]),
+        "rx_step_ranges": (ctypes.c_int, [P, I32, P, I32, P, I32, P]),
         "rx_stage_wait": (ctypes.c_int, [P]),
         "kv_pool_write": (ctypes.c_int, [P, I32, P, P, P, P, P, P, P, P, P, I64, I64, P, P]),
         "prefix_extend_attention": (ctypes.c_int, [P, I32, P, P, P, P, I64, P, P, P, P, I32, P, P, SZ, P, P]),
@@ -406,6 +407,17 @@ def rx_step_prefetch(desc, n_new: np.ndarray, io, stream) -> None:
     nn = np.ascontiguousarray(np.asarray(n_new, np.int32))
     _check("rx_step_prefetch", load().rx_step_prefetch(ctypes.byref(desc), len(nn), _addr(nn) if len(nn) else None,
                                                        ctypes.byref(io), _stream(stream)))
+
+
+def rx_step_ranges(desc, n_new: np.ndarray, chunks: int = 0) -> np.ndarray:
+    """The request cut points (first 0, last batch) of a host-buffer step's copy pipeline."""
+    nn = np.ascontiguousarray(np.asarray(n_new, np.int32))
+    cap = max(int(chunks), 4) + 2
+    cuts = np.zeros(cap, np.int32)
+    n = ctypes.c_int32(0)
+    _check("rx_step_ranges", load().rx_step_ranges(ctypes.byref(desc), len(nn), _addr(nn) if len(nn) else None,
+                                                   int(chunks), _addr(cuts), cap, ctypes.byref(n)))
+    return cuts[: n.value + 1].copy()
 
 
 def rx_step_launch(tree, desc, tokens: np.ndarray, tok_indptr: np.ndarray, last_nodes: np.ndarray, stage_addr: int,

@@ -604,6 +604,23 @@ extern "C" int rx_step_run(const rx_step_args* a) {
                           stream);
 }
 
+extern "C" int rx_step_ranges(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, int32_t chunks,
+                              int32_t* out_cuts, int32_t cap, int32_t* out_n) {
+    RX_REQUIRE(desc && batch >= 0 && (batch == 0 || n_new) && out_cuts && out_n && cap > 0,
+               "rx_step_ranges: bad arguments");
+    RX_REQUIRE(desc->hq > 0 && desc->hkv > 0 && desc->head_dim > 0, "rx_step_ranges: bad descriptor");
+    std::vector<int64_t> qo((size_t)batch + 1, 0);
+    for (int32_t b = 0; b < batch; ++b) {
+        RX_REQUIRE(n_new[b] >= 0, "rx_step_ranges: request %d has %d new tokens", b, n_new[b]);
+        qo[(size_t)b + 1] = qo[(size_t)b] + n_new[b];
+    }
+    const std::vector<int32_t> cut = range_cuts(desc, qo.data(), batch, chunks);
+    RX_REQUIRE((int64_t)cut.size() <= cap, "rx_step_ranges: %zu cut points, capacity %d", cut.size(), cap);
+    std::copy(cut.begin(), cut.end(), out_cuts);
+    *out_n = (int32_t)cut.size() - 1;
+    return RX_OK;
+}
+
 extern "C" int rx_step_prefetch(const rx_attn_desc* desc, int32_t batch, const int32_t* n_new, const rx_step_io* io,
                                 void* stream_) {
     RX_TRACE("rx_step_prefetch");

@@ -2,7 +2,9 @@
 
 Host code only: a step's match, allocation, pinning, index layout, shared-prefix groups,
 insert, free of duplicate slots, eviction and unpinning must equal the same operations
-replayed on the oracle, bit for bit, over multi-step scripts.
+replayed on the oracle, bit for bit, over multi-step scripts.  The host-buffer pipeline's
+request ranges (rx_step_ranges, the cuts rx_step_prefetch and rx_step_launch make) are checked
+against the policy the header states, restated here.
 """
 import numpy as np
 import pytest
@@ -262,3 +264,68 @@ def test_long_prompt_step_equals_per_call_replay():
         t1.check()
     # identical stamps and structure: everything evicts in the same order
     assert t1.evict(10 ** 7).tolist() == t2.evict(10 ** 7).tolist()
+
+
+# ---------------------------------------------------------------- host-buffer pipeline ranges
+def _expected_ranges(n_new, hq, hkv, d, elt, chunks):
+    """The pipeline's cuts restated from the header: `chunks` ranges of about equal token counts
+    (range c starts at the first request whose rows start at or after c/n of the tokens), or,
+    for chunks = 0, one range per 64 MB of rows moved (at most 4) with the last eighth of the
+    last range's tokens (at least one request) split off when there are several."""
+    B = len(n_new)
+    qo = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int64)
+    T = int(qo[-1])
+    moved = T * (2 * hq * d * elt + 2 * hkv * d * elt)
+    nc = chunks if chunks > 0 else min(4, max(1, moved >> 26))
+    nc = max(1, min(nc, max(B, 1)))
+    cut = [0]
+    for c in range(1, nc):
+        target = T * c // nc
+        first = next((b for b in range(B) if qo[b] >= target), B)
+        cut.append(max(first, cut[-1]))
+    cut.append(B)
+    if chunks <= 0 and nc > 1 and B - cut[-2] >= 2:
+        b0 = cut[-2]
+        target = qo[B] - (qo[B] - qo[b0]) // 8
+        s = next((b for b in range(b0 + 1, B) if qo[b] >= target), B)
+        cut.insert(len(cut) - 1, min(s, B - 1))
+    return np.asarray(cut, np.int32)
+
+
+@pytest.mark.parametrize("shape", [(64, 8, 128, 2), (32, 8, 128, 2), (12, 12, 64, 2), (4, 4, 64, 4)])
+@pytest.mark.parametrize("chunks", [0, 1, 3, 4, 8])
+def test_step_ranges_follow_the_stated_policy(shape, chunks):
+    hq, hkv, d, elt = shape
+    desc = api.make_desc(api.RX_F32 if elt == 4 else api.RX_BF16, hq, hkv, d, 1 << 22, d ** -0.5)
+    rng = np.random.default_rng(hq * 100 + chunks)
+    cases = [[1024] * 32, [128] * 128, [800] * 9 + [0], [0, 0, 5000, 0, 3000, 0], [7, 8] * 32, [], [3],
+             list(rng.integers(0, 3000, size=57)), [20000, 1, 1, 1], [1, 1, 1, 20000]]
+    for n_new in cases:
+        got = api.rx_step_ranges(desc, np.asarray(n_new, np.int32), chunks)
+        want = _expected_ranges(np.asarray(n_new, np.int64), hq, hkv, d, elt, chunks)
+        assert np.array_equal(got, want), (n_new[:8], got, want)
+        assert got[0] == 0 and got[-1] == len(n_new) and (np.diff(got) >= 0).all()
+
+
+def test_step_ranges_at_the_benchmark_shapes():
+    """c5 (32 x 1024 new rows, 64/8 heads x 128): four ranges of 8 requests with the last one's
+    final request on its own; c3 (128 x 128, 32/8 x 128): the last 4 requests on their own."""
+    c5 = api.make_desc(api.RX_BF16, 64, 8, 128, 1 << 22, 128 ** -0.5)
+    assert api.rx_step_ranges(c5, [1024] * 32).tolist() == [0, 8, 16, 24, 31, 32]
+    assert api.rx_step_ranges(c5, [1024] * 32, 4).tolist() == [0, 8, 16, 24, 32]
+    c3 = api.make_desc(api.RX_BF16, 32, 8, 128, 1 << 20, 128 ** -0.5)
+    assert api.rx_step_ranges(c3, [128] * 128).tolist() == [0, 32, 64, 96, 124, 128]
+    c2 = api.make_desc(api.RX_BF16, 12, 12, 64, 1 << 16, 64 ** -0.5)
+    assert api.rx_step_ranges(c2, [8] * 64).tolist() == [0, 64]          # 3 MB: one range
+
+
+def test_step_ranges_reject_bad_arguments():
+    desc = api.make_desc(api.RX_BF16, 32, 8, 128, 1 << 20, 128 ** -0.5)
+    with pytest.raises(RuntimeError):
+        api.rx_step_ranges(desc, np.asarray([5, -1, 3], np.int32))
+    lib = api.load()
+    nn = np.asarray([128] * 128, np.int32)
+    cuts = np.zeros(3, np.int32)
+    n = np.zeros(1, np.int32)
+    assert lib.rx_step_ranges(api.ctypes.byref(desc), len(nn), nn.ctypes.data, 0, cuts.ctypes.data, 3,
+                              n.ctypes.data) == api.RX_EINVAL

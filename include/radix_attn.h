@@ -332,7 +332,10 @@ size_t decode_workspace_bytes(const rx_attn_desc* desc, int32_t batch, int32_t m
  * member's private remainder.
  * d_q, d_out: [batch, hq, head_dim]; d_lse optional [batch, hq] float32.
  * max_kv_len (host) must be >= every L_b.  d_workspace: >= decode_workspace_bytes(...)
- * bytes of device memory, contents need not be initialised. */
+ * bytes of device memory, contents need not be initialised.  The requests are a launch
+ * dimension of the bf16 kernels: a call takes at most 65535 of them (more fail to launch and
+ * return RX_ECUDA with the launch error in rx_last_error); larger batches are split by the
+ * caller. */
 int decode_attention(const rx_attn_desc* desc, int32_t batch,
                      const void* d_q, const int32_t* d_req_to_token, int64_t r2t_stride,
                      const int32_t* d_kv_lens, const rx_shared_groups* groups,

@@ -304,7 +304,8 @@ typedef struct {
  * cores, and the two softmax parts are merged exactly.  Worth it when the new rows per
  * request are few and the private parts short (e.g. many short questions on one system
  * prompt).  d_workspace: >= extend_workspace_bytes(...) bytes, 256-byte aligned, needed only
- * with groups (else NULL / 0). */
+ * with groups (else NULL / 0).  bf16 calls take at most 65535 requests and, on the tcgen05
+ * kernel, max_qo_len * hq/hkv below 65536 * 256 (RX_EINVAL beyond: split the batch). */
 int prefix_extend_attention(const rx_attn_desc* desc, int32_t batch,
                             const void* d_q, const int64_t* d_qo_indptr, const int32_t* d_prefix_lens,
                             const int32_t* d_req_to_token, int64_t r2t_stride,
